@@ -1,0 +1,110 @@
+"""Pins of the input generator, the byte/flop model and the dispatch formula (CPU)."""
+import math
+
+import numpy as np
+import pytest
+
+from conftest import golden
+from oracle import dispatch, model
+from synth import gen, workloads
+
+
+def test_generator_published_vector():
+    g = golden("splitmix64_vector.json")
+    s = gen.SplitMix64(g["seed"])
+    assert [s.next() for _ in range(5)] == [int(x) for x in g["outputs"]]
+    # counter form: output n of a stream started at state s is mix64(s + n * gamma)
+    assert gen.mix64(g["seed"] + 3 * gen.GAMMA) == int(g["outputs"][2])
+
+
+def test_normal_table_is_a_quantile_table():
+    t = gen.bf16_bits_to_f64(gen.normal_table_bits())
+    assert np.all(np.diff(t) >= 0)
+    np.testing.assert_array_equal(t, -t[::-1])            # symmetric quantiles
+    assert abs(t.mean()) < 1e-12 and abs(t.std() - 1.0) < 2e-3
+    assert abs(t[32767]) < 1e-4 and abs(t[int(0.975 * 65536)] - 1.96) < 0.01
+
+
+def test_normal_bits_counter_based_and_chunk_independent():
+    key = gen.stream_key(7, 1, 2, 3)
+    a = gen.normal_bits(key, 0, 5000)
+    b = gen.normal_bits(key, 1234, 100)
+    np.testing.assert_array_equal(a[1234:1334], b)
+    table = gen.normal_table_bits()
+    for i in (0, 17, 4999):
+        assert a[i] == table[gen.mix64(key + (i + 1) * gen.GAMMA) >> 48]
+
+
+def test_pow2_scaling_is_exact():
+    bits = gen.normal_bits(gen.stream_key(1, 5), 0, 1000)
+    np.testing.assert_array_equal(gen.bf16_bits_to_f64(gen.scale_bf16_bits_pow2(bits, 3)),
+                                  gen.bf16_bits_to_f64(bits) * 8.0)
+
+
+def test_workload_shapes():
+    w = workloads.config(1)
+    assert (w.L, w.Hq, w.Hkv, w.d, w.B, w.prefix_lens) == (1, 4, 2, 64, 4, [64])
+    assert all(1 <= r.suffix_len <= 48 for r in w.requests)
+    w = workloads.config(2)
+    assert (w.L, w.Hq, w.Hkv, w.d, w.B, w.prefix_lens) == (32, 32, 8, 128, 64, [16384])
+    assert all(256 <= r.suffix_len <= 2048 for r in w.requests)
+    w = workloads.config(4)
+    assert len(w.prefix_lens) == 8 and all(2048 <= lp <= 16384 for lp in w.prefix_lens)
+    counts = np.bincount([r.prefix for r in w.requests])
+    assert all(16 <= c <= 64 for c in counts)
+    w = workloads.config(5)
+    assert w.B == 128 and w.page_size == 16 and w.steps == 32 and len(w.parents) == 32
+
+
+def test_kv_bytes_per_token_printed():
+    for c in golden("kv_bytes_per_token.json")["cases"]:
+        assert model.kv_bytes_per_token(c["layers"], c["kv_heads"], c["head_dim"], c["elem_bytes"]) == c["bytes"]
+
+
+def test_table23_byte_and_flop_model():
+    g = golden("granikv_table23_byte_model.json")
+    s, p, tol = g["shape"], g["printed"], g["tolerance_rel"]
+    paged = model.paged_prefix_bytes(s["B"], s["Lp"], s["Hkv"], s["d"], s["elem_bytes"])
+    shared = model.shared_prefix_bytes(s["Lp"], s["Hkv"], s["d"], s["elem_bytes"])
+    flops = model.prefix_flops(s["B"], s["Hq"], s["Lp"], s["d"])
+    assert abs(paged / 1e9 - p["paged_bytes_model_GB"]) / p["paged_bytes_model_GB"] < tol
+    assert abs(shared / 1e6 - p["shared_bytes_model_MB"]) / p["shared_bytes_model_MB"] < tol
+    assert abs(flops / 1e9 - p["useful_GFLOP"]) / p["useful_GFLOP"] < tol
+    assert abs(flops / (p["paged_bytes_measured_GB"] * 1e9) - p["paged_arith_intensity_measured"]) < 0.01
+    assert abs(flops / (p["hot_dram_measured_MB"] * 1e6) - p["hot_arith_intensity_measured"]) < 1.0
+
+
+def test_eq2_meff_and_a100_threshold_rows():
+    g = golden("granikv_table16_meff.json")
+    for B, meff, route in g["rows"]:
+        m = dispatch.m_eff(B, g["n_q_per_kv"])
+        assert m == meff
+        assert ("dense" if m >= g["m_sat_a100"] else "cascade") == route
+
+
+def test_tc_curve_closed_form():
+    pts = [[128, 400.0], [512, 1200.0], [1024, 1500.0]]
+    assert dispatch.tc_at(pts, 64) == 200.0
+    assert dispatch.tc_at(pts, 128) == 400.0
+    assert dispatch.tc_at(pts, 320) == 800.0
+    assert dispatch.tc_at(pts, 768) == 1350.0
+    assert dispatch.tc_at(pts, 4096) == 1500.0
+
+
+def test_cost_model_closed_form():
+    cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0,
+              tc_points=[[128, 500.0], [1024, 1500.0]], bw_suffix_gbs=4000.0, c_merge_us=0.001)
+    # one group of 64 requests (g = 4 -> M = 256), Lp = 1000, suffixes 100 each, Hkv = 8, d = 128
+    f = dispatch.features([1000] * 64, [100] * 64, [0] * 64, 32, 8, 128)
+    kv = 2 * 8 * 128 * 2
+    assert f["bytes_flat"] == 64 * 1100 * kv and f["bytes_suffix"] == 64 * 100 * kv
+    assert f["prefix"] == [dict(M=256, bytes=1000 * kv, flops=4 * 64 * 32 * 1000 * 128)]
+    t_flat, t_cas = dispatch.predict(cm, f)
+    assert math.isclose(t_flat, 5.0 + 64 * 1100 * kv / 4e6)
+    tc = 500.0 + 1000.0 * (256 - 128) / (1024 - 128)
+    t_pre = max(1000 * kv / 5e6, 4 * 64 * 32 * 1000 * 128 / (tc * 1e6))
+    assert math.isclose(t_cas, 10.0 + t_pre + 64 * 100 * kv / 4e6 + 0.001 * 64 * 32)
+    assert dispatch.choose(cm, f)[0] == ("dense" if t_flat < t_cas else "cascade")
+    # a request without a HOT prefix counts only toward the flat and suffix bytes
+    f2 = dispatch.features([0, 1000], [300, 10], [-1, 0], 32, 8, 128)
+    assert f2["bytes_flat"] == 1310 * kv and len(f2["prefix"]) == 1 and f2["prefix"][0]["M"] == 4
