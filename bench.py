@@ -1,0 +1,470 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the shared-prefix paged attention library on GB300.
+
+Workload (default): Llama-3.1-8B attention geometry (Hq 32, Hkv 8, d 128, bf16,
+32 layers), one shared prefix of 16384 tokens in the HOT pool and 64 requests
+with suffixes uniform in 256..2048 tokens in a page-size-1 COLD pool with
+shuffled slots.  One step = the whole decode step of all layers:
+  host: gk_seq_append_slots (64 tokens), gk_seq_tables, gk_plan_update, gk_dispatch
+  device, per layer: gk_append_kv (the step's token), then the dispatcher's
+  backend (cascade: prefix contraction, suffix gather, LSE merge; or dense).
+Metric: decode attention queries/s per layer = B * L / step time.
+
+--impl reference times the fp64 CPU oracle instead (there is no other
+implementation to run); each of its steps is a bounded sample of one layer.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+for _p in (ROOT, os.path.join(ROOT, "tests")):
+    if _p not in sys.path:
+        sys.path.insert(0, _p)
+
+METRIC = "decode attention queries/s per layer"
+UNIT = "queries/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--backend", choices=["auto", "cascade", "dense"], default="auto")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except OSError:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class Clocks:
+    """nvidia-smi samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(smax), "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _profile_traffic(kernel_tag, src_file):
+    """dram bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not m or not h:
+        return None
+    cur = hashlib.sha256(open(os.path.join(ROOT, "paged_kv_cache_pool_gb300", "csrc", src_file), "rb").read()).hexdigest()
+    return float(m.group(1)) if cur == h.group(1) else None
+
+
+# ----------------------------------------------------------------------------------------------
+# oracle (CPU) timing: the --impl reference arm and the cpu_baseline field
+# ----------------------------------------------------------------------------------------------
+def _oracle_sample(w, n_req, start=0):
+    """Time the oracle on n_req requests of layer 0 -> (seconds, requests, threads)."""
+    from oracle import attention, reference
+    from synth.gen import bf16_bits_to_f64
+    cache = reference.ContextCache(w)
+    q = reference.q_bits(w, 0, 0)
+    reqs = [(start + i) % w.B for i in range(n_req)]
+    ctx = [reference.context(w, r, 0, 0, cache) for r in reqs]     # gather (untimed)
+    t0 = time.perf_counter()
+    for r, (K, V) in zip(reqs, ctx):
+        attention.attend_heads(bf16_bits_to_f64(q[r]), K, V)
+    dt = time.perf_counter() - t0
+    return dt, len(reqs), attention.threads()
+
+
+def cpu_baseline(w, budget_s=12.0):
+    from oracle import attention
+    attention.build()
+    dt, n, thr = _oracle_sample(w, 1)
+    per = max(dt, 1e-3)
+    n_req = max(1, min(w.B, int(budget_s / per)))
+    dt, n, thr = _oracle_sample(w, n_req, start=1)
+    return {"value": n / dt, "unit": UNIT, "cores": thr, "kind": "oracle",
+            "sample": f"fp64 C oracle, layer 0 of the workload, {n} of {w.B} requests "
+                      f"(all {w.Hq} query heads, contexts gathered beforehand), {dt:.1f} s"}
+
+
+def run_reference(a, w):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    from oracle import attention
+    attention.build()
+    dt1, _, thr = _oracle_sample(w, 1)
+    n_req = max(1, min(w.B, int(4.0 / max(dt1, 1e-3))))
+    for i in range(a.warmup):
+        _oracle_sample(w, 1, start=i)
+    total_t, total_q = 0.0, 0
+    for i in range(a.steps):
+        dt, n, thr = _oracle_sample(w, n_req, start=i * n_req)
+        total_t += dt
+        total_q += n
+    value = total_q / total_t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": a.gpus,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1e3 * total_t / a.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": _config_dict(w, "oracle"),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
+                             "sample": f"each step: {n_req} requests of layer 0 (all query heads), fp64 C oracle"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def _config_dict(w, backend):
+    s = [r.suffix_len for r in w.requests]
+    return {"workload": w.name, "B": w.B, "layers": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d,
+            "prefix_lens": w.prefix_lens, "suffix_min": min(s), "suffix_max": max(s), "suffix_sum": sum(s),
+            "cold_page_size": w.page_size, "backend": backend, "parallelism": "replicas",
+            "l2": "inputs larger than L2 (each layer reads a distinct 352 MiB of K/V; 11 GB per step)"}
+
+
+# ----------------------------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------------------------
+def run_ours(a, w):
+    import numpy as np
+    import torch
+    from gpu_workload import GpuWorkload
+    from paged_kv_cache_pool_gb300 import binding as gk
+    from synth import device as sdev
+    from synth.gen import KIND_NEW_K, KIND_NEW_V, KIND_Q, stream_key
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    total_steps = a.warmup + a.steps + (a.warmup + a.steps if not a.no_e2e else 0) + 2
+    gw = GpuWorkload(w, extra_steps=total_steps)
+    eng = gw.eng
+    pool = eng.pool
+    L, B, Hq, Hkv, d = w.L, w.B, w.Hq, w.Hkv, w.d
+    stream = torch.cuda.current_stream()
+    bf = torch.bfloat16
+
+    # step inputs, resident on the device (one set reused every step)
+    q_all = torch.empty((L, B, Hq, d), dtype=bf, device="cuda")
+    newk = torch.empty((L, B, Hkv, d), dtype=bf, device="cuda")
+    newv = torch.empty_like(newk)
+    for l in range(L):
+        sdev.fill_normal(q_all[l].view(-1), stream_key(w.seed, KIND_Q, l, 0))
+        sdev.fill_normal(newk[l].view(-1), stream_key(w.seed, KIND_NEW_K, l, 0))
+        sdev.fill_normal(newv[l].view(-1), stream_key(w.seed, KIND_NEW_V, l, 0))
+    out_all = torch.empty((L, B, Hq, d), dtype=torch.float32, device="cuda")
+    lse_all = torch.empty((L, B, Hq), dtype=torch.float32, device="cuda")
+
+    seqs = np.asarray(gw.seqs, dtype=np.int32)
+    P = gw.P
+    max_len = max(r.suffix_len for r in w.requests) + total_steps + 1
+    max_blocks = -(-max_len // P)
+    h_table = torch.empty((B, max_blocks), dtype=torch.int32).pin_memory()
+    h_lens = np.empty(B, dtype=np.int32)
+    h_slots = torch.empty(B, dtype=torch.int64).pin_memory()
+    h_cow = torch.empty(2 * B, dtype=torch.int32).pin_memory()
+    d_table = torch.empty((B, max_blocks), dtype=torch.int32, device="cuda")
+    d_slots = torch.empty(B, dtype=torch.int64, device="cuda")
+    d_cow = torch.empty(2 * B, dtype=torch.int32, device="cuda")
+    staged = torch.cuda.Event()
+    bases = np.array([gw.bases[r.prefix] if r.prefix >= 0 else -1 for r in w.requests], dtype=np.int64)
+    lps = np.array([w.prefix_lens[r.prefix] if r.prefix >= 0 else 0 for r in w.requests], dtype=np.int32)
+    batch = gk.Batch(bases, lps, np.zeros(B, np.int32), d_table, max_blocks)
+    plan = [None]
+    forced = {"cascade": gk.GK_BACKEND_CASCADE, "dense": gk.GK_BACKEND_DENSE}.get(a.backend)
+    launches = [0]
+    dense_merge = [0]
+    choices = []
+
+    def step(events=None, q=q_all, k=newk, v=newv, out=out_all, lse=lse_all):
+        # a0: host plan (append one token per request, tables, plan, dispatch)
+        slots, cow = gk.gk_seq_append_slots(pool, seqs)
+        staged.synchronize()                    # the previous step's staging copies have left
+        h_slots.numpy()[:] = slots
+        ncow = len(cow)
+        if ncow:
+            h_cow.numpy()[:2 * ncow] = cow.reshape(-1)
+        gk.gk_seq_tables(pool, seqs, max_blocks, h_table.numpy(), h_lens)
+        batch.suffix_len[:] = h_lens
+        d_slots.copy_(h_slots, non_blocking=True)
+        d_table.copy_(h_table, non_blocking=True)
+        if ncow:
+            d_cow[:2 * ncow].copy_(h_cow[:2 * ncow], non_blocking=True)
+        staged.record(stream)
+        if plan[0] is None:
+            plan[0] = gk.gk_plan_build(pool, batch, stream)
+        else:
+            gk.gk_plan_update(pool, plan[0], batch, stream)
+        dense_merge[0] = gk.gk_plan_info(plan[0])["dense_merge"]
+        choice, _, _ = gk.gk_dispatch(pool, plan[0])
+        if forced is not None:
+            choice = forced
+        choices.append(choice)
+        for l in range(L):
+            if events is not None:
+                events[l][0].record(stream)
+            gk.gk_append_kv(pool, stream, l, d_slots, k[l], v[l], d_cow if ncow else None, n=B, n_cow=ncow)
+            launches[0] += 1 + (1 if ncow else 0)
+            batch.set_device(d_q=q[l], d_out=out[l], d_lse=lse[l])
+            if events is not None:
+                events[l][1].record(stream)
+            if choice == gk.GK_BACKEND_CASCADE:
+                gk.gk_cascade_prefix(pool, stream, l, batch, plan[0])
+                if events is not None:
+                    events[l][2].record(stream)
+                gk.gk_cascade_suffix(pool, stream, l, batch, plan[0])
+                if events is not None:
+                    events[l][3].record(stream)
+                gk.gk_cascade_merge(pool, stream, l, batch, plan[0])
+                launches[0] += 3
+            else:
+                gk.gk_decode_dense(pool, stream, l, batch, plan[0])
+                launches[0] += 1 + dense_merge[0]
+            if events is not None:
+                events[l][4].record(stream)
+
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+    err = gk.gk_device_error(pool, stream)
+    if err:
+        raise RuntimeError(f"device error word {err} during warm-up")
+    if world > 1:
+        torch.distributed.barrier()
+
+    # ---- timed region: device-resident inputs ----
+    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(L)] for _ in range(a.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    vis_list = [x for x in vis.split(",") if x.strip()]
+    gpu_index = vis_list[local].strip() if local < len(vis_list) else str(local)
+    clocks = Clocks(gpu_index)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    launches[0] = 0
+    n_choice0 = len(choices)
+    t_start.record(stream)
+    for i in range(a.steps):
+        step(events[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    gpu_launches = launches[0]
+    elapsed_ms = t_start.elapsed_time(t_end)
+    err = gk.gk_device_error(pool, stream)
+    if err:
+        raise RuntimeError(f"device error word {err} in the timed region")
+    step_choices = choices[n_choice0:]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / a.steps
+    value = world * B * L * a.steps / (elapsed_ms / 1e3)
+
+    # per-kernel averages over the timed region
+    k_ms = {"append": [], "prefix": [], "suffix": [], "merge": [], "dense": []}
+    for i in range(a.steps):
+        cas = step_choices[i] == gk.GK_BACKEND_CASCADE
+        for l in range(L):
+            e = events[i][l]
+            k_ms["append"].append(e[0].elapsed_time(e[1]))
+            if cas:
+                k_ms["prefix"].append(e[1].elapsed_time(e[2]))
+                k_ms["suffix"].append(e[2].elapsed_time(e[3]))
+                k_ms["merge"].append(e[3].elapsed_time(e[4]))
+            else:
+                k_ms["dense"].append(e[1].elapsed_time(e[4]))
+    avg = {k: (sum(v) / len(v) if v else None) for k, v in k_ms.items()}
+    info = gk.gk_plan_info(plan[0])
+    peaks, peak_src = _peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    s_tot = int(batch.suffix_len.sum())
+    # algorithmic bytes per launch
+    suffix_bytes = info["suffix_bytes"] + s_tot * 4 // P + B * Hq * d * 2 + info["num_partials"] * Hq * (d + 1) * 4
+    prefix_bytes = info["prefix_bytes"] + B * Hq * d * 2
+    dense_bytes = info["dense_bytes"] + s_tot * 4 // P + B * Hq * d * 2 + B * Hq * (d + 1) * 4
+    kernels = {}
+    if avg["suffix"]:
+        kernels["suffix_gather"] = {"ms": avg["suffix"], "bytes": suffix_bytes,
+                                    "gbs": suffix_bytes / (avg["suffix"] * 1e-3) / 1e9}
+    if avg["prefix"]:
+        kernels["cascade_prefix"] = {"ms": avg["prefix"], "bytes": prefix_bytes, "flops": info["prefix_flops"],
+                                     "gbs": prefix_bytes / (avg["prefix"] * 1e-3) / 1e9,
+                                     "tflops": info["prefix_flops"] / (avg["prefix"] * 1e-3) / 1e12}
+    if avg["merge"]:
+        kernels["lse_merge"] = {"ms": avg["merge"]}
+    if avg["dense"]:
+        kernels["dense_gather"] = {"ms": avg["dense"], "bytes": dense_bytes,
+                                   "gbs": dense_bytes / (avg["dense"] * 1e-3) / 1e9}
+    kernels["append_kv"] = {"ms": avg["append"]}
+    # dominant kernel -> roofline
+    dom = max(((k, v["ms"]) for k, v in kernels.items() if "bytes" in v), key=lambda x: x[1])[0]
+    kd = kernels[dom]
+    if dom == "cascade_prefix" and kd["flops"] / kd["bytes"] > tc_peak * 1e3 / hbm:
+        roof = {"kernel": dom, "bound": "tensor", "achieved": kd["tflops"], "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": kd["tflops"] / tc_peak, "traffic": _profile_traffic("cascade_prefix_llama8b_lp16384_b64", "prefix_tc.cu")}
+    else:
+        tag = {"suffix_gather": ("suffix_gather_llama8b_lp16384_b64", "gather_attn.cu"),
+               "dense_gather": ("dense_gather_llama8b_lp16384_b64", "gather_attn.cu"),
+               "cascade_prefix": ("cascade_prefix_llama8b_lp16384_b64", "prefix_tc.cu")}[dom]
+        roof = {"kernel": dom, "bound": "hbm", "achieved": kd["gbs"], "peak": hbm, "unit": "GB/s",
+                "frac": kd["gbs"] / hbm, "traffic": _profile_traffic(*tag)}
+    roof["peak_source"] = f"{peak_src} ({'bf16_tflops_sustained' if roof['bound'] == 'tensor' else 'hbm_gbs'})"
+
+    # ---- e2e: host buffers, copies inside the timed region ----
+    e2e = None
+    if not a.no_e2e:
+        hq = torch.empty_like(q_all, device="cpu").pin_memory()
+        hk = torch.empty_like(newk, device="cpu").pin_memory()
+        hv = torch.empty_like(newv, device="cpu").pin_memory()
+        hq.copy_(q_all)
+        hk.copy_(newk)
+        hv.copy_(newv)
+        ho = torch.empty_like(out_all, device="cpu").pin_memory()
+        hl = torch.empty_like(lse_all, device="cpu").pin_memory()
+        dq, dk, dv = torch.empty_like(q_all), torch.empty_like(newk), torch.empty_like(newv)
+        do, dl = torch.empty_like(out_all), torch.empty_like(lse_all)
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            step(None, dq, dk, dv, do, dl)
+            ho.copy_(do, non_blocking=True)
+            hl.copy_(dl, non_blocking=True)
+
+        for _ in range(a.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(a.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + B * 8 + B * max_blocks * 4
+        d2h = ho.numel() * 4 + hl.numel() * 4
+        e2e = {"value": world * B * L * a.steps / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems / a.steps}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        gw.close()
+        return
+    cpu = None
+    if not a.no_cpu:
+        cpu = cpu_baseline(w)
+    backend_name = "cascade" if step_choices and step_choices[0] == gk.GK_BACKEND_CASCADE else "dense"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic", "config": _config_dict(w, backend_name),
+            "clocks": clk, "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roof,
+            "cpu_baseline": cpu, "kernels": kernels,
+            "query_rows_per_s": value * Hq,
+            "plan": info}
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    gw.close()
+
+
+def main():
+    a = _args()
+    from synth import workloads
+    w = workloads.config(a.config)
+    if a.impl == "reference":
+        run_reference(a, w)
+    else:
+        from paged_kv_cache_pool_gb300 import build
+        from synth import device
+        build.build()
+        device.build()
+        run_ours(a, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,256 @@
+/*
+ * gk.h -- C ABI of the shared-prefix paged decode-attention library (libgk.so).
+ *
+ * Storage follows "GraniKV: Asymmetric Granularity KV-Cache Paging for
+ * Multi-Agent Systems with Long Shared Prefix": a shared prefix lives in a
+ * contiguous HOT pool (Section 3.2) and each request's own tokens live in a
+ * token-granular COLD pool (Section 3.3) reached through a block table whose
+ * bookkeeping is the refcounted copy-on-write block manager of "Paged KV cache"
+ * (How it works; Code).
+ *
+ * Conventions for every call:
+ *  - The return value is a gk_status; GK_OK is 0.  On failure the pool's
+ *    gk_last_error() text says what was wrong.  No C++ exception crosses the ABI.
+ *  - "device" pointers are CUDA global-memory addresses owned by the caller;
+ *    the library never frees them.  "host" pointers are ordinary memory.
+ *  - Device work is enqueued on the caller's stream (a cudaStream_t passed as
+ *    void*; NULL is the legacy default stream) and returns before it finishes.
+ *  - Host metadata (block tables, refcounts, HOT free list, plans) is owned by
+ *    the library.  A pool and its plans are not thread-safe.
+ *  - bf16 is passed as raw 16-bit storage (void*); fp32 as float*.
+ *
+ * Layouts (all row-major, d = head_dim, Hkv = num_kv_heads, L = num_layers):
+ *  - HOT K and V: [hot_tokens * L * Hkv * d] bf16 each.  A prefix at token base
+ *    b with Lp tokens owns elements [b*L*Hkv*d, (b+Lp)*L*Hkv*d), laid out
+ *    [L][Hkv][Lp][d], so the (layer, head) slice is one contiguous [Lp][d]
+ *    block ("base + l*Lp*Hkv + h*Lp" of Section 3.2 with the allocator
+ *    counting tokens).
+ *  - COLD K and V: [L][cold_slots][Hkv][d] bf16 each; the slot of token t of a
+ *    sequence is table[t / P] * P + t % P with P = cold_page_size
+ *    ("Paged KV cache", How it works).
+ *  - Queries [B][Hq][d] bf16, outputs [B][Hq][d] fp32, LSE [B][Hq] fp32
+ *    (natural log).  Query head qh reads KV head qh / (Hq / Hkv).
+ */
+#ifndef GK_H_
+#define GK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gk_status {
+  GK_OK = 0,
+  GK_ERR_INVALID = 1,        /* bad argument, unknown id, inconsistent sizes */
+  GK_ERR_OOM = 2,            /* COLD pool out of blocks: preempt a sequence ("Paged KV cache", step 4) */
+  GK_ERR_HOT_FULL = 3,       /* no HOT range fits: place the prefix in COLD (GraniKV Appendix B.10) */
+  GK_ERR_CUDA = 4,           /* a CUDA runtime or driver call failed */
+  GK_ERR_DEVICE_BOUNDS = 5,  /* a kernel met an out-of-range block or slot id and skipped it */
+  GK_ERR_TIMEOUT = 6,        /* a kernel's bounded wait ran out; its results are not valid */
+  GK_ERR_UNSUPPORTED = 7     /* geometry the kernels were not built for */
+} gk_status;
+
+typedef enum gk_backend {
+  GK_BACKEND_DENSE = 0,      /* flat paged attention: every request reads its whole context */
+  GK_BACKEND_CASCADE = 1     /* shared-prefix contraction + suffix gather + LSE merge */
+} gk_backend;
+
+typedef struct gk_pool gk_pool;
+typedef struct gk_plan gk_plan;
+
+typedef struct gk_pool_config {
+  int32_t num_layers;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;      /* 1..8, divides num_q_heads */
+  int32_t head_dim;          /* 64 or 128; Hq/Hkv in {1,2,4} at 64, {1,2,4,5,8} at 128 */
+  int64_t hot_tokens;        /* HOT capacity in tokens */
+  int64_t cold_slots;        /* COLD capacity in token slots; a multiple of cold_page_size */
+  int32_t cold_page_size;    /* P: tokens per COLD block (GraniKV uses 1; "Paged KV cache" uses 16) */
+  int32_t reserved0;
+  uint64_t seed;             /* 0: blocks are handed out 0,1,2,...; otherwise in a splitmix64-driven
+                                Fisher-Yates order (shuffled physical slots) */
+  void *hot_k, *hot_v;       /* device, layouts above; all four NULL = host-only pool (bookkeeping,
+                                planning and dispatch work without a GPU) */
+  void *cold_k, *cold_v;
+} gk_pool_config;
+
+/* ---- pool ------------------------------------------------------------------ */
+
+/* Create a pool over caller-allocated storage.  Does not touch the device
+ * contents.  *out is owned by the caller and freed with gk_pool_destroy. */
+gk_status gk_pool_create(const gk_pool_config* cfg, gk_pool** out);
+void gk_pool_destroy(gk_pool* pool);
+/* Text of the pool's last error ("" if none); valid until the next call on the pool. */
+const char* gk_last_error(const gk_pool* pool);
+const char* gk_status_string(gk_status s);
+
+/* ---- HOT pool (GraniKV Section 3.2; first-fit packing, Appendix B.8b) -------- */
+
+/* Reserve prefix_len contiguous tokens: first fit over the address-ordered,
+ * coalesced free list, else the bump pointer.  GK_ERR_HOT_FULL when nothing fits
+ * (the caller keeps the prefix in COLD; no demotion, Appendix B.10). */
+gk_status gk_prefix_alloc(gk_pool* pool, int64_t prefix_len, int64_t* hot_base);
+/* Return a prefix's range; it merges with adjacent free ranges, and a range
+ * ending at the bump pointer lowers it. */
+gk_status gk_prefix_release(gk_pool* pool, int64_t hot_base);
+gk_status gk_hot_stats(const gk_pool* pool, int64_t* bump_top, int64_t* free_ranges,
+                       int64_t* free_tokens);
+
+/* ---- COLD pool block manager ("Paged KV cache", How it works steps 1-4; Code) - */
+
+gk_status gk_seq_create(gk_pool* pool, int32_t* seq);
+/* Child shares every block of parent (refcount + 1); nothing is copied. */
+gk_status gk_seq_fork(gk_pool* pool, int32_t parent, int32_t* child);
+/* Drop one reference to every block of seq; blocks reaching zero return to the
+ * free list (most recently freed is handed out first).  The id becomes invalid. */
+gk_status gk_seq_release(gk_pool* pool, int32_t seq);
+/* Borrow seq's block table (valid until the next call that changes the pool). */
+gk_status gk_seq_table(const gk_pool* pool, int32_t seq, const int32_t** table, int32_t* nblocks,
+                       int64_t* len);
+/* Reserve one slot for each entry of seqs[0..n) in order (a sequence may repeat).
+ * slot_mapping_out[i] receives the slot of that token.  When the token lands in
+ * a shared partial block, the sequence first takes a fresh block; the pair
+ * (shared, fresh) is appended to cow_pairs_out (capacity 2*n int32) and counted
+ * in *n_cow.  GK_ERR_OOM: the first failing entry is reported in *n_done and the
+ * entries before it stay applied (so the caller can preempt and retry the rest);
+ * *n_done = n on success.  n_done may be NULL. */
+gk_status gk_seq_append_slots(gk_pool* pool, int32_t n, const int32_t* seqs, int64_t* slot_mapping_out,
+                              int32_t* n_cow, int32_t* cow_pairs_out, int32_t* n_done);
+/* Block tables of n sequences as one row-major [n][max_blocks] int32 array
+ * (rows padded with block 0 past each table's end; the padding is never read
+ * because a request reads only its own length) and their lengths in tokens.
+ * GK_ERR_INVALID if a table is longer than max_blocks. */
+gk_status gk_seq_tables(const gk_pool* pool, int32_t n, const int32_t* seqs, int32_t max_blocks,
+                        int32_t* table_out, int32_t* len_out);
+gk_status gk_cold_stats(const gk_pool* pool, int64_t* free_blocks, int64_t* total_blocks);
+gk_status gk_block_refcount(const gk_pool* pool, int32_t block, int32_t* refcount);
+
+/* ---- KV writes (device) ---------------------------------------------------- */
+
+/* reshape_and_cache ("Paged KV cache", step 1) for one layer: first copy every
+ * copy-on-write pair's whole source block to its destination block, then write
+ * token i's K and V [Hkv][d] to COLD slot d_slot_mapping[i].
+ * d_slot_mapping: device int64 [n]; d_k, d_v: device bf16 [n][Hkv][d];
+ * d_cow_pairs: device int32 [n_cow][2] (src, dst) or NULL when n_cow = 0.
+ * Out-of-range slots or blocks are skipped and reported as GK_ERR_DEVICE_BOUNDS
+ * by gk_device_error(). */
+gk_status gk_append_kv(gk_pool* pool, void* stream, int32_t layer, int32_t n, const int64_t* d_slot_mapping,
+                       const void* d_k, const void* d_v, int32_t n_cow, const int32_t* d_cow_pairs);
+/* Write prefix tokens [t0, t0+n) of one layer into the HOT slab at hot_base
+ * (a range from gk_prefix_alloc of prefix_len tokens).  d_k, d_v: device bf16
+ * [n][Hkv][d] (token-major, the same input layout as gk_append_kv). */
+gk_status gk_write_prefix_kv(gk_pool* pool, void* stream, int32_t layer, int64_t hot_base,
+                             int64_t prefix_len, int64_t t0, int64_t n, const void* d_k, const void* d_v);
+
+/* ---- one decode step ------------------------------------------------------- */
+
+typedef struct gk_batch {
+  int32_t num_requests;           /* B */
+  int32_t max_blocks;             /* row stride of d_block_table */
+  const int64_t* prefix_hot_base; /* host [B]: HOT base of the request's shared prefix, -1 = none */
+  const int32_t* prefix_len;      /* host [B]: its length in tokens (0 when the base is -1) */
+  const int32_t* suffix_len;      /* host [B]: tokens the request reads from COLD */
+  const int32_t* d_block_table;   /* device [B][max_blocks]: COLD block ids of each request */
+  const void* d_q;                /* device bf16 [B][Hq][d] (this layer's queries) */
+  float* d_out;                   /* device fp32 [B][Hq][d] */
+  float* d_lse;                   /* device fp32 [B][Hq], natural log; may be NULL */
+} gk_batch;
+
+typedef struct gk_plan_summary {
+  int32_t num_requests;
+  int32_t num_groups;             /* distinct HOT prefixes in the step */
+  int32_t max_m_eff;              /* largest M_eff = B_g * Hq/Hkv over the groups (GraniKV Eq. 2) */
+  int32_t prefix_ctas;            /* cascade prefix-kernel CTAs per layer */
+  int32_t suffix_ctas;            /* suffix-gather CTAs per layer */
+  int32_t dense_ctas;             /* flat-gather CTAs per layer */
+  int32_t num_partials;           /* partial (O, LSE) states the merge combines per layer */
+  int32_t dense_merge;            /* 1 if gk_decode_dense launches a merge (a request spans CTAs) */
+  int64_t prefix_bytes;           /* algorithmic bytes per layer: HOT K+V read once per group */
+  int64_t prefix_flops;           /* 4 * B_g * Hq * Lp * d summed over groups */
+  int64_t suffix_bytes;           /* COLD K+V of all suffixes */
+  int64_t dense_bytes;            /* K+V of every request's whole context */
+} gk_plan_summary;
+
+/* Plan one decode step: group requests by HOT prefix (stable, first appearance),
+ * split the prefix contraction and the gathers into balanced CTA work lists,
+ * and lay out the partial states.  Depends only on the host arrays of the
+ * batch, so one plan serves every layer of the step.  When the pool has device
+ * storage the plan's tables are copied to the device on `stream` and scratch
+ * for the partial states is allocated (owned by the plan).  Calls that use a
+ * plan must be ordered on one stream. */
+gk_status gk_plan_build(gk_pool* pool, const gk_batch* batch, void* stream, gk_plan** out);
+/* Re-plan an existing plan for the next step (same pool), reusing its host and
+ * device buffers when they are large enough.  Must be called on the stream the
+ * plan's earlier work was enqueued on: the new tables are copied after that work. */
+gk_status gk_plan_update(gk_plan* plan, const gk_batch* batch, void* stream);
+/* Frees the plan's buffers; its enqueued work must have completed. */
+void gk_plan_destroy(gk_plan* plan);
+gk_status gk_plan_info(const gk_plan* plan, gk_plan_summary* out);
+
+/* Flat paged attention (the dense backend): each request attends its prefix
+ * (read from HOT, once per request) and its COLD suffix in one online-softmax
+ * pass; writes d_out and d_lse of the batch for this layer. */
+gk_status gk_decode_dense(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch,
+                          const gk_plan* plan);
+/* Cascade backend: (a) per prefix group and KV head, all query rows sharing the
+ * prefix are stacked into one QK^T / PV contraction on the tensor cores, read
+ * once from HOT (GraniKV Section 2.3, shared-prefix matmul; Section 3.5);
+ * (b) the suffix is gathered through the block table; (c) the partial states
+ * are merged by log-sum-exp (GraniKV Eq. 1). */
+gk_status gk_decode_cascade(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch,
+                            const gk_plan* plan);
+/* The three stages of gk_decode_cascade, for callers that time them or run
+ * (a) and (b) on two streams: the prefix and suffix stages write disjoint
+ * partial states, and the merge must follow both.  gk_decode_cascade is
+ * exactly prefix, suffix, merge on one stream. */
+gk_status gk_cascade_prefix(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch,
+                            const gk_plan* plan);
+gk_status gk_cascade_suffix(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch,
+                            const gk_plan* plan);
+gk_status gk_cascade_merge(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch,
+                           const gk_plan* plan);
+
+/* ---- per-step dispatch (GraniKV Section 3.6, Eq. 2) -------------------------- */
+
+typedef struct gk_cost_model {
+  double c_flat_us;               /* fixed cost of the dense backend per layer */
+  double bw_flat_gbs;             /* its sustained gather bandwidth */
+  double c_cascade_us;            /* fixed cost of the cascade backend per layer */
+  double bw_prefix_gbs;           /* prefix-kernel HOT read bandwidth */
+  double bw_suffix_gbs;           /* suffix gather bandwidth */
+  double c_merge_us;              /* merge cost per (request, query head) */
+  int32_t n_tc_points;            /* 1..16 */
+  int32_t reserved0;
+  double tc_m[16];                /* M_eff of each calibration point, increasing */
+  double tc_tflops[16];           /* achieved prefix-kernel TFLOP/s at that M_eff */
+} gk_cost_model;
+
+/* Predict both backends for the plan and pick the smaller:
+ *   T_dense   = c_flat + dense_bytes / bw_flat
+ *   T_cascade = c_cascade + sum_g max(prefix_bytes_g / bw_prefix, prefix_flops_g / TC(M_eff_g))
+ *               + suffix_bytes / bw_suffix + c_merge * B * Hq
+ * TC is piecewise linear through the points (proportional below the first,
+ * flat above the last).  Dense is chosen only when strictly faster.  Host only. */
+gk_status gk_dispatch(const gk_pool* pool, const gk_plan* plan, gk_backend* choice, double* t_dense_us,
+                      double* t_cascade_us);
+gk_status gk_cost_model_set(gk_pool* pool, const gk_cost_model* cm);
+gk_status gk_cost_model_get(const gk_pool* pool, gk_cost_model* cm);
+/* Same as gk_cost_model_set from JSON text: {"c_flat_us": .., "bw_flat_gbs": ..,
+ * "c_cascade_us": .., "bw_prefix_gbs": .., "bw_suffix_gbs": .., "c_merge_us": ..,
+ * "tc_points": [[M, TFLOP/s], ...]}. */
+gk_status gk_cost_model_load(gk_pool* pool, const char* json);
+
+/* ---- device error word -------------------------------------------------------- */
+
+/* Synchronize `stream`, read and clear the pool's device error word.  *code is
+ * GK_OK, GK_ERR_DEVICE_BOUNDS or GK_ERR_TIMEOUT; the return value reports
+ * failures of the read itself. */
+gk_status gk_device_error(gk_pool* pool, void* stream, int32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GK_H_ */

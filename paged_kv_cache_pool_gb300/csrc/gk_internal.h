@@ -1,0 +1,176 @@
+// Internal declarations shared by the host runtime (.cpp) and the kernel
+// launchers (.cu) of libgk.  Nothing here is part of the public ABI.
+#pragma once
+
+#include <cuda_runtime_api.h>
+
+#include <cstdint>
+#include <string>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/gk.h"
+
+namespace gk {
+
+// ---- HOT allocator (GraniKV Section 3.2, Appendix B.8b) ----------------------
+struct HotAllocator {
+  int64_t capacity = 0;
+  int64_t top = 0;                                  // bump pointer
+  std::vector<std::pair<int64_t, int64_t>> free;    // address-ordered [start, end), coalesced
+  std::unordered_map<int64_t, int64_t> live;        // base -> length
+
+  bool alloc(int64_t n, int64_t* base);
+  bool release(int64_t base);
+};
+
+// ---- COLD block manager ("Paged KV cache", How it works; Code) ---------------
+struct Sequence {
+  std::vector<int32_t> table;
+  int64_t len = 0;
+  bool alive = false;
+};
+
+struct BlockManager {
+  int32_t page = 1;
+  std::vector<int32_t> free_stack;   // back() is handed out next
+  std::vector<int32_t> ref;
+  std::vector<Sequence> seqs;
+  std::vector<int32_t> free_seq_ids;
+
+  void init(int64_t n_blocks, int32_t page_size, uint64_t seed);
+  int32_t take();                    // -1 when empty
+  void drop(int32_t b);
+};
+
+// ---- geometry-dependent kernel limits ---------------------------------------
+constexpr int kPrefixTileM = 128;    // stacked query rows per tensor-core tile
+constexpr int kPrefixTileN = 128;    // prefix keys per tile
+constexpr int kMaxKvHeads = 8;
+
+struct DeviceInfo {
+  int device = -1;
+  int num_sms = 152;
+  bool queried = false;
+};
+
+struct Pool {
+  gk_pool_config cfg{};
+  bool has_device = false;
+  HotAllocator hot;
+  BlockManager cold;
+  gk_cost_model cost{};
+  std::string last_error;
+  DeviceInfo dev;
+  int32_t* d_error = nullptr;        // device error word (allocated on first device use)
+  int32_t g() const { return cfg.num_q_heads / cfg.num_kv_heads; }
+};
+
+// ---- plan ---------------------------------------------------------------------
+// Device-side records (plain structs, copied with one H2D memcpy).
+struct PrefixGroupDev {
+  int32_t lp;          // prefix length (keys)
+  int32_t m;           // stacked rows B_g * g
+  int32_t req_base;    // offset into prefix_reqs
+  int32_t nsplit;      // splits over the prefix keys
+  int32_t split_tiles; // key tiles (of kPrefixTileN) per split
+  int32_t tmap_index;  // index of the group's K tensor map (V follows)
+  int32_t pad0, pad1;
+};
+
+struct PrefixItemDev {  // one CTA of the tensor-core prefix kernel
+  int32_t group;
+  int32_t mtile;
+  int32_t head;
+  int32_t split;
+};
+
+struct SegmentDev {     // one contiguous run of one request's tokens inside a gather CTA
+  int32_t req;
+  int32_t t0, t1;      // token range in the request's own order (dense: prefix then suffix)
+  int32_t entry;       // partial-state index, or -1 = write the final output directly
+};
+
+struct RequestDev {
+  int64_t hot_base;    // -1 = no HOT prefix
+  int32_t lp;          // HOT prefix tokens (0 when none)
+  int32_t slen;        // COLD tokens
+  int32_t entry_cas;   // first partial entry in the cascade layout
+  int32_t n_entry_cas;
+  int32_t entry_dense;
+  int32_t n_entry_dense;
+};
+
+struct Plan {
+  Pool* pool = nullptr;
+  int32_t B = 0;
+  gk_plan_summary summary{};
+  // host mirrors
+  std::vector<PrefixGroupDev> groups;
+  std::vector<int64_t> group_hot_base;
+  std::vector<int32_t> prefix_reqs;      // requests of each group, concatenated
+  std::vector<PrefixItemDev> prefix_items;
+  std::vector<RequestDev> reqs;
+  std::vector<int32_t> suf_seg_begin;    // [suffix_ctas + 1]
+  std::vector<SegmentDev> suf_segs;
+  std::vector<int32_t> dense_seg_begin;  // [dense_ctas + 1]
+  std::vector<SegmentDev> dense_segs;
+  int32_t n_entries_cas = 0, n_entries_dense = 0;
+  bool dense_needs_merge = false;
+  std::vector<int64_t> group_bytes, group_flops;
+  // device copies
+  void* d_buf = nullptr;
+  void* h_stage = nullptr;               // pinned staging of the device tables
+  cudaEvent_t upload_done = nullptr;     // the last upload has left h_stage
+  bool staged = false;
+  size_t d_bytes = 0;
+  size_t off_groups = 0, off_prefix_reqs = 0, off_prefix_items = 0, off_reqs = 0;
+  size_t off_suf_begin = 0, off_suf_segs = 0, off_dense_begin = 0, off_dense_segs = 0;
+  size_t off_tmaps = 0;
+  float* d_part_o = nullptr;             // [entries][Hq][d]
+  float* d_part_l = nullptr;             // [entries][Hq] (log2 domain)
+  size_t part_entries = 0;
+  bool uploaded = false;
+};
+
+// ---- status helpers -------------------------------------------------------------
+gk_status fail(Pool* p, gk_status s, const std::string& msg);
+gk_status cuda_fail(Pool* p, int err, const char* what);
+gk_status ensure_device(Pool* p);
+
+// ---- kernel launchers (.cu) --------------------------------------------------------
+struct LaunchCommon {
+  const gk_pool_config* cfg;
+  int32_t* d_error;
+  int num_sms;
+};
+
+int launch_cow_copy(const LaunchCommon& lc, void* stream, int32_t layer, int32_t n_cow,
+                    const int32_t* d_pairs);
+int launch_scatter(const LaunchCommon& lc, void* stream, int32_t layer, int32_t n,
+                   const int64_t* d_slots, const void* d_k, const void* d_v);
+int launch_write_prefix(const LaunchCommon& lc, void* stream, int32_t layer, int64_t base,
+                        int64_t lp, int64_t t0, int64_t n, const void* d_k, const void* d_v);
+
+// gather attention over COLD (and HOT when dense) tokens; writes partials or outputs
+int launch_gather(const LaunchCommon& lc, void* stream, int32_t layer, const gk_batch* b,
+                  const Plan* plan, bool dense);
+int launch_merge(const LaunchCommon& lc, void* stream, const gk_batch* b, const Plan* plan,
+                 bool dense);
+int launch_prefix(const LaunchCommon& lc, void* stream, int32_t layer, const gk_batch* b,
+                  const Plan* plan);
+// resident gather CTAs per SM for the pool's geometry (from its shared-memory
+// footprint; no device query, so host-only pools plan identically)
+int gather_ctas_per_sm(const gk_pool_config* cfg);
+// encode the tensor maps of a plan's prefix groups into host memory (128 B each)
+int encode_prefix_tmaps(const gk_pool_config* cfg, const Plan* plan, std::vector<uint8_t>* out);
+size_t tmap_bytes();
+
+}  // namespace gk
+
+struct gk_pool {
+  gk::Pool impl;
+};
+struct gk_plan {
+  gk::Plan impl;
+};

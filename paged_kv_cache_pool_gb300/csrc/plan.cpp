@@ -1,0 +1,585 @@
+// Per-step planner, dispatcher and the decode entry points of libgk.
+//
+// One plan per decode step, reused by every layer (the plan depends only on
+// which requests share which prefix and on the context lengths).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cctype>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <unordered_map>
+
+#include "gk_internal.h"
+
+namespace gk {
+
+namespace {
+
+constexpr int kGatherQuantum = 16;        // gather CTAs get token quotas in multiples of this
+constexpr int kMinGatherQuota = 64;
+constexpr double kPrefixCtaOverheadTiles = 1.5;
+
+template <class T>
+size_t append_region(size_t* off, size_t count, size_t align = 16) {
+  size_t o = (*off + align - 1) / align * align;
+  *off = o + count * sizeof(T);
+  return o;
+}
+
+// Split the concatenated token stream of all requests (lengths n[r]) into CTA
+// quotas; each CTA's slice becomes one segment per request it touches.
+void partition_tokens(const std::vector<int64_t>& n, int64_t max_ctas, std::vector<int32_t>* begin,
+                      std::vector<SegmentDev>* segs) {
+  begin->clear();
+  segs->clear();
+  int64_t total = 0;
+  for (int64_t x : n) total += x;
+  begin->push_back(0);
+  if (total == 0) return;
+  int64_t quota = (total + max_ctas - 1) / max_ctas;
+  quota = std::max<int64_t>(quota, kMinGatherQuota);
+  quota = (quota + kGatherQuantum - 1) / kGatherQuantum * kGatherQuantum;
+  int64_t left = quota;
+  for (size_t r = 0; r < n.size(); ++r) {
+    int64_t t = 0;
+    while (t < n[r]) {
+      int64_t take = std::min(left, n[r] - t);
+      segs->push_back(SegmentDev{(int32_t)r, (int32_t)t, (int32_t)(t + take), -1});
+      t += take;
+      left -= take;
+      if (left == 0) {
+        begin->push_back((int32_t)segs->size());
+        left = quota;
+      }
+    }
+  }
+  if (begin->back() != (int32_t)segs->size()) begin->push_back((int32_t)segs->size());
+}
+
+}  // namespace
+
+static gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
+  const gk_pool_config& c = p->cfg;
+  const int32_t B = b->num_requests;
+  const int32_t Hkv = c.num_kv_heads, Hq = c.num_q_heads, d = c.head_dim, g = Hq / Hkv;
+  const int64_t P = c.cold_page_size;
+  if (B < 0) return fail(p, GK_ERR_INVALID, "num_requests < 0");
+  if (B > 0 && (!b->prefix_hot_base || !b->prefix_len || !b->suffix_len))
+    return fail(p, GK_ERR_INVALID, "batch host arrays missing");
+  pl->pool = p;
+  pl->B = B;
+  pl->groups.clear();
+  pl->group_hot_base.clear();
+  pl->prefix_reqs.clear();
+  pl->prefix_items.clear();
+  pl->reqs.assign((size_t)B, RequestDev{});
+  pl->group_bytes.clear();
+  pl->group_flops.clear();
+
+  // ---- validate and group by HOT prefix (stable: first appearance) -------------
+  std::unordered_map<int64_t, int32_t> gid;
+  std::vector<std::vector<int32_t>> members;
+  for (int32_t r = 0; r < B; ++r) {
+    int64_t base = b->prefix_hot_base[r];
+    int32_t lp = b->prefix_len[r], s = b->suffix_len[r];
+    if (s < 0) return fail(p, GK_ERR_INVALID, "negative suffix length");
+    if ((int64_t)s > (int64_t)b->max_blocks * P)
+      return fail(p, GK_ERR_INVALID, "suffix longer than the block-table row");
+    RequestDev& rq = pl->reqs[(size_t)r];
+    rq.hot_base = base;
+    rq.slen = s;
+    if (base < 0) {
+      if (lp != 0) return fail(p, GK_ERR_INVALID, "prefix_len must be 0 without a HOT prefix");
+      rq.hot_base = -1;
+      rq.lp = 0;
+      continue;
+    }
+    auto it = p->hot.live.find(base);
+    if (it == p->hot.live.end() || it->second != lp)
+      return fail(p, GK_ERR_INVALID, "request names a HOT prefix that is not live with that length");
+    rq.lp = lp;
+    auto f = gid.find(base);
+    int32_t grp;
+    if (f == gid.end()) {
+      grp = (int32_t)members.size();
+      gid[base] = grp;
+      members.emplace_back();
+      pl->group_hot_base.push_back(base);
+    } else {
+      grp = f->second;
+    }
+    members[(size_t)grp].push_back(r);
+  }
+
+  // ---- prefix contraction work: choose keys per split to balance the SMs --------
+  const int num_sms = p->dev.num_sms;
+  const int32_t G = (int32_t)members.size();
+  std::vector<int32_t> mtiles((size_t)G), ntiles((size_t)G);
+  int32_t max_ntiles = 1;
+  for (int32_t gi = 0; gi < G; ++gi) {
+    int32_t m = (int32_t)members[(size_t)gi].size() * g;
+    int32_t lp = pl->reqs[(size_t)members[(size_t)gi][0]].lp;
+    mtiles[(size_t)gi] = (m + kPrefixTileM - 1) / kPrefixTileM;
+    ntiles[(size_t)gi] = (lp + kPrefixTileN - 1) / kPrefixTileN;
+    max_ntiles = std::max(max_ntiles, ntiles[(size_t)gi]);
+  }
+  int32_t best_c = max_ntiles;
+  double best_cost = 1e300;
+  if (G > 0) {
+    for (int32_t C = 1; C <= max_ntiles; ++C) {
+      int64_t units = 0;
+      for (int32_t gi = 0; gi < G; ++gi)
+        units += (int64_t)mtiles[(size_t)gi] * Hkv * ((ntiles[(size_t)gi] + C - 1) / C);
+      int64_t waves = (units + num_sms - 1) / num_sms;
+      double cost = (double)waves * (C + kPrefixCtaOverheadTiles);
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best_c = C;
+      }
+    }
+  }
+  int32_t max_m = 0;
+  int64_t pre_bytes = 0, pre_flops = 0;
+  for (int32_t gi = 0; gi < G; ++gi) {
+    PrefixGroupDev gd{};
+    gd.lp = pl->reqs[(size_t)members[(size_t)gi][0]].lp;
+    gd.m = (int32_t)members[(size_t)gi].size() * g;
+    gd.req_base = (int32_t)pl->prefix_reqs.size();
+    gd.split_tiles = best_c;
+    gd.nsplit = (ntiles[(size_t)gi] + best_c - 1) / best_c;
+    gd.tmap_index = 2 * gi;
+    for (int32_t r : members[(size_t)gi]) pl->prefix_reqs.push_back(r);
+    pl->groups.push_back(gd);
+    max_m = std::max(max_m, gd.m);
+    int64_t gb = (int64_t)gd.lp * 2 * Hkv * d * 2;
+    int64_t gf = 4LL * (int64_t)members[(size_t)gi].size() * Hq * gd.lp * d;
+    pl->group_bytes.push_back(gb);
+    pl->group_flops.push_back(gf);
+    pre_bytes += gb;
+    pre_flops += gf;
+  }
+  // CTA order: longest splits first; within a length, (group, split, head, mtile)
+  // so CTAs reading the same K/V tiles run side by side.
+  struct Item { PrefixItemDev it; int32_t tiles; };
+  std::vector<Item> items;
+  for (int32_t gi = 0; gi < G; ++gi) {
+    const PrefixGroupDev& gd = pl->groups[(size_t)gi];
+    for (int32_t s = 0; s < gd.nsplit; ++s) {
+      int32_t t0 = s * gd.split_tiles;
+      int32_t t1 = std::min(ntiles[(size_t)gi], t0 + gd.split_tiles);
+      for (int32_t h = 0; h < Hkv; ++h)
+        for (int32_t mt = 0; mt < mtiles[(size_t)gi]; ++mt) items.push_back({PrefixItemDev{gi, mt, h, s}, t1 - t0});
+    }
+  }
+  std::stable_sort(items.begin(), items.end(), [](const Item& a, const Item& b2) { return a.tiles > b2.tiles; });
+  for (auto& it : items) pl->prefix_items.push_back(it.it);
+
+  // ---- gather work: cascade suffix and dense (flat) ------------------------------
+  int64_t max_ctas = (int64_t)num_sms * std::max(1, gather_ctas_per_sm(&c));
+  std::vector<int64_t> n_suf((size_t)B), n_dense((size_t)B);
+  int64_t suf_tokens = 0, dense_tokens = 0;
+  for (int32_t r = 0; r < B; ++r) {
+    n_suf[(size_t)r] = pl->reqs[(size_t)r].slen;
+    n_dense[(size_t)r] = (int64_t)pl->reqs[(size_t)r].lp + pl->reqs[(size_t)r].slen;
+    suf_tokens += n_suf[(size_t)r];
+    dense_tokens += n_dense[(size_t)r];
+  }
+  partition_tokens(n_suf, max_ctas, &pl->suf_seg_begin, &pl->suf_segs);
+  partition_tokens(n_dense, max_ctas, &pl->dense_seg_begin, &pl->dense_segs);
+
+  // ---- partial-state entries ----------------------------------------------------
+  // cascade: request r owns [entry_cas, entry_cas + n_entry_cas): its prefix
+  // splits first, then its suffix segments.
+  std::vector<int32_t> nseg_suf((size_t)B, 0), nseg_dense((size_t)B, 0);
+  for (auto& sgm : pl->suf_segs) ++nseg_suf[(size_t)sgm.req];
+  for (auto& sgm : pl->dense_segs) ++nseg_dense[(size_t)sgm.req];
+  int32_t e = 0;
+  std::vector<int32_t> prefix_splits((size_t)B, 0);
+  for (int32_t gi = 0; gi < G; ++gi)
+    for (int32_t r : members[(size_t)gi]) prefix_splits[(size_t)r] = pl->groups[(size_t)gi].nsplit;
+  for (int32_t r = 0; r < B; ++r) {
+    RequestDev& rq = pl->reqs[(size_t)r];
+    rq.entry_cas = e;
+    rq.n_entry_cas = prefix_splits[(size_t)r] + nseg_suf[(size_t)r];
+    e += rq.n_entry_cas;
+  }
+  pl->n_entries_cas = e;
+  std::vector<int32_t> next((size_t)B);
+  for (int32_t r = 0; r < B; ++r) next[(size_t)r] = pl->reqs[(size_t)r].entry_cas + prefix_splits[(size_t)r];
+  for (auto& sgm : pl->suf_segs) sgm.entry = next[(size_t)sgm.req]++;
+  // dense: a request covered by one segment writes its output directly
+  e = 0;
+  pl->dense_needs_merge = false;
+  for (int32_t r = 0; r < B; ++r) {
+    RequestDev& rq = pl->reqs[(size_t)r];
+    rq.entry_dense = e;
+    if (nseg_dense[(size_t)r] == 1) {
+      rq.n_entry_dense = -1;
+    } else {
+      rq.n_entry_dense = nseg_dense[(size_t)r];
+      e += nseg_dense[(size_t)r];
+      pl->dense_needs_merge = true;
+    }
+  }
+  pl->n_entries_dense = e;
+  for (int32_t r = 0; r < B; ++r) next[(size_t)r] = pl->reqs[(size_t)r].entry_dense;
+  for (auto& sgm : pl->dense_segs)
+    sgm.entry = pl->reqs[(size_t)sgm.req].n_entry_dense < 0 ? -1 : next[(size_t)sgm.req]++;
+
+  gk_plan_summary& sm = pl->summary;
+  sm = gk_plan_summary{};
+  sm.num_requests = B;
+  sm.num_groups = G;
+  sm.max_m_eff = max_m;
+  sm.prefix_ctas = (int32_t)pl->prefix_items.size();
+  sm.suffix_ctas = (int32_t)pl->suf_seg_begin.size() - 1;
+  sm.dense_ctas = (int32_t)pl->dense_seg_begin.size() - 1;
+  sm.num_partials = pl->n_entries_cas;
+  sm.dense_merge = pl->dense_needs_merge ? 1 : 0;
+  sm.prefix_bytes = pre_bytes;
+  sm.prefix_flops = pre_flops;
+  sm.suffix_bytes = suf_tokens * 2 * Hkv * d * 2;
+  sm.dense_bytes = dense_tokens * 2 * Hkv * d * 2;
+  return GK_OK;
+}
+
+static gk_status upload_plan(Pool* p, Plan* pl, void* stream) {
+  const gk_pool_config& c = p->cfg;
+  size_t off = 0;
+  pl->off_groups = append_region<PrefixGroupDev>(&off, pl->groups.size());
+  pl->off_prefix_reqs = append_region<int32_t>(&off, pl->prefix_reqs.size());
+  pl->off_prefix_items = append_region<PrefixItemDev>(&off, pl->prefix_items.size());
+  pl->off_reqs = append_region<RequestDev>(&off, pl->reqs.size());
+  pl->off_suf_begin = append_region<int32_t>(&off, pl->suf_seg_begin.size());
+  pl->off_suf_segs = append_region<SegmentDev>(&off, pl->suf_segs.size());
+  pl->off_dense_begin = append_region<int32_t>(&off, pl->dense_seg_begin.size());
+  pl->off_dense_segs = append_region<SegmentDev>(&off, pl->dense_segs.size());
+  std::vector<uint8_t> tmaps;
+  int te = encode_prefix_tmaps(&c, pl, &tmaps);
+  if (te) return fail(p, GK_ERR_CUDA, "encoding the prefix tensor maps failed");
+  pl->off_tmaps = append_region<uint8_t>(&off, tmaps.size(), 128);
+  size_t need = std::max<size_t>(off, 256);
+
+  cudaError_t e;
+  if (need > pl->d_bytes) {
+    if (pl->d_buf) {
+      e = cudaStreamSynchronize((cudaStream_t)stream);
+      if (e != cudaSuccess) return cuda_fail(p, e, "cudaStreamSynchronize");
+      cudaFree(pl->d_buf);
+      cudaFreeHost(pl->h_stage);
+      pl->d_buf = nullptr;
+      pl->h_stage = nullptr;
+    }
+    size_t cap = need + need / 2;
+    e = cudaMalloc(&pl->d_buf, cap);
+    if (e != cudaSuccess) return cuda_fail(p, e, "cudaMalloc(plan)");
+    e = cudaHostAlloc(&pl->h_stage, cap, cudaHostAllocDefault);
+    if (e != cudaSuccess) return cuda_fail(p, e, "cudaHostAlloc(plan staging)");
+    pl->d_bytes = cap;
+  } else if (pl->staged) {
+    // the previous upload must have left the staging buffer before it is rewritten
+    e = cudaEventSynchronize(pl->upload_done);
+    if (e != cudaSuccess) return cuda_fail(p, e, "cudaEventSynchronize");
+  }
+  uint8_t* h = (uint8_t*)pl->h_stage;
+  auto put = [&](size_t o, const void* src, size_t bytes) { if (bytes) std::memcpy(h + o, src, bytes); };
+  put(pl->off_groups, pl->groups.data(), pl->groups.size() * sizeof(PrefixGroupDev));
+  put(pl->off_prefix_reqs, pl->prefix_reqs.data(), pl->prefix_reqs.size() * sizeof(int32_t));
+  put(pl->off_prefix_items, pl->prefix_items.data(), pl->prefix_items.size() * sizeof(PrefixItemDev));
+  put(pl->off_reqs, pl->reqs.data(), pl->reqs.size() * sizeof(RequestDev));
+  put(pl->off_suf_begin, pl->suf_seg_begin.data(), pl->suf_seg_begin.size() * sizeof(int32_t));
+  put(pl->off_suf_segs, pl->suf_segs.data(), pl->suf_segs.size() * sizeof(SegmentDev));
+  put(pl->off_dense_begin, pl->dense_seg_begin.data(), pl->dense_seg_begin.size() * sizeof(int32_t));
+  put(pl->off_dense_segs, pl->dense_segs.data(), pl->dense_segs.size() * sizeof(SegmentDev));
+  put(pl->off_tmaps, tmaps.data(), tmaps.size());
+  e = cudaMemcpyAsync(pl->d_buf, h, off, cudaMemcpyHostToDevice, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(p, e, "plan upload");
+  if (!pl->upload_done) {
+    e = cudaEventCreateWithFlags(&pl->upload_done, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(p, e, "cudaEventCreate");
+  }
+  e = cudaEventRecord(pl->upload_done, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(p, e, "cudaEventRecord");
+  pl->staged = true;
+
+  size_t entries = (size_t)std::max(pl->n_entries_cas, pl->n_entries_dense);
+  if (entries > pl->part_entries) {
+    if (pl->d_part_o) {
+      e = cudaStreamSynchronize((cudaStream_t)stream);
+      if (e != cudaSuccess) return cuda_fail(p, e, "cudaStreamSynchronize");
+      cudaFree(pl->d_part_o);
+      cudaFree(pl->d_part_l);
+      pl->d_part_o = pl->d_part_l = nullptr;
+    }
+    size_t cap = entries + entries / 4 + 16;
+    e = cudaMalloc(&pl->d_part_o, cap * (size_t)c.num_q_heads * c.head_dim * sizeof(float));
+    if (e != cudaSuccess) return cuda_fail(p, e, "cudaMalloc(partial outputs)");
+    e = cudaMalloc(&pl->d_part_l, cap * (size_t)c.num_q_heads * sizeof(float));
+    if (e != cudaSuccess) return cuda_fail(p, e, "cudaMalloc(partial lse)");
+    pl->part_entries = cap;
+  }
+  pl->uploaded = true;
+  return GK_OK;
+}
+
+static gk_status plan_for(Pool* p, Plan* pl, const gk_batch* b, void* stream) {
+  if (p->has_device) {
+    gk_status st = ensure_device(p);
+    if (st != GK_OK) return st;
+  }
+  gk_status st = build_host_plan(p, b, pl);
+  if (st != GK_OK) return st;
+  if (p->has_device) return upload_plan(p, pl, stream);
+  return GK_OK;
+}
+
+static void free_plan_buffers(Plan* pl) {
+  if (pl->d_buf) cudaFree(pl->d_buf);
+  if (pl->h_stage) cudaFreeHost(pl->h_stage);
+  if (pl->d_part_o) cudaFree(pl->d_part_o);
+  if (pl->d_part_l) cudaFree(pl->d_part_l);
+  if (pl->upload_done) cudaEventDestroy(pl->upload_done);
+  pl->d_buf = pl->h_stage = nullptr;
+  pl->d_part_o = pl->d_part_l = nullptr;
+  pl->upload_done = nullptr;
+}
+
+// ---- cost model ----------------------------------------------------------------
+static double tc_at(const gk_cost_model& cm, double M) {
+  int n = cm.n_tc_points;
+  if (M <= cm.tc_m[0]) return cm.tc_tflops[0] * M / cm.tc_m[0];
+  for (int i = 0; i + 1 < n; ++i)
+    if (M <= cm.tc_m[i + 1])
+      return cm.tc_tflops[i] + (cm.tc_tflops[i + 1] - cm.tc_tflops[i]) * (M - cm.tc_m[i]) / (cm.tc_m[i + 1] - cm.tc_m[i]);
+  return cm.tc_tflops[n - 1];
+}
+
+static bool valid_cost_model(const gk_cost_model& cm) {
+  if (cm.n_tc_points < 1 || cm.n_tc_points > 16) return false;
+  if (!(cm.bw_flat_gbs > 0 && cm.bw_prefix_gbs > 0 && cm.bw_suffix_gbs > 0)) return false;
+  for (int i = 0; i < cm.n_tc_points; ++i) {
+    if (!(cm.tc_m[i] > 0 && cm.tc_tflops[i] > 0)) return false;
+    if (i && !(cm.tc_m[i] > cm.tc_m[i - 1])) return false;
+  }
+  return true;
+}
+
+// Minimal JSON reader for the cost-model object (numbers and one array of pairs).
+struct JsonReader {
+  const char* s;
+  bool ok = true;
+  void ws() { while (*s && std::isspace((unsigned char)*s)) ++s; }
+  bool eat(char ch) { ws(); if (*s == ch) { ++s; return true; } return false; }
+  bool str(std::string* out) {
+    ws();
+    if (*s != '"') return false;
+    ++s;
+    out->clear();
+    while (*s && *s != '"') out->push_back(*s++);
+    if (*s != '"') return false;
+    ++s;
+    return true;
+  }
+  bool num(double* v) {
+    ws();
+    char* end = nullptr;
+    *v = std::strtod(s, &end);
+    if (end == s) return false;
+    s = end;
+    return true;
+  }
+};
+
+}  // namespace gk
+
+using gk::Plan;
+using gk::Pool;
+
+extern "C" {
+
+gk_status gk_plan_build(gk_pool* pool, const gk_batch* batch, void* stream, gk_plan** out) {
+  if (!pool || !batch || !out) return GK_ERR_INVALID;
+  *out = nullptr;
+  gk_plan* pl = new (std::nothrow) gk_plan;
+  if (!pl) return GK_ERR_INVALID;
+  gk_status st = gk::plan_for(&pool->impl, &pl->impl, batch, stream);
+  if (st != GK_OK) {
+    gk::free_plan_buffers(&pl->impl);
+    delete pl;
+    return st;
+  }
+  *out = pl;
+  return GK_OK;
+}
+
+gk_status gk_plan_update(gk_plan* plan, const gk_batch* batch, void* stream) {
+  if (!plan || !batch || !plan->impl.pool) return GK_ERR_INVALID;
+  plan->impl.uploaded = false;
+  return gk::plan_for(plan->impl.pool, &plan->impl, batch, stream);
+}
+
+void gk_plan_destroy(gk_plan* plan) {
+  if (!plan) return;
+  gk::free_plan_buffers(&plan->impl);
+  delete plan;
+}
+
+gk_status gk_plan_info(const gk_plan* plan, gk_plan_summary* out) {
+  if (!plan || !out) return GK_ERR_INVALID;
+  *out = plan->impl.summary;
+  return GK_OK;
+}
+
+gk_status gk_dispatch(const gk_pool* pool, const gk_plan* plan, gk_backend* choice, double* t_dense_us,
+                      double* t_cascade_us) {
+  if (!pool || !plan || !choice) return GK_ERR_INVALID;
+  const gk_cost_model& cm = pool->impl.cost;
+  const Plan& pl = plan->impl;
+  double t_flat = cm.c_flat_us + (double)pl.summary.dense_bytes / (cm.bw_flat_gbs * 1e3);
+  double t_pre = 0.0;
+  for (size_t gi = 0; gi < pl.groups.size(); ++gi) {
+    double tb = (double)pl.group_bytes[gi] / (cm.bw_prefix_gbs * 1e3);
+    double tf = (double)pl.group_flops[gi] / (gk::tc_at(cm, (double)pl.groups[gi].m) * 1e6);
+    t_pre += std::max(tb, tf);
+  }
+  double t_cas = cm.c_cascade_us + t_pre + (double)pl.summary.suffix_bytes / (cm.bw_suffix_gbs * 1e3) +
+                 cm.c_merge_us * (double)pl.B * pool->impl.cfg.num_q_heads;
+  *choice = t_flat < t_cas ? GK_BACKEND_DENSE : GK_BACKEND_CASCADE;
+  if (t_dense_us) *t_dense_us = t_flat;
+  if (t_cascade_us) *t_cascade_us = t_cas;
+  return GK_OK;
+}
+
+gk_status gk_cost_model_set(gk_pool* pool, const gk_cost_model* cm) {
+  if (!pool || !cm) return GK_ERR_INVALID;
+  if (!gk::valid_cost_model(*cm)) return gk::fail(&pool->impl, GK_ERR_INVALID, "invalid cost model");
+  pool->impl.cost = *cm;
+  return GK_OK;
+}
+
+gk_status gk_cost_model_get(const gk_pool* pool, gk_cost_model* cm) {
+  if (!pool || !cm) return GK_ERR_INVALID;
+  *cm = pool->impl.cost;
+  return GK_OK;
+}
+
+gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
+  if (!pool || !json) return GK_ERR_INVALID;
+  gk_cost_model cm = pool->impl.cost;
+  gk::JsonReader rd{json};
+  auto bad = [&](const char* why) { return gk::fail(&pool->impl, GK_ERR_INVALID, std::string("cost model JSON: ") + why); };
+  if (!rd.eat('{')) return bad("expected an object");
+  bool first = true;
+  while (true) {
+    if (rd.eat('}')) break;
+    if (!first && !rd.eat(',')) return bad("expected ','");
+    first = false;
+    std::string key;
+    if (!rd.str(&key)) return bad("expected a key");
+    if (!rd.eat(':')) return bad("expected ':'");
+    if (key == "tc_points") {
+      if (!rd.eat('[')) return bad("tc_points must be an array");
+      int n = 0;
+      while (!rd.eat(']')) {
+        if (n && !rd.eat(',')) return bad("expected ',' in tc_points");
+        if (n >= 16) return bad("at most 16 tc_points");
+        double m, t;
+        if (!rd.eat('[') || !rd.num(&m) || !rd.eat(',') || !rd.num(&t) || !rd.eat(']'))
+          return bad("tc_points entries are [M, TFLOP/s]");
+        cm.tc_m[n] = m;
+        cm.tc_tflops[n] = t;
+        ++n;
+      }
+      cm.n_tc_points = n;
+      continue;
+    }
+    double v;
+    if (!rd.num(&v)) {
+      // skip a string value (comments such as "source")
+      std::string tmp;
+      if (!rd.str(&tmp)) return bad("values must be numbers");
+      continue;
+    }
+    if (key == "c_flat_us") cm.c_flat_us = v;
+    else if (key == "bw_flat_gbs") cm.bw_flat_gbs = v;
+    else if (key == "c_cascade_us") cm.c_cascade_us = v;
+    else if (key == "bw_prefix_gbs") cm.bw_prefix_gbs = v;
+    else if (key == "bw_suffix_gbs") cm.bw_suffix_gbs = v;
+    else if (key == "c_merge_us") cm.c_merge_us = v;
+  }
+  return gk_cost_model_set(pool, &cm);
+}
+
+static gk_status check_decode(Pool* p, int32_t layer, const gk_batch* b, const Plan* pl) {
+  if (layer < 0 || layer >= p->cfg.num_layers) return gk::fail(p, GK_ERR_INVALID, "layer out of range");
+  if (pl->pool != p) return gk::fail(p, GK_ERR_INVALID, "plan belongs to another pool");
+  if (!pl->uploaded) return gk::fail(p, GK_ERR_INVALID, "plan has no device tables");
+  if (b->num_requests != pl->B) return gk::fail(p, GK_ERR_INVALID, "batch size differs from the plan");
+  if (pl->B > 0 && (!b->d_q || !b->d_out || !b->d_block_table))
+    return gk::fail(p, GK_ERR_INVALID, "batch device pointers missing");
+  return gk::ensure_device(p);
+}
+
+gk_status gk_cascade_prefix(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch, const gk_plan* plan) {
+  if (!pool || !batch || !plan) return GK_ERR_INVALID;
+  Pool* p = &pool->impl;
+  const Plan* pl = &plan->impl;
+  gk_status st = check_decode(p, layer, batch, pl);
+  if (st != GK_OK) return st;
+  if (pl->prefix_items.empty()) return GK_OK;
+  gk::LaunchCommon lc{&p->cfg, p->d_error, p->dev.num_sms};
+  int e = gk::launch_prefix(lc, stream, layer, batch, pl);
+  return e ? gk::cuda_fail(p, e, "cascade prefix kernel") : GK_OK;
+}
+
+gk_status gk_cascade_suffix(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch, const gk_plan* plan) {
+  if (!pool || !batch || !plan) return GK_ERR_INVALID;
+  Pool* p = &pool->impl;
+  const Plan* pl = &plan->impl;
+  gk_status st = check_decode(p, layer, batch, pl);
+  if (st != GK_OK) return st;
+  if (pl->suf_segs.empty()) return GK_OK;
+  gk::LaunchCommon lc{&p->cfg, p->d_error, p->dev.num_sms};
+  int e = gk::launch_gather(lc, stream, layer, batch, pl, false);
+  return e ? gk::cuda_fail(p, e, "suffix gather kernel") : GK_OK;
+}
+
+gk_status gk_cascade_merge(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch, const gk_plan* plan) {
+  if (!pool || !batch || !plan) return GK_ERR_INVALID;
+  Pool* p = &pool->impl;
+  const Plan* pl = &plan->impl;
+  gk_status st = check_decode(p, layer, batch, pl);
+  if (st != GK_OK) return st;
+  if (pl->B == 0) return GK_OK;
+  gk::LaunchCommon lc{&p->cfg, p->d_error, p->dev.num_sms};
+  int e = gk::launch_merge(lc, stream, batch, pl, false);
+  return e ? gk::cuda_fail(p, e, "merge kernel") : GK_OK;
+}
+
+gk_status gk_decode_cascade(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch, const gk_plan* plan) {
+  gk_status st = gk_cascade_prefix(pool, stream, layer, batch, plan);
+  if (st == GK_OK) st = gk_cascade_suffix(pool, stream, layer, batch, plan);
+  if (st == GK_OK) st = gk_cascade_merge(pool, stream, layer, batch, plan);
+  return st;
+}
+
+gk_status gk_decode_dense(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch, const gk_plan* plan) {
+  if (!pool || !batch || !plan) return GK_ERR_INVALID;
+  Pool* p = &pool->impl;
+  const Plan* pl = &plan->impl;
+  gk_status st = check_decode(p, layer, batch, pl);
+  if (st != GK_OK) return st;
+  if (pl->B == 0) return GK_OK;
+  gk::LaunchCommon lc{&p->cfg, p->d_error, p->dev.num_sms};
+  int e;
+  if (!pl->dense_segs.empty() && (e = gk::launch_gather(lc, stream, layer, batch, pl, true)))
+    return gk::cuda_fail(p, e, "dense gather kernel");
+  if (pl->dense_needs_merge && (e = gk::launch_merge(lc, stream, batch, pl, true)))
+    return gk::cuda_fail(p, e, "merge kernel");
+  return GK_OK;
+}
+
+}  // extern "C"

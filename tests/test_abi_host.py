@@ -1,0 +1,279 @@
+"""The C-ABI library on the host (no GPU): exported symbols, the block manager
+and HOT allocator against the oracle restatements (bit-exact), planning and the
+dispatcher against the oracle formula, and the error paths."""
+import json
+import math
+import random
+import re
+import os
+
+import numpy as np
+import pytest
+
+from conftest import ROOT, golden
+from oracle import dispatch as odisp
+from oracle.block_manager import BlockPool, Seq, initial_order
+from oracle.hot_pool import HotFull, HotPool
+
+
+@pytest.fixture(scope="module")
+def gk():
+    from paged_kv_cache_pool_gb300 import build
+    build.build()
+    from paged_kv_cache_pool_gb300 import binding
+    return binding
+
+
+def test_every_declared_symbol_is_exported(gk):
+    hdr = open(os.path.join(ROOT, "include", "gk.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    names = sorted(set(re.findall(r"\b(gk_[a-z_0-9]+)\s*\(", hdr)))
+    assert len(names) >= 25
+    lib = gk.lib()
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def _pool(gk, n_blocks=64, P=16, seed=0, hot=1000, L=2, Hq=8, Hkv=2, d=128):
+    return gk.gk_pool_create(L, Hq, Hkv, d, hot, n_blocks * P, P, seed)
+
+
+def test_worked_example_through_the_abi(gk):
+    g = golden("paged_kv_worked_example.json")
+    pool = _pool(gk, n_blocks=8, P=16)
+    try:
+        a = gk.gk_seq_create(pool)
+        slots, cow = gk.gk_seq_append_slots(pool, [a] * 20)
+        assert len(cow) == 0 and list(slots) == list(range(20))
+        assert gk.gk_cold_stats(pool) == (6, 8)
+        b = gk.gk_seq_fork(pool, a)
+        slots, cow = gk.gk_seq_append_slots(pool, [b])
+        assert cow.tolist() == [g["derived"]["cow_pair"]] and slots[0] == g["derived"]["child_slot"]
+        ta, _ = gk.gk_seq_table(pool, a)
+        tb, lb = gk.gk_seq_table(pool, b)
+        assert ta.tolist() == g["derived"]["parent_table"] and tb.tolist() == g["derived"]["child_table"]
+        assert lb == 21
+        gk.gk_seq_release(pool, a)
+        gk.gk_seq_release(pool, b)
+        assert gk.gk_cold_stats(pool)[0] == 8
+    finally:
+        gk.gk_pool_destroy(pool)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 7, 12345])
+def test_seeded_initial_order_matches_oracle(gk, seed):
+    pool = _pool(gk, n_blocks=500, P=1, seed=seed)
+    try:
+        s = gk.gk_seq_create(pool)
+        slots, _ = gk.gk_seq_append_slots(pool, [s] * 500)
+        assert slots.tolist() == initial_order(500, seed)
+    finally:
+        gk.gk_pool_destroy(pool)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_block_manager_bit_exact(gk, seed):
+    rnd = random.Random(seed)
+    P = rnd.choice([1, 4, 16])
+    nb = 120
+    pool = _pool(gk, n_blocks=nb, P=P, seed=seed * 3)
+    ref = BlockPool(nb, P, seed * 3)
+    ids = {}      # oracle Seq -> library id
+    live = []
+    try:
+        for _ in range(1500):
+            op = rnd.random()
+            if op < 0.6 and live:
+                batch = [rnd.choice(live) for _ in range(rnd.randint(1, 6))]
+                exp_slots, exp_cow, ok = [], [], True
+                for s in batch:
+                    res = ref.append(s)
+                    if res is None:
+                        ok = False
+                        break
+                    exp_slots.append(res[0])
+                    if res[1]:
+                        exp_cow.append(list(res[1]))
+                try:
+                    slots, cow = gk.gk_seq_append_slots(pool, [ids[id(s)] for s in batch])
+                    assert ok
+                except gk.GkError as e:
+                    assert not ok and e.status == gk.GK_ERR_OOM
+                    slots, cow = e.slots, e.cow_pairs
+                assert slots.tolist() == exp_slots and cow.tolist() == exp_cow
+            elif op < 0.75 and live:
+                parent = rnd.choice(live)
+                child = ref.fork(parent)
+                ids[id(child)] = gk.gk_seq_fork(pool, ids[id(parent)])
+                live.append(child)
+            elif op < 0.88 and live:
+                s = live.pop(rnd.randrange(len(live)))
+                ref.release(s)
+                gk.gk_seq_release(pool, ids.pop(id(s)))
+            else:
+                s = Seq()
+                ids[id(s)] = gk.gk_seq_create(pool)
+                live.append(s)
+            for s in live:
+                t, ln = gk.gk_seq_table(pool, ids[id(s)])
+                assert t.tolist() == s.table and ln == s.len
+            assert gk.gk_cold_stats(pool)[0] == ref.num_free()
+        for b in range(nb):
+            assert gk.gk_block_refcount(pool, b) == ref.ref[b]
+    finally:
+        gk.gk_pool_destroy(pool)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_hot_allocator_bit_exact(gk, seed):
+    rnd = random.Random(100 + seed)
+    cap = 4000
+    pool = _pool(gk, hot=cap)
+    ref = HotPool(cap)
+    live = []
+    try:
+        for _ in range(1500):
+            if live and rnd.random() < 0.45:
+                b = live.pop(rnd.randrange(len(live)))
+                ref.release(b)
+                gk.gk_prefix_release(pool, b)
+            else:
+                n = rnd.randint(1, 300)
+                try:
+                    want = ref.alloc(n)
+                except HotFull:
+                    want = None
+                try:
+                    got = gk.gk_prefix_alloc(pool, n)
+                except gk.GkError as e:
+                    assert e.status == gk.GK_ERR_HOT_FULL
+                    got = None
+                assert got == want
+                if got is not None:
+                    live.append(got)
+            top, nfree, free_tokens = gk.gk_hot_stats(pool)
+            assert top == ref.top and nfree == len(ref.free) and free_tokens == ref.free_tokens()
+    finally:
+        gk.gk_pool_destroy(pool)
+
+
+def test_error_paths(gk):
+    with pytest.raises(gk.GkError) as e:
+        gk.gk_pool_create(1, 6, 4, 128, 10, 16, 16)       # Hq not a multiple of Hkv
+    assert e.value.status == gk.GK_ERR_INVALID
+    with pytest.raises(gk.GkError) as e:
+        gk.gk_pool_create(1, 8, 2, 96, 10, 16, 16)        # head_dim
+    assert e.value.status == gk.GK_ERR_UNSUPPORTED
+    pool = _pool(gk, n_blocks=2, P=4, hot=100)
+    try:
+        with pytest.raises(gk.GkError) as e:
+            gk.gk_prefix_alloc(pool, 101)
+        assert e.value.status == gk.GK_ERR_HOT_FULL
+        with pytest.raises(gk.GkError) as e:
+            gk.gk_prefix_release(pool, 5)
+        assert e.value.status == gk.GK_ERR_INVALID
+        s = gk.gk_seq_create(pool)
+        with pytest.raises(gk.GkError) as e:
+            gk.gk_seq_append_slots(pool, [s] * 9)
+        assert e.value.status == gk.GK_ERR_OOM and e.value.n_done == 8
+        with pytest.raises(gk.GkError):
+            gk.gk_seq_fork(pool, 99)
+        with pytest.raises(gk.GkError):
+            gk.gk_seq_release(pool, 99)
+        # device calls on a host-only pool are refused, not attempted
+        with pytest.raises(gk.GkError) as e:
+            gk.gk_append_kv(pool, None, 0, None, None, None, n=0, n_cow=0)
+        assert e.value.status == gk.GK_ERR_INVALID
+    finally:
+        gk.gk_pool_destroy(pool)
+
+
+def _host_plan(gk, pool, bases, lps, slens, max_blocks=4096):
+    b = gk.Batch(bases, lps, slens, None, max_blocks)
+    plan = gk.gk_plan_build(pool, b)
+    return b, plan
+
+
+def test_plan_summary_against_the_byte_and_flop_model(gk):
+    from oracle import model
+    Hq, Hkv, d, L = 40, 8, 128, 2
+    pool = gk.gk_pool_create(L, Hq, Hkv, d, 100000, 64, 1, 0)
+    try:
+        lp1 = gk.gk_prefix_alloc(pool, 5000)
+        lp2 = gk.gk_prefix_alloc(pool, 300)
+        rnd = random.Random(3)
+        bases, lps, slens, grp = [], [], [], []
+        for r in range(70):
+            c = rnd.choice([0, 1, 2])
+            if c == 0:
+                bases.append(lp1); lps.append(5000); grp.append(0)
+            elif c == 1:
+                bases.append(lp2); lps.append(300); grp.append(1)
+            else:
+                bases.append(-1); lps.append(0); grp.append(-1)
+            slens.append(rnd.randint(0, 3000))
+        b, plan = _host_plan(gk, pool, bases, lps, slens)
+        s = gk.gk_plan_info(plan)
+        g = Hq // Hkv
+        B0, B1 = grp.count(0), grp.count(1)
+        assert s["num_groups"] == 2 and s["max_m_eff"] == max(B0, B1) * g
+        assert s["prefix_bytes"] == model.shared_prefix_bytes(5000, Hkv, d) + model.shared_prefix_bytes(300, Hkv, d)
+        assert s["prefix_flops"] == model.prefix_flops(B0, Hq, 5000, d) + model.prefix_flops(B1, Hq, 300, d)
+        assert s["suffix_bytes"] == model.suffix_kv_bytes(slens, Hkv, d)
+        assert s["dense_bytes"] == model.dense_kv_bytes(lps, slens, Hkv, d)
+        assert 0 < s["suffix_ctas"] <= 152 * 2 and 0 < s["dense_ctas"] <= 152 * 2
+        assert s["prefix_ctas"] >= 2 * Hkv
+        gk.gk_plan_destroy(plan)
+        # a request naming a prefix that is not live is refused
+        with pytest.raises(gk.GkError):
+            _host_plan(gk, pool, [12345], [10], [5])
+    finally:
+        gk.gk_pool_destroy(pool)
+
+
+@pytest.mark.parametrize("case", range(5))
+def test_dispatch_matches_oracle_formula(gk, case):
+    rnd = random.Random(case)
+    Hq, Hkv, d = rnd.choice([(32, 8, 128), (40, 8, 128)])
+    cm = dict(c_flat_us=rnd.uniform(2, 20), bw_flat_gbs=rnd.uniform(3000, 7000), c_cascade_us=rnd.uniform(5, 40),
+              bw_prefix_gbs=rnd.uniform(3000, 7000), bw_suffix_gbs=rnd.uniform(3000, 7000),
+              c_merge_us=rnd.uniform(0, 0.002),
+              tc_points=[[128, rnd.uniform(100, 400)], [512, rnd.uniform(400, 900)], [2048, rnd.uniform(900, 1600)]])
+    pool = gk.gk_pool_create(1, Hq, Hkv, d, 200000, 64, 1, 0)
+    try:
+        gk.gk_cost_model_load(pool, json.dumps(cm))
+        got_cm = gk.gk_cost_model_get(pool)
+        for k in ("c_flat_us", "bw_flat_gbs", "c_cascade_us", "bw_prefix_gbs", "bw_suffix_gbs", "c_merge_us"):
+            assert got_cm[k] == cm[k]
+        assert got_cm["tc_points"] == cm["tc_points"]
+        n_pref = rnd.randint(0, 3)
+        pref = [(gk.gk_prefix_alloc(pool, lp), lp) for lp in [rnd.randint(64, 20000) for _ in range(n_pref)]]
+        B = rnd.randint(1, 300)
+        bases, lps, slens, grp = [], [], [], []
+        for r in range(B):
+            c = rnd.randrange(n_pref + 1) - 1
+            bases.append(pref[c][0] if c >= 0 else -1)
+            lps.append(pref[c][1] if c >= 0 else 0)
+            grp.append(c)
+            slens.append(rnd.randint(0, 4000))
+        b, plan = _host_plan(gk, pool, bases, lps, slens)
+        choice, td, tc = gk.gk_dispatch(pool, plan)
+        f = odisp.features(lps, slens, grp, Hq, Hkv, d)
+        want, wd, wc = odisp.choose(cm, f)
+        assert math.isclose(td, wd, rel_tol=1e-12) and math.isclose(tc, wc, rel_tol=1e-12)
+        assert choice == (gk.GK_BACKEND_DENSE if want == "dense" else gk.GK_BACKEND_CASCADE)
+        gk.gk_plan_destroy(plan)
+    finally:
+        gk.gk_pool_destroy(pool)
+
+
+def test_cost_model_json_rejects_bad_input(gk):
+    pool = _pool(gk)
+    try:
+        for bad in ["", "[1]", '{"c_flat_us": }', '{"tc_points": [[1]]}', '{"bw_flat_gbs": -1}',
+                    '{"tc_points": [[512, 1], [128, 2]]}']:
+            with pytest.raises(gk.GkError) as e:
+                gk.gk_cost_model_load(pool, bad)
+            assert e.value.status == gk.GK_ERR_INVALID
+    finally:
+        gk.gk_pool_destroy(pool)
