@@ -44,6 +44,7 @@ def _args():
     ap.add_argument("--backend", choices=["auto", "cascade", "dense"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="run only this many layers (small profiling case)")
     return ap.parse_args()
 
 
@@ -456,6 +457,9 @@ def main():
     a = _args()
     from synth import workloads
     w = workloads.config(a.config)
+    if a.layers:
+        w.L = a.layers
+        w.name += f"_first{a.layers}layers"
     if a.impl == "reference":
         run_reference(a, w)
     else:

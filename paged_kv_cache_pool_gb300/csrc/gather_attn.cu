@@ -293,37 +293,43 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), (G <= 4 ? 2 : 1)) gath
 // LSE merge (GraniKV Eq. 1, applied to any number of partial states): for each
 // request and query head, O = sum_e 2^(l_e - m) O_e / sum_e 2^(l_e - m),
 // LSE = (m + log2 sum_e 2^(l_e - m)) * ln 2, with m = max_e l_e (log2 domain).
-__global__ void merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_l,
-                             const RequestDev* __restrict__ reqs, int32_t dense, int32_t Hq, int32_t D,
-                             float* __restrict__ out, float* __restrict__ lse) {
-  const int r = blockIdx.x;
+// One warp per (request, query head): lanes first reduce the max over the
+// entries' LSEs, then each lane accumulates its 4-float slice of d.
+__global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_l,
+                                                    const RequestDev* __restrict__ reqs, int32_t B, int32_t dense,
+                                                    int32_t Hq, int32_t D, float* __restrict__ out,
+                                                    float* __restrict__ lse) {
+  const int gw = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= B * Hq) return;
+  const int r = gw / Hq, qh = gw % Hq;
   const RequestDev rq = reqs[r];
   const int e0 = dense ? rq.entry_dense : rq.entry_cas;
   const int ne = dense ? rq.n_entry_dense : rq.n_entry_cas;
   if (ne < 0) return;  // written directly by its only segment
-  const int vecs = D / 4;
-  for (int idx = threadIdx.x; idx < Hq * vecs; idx += blockDim.x) {
-    const int qh = idx / vecs, c = idx % vecs;
-    float mx = -INFINITY;
-    for (int e = 0; e < ne; ++e) mx = fmaxf(mx, part_l[(int64_t)(e0 + e) * Hq + qh]);
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    float z = 0.f;
-    if (mx != -INFINITY) {
-      for (int e = 0; e < ne; ++e) {
-        const float w = ex2(part_l[(int64_t)(e0 + e) * Hq + qh] - mx);
-        const float4 pe = reinterpret_cast<const float4*>(part_o + ((int64_t)(e0 + e) * Hq + qh) * D)[c];
-        o.x = fmaf(w, pe.x, o.x);
-        o.y = fmaf(w, pe.y, o.y);
-        o.z = fmaf(w, pe.z, o.z);
-        o.w = fmaf(w, pe.w, o.w);
-        z += w;
-      }
-      const float inv = 1.f / z;
-      o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
+  float mx = -INFINITY;
+  for (int e = lane; e < ne; e += 32) mx = fmaxf(mx, part_l[(int64_t)(e0 + e) * Hq + qh]);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  const int vecs = D / 4;  // 16 or 32 float4 per row
+  float z = 0.f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (mx != -INFINITY && lane < vecs) {
+#pragma unroll 4
+    for (int e = 0; e < ne; ++e) {
+      const float w = ex2(part_l[(int64_t)(e0 + e) * Hq + qh] - mx);
+      const float4 pe = reinterpret_cast<const float4*>(part_o + ((int64_t)(e0 + e) * Hq + qh) * D)[lane];
+      o.x = fmaf(w, pe.x, o.x);
+      o.y = fmaf(w, pe.y, o.y);
+      o.z = fmaf(w, pe.z, o.z);
+      o.w = fmaf(w, pe.w, o.w);
+      z += w;
     }
-    reinterpret_cast<float4*>(out + ((int64_t)r * Hq + qh) * D)[c] = o;
-    if (c == 0 && lse) lse[(int64_t)r * Hq + qh] = mx == -INFINITY ? -INFINITY : (mx + __log2f(z)) * kLn2;
+    const float inv = 1.f / z;
+    o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
   }
+  if (lane < vecs) reinterpret_cast<float4*>(out + ((int64_t)r * Hq + qh) * D)[lane] = o;
+  if (lane == 0 && lse) lse[(int64_t)r * Hq + qh] = mx == -INFINITY ? -INFINITY : (mx + __log2f(z)) * kLn2;
 }
 
 template <int D, int G>
@@ -404,9 +410,11 @@ int launch_gather(const LaunchCommon& lc, void* stream, int32_t layer, const gk_
 int launch_merge(const LaunchCommon& lc, void* stream, const gk_batch* b, const Plan* pl, bool dense) {
   const gk_pool_config& c = *lc.cfg;
   const uint8_t* base = (const uint8_t*)pl->d_buf;
-  merge_kernel<<<pl->B, 256, 0, (cudaStream_t)stream>>>(pl->d_part_o, pl->d_part_l,
-                                                        (const RequestDev*)(base + pl->off_reqs), dense ? 1 : 0,
-                                                        c.num_q_heads, c.head_dim, b->d_out, b->d_lse);
+  const int64_t warps = (int64_t)pl->B * c.num_q_heads;
+  const int blocks = (int)((warps + 7) / 8);
+  merge_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(pl->d_part_o, pl->d_part_l,
+                                                         (const RequestDev*)(base + pl->off_reqs), pl->B,
+                                                         dense ? 1 : 0, c.num_q_heads, c.head_dim, b->d_out, b->d_lse);
   return (int)cudaGetLastError();
 }
 

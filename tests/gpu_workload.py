@@ -40,7 +40,7 @@ class GpuWorkload:
                 v = torch.empty_like(k)
                 sdev.fill_normal(k, stream_key(w.seed, KIND_PREFIX_K, p, layer))
                 sdev.fill_normal(v, stream_key(w.seed, KIND_PREFIX_V, p, layer))
-                self.eng.write_prefix(layer, self.bases[p], lp, 0, k, v)
+                self.eng.write_prefix(layer, self.bases[p], lp, 0, k.view(lp, w.Hkv, w.d), v.view(lp, w.Hkv, w.d))
         # COLD suffixes: one append call covering every source sequence
         if w.fork_children:
             sources = [(p, n) for p, n in enumerate(w.parents)]
