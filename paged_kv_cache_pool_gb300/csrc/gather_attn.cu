@@ -12,13 +12,22 @@
 // request boundary yields one segment per request.  Each segment produces a
 // partial (O, LSE) state or, when it covers a whole request, the final output.
 //
-// CTA layout: warps 0..Hkv-1 are consumers (warp h = KV head h, its g query
-// heads), warp Hkv is the producer.  The producer moves T tokens per stage
-// into shared memory with bulk async copies (the TMA engine; one 16-byte
-// aligned copy per COLD token row of Hkv*d bf16, or per HOT head run of T*d)
-// and signals an mbarrier; consumers read 16-byte vectors from shared memory,
-// reduce q.k across the lanes of a token with warp shuffles and keep a
-// running max / sum (online softmax) in registers.
+// CTA layout: warps 0..Hkv-1 are consumers (warp h = KV head h and its g query
+// heads), warp Hkv is the producer.  The producer stages 16 tokens at a time in
+// shared memory with the TMA engine: one 16-byte aligned bulk copy per COLD
+// token (its Hkv*d row of K, and of V), rows placed 16 bytes apart modulo 128
+// so that eight consecutive tokens fall in eight different bank groups; HOT
+// runs (dense backend) arrive as 128-byte-swizzled tensor tiles.  Consumers
+// load 8x8 tiles with ldmatrix and run the two small per-head products on the
+// warp-level tensor-core MMA (m16n8k16, bf16 in, fp32 accumulate):
+//   S^T[16 tok x 8] = K[16 tok x d] . Q_h^T[d x 8]   (the g query heads, padded to 8)
+//   O^T[d x 8]     += V^T[d x 16 tok] . P^T[16 tok x 8]
+// with the online softmax (running max, rescale, sum) on the S^T fragments and
+// warp shuffles across the lanes that hold one head.  P^T is re-packed into
+// the B-operand layout with movmatrix.  The K/V rows do not form any operand
+// layout the 5th-generation MMA reads from shared memory (they are 256-byte
+// runs at a 2 KB stride), and this product is 2*g flops per byte: the kernel
+// is bound by HBM, the MMA only keeps the issue slots free for it.
 #include <cfloat>
 
 #include "device_common.cuh"
@@ -27,8 +36,8 @@
 namespace gk {
 namespace {
 
-constexpr int kT = 8;       // tokens per stage
-constexpr int kStages = 3;  // pipeline depth
+constexpr int kT = kGatherT;  // tokens per stage (one m16 / k16 MMA step)
+constexpr int kStages = 3;    // pipeline depth
 
 struct GatherParams {
   const uint16_t* hot_k;
@@ -50,30 +59,66 @@ struct GatherParams {
   const RequestDev* reqs;
   const int32_t* seg_begin;
   const SegmentDev* segs;
+  const uint8_t* tmaps;
   int32_t* err;
   float q_scale;  // log2(e) / sqrt(d): scores come out in the log2 domain
 };
 
-__host__ __device__ constexpr size_t stage_bytes(int hkv, int d) { return (size_t)kT * hkv * d * 2; }
+// shared-memory geometry of one K (or V) stage
+__host__ __device__ constexpr uint32_t cold_row_bytes(int hkv, int d) { return (uint32_t)hkv * d * 2 + 16; }
+__host__ __device__ constexpr uint32_t half_stage_bytes(int hkv, int d) {
+  // max of the COLD rows (kT x row) and the HOT tiles (hkv x d/64 regions of kT x 128 B), 1 KB aligned
+  uint32_t cold = (uint32_t)kT * cold_row_bytes(hkv, d);
+  uint32_t hot = (uint32_t)hkv * (d / 64) * kT * 128;
+  uint32_t m = cold > hot ? cold : hot;
+  return (m + 1023u) & ~1023u;
+}
+__host__ __device__ constexpr size_t gather_smem_bytes(int hkv, int d) {
+  return 1024 + 2 * kStages * (size_t)half_stage_bytes(hkv, d) + 2 * kStages * 8;
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+// D = A(16x16, row) . B(16x8, col) + D ; bf16 in, fp32 accumulate
+__device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
 template <int D, int G>
-__global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), (G <= 4 ? 2 : 1)) gather_kernel(const GatherParams p) {
-  constexpr int LPT = D / 8;     // lanes per token row (one 16-byte vector each)
-  constexpr int TPI = 32 / LPT;  // token rows per warp-wide vector load
-  constexpr int R = kT / TPI;    // rows per lane per stage
-  static_assert(kT % TPI == 0, "stage must hold whole warp loads");
-
-  extern __shared__ __align__(1024) uint8_t smem[];
+__global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1) gather_kernel(const GatherParams p) {
+  constexpr int KSTEPS = D / 16;  // k16 steps of the QK product, m16 tiles of the PV product
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
   const int Hkv = p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t sb = stage_bytes(Hkv, D);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kStages * sb);
-  const uint32_t smem0 = smem_u32(smem);
-  auto k_stage = [&](int s) { return smem0 + (uint32_t)(2 * s * sb); };
-  auto v_stage = [&](int s) { return smem0 + (uint32_t)((2 * s + 1) * sb); };
-  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
-  auto empty_bar = [&](int s) { return smem_u32(&bars[kStages + s]); };
+  const uint32_t hs = half_stage_bytes(Hkv, D);
+  const uint32_t rs = cold_row_bytes(Hkv, D);
+  auto k_stage = [&](int s) { return base + (uint32_t)(2 * s) * hs; };
+  auto v_stage = [&](int s) { return base + (uint32_t)(2 * s + 1) * hs; };
+  const uint32_t bars = base + 2 * kStages * hs;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
 
+  // Zero the stages once: a partial stage leaves rows past its tokens untouched,
+  // and those rows must hold finite values (they meet P = 0 in the MMA).
+  for (uint32_t off = threadIdx.x * 16; off < 2 * kStages * hs; off += blockDim.x * 16)
+    sts128(base + off, make_uint4(0, 0, 0, 0));
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
@@ -81,6 +126,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), (G <= 4 ? 2 : 1)) gath
     }
     fence_mbar_init();
   }
+  fence_async_shared();
   __syncthreads();
 
   const int seg0 = p.seg_begin[blockIdx.x], seg1 = p.seg_begin[blockIdx.x + 1];
@@ -95,92 +141,97 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), (G <= 4 ? 2 : 1)) gath
       const RequestDev rq = p.reqs[seg.req];
       const int lp = p.dense ? rq.lp : 0;
       const int32_t* table = p.block_table + (int64_t)seg.req * p.max_blocks;
+      const uint8_t* tm = rq.group >= 0 ? p.tmaps + (size_t)(4 * rq.group + 2) * 128 : nullptr;
+      if (lp > 0 && lane == 0) {
+        tmap_acquire(tm);
+        tmap_acquire(tm + 128);
+      }
       for (int t = seg.t0; t < seg.t1;) {
         int n = min(kT, seg.t1 - t);
         if (t < lp) n = min(n, lp - t);
         const int s = k % kStages;
+        // look up the stage's COLD blocks before waiting for the buffer
+        int32_t blk = -1;
+        int64_t tt = 0;
+        if (t >= lp && lane < n) {
+          tt = (int64_t)(t - lp) + lane;
+          blk = table[tt / p.page];
+        }
         const int round = k / kStages;
         if (round > 0 && !mbar_wait(empty_bar(s), (round - 1) & 1, p.err)) {
           ok = false;
           break;
         }
-        const uint16_t *src_k = nullptr, *src_v = nullptr;
-        uint32_t dst_off = 0, unit_bytes;
-        bool issue;
         if (t < lp) {
-          // HOT: one run of n tokens per head; slab layout [L][Hkv][Lp][d]
-          unit_bytes = (uint32_t)n * D * 2;
-          issue = lane < Hkv;
-          if (issue) {
-            int64_t row = rq.hot_base * (int64_t)p.L * Hkv + ((int64_t)p.layer * Hkv + lane) * lp + t;
-            src_k = p.hot_k + row * D;
-            src_v = p.hot_v + row * D;
-            dst_off = (uint32_t)lane * kT * D * 2;
+          // HOT: per head, D/64 swizzled boxes of 16 keys x 64 dims (zeros past Lp)
+          if (lane == 0) {
+            const uint32_t bytes = (uint32_t)Hkv * (D / 64) * kT * 128;
+            mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
+            for (int h = 0; h < Hkv; ++h)
+              for (int x = 0; x < D / 64; ++x) {
+                const uint32_t off = (uint32_t)(h * (D / 64) + x) * kT * 128;
+                tma_load_3d(k_stage(s) + off, tm, x * 64, t, p.layer * Hkv + h, full_bar(s));
+                tma_load_3d(v_stage(s) + off, tm + 128, x * 64, t, p.layer * Hkv + h, full_bar(s));
+              }
           }
         } else {
-          // COLD: one row of Hkv*d per token, through the block table
-          unit_bytes = (uint32_t)Hkv * D * 2;
-          issue = false;
+          // COLD: one bulk copy per token row of Hkv*d through the block table
+          bool issue = false;
+          const uint16_t *src_k = nullptr, *src_v = nullptr;
           if (lane < n) {
-            int64_t tt = (int64_t)(t - lp) + lane;
-            int32_t blk = table[tt / p.page];
             if (blk >= 0 && blk < p.n_blocks) {
-              int64_t slot = (int64_t)blk * p.page + tt % p.page;
+              const int64_t slot = (int64_t)blk * p.page + tt % p.page;
               src_k = p.cold_k + (layer_rows + slot) * Hkv * D;
               src_v = p.cold_v + (layer_rows + slot) * Hkv * D;
-              dst_off = (uint32_t)lane * Hkv * D * 2;
               issue = true;
             } else {
               report_error(p.err, kErrBounds);
             }
           }
+          const unsigned mask = __ballot_sync(0xffffffffu, issue);
+          const uint32_t row = (uint32_t)Hkv * D * 2;
+          if (lane == 0) mbar_arrive_expect_tx(full_bar(s), (uint32_t)__popc(mask) * row * 2);
+          __syncwarp();
+          if (issue) {
+            bulk_g2s(k_stage(s) + lane * rs, src_k, row, full_bar(s));
+            bulk_g2s(v_stage(s) + lane * rs, src_v, row, full_bar(s));
+          }
         }
-        const unsigned mask = __ballot_sync(0xffffffffu, issue);
-        if (lane == 0) mbar_arrive_expect_tx(full_bar(s), (uint32_t)__popc(mask) * unit_bytes * 2);
         __syncwarp();
-        if (issue) {
-          bulk_g2s(k_stage(s) + dst_off, src_k, unit_bytes, full_bar(s));
-          bulk_g2s(v_stage(s) + dst_off, src_v, unit_bytes, full_bar(s));
-        }
         t += n;
         ++k;
       }
     }
     if (!ok) {
-      // an abort: let copies already in flight land before the CTA exits
       for (int j = max(0, k - kStages); j < k; ++j) mbar_wait(full_bar(j % kStages), (j / kStages) & 1, nullptr);
     }
     return;
   }
-  if (warp > Hkv) return;
 
   // ------------------------------- consumers --------------------------------
   const int h = warp;
-  const int sub = lane % LPT;  // 8-dim slice [8*sub, 8*sub+8)
-  const int grp = lane / LPT;  // token row within a warp load
+  const int gq = lane >> 2;  // fragment row group
+  const int tq = lane & 3;   // fragment column pair
+  const int mi = lane >> 3, mj = lane & 7;  // ldmatrix: matrix index, row within it
   int k = 0;
   for (int sg = seg0; sg < seg1; ++sg) {
     const SegmentDev seg = p.segs[sg];
-    const RequestDev rq = p.reqs[seg.req];
-    const int lp = p.dense ? rq.lp : 0;
+    const int lp = p.dense ? p.reqs[seg.req].lp : 0;
 
-    float qf[G][8];
+    // Q_h^T as the B operand: b[kk][0] = (d 16kk+2tq, +1; head gq), b[kk][1] = (d +8, +9; head gq)
+    uint32_t qb[KSTEPS][2];
+    {
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((int64_t)seg.req * p.Hq + h * G + min(gq, G - 1)) * D);
 #pragma unroll
-    for (int j = 0; j < G; ++j) {
-      const uint4 w = *reinterpret_cast<const uint4*>(p.q + ((int64_t)seg.req * p.Hq + h * G + j) * D + sub * 8);
-      qf[j][0] = bf_lo(w.x) * p.q_scale; qf[j][1] = bf_hi(w.x) * p.q_scale;
-      qf[j][2] = bf_lo(w.y) * p.q_scale; qf[j][3] = bf_hi(w.y) * p.q_scale;
-      qf[j][4] = bf_lo(w.z) * p.q_scale; qf[j][5] = bf_hi(w.z) * p.q_scale;
-      qf[j][6] = bf_lo(w.w) * p.q_scale; qf[j][7] = bf_hi(w.w) * p.q_scale;
+      for (int kk = 0; kk < KSTEPS; ++kk) {
+        qb[kk][0] = gq < G ? qrow[kk * 8 + tq] : 0u;
+        qb[kk][1] = gq < G ? qrow[kk * 8 + 4 + tq] : 0u;
+      }
     }
-    float m[G], ls[G], acc[G][8];
+    float o[KSTEPS][4];
 #pragma unroll
-    for (int j = 0; j < G; ++j) {
-      m[j] = -INFINITY;
-      ls[j] = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
-    }
+    for (int mt = 0; mt < KSTEPS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2tq and 2tq+1
 
     bool ok = true;
     for (int t = seg.t0; t < seg.t1;) {
@@ -192,64 +243,56 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), (G <= 4 ? 2 : 1)) gath
         break;
       }
       const bool hot = t < lp;
-      const uint32_t tok_stride = hot ? D * 2 : (uint32_t)Hkv * D * 2;
-      const uint32_t head_off = hot ? (uint32_t)h * kT * D * 2 : (uint32_t)h * D * 2;
-      const uint32_t kb = k_stage(s) + head_off + sub * 16;
-      const uint32_t vb = v_stage(s) + head_off + sub * 16;
-
-      float sc[R][G];
+      // address of 16-byte chunk c of token row tok of head h in a stage
+      auto chunk_addr = [&](uint32_t stage, int tok, int c) -> uint32_t {
+        if (hot)
+          return stage + (uint32_t)(h * (D / 64) + (c >> 3)) * kT * 128 + tok * 128 + ((((c & 7) ^ (tok & 7))) << 4);
+        return stage + (uint32_t)tok * rs + (uint32_t)h * D * 2 + c * 16;
+      };
+      // S^T = K Q_h^T
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < R; ++i) {
-        const uint4 w = lds128(kb + (uint32_t)(i * TPI + grp) * tok_stride);
-        float kf[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y), bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-          float a = 0.f;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) a = fmaf(qf[j][e], kf[e], a);
-          sc[i][j] = a;
-        }
+      for (int kk = 0; kk < KSTEPS; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(chunk_addr(k_stage(s), mj + 8 * (mi & 1), 2 * kk + (mi >> 1)), a0, a1, a2, a3);
+        mma16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
       }
+      // online softmax over the 16 tokens (rows gq and gq+8) for heads 2tq, 2tq+1
+      const bool v_lo = gq < n, v_hi = gq + 8 < n;
+      const float s00 = v_lo ? sc[0] * p.q_scale : -INFINITY;
+      const float s01 = v_lo ? sc[1] * p.q_scale : -INFINITY;
+      const float s10 = v_hi ? sc[2] * p.q_scale : -INFINITY;
+      const float s11 = v_hi ? sc[3] * p.q_scale : -INFINITY;
+      float x0 = fmaxf(s00, s10), x1 = fmaxf(s01, s11);
 #pragma unroll
-      for (int off = LPT / 2; off >= 1; off >>= 1)
-#pragma unroll
-        for (int i = 0; i < R; ++i)
-#pragma unroll
-          for (int j = 0; j < G; ++j) sc[i][j] += __shfl_xor_sync(0xffffffffu, sc[i][j], off);
-
-      float alpha[G];
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < R; ++i) {
-          if (i * TPI + grp >= n) sc[i][j] = -INFINITY;
-          mx = fmaxf(mx, sc[i][j]);
-        }
-#pragma unroll
-        for (int off = LPT; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        const float mn = fmaxf(m[j], mx);
-        alpha[j] = ex2(m[j] - mn);
-        m[j] = mn;
-        float sum = 0.f;
-#pragma unroll
-        for (int i = 0; i < R; ++i) {
-          sc[i][j] = ex2(sc[i][j] - mn);
-          sum += sc[i][j];
-        }
-        ls[j] = ls[j] * alpha[j] + sum;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[j][e] *= alpha[j];
+      for (int off = 4; off < 32; off <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
       }
+      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+      if (__any_sync(0xffffffffu, n0 != m0 || n1 != m1)) {
+        const float a0 = ex2(m0 - n0), a1 = ex2(m1 - n1);
+        l0 *= a0;
+        l1 *= a1;
 #pragma unroll
-      for (int i = 0; i < R; ++i) {
-        uint4 w = lds128(vb + (uint32_t)(i * TPI + grp) * tok_stride);
-        if (i * TPI + grp >= n) w = make_uint4(0, 0, 0, 0);
-        float vf[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y), bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
+        for (int mt = 0; mt < KSTEPS; ++mt) {
+          o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
+        }
+        m0 = n0;
+        m1 = n1;
+      }
+      const float p00 = ex2(s00 - m0), p01 = ex2(s01 - m1), p10 = ex2(s10 - m0), p11 = ex2(s11 - m1);
+      l0 += p00 + p10;
+      l1 += p01 + p11;
+      // P^T (16 tok x 8 heads) -> B operand of the PV product
+      const uint32_t pb0 = movm_t(pack_bf16x2(p00, p01));
+      const uint32_t pb1 = movm_t(pack_bf16x2(p10, p11));
+      // O^T += V^T P^T
 #pragma unroll
-        for (int j = 0; j < G; ++j)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(sc[i][j], vf[e], acc[j][e]);
+      for (int mt = 0; mt < KSTEPS; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(chunk_addr(v_stage(s), mj + 8 * (mi >> 1), 2 * mt + (mi & 1)), a0, a1, a2, a3);
+        mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(s));
@@ -258,34 +301,42 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), (G <= 4 ? 2 : 1)) gath
     }
     if (!ok) return;
 
-    // combine the token rows of the warp (lanes with the same 8-dim slice)
+    // finish: the row sums live on the 8 lanes that share tq
 #pragma unroll
-    for (int off = LPT; off < 32; off <<= 1)
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    const float i0 = 1.f / l0, i1 = 1.f / l1;
+    const int hh0 = 2 * tq, hh1 = 2 * tq + 1;
+    float* dst;
+    float* dl;
+    int64_t row0;
+    if (seg.entry >= 0) {
+      row0 = (int64_t)seg.entry * p.Hq + h * G;
+      dst = p.part_o;
+      dl = p.part_l;
+    } else {
+      row0 = (int64_t)seg.req * p.Hq + h * G;
+      dst = p.out;
+      dl = p.lse;
+    }
 #pragma unroll
-      for (int j = 0; j < G; ++j) {
-        ls[j] += __shfl_xor_sync(0xffffffffu, ls[j], off);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[j][e] += __shfl_xor_sync(0xffffffffu, acc[j][e], off);
+    for (int mt = 0; mt < KSTEPS; ++mt) {
+      const int d0 = mt * 16 + gq;
+      if (hh0 < G) {
+        dst[(row0 + hh0) * D + d0] = o[mt][0] * i0;
+        dst[(row0 + hh0) * D + d0 + 8] = o[mt][2] * i0;
       }
-    if (grp == 0) {
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        const float inv = 1.f / ls[j];
-        const float lse2 = m[j] + __log2f(ls[j]);
-        const int qh = h * G + j;
-        float4 o0 = make_float4(acc[j][0] * inv, acc[j][1] * inv, acc[j][2] * inv, acc[j][3] * inv);
-        float4 o1 = make_float4(acc[j][4] * inv, acc[j][5] * inv, acc[j][6] * inv, acc[j][7] * inv);
-        float* dst;
-        if (seg.entry >= 0) {
-          dst = p.part_o + ((int64_t)seg.entry * p.Hq + qh) * D + sub * 8;
-          if (sub == 0) p.part_l[(int64_t)seg.entry * p.Hq + qh] = lse2;
-        } else {
-          dst = p.out + ((int64_t)seg.req * p.Hq + qh) * D + sub * 8;
-          if (sub == 0 && p.lse) p.lse[(int64_t)seg.req * p.Hq + qh] = lse2 * kLn2;
-        }
-        reinterpret_cast<float4*>(dst)[0] = o0;
-        reinterpret_cast<float4*>(dst)[1] = o1;
+      if (hh1 < G) {
+        dst[(row0 + hh1) * D + d0] = o[mt][1] * i1;
+        dst[(row0 + hh1) * D + d0 + 8] = o[mt][3] * i1;
       }
+    }
+    if (gq == 0 && dl) {
+      const float f = seg.entry >= 0 ? 1.f : kLn2;   // partials keep log2, outputs are natural log
+      if (hh0 < G) dl[row0 + hh0] = (m0 + __log2f(l0)) * f;
+      if (hh1 < G) dl[row0 + hh1] = (m1 + __log2f(l1)) * f;
     }
   }
 }
@@ -334,7 +385,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ pa
 
 template <int D, int G>
 int launch_gather_t(const GatherParams& gp, int ctas, cudaStream_t st) {
-  const size_t smem = 2 * kStages * stage_bytes(gp.Hkv, D) + 2 * kStages * sizeof(uint64_t);
+  const size_t smem = gather_smem_bytes(gp.Hkv, D);
   auto kern = gather_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
@@ -345,14 +396,9 @@ int launch_gather_t(const GatherParams& gp, int ctas, cudaStream_t st) {
 }  // namespace
 
 int gather_ctas_per_sm(const gk_pool_config* cfg) {
-  const size_t smem = 2 * kStages * stage_bytes(cfg->num_kv_heads, cfg->head_dim) + 1024;
-  int by_smem = (int)((227 * 1024) / (smem + 1024));
-  int threads = 32 * (cfg->num_kv_heads + 1);
-  int by_threads = 2048 / threads;
-  int g = cfg->num_q_heads / cfg->num_kv_heads;
-  int by_regs = g <= 4 ? 2 : 1;   // register footprint grows with the query heads per warp
-  int n = by_smem < by_threads ? by_smem : by_threads;
-  n = n < by_regs ? n : by_regs;
+  const size_t smem = gather_smem_bytes(cfg->num_kv_heads, cfg->head_dim);
+  int by_smem = (int)((228 * 1024) / (smem + 1024));
+  int n = by_smem < 4 ? by_smem : 4;
   return n < 1 ? 1 : n;
 }
 
@@ -383,6 +429,7 @@ int launch_gather(const LaunchCommon& lc, void* stream, int32_t layer, const gk_
   gp.reqs = (const RequestDev*)(base + pl->off_reqs);
   gp.seg_begin = (const int32_t*)(base + (dense ? pl->off_dense_begin : pl->off_suf_begin));
   gp.segs = (const SegmentDev*)(base + (dense ? pl->off_dense_segs : pl->off_suf_segs));
+  gp.tmaps = base + pl->off_tmaps;
   gp.err = lc.d_error;
   gp.q_scale = kLog2e / sqrtf((float)c.head_dim);
   const int ctas = dense ? pl->summary.dense_ctas : pl->summary.suffix_ctas;

@@ -46,6 +46,7 @@ struct BlockManager {
 // ---- geometry-dependent kernel limits ---------------------------------------
 constexpr int kPrefixTileM = 128;    // stacked query rows per tensor-core tile
 constexpr int kPrefixTileN = 128;    // prefix keys per tile
+constexpr int kGatherT = 16;         // tokens per gather pipeline stage
 constexpr int kMaxKvHeads = 8;
 
 struct DeviceInfo {
@@ -74,7 +75,7 @@ struct PrefixGroupDev {
   int32_t req_base;    // offset into prefix_reqs
   int32_t nsplit;      // splits over the prefix keys
   int32_t split_tiles; // key tiles (of kPrefixTileN) per split
-  int32_t tmap_index;  // index of the group's K tensor map (V follows)
+  int32_t tmap_index;  // first of the group's 4 tensor maps: K, V (128-key box), K, V (16-key box)
   int32_t pad0, pad1;
 };
 
@@ -99,6 +100,8 @@ struct RequestDev {
   int32_t n_entry_cas;
   int32_t entry_dense;
   int32_t n_entry_dense;
+  int32_t group;       // HOT prefix group (tensor maps 4*group..4*group+3), -1 = none
+  int32_t pad0;
 };
 
 struct Plan {
@@ -162,7 +165,9 @@ int launch_prefix(const LaunchCommon& lc, void* stream, int32_t layer, const gk_
 // resident gather CTAs per SM for the pool's geometry (from its shared-memory
 // footprint; no device query, so host-only pools plan identically)
 int gather_ctas_per_sm(const gk_pool_config* cfg);
-// encode the tensor maps of a plan's prefix groups into host memory (128 B each)
+// encode the tensor maps of a plan's prefix groups into host memory (128 B each,
+// 4 per group: K and V with a 128-key box for the prefix kernel, K and V with a
+// 16-key box for the dense gather)
 int encode_prefix_tmaps(const gk_pool_config* cfg, const Plan* plan, std::vector<uint8_t>* out);
 size_t tmap_bytes();
 

@@ -53,7 +53,7 @@ __global__ void scatter_kernel(uint4* __restrict__ cold_k, uint4* __restrict__ c
 }
 
 // Prefix tokens [t0, t0+n) of one layer: input [n][Hkv][d] -> slab [Hkv][Lp][d] at (layer).
-__global__ void write_prefix_kernel(uint4* __restrict__ hot_k, uint4* __restrict__ hot_v, int64_t slab_vecs,
+__global__ void hot_slab_write_kernel(uint4* __restrict__ hot_k, uint4* __restrict__ hot_v, int64_t slab_vecs,
                                     int32_t hkv, int32_t d_vecs, int64_t lp, int64_t t0, int64_t n,
                                     const uint4* __restrict__ k, const uint4* __restrict__ v) {
   int64_t total = n * hkv * d_vecs;
@@ -103,7 +103,7 @@ int launch_write_prefix(const LaunchCommon& lc, void* stream, int32_t layer, int
   int64_t total = n * c.num_kv_heads * d_vecs;
   int64_t blocks = (total + 255) / 256;
   if (blocks > (int64_t)lc.num_sms * 16) blocks = (int64_t)lc.num_sms * 16;
-  write_prefix_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
+  hot_slab_write_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
       (uint4*)c.hot_k, (uint4*)c.hot_v, slab_vecs, c.num_kv_heads, d_vecs, lp, t0, n, (const uint4*)d_k,
       (const uint4*)d_v);
   return (int)cudaGetLastError();

@@ -95,6 +95,7 @@ static gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
       if (lp != 0) return fail(p, GK_ERR_INVALID, "prefix_len must be 0 without a HOT prefix");
       rq.hot_base = -1;
       rq.lp = 0;
+      rq.group = -1;
       continue;
     }
     auto it = p->hot.live.find(base);
@@ -112,6 +113,7 @@ static gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
       grp = f->second;
     }
     members[(size_t)grp].push_back(r);
+    rq.group = grp;
   }
 
   // ---- prefix contraction work: choose keys per split to balance the SMs --------
@@ -150,7 +152,7 @@ static gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     gd.req_base = (int32_t)pl->prefix_reqs.size();
     gd.split_tiles = best_c;
     gd.nsplit = (ntiles[(size_t)gi] + best_c - 1) / best_c;
-    gd.tmap_index = 2 * gi;
+    gd.tmap_index = 4 * gi;
     for (int32_t r : members[(size_t)gi]) pl->prefix_reqs.push_back(r);
     pl->groups.push_back(gd);
     max_m = std::max(max_m, gd.m);

@@ -391,10 +391,11 @@ int launch_prefix_t(const PrefixParams& pp, int ctas, cudaStream_t st) {
 
 size_t tmap_bytes() { return sizeof(CUtensorMap); }
 
-// Two 3D maps per prefix group (K then V) over its slab: dims (d, Lp, L*Hkv),
-// box (64, 128, 1), 128-byte swizzle; keys past Lp read as zeros.
+// Four 3D maps per prefix group over its slab: dims (d, Lp, L*Hkv), 128-byte
+// swizzle, keys past Lp read as zeros; K and V with a (64, 128, 1) box for the
+// prefix kernel, then K and V with a (64, 16, 1) box for the dense gather.
 int encode_prefix_tmaps(const gk_pool_config* cfg, const Plan* pl, std::vector<uint8_t>* out) {
-  out->assign(pl->groups.size() * 2 * sizeof(CUtensorMap), 0);
+  out->assign(pl->groups.size() * 4 * sizeof(CUtensorMap), 0);
   if (pl->groups.empty()) return 0;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return 1;
@@ -402,18 +403,19 @@ int encode_prefix_tmaps(const gk_pool_config* cfg, const Plan* pl, std::vector<u
   for (size_t gi = 0; gi < pl->groups.size(); ++gi) {
     const int64_t lp = pl->groups[gi].lp;
     const int64_t slab = pl->group_hot_base[gi] * cfg->num_layers * cfg->num_kv_heads * D;
-    for (int kv = 0; kv < 2; ++kv) {
+    for (int m = 0; m < 4; ++m) {
+      const int kv = m & 1;
       uint16_t* basep = (uint16_t*)(kv == 0 ? cfg->hot_k : cfg->hot_v) + slab;
       cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)lp, (cuuint64_t)cfg->num_layers * cfg->num_kv_heads};
       cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)lp * D * 2};
-      cuuint32_t box[3] = {64, (cuuint32_t)BN, 1};
+      cuuint32_t box[3] = {64, (cuuint32_t)(m < 2 ? BN : kGatherT), 1};
       cuuint32_t estr[3] = {1, 1, 1};
-      CUtensorMap m;
-      CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, basep, dims, strides, box, estr,
+      CUtensorMap tm;
+      CUresult r = enc(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, basep, dims, strides, box, estr,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return 2;
-      std::memcpy(out->data() + (gi * 2 + kv) * sizeof(CUtensorMap), &m, sizeof(CUtensorMap));
+      std::memcpy(out->data() + (gi * 4 + m) * sizeof(CUtensorMap), &tm, sizeof(CUtensorMap));
     }
   }
   return 0;
