@@ -201,6 +201,25 @@ gk_status gk_decode_dense(gk_pool* pool, void* stream, int32_t layer, const gk_b
  * are merged by log-sum-exp (GraniKV Eq. 1). */
 gk_status gk_decode_cascade(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch,
                             const gk_plan* plan);
+/* Allocation-free dense decode.  No counterpart in the paper: it exists for
+ * callers that cannot allocate device memory while serving -- an engine that
+ * hands all free HBM to its KV pool at start-up, or one whose allocator is
+ * owned by a framework that rejects allocations made outside it.  Same result
+ * as gk_plan_build + gk_decode_dense on this batch (see those calls for the
+ * arguments), but the work tables and split-K partial states live in one
+ * 8 MiB array compiled into libgk (every GPU that loads the library keeps it
+ * until the process exits) and no call allocates device or pinned memory.
+ *  - The first call on each device looks the array's address up
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - A batch whose tables and partial states exceed 8 MiB is refused with
+ *    GK_ERR_INVALID (gk_last_error gives the bytes needed); use the plan path.
+ *  - Every call reuses the same array: calls that overlap on the GPU (two
+ *    streams, or two pools on one device) race and give wrong results; order
+ *    them on one stream.  Nothing in the array needs to start at zero.
+ *  - The pool must already have done device work (any KV write), which is when
+ *    its error word is created; otherwise GK_ERR_INVALID. */
+gk_status gk_decode_dense_static(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch);
 /* The three stages of gk_decode_cascade, for callers that time them or run
  * (a) and (b) on two streams: the prefix and suffix stages write disjoint
  * partial states, and the merge must follow both.  gk_decode_cascade is

@@ -85,6 +85,7 @@ _SIGS = {
     "gk_plan_info": (c_i32, [c_vp, P(gk_plan_summary)]),
     "gk_decode_dense": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch), c_vp]),
     "gk_decode_cascade": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch), c_vp]),
+    "gk_decode_dense_static": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch)]),
     "gk_cascade_prefix": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch), c_vp]),
     "gk_cascade_suffix": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch), c_vp]),
     "gk_cascade_merge": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch), c_vp]),
@@ -318,6 +319,10 @@ def gk_decode_dense(pool, stream, layer, batch, plan):
 
 def gk_decode_cascade(pool, stream, layer, batch, plan):
     _check(lib().gk_decode_cascade(pool, _stream(stream), layer, ctypes.byref(batch.c), plan), pool)
+
+
+def gk_decode_dense_static(pool, stream, layer, batch):
+    _check(lib().gk_decode_dense_static(pool, _stream(stream), layer, ctypes.byref(batch.c)), pool)
 
 
 def gk_cascade_prefix(pool, stream, layer, batch, plan):

@@ -136,6 +136,9 @@ struct Plan {
   bool uploaded = false;
 };
 
+// host half of gk_plan_build: grouping, work lists and partial-state layout (no device work)
+gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl);
+
 // ---- status helpers -------------------------------------------------------------
 gk_status fail(Pool* p, gk_status s, const std::string& msg);
 gk_status cuda_fail(Pool* p, int err, const char* what);

@@ -61,7 +61,7 @@ void partition_tokens(const std::vector<int64_t>& n, int64_t max_ctas, std::vect
 
 }  // namespace
 
-static gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
+gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   const gk_pool_config& c = p->cfg;
   const int32_t B = b->num_requests;
   const int32_t Hkv = c.num_kv_heads, Hq = c.num_q_heads, d = c.head_dim, g = Hq / Hkv;
