@@ -273,27 +273,28 @@ def run_ours(a, w):
             choice = forced
         choices.append(choice)
         for l in range(L):
-            if events is not None:
-                events[l][0].record(stream)
+            ev = events[l] if (events is not None and l in events) else None
+            if ev is not None:
+                ev[0].record(stream)
             gk.gk_append_kv(pool, stream, l, d_slots, k[l], v[l], d_cow if ncow else None, n=B, n_cow=ncow)
             launches[0] += 1 + (1 if ncow else 0)
             batch.set_device(d_q=q[l], d_out=out[l], d_lse=lse[l])
-            if events is not None:
-                events[l][1].record(stream)
+            if ev is not None:
+                ev[1].record(stream)
             if choice == gk.GK_BACKEND_CASCADE:
                 gk.gk_cascade_prefix(pool, stream, l, batch, plan[0])
-                if events is not None:
-                    events[l][2].record(stream)
+                if ev is not None:
+                    ev[2].record(stream)
                 gk.gk_cascade_suffix(pool, stream, l, batch, plan[0])
-                if events is not None:
-                    events[l][3].record(stream)
+                if ev is not None:
+                    ev[3].record(stream)
                 gk.gk_cascade_merge(pool, stream, l, batch, plan[0])
                 launches[0] += 3
             else:
                 gk.gk_decode_dense(pool, stream, l, batch, plan[0])
                 launches[0] += 1 + dense_merge[0]
-            if events is not None:
-                events[l][4].record(stream)
+            if ev is not None:
+                ev[4].record(stream)
 
     for _ in range(a.warmup):
         step()
@@ -305,7 +306,11 @@ def run_ours(a, w):
         torch.distributed.barrier()
 
     # ---- timed region: device-resident inputs ----
-    events = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(L)] for _ in range(a.steps)]
+    # Per-kernel events bracket one layer per step (a different layer each step):
+    # an event between two kernels stops the next one from launching early, so
+    # the other layers run undisturbed.
+    probe_layer = [i % L for i in range(a.steps)]
+    events = [{probe_layer[i]: [torch.cuda.Event(enable_timing=True) for _ in range(5)]} for i in range(a.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     vis_list = [x for x in vis.split(",") if x.strip()]
@@ -339,8 +344,7 @@ def run_ours(a, w):
     k_ms = {"append": [], "prefix": [], "suffix": [], "merge": [], "dense": []}
     for i in range(a.steps):
         cas = step_choices[i] == gk.GK_BACKEND_CASCADE
-        for l in range(L):
-            e = events[i][l]
+        for l, e in events[i].items():
             k_ms["append"].append(e[0].elapsed_time(e[1]))
             if cas:
                 k_ms["prefix"].append(e[1].elapsed_time(e[2]))

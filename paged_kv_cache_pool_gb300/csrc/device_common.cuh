@@ -9,6 +9,22 @@
 
 namespace gk {
 
+// Launch with programmatic stream serialization (see griddep_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 constexpr int32_t kErrBounds = 5;    // GK_ERR_DEVICE_BOUNDS
 constexpr int32_t kErrTimeout = 6;   // GK_ERR_TIMEOUT
 // A wait that has not completed after this long (ns of %globaltimer) gives up.
@@ -184,6 +200,64 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
+}
+
+// ---- packed fp32 pairs (sm_100+ f32x2 pipes) ------------------------------------------
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 2^x on the FMA pipe, for x <= 64 (returns 0 below -125).  Range reduction
+// x = n + f with n = round(x) taken from the mantissa of x + 1.5*2^23 and
+// f in [-1/2, 1/2]; 2^f by a cubic fitted here to minimise the relative error
+// on [-1/2, 1/2] (iteratively reweighted least squares, max rel. error
+// 7.6e-5); 2^n is added to the exponent field.  Used where the result is
+// rounded to bf16 next (rel. step 3.9e-3), to offload the MUFU pipe.
+__device__ __forceinline__ void exp2_poly_pair(float xa, float xb, float& ya, float& yb) {
+  const float ca = fmaxf(xa, -125.f), cb = fmaxf(xb, -125.f);
+  const uint64_t magic = f2pack(12582912.f, 12582912.f);
+  const uint64_t t = fadd2(f2pack(ca, cb), magic);
+  float ta, tb;
+  f2unpack(t, ta, tb);
+  const float na = ta - 12582912.f, nb = tb - 12582912.f;
+  uint64_t f = fadd2(f2pack(ca, cb), f2pack(-na, -nb));
+  uint64_t p = ffma2(f, f2pack(0.05517047643661499f, 0.05517047643661499f), f2pack(0.2426084578037262f, 0.2426084578037262f));
+  p = ffma2(f, p, f2pack(0.6932609677314758f, 0.6932609677314758f));
+  p = ffma2(f, p, f2pack(0.9999282360076904f, 0.9999282360076904f));
+  float pa, pb;
+  f2unpack(p, pa, pb);
+  ya = xa < -125.f ? 0.f : __int_as_float(__float_as_int(pa) + (__float_as_int(ta) << 23));
+  yb = xb < -125.f ? 0.f : __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23));
+}
+
+// ---- programmatic dependent launch ----------------------------------------------------
+// Kernels of the decode path are launched with programmatic stream
+// serialization: a kernel may start (and do its set-up) while the previous
+// kernel on the stream drains, and waits here before touching any memory that
+// kernel, or one before it, writes.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 constexpr float kLn2 = 0.693147180559945309f;

@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1) gather_kernel(const
   auto full_bar = [&](int s) { return bars + 8u * s; };
   auto empty_bar = [&](int s) { return bars + 8u * (kStages + s); };
 
+  griddep_launch_dependents();
   // Zero the stages once: a partial stage leaves rows past its tokens untouched,
   // and those rows must hold finite values (they meet P = 0 in the MMA).
   for (uint32_t off = threadIdx.x * 16; off < 2 * kStages * hs; off += blockDim.x * 16)
@@ -128,79 +129,124 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1) gather_kernel(const
   }
   fence_async_shared();
   __syncthreads();
+  griddep_wait();   // queries, pool rows and the partial-state buffer are written upstream
 
   const int seg0 = p.seg_begin[blockIdx.x], seg1 = p.seg_begin[blockIdx.x + 1];
   const int64_t layer_rows = (int64_t)p.layer * p.cold_slots;
 
   if (warp == Hkv) {
     // ------------------------------- producer -------------------------------
+    // Stages are visited in the consumers' order.  The block ids of the next
+    // stage are loaded while this stage's buffer is awaited, so the table
+    // lookup never sits between a free buffer and its copies.
+    struct SegState {
+      SegmentDev seg;
+      int lp;
+      int64_t hot_base;
+      const int32_t* table;
+      const uint8_t* tm;
+    };
+    auto seg_state = [&](int sg) {
+      SegState st;
+      st.seg = p.segs[sg];
+      const RequestDev rq = p.reqs[st.seg.req];
+      st.lp = p.dense ? rq.lp : 0;
+      st.hot_base = rq.hot_base;
+      st.table = p.block_table + (int64_t)st.seg.req * p.max_blocks;
+      st.tm = rq.group >= 0 ? p.tmaps + (size_t)(4 * rq.group + 2) * 128 : nullptr;
+      return st;
+    };
+    auto stage_len = [&](const SegState& st, int t) {
+      int n = min(kT, st.seg.t1 - t);
+      if (t < st.lp) n = min(n, st.lp - t);
+      return n;
+    };
+    auto block_id = [&](const SegState& st, int t, int n) -> int32_t {
+      if (t < st.lp || lane >= n) return -1;
+      return st.table[((int64_t)(t - st.lp) + lane) / p.page];
+    };
     int k = 0;
-    bool ok = true;
-    for (int sg = seg0; sg < seg1 && ok; ++sg) {
-      const SegmentDev seg = p.segs[sg];
-      const RequestDev rq = p.reqs[seg.req];
-      const int lp = p.dense ? rq.lp : 0;
-      const int32_t* table = p.block_table + (int64_t)seg.req * p.max_blocks;
-      const uint8_t* tm = rq.group >= 0 ? p.tmaps + (size_t)(4 * rq.group + 2) * 128 : nullptr;
-      if (lp > 0 && lane == 0) {
-        tmap_acquire(tm);
-        tmap_acquire(tm + 128);
+    bool ok = seg0 < seg1;
+    SegState cur{};
+    int t = 0, sg = seg0;
+    int32_t blk = -1;
+    if (ok) {
+      cur = seg_state(sg);
+      t = cur.seg.t0;
+      blk = block_id(cur, t, stage_len(cur, t));
+      if (cur.lp > 0 && lane == 0) {
+        tmap_acquire(cur.tm);
+        tmap_acquire(cur.tm + 128);
       }
-      for (int t = seg.t0; t < seg.t1;) {
-        int n = min(kT, seg.t1 - t);
-        if (t < lp) n = min(n, lp - t);
-        const int s = k % kStages;
-        // look up the stage's COLD blocks before waiting for the buffer
-        int32_t blk = -1;
-        int64_t tt = 0;
-        if (t >= lp && lane < n) {
-          tt = (int64_t)(t - lp) + lane;
-          blk = table[tt / p.page];
+    }
+    while (ok) {
+      const int n = stage_len(cur, t);
+      // next stage position and its block ids (prefetch)
+      SegState nxt = cur;
+      int t_next = t + n, sg_next = sg;
+      bool has_next = true;
+      if (t_next >= cur.seg.t1) {
+        sg_next = sg + 1;
+        has_next = sg_next < seg1;
+        if (has_next) {
+          nxt = seg_state(sg_next);
+          t_next = nxt.seg.t0;
         }
-        const int round = k / kStages;
-        if (round > 0 && !mbar_wait(empty_bar(s), (round - 1) & 1, p.err)) {
-          ok = false;
-          break;
-        }
-        if (t < lp) {
-          // HOT: per head, D/64 swizzled boxes of 16 keys x 64 dims (zeros past Lp)
-          if (lane == 0) {
-            const uint32_t bytes = (uint32_t)Hkv * (D / 64) * kT * 128;
-            mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
-            for (int h = 0; h < Hkv; ++h)
-              for (int x = 0; x < D / 64; ++x) {
-                const uint32_t off = (uint32_t)(h * (D / 64) + x) * kT * 128;
-                tma_load_3d(k_stage(s) + off, tm, x * 64, t, p.layer * Hkv + h, full_bar(s));
-                tma_load_3d(v_stage(s) + off, tm + 128, x * 64, t, p.layer * Hkv + h, full_bar(s));
-              }
-          }
-        } else {
-          // COLD: one bulk copy per token row of Hkv*d through the block table
-          bool issue = false;
-          const uint16_t *src_k = nullptr, *src_v = nullptr;
-          if (lane < n) {
-            if (blk >= 0 && blk < p.n_blocks) {
-              const int64_t slot = (int64_t)blk * p.page + tt % p.page;
-              src_k = p.cold_k + (layer_rows + slot) * Hkv * D;
-              src_v = p.cold_v + (layer_rows + slot) * Hkv * D;
-              issue = true;
-            } else {
-              report_error(p.err, kErrBounds);
+      }
+      const int32_t blk_next = has_next ? block_id(nxt, t_next, stage_len(nxt, t_next)) : -1;
+
+      const int s = k % kStages;
+      const int round = k / kStages;
+      if (round > 0 && !mbar_wait(empty_bar(s), (round - 1) & 1, p.err)) {
+        ok = false;
+        break;
+      }
+      if (t < cur.lp) {
+        // HOT: per head, D/64 swizzled boxes of 16 keys x 64 dims (zeros past Lp)
+        if (lane == 0) {
+          const uint32_t bytes = (uint32_t)Hkv * (D / 64) * kT * 128;
+          mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
+          for (int h = 0; h < Hkv; ++h)
+            for (int x = 0; x < D / 64; ++x) {
+              const uint32_t off = (uint32_t)(h * (D / 64) + x) * kT * 128;
+              tma_load_3d(k_stage(s) + off, cur.tm, x * 64, t, p.layer * Hkv + h, full_bar(s));
+              tma_load_3d(v_stage(s) + off, cur.tm + 128, x * 64, t, p.layer * Hkv + h, full_bar(s));
             }
-          }
-          const unsigned mask = __ballot_sync(0xffffffffu, issue);
-          const uint32_t row = (uint32_t)Hkv * D * 2;
-          if (lane == 0) mbar_arrive_expect_tx(full_bar(s), (uint32_t)__popc(mask) * row * 2);
-          __syncwarp();
-          if (issue) {
-            bulk_g2s(k_stage(s) + lane * rs, src_k, row, full_bar(s));
-            bulk_g2s(v_stage(s) + lane * rs, src_v, row, full_bar(s));
+        }
+      } else {
+        // COLD: one bulk copy per token row of Hkv*d through the block table
+        bool issue = false;
+        const uint16_t *src_k = nullptr, *src_v = nullptr;
+        if (lane < n) {
+          if (blk >= 0 && blk < p.n_blocks) {
+            const int64_t slot = (int64_t)blk * p.page + ((int64_t)(t - cur.lp) + lane) % p.page;
+            src_k = p.cold_k + (layer_rows + slot) * Hkv * D;
+            src_v = p.cold_v + (layer_rows + slot) * Hkv * D;
+            issue = true;
+          } else {
+            report_error(p.err, kErrBounds);
           }
         }
+        const unsigned mask = __ballot_sync(0xffffffffu, issue);
+        const uint32_t row = (uint32_t)Hkv * D * 2;
+        if (lane == 0) mbar_arrive_expect_tx(full_bar(s), (uint32_t)__popc(mask) * row * 2);
         __syncwarp();
-        t += n;
-        ++k;
+        if (issue) {
+          bulk_g2s(k_stage(s) + lane * rs, src_k, row, full_bar(s));
+          bulk_g2s(v_stage(s) + lane * rs, src_v, row, full_bar(s));
+        }
       }
+      __syncwarp();
+      ++k;
+      if (!has_next) break;
+      if (sg_next != sg && nxt.lp > 0 && lane == 0) {
+        tmap_acquire(nxt.tm);
+        tmap_acquire(nxt.tm + 128);
+      }
+      cur = nxt;
+      sg = sg_next;
+      t = t_next;
+      blk = blk_next;
     }
     if (!ok) {
       for (int j = max(0, k - kStages); j < k; ++j) mbar_wait(full_bar(j % kStages), (j / kStages) & 1, nullptr);
@@ -344,17 +390,20 @@ __global__ void __launch_bounds__(32 * (kMaxKvHeads + 1), 1) gather_kernel(const
 // LSE merge (GraniKV Eq. 1, applied to any number of partial states): for each
 // request and query head, O = sum_e 2^(l_e - m) O_e / sum_e 2^(l_e - m),
 // LSE = (m + log2 sum_e 2^(l_e - m)) * ln 2, with m = max_e l_e (log2 domain).
-// One warp per (request, query head): lanes first reduce the max over the
-// entries' LSEs, then each lane accumulates its 4-float slice of d.
+// One warp per (request, query head).  Lane e holds entry e's LSE and weight
+// (entries beyond 32 are folded in a second round); the d-wide rows are then
+// read 16 entries at a time with every load in flight before any is used.
 __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_l,
                                                     const RequestDev* __restrict__ reqs, int32_t B, int32_t dense,
                                                     int32_t Hq, int32_t D, float* __restrict__ out,
                                                     float* __restrict__ lse) {
+  griddep_launch_dependents();
   const int gw = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= B * Hq) return;
   const int r = gw / Hq, qh = gw % Hq;
   const RequestDev rq = reqs[r];
+  griddep_wait();
   const int e0 = dense ? rq.entry_dense : rq.entry_cas;
   const int ne = dense ? rq.n_entry_dense : rq.n_entry_cas;
   if (ne < 0) return;  // written directly by its only segment
@@ -362,24 +411,40 @@ __global__ void __launch_bounds__(256) merge_kernel(const float* __restrict__ pa
   for (int e = lane; e < ne; e += 32) mx = fmaxf(mx, part_l[(int64_t)(e0 + e) * Hq + qh]);
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  const int vecs = D / 4;  // 16 or 32 float4 per row
-  float z = 0.f;
+  const int vecs = D / 4;  // float4 per row: 16 or 32
+  const bool has = lane < vecs;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (mx != -INFINITY && lane < vecs) {
-#pragma unroll 4
-    for (int e = 0; e < ne; ++e) {
-      const float w = ex2(part_l[(int64_t)(e0 + e) * Hq + qh] - mx);
-      const float4 pe = reinterpret_cast<const float4*>(part_o + ((int64_t)(e0 + e) * Hq + qh) * D)[lane];
-      o.x = fmaf(w, pe.x, o.x);
-      o.y = fmaf(w, pe.y, o.y);
-      o.z = fmaf(w, pe.z, o.z);
-      o.w = fmaf(w, pe.w, o.w);
-      z += w;
+  float z = 0.f;
+  if (mx != -INFINITY) {
+    for (int eb = 0; eb < ne; eb += 32) {
+      const int e = eb + lane;
+      const float w = e < ne ? ex2(part_l[(int64_t)(e0 + e) * Hq + qh] - mx) : 0.f;
+      float wz = w;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) wz += __shfl_xor_sync(0xffffffffu, wz, off);
+      z += wz;
+      const int nb = min(32, ne - eb);
+      for (int c0 = 0; c0 < nb; c0 += 16) {
+        float4 v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          v[k] = (has && c0 + k < nb)
+                     ? reinterpret_cast<const float4*>(part_o + ((int64_t)(e0 + eb + c0 + k) * Hq + qh) * D)[lane]
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float wk = __shfl_sync(0xffffffffu, w, (c0 + k) & 31);
+          o.x = fmaf(wk, v[k].x, o.x);
+          o.y = fmaf(wk, v[k].y, o.y);
+          o.z = fmaf(wk, v[k].z, o.z);
+          o.w = fmaf(wk, v[k].w, o.w);
+        }
+      }
     }
     const float inv = 1.f / z;
     o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
   }
-  if (lane < vecs) reinterpret_cast<float4*>(out + ((int64_t)r * Hq + qh) * D)[lane] = o;
+  if (has) reinterpret_cast<float4*>(out + ((int64_t)r * Hq + qh) * D)[lane] = o;
   if (lane == 0 && lse) lse[(int64_t)r * Hq + qh] = mx == -INFINITY ? -INFINITY : (mx + __log2f(z)) * kLn2;
 }
 
@@ -389,8 +454,8 @@ int launch_gather_t(const GatherParams& gp, int ctas, cudaStream_t st) {
   auto kern = gather_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  kern<<<ctas, 32 * (gp.Hkv + 1), smem, st>>>(gp);
-  return (int)cudaGetLastError();
+  e = launch_pdl(kern, dim3(ctas), dim3(32 * (gp.Hkv + 1)), smem, st, gp);
+  return (int)e;
 }
 
 }  // namespace
@@ -459,10 +524,9 @@ int launch_merge(const LaunchCommon& lc, void* stream, const gk_batch* b, const 
   const uint8_t* base = (const uint8_t*)pl->d_buf;
   const int64_t warps = (int64_t)pl->B * c.num_q_heads;
   const int blocks = (int)((warps + 7) / 8);
-  merge_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(pl->d_part_o, pl->d_part_l,
-                                                         (const RequestDev*)(base + pl->off_reqs), pl->B,
-                                                         dense ? 1 : 0, c.num_q_heads, c.head_dim, b->d_out, b->d_lse);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(merge_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, pl->d_part_o,
+                         pl->d_part_l, (const RequestDev*)(base + pl->off_reqs), pl->B, dense ? 1 : 0,
+                         c.num_q_heads, c.head_dim, b->d_out, b->d_lse);
 }
 
 }  // namespace gk

@@ -45,6 +45,7 @@ struct BlockManager {
 
 // ---- geometry-dependent kernel limits ---------------------------------------
 constexpr int kPrefixTileM = 128;    // stacked query rows per tensor-core tile
+constexpr int kPrefixRowsPerCta = 2 * kPrefixTileM;  // two Q tiles per prefix CTA
 constexpr int kPrefixTileN = 128;    // prefix keys per tile
 constexpr int kGatherT = 16;         // tokens per gather pipeline stage
 constexpr int kMaxKvHeads = 8;
@@ -81,7 +82,7 @@ struct PrefixGroupDev {
 
 struct PrefixItemDev {  // one CTA of the tensor-core prefix kernel
   int32_t group;
-  int32_t mtile;
+  int32_t mblock;      // 256-row block of the stacked Q rows
   int32_t head;
   int32_t split;
 };

@@ -15,6 +15,8 @@ namespace {
 __global__ void cow_copy_kernel(uint4* __restrict__ cold_k, uint4* __restrict__ cold_v, int64_t layer_vecs,
                                 int64_t block_vecs, int64_t n_blocks, const int32_t* __restrict__ pairs,
                                 int32_t* err) {
+  griddep_launch_dependents();
+  griddep_wait();
   int32_t src = pairs[2 * blockIdx.x], dst = pairs[2 * blockIdx.x + 1];
   if (src < 0 || dst < 0 || src >= n_blocks || dst >= n_blocks) {
     if (threadIdx.x == 0) report_error(err, kErrBounds);
@@ -34,6 +36,8 @@ __global__ void cow_copy_kernel(uint4* __restrict__ cold_k, uint4* __restrict__ 
 __global__ void scatter_kernel(uint4* __restrict__ cold_k, uint4* __restrict__ cold_v, int64_t layer_vecs,
                                int32_t row_vecs, int64_t cold_slots, int32_t n, const int64_t* __restrict__ slots,
                                const uint4* __restrict__ k, const uint4* __restrict__ v, int32_t* err) {
+  griddep_launch_dependents();
+  griddep_wait();
   int32_t tok = (int32_t)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
   int lane = threadIdx.x & 31;
   if (tok >= n) return;
@@ -56,6 +60,8 @@ __global__ void scatter_kernel(uint4* __restrict__ cold_k, uint4* __restrict__ c
 __global__ void hot_slab_write_kernel(uint4* __restrict__ hot_k, uint4* __restrict__ hot_v, int64_t slab_vecs,
                                     int32_t hkv, int32_t d_vecs, int64_t lp, int64_t t0, int64_t n,
                                     const uint4* __restrict__ k, const uint4* __restrict__ v) {
+  griddep_launch_dependents();
+  griddep_wait();
   int64_t total = n * hkv * d_vecs;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -75,10 +81,9 @@ int launch_cow_copy(const LaunchCommon& lc, void* stream, int32_t layer, int32_t
   int64_t row_vecs = (int64_t)c.num_kv_heads * c.head_dim / 8;
   int64_t layer_vecs = (int64_t)layer * c.cold_slots * row_vecs;
   int64_t block_vecs = (int64_t)c.cold_page_size * row_vecs;
-  cow_copy_kernel<<<n_cow, 256, 0, (cudaStream_t)stream>>>((uint4*)c.cold_k, (uint4*)c.cold_v, layer_vecs,
-                                                            block_vecs, c.cold_slots / c.cold_page_size, d_pairs,
-                                                            lc.d_error);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(cow_copy_kernel, dim3(n_cow), dim3(256), 0, (cudaStream_t)stream, (uint4*)c.cold_k,
+                         (uint4*)c.cold_v, layer_vecs, block_vecs, (int64_t)(c.cold_slots / c.cold_page_size),
+                         d_pairs, lc.d_error);
 }
 
 int launch_scatter(const LaunchCommon& lc, void* stream, int32_t layer, int32_t n, const int64_t* d_slots,
@@ -88,10 +93,9 @@ int launch_scatter(const LaunchCommon& lc, void* stream, int32_t layer, int32_t 
   int64_t layer_vecs = (int64_t)layer * c.cold_slots * row_vecs;
   int warps_per_block = 8;
   int blocks = (n + warps_per_block - 1) / warps_per_block;
-  scatter_kernel<<<blocks, 32 * warps_per_block, 0, (cudaStream_t)stream>>>(
-      (uint4*)c.cold_k, (uint4*)c.cold_v, layer_vecs, row_vecs, c.cold_slots, n, d_slots, (const uint4*)d_k,
-      (const uint4*)d_v, lc.d_error);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(scatter_kernel, dim3(blocks), dim3(32 * warps_per_block), 0, (cudaStream_t)stream,
+                         (uint4*)c.cold_k, (uint4*)c.cold_v, layer_vecs, row_vecs, (int64_t)c.cold_slots, n, d_slots,
+                         (const uint4*)d_k, (const uint4*)d_v, lc.d_error);
 }
 
 int launch_write_prefix(const LaunchCommon& lc, void* stream, int32_t layer, int64_t base, int64_t lp, int64_t t0,
@@ -103,10 +107,9 @@ int launch_write_prefix(const LaunchCommon& lc, void* stream, int32_t layer, int
   int64_t total = n * c.num_kv_heads * d_vecs;
   int64_t blocks = (total + 255) / 256;
   if (blocks > (int64_t)lc.num_sms * 16) blocks = (int64_t)lc.num_sms * 16;
-  hot_slab_write_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
-      (uint4*)c.hot_k, (uint4*)c.hot_v, slab_vecs, c.num_kv_heads, d_vecs, lp, t0, n, (const uint4*)d_k,
-      (const uint4*)d_v);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(hot_slab_write_kernel, dim3((unsigned)blocks), dim3(256), 0, (cudaStream_t)stream,
+                         (uint4*)c.hot_k, (uint4*)c.hot_v, slab_vecs, (int32_t)c.num_kv_heads, d_vecs, lp, t0, n,
+                         (const uint4*)d_k, (const uint4*)d_v);
 }
 
 }  // namespace gk

@@ -124,7 +124,7 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   for (int32_t gi = 0; gi < G; ++gi) {
     int32_t m = (int32_t)members[(size_t)gi].size() * g;
     int32_t lp = pl->reqs[(size_t)members[(size_t)gi][0]].lp;
-    mtiles[(size_t)gi] = (m + kPrefixTileM - 1) / kPrefixTileM;
+    mtiles[(size_t)gi] = (m + kPrefixRowsPerCta - 1) / kPrefixRowsPerCta;
     ntiles[(size_t)gi] = (lp + kPrefixTileN - 1) / kPrefixTileN;
     max_ntiles = std::max(max_ntiles, ntiles[(size_t)gi]);
   }
@@ -163,7 +163,7 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     pre_bytes += gb;
     pre_flops += gf;
   }
-  // CTA order: longest splits first; within a length, (group, split, head, mtile)
+  // CTA order: longest splits first; within a length, (group, split, head, row block)
   // so CTAs reading the same K/V tiles run side by side.
   struct Item { PrefixItemDev it; int32_t tiles; };
   std::vector<Item> items;

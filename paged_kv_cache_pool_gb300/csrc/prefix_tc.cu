@@ -8,26 +8,32 @@
 // O_p = softmax(Q K_p^T / sqrt(d)) V_p against the contiguous [Lp, d] slab of
 // (layer, KV head), read once per step instead of once per request.
 //
-// One CTA = one 128-row tile of Q x one KV head x one split of the prefix keys
-// (the plan balances splits over the SMs).  The CTA walks its split in tiles of
-// 128 keys: S = Q K^T (tcgen05.mma, bf16 in, fp32 accumulate, S in TMEM),
-// softmax warps read S rows from TMEM, write P = 2^(S*log2e/sqrt(d) - m) as bf16
-// into shared memory, and O += P V accumulates in TMEM.  The running max m is
-// only moved (and O rescaled in TMEM) when a row's max grows by more than 2^8,
-// so most tiles skip the rescale; the sum and the output use the same m, which
-// keeps the result exact up to rounding.  Each CTA emits a partial state
+// One CTA = 256 stacked rows (two 128-row Q tiles) x one KV head x one split of
+// the prefix keys (the plan balances splits over the SMs).  For each tile of
+// 128 keys the tensor core computes S_i = Q_i K^T into tensor memory (TMEM),
+// softmax warpgroup i turns S_i into P_i = 2^(S_i*log2e/sqrt(d) - m) (bf16,
+// written back over S_i in TMEM), and O_i += P_i V accumulates in TMEM with P_i
+// as the TMEM-resident A operand.  The single MMA thread issues, per key tile j,
+//     PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
+// so each softmax warpgroup has the other tile's two MMAs to hide behind, and
+// because tcgen05.mma instructions from one thread complete in issue order,
+// observing S_i(j) also proves PV_i(j-1) has finished with P_i and O_i.
+// The running max m is only raised (and O_i rescaled in TMEM) when a row's max
+// grows by more than 2^8; the row sum and the output always use the same m,
+// so the result is exact up to rounding.  Each CTA emits a partial state
 // (O normalised, LSE in log2) per row; the merge kernel combines the splits with
 // the suffix states by GraniKV Eq. 1.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads (K and V tiles, double
-// buffered), warp 1 owns tensor memory and issues the MMAs from one thread,
-// warps 2-5 stage Q, run the softmax and write the partial outputs.
+// Warp roles (320 threads): warp 0 issues TMA loads (K and V tiles, double
+// buffered), warp 1 owns tensor memory and issues every MMA from one thread,
+// warps 2-5 and 6-9 are the softmax warpgroups of Q tiles 0 and 1 (they also
+// stage Q and write the partial outputs).
 //
 // Shared-memory operand layout: every [rows x 64] bf16 region is the 128-byte
 // swizzled K-major layout (8-row x 128-byte atoms, 16-byte chunk c of row r
 // stored at chunk c ^ (r mod 8)), written by TMA for K and V and by the threads
-// for Q and P.  V is consumed as the MN-major B operand (N = d), K and P/Q as
-// K-major operands.
+// for Q.  V is consumed as the MN-major B operand (N = d), K and Q as K-major
+// operands.
 #include <cuda.h>
 
 #include <cstring>
@@ -38,11 +44,12 @@
 namespace gk {
 namespace {
 
-constexpr int BM = kPrefixTileM;   // 128 stacked rows
-constexpr int BN = kPrefixTileN;   // 128 keys
-constexpr int NSTK = 2, NSTV = 2;  // K and V pipeline depth
+constexpr int BM = kPrefixTileM;   // 128 rows per Q tile
+constexpr int BN = kPrefixTileN;   // 128 keys per K/V tile
+constexpr int NST = 2;             // K and V pipeline depth
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kRegion = BM * 128;  // one [128 rows x 64 bf16] swizzled region = 16 KB
+constexpr int kThreads = 320;
 
 struct PrefixParams {
   const PrefixGroupDev* groups;
@@ -61,26 +68,24 @@ struct PrefixParams {
 // barrier slots
 enum : int {
   B_QFULL = 0,
-  B_KFULL = 1,                 // NSTK
-  B_KEMPTY = B_KFULL + NSTK,   // NSTK
-  B_VFULL = B_KEMPTY + NSTK,   // NSTV
-  B_VEMPTY = B_VFULL + NSTV,   // NSTV
-  B_SFULL = B_VEMPTY + NSTV,   // 2
-  B_SEMPTY = B_SFULL + 2,      // 2
-  B_PFULL = B_SEMPTY + 2,
-  B_PVDONE = B_PFULL + 1,
-  B_DRAIN = B_PVDONE + 1,
-  B_COUNT = B_DRAIN + 1
+  B_KFULL = 1,                // NST
+  B_KEMPTY = B_KFULL + NST,   // NST
+  B_VFULL = B_KEMPTY + NST,   // NST
+  B_VEMPTY = B_VFULL + NST,   // NST
+  B_SFULL = B_VEMPTY + NST,   // one per Q tile
+  B_PFULL = B_SFULL + 2,      // one per Q tile
+  B_OFINAL = B_PFULL + 2,
+  B_COUNT = B_OFINAL + 1
 };
 
 template <int D>
 struct Layout {
-  static constexpr uint32_t kTile = BN * D * 2;  // one K or V tile (= Q tile bytes)
+  static constexpr uint32_t kTile = BN * D * 2;      // one K or V tile
+  static constexpr uint32_t kQTile = BM * D * 2;     // one Q tile
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + BM * D * 2;
-  static constexpr uint32_t kV = kK + NSTK * kTile;
-  static constexpr uint32_t kP = kV + NSTV * kTile;
-  static constexpr uint32_t kBars = kP + BM * BN * 2;
+  static constexpr uint32_t kK = kQ + 2 * kQTile;
+  static constexpr uint32_t kV = kK + NST * kTile;
+  static constexpr uint32_t kBars = kV + NST * kTile;
   static constexpr uint32_t kTmemSlot = kBars + B_COUNT * 8;
   static constexpr uint32_t kFlag = kTmemSlot + 4;
   static constexpr uint32_t kBytes = kFlag + 4;
@@ -101,6 +106,16 @@ __host__ __device__ constexpr uint32_t idesc(int n, bool b_mn_major) {
          ((uint32_t)(BM >> 4) << 24);
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]^T
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t id,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(id), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int32_t* err, volatile int* abort_flag) {
   for (int i = 0; i < 64; ++i)
     if (mbar_try_wait(bar, parity)) return true;
@@ -117,13 +132,13 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1) prefix_kernel(const PrefixParams p) {
+__global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams p) {
   using Lay = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  const uint32_t sQ = base + Lay::kQ, sK = base + Lay::kK, sV = base + Lay::kV, sP = base + Lay::kP;
+  const uint32_t sQ = base + Lay::kQ, sK = base + Lay::kK, sV = base + Lay::kV;
   auto bar = [&](int i) { return base + Lay::kBars + 8u * (uint32_t)i; };
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Lay::kTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kFlag);
@@ -135,26 +150,65 @@ __global__ void __launch_bounds__(192, 1) prefix_kernel(const PrefixParams p) {
   const int tile0 = it.split * gr.split_tiles;
   const int ntiles = min(gr.split_tiles, ntiles_all - tile0);
   const int key0 = tile0 * BN;
+  const int row0 = it.mblock * kPrefixRowsPerCta;
+  const bool two = row0 + BM < gr.m;  // does Q tile 1 hold any row?
 
+  griddep_launch_dependents();
+  // plan tables and the HOT pool are not written by the kernels of a decode
+  // step; the queries and the partial-state buffer may be, so wait for them
+  griddep_wait();
+  // softmax threads fetch their Q row now, so the global-load latency overlaps the set-up
+  const int qi_ = (warp - 2) >> 2;
+  const int row_ = (warp & 3) * 32 + lane;
+  const int grow_ = row0 + qi_ * BM + row_;
+  const bool row_valid_ = warp >= 2 && grow_ < gr.m;
+  int req_ = 0, qh_ = 0;
+  if (row_valid_) {
+    req_ = p.prefix_reqs[gr.req_base + grow_ / p.G];
+    qh_ = it.head * p.G + grow_ % p.G;
+  }
+  uint4 qrow[D / 8];
+  if (warp >= 2) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)req_ * p.Hq + qh_) * D);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) qrow[c] = row_valid_ ? src[c] : make_uint4(0, 0, 0, 0);
+  }
+  if (warp == 0 && lane == 0 && ntiles > 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(p.tmaps + (size_t)gr.tmap_index * 128) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(p.tmaps + (size_t)(gr.tmap_index + 1) * 128) : "memory");
+  }
   if (threadIdx.x == 0) {
-    mbar_init(bar(B_QFULL), 128);
-    for (int s = 0; s < NSTK; ++s) {
+    mbar_init(bar(B_QFULL), 256);
+    for (int s = 0; s < NST; ++s) {
       mbar_init(bar(B_KFULL + s), 1);
       mbar_init(bar(B_KEMPTY + s), 1);
-    }
-    for (int s = 0; s < NSTV; ++s) {
       mbar_init(bar(B_VFULL + s), 1);
       mbar_init(bar(B_VEMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_SFULL + s), 1);
-      mbar_init(bar(B_SEMPTY + s), 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_SFULL + i), 1);
+      mbar_init(bar(B_PFULL + i), 128);
     }
-    mbar_init(bar(B_PFULL), 128);
-    mbar_init(bar(B_PVDONE), 1);
-    mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_OFINAL), 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // the first K/V tiles need nothing but the barriers: start them now so their
+    // latency overlaps the tensor-memory allocation and the Q staging
+    if (ntiles > 0) {
+      const void* tmK = p.tmaps + (size_t)gr.tmap_index * 128;
+      const void* tmV = p.tmaps + (size_t)(gr.tmap_index + 1) * 128;
+      tmap_acquire(tmK);
+      tmap_acquire(tmV);
+      const int z = p.layer * p.Hkv + it.head;
+      for (int j = 0; j < NST && j < ntiles; ++j) {
+        mbar_arrive_expect_tx(bar(B_KFULL + j), Lay::kTile);
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(sK + j * Lay::kTile + h * kRegion, tmK, h * 64, key0 + j * BN, z, bar(B_KFULL + j));
+        mbar_arrive_expect_tx(bar(B_VFULL + j), Lay::kTile);
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_3d(sV + j * Lay::kTile + h * kRegion, tmV, h * 64, key0 + j * BN, z, bar(B_VFULL + j));
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(base + Lay::kTmemSlot, kTmemCols);
@@ -164,39 +218,35 @@ __global__ void __launch_bounds__(192, 1) prefix_kernel(const PrefixParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 2 * BN;
+  // columns: S/P of tile 0 at 0, of tile 1 at 128; O of tile 0 at 256, of tile 1 at 384
+  auto tS = [&](int i) { return tmem + (uint32_t)i * BN; };
+  auto tO = [&](int i) { return tmem + 2u * BN + (uint32_t)i * 128u; };
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
     if (lane == 0 && ntiles > 0) {
       const void* tmK = p.tmaps + (size_t)gr.tmap_index * 128;
       const void* tmV = p.tmaps + (size_t)(gr.tmap_index + 1) * 128;
-      tmap_acquire(tmK);
-      tmap_acquire(tmV);
       const int z = p.layer * p.Hkv + it.head;
-      int issued = 0;
-      for (int j = 0; j < ntiles; ++j) {
-        const int sk = j % NSTK, rk = j / NSTK;
-        if (rk > 0 && !wait_or_abort(bar(B_KEMPTY + sk), (rk - 1) & 1, p.err, abort_flag)) break;
-        mbar_arrive_expect_tx(bar(B_KFULL + sk), Lay::kTile);
+      int issued = 2 * min(NST, ntiles);
+      for (int j = NST; j < ntiles; ++j) {
+        const int st = j % NST, r = j / NST;
+        if (r > 0 && !wait_or_abort(bar(B_KEMPTY + st), (r - 1) & 1, p.err, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(B_KFULL + st), Lay::kTile);
         for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(sK + sk * Lay::kTile + h * kRegion, tmK, h * 64, key0 + j * BN, z, bar(B_KFULL + sk));
-        const int sv = j % NSTV, rv = j / NSTV;
-        if (rv > 0 && !wait_or_abort(bar(B_VEMPTY + sv), (rv - 1) & 1, p.err, abort_flag)) {
-          issued = 2 * j + 1;
-          break;
-        }
-        mbar_arrive_expect_tx(bar(B_VFULL + sv), Lay::kTile);
+          tma_load_3d(sK + st * Lay::kTile + h * kRegion, tmK, h * 64, key0 + j * BN, z, bar(B_KFULL + st));
+        issued = 2 * j + 1;
+        if (r > 0 && !wait_or_abort(bar(B_VEMPTY + st), (r - 1) & 1, p.err, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(B_VFULL + st), Lay::kTile);
         for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(sV + sv * Lay::kTile + h * kRegion, tmV, h * 64, key0 + j * BN, z, bar(B_VFULL + sv));
+          tma_load_3d(sV + st * Lay::kTile + h * kRegion, tmV, h * 64, key0 + j * BN, z, bar(B_VFULL + st));
         issued = 2 * j + 2;
       }
       if (*abort_flag) {
         // let the loads already issued land before shared memory goes away
-        for (int q = max(0, issued - 2 * NSTK); q < issued; ++q) {
+        for (int q = max(0, issued - 2 * NST); q < issued; ++q) {
           const int j = q / 2;
-          if (q % 2 == 0) mbar_wait(bar(B_KFULL + j % NSTK), (j / NSTK) & 1, nullptr);
-          else mbar_wait(bar(B_VFULL + j % NSTV), (j / NSTV) & 1, nullptr);
+          mbar_wait(bar((q % 2 == 0 ? B_KFULL : B_VFULL) + j % NST), (j / NST) & 1, nullptr);
         }
       }
     }
@@ -205,151 +255,192 @@ __global__ void __launch_bounds__(192, 1) prefix_kernel(const PrefixParams p) {
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t kIdQK = idesc(BN, false);
       constexpr uint32_t kIdPV = idesc(D, true);
-      bool ok = wait_or_abort(bar(B_QFULL), 0, p.err, abort_flag);
-      auto issue_pv = [&](int i) -> bool {
-        if (!wait_or_abort(bar(B_PFULL), i & 1, p.err, abort_flag)) return false;
-        const int sv = i % NSTV;
-        if (!wait_or_abort(bar(B_VFULL + sv), (i / NSTV) & 1, p.err, abort_flag)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t a = sdesc(sP + (kk / 4) * kRegion + (kk % 4) * 32, 16, 1024);
-          const uint64_t b = sdesc(sV + sv * Lay::kTile + kk * 2048, kRegion, 1024);
-          tc_mma_ss(tO, a, b, kIdPV, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(bar(B_PVDONE));
-        tc_commit(bar(B_VEMPTY + sv));
-        return true;
-      };
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int sk = j % NSTK, sb = j & 1;
-        if (!wait_or_abort(bar(B_KFULL + sk), (j / NSTK) & 1, p.err, abort_flag)) { ok = false; break; }
-        if (j >= 2 && !wait_or_abort(bar(B_SEMPTY + sb), ((j - 2) >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
-        tc_fence_after();
+      const int nq = two ? 2 : 1;
+      auto issue_s = [&](int i, int j) {
+        const int st = j % NST;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = sdesc(sQ + (kk / 4) * kRegion + (kk % 4) * 32, 16, 1024);
-          const uint64_t b = sdesc(sK + sk * Lay::kTile + (kk / 4) * kRegion + (kk % 4) * 32, 16, 1024);
-          tc_mma_ss(tS + sb * BN, a, b, kIdQK, kk > 0 ? 1u : 0u);
+          const uint64_t a = sdesc(sQ + i * Lay::kQTile + (kk / 4) * kRegion + (kk % 4) * 32, 16, 1024);
+          const uint64_t b = sdesc(sK + st * Lay::kTile + (kk / 4) * kRegion + (kk % 4) * 32, 16, 1024);
+          tc_mma_ss(tS(i), a, b, kIdQK, kk > 0 ? 1u : 0u);
         }
-        tc_commit(bar(B_SFULL + sb));
-        tc_commit(bar(B_KEMPTY + sk));
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        tc_commit(bar(B_SFULL + i));
+      };
+      auto issue_pv = [&](int i, int j) {
+        const int st = j % NST;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t b = sdesc(sV + st * Lay::kTile + kk * 2048, kRegion, 1024);
+          tc_mma_ts(tO(i), tS(i) + kk * 8, b, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = wait_or_abort(bar(B_QFULL), 0, p.err, abort_flag) &&
+                wait_or_abort(bar(B_KFULL), 0, p.err, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        for (int i = 0; i < nq; ++i) issue_s(i, 0);
+        tc_commit(bar(B_KEMPTY));
       }
-      if (ok) issue_pv(ntiles - 1);
-      // every MMA issued above has finished before tensor memory is released
-      tc_commit(bar(B_DRAIN));
-      mbar_wait(bar(B_DRAIN), 0, nullptr);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        const int st = j % NST;
+        const bool more = j + 1 < ntiles;
+        if (!wait_or_abort(bar(B_VFULL + st), (j / NST) & 1, p.err, abort_flag)) { ok = false; break; }
+        if (more && !wait_or_abort(bar(B_KFULL + (j + 1) % NST), ((j + 1) / NST) & 1, p.err, abort_flag)) { ok = false; break; }
+        for (int i = 0; i < nq; ++i) {
+          if (!wait_or_abort(bar(B_PFULL + i), j & 1, p.err, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(i, j);          // reads P_i(j) from TMEM ...
+          if (more) issue_s(i, j + 1);   // ... before S_i(j+1) overwrites it (in-order completion)
+        }
+        if (!ok) break;
+        tc_commit(bar(B_VEMPTY + st));
+        if (more) tc_commit(bar(B_KEMPTY + (j + 1) % NST));
+      }
+      // every MMA issued above has finished before the epilogue reads O and TMEM is released
+      tc_commit(bar(B_OFINAL));
     }
   } else {
     // ---------------------- softmax / correction / epilogue ---------------------
-    const int wq = warp & 3;                // TMEM sub-partition of this warp
-    const int row = wq * 32 + lane;         // tile row = TMEM lane
+    const int qi = qi_;                      // Q tile of this warpgroup
+    const int wq = warp & 3;                 // TMEM sub-partition of this warp
+    const int row = row_;                    // tile row = TMEM lane
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const int grow = it.mtile * BM + row;   // stacked row within the group
-    const bool row_valid = grow < gr.m;
-    int req = 0, qh = 0;
-    if (row_valid) {
-      req = p.prefix_reqs[gr.req_base + grow / p.G];
-      qh = it.head * p.G + grow % p.G;
-    }
-    // stage Q (zero rows pad the tile)
+    const bool row_valid = row_valid_;
+    const int req = req_, qh = qh_;
     {
-      const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)req * p.Hq + qh) * D);
+      const uint32_t qbase = sQ + qi * Lay::kQTile;
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
-        uint4 v = row_valid ? src[c] : make_uint4(0, 0, 0, 0);
         const int cc = c & 7;
-        sts128(sQ + (c >> 3) * kRegion + row * 128 + ((cc ^ (row & 7)) << 4), v);
+        sts128(qbase + (c >> 3) * kRegion + row * 128 + ((cc ^ (row & 7)) << 4), qrow[c]);
       }
       fence_async_shared();
       mbar_arrive(bar(B_QFULL));
     }
+    const bool active = ntiles > 0 && (qi == 0 || two);
     float m_used = -INFINITY, l = 0.f;
-    bool ok = ntiles > 0;
+    bool ok = active;
     for (int j = 0; ok && j < ntiles; ++j) {
-      const int sb = j & 1;
-      if (!wait_or_abort(bar(B_SFULL + sb), (j >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
+      if (!wait_or_abort(bar(B_SFULL + qi), j & 1, p.err, abort_flag)) { ok = false; break; }
       tc_fence_after();
       float s[BN];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + sb * BN + c * 32 + lane_off, s + c * 32);
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS(qi) + c * 32 + lane_off, s + c * 32);
       tc_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(B_SEMPTY + sb));
-
-      const int nvalid = min(BN, gr.lp - (key0 + j * BN));
-      float mx = -INFINITY;
+      const int nvalid = gr.lp - (key0 + j * BN);
+      if (nvalid < BN) {
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        s[c] = c < nvalid ? s[c] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[c]);
+        for (int c = 0; c < BN; ++c) s[c] = c < nvalid ? s[c] : -INFINITY;
       }
-      bool pv_waited = false;
-      const bool need = mx > m_used + 8.0f;
-      if (__any_sync(0xffffffffu, need)) {
+      // row max: eight independent chains of 3-input max
+      float mx8[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) mx8[c] = s[c];
+#pragma unroll
+      for (int c = 8; c + 16 <= BN; c += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], s[c + k], s[c + 8 + k]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], s[BN - 8 + k]);
+      float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+      mx *= p.scale_log2;
+      if (__any_sync(0xffffffffu, mx > m_used + 8.0f)) {
         const float m_new = fmaxf(m_used, mx);
         if (j > 0) {
-          // O holds tiles 0..j-1 scaled by 2^-m_used: wait for PV(j-1), then rescale in TMEM
-          if (!wait_or_abort(bar(B_PVDONE), (j - 1) & 1, p.err, abort_flag)) { ok = false; break; }
-          pv_waited = true;
-          tc_fence_after();
+          // S(j) completed after PV(j-1): O holds keys 0..j-1 scaled by 2^-m_used
           const float f = ex2(m_used - m_new);
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             float o[32];
-            tmem_ld32(tO + c * 32 + lane_off, o);
+            tmem_ld32(tO(qi) + c * 32 + lane_off, o);
             tc_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) o[e] *= f;
-            tmem_st32(tO + c * 32 + lane_off, o);
+            tmem_st32(tO(qi) + c * 32 + lane_off, o);
           }
-          tc_wait_st();
           l *= f;
         }
         m_used = m_new;
       }
+      // P = 2^(s*scale - m): three pairs in four on MUFU, one on the FMA pipe
+      const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2), nm2 = f2pack(-m_used, -m_used);
       uint32_t pk[BN / 2];
-      float sum = 0.f;
+      uint64_t sum4[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int c = 0; c < BN / 2; ++c) {
-        const float a = ex2(s[2 * c] - m_used), b = ex2(s[2 * c + 1] - m_used);
-        sum += a + b;
+        float xa, xb, a, b;
+        f2unpack(ffma2(f2pack(s[2 * c], s[2 * c + 1]), sc2, nm2), xa, xb);
+        if ((c & 3) == 3) {
+          exp2_poly_pair(xa, xb, a, b);
+        } else {
+          a = ex2(xa);
+          b = ex2(xb);
+        }
+        sum4[c & 3] = fadd2(sum4[c & 3], f2pack(a, b));
         pk[c] = pack_bf16x2(a, b);
       }
-      l += sum;
-      if (!pv_waited && j > 0) {
-        // the P buffer is free once PV(j-1) has read it
-        if (!wait_or_abort(bar(B_PVDONE), (j - 1) & 1, p.err, abort_flag)) { ok = false; break; }
+      {
+        float s0, s1, s2, s3, s4, s5, s6, s7;
+        f2unpack(fadd2(sum4[0], sum4[1]), s0, s1);
+        f2unpack(fadd2(sum4[2], sum4[3]), s2, s3);
+        (void)s4; (void)s5; (void)s6; (void)s7;
+        l += (s0 + s1) + (s2 + s3);
       }
-#pragma unroll
-      for (int c = 0; c < BN / 8; ++c) {
-        const int cc = c & 7;
-        sts128(sP + (c >> 3) * kRegion + row * 128 + ((cc ^ (row & 7)) << 4),
-               make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
-      }
-      fence_async_shared();
+      // P over S in TMEM (packed bf16 pairs, key 2c in the low half of column c)
+      tmem_st32(tS(qi) + lane_off, reinterpret_cast<const float*>(pk));
+      tmem_st32(tS(qi) + 32 + lane_off, reinterpret_cast<const float*>(pk + 32));
+      tc_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(B_PFULL));
+      mbar_arrive(bar(B_PFULL + qi));
     }
-    if (ok && wait_or_abort(bar(B_PVDONE), (ntiles - 1) & 1, p.err, abort_flag)) {
+    if (ok && wait_or_abort(bar(B_OFINAL), 0, p.err, abort_flag)) {
+      // Every MMA has finished, so the Q/K/V staging area is free: each thread
+      // parks its normalised O row there, then each warp stores whole rows
+      // (one coalesced d*4-byte store per row) to its partial-state slot.
       tc_fence_after();
+      constexpr uint32_t kRowBytes = D * 4 + 16;          // padded: conflict-free row writes
+      const uint32_t stage = sQ + (uint32_t)qi * BM * kRowBytes;
+      // destination of each row, looked up once by the row's own thread
+      const uint32_t dst_tab = sQ + 2u * BM * kRowBytes + (uint32_t)qi * BM * 8;
+      {
+        float* dst = nullptr;
+        if (row_valid) {
+          const int64_t entry = (int64_t)p.reqs[req].entry_cas + it.split;
+          dst = p.part_o + (entry * p.Hq + qh) * D;
+          p.part_l[entry * p.Hq + qh] = m_used + __log2f(l);
+        }
+        asm volatile("st.shared.u64 [%0], %1;" ::"r"(dst_tab + row * 8), "l"((uint64_t)dst) : "memory");
+      }
       const float inv = 1.f / l;
-      const float lse2 = m_used + __log2f(l);
-      const int64_t entry = row_valid ? (int64_t)p.reqs[req].entry_cas + it.split : 0;
-      float* dst = p.part_o + (entry * p.Hq + qh) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
-        tmem_ld32(tO + c * 32 + lane_off, o);
+        tmem_ld32(tO(qi) + c * 32 + lane_off, o);
         tc_wait_ld();
-        if (row_valid) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + c * 32 + e) = make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+        for (int e = 0; e < 32; e += 4)
+          sts128(stage + row * kRowBytes + (c * 32 + e) * 4,
+                 make_uint4(__float_as_uint(o[e] * inv), __float_as_uint(o[e + 1] * inv),
+                            __float_as_uint(o[e + 2] * inv), __float_as_uint(o[e + 3] * inv)));
+      }
+      asm volatile("bar.sync %0, 128;" ::"r"(1 + qi) : "memory");
+      // rows of this warp's 32-row slice; D/4 lanes cover a row
+      constexpr int kLanesPerRow = D / 4;
+      constexpr int kRowsPerPass = 32 / kLanesPerRow;
+      const int sub = lane % kLanesPerRow;
+#pragma unroll 1
+      for (int r0 = 0; r0 < 32; r0 += kRowsPerPass) {
+        const int rr = wq * 32 + r0 + lane / kLanesPerRow;
+        uint64_t dst;
+        asm volatile("ld.shared.u64 %0, [%1];" : "=l"(dst) : "r"(dst_tab + rr * 8));
+        if (dst) {
+          const uint4 v = lds128(stage + rr * kRowBytes + sub * 16);
+          reinterpret_cast<uint4*>(dst)[sub] = v;
         }
       }
-      if (row_valid) p.part_l[entry * p.Hq + qh] = lse2;
+    } else if (!active && warp >= 2) {
+      // an idle warpgroup (single-tile CTA) waits for the MMAs before TMEM is released
+      if (ntiles > 0) wait_or_abort(bar(B_OFINAL), 0, p.err, abort_flag);
     }
     tc_fence_before();
   }
@@ -383,8 +474,8 @@ int launch_prefix_t(const PrefixParams& pp, int ctas, cudaStream_t st) {
   auto kern = prefix_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Layout<D>::kDynamic);
   if (e != cudaSuccess) return (int)e;
-  kern<<<ctas, 192, Layout<D>::kDynamic, st>>>(pp);
-  return (int)cudaGetLastError();
+  e = launch_pdl(kern, dim3(ctas), dim3(kThreads), Layout<D>::kDynamic, st, pp);
+  return (int)e;
 }
 
 }  // namespace
