@@ -212,6 +212,9 @@ def run_ours(a, w):
     gw = GpuWorkload(w, extra_steps=total_steps)
     eng = gw.eng
     pool = eng.pool
+    cm_path = os.path.join(ROOT, "paged_kv_cache_pool_gb300", "cost_model_gb300.json")
+    if os.path.exists(cm_path):
+        gk.gk_cost_model_load(pool, open(cm_path).read())
     L, B, Hq, Hkv, d = w.L, w.B, w.Hq, w.Hkv, w.d
     stream = torch.cuda.current_stream()
     bf = torch.bfloat16
@@ -247,6 +250,7 @@ def run_ours(a, w):
     launches = [0]
     dense_merge = [0]
     choices = []
+    predicted = []
 
     def step(events=None, q=q_all, k=newk, v=newv, out=out_all, lse=lse_all):
         # a0: host plan (append one token per request, tables, plan, dispatch)
@@ -268,7 +272,8 @@ def run_ours(a, w):
         else:
             gk.gk_plan_update(pool, plan[0], batch, stream)
         dense_merge[0] = gk.gk_plan_info(plan[0])["dense_merge"]
-        choice, _, _ = gk.gk_dispatch(pool, plan[0])
+        choice, t_d, t_c = gk.gk_dispatch(pool, plan[0])
+        predicted.append((t_d, t_c))
         if forced is not None:
             choice = forced
         choices.append(choice)
@@ -443,11 +448,17 @@ def run_ours(a, w):
     if not a.no_cpu:
         cpu = cpu_baseline(w)
     backend_name = "cascade" if step_choices and step_choices[0] == gk.GK_BACKEND_CASCADE else "dense"
+    pd, pc = predicted[-1]
+    layer_us = ms_per_step * 1e3 / L
+    dispatch = {"choice": backend_name, "predicted_dense_us": pd, "predicted_cascade_us": pc,
+                "measured_layer_us": layer_us,
+                "prediction_error": ((pc if backend_name == "cascade" else pd) - layer_us) / layer_us,
+                "cost_model": "paged_kv_cache_pool_gb300/cost_model_gb300.json" if os.path.exists(cm_path) else "library defaults"}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic", "config": _config_dict(w, backend_name),
             "clocks": clk, "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roof,
-            "cpu_baseline": cpu, "kernels": kernels,
+            "cpu_baseline": cpu, "kernels": kernels, "dispatch": dispatch,
             "query_rows_per_s": value * Hq,
             "plan": info}
     print(json.dumps(line))

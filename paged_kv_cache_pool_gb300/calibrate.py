@@ -1,0 +1,159 @@
+"""Measure the dispatcher's cost model on this GPU (GraniKV Section 3.6: the
+routing rule stays, its numbers are re-fit per GPU; Appendix B.4b's sweep).
+
+Times, with CUDA events, on one layer of synthetic pools (random bf16 data):
+  * the flat backend over several (B, Lp, s)           -> c_flat_us, bw_flat_gbs
+  * the suffix gather over several suffix volumes        -> bw_suffix_gbs
+  * the prefix kernel at M_eff = B * g from 32 to 2048   -> tc_points (achieved TFLOP/s)
+  * the merge                                            -> c_merge_us per (request, head)
+  * the whole cascade                                    -> c_cascade_us (mean residual)
+and writes the JSON that gk_cost_model_load reads.
+
+    python -m paged_kv_cache_pool_gb300.calibrate --out cost_model_gb300.json
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import numpy as np
+
+from . import binding as gk
+from .engine import Engine
+
+
+def _time(fn, reps=10, warm=3):
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / reps  # us
+
+
+class _Case:
+    """One layer of a pool with B requests sharing a prefix of Lp and suffixes of s tokens."""
+
+    def __init__(self, eng, B, lp, s, Hq, d):
+        import torch
+        self.eng = eng
+        base = eng.prefix_alloc(lp)
+        self.base = base
+        seqs = [eng.seq_create() for _ in range(B)]
+        order = np.repeat(np.asarray(seqs, np.int32), s)
+        if len(order):
+            eng.append_slots(order)
+        self.seqs = seqs
+        table = eng.block_tables(seqs)
+        self.d_table = eng.to_device(table)
+        self.batch = eng.batch([base] * B, [lp] * B, [s] * B, self.d_table, table.shape[1])
+        self.q = torch.randn((B, Hq, d), device=eng.device).to(torch.bfloat16)
+        self.out = torch.empty((B, Hq, d), device=eng.device)
+        self.lse = torch.empty((B, Hq), device=eng.device)
+        self.batch.set_device(d_q=self.q, d_out=self.out, d_lse=self.lse)
+        self.plan = gk.gk_plan_build(eng.pool, self.batch)
+        self.info = gk.gk_plan_info(self.plan)
+
+    def close(self):
+        gk.gk_plan_destroy(self.plan)
+        for s in self.seqs:
+            self.eng.seq_release(s)
+        gk.gk_prefix_release(self.eng.pool, self.base)
+
+
+def calibrate(Hq=32, Hkv=8, d=128, device="cuda"):
+    import torch
+    g = Hq // Hkv
+    hot = 32768 + 16
+    cold = 256 * 2048 + 64 * 4096 + 4096
+    eng = Engine(1, Hq, Hkv, d, hot, cold, 1, seed=1, device=device)
+    eng.hot_k.normal_()
+    eng.hot_v.normal_()
+    eng.cold_k.normal_()
+    eng.cold_v.normal_()
+    pool = eng.pool
+    kv_tok = 2 * Hkv * d * 2
+
+    flat_pts, suf_pts, cas_pts, merge_pts = [], [], [], []
+    tc_points = []
+    for B, lp, s in [(8, 2048, 256), (32, 4096, 512), (64, 16384, 1024), (128, 8192, 512), (256, 4096, 1024)]:
+        c = _Case(eng, B, lp, s, Hq, d)
+        t_flat = _time(lambda: gk.gk_decode_dense(pool, None, 0, c.batch, c.plan))
+        t_pre = _time(lambda: gk.gk_cascade_prefix(pool, None, 0, c.batch, c.plan))
+        t_suf = _time(lambda: gk.gk_cascade_suffix(pool, None, 0, c.batch, c.plan))
+        t_mrg = _time(lambda: gk.gk_cascade_merge(pool, None, 0, c.batch, c.plan))
+        t_cas = _time(lambda: gk.gk_decode_cascade(pool, None, 0, c.batch, c.plan))
+        flat_pts.append((c.info["dense_bytes"], t_flat))
+        suf_pts.append((c.info["suffix_bytes"], t_suf))
+        merge_pts.append((B * Hq, t_mrg))
+        cas_pts.append((c.info, t_cas, B))
+        c.close()
+    # prefix throughput against M_eff at a fixed long prefix
+    for B in (8, 16, 32, 64, 128, 256, 512):
+        c = _Case(eng, B, 8192, 0, Hq, d)
+        t_pre = _time(lambda: gk.gk_cascade_prefix(pool, None, 0, c.batch, c.plan))
+        tc_points.append([float(B * g), c.info["prefix_flops"] / (t_pre * 1e-6) / 1e12])
+        c.close()
+    eng.close()
+    torch.cuda.synchronize()
+
+    return refit(dict(flat=flat_pts, suffix=suf_pts, merge=merge_pts,
+                      cascade=[(i["max_m_eff"], t) for i, t, _ in cas_pts],
+                      cascade_info=[dict(max_m_eff=i["max_m_eff"], prefix_bytes=i["prefix_bytes"],
+                                         prefix_flops=i["prefix_flops"], suffix_bytes=i["suffix_bytes"], B=B,
+                                         Hq=Hq) for i, _, B in cas_pts],
+                      tc_points=tc_points))
+
+
+def _linfit(pts):
+    x = np.array([p[0] for p in pts], float)
+    y = np.array([p[1] for p in pts], float)
+    A = np.vstack([np.ones_like(x), x]).T
+    (c0, slope), *_ = np.linalg.lstsq(A, y, rcond=None)
+    return max(0.0, float(c0)), float(slope)
+
+
+def refit(measured):
+    """Cost-model coefficients from the measured points (intercepts are fixed costs)."""
+    c_flat, s_flat = _linfit(measured["flat"])
+    c_suf, s_suf = _linfit(measured["suffix"])
+    c_mrg, s_mrg = _linfit(measured["merge"])
+    tc_points = sorted([list(p) for p in measured["tc_points"]])
+    cm = dict(c_flat_us=c_flat, bw_flat_gbs=1.0 / max(s_flat, 1e-12) / 1e3, c_cascade_us=0.0,
+              bw_prefix_gbs=6000.0, bw_suffix_gbs=1.0 / max(s_suf, 1e-12) / 1e3, c_merge_us=max(s_mrg, 0.0),
+              tc_points=tc_points)
+    # the cascade's fixed cost: the suffix and merge launches' intercepts, plus the mean
+    # residual of the whole cascade over that model when it is positive
+    base = c_suf + c_mrg
+    res = []
+    for info, (_, t_cas) in zip(measured["cascade_info"], measured["cascade"]):
+        tc = float(np.interp(info["max_m_eff"], [p[0] for p in tc_points], [p[1] for p in tc_points]))
+        t_pre = max(info["prefix_bytes"] / (cm["bw_prefix_gbs"] * 1e3), info["prefix_flops"] / (tc * 1e6))
+        model = base + t_pre + info["suffix_bytes"] / (cm["bw_suffix_gbs"] * 1e3) + cm["c_merge_us"] * info["B"] * info["Hq"]
+        res.append(t_cas - model)
+    cm["c_cascade_us"] = base + max(0.0, float(np.mean(res)))
+    cm["measured"] = measured
+    return cm
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--out", default=None)
+    a = ap.parse_args()
+    from . import build
+    build.build()
+    cm = calibrate()
+    text = json.dumps(cm, indent=1)
+    if a.out:
+        with open(a.out, "w") as f:
+            f.write(text)
+    print(text)
+
+
+if __name__ == "__main__":
+    main()

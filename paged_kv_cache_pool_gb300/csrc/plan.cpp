@@ -393,6 +393,38 @@ struct JsonReader {
     s = end;
     return true;
   }
+  // skip any value (number, string, literal, array, object) of a key we do not use
+  bool skip() {
+    ws();
+    if (*s == '"') {
+      std::string t;
+      return str(&t);
+    }
+    if (*s == '[' || *s == '{') {
+      const char open = *s, close = (*s == '[') ? ']' : '}';
+      ++s;
+      ws();
+      if (*s == close) { ++s; return true; }
+      while (true) {
+        if (open == '{') {
+          std::string k;
+          if (!str(&k) || !eat(':')) return false;
+        }
+        if (!skip()) return false;
+        ws();
+        if (*s == ',') { ++s; continue; }
+        if (*s == close) { ++s; return true; }
+        return false;
+      }
+    }
+    double v;
+    if (num(&v)) return true;
+    for (const char* lit : {"true", "false", "null"}) {
+      size_t n = std::strlen(lit);
+      if (std::strncmp(s, lit, n) == 0) { s += n; return true; }
+    }
+    return false;
+  }
 };
 
 }  // namespace gk
@@ -498,13 +530,16 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
       cm.n_tc_points = n;
       continue;
     }
-    double v;
-    if (!rd.num(&v)) {
-      // skip a string value (comments such as "source")
-      std::string tmp;
-      if (!rd.str(&tmp)) return bad("values must be numbers");
+    static const char* kNumeric[] = {"c_flat_us", "bw_flat_gbs", "c_cascade_us", "bw_prefix_gbs", "bw_suffix_gbs",
+                                     "c_merge_us"};
+    bool known = false;
+    for (const char* k : kNumeric) known = known || key == k;
+    if (!known) {
+      if (!rd.skip()) return bad("malformed value");
       continue;
     }
+    double v;
+    if (!rd.num(&v)) return bad("values must be numbers");
     if (key == "c_flat_us") cm.c_flat_us = v;
     else if (key == "bw_flat_gbs") cm.bw_flat_gbs = v;
     else if (key == "c_cascade_us") cm.c_cascade_us = v;

@@ -277,3 +277,38 @@ def test_cost_model_json_rejects_bad_input(gk):
             assert e.value.status == gk.GK_ERR_INVALID
     finally:
         gk.gk_pool_destroy(pool)
+
+
+def test_measured_cost_model_routes_the_workloads(gk):
+    """The committed GB300 cost model loads, and routes the five workloads (long shared
+    prefixes) to the cascade while a batch of one with a short prefix goes flat."""
+    from synth import workloads
+    text = open(os.path.join(ROOT, "paged_kv_cache_pool_gb300", "cost_model_gb300.json")).read()
+    for n in (1, 2, 3, 4, 5):
+        w = workloads.config(n)
+        pool = gk.gk_pool_create(w.L, w.Hq, w.Hkv, w.d, w.hot_tokens(), w.cold_slots(), w.page_size, 0)
+        try:
+            gk.gk_cost_model_load(pool, text)
+            bases = [gk.gk_prefix_alloc(pool, lp) for lp in w.prefix_lens]
+            b = gk.Batch([bases[r.prefix] for r in w.requests], [w.prefix_lens[r.prefix] for r in w.requests],
+                         [r.suffix_len for r in w.requests], None, 8192)
+            plan = gk.gk_plan_build(pool, b)
+            choice, td, tc = gk.gk_dispatch(pool, plan)
+            if n > 1:
+                assert choice == gk.GK_BACKEND_CASCADE and tc < td
+            gk.gk_plan_destroy(plan)
+        finally:
+            gk.gk_pool_destroy(pool)
+    # no sharing: 64 requests, each with its own 4096-token prefix -> 64 groups of M_eff 4,
+    # where the stacked contraction runs at a sliver of the tensor peak and flat attention wins
+    pool = gk.gk_pool_create(1, 32, 8, 128, 64 * 4096, 64 * 256, 1, 0)
+    try:
+        gk.gk_cost_model_load(pool, text)
+        bases = [gk.gk_prefix_alloc(pool, 4096) for _ in range(64)]
+        b = gk.Batch(bases, [4096] * 64, [100] * 64, None, 256)
+        plan = gk.gk_plan_build(pool, b)
+        choice, td, tc = gk.gk_dispatch(pool, plan)
+        assert choice == gk.GK_BACKEND_DENSE and td < tc
+        gk.gk_plan_destroy(plan)
+    finally:
+        gk.gk_pool_destroy(pool)
