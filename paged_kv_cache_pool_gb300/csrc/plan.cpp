@@ -20,7 +20,7 @@ namespace {
 
 constexpr int kGatherQuantum = 16;        // gather CTAs get token quotas in multiples of this
 constexpr int kMinGatherQuota = 64;
-constexpr double kPrefixCtaOverheadTiles = 1.5;
+constexpr double kPrefixCtaOverheadTiles = 2.5;   // CTA set-up + epilogue, in 128-key tiles
 
 template <class T>
 size_t append_region(size_t* off, size_t count, size_t align = 16) {

@@ -15,17 +15,19 @@
 // written back over S_i in TMEM), and O_i += P_i V accumulates in TMEM with P_i
 // as the TMEM-resident A operand.  The single MMA thread issues, per key tile j,
 //     PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
-// so each softmax warpgroup has the other tile's two MMAs to hide behind, and
-// because tcgen05.mma instructions from one thread complete in issue order,
-// observing S_i(j) also proves PV_i(j-1) has finished with P_i and O_i.
-// The running max m is only raised (and O_i rescaled in TMEM) when a row's max
-// grows by more than 2^8; the row sum and the output always use the same m,
-// so the result is exact up to rounding.  Each CTA emits a partial state
-// (O normalised, LSE in log2) per row; the merge kernel combines the splits with
-// the suffix states by GraniKV Eq. 1.
+// so each softmax warpgroup has the other tile's two MMA groups to hide behind.
+// tcgen05.mma instructions from one thread complete in issue order, so
+// observing S_i(j) also proves PV_i(j-1) has finished with P_i and O_i.  Tiles
+// of 128 keys keep every MMA at 64 tensor cycles or more: issuing one costs the
+// issuing thread about 50 cycles, so narrower tiles leave the tensor core
+// waiting on the issue loop.  The running max m is only raised (and O_i
+// rescaled in TMEM) when a row's max grows by more than 2^8; the row sum and
+// the output always use the same m, so the result is exact up to rounding.
+// Each CTA emits a partial state (O normalised, LSE in log2) per row; the merge
+// kernel combines the splits with the suffix states by GraniKV Eq. 1.
 //
-// Warp roles (320 threads): warp 0 issues TMA loads (K and V tiles, double
-// buffered), warp 1 owns tensor memory and issues every MMA from one thread,
+// Warp roles (320 threads): warp 0 issues TMA loads (K and V tiles, two
+// stages each), warp 1 owns tensor memory and issues every MMA from one thread,
 // warps 2-5 and 6-9 are the softmax warpgroups of Q tiles 0 and 1 (they also
 // stage Q and write the partial outputs).
 //
@@ -48,7 +50,8 @@ constexpr int BM = kPrefixTileM;   // 128 rows per Q tile
 constexpr int BN = kPrefixTileN;   // 128 keys per K/V tile
 constexpr int NST = 2;             // K and V pipeline depth
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kRegion = BM * 128;  // one [128 rows x 64 bf16] swizzled region = 16 KB
+constexpr uint32_t kRegionQ = BM * 128;   // [128 rows x 64 bf16] swizzled region
+constexpr uint32_t kRegionKV = BN * 128;  // [128 keys x 64 bf16] swizzled region
 constexpr int kThreads = 320;
 
 struct PrefixParams {
@@ -92,6 +95,7 @@ struct Layout {
   // slack to align the base to 1024; at least 120 KB so that one CTA (and one
   // 512-column tensor-memory allocation) is resident per SM
   static constexpr size_t kDynamic = kBytes + 1024 > 120 * 1024 ? kBytes + 1024 : 120 * 1024;
+  static_assert(2 * BM * (D * 4 + 16) + 2 * BM * 8 <= kBars, "epilogue staging must fit in the Q/K/V area");
 };
 
 // tcgen05 shared-memory matrix descriptor, 128-byte swizzle.
@@ -112,8 +116,7 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(id), "r"(accumulate)
-      : "memory");
+      "r"(a_tmem), "l"(b_desc), "r"(id), "r"(accumulate));
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int32_t* err, volatile int* abort_flag) {
@@ -152,6 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams 
   const int key0 = tile0 * BN;
   const int row0 = it.mblock * kPrefixRowsPerCta;
   const bool two = row0 + BM < gr.m;  // does Q tile 1 hold any row?
+  const void* tmK = p.tmaps + (size_t)gr.tmap_index * 128;
+  const void* tmV = p.tmaps + (size_t)(gr.tmap_index + 1) * 128;
+  const int zc = p.layer * p.Hkv + it.head;
 
   griddep_launch_dependents();
   // plan tables and the HOT pool are not written by the kernels of a decode
@@ -173,10 +179,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams 
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) qrow[c] = row_valid_ ? src[c] : make_uint4(0, 0, 0, 0);
   }
-  if (warp == 0 && lane == 0 && ntiles > 0) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(p.tmaps + (size_t)gr.tmap_index * 128) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(p.tmaps + (size_t)(gr.tmap_index + 1) * 128) : "memory");
-  }
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 256);
     for (int s = 0; s < NST; ++s) {
@@ -195,18 +197,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams 
     // the first K/V tiles need nothing but the barriers: start them now so their
     // latency overlaps the tensor-memory allocation and the Q staging
     if (ntiles > 0) {
-      const void* tmK = p.tmaps + (size_t)gr.tmap_index * 128;
-      const void* tmV = p.tmaps + (size_t)(gr.tmap_index + 1) * 128;
       tmap_acquire(tmK);
       tmap_acquire(tmV);
-      const int z = p.layer * p.Hkv + it.head;
       for (int j = 0; j < NST && j < ntiles; ++j) {
         mbar_arrive_expect_tx(bar(B_KFULL + j), Lay::kTile);
         for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(sK + j * Lay::kTile + h * kRegion, tmK, h * 64, key0 + j * BN, z, bar(B_KFULL + j));
+          tma_load_3d(sK + j * Lay::kTile + h * kRegionKV, tmK, h * 64, key0 + j * BN, zc, bar(B_KFULL + j));
         mbar_arrive_expect_tx(bar(B_VFULL + j), Lay::kTile);
         for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(sV + j * Lay::kTile + h * kRegion, tmV, h * 64, key0 + j * BN, z, bar(B_VFULL + j));
+          tma_load_3d(sV + j * Lay::kTile + h * kRegionKV, tmV, h * 64, key0 + j * BN, zc, bar(B_VFULL + j));
       }
     }
   }
@@ -218,28 +217,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // columns: S/P of tile 0 at 0, of tile 1 at 128; O of tile 0 at 256, of tile 1 at 384
-  auto tS = [&](int i) { return tmem + (uint32_t)i * BN; };
-  auto tO = [&](int i) { return tmem + 2u * BN + (uint32_t)i * 128u; };
+  // columns: S of Q tile i at i*128 (P is written over it); O of Q tile i at 256 + i*128
+  auto tS = [&](int i) { return tmem + (uint32_t)(i * 128); };
+  auto tO = [&](int i) { return tmem + 256u + (uint32_t)i * 128u; };
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
-    if (lane == 0 && ntiles > 0) {
-      const void* tmK = p.tmaps + (size_t)gr.tmap_index * 128;
-      const void* tmV = p.tmaps + (size_t)(gr.tmap_index + 1) * 128;
-      const int z = p.layer * p.Hkv + it.head;
-      int issued = 2 * min(NST, ntiles);
+    if (lane == 0 && ntiles > NST) {
+      int issued = 2 * NST;
       for (int j = NST; j < ntiles; ++j) {
         const int st = j % NST, r = j / NST;
-        if (r > 0 && !wait_or_abort(bar(B_KEMPTY + st), (r - 1) & 1, p.err, abort_flag)) break;
+        if (!wait_or_abort(bar(B_KEMPTY + st), (r - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(bar(B_KFULL + st), Lay::kTile);
         for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(sK + st * Lay::kTile + h * kRegion, tmK, h * 64, key0 + j * BN, z, bar(B_KFULL + st));
+          tma_load_3d(sK + st * Lay::kTile + h * kRegionKV, tmK, h * 64, key0 + j * BN, zc, bar(B_KFULL + st));
         issued = 2 * j + 1;
-        if (r > 0 && !wait_or_abort(bar(B_VEMPTY + st), (r - 1) & 1, p.err, abort_flag)) break;
+        if (!wait_or_abort(bar(B_VEMPTY + st), (r - 1) & 1, p.err, abort_flag)) break;
         mbar_arrive_expect_tx(bar(B_VFULL + st), Lay::kTile);
         for (int h = 0; h < D / 64; ++h)
-          tma_load_3d(sV + st * Lay::kTile + h * kRegion, tmV, h * 64, key0 + j * BN, z, bar(B_VFULL + st));
+          tma_load_3d(sV + st * Lay::kTile + h * kRegionKV, tmV, h * 64, key0 + j * BN, zc, bar(B_VFULL + st));
         issued = 2 * j + 2;
       }
       if (*abort_flag) {
@@ -256,48 +252,59 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams 
       constexpr uint32_t kIdQK = idesc(BN, false);
       constexpr uint32_t kIdPV = idesc(D, true);
       const int nq = two ? 2 : 1;
-      auto issue_s = [&](int i, int j) {
-        const int st = j % NST;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t a = sdesc(sQ + i * Lay::kQTile + (kk / 4) * kRegion + (kk % 4) * 32, 16, 1024);
-          const uint64_t b = sdesc(sK + st * Lay::kTile + (kk / 4) * kRegion + (kk % 4) * 32, 16, 1024);
-          tc_mma_ss(tS(i), a, b, kIdQK, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(B_SFULL + i));
-      };
-      auto issue_pv = [&](int i, int j) {
-        const int st = j % NST;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t b = sdesc(sV + st * Lay::kTile + kk * 2048, kRegion, 1024);
-          tc_mma_ts(tO(i), tS(i) + kk * 8, b, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-      };
-      bool ok = wait_or_abort(bar(B_QFULL), 0, p.err, abort_flag) &&
-                wait_or_abort(bar(B_KFULL), 0, p.err, abort_flag);
+      // Descriptors are built once; an operand at a byte offset is the base
+      // descriptor plus offset/16 in the start-address field.
+      const uint64_t dQ = sdesc(sQ, 16, 1024), dK = sdesc(sK, 16, 1024), dV = sdesc(sV, kRegionKV, 1024);
+      const uint32_t bar0 = base + Lay::kBars;
+      const uint32_t tS0 = tmem, tO0 = tmem + 256u;
+      bool ok = wait_or_abort(bar0 + 8u * B_QFULL, 0, p.err, abort_flag) &&
+                wait_or_abort(bar0 + 8u * B_KFULL, 0, p.err, abort_flag);
       if (ok) {
         tc_fence_after();
-        for (int i = 0; i < nq; ++i) issue_s(i, 0);
-        tc_commit(bar(B_KEMPTY));
+        for (int i = 0; i < nq; ++i) {
+          const uint64_t a0 = dQ + ((uint32_t)i * Lay::kQTile >> 4);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc_mma_ss(tS0 + (uint32_t)i * 128u, a0 + (((kk / 4) * kRegionQ + (kk % 4) * 32) >> 4),
+                      dK + (((kk / 4) * kRegionKV + (kk % 4) * 32) >> 4), kIdQK, kk > 0 ? 1u : 0u);
+          tc_commit(bar0 + 8u * (B_SFULL + i));
+        }
+        tc_commit(bar0 + 8u * B_KEMPTY);
       }
       for (int j = 0; ok && j < ntiles; ++j) {
         const int st = j % NST;
-        const bool more = j + 1 < ntiles;
-        if (!wait_or_abort(bar(B_VFULL + st), (j / NST) & 1, p.err, abort_flag)) { ok = false; break; }
-        if (more && !wait_or_abort(bar(B_KFULL + (j + 1) % NST), ((j + 1) / NST) & 1, p.err, abort_flag)) { ok = false; break; }
+        const int jn = j + 1;
+        const bool more = jn < ntiles;
+        const int stn = jn % NST;
+        if (!wait_or_abort(bar0 + 8u * (B_VFULL + st), (j / NST) & 1, p.err, abort_flag)) { ok = false; break; }
+        const uint64_t bv = dV + ((uint32_t)st * Lay::kTile >> 4);
+        const uint64_t bk = dK + ((uint32_t)stn * Lay::kTile >> 4);
         for (int i = 0; i < nq; ++i) {
-          if (!wait_or_abort(bar(B_PFULL + i), j & 1, p.err, abort_flag)) { ok = false; break; }
+          if (!wait_or_abort(bar0 + 8u * (B_PFULL + i), j & 1, p.err, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          issue_pv(i, j);          // reads P_i(j) from TMEM ...
-          if (more) issue_s(i, j + 1);   // ... before S_i(j+1) overwrites it (in-order completion)
+          // O_i += P_i(j) V_j with P_i(j) as the TMEM A operand ...
+          const uint32_t sbuf = tS0 + (uint32_t)i * 128u;
+          const uint32_t dO = tO0 + (uint32_t)i * 128u;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            tc_mma_ts(dO, sbuf + kk * 8, bv + ((kk * 2048) >> 4), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+          // ... then S_i(j+1) over it (in-order completion)
+          if (more) {
+            if (i == 0 && !wait_or_abort(bar0 + 8u * (B_KFULL + stn), (jn / NST) & 1, p.err, abort_flag)) { ok = false; break; }
+            const uint64_t a0 = dQ + ((uint32_t)i * Lay::kQTile >> 4);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc_mma_ss(sbuf, a0 + (((kk / 4) * kRegionQ + (kk % 4) * 32) >> 4),
+                        bk + (((kk / 4) * kRegionKV + (kk % 4) * 32) >> 4), kIdQK, kk > 0 ? 1u : 0u);
+            tc_commit(bar0 + 8u * (B_SFULL + i));
+          }
         }
         if (!ok) break;
-        tc_commit(bar(B_VEMPTY + st));
-        if (more) tc_commit(bar(B_KEMPTY + (j + 1) % NST));
+        tc_commit(bar0 + 8u * (B_VEMPTY + st));
+        if (more) tc_commit(bar0 + 8u * (B_KEMPTY + stn));
       }
       // every MMA issued above has finished before the epilogue reads O and TMEM is released
-      tc_commit(bar(B_OFINAL));
+      tc_commit(bar0 + 8u * B_OFINAL);
     }
   } else {
     // ---------------------- softmax / correction / epilogue ---------------------
@@ -312,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams 
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
         const int cc = c & 7;
-        sts128(qbase + (c >> 3) * kRegion + row * 128 + ((cc ^ (row & 7)) << 4), qrow[c]);
+        sts128(qbase + (c >> 3) * kRegionQ + row * 128 + ((cc ^ (row & 7)) << 4), qrow[c]);
       }
       fence_async_shared();
       mbar_arrive(bar(B_QFULL));
@@ -368,27 +375,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams 
       uint64_t sum4[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int c = 0; c < BN / 2; ++c) {
-        float xa, xb, a, b;
+        float xa, xb, a, b2;
         f2unpack(ffma2(f2pack(s[2 * c], s[2 * c + 1]), sc2, nm2), xa, xb);
         if ((c & 3) == 3) {
-          exp2_poly_pair(xa, xb, a, b);
+          exp2_poly_pair(xa, xb, a, b2);
         } else {
           a = ex2(xa);
-          b = ex2(xb);
+          b2 = ex2(xb);
         }
-        sum4[c & 3] = fadd2(sum4[c & 3], f2pack(a, b));
-        pk[c] = pack_bf16x2(a, b);
+        sum4[c & 3] = fadd2(sum4[c & 3], f2pack(a, b2));
+        pk[c] = pack_bf16x2(a, b2);
       }
       {
-        float s0, s1, s2, s3, s4, s5, s6, s7;
+        float s0, s1, s2, s3;
         f2unpack(fadd2(sum4[0], sum4[1]), s0, s1);
         f2unpack(fadd2(sum4[2], sum4[3]), s2, s3);
-        (void)s4; (void)s5; (void)s6; (void)s7;
         l += (s0 + s1) + (s2 + s3);
       }
       // P over S in TMEM (packed bf16 pairs, key 2c in the low half of column c)
-      tmem_st32(tS(qi) + lane_off, reinterpret_cast<const float*>(pk));
-      tmem_st32(tS(qi) + 32 + lane_off, reinterpret_cast<const float*>(pk + 32));
+#pragma unroll
+      for (int c = 0; c < BN / 64; ++c) tmem_st32(tS(qi) + c * 32 + lane_off, reinterpret_cast<const float*>(pk + c * 32));
       tc_wait_st();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + qi));
