@@ -113,8 +113,20 @@ class Clocks:
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(smax), "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _profile_traffic(kernel_tag, src_file):
-    """dram bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+# sources of each profiled kernel: a committed ncu summary counts only while they are unchanged
+LEVELS_SRC = ("cascade_split.cu", "prefix_body.cuh", "gather_body.cuh", "device_common.cuh")
+GATHER_SRC = ("gather_attn.cu", "gather_body.cuh", "device_common.cuh")
+
+
+def source_sha256(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_pool_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
+def _profile_traffic(kernel_tag, src_files):
+    """dram bytes per launch from the committed ncu summary, if the kernel sources are unchanged."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
     try:
         text = open(path).read()
@@ -124,8 +136,7 @@ def _profile_traffic(kernel_tag, src_file):
     h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     if not m or not h:
         return None
-    cur = hashlib.sha256(open(os.path.join(ROOT, "paged_kv_cache_pool_gb300", "csrc", src_file), "rb").read()).hexdigest()
-    return float(m.group(1)) if cur == h.group(1) else None
+    return float(m.group(1)) if source_sha256(src_files) == h.group(1) else None
 
 
 # ----------------------------------------------------------------------------------------------
@@ -249,6 +260,7 @@ def run_ours(a, w):
     forced = {"cascade": gk.GK_BACKEND_CASCADE, "dense": gk.GK_BACKEND_DENSE}.get(a.backend)
     launches = [0]
     dense_merge = [0]
+    split = [0]
     choices = []
     predicted = []
 
@@ -271,7 +283,9 @@ def run_ours(a, w):
             plan[0] = gk.gk_plan_build(pool, batch, stream)
         else:
             gk.gk_plan_update(pool, plan[0], batch, stream)
-        dense_merge[0] = gk.gk_plan_info(plan[0])["dense_merge"]
+        pinfo = gk.gk_plan_info(plan[0])
+        dense_merge[0] = pinfo["dense_merge"]
+        split[0] = pinfo["cascade_split"]
         choice, t_d, t_c = gk.gk_dispatch(pool, plan[0])
         predicted.append((t_d, t_c))
         if forced is not None:
@@ -287,19 +301,21 @@ def run_ours(a, w):
             if ev is not None:
                 ev[1].record(stream)
             if choice == gk.GK_BACKEND_CASCADE:
-                gk.gk_cascade_prefix(pool, stream, l, batch, plan[0])
+                # the probe layer runs gk_decode_cascade's two calls with an event between
                 if ev is not None:
+                    gk.gk_cascade_levels(pool, stream, l, batch, plan[0])
                     ev[2].record(stream)
-                gk.gk_cascade_suffix(pool, stream, l, batch, plan[0])
-                if ev is not None:
-                    ev[3].record(stream)
-                gk.gk_cascade_merge(pool, stream, l, batch, plan[0])
-                launches[0] += 3
+                    gk.gk_cascade_merge(pool, stream, l, batch, plan[0])
+                else:
+                    gk.gk_decode_cascade(pool, stream, l, batch, plan[0])
+                launches[0] += (1 if split[0] else 2) + 1
             else:
                 gk.gk_decode_dense(pool, stream, l, batch, plan[0])
+                if ev is not None:
+                    ev[2].record(stream)
                 launches[0] += 1 + dense_merge[0]
             if ev is not None:
-                ev[4].record(stream)
+                ev[3].record(stream)
 
     for _ in range(a.warmup):
         step()
@@ -315,7 +331,7 @@ def run_ours(a, w):
     # an event between two kernels stops the next one from launching early, so
     # the other layers run undisturbed.
     probe_layer = [i % L for i in range(a.steps)]
-    events = [{probe_layer[i]: [torch.cuda.Event(enable_timing=True) for _ in range(5)]} for i in range(a.steps)]
+    events = [{probe_layer[i]: [torch.cuda.Event(enable_timing=True) for _ in range(4)]} for i in range(a.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     vis_list = [x for x in vis.split(",") if x.strip()]
@@ -346,51 +362,47 @@ def run_ours(a, w):
     value = world * B * L * a.steps / (elapsed_ms / 1e3)
 
     # per-kernel averages over the timed region
-    k_ms = {"append": [], "prefix": [], "suffix": [], "merge": [], "dense": []}
+    k_ms = {"append": [], "levels": [], "merge": [], "dense": []}
     for i in range(a.steps):
         cas = step_choices[i] == gk.GK_BACKEND_CASCADE
         for l, e in events[i].items():
             k_ms["append"].append(e[0].elapsed_time(e[1]))
             if cas:
-                k_ms["prefix"].append(e[1].elapsed_time(e[2]))
-                k_ms["suffix"].append(e[2].elapsed_time(e[3]))
-                k_ms["merge"].append(e[3].elapsed_time(e[4]))
+                k_ms["levels"].append(e[1].elapsed_time(e[2]))
+                k_ms["merge"].append(e[2].elapsed_time(e[3]))
             else:
-                k_ms["dense"].append(e[1].elapsed_time(e[4]))
+                k_ms["dense"].append(e[1].elapsed_time(e[3]))
     avg = {k: (sum(v) / len(v) if v else None) for k, v in k_ms.items()}
     info = gk.gk_plan_info(plan[0])
     peaks, peak_src = _peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     s_tot = int(batch.suffix_len.sum())
-    # algorithmic bytes per launch
-    suffix_bytes = info["suffix_bytes"] + s_tot * 4 // P + B * Hq * d * 2 + info["num_partials"] * Hq * (d + 1) * 4
-    prefix_bytes = info["prefix_bytes"] + B * Hq * d * 2
+    # algorithmic bytes per launch (prefix K/V once per group, suffix K/V, slots, queries, partial states)
+    partial_bytes = info["num_partials"] * Hq * (d + 1) * 4
+    levels_bytes = (info["prefix_bytes"] + info["suffix_bytes"] + s_tot * 4 // P + B * Hq * d * 2 + partial_bytes)
     dense_bytes = info["dense_bytes"] + s_tot * 4 // P + B * Hq * d * 2 + B * Hq * (d + 1) * 4
     kernels = {}
-    if avg["suffix"]:
-        kernels["suffix_gather"] = {"ms": avg["suffix"], "bytes": suffix_bytes,
-                                    "gbs": suffix_bytes / (avg["suffix"] * 1e-3) / 1e9}
-    if avg["prefix"]:
-        kernels["cascade_prefix"] = {"ms": avg["prefix"], "bytes": prefix_bytes, "flops": info["prefix_flops"],
-                                     "gbs": prefix_bytes / (avg["prefix"] * 1e-3) / 1e9,
-                                     "tflops": info["prefix_flops"] / (avg["prefix"] * 1e-3) / 1e12}
+    if avg["levels"]:
+        kernels["cascade_levels"] = {"ms": avg["levels"], "bytes": levels_bytes, "flops": info["prefix_flops"],
+                                     "gbs": levels_bytes / (avg["levels"] * 1e-3) / 1e9,
+                                     "tflops": info["prefix_flops"] / (avg["levels"] * 1e-3) / 1e12,
+                                     "arrangement": "split" if info["cascade_split"] else "sequential"}
     if avg["merge"]:
         kernels["lse_merge"] = {"ms": avg["merge"]}
     if avg["dense"]:
         kernels["dense_gather"] = {"ms": avg["dense"], "bytes": dense_bytes,
                                    "gbs": dense_bytes / (avg["dense"] * 1e-3) / 1e9}
     kernels["append_kv"] = {"ms": avg["append"]}
-    # dominant kernel -> roofline
+    # dominant kernel -> roofline (the cascade's two levels are one launch in a split plan)
     dom = max(((k, v["ms"]) for k, v in kernels.items() if "bytes" in v), key=lambda x: x[1])[0]
     kd = kernels[dom]
-    if dom == "cascade_prefix" and kd["flops"] / kd["bytes"] > tc_peak * 1e3 / hbm:
+    if dom == "cascade_levels" and kd["flops"] / kd["bytes"] > tc_peak * 1e3 / hbm:
         roof = {"kernel": dom, "bound": "tensor", "achieved": kd["tflops"], "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": kd["tflops"] / tc_peak, "traffic": _profile_traffic("cascade_prefix_llama8b_lp16384_b64", "prefix_tc.cu")}
+                "frac": kd["tflops"] / tc_peak, "traffic": _profile_traffic("cascade_levels_llama8b_lp16384_b64", LEVELS_SRC)}
     else:
-        tag = {"suffix_gather": ("suffix_gather_llama8b_lp16384_b64", "gather_attn.cu"),
-               "dense_gather": ("dense_gather_llama8b_lp16384_b64", "gather_attn.cu"),
-               "cascade_prefix": ("cascade_prefix_llama8b_lp16384_b64", "prefix_tc.cu")}[dom]
+        tag = {"cascade_levels": ("cascade_levels_llama8b_lp16384_b64", LEVELS_SRC),
+               "dense_gather": ("dense_gather_llama8b_lp16384_b64", GATHER_SRC)}[dom]
         roof = {"kernel": dom, "bound": "hbm", "achieved": kd["gbs"], "peak": hbm, "unit": "GB/s",
                 "frac": kd["gbs"] / hbm, "traffic": _profile_traffic(*tag)}
     roof["peak_source"] = f"{peak_src} ({'bf16_tflops_sustained' if roof['bound'] == 'tensor' else 'hbm_gbs'})"

@@ -171,6 +171,10 @@ typedef struct gk_plan_summary {
   int64_t prefix_flops;           /* 4 * B_g * Hq * Lp * d summed over groups */
   int64_t suffix_bytes;           /* COLD K+V of all suffixes */
   int64_t dense_bytes;            /* K+V of every request's whole context */
+  int32_t cascade_split;          /* 1: gk_decode_cascade runs the prefix items (prefix_ctas SMs) and
+                                     the suffix gather (suffix_ctas SMs) side by side in one launch;
+                                     0: one after the other, each over every SM */
+  int32_t prefix_tiles_per_item;  /* 128-key tiles of the longest prefix work item */
 } gk_plan_summary;
 
 /* Plan one decode step: group requests by HOT prefix (stable, first appearance),
@@ -198,7 +202,10 @@ gk_status gk_decode_dense(gk_pool* pool, void* stream, int32_t layer, const gk_b
  * prefix are stacked into one QK^T / PV contraction on the tensor cores, read
  * once from HOT (GraniKV Section 2.3, shared-prefix matmul; Section 3.5);
  * (b) the suffix is gathered through the block table; (c) the partial states
- * are merged by log-sum-exp (GraniKV Eq. 1). */
+ * are merged by log-sum-exp (GraniKV Eq. 1).  A split plan
+ * (gk_plan_summary.cascade_split) runs (a) and (b) in one launch on disjoint
+ * SMs, then (c); otherwise (a), (b), (c) are three launches.  Both give the
+ * same bits as the three stage calls below. */
 gk_status gk_decode_cascade(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch,
                             const gk_plan* plan);
 /* Allocation-free dense decode.  No counterpart in the paper: it exists for
@@ -220,10 +227,15 @@ gk_status gk_decode_cascade(gk_pool* pool, void* stream, int32_t layer, const gk
  *  - The pool must already have done device work (any KV write), which is when
  *    its error word is created; otherwise GK_ERR_INVALID. */
 gk_status gk_decode_dense_static(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch);
+/* Stages (a) and (b) of gk_decode_cascade as the plan arranges them: one split
+ * launch, or the prefix then the suffix kernel.  gk_decode_cascade is exactly
+ * this followed by gk_cascade_merge. */
+gk_status gk_cascade_levels(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch,
+                            const gk_plan* plan);
 /* The three stages of gk_decode_cascade, for callers that time them or run
  * (a) and (b) on two streams: the prefix and suffix stages write disjoint
- * partial states, and the merge must follow both.  gk_decode_cascade is
- * exactly prefix, suffix, merge on one stream. */
+ * partial states, and the merge must follow both.  They run the plan's work
+ * lists (for a split plan: prefix_ctas long items, suffix_ctas gather CTAs). */
 gk_status gk_cascade_prefix(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch,
                             const gk_plan* plan);
 gk_status gk_cascade_suffix(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch,
@@ -240,6 +252,9 @@ typedef struct gk_cost_model {
   double bw_prefix_gbs;           /* prefix-kernel HOT read bandwidth */
   double bw_suffix_gbs;           /* suffix gather bandwidth */
   double c_merge_us;              /* merge cost per (request, query head) */
+  double prefix_tile_us;          /* split cascade: one 128-key tile of a prefix work item on one SM */
+  double prefix_item_us;          /* split cascade: fixed cost of one prefix work item */
+  double gather_sm_gbs;           /* split cascade: suffix gather bandwidth one SM sustains */
   int32_t n_tc_points;            /* 1..16 */
   int32_t reserved0;
   double tc_m[16];                /* M_eff of each calibration point, increasing */
@@ -248,17 +263,40 @@ typedef struct gk_cost_model {
 
 /* Predict both backends for the plan and pick the smaller:
  *   T_dense   = c_flat + dense_bytes / bw_flat
- *   T_cascade = c_cascade + sum_g max(prefix_bytes_g / bw_prefix, prefix_flops_g / TC(M_eff_g))
- *               + suffix_bytes / bw_suffix + c_merge * B * Hq
+ *   T_cascade = c_cascade + T_levels + c_merge * B * Hq, where for a sequential plan
+ *     T_levels = sum_g max(prefix_bytes_g / bw_prefix, prefix_flops_g / TC(M_eff_g))
+ *                + suffix_bytes / bw_suffix
+ *   and for a split plan (prefix items and suffix gather side by side, see
+ *   gk_plan_summary.cascade_split), with C key tiles per item and n_gather SMs,
+ *     T_levels = max(C * prefix_tile_us + prefix_item_us,
+ *                    suffix_bytes / min(bw_suffix, n_gather * gather_sm))
  * TC is piecewise linear through the points (proportional below the first,
  * flat above the last).  Dense is chosen only when strictly faster.  Host only. */
 gk_status gk_dispatch(const gk_pool* pool, const gk_plan* plan, gk_backend* choice, double* t_dense_us,
                       double* t_cascade_us);
 gk_status gk_cost_model_set(gk_pool* pool, const gk_cost_model* cm);
+
+/* Cascade arrangement of the plans the pool builds from now on.
+ *  GK_CASCADE_AUTO (default): split when the cost model predicts it faster.
+ *  GK_CASCADE_SEQUENTIAL: prefix items over every SM, then the suffix gather.
+ *  GK_CASCADE_SPLIT: prefix items beside the suffix gather in one launch, with
+ *    tiles_per_item 128-key tiles per item (0: the cost model's best split).
+ *    A step without prefix or suffix work, or whose items would leave no SM
+ *    for the gather, is planned sequentially.
+ * The choice changes the work lists and the partial states, not the
+ * attention computed.  Host only.  GK_ERR_INVALID for an unknown mode or a
+ * negative tiles_per_item. */
+typedef enum gk_cascade_mode {
+  GK_CASCADE_AUTO = 0,
+  GK_CASCADE_SEQUENTIAL = 1,
+  GK_CASCADE_SPLIT = 2
+} gk_cascade_mode;
+gk_status gk_pool_set_cascade_mode(gk_pool* pool, gk_cascade_mode mode, int32_t tiles_per_item);
 gk_status gk_cost_model_get(const gk_pool* pool, gk_cost_model* cm);
 /* Same as gk_cost_model_set from JSON text: {"c_flat_us": .., "bw_flat_gbs": ..,
  * "c_cascade_us": .., "bw_prefix_gbs": .., "bw_suffix_gbs": .., "c_merge_us": ..,
- * "tc_points": [[M, TFLOP/s], ...]}. */
+ * "prefix_tile_us": .., "prefix_item_us": .., "gather_sm_gbs": ..,
+ * "tc_points": [[M, TFLOP/s], ...]}.  Keys left out keep their current values. */
 gk_status gk_cost_model_load(gk_pool* pool, const char* json);
 
 /* ---- device error word -------------------------------------------------------- */

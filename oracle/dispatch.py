@@ -8,10 +8,23 @@ measured cost model evaluated on the step's plan; the backend with the smaller
 predicted time runs (flat wins only when strictly faster):
 
   T_flat    = c_flat + bytes_flat / bw_flat
-  T_cascade = c_cascade + sum_g max(bytes_pre_g / bw_prefix, flops_pre_g / TC(M_eff_g))
-              + bytes_suffix / bw_suffix + c_merge * B * Hq
+  T_cascade = c_cascade + T_levels + c_merge * B * Hq
+  T_levels  = sum_g max(bytes_pre_g / bw_prefix, flops_pre_g / TC(M_eff_g))
+              + bytes_suffix / bw_suffix                         (sequential plan)
+            = max(C * prefix_tile + prefix_item,
+                  bytes_suffix / min(bw_suffix, n_gather * gather_sm))   (split plan)
   TC(M)     = piecewise-linear through the calibrated (M, TFLOP/s) points,
               proportional to M below the first point, flat above the last.
+
+A split plan runs the prefix contraction on n_pre SMs (one work item of C
+128-key tiles each; a group contributes ceil(M/256) row blocks x Hkv heads x
+ceil(ceil(Lp/128)/C) items) beside the suffix gather on the n_gather SMs left.
+The planner takes the C with the smallest split prediction (the largest C among
+equal ones, i.e. the fewest items), among those that leave an SM for the
+gather, then lowers C to the smallest value giving as many items (balanced
+items), and splits when that beats the sequential T_levels.  The gather partition cuts the suffix tokens
+into quotas of ceil(total/n) rounded up to 64 and then to a multiple of 16, so
+it may use fewer CTAs than it was given.
 
 Times are in microseconds, bandwidths in GB/s (1 GB/s = 1e3 bytes per us),
 tensor throughput in TFLOP/s (1e6 flop per us).
@@ -48,24 +61,68 @@ def features(prefix_lens, suffix_lens, group_of, Hq, Hkv, d):
     for grp, members in groups.items():
         lp = prefix_lens[members[0]]
         pre.append(dict(M=m_eff(len(members), g), bytes=lp * kv_tok,
-                        flops=4 * len(members) * Hq * lp * d))
+                        flops=4 * len(members) * Hq * lp * d, lp=lp))
     return dict(
         bytes_flat=sum(p + s for p, s in zip(prefix_lens, suffix_lens)) * kv_tok,
         bytes_suffix=sum(suffix_lens) * kv_tok,
-        prefix=pre, B=len(group_of), Hq=Hq)
+        prefix=pre, B=len(group_of), Hq=Hq, Hkv=Hkv, suffix_tokens=sum(suffix_lens))
 
 
-def predict(cm, f):
-    t_flat = cm["c_flat_us"] + f["bytes_flat"] / (cm["bw_flat_gbs"] * 1e3)
-    t_pre = 0.0
+def gather_ctas(tokens, n):
+    """CTAs the gather partition of `tokens` over at most n CTAs uses."""
+    if tokens == 0:
+        return 0
+    quota = max(-(-tokens // n), 64)
+    quota = -(-quota // 16) * 16
+    return -(-tokens // quota)
+
+
+def sequential_levels(cm, f):
+    t = f["bytes_suffix"] / (cm["bw_suffix_gbs"] * 1e3)
     for p in f["prefix"]:
-        t_pre += max(p["bytes"] / (cm["bw_prefix_gbs"] * 1e3),
-                     p["flops"] / (tc_at(cm["tc_points"], p["M"]) * 1e6))
-    t_cas = (cm["c_cascade_us"] + t_pre + f["bytes_suffix"] / (cm["bw_suffix_gbs"] * 1e3)
-             + cm["c_merge_us"] * f["B"] * f["Hq"])
+        t += max(p["bytes"] / (cm["bw_prefix_gbs"] * 1e3), p["flops"] / (tc_at(cm["tc_points"], p["M"]) * 1e6))
+    return t
+
+
+def split_levels(cm, f, C, n_gather):
+    bw = min(cm["bw_suffix_gbs"], n_gather * cm["gather_sm_gbs"])
+    return max(C * cm["prefix_tile_us"] + cm["prefix_item_us"], f["bytes_suffix"] / (bw * 1e3))
+
+
+def arrangement(cm, f, num_sms):
+    """-> dict(split, C, n_pre, n_gather): the planner's choice for the step."""
+    pre = f["prefix"]
+    ntiles = [-(-p["lp"] // 128) for p in pre]
+    mtiles = [-(-p["M"] // 256) for p in pre]
+    seq = dict(split=False, C=None, n_pre=None, n_gather=gather_ctas(f["suffix_tokens"], num_sms))
+    if not pre or f["suffix_tokens"] == 0:
+        return seq
+    best, best_c = None, None
+    for C in range(max(ntiles), 0, -1):
+        items = sum(m * f["Hkv"] * -(-n // C) for m, n in zip(mtiles, ntiles))
+        if items > num_sms - 1:
+            break
+        bw = min(cm["bw_suffix_gbs"], (num_sms - items) * cm["gather_sm_gbs"])
+        t = max(C * cm["prefix_tile_us"] + cm["prefix_item_us"], f["bytes_suffix"] / (bw * 1e3))
+        if best is None or t < best - 1e-9:
+            best, best_c = t, C
+    if best is None or not best < sequential_levels(cm, f):
+        return seq
+    n_pre = sum(m * f["Hkv"] * -(-n // best_c) for m, n in zip(mtiles, ntiles))
+    while best_c > 1 and sum(m * f["Hkv"] * -(-n // (best_c - 1)) for m, n in zip(mtiles, ntiles)) == n_pre:
+        best_c -= 1
+    return dict(split=True, C=min(best_c, max(ntiles)), n_pre=n_pre,
+                n_gather=gather_ctas(f["suffix_tokens"], num_sms - n_pre))
+
+
+def predict(cm, f, num_sms=152):
+    t_flat = cm["c_flat_us"] + f["bytes_flat"] / (cm["bw_flat_gbs"] * 1e3)
+    a = arrangement(cm, f, num_sms)
+    t_levels = split_levels(cm, f, a["C"], a["n_gather"]) if a["split"] else sequential_levels(cm, f)
+    t_cas = cm["c_cascade_us"] + t_levels + cm["c_merge_us"] * f["B"] * f["Hq"]
     return t_flat, t_cas
 
 
-def choose(cm, f):
-    t_flat, t_cas = predict(cm, f)
+def choose(cm, f, num_sms=152):
+    t_flat, t_cas = predict(cm, f, num_sms)
     return ("dense" if t_flat < t_cas else "cascade"), t_flat, t_cas

@@ -51,12 +51,14 @@ class gk_batch(ctypes.Structure):
 class gk_plan_summary(ctypes.Structure):
     _fields_ = [("num_requests", c_i32), ("num_groups", c_i32), ("max_m_eff", c_i32), ("prefix_ctas", c_i32),
                 ("suffix_ctas", c_i32), ("dense_ctas", c_i32), ("num_partials", c_i32), ("dense_merge", c_i32),
-                ("prefix_bytes", c_i64), ("prefix_flops", c_i64), ("suffix_bytes", c_i64), ("dense_bytes", c_i64)]
+                ("prefix_bytes", c_i64), ("prefix_flops", c_i64), ("suffix_bytes", c_i64), ("dense_bytes", c_i64),
+                ("cascade_split", c_i32), ("prefix_tiles_per_item", c_i32)]
 
 
 class gk_cost_model(ctypes.Structure):
     _fields_ = [("c_flat_us", c_dbl), ("bw_flat_gbs", c_dbl), ("c_cascade_us", c_dbl), ("bw_prefix_gbs", c_dbl),
-                ("bw_suffix_gbs", c_dbl), ("c_merge_us", c_dbl), ("n_tc_points", c_i32), ("reserved0", c_i32),
+                ("bw_suffix_gbs", c_dbl), ("c_merge_us", c_dbl), ("prefix_tile_us", c_dbl), ("prefix_item_us", c_dbl),
+                ("gather_sm_gbs", c_dbl), ("n_tc_points", c_i32), ("reserved0", c_i32),
                 ("tc_m", c_dbl * 16), ("tc_tflops", c_dbl * 16)]
 
 
@@ -86,6 +88,7 @@ _SIGS = {
     "gk_decode_dense": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch), c_vp]),
     "gk_decode_cascade": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch), c_vp]),
     "gk_decode_dense_static": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch)]),
+    "gk_cascade_levels": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch), c_vp]),
     "gk_cascade_prefix": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch), c_vp]),
     "gk_cascade_suffix": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch), c_vp]),
     "gk_cascade_merge": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch), c_vp]),
@@ -93,6 +96,7 @@ _SIGS = {
     "gk_cost_model_set": (c_i32, [c_vp, P(gk_cost_model)]),
     "gk_cost_model_get": (c_i32, [c_vp, P(gk_cost_model)]),
     "gk_cost_model_load": (c_i32, [c_vp, ctypes.c_char_p]),
+    "gk_pool_set_cascade_mode": (c_i32, [c_vp, c_i32, c_i32]),
     "gk_device_error": (c_i32, [c_vp, c_vp, P(c_i32)]),
 }
 
@@ -325,6 +329,10 @@ def gk_decode_dense_static(pool, stream, layer, batch):
     _check(lib().gk_decode_dense_static(pool, _stream(stream), layer, ctypes.byref(batch.c)), pool)
 
 
+def gk_cascade_levels(pool, stream, layer, batch, plan):
+    _check(lib().gk_cascade_levels(pool, _stream(stream), layer, ctypes.byref(batch.c), plan), pool)
+
+
 def gk_cascade_prefix(pool, stream, layer, batch, plan):
     _check(lib().gk_cascade_prefix(pool, _stream(stream), layer, ctypes.byref(batch.c), plan), pool)
 
@@ -348,14 +356,18 @@ def gk_cost_model_get(pool):
     cm = gk_cost_model()
     _check(lib().gk_cost_model_get(pool, ctypes.byref(cm)), pool)
     n = cm.n_tc_points
-    return dict(c_flat_us=cm.c_flat_us, bw_flat_gbs=cm.bw_flat_gbs, c_cascade_us=cm.c_cascade_us,
-                bw_prefix_gbs=cm.bw_prefix_gbs, bw_suffix_gbs=cm.bw_suffix_gbs, c_merge_us=cm.c_merge_us,
-                tc_points=[[cm.tc_m[i], cm.tc_tflops[i]] for i in range(n)])
+    d = {k: getattr(cm, k) for k in COST_MODEL_KEYS}
+    d["tc_points"] = [[cm.tc_m[i], cm.tc_tflops[i]] for i in range(n)]
+    return d
+
+
+COST_MODEL_KEYS = ("c_flat_us", "bw_flat_gbs", "c_cascade_us", "bw_prefix_gbs", "bw_suffix_gbs", "c_merge_us",
+                   "prefix_tile_us", "prefix_item_us", "gather_sm_gbs")
 
 
 def gk_cost_model_set(pool, cm: dict):
     c = gk_cost_model()
-    for k in ("c_flat_us", "bw_flat_gbs", "c_cascade_us", "bw_prefix_gbs", "bw_suffix_gbs", "c_merge_us"):
+    for k in COST_MODEL_KEYS:
         setattr(c, k, float(cm[k]))
     pts = cm["tc_points"]
     c.n_tc_points = len(pts)
@@ -363,6 +375,13 @@ def gk_cost_model_set(pool, cm: dict):
         c.tc_m[i] = m
         c.tc_tflops[i] = t
     _check(lib().gk_cost_model_set(pool, ctypes.byref(c)), pool)
+
+
+GK_CASCADE_AUTO, GK_CASCADE_SEQUENTIAL, GK_CASCADE_SPLIT = 0, 1, 2
+
+
+def gk_pool_set_cascade_mode(pool, mode, tiles_per_item=0):
+    _check(lib().gk_pool_set_cascade_mode(pool, int(mode), int(tiles_per_item)), pool)
 
 
 def gk_cost_model_load(pool, json_text: str):

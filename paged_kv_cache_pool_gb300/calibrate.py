@@ -2,11 +2,13 @@
 routing rule stays, its numbers are re-fit per GPU; Appendix B.4b's sweep).
 
 Times, with CUDA events, on one layer of synthetic pools (random bf16 data):
-  * the flat backend over several (B, Lp, s)           -> c_flat_us, bw_flat_gbs
-  * the suffix gather over several suffix volumes        -> bw_suffix_gbs
-  * the prefix kernel at M_eff = B * g from 32 to 2048   -> tc_points (achieved TFLOP/s)
-  * the merge                                            -> c_merge_us per (request, head)
-  * the whole cascade                                    -> c_cascade_us (mean residual)
+  * the flat backend over several (B, Lp, s)              -> c_flat_us, bw_flat_gbs
+  * the suffix gather over every SM, several volumes        -> bw_suffix_gbs
+  * the prefix kernel at M_eff = B * g from 32 to 2048      -> tc_points (achieved TFLOP/s)
+  * split plans forced to C key tiles per item: the prefix  -> prefix_item_us + C * prefix_tile_us
+    items alone, and the gather alone on the SMs left       -> gather_sm_gbs
+  * the merge                                               -> c_merge_us per (request, head)
+  * the whole cascade                                       -> c_cascade_us (mean residual)
 and writes the JSON that gk_cost_model_load reads.
 
     python -m paged_kv_cache_pool_gb300.calibrate --out cost_model_gb300.json
@@ -39,7 +41,7 @@ def _time(fn, reps=10, warm=3):
 class _Case:
     """One layer of a pool with B requests sharing a prefix of Lp and suffixes of s tokens."""
 
-    def __init__(self, eng, B, lp, s, Hq, d):
+    def __init__(self, eng, B, lp, s, Hq, d, mode=gk.GK_CASCADE_SEQUENTIAL, tiles=0):
         import torch
         self.eng = eng
         base = eng.prefix_alloc(lp)
@@ -56,7 +58,9 @@ class _Case:
         self.out = torch.empty((B, Hq, d), device=eng.device)
         self.lse = torch.empty((B, Hq), device=eng.device)
         self.batch.set_device(d_q=self.q, d_out=self.out, d_lse=self.lse)
+        gk.gk_pool_set_cascade_mode(eng.pool, mode, tiles)
         self.plan = gk.gk_plan_build(eng.pool, self.batch)
+        gk.gk_pool_set_cascade_mode(eng.pool, gk.GK_CASCADE_AUTO)
         self.info = gk.gk_plan_info(self.plan)
 
     def close(self):
@@ -80,18 +84,18 @@ def calibrate(Hq=32, Hkv=8, d=128, device="cuda"):
     kv_tok = 2 * Hkv * d * 2
 
     flat_pts, suf_pts, cas_pts, merge_pts = [], [], [], []
-    tc_points = []
+    tc_points, tile_pts, sm_pts = [], [], []
+    kv_tok = 2 * Hkv * d * 2
     for B, lp, s in [(8, 2048, 256), (32, 4096, 512), (64, 16384, 1024), (128, 8192, 512), (256, 4096, 1024)]:
         c = _Case(eng, B, lp, s, Hq, d)
         t_flat = _time(lambda: gk.gk_decode_dense(pool, None, 0, c.batch, c.plan))
-        t_pre = _time(lambda: gk.gk_cascade_prefix(pool, None, 0, c.batch, c.plan))
         t_suf = _time(lambda: gk.gk_cascade_suffix(pool, None, 0, c.batch, c.plan))
         t_mrg = _time(lambda: gk.gk_cascade_merge(pool, None, 0, c.batch, c.plan))
         t_cas = _time(lambda: gk.gk_decode_cascade(pool, None, 0, c.batch, c.plan))
         flat_pts.append((c.info["dense_bytes"], t_flat))
         suf_pts.append((c.info["suffix_bytes"], t_suf))
         merge_pts.append((B * Hq, t_mrg))
-        cas_pts.append((c.info, t_cas, B))
+        cas_pts.append((dict(c.info), t_cas, B))
         c.close()
     # prefix throughput against M_eff at a fixed long prefix
     for B in (8, 16, 32, 64, 128, 256, 512):
@@ -99,14 +103,26 @@ def calibrate(Hq=32, Hkv=8, d=128, device="cuda"):
         t_pre = _time(lambda: gk.gk_cascade_prefix(pool, None, 0, c.batch, c.plan))
         tc_points.append([float(B * g), c.info["prefix_flops"] / (t_pre * 1e-6) / 1e12])
         c.close()
+    # split plans: prefix items of C tiles alone, and the gather alone on the SMs left
+    for C in (16, 32, 64, 128):
+        c = _Case(eng, 64, 16384, 1024, Hq, d, gk.GK_CASCADE_SPLIT, C)
+        if c.info["cascade_split"]:
+            t_pre = _time(lambda: gk.gk_cascade_prefix(pool, None, 0, c.batch, c.plan))
+            t_suf = _time(lambda: gk.gk_cascade_suffix(pool, None, 0, c.batch, c.plan))
+            t_cas = _time(lambda: gk.gk_decode_cascade(pool, None, 0, c.batch, c.plan))
+            tile_pts.append((c.info["prefix_tiles_per_item"], t_pre))
+            sm_pts.append((c.info["suffix_ctas"], c.info["suffix_bytes"] / (t_suf * 1e3)))
+            cas_pts.append((dict(c.info), t_cas, 64))
+        c.close()
     eng.close()
     torch.cuda.synchronize()
 
-    return refit(dict(flat=flat_pts, suffix=suf_pts, merge=merge_pts,
+    return refit(dict(flat=flat_pts, suffix=suf_pts, merge=merge_pts, tile=tile_pts, gather_sm=sm_pts,
                       cascade=[(i["max_m_eff"], t) for i, t, _ in cas_pts],
                       cascade_info=[dict(max_m_eff=i["max_m_eff"], prefix_bytes=i["prefix_bytes"],
                                          prefix_flops=i["prefix_flops"], suffix_bytes=i["suffix_bytes"], B=B,
-                                         Hq=Hq) for i, _, B in cas_pts],
+                                         Hq=Hq, split=i["cascade_split"], tiles=i["prefix_tiles_per_item"],
+                                         suffix_ctas=i["suffix_ctas"]) for i, _, B in cas_pts],
                       tc_points=tc_points))
 
 
@@ -126,16 +142,27 @@ def refit(measured):
     tc_points = sorted([list(p) for p in measured["tc_points"]])
     cm = dict(c_flat_us=c_flat, bw_flat_gbs=1.0 / max(s_flat, 1e-12) / 1e3, c_cascade_us=0.0,
               bw_prefix_gbs=6000.0, bw_suffix_gbs=1.0 / max(s_suf, 1e-12) / 1e3, c_merge_us=max(s_mrg, 0.0),
-              tc_points=tc_points)
+              prefix_tile_us=1.65, prefix_item_us=10.5, gather_sm_gbs=44.0, tc_points=tc_points)
+    if len(measured.get("tile", [])) >= 2:
+        item, tile = _linfit(measured["tile"])
+        cm["prefix_tile_us"], cm["prefix_item_us"] = max(tile, 1e-3), item
+    # per-SM gather bandwidth: points whose SMs stay well below the all-SM bandwidth
+    per_sm = [bw / n for n, bw in measured.get("gather_sm", []) if n * 50.0 < cm["bw_suffix_gbs"]]
+    if per_sm:
+        cm["gather_sm_gbs"] = float(np.median(per_sm))
     # the cascade's fixed cost: the suffix and merge launches' intercepts, plus the mean
     # residual of the whole cascade over that model when it is positive
     base = c_suf + c_mrg
     res = []
     for info, (_, t_cas) in zip(measured["cascade_info"], measured["cascade"]):
-        tc = float(np.interp(info["max_m_eff"], [p[0] for p in tc_points], [p[1] for p in tc_points]))
-        t_pre = max(info["prefix_bytes"] / (cm["bw_prefix_gbs"] * 1e3), info["prefix_flops"] / (tc * 1e6))
-        model = base + t_pre + info["suffix_bytes"] / (cm["bw_suffix_gbs"] * 1e3) + cm["c_merge_us"] * info["B"] * info["Hq"]
-        res.append(t_cas - model)
+        if info.get("split"):
+            bw = min(cm["bw_suffix_gbs"], info["suffix_ctas"] * cm["gather_sm_gbs"])
+            levels = max(info["tiles"] * cm["prefix_tile_us"] + cm["prefix_item_us"], info["suffix_bytes"] / (bw * 1e3))
+        else:
+            tc = float(np.interp(info["max_m_eff"], [p[0] for p in tc_points], [p[1] for p in tc_points]))
+            levels = (max(info["prefix_bytes"] / (cm["bw_prefix_gbs"] * 1e3), info["prefix_flops"] / (tc * 1e6))
+                      + info["suffix_bytes"] / (cm["bw_suffix_gbs"] * 1e3))
+        res.append(t_cas - (base + levels + cm["c_merge_us"] * info["B"] * info["Hq"]))
     cm["c_cascade_us"] = base + max(0.0, float(np.mean(res)))
     cm["measured"] = measured
     return cm

@@ -1,0 +1,118 @@
+// Split cascade launch: the prefix contraction and the suffix gather of one
+// layer (GraniKV Section 3.3, the two levels of the cascade) side by side in
+// one launch, on disjoint sets of SMs.
+//
+// The prefix level is a dense contraction on the tensor cores that reads each
+// prefix K/V tile once; the suffix level is a gather bound by HBM.  Run one
+// after the other, every SM first waits on tensor-core work with HBM half
+// idle, then streams with the tensor cores idle.  Here CTA b < n_pre runs
+// prefix work item b (one CTA per SM, so the plan makes the items long: few
+// key splits), and every other CTA runs a slot of the suffix partition, so the
+// tensor-core items and the HBM stream overlap for the whole launch.  The
+// plan picks n_pre so that both sides are predicted to finish together.  Both
+// sides write partial states; the merge (GraniKV Eq. 1) follows as its own
+// launch.
+#include "gather_body.cuh"
+#include "prefix_body.cuh"
+
+namespace gk {
+namespace {
+
+struct SplitParams {
+  prefix::PrefixParams pp;
+  gather::GatherParams gp;
+  int32_t n_pre;        // CTAs [0, n_pre) run prefix item b
+  int32_t n_gather;     // CTAs [n_pre, n_pre + n_gather) run suffix slot b - n_pre
+  uint32_t data_bytes;  // shared data area: max of the prefix and gather layouts
+};
+
+constexpr uint32_t kSplitCtlBytes = prefix::kCtlBytes;
+static_assert(1024 + kSplitCtlBytes <= gather::kSoleCtaReserve, "control area exceeds the gather reserve");
+
+template <int D>
+size_t split_data_bytes(int hkv) {
+  const size_t g = gather::gather_data_bytes(hkv, D, gather::single_cta_stages(hkv, D));
+  return g > prefix::Layout<D>::kData ? g : prefix::Layout<D>::kData;
+}
+
+// the block serves both roles: the prefix body's warps and the gather's
+constexpr int kSplitThreads = prefix::kThreads > gather::kGatherThreads ? prefix::kThreads : gather::kGatherThreads;
+static_assert(32 * kMaxKvHeads <= kSplitThreads, "a gather CTA needs a warp per KV head");
+
+template <int D, int G>
+__global__ void __launch_bounds__(kSplitThreads, 1) cascade_split_kernel(const SplitParams f) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t ctl = base + f.data_bytes;
+  uint8_t* ctl_ptr = smem_raw + (ctl - raw);
+  const int b = blockIdx.x;
+
+  griddep_launch_dependents();
+  if (b < f.n_pre) {
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl_ptr + prefix::kCtlTmemSlot);
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) *reinterpret_cast<volatile int*>(ctl_ptr + prefix::kCtlFlag) = 0;
+    if (warp == 1) {
+      tmem_alloc(ctl + prefix::kCtlTmemSlot, prefix::kTmemCols);
+      tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    griddep_wait();
+    prefix::prefix_item<D>(f.pp, f.pp.items[b], base, ctl, ctl_ptr, tmem);
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem, prefix::kTmemCols);
+    }
+  } else if (b - f.n_pre < f.n_gather) {
+    gather::gather_segments<D, G, false>(f.gp, base, b - f.n_pre);
+  }
+}
+
+template <int D, int G>
+int launch_split_t(const SplitParams& fp, int ctas, cudaStream_t st) {
+  const size_t smem = 1024 + fp.data_bytes + kSplitCtlBytes;
+  auto kern = cascade_split_kernel<D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return (int)e;
+  return (int)launch_pdl(kern, dim3(ctas), dim3(kSplitThreads), smem, st, fp);
+}
+
+}  // namespace
+
+int launch_cascade_split(const LaunchCommon& lc, void* stream, int32_t layer, const gk_batch* b, const Plan* pl) {
+  const gk_pool_config& c = *lc.cfg;
+  SplitParams fp{};
+  fill_prefix_params(lc, layer, b, pl, &fp.pp);
+  fill_gather_params(lc, layer, b, pl, false, &fp.gp);
+  fp.n_pre = (int32_t)pl->prefix_items.size();
+  fp.n_gather = pl->summary.suffix_ctas;
+  const int ctas = fp.n_pre + fp.n_gather;
+  if (ctas == 0) return 0;
+  const int g = c.num_q_heads / c.num_kv_heads;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (c.head_dim == 128) {
+    fp.data_bytes = (uint32_t)split_data_bytes<128>(c.num_kv_heads);
+    switch (g) {
+      case 1: return launch_split_t<128, 1>(fp, ctas, st);
+      case 2: return launch_split_t<128, 2>(fp, ctas, st);
+      case 4: return launch_split_t<128, 4>(fp, ctas, st);
+      case 5: return launch_split_t<128, 5>(fp, ctas, st);
+      case 8: return launch_split_t<128, 8>(fp, ctas, st);
+    }
+  } else if (c.head_dim == 64) {
+    fp.data_bytes = (uint32_t)split_data_bytes<64>(c.num_kv_heads);
+    switch (g) {
+      case 1: return launch_split_t<64, 1>(fp, ctas, st);
+      case 2: return launch_split_t<64, 2>(fp, ctas, st);
+      case 4: return launch_split_t<64, 4>(fp, ctas, st);
+    }
+  }
+  return (int)cudaErrorInvalidValue;
+}
+
+}  // namespace gk

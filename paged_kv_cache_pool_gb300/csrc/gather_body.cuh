@@ -1,0 +1,459 @@
+// Body of the gather attention (suffix kernel, flat backend) and of the LSE
+// merge, shared by the stand-alone kernels and the split cascade kernel.
+//
+// Suffix kernel (GraniKV Section 3.3 / 3.5, cascade level 1): each request's
+// COLD tokens are gathered through its block table ("Paged KV cache", How it
+// works step 3: slot = table[t / P] * P + t % P) and attended with an online
+// softmax.  Dense backend: the same kernel walks a request's whole context,
+// its HOT prefix (contiguous per KV head, re-read for every request) then its
+// COLD suffix, the flat paged decode the pages compare against.
+//
+// Work split: the plan cuts the concatenated token stream of all requests into
+// one equal quota per CTA (one CTA per SM); a quota that spans a request
+// boundary yields one segment per request.  Each segment produces a partial
+// (O, LSE) state or, when it covers a whole request, the final output.
+//
+// CTA layout: warp h is KV head h and its g query heads, and it moves its own
+// data.  A COLD token's row is Hkv*d contiguous bf16 in the pool; warp h
+// copies only its head's d-wide slice of K and of V (256 bytes at d = 128)
+// with 16-byte cp.async, 16 tokens per stage, into a private ring of stages in
+// shared memory, nst - 1 stages ahead of its compute.  Many warps each with a
+// few stages in flight keep more bytes moving per SM than one copy engine fed
+// 2 KB rows, and no warp ever waits for another.  The warp loads 8x8 tiles
+// with ldmatrix and runs the two small per-head products on the warp-level
+// tensor-core MMA (m16n8k16, bf16 in, fp32 accumulate):
+//   S^T[16 tok x 8] = K[16 tok x d] . Q_h^T[d x 8]   (the g query heads, padded to 8)
+//   O^T[d x 8]     += V^T[d x 16 tok] . P^T[16 tok x 8]
+// with the online softmax (running max, rescale, sum) on the S^T fragments and
+// warp shuffles across the lanes that hold one head.  P^T is re-packed into
+// the B-operand layout with movmatrix.  The product is 2*g flops per byte, so
+// the kernel is bound by HBM; the MMA only keeps the issue slots free for the
+// copies.
+#pragma once
+#include <cfloat>
+
+#include "device_common.cuh"
+#include "gk_internal.h"
+
+namespace gk {
+namespace gather {
+
+constexpr int kT = kGatherT;  // tokens per stage (one m16 / k16 MMA step)
+constexpr int kLookAhead = 4; // block-table reads run this many stages ahead of the copies
+constexpr int kMaxStages = 16;  // ring depth cap (the rings take what shared memory the SM has)
+constexpr int kGatherThreads = 32 * kMaxKvHeads;  // block size of the stand-alone kernel (warps = Hkv)
+
+struct GatherParams {
+  const uint16_t* hot_k;
+  const uint16_t* hot_v;
+  const uint16_t* cold_k;
+  const uint16_t* cold_v;
+  int64_t cold_slots;
+  int64_t n_blocks;
+  int32_t L, Hkv, Hq, page;
+  int32_t layer;
+  int32_t dense;
+  const int32_t* block_table;
+  int32_t max_blocks;
+  const uint16_t* q;
+  float* out;
+  float* lse;
+  float* part_o;
+  float* part_l;
+  const RequestDev* reqs;
+  const int32_t* seg_begin;
+  const SegmentDev* segs;
+  const uint8_t* tmaps;
+  int32_t* err;
+  float q_scale;  // log2(e) / sqrt(d): scores come out in the log2 domain
+  int32_t nst;    // pipeline stages (<= kMaxStages)
+};
+
+// Shared memory: each consumer warp owns a ring of nst stages; a stage holds
+// its head's slices of kT tokens, K then V, one token row (d bf16) every
+// slice_row_bytes -- 16 bytes more than the row, so that the eight rows an
+// ldmatrix reads fall in eight different 16-byte bank groups.
+__host__ __device__ constexpr uint32_t slice_row_bytes(int d) { return (uint32_t)d * 2 + 16; }
+__host__ __device__ constexpr uint32_t warp_stage_bytes(int d) { return 2u * kT * slice_row_bytes(d); }
+__host__ __device__ constexpr size_t gather_data_bytes(int hkv, int d, int nst) {
+  return (size_t)hkv * nst * warp_stage_bytes(d);
+}
+__host__ __device__ constexpr size_t gather_smem_bytes(int hkv, int d, int nst) {
+  return 1024 + gather_data_bytes(hkv, d, nst);
+}
+// opt-in dynamic shared memory of one CTA, and what a CTA that has the SM to
+// itself keeps outside the rings (alignment slack, control blocks)
+constexpr size_t kSmemPerCtaMax = 232448;
+constexpr size_t kSoleCtaReserve = 1024 + 3072;
+// ring depth when the gather CTA has the SM (and its shared memory) to itself
+__host__ __device__ constexpr int single_cta_stages(int hkv, int d) {
+  const int n = (int)((kSmemPerCtaMax - kSoleCtaReserve) / gather_data_bytes(hkv, d, 1));
+  return n > kMaxStages ? kMaxStages : n;
+}
+
+// wait until at most n (0..kMaxStages-1) of this thread's cp.async groups are pending
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+  switch (n) {
+#define GK_WAIT_CASE(i) \
+  case i:               \
+    asm volatile("cp.async.wait_group %0;" ::"n"(i) : "memory"); \
+    break;
+    GK_WAIT_CASE(0) GK_WAIT_CASE(1) GK_WAIT_CASE(2) GK_WAIT_CASE(3) GK_WAIT_CASE(4) GK_WAIT_CASE(5)
+    GK_WAIT_CASE(6) GK_WAIT_CASE(7) GK_WAIT_CASE(8) GK_WAIT_CASE(9) GK_WAIT_CASE(10) GK_WAIT_CASE(11)
+    GK_WAIT_CASE(12) GK_WAIT_CASE(13) GK_WAIT_CASE(14)
+#undef GK_WAIT_CASE
+    default:
+      asm volatile("cp.async.wait_group 15;" ::: "memory");
+  }
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+// D = A(16x16, row) . B(16x8, col) + D ; bf16 in, fp32 accumulate
+__device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The gather work of CTA `cta` (its segments of the plan's partition) on the
+// calling CTA.  Warp h < Hkv is KV head h and its g query heads; further warps
+// return at once.  Each warp streams its own data: it copies its head's K and
+// V slices of the stage nst-1 ahead into its ring with 16-byte cp.async (one
+// commit group per stage), waits for the oldest group, and computes on it, so
+// no warp waits for another.  The block-table lookups of a stage are issued a
+// stage before its copies.  `base` (16-byte aligned) holds
+// gather_data_bytes(Hkv, D, p.nst).  All threads of the CTA call it.
+template <int D, int G, bool DENSE>
+__device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t base, int cta) {
+  constexpr int KSTEPS = D / 16;       // k16 steps of the QK product, m16 tiles of the PV product
+  constexpr uint32_t SR = slice_row_bytes(D);
+  constexpr uint32_t WS = warp_stage_bytes(D);
+  constexpr int CPT = D / 8;           // 16-byte chunks per token slice
+  constexpr int CPL = kT * CPT / 32;   // chunks per lane per stage and tensor
+  const int Hkv = p.Hkv;
+  const int nst = p.nst;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Zero the rings once: a partial stage leaves rows past its tokens untouched,
+  // and those rows must hold finite values (they meet P = 0 in the MMA).
+  for (uint32_t off = threadIdx.x * 16; off < (uint32_t)gather_data_bytes(Hkv, D, nst); off += blockDim.x * 16)
+    sts128(base + off, make_uint4(0, 0, 0, 0));
+  __syncthreads();
+  griddep_wait();   // queries, pool rows and the partial-state buffer are written upstream
+  if (warp >= Hkv) return;
+
+  const int h = warp;
+  const uint32_t ring = base + (uint32_t)h * nst * WS;
+  const int seg0 = p.seg_begin[cta], seg1 = p.seg_begin[cta + 1];
+  const int64_t layer_rows = (int64_t)p.layer * p.cold_slots;
+
+  // ---- lookups kLookAhead stages ahead of the copies ----
+  // A stage's copies need its tokens' block ids, and a table read is a round
+  // trip to memory (the table does not stay in L2 under the KV stream).  So a
+  // stage's ids are read kLookAhead stages before its copies and carried in
+  // registers; nothing uses a loaded id until the copy, where the slot
+  // arithmetic happens.
+  struct Cursor {
+    int sg, t, t1, lp;
+    const int32_t* table;
+    int64_t hot_row0;  // element offset of the (layer, head h) rows of the request's HOT prefix
+  };
+  struct Entry {
+    int32_t blk;    // COLD, lane < n: block id of the stage's token `lane`
+    int32_t tt0;    // COLD: suffix index of the stage's token 0
+    int32_t n;      // tokens in the stage (0: no stage)
+    int32_t hot;    // 1: a HOT run
+    int64_t row0;   // HOT: element offset of token 0's row
+  };
+  auto cursor_at = [&](int sg) {
+    Cursor c{};
+    c.sg = sg;
+    if (sg < seg1) {
+      const SegmentDev sd = p.segs[sg];
+      const RequestDev rq = p.reqs[sd.req];
+      c.t = sd.t0;
+      c.t1 = sd.t1;
+      c.lp = DENSE ? rq.lp : 0;
+      c.table = p.block_table + (int64_t)sd.req * p.max_blocks;
+      if (DENSE && c.lp > 0) c.hot_row0 = rq.hot_base * p.L * Hkv * D + ((int64_t)p.layer * Hkv + h) * c.lp * D;
+    }
+    return c;
+  };
+  auto stage_len = [&](const Cursor& c) {
+    int n = min(kT, c.t1 - c.t);
+    if (DENSE && c.t < c.lp) n = min(n, c.lp - c.t);
+    return n;
+  };
+  auto advance = [&](const Cursor& c) {
+    if (c.sg >= seg1) return c;
+    Cursor r = c;
+    r.t += stage_len(c);
+    return r.t < r.t1 ? r : cursor_at(c.sg + 1);
+  };
+  auto make_entry = [&](const Cursor& c) {
+    Entry e{};
+    if (c.sg >= seg1) return e;
+    e.n = stage_len(c);
+    if (DENSE && c.t < c.lp) {
+      e.hot = 1;
+      e.row0 = c.hot_row0 + (int64_t)c.t * D;
+    } else {
+      e.tt0 = c.t - c.lp;
+      e.blk = lane < e.n ? c.table[(e.tt0 + lane) / p.page] : -1;
+    }
+    return e;
+  };
+  int issued = 0;
+  auto copy_stage = [&](const Entry& e) {
+    if (e.n > 0) {
+      const uint32_t kdst = ring + (uint32_t)(issued % nst) * WS, vdst = kdst + kT * SR;
+      if (DENSE && e.hot) {
+        // HOT: the stage's rows of this head are contiguous
+        for (int ci = lane; ci < e.n * CPT; ci += 32) {
+          const uint32_t o = (uint32_t)(ci / CPT) * SR + (ci % CPT) * 16;
+          cp_async16(kdst + o, p.hot_k + e.row0 + ci * 8);
+          cp_async16(vdst + o, p.hot_v + e.row0 + ci * 8);
+        }
+      } else {
+        // COLD: lane i < n turns its token's block id into the row offset of head h
+        int64_t off = -1;
+        if (lane < e.n) {
+          if (e.blk >= 0 && e.blk < p.n_blocks)
+            off = ((layer_rows + (int64_t)e.blk * p.page + (e.tt0 + lane) % p.page) * Hkv + h) * D;
+          else
+            report_error(p.err, kErrBounds);
+        }
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+          const int ci = lane + 32 * j, tok = ci / CPT, ch = ci % CPT;
+          const int64_t src = __shfl_sync(0xffffffffu, off, tok);
+          if (tok < e.n && src >= 0) {
+            const uint32_t o = (uint32_t)tok * SR + ch * 16;
+            cp_async16(kdst + o, p.cold_k + src + ch * 8);
+            cp_async16(vdst + o, p.cold_v + src + ch * 8);
+          }
+        }
+      }
+    }
+    cp_async_commit();
+    ++issued;
+  };
+  // the queue: q0 is copied next, q3 was looked up last
+  Cursor lk = cursor_at(seg0);
+  Entry q0 = make_entry(lk);
+  lk = advance(lk);
+  Entry q1 = make_entry(lk);
+  lk = advance(lk);
+  Entry q2 = make_entry(lk);
+  lk = advance(lk);
+  Entry q3 = make_entry(lk);
+  lk = advance(lk);
+  auto issue_next = [&]() {
+    copy_stage(q0);
+    q0 = q1;
+    q1 = q2;
+    q2 = q3;
+    q3 = make_entry(lk);
+    lk = advance(lk);
+  };
+  for (int i = 0; i < nst - 1; ++i) issue_next();
+
+  // ---- compute, segment by segment ----
+  const int gq = lane >> 2;  // fragment row group
+  const int tq = lane & 3;   // fragment column pair
+  const int mi = lane >> 3, mj = lane & 7;  // ldmatrix: matrix index, row within it
+  int k = 0;
+  for (int sg = seg0; sg < seg1; ++sg) {
+    const SegmentDev seg = p.segs[sg];
+    const int lp = DENSE ? p.reqs[seg.req].lp : 0;
+
+    // Q_h^T as the B operand: b[kk][0] = (d 16kk+2tq, +1; head gq), b[kk][1] = (d +8, +9; head gq)
+    uint32_t qb[KSTEPS][2];
+    {
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((int64_t)seg.req * p.Hq + h * G + min(gq, G - 1)) * D);
+#pragma unroll
+      for (int kk = 0; kk < KSTEPS; ++kk) {
+        qb[kk][0] = gq < G ? qrow[kk * 8 + tq] : 0u;
+        qb[kk][1] = gq < G ? qrow[kk * 8 + 4 + tq] : 0u;
+      }
+    }
+    float o[KSTEPS][4];
+#pragma unroll
+    for (int mt = 0; mt < KSTEPS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2tq and 2tq+1
+
+    for (int t = seg.t0; t < seg.t1;) {
+      int n = min(kT, seg.t1 - t);
+      if (DENSE && t < lp) n = min(n, lp - t);
+      issue_next();                  // stage k + nst - 1
+      cp_async_wait_pending(nst - 1);  // stage k has landed (this lane's copies) ...
+      __syncwarp();                  // ... and every lane's
+      const uint32_t ks = ring + (uint32_t)(k % nst) * WS, vs = ks + kT * SR;
+      // address of 16-byte chunk c of token row tok in a slice
+      auto chunk_addr = [&](uint32_t slice, int tok, int c) -> uint32_t { return slice + (uint32_t)tok * SR + c * 16; };
+      // S^T = K Q_h^T
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < KSTEPS; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(chunk_addr(ks, mj + 8 * (mi & 1), 2 * kk + (mi >> 1)), a0, a1, a2, a3);
+        mma16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+      }
+      // online softmax over the 16 tokens (rows gq and gq+8) for heads 2tq, 2tq+1
+      const bool v_lo = gq < n, v_hi = gq + 8 < n;
+      const float s00 = v_lo ? sc[0] * p.q_scale : -INFINITY;
+      const float s01 = v_lo ? sc[1] * p.q_scale : -INFINITY;
+      const float s10 = v_hi ? sc[2] * p.q_scale : -INFINITY;
+      const float s11 = v_hi ? sc[3] * p.q_scale : -INFINITY;
+      float x0 = fmaxf(s00, s10), x1 = fmaxf(s01, s11);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+      }
+      const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+      if (__any_sync(0xffffffffu, n0 != m0 || n1 != m1)) {
+        const float a0 = ex2(m0 - n0), a1 = ex2(m1 - n1);
+        l0 *= a0;
+        l1 *= a1;
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt) {
+          o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
+        }
+        m0 = n0;
+        m1 = n1;
+      }
+      const float p00 = ex2(s00 - m0), p01 = ex2(s01 - m1), p10 = ex2(s10 - m0), p11 = ex2(s11 - m1);
+      l0 += p00 + p10;
+      l1 += p01 + p11;
+      // P^T (16 tok x 8 heads) -> B operand of the PV product
+      const uint32_t pb0 = movm_t(pack_bf16x2(p00, p01));
+      const uint32_t pb1 = movm_t(pack_bf16x2(p10, p11));
+      // O^T += V^T P^T
+#pragma unroll
+      for (int mt = 0; mt < KSTEPS; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(chunk_addr(vs, mj + 8 * (mi >> 1), 2 * mt + (mi & 1)), a0, a1, a2, a3);
+        mma16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+      }
+      __syncwarp();                  // every lane has read the stage before it is refilled
+      t += n;
+      ++k;
+    }
+
+    // finish: the row sums live on the 8 lanes that share tq
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    const float i0 = 1.f / l0, i1 = 1.f / l1;
+    const int hh0 = 2 * tq, hh1 = 2 * tq + 1;
+    float* dst;
+    float* dl;
+    int64_t row0;
+    if (seg.entry >= 0) {
+      row0 = (int64_t)seg.entry * p.Hq + h * G;
+      dst = p.part_o;
+      dl = p.part_l;
+    } else {
+      row0 = (int64_t)seg.req * p.Hq + h * G;
+      dst = p.out;
+      dl = p.lse;
+    }
+#pragma unroll
+    for (int mt = 0; mt < KSTEPS; ++mt) {
+      const int d0 = mt * 16 + gq;
+      if (hh0 < G) {
+        dst[(row0 + hh0) * D + d0] = o[mt][0] * i0;
+        dst[(row0 + hh0) * D + d0 + 8] = o[mt][2] * i0;
+      }
+      if (hh1 < G) {
+        dst[(row0 + hh1) * D + d0] = o[mt][1] * i1;
+        dst[(row0 + hh1) * D + d0 + 8] = o[mt][3] * i1;
+      }
+    }
+    if (gq == 0 && dl) {
+      const float f = seg.entry >= 0 ? 1.f : kLn2;   // partials keep log2, outputs are natural log
+      if (hh0 < G) dl[row0 + hh0] = (m0 + __log2f(l0)) * f;
+      if (hh1 < G) dl[row0 + hh1] = (m1 + __log2f(l1)) * f;
+    }
+  }
+  cp_async_wait_pending(0);
+}
+
+// LSE merge (GraniKV Eq. 1, applied to any number of partial states): for each
+// request and query head, O = sum_e 2^(l_e - m) O_e / sum_e 2^(l_e - m),
+// LSE = (m + log2 sum_e 2^(l_e - m)) * ln 2, with m = max_e l_e (log2 domain).
+// One warp per (request, query head): entries [e0, e0 + ne).  Lane e holds
+// entry e's LSE and weight (entries beyond 32 are folded in a second round);
+// the d-wide rows are then read 16 entries at a time with every load in
+// flight before any is used.  Partial states come from other CTAs, so they are
+// read at L2 (ld.global.cg).
+__device__ __forceinline__ void merge_head(const float* part_o, const float* part_l, int e0, int ne, int r, int qh,
+                                           int Hq, int D, float* out, float* lse) {
+  const int lane = threadIdx.x & 31;
+  float mx = -INFINITY;
+  for (int e = lane; e < ne; e += 32) mx = fmaxf(mx, __ldcg(part_l + (int64_t)(e0 + e) * Hq + qh));
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  const int vecs = D / 4;  // float4 per row: 16 or 32
+  const bool has = lane < vecs;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  float z = 0.f;
+  if (mx != -INFINITY) {
+    for (int eb = 0; eb < ne; eb += 32) {
+      const int e = eb + lane;
+      const float w = e < ne ? ex2(__ldcg(part_l + (int64_t)(e0 + e) * Hq + qh) - mx) : 0.f;
+      float wz = w;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) wz += __shfl_xor_sync(0xffffffffu, wz, off);
+      z += wz;
+      const int nb = min(32, ne - eb);
+      for (int c0 = 0; c0 < nb; c0 += 16) {
+        float4 v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          v[k] = (has && c0 + k < nb)
+                     ? __ldcg(reinterpret_cast<const float4*>(part_o + ((int64_t)(e0 + eb + c0 + k) * Hq + qh) * D) + lane)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float wk = __shfl_sync(0xffffffffu, w, (c0 + k) & 31);
+          o.x = fmaf(wk, v[k].x, o.x);
+          o.y = fmaf(wk, v[k].y, o.y);
+          o.z = fmaf(wk, v[k].z, o.z);
+          o.w = fmaf(wk, v[k].w, o.w);
+        }
+      }
+    }
+    const float inv = 1.f / z;
+    o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
+  }
+  if (has) reinterpret_cast<float4*>(out + ((int64_t)r * Hq + qh) * D)[lane] = o;
+  if (lane == 0 && lse) lse[(int64_t)r * Hq + qh] = mx == -INFINITY ? -INFINITY : (mx + __log2f(z)) * kLn2;
+}
+
+}  // namespace gather
+
+// kernel arguments of the gather for one layer of a planned batch (dense: the
+// flat backend's partition, else the cascade suffix partition)
+int fill_gather_params(const LaunchCommon& lc, int32_t layer, const gk_batch* b, const Plan* pl, bool dense,
+                       gather::GatherParams* out);
+
+}  // namespace gk

@@ -62,6 +62,8 @@ struct Pool {
   HotAllocator hot;
   BlockManager cold;
   gk_cost_model cost{};
+  gk_cascade_mode cascade_mode = GK_CASCADE_AUTO;
+  int32_t cascade_tiles = 0;         // GK_CASCADE_SPLIT: tiles per item (0 = best predicted)
   std::string last_error;
   DeviceInfo dev;
   int32_t* d_error = nullptr;        // device error word (allocated on first device use)
@@ -76,7 +78,7 @@ struct PrefixGroupDev {
   int32_t req_base;    // offset into prefix_reqs
   int32_t nsplit;      // splits over the prefix keys
   int32_t split_tiles; // key tiles (of kPrefixTileN) per split
-  int32_t tmap_index;  // first of the group's 4 tensor maps: K, V (128-key box), K, V (16-key box)
+  int32_t tmap_index;  // first of the group's 2 tensor maps: K, V (128-key box)
   int32_t pad0, pad1;
 };
 
@@ -101,7 +103,7 @@ struct RequestDev {
   int32_t n_entry_cas;
   int32_t entry_dense;
   int32_t n_entry_dense;
-  int32_t group;       // HOT prefix group (tensor maps 4*group..4*group+3), -1 = none
+  int32_t group;       // HOT prefix group, -1 = none
   int32_t pad0;
 };
 
@@ -135,6 +137,7 @@ struct Plan {
   float* d_part_l = nullptr;             // [entries][Hq] (log2 domain)
   size_t part_entries = 0;
   bool uploaded = false;
+  bool split = false;                    // cascade arrangement: prefix items and suffix gather side by side
 };
 
 // host half of gk_plan_build: grouping, work lists and partial-state layout (no device work)
@@ -166,12 +169,15 @@ int launch_merge(const LaunchCommon& lc, void* stream, const gk_batch* b, const 
                  bool dense);
 int launch_prefix(const LaunchCommon& lc, void* stream, int32_t layer, const gk_batch* b,
                   const Plan* plan);
-// resident gather CTAs per SM for the pool's geometry (from its shared-memory
-// footprint; no device query, so host-only pools plan identically)
+// split arrangement: the prefix items and the suffix gather of one layer in one
+// launch, on disjoint SMs (the merge follows as its own launch)
+int launch_cascade_split(const LaunchCommon& lc, void* stream, int32_t layer, const gk_batch* b,
+                         const Plan* plan);
+// resident gather CTAs per SM for the pool's geometry (no device query, so
+// host-only pools plan identically)
 int gather_ctas_per_sm(const gk_pool_config* cfg);
 // encode the tensor maps of a plan's prefix groups into host memory (128 B each,
-// 4 per group: K and V with a 128-key box for the prefix kernel, K and V with a
-// 16-key box for the dense gather)
+// 2 per group: K and V with a 128-key box for the prefix kernel)
 int encode_prefix_tmaps(const gk_pool_config* cfg, const Plan* plan, std::vector<uint8_t>* out);
 size_t tmap_bytes();
 

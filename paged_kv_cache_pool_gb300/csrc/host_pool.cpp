@@ -215,6 +215,9 @@ gk_status gk_pool_create(const gk_pool_config* cfg, gk_pool** out) {
   cm.bw_prefix_gbs = 5500.0;
   cm.bw_suffix_gbs = 5000.0;
   cm.c_merge_us = 0.0;
+  cm.prefix_tile_us = 1.65;
+  cm.prefix_item_us = 10.5;
+  cm.gather_sm_gbs = 44.0;
   cm.n_tc_points = 3;
   cm.tc_m[0] = 128; cm.tc_tflops[0] = 300;
   cm.tc_m[1] = 512; cm.tc_tflops[1] = 700;

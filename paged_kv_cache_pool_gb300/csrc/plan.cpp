@@ -16,6 +16,8 @@
 
 namespace gk {
 
+static double tc_at(const gk_cost_model& cm, double M);
+
 namespace {
 
 constexpr int kGatherQuantum = 16;        // gather CTAs get token quotas in multiples of this
@@ -128,21 +130,68 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     ntiles[(size_t)gi] = (lp + kPrefixTileN - 1) / kPrefixTileN;
     max_ntiles = std::max(max_ntiles, ntiles[(size_t)gi]);
   }
-  int32_t best_c = max_ntiles;
-  double best_cost = 1e300;
-  if (G > 0) {
-    for (int32_t C = 1; C <= max_ntiles; ++C) {
-      int64_t units = 0;
-      for (int32_t gi = 0; gi < G; ++gi)
-        units += (int64_t)mtiles[(size_t)gi] * Hkv * ((ntiles[(size_t)gi] + C - 1) / C);
-      int64_t waves = (units + num_sms - 1) / num_sms;
-      double cost = (double)waves * (C + kPrefixCtaOverheadTiles);
+  // Sequential arrangement: every SM takes prefix items (waves of them), then
+  // every SM gathers.  Keys per split balance the waves, counting a CTA's
+  // set-up and epilogue as kPrefixCtaOverheadTiles tiles.
+  auto n_items = [&](int32_t C) {
+    int64_t units = 0;
+    for (int32_t gi = 0; gi < G; ++gi)
+      units += (int64_t)mtiles[(size_t)gi] * Hkv * ((ntiles[(size_t)gi] + C - 1) / C);
+    return units;
+  };
+  int32_t c_seq = max_ntiles;
+  {
+    double best_cost = 1e300;
+    for (int32_t C = 1; G > 0 && C <= max_ntiles; ++C) {
+      const double cost = (double)((n_items(C) + num_sms - 1) / num_sms) * (C + kPrefixCtaOverheadTiles);
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
-        best_c = C;
+        c_seq = C;
       }
     }
   }
+  // Split arrangement: n_pre SMs each run one prefix item of C key tiles while
+  // the other SMs gather the suffix, in one launch.  Predicted
+  //   T_split(C) = max(C * prefix_tile_us + prefix_item_us,
+  //                    S / min(bw_suffix, (SMs - n_pre) * gather_sm)),
+  // against T_seq = sum_g max(bytes_g / bw_prefix, flops_g / TC(M_g)) + S / bw_suffix.
+  // The split is taken when some C is predicted faster than the sequential
+  // arrangement; among equal predictions the fewest items (fewest partials)
+  // win, and the chosen item count is then spread evenly over the key tiles.
+  const gk_cost_model& cm = p->cost;
+  const int64_t kv_tok = 2LL * Hkv * d * 2;
+  int64_t suffix_tokens = 0;
+  for (int32_t r = 0; r < B; ++r) suffix_tokens += pl->reqs[(size_t)r].slen;
+  const double S = (double)suffix_tokens * (double)kv_tok;
+  double t_seq = S / (cm.bw_suffix_gbs * 1e3);
+  for (int32_t gi = 0; gi < G; ++gi) {
+    const double lp = (double)pl->reqs[(size_t)members[(size_t)gi][0]].lp;
+    const double tb = lp * (double)kv_tok / (cm.bw_prefix_gbs * 1e3);
+    const double tf = 4.0 * (double)members[(size_t)gi].size() * Hq * lp * d / (tc_at(cm, (double)members[(size_t)gi].size() * g) * 1e6);
+    t_seq += std::max(tb, tf);
+  }
+  int32_t c_split = 0;
+  double t_split = 1e300;
+  const bool can_split = G > 0 && suffix_tokens > 0 && p->cascade_mode != GK_CASCADE_SEQUENTIAL;
+  if (can_split && p->cascade_mode == GK_CASCADE_SPLIT && p->cascade_tiles > 0) {
+    const int32_t C = std::min(p->cascade_tiles, max_ntiles);
+    if (n_items(C) <= num_sms - 1) c_split = C;
+  } else {
+    for (int32_t C = max_ntiles; can_split && C >= 1; --C) {
+      const int64_t items = n_items(C);
+      if (items > num_sms - 1) break;  // items only grow as C shrinks
+      const double bw = std::min(cm.bw_suffix_gbs, (double)(num_sms - items) * cm.gather_sm_gbs);
+      const double t = std::max(C * cm.prefix_tile_us + cm.prefix_item_us, S / (bw * 1e3));
+      if (t < t_split - 1e-9) {
+        t_split = t;
+        c_split = C;
+      }
+    }
+  }
+  // balance the chosen split: the fewest tiles per item that gives as many items
+  while (c_split > 1 && n_items(c_split - 1) == n_items(c_split)) --c_split;
+  pl->split = c_split > 0 && (p->cascade_mode == GK_CASCADE_SPLIT || t_split < t_seq);
+  const int32_t best_c = pl->split ? c_split : c_seq;
   int32_t max_m = 0;
   int64_t pre_bytes = 0, pre_flops = 0;
   for (int32_t gi = 0; gi < G; ++gi) {
@@ -152,7 +201,7 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     gd.req_base = (int32_t)pl->prefix_reqs.size();
     gd.split_tiles = best_c;
     gd.nsplit = (ntiles[(size_t)gi] + best_c - 1) / best_c;
-    gd.tmap_index = 4 * gi;
+    gd.tmap_index = 2 * gi;
     for (int32_t r : members[(size_t)gi]) pl->prefix_reqs.push_back(r);
     pl->groups.push_back(gd);
     max_m = std::max(max_m, gd.m);
@@ -180,6 +229,8 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   for (auto& it : items) pl->prefix_items.push_back(it.it);
 
   // ---- gather work: cascade suffix and dense (flat) ------------------------------
+  // Gather CTAs own an SM each; a split plan leaves the gather the SMs its
+  // prefix items do not take.
   int64_t max_ctas = (int64_t)num_sms * std::max(1, gather_ctas_per_sm(&c));
   std::vector<int64_t> n_suf((size_t)B), n_dense((size_t)B);
   int64_t suf_tokens = 0, dense_tokens = 0;
@@ -189,7 +240,8 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     suf_tokens += n_suf[(size_t)r];
     dense_tokens += n_dense[(size_t)r];
   }
-  partition_tokens(n_suf, max_ctas, &pl->suf_seg_begin, &pl->suf_segs);
+  partition_tokens(n_suf, pl->split ? num_sms - (int64_t)pl->prefix_items.size() : num_sms, &pl->suf_seg_begin,
+                   &pl->suf_segs);
   partition_tokens(n_dense, max_ctas, &pl->dense_seg_begin, &pl->dense_segs);
 
   // ---- partial-state entries ----------------------------------------------------
@@ -245,6 +297,9 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   sm.prefix_flops = pre_flops;
   sm.suffix_bytes = suf_tokens * 2 * Hkv * d * 2;
   sm.dense_bytes = dense_tokens * 2 * Hkv * d * 2;
+  sm.cascade_split = pl->split ? 1 : 0;
+  sm.prefix_tiles_per_item = 0;
+  for (int32_t gi = 0; gi < G; ++gi) sm.prefix_tiles_per_item = std::max(sm.prefix_tiles_per_item, std::min(best_c, ntiles[(size_t)gi]));
   return GK_OK;
 }
 
@@ -362,6 +417,7 @@ static double tc_at(const gk_cost_model& cm, double M) {
 static bool valid_cost_model(const gk_cost_model& cm) {
   if (cm.n_tc_points < 1 || cm.n_tc_points > 16) return false;
   if (!(cm.bw_flat_gbs > 0 && cm.bw_prefix_gbs > 0 && cm.bw_suffix_gbs > 0)) return false;
+  if (!(cm.prefix_tile_us > 0 && cm.prefix_item_us >= 0 && cm.gather_sm_gbs > 0)) return false;
   for (int i = 0; i < cm.n_tc_points; ++i) {
     if (!(cm.tc_m[i] > 0 && cm.tc_tflops[i] > 0)) return false;
     if (i && !(cm.tc_m[i] > cm.tc_m[i - 1])) return false;
@@ -473,17 +529,33 @@ gk_status gk_dispatch(const gk_pool* pool, const gk_plan* plan, gk_backend* choi
   const gk_cost_model& cm = pool->impl.cost;
   const Plan& pl = plan->impl;
   double t_flat = cm.c_flat_us + (double)pl.summary.dense_bytes / (cm.bw_flat_gbs * 1e3);
-  double t_pre = 0.0;
-  for (size_t gi = 0; gi < pl.groups.size(); ++gi) {
-    double tb = (double)pl.group_bytes[gi] / (cm.bw_prefix_gbs * 1e3);
-    double tf = (double)pl.group_flops[gi] / (gk::tc_at(cm, (double)pl.groups[gi].m) * 1e6);
-    t_pre += std::max(tb, tf);
+  double t_levels = 0.0;
+  if (pl.split) {
+    const double bw = std::min(cm.bw_suffix_gbs, (double)pl.summary.suffix_ctas * cm.gather_sm_gbs);
+    t_levels = std::max(pl.summary.prefix_tiles_per_item * cm.prefix_tile_us + cm.prefix_item_us,
+                        (double)pl.summary.suffix_bytes / (bw * 1e3));
+  } else {
+    for (size_t gi = 0; gi < pl.groups.size(); ++gi) {
+      double tb = (double)pl.group_bytes[gi] / (cm.bw_prefix_gbs * 1e3);
+      double tf = (double)pl.group_flops[gi] / (gk::tc_at(cm, (double)pl.groups[gi].m) * 1e6);
+      t_levels += std::max(tb, tf);
+    }
+    t_levels += (double)pl.summary.suffix_bytes / (cm.bw_suffix_gbs * 1e3);
   }
-  double t_cas = cm.c_cascade_us + t_pre + (double)pl.summary.suffix_bytes / (cm.bw_suffix_gbs * 1e3) +
-                 cm.c_merge_us * (double)pl.B * pool->impl.cfg.num_q_heads;
+  double t_cas = cm.c_cascade_us + t_levels + cm.c_merge_us * (double)pl.B * pool->impl.cfg.num_q_heads;
   *choice = t_flat < t_cas ? GK_BACKEND_DENSE : GK_BACKEND_CASCADE;
   if (t_dense_us) *t_dense_us = t_flat;
   if (t_cascade_us) *t_cascade_us = t_cas;
+  return GK_OK;
+}
+
+gk_status gk_pool_set_cascade_mode(gk_pool* pool, gk_cascade_mode mode, int32_t tiles_per_item) {
+  if (!pool) return GK_ERR_INVALID;
+  if (mode != GK_CASCADE_AUTO && mode != GK_CASCADE_SEQUENTIAL && mode != GK_CASCADE_SPLIT)
+    return gk::fail(&pool->impl, GK_ERR_INVALID, "unknown cascade mode");
+  if (tiles_per_item < 0) return gk::fail(&pool->impl, GK_ERR_INVALID, "tiles_per_item < 0");
+  pool->impl.cascade_mode = mode;
+  pool->impl.cascade_tiles = tiles_per_item;
   return GK_OK;
 }
 
@@ -530,8 +602,9 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
       cm.n_tc_points = n;
       continue;
     }
-    static const char* kNumeric[] = {"c_flat_us", "bw_flat_gbs", "c_cascade_us", "bw_prefix_gbs", "bw_suffix_gbs",
-                                     "c_merge_us"};
+    static const char* kNumeric[] = {"c_flat_us",      "bw_flat_gbs",    "c_cascade_us",  "bw_prefix_gbs",
+                                     "bw_suffix_gbs",  "c_merge_us",     "prefix_tile_us", "prefix_item_us",
+                                     "gather_sm_gbs"};
     bool known = false;
     for (const char* k : kNumeric) known = known || key == k;
     if (!known) {
@@ -546,6 +619,9 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
     else if (key == "bw_prefix_gbs") cm.bw_prefix_gbs = v;
     else if (key == "bw_suffix_gbs") cm.bw_suffix_gbs = v;
     else if (key == "c_merge_us") cm.c_merge_us = v;
+    else if (key == "prefix_tile_us") cm.prefix_tile_us = v;
+    else if (key == "prefix_item_us") cm.prefix_item_us = v;
+    else if (key == "gather_sm_gbs") cm.gather_sm_gbs = v;
   }
   return gk_cost_model_set(pool, &cm);
 }
@@ -596,11 +672,25 @@ gk_status gk_cascade_merge(gk_pool* pool, void* stream, int32_t layer, const gk_
   return e ? gk::cuda_fail(p, e, "merge kernel") : GK_OK;
 }
 
+gk_status gk_cascade_levels(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch, const gk_plan* plan) {
+  if (!pool || !batch || !plan) return GK_ERR_INVALID;
+  Pool* p = &pool->impl;
+  const Plan* pl = &plan->impl;
+  gk_status st = check_decode(p, layer, batch, pl);
+  if (st != GK_OK) return st;
+  if (pl->B == 0) return GK_OK;
+  if (!pl->split) {
+    st = gk_cascade_prefix(pool, stream, layer, batch, plan);
+    return st == GK_OK ? gk_cascade_suffix(pool, stream, layer, batch, plan) : st;
+  }
+  gk::LaunchCommon lc{&p->cfg, p->d_error, p->dev.num_sms};
+  int e = gk::launch_cascade_split(lc, stream, layer, batch, pl);
+  return e ? gk::cuda_fail(p, e, "split cascade kernel") : GK_OK;
+}
+
 gk_status gk_decode_cascade(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch, const gk_plan* plan) {
-  gk_status st = gk_cascade_prefix(pool, stream, layer, batch, plan);
-  if (st == GK_OK) st = gk_cascade_suffix(pool, stream, layer, batch, plan);
-  if (st == GK_OK) st = gk_cascade_merge(pool, stream, layer, batch, plan);
-  return st;
+  gk_status st = gk_cascade_levels(pool, stream, layer, batch, plan);
+  return st == GK_OK ? gk_cascade_merge(pool, stream, layer, batch, plan) : st;
 }
 
 gk_status gk_decode_dense(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch, const gk_plan* plan) {

@@ -29,7 +29,8 @@ def attention_errors(O, LSE, O_ref, LSE_ref):
     l = np.asarray(LSE, dtype=np.float64).ravel()
     lr = np.asarray(LSE_ref, dtype=np.float64).ravel()
     both_inf = np.isneginf(l) & np.isneginf(lr)
-    lse_err = np.where(both_inf, 0.0, np.abs(l - lr))
+    with np.errstate(invalid="ignore"):
+        lse_err = np.where(both_inf, 0.0, np.abs(l - lr))
     lse_max = float(lse_err.max()) if lse_err.size else 0.0
     return dict(max_abs=max_abs, rel_l2=rel_max, lse_abs=lse_max)
 

@@ -237,13 +237,14 @@ def test_dispatch_matches_oracle_formula(gk, case):
     Hq, Hkv, d = rnd.choice([(32, 8, 128), (40, 8, 128)])
     cm = dict(c_flat_us=rnd.uniform(2, 20), bw_flat_gbs=rnd.uniform(3000, 7000), c_cascade_us=rnd.uniform(5, 40),
               bw_prefix_gbs=rnd.uniform(3000, 7000), bw_suffix_gbs=rnd.uniform(3000, 7000),
-              c_merge_us=rnd.uniform(0, 0.002),
+              c_merge_us=rnd.uniform(0, 0.002), prefix_tile_us=rnd.uniform(0.5, 3.0),
+              prefix_item_us=rnd.uniform(0, 20), gather_sm_gbs=rnd.uniform(20, 80),
               tc_points=[[128, rnd.uniform(100, 400)], [512, rnd.uniform(400, 900)], [2048, rnd.uniform(900, 1600)]])
     pool = gk.gk_pool_create(1, Hq, Hkv, d, 200000, 64, 1, 0)
     try:
         gk.gk_cost_model_load(pool, json.dumps(cm))
         got_cm = gk.gk_cost_model_get(pool)
-        for k in ("c_flat_us", "bw_flat_gbs", "c_cascade_us", "bw_prefix_gbs", "bw_suffix_gbs", "c_merge_us"):
+        for k in gk.COST_MODEL_KEYS:
             assert got_cm[k] == cm[k]
         assert got_cm["tc_points"] == cm["tc_points"]
         n_pref = rnd.randint(0, 3)
@@ -260,6 +261,12 @@ def test_dispatch_matches_oracle_formula(gk, case):
         choice, td, tc = gk.gk_dispatch(pool, plan)
         f = odisp.features(lps, slens, grp, Hq, Hkv, d)
         want, wd, wc = odisp.choose(cm, f)
+        arr = odisp.arrangement(cm, f, 152)
+        s = gk.gk_plan_info(plan)
+        assert s["cascade_split"] == int(arr["split"]) and s["suffix_ctas"] == arr["n_gather"]
+        if arr["split"]:
+            assert s["prefix_ctas"] == arr["n_pre"] and s["prefix_tiles_per_item"] == arr["C"]
+            assert s["prefix_ctas"] + s["suffix_ctas"] <= 152
         assert math.isclose(td, wd, rel_tol=1e-12) and math.isclose(tc, wc, rel_tol=1e-12)
         assert choice == (gk.GK_BACKEND_DENSE if want == "dense" else gk.GK_BACKEND_CASCADE)
         gk.gk_plan_destroy(plan)
@@ -310,5 +317,45 @@ def test_measured_cost_model_routes_the_workloads(gk):
         choice, td, tc = gk.gk_dispatch(pool, plan)
         assert choice == gk.GK_BACKEND_DENSE and td < tc
         gk.gk_plan_destroy(plan)
+    finally:
+        gk.gk_pool_destroy(pool)
+
+
+def test_cascade_mode_forces_the_arrangement(gk):
+    """One group of 64 requests (g = 4: one 256-row block per KV head), Lp = 16384
+    (128 key tiles), Hkv = 8, 1000 suffix tokens each, 152 SMs on a host-only pool."""
+    from oracle import dispatch as odisp
+    pool = gk.gk_pool_create(1, 32, 8, 128, 16384 + 16, 64 * 1000 + 64, 1, 0)
+    try:
+        base = gk.gk_prefix_alloc(pool, 16384)
+
+        def summary():
+            b, plan = _host_plan(gk, pool, [base] * 64, [16384] * 64, [1000] * 64)
+            s = gk.gk_plan_info(plan)
+            gk.gk_plan_destroy(plan)
+            return s
+
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SEQUENTIAL)
+        s = summary()
+        assert s["cascade_split"] == 0 and s["suffix_ctas"] == odisp.gather_ctas(64000, 152)
+        for C in (64, 32, 10):
+            gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SPLIT, C)
+            s = summary()
+            n_pre = 8 * -(-128 // C)
+            assert s["cascade_split"] == 1 and s["prefix_ctas"] == n_pre and s["prefix_tiles_per_item"] == C
+            assert s["suffix_ctas"] == odisp.gather_ctas(64000, 152 - n_pre)
+            # partial states: one per (request, key split), plus at least one per request's suffix
+            assert s["num_partials"] >= 64 * -(-128 // C) + 64
+        # 7 tiles per item would need 152 items: no SM left for the gather -> sequential
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SPLIT, 7)
+        assert summary()["cascade_split"] == 0
+        # 0: the cost model's best split, taken even where the sequential plan is predicted faster
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SPLIT, 0)
+        s = summary()
+        assert s["cascade_split"] == 1 and s["prefix_ctas"] + s["suffix_ctas"] <= 152
+        with pytest.raises(gk.GkError):
+            gk.gk_pool_set_cascade_mode(pool, 7)
+        with pytest.raises(gk.GkError):
+            gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SPLIT, -1)
     finally:
         gk.gk_pool_destroy(pool)

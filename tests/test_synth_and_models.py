@@ -92,19 +92,49 @@ def test_tc_curve_closed_form():
 
 
 def test_cost_model_closed_form():
+    # prefix tiles so slow that the split arrangement never wins: the sequential formula
     cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0,
-              tc_points=[[128, 500.0], [1024, 1500.0]], bw_suffix_gbs=4000.0, c_merge_us=0.001)
+              tc_points=[[128, 500.0], [1024, 1500.0]], bw_suffix_gbs=4000.0, c_merge_us=0.001,
+              prefix_tile_us=1e6, prefix_item_us=0.0, gather_sm_gbs=50.0)
     # one group of 64 requests (g = 4 -> M = 256), Lp = 1000, suffixes 100 each, Hkv = 8, d = 128
     f = dispatch.features([1000] * 64, [100] * 64, [0] * 64, 32, 8, 128)
     kv = 2 * 8 * 128 * 2
     assert f["bytes_flat"] == 64 * 1100 * kv and f["bytes_suffix"] == 64 * 100 * kv
-    assert f["prefix"] == [dict(M=256, bytes=1000 * kv, flops=4 * 64 * 32 * 1000 * 128)]
+    assert f["prefix"] == [dict(M=256, bytes=1000 * kv, flops=4 * 64 * 32 * 1000 * 128, lp=1000)]
     t_flat, t_cas = dispatch.predict(cm, f)
     assert math.isclose(t_flat, 5.0 + 64 * 1100 * kv / 4e6)
     tc = 500.0 + 1000.0 * (256 - 128) / (1024 - 128)
     t_pre = max(1000 * kv / 5e6, 4 * 64 * 32 * 1000 * 128 / (tc * 1e6))
     assert math.isclose(t_cas, 10.0 + t_pre + 64 * 100 * kv / 4e6 + 0.001 * 64 * 32)
     assert dispatch.choose(cm, f)[0] == ("dense" if t_flat < t_cas else "cascade")
+    assert not dispatch.arrangement(cm, f, 152)["split"]
     # a request without a HOT prefix counts only toward the flat and suffix bytes
     f2 = dispatch.features([0, 1000], [300, 10], [-1, 0], 32, 8, 128)
     assert f2["bytes_flat"] == 1310 * kv and len(f2["prefix"]) == 1 and f2["prefix"][0]["M"] == 4
+
+
+def test_split_arrangement_worked_example():
+    """One group of 64 requests (g = 4 -> one 256-row block), Lp = 16384 (128 key tiles),
+    Hkv = 8, 1000 suffix tokens each; tile 1 us, item 5 us, 50 GB/s per SM, 6000 GB/s.
+    Items(C) = 8 * ceil(128 / C); T(C) = max(C + 5, S / min(6000, (152 - items) * 50)).
+    C = 32..38 leave 120 SMs (S / 6000 GB/s = 43.69 us binds); the largest, 38, wins the
+    scan, and 32 is the fewest tiles per item that still gives its 32 items."""
+    cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0,
+              tc_points=[[128, 500.0], [1024, 1500.0]], bw_suffix_gbs=6000.0, c_merge_us=0.001,
+              prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0)
+    f = dispatch.features([16384] * 64, [1000] * 64, [0] * 64, 32, 8, 128)
+    S = 64 * 1000 * 4096
+    assert f["bytes_suffix"] == S
+    a = dispatch.arrangement(cm, f, 152)
+    assert a == dict(split=True, C=32, n_pre=32, n_gather=118)
+    # the gather partition: quota ceil(64000 / 120) = 534 -> 544 (multiple of 16) -> 118 CTAs
+    assert dispatch.gather_ctas(64000, 120) == 118
+    t_flat, t_cas = dispatch.predict(cm, f, 152)
+    assert math.isclose(t_cas, 10.0 + max(32 + 5.0, S / (118 * 50.0 * 1e3)) + 0.001 * 64 * 32)
+    # the sequential alternative it beat: suffix at 6000 GB/s plus the prefix at TC(256)
+    tc = 500.0 + 1000.0 * (256 - 128) / (1024 - 128)
+    t_seq = S / 6e6 + max(16384 * 4096 / 5e6, 4 * 64 * 32 * 16384 * 128 / (tc * 1e6))
+    assert math.isclose(dispatch.sequential_levels(cm, f), t_seq) and t_seq > 43.69
+    # no suffix, or no shared prefix: never split
+    assert not dispatch.arrangement(cm, dispatch.features([16384] * 64, [0] * 64, [0] * 64, 32, 8, 128), 152)["split"]
+    assert not dispatch.arrangement(cm, dispatch.features([0] * 64, [1000] * 64, [-1] * 64, 32, 8, 128), 152)["split"]
