@@ -249,29 +249,29 @@ typedef struct gk_cost_model {
   double c_flat_us;               /* fixed cost of the dense backend per layer */
   double bw_flat_gbs;             /* its sustained gather bandwidth */
   double c_cascade_us;            /* fixed cost of the cascade backend per layer */
-  double bw_prefix_gbs;           /* prefix-kernel HOT read bandwidth */
-  double bw_suffix_gbs;           /* suffix gather bandwidth */
+  double bw_prefix_gbs;           /* bandwidth bound of the prefix contraction (HOT reads) */
+  double bw_suffix_gbs;           /* suffix gather bandwidth over every SM */
   double c_merge_us;              /* merge cost per (request, query head) */
-  double prefix_tile_us;          /* split cascade: one 128-key tile of a prefix work item on one SM */
-  double prefix_item_us;          /* split cascade: fixed cost of one prefix work item */
-  double gather_sm_gbs;           /* split cascade: suffix gather bandwidth one SM sustains */
-  int32_t n_tc_points;            /* 1..16 */
-  int32_t reserved0;
-  double tc_m[16];                /* M_eff of each calibration point, increasing */
-  double tc_tflops[16];           /* achieved prefix-kernel TFLOP/s at that M_eff */
+  double prefix_tile_us;          /* one 128-key tile of a 256-row prefix work item on one SM */
+  double prefix_item_us;          /* fixed cost of a prefix work item (of each wave of them) */
+  double gather_sm_gbs;           /* suffix gather bandwidth one SM sustains (split plans) */
+  double c_gather_us;             /* fixed cost of a separate suffix-gather launch (sequential plans) */
 } gk_cost_model;
 
 /* Predict both backends for the plan and pick the smaller:
  *   T_dense   = c_flat + dense_bytes / bw_flat
- *   T_cascade = c_cascade + T_levels + c_merge * B * Hq, where for a sequential plan
- *     T_levels = sum_g max(prefix_bytes_g / bw_prefix, prefix_flops_g / TC(M_eff_g))
- *                + suffix_bytes / bw_suffix
- *   and for a split plan (prefix items and suffix gather side by side, see
- *   gk_plan_summary.cascade_split), with C key tiles per item and n_gather SMs,
- *     T_levels = max(C * prefix_tile_us + prefix_item_us,
- *                    suffix_bytes / min(bw_suffix, n_gather * gather_sm))
- * TC is piecewise linear through the points (proportional below the first,
- * flat above the last).  Dense is chosen only when strictly faster.  Host only. */
+ *   T_cascade = c_cascade + T_levels + c_merge * B * Hq
+ * with C = gk_plan_summary.prefix_tiles_per_item key tiles per prefix item and
+ *   sequential plan (W = ceil(prefix_ctas / SMs) waves of prefix items):
+ *     T_levels = max(prefix_bytes / bw_prefix, W * (C * prefix_tile + prefix_item))
+ *                + c_gather + suffix_bytes / bw_suffix
+ *   split plan (see gk_plan_summary.cascade_split):
+ *     T_levels = max(C * prefix_tile + prefix_item,
+ *                    suffix_bytes / min(bw_suffix, suffix_ctas * gather_sm))
+ * A plan without prefix work has no prefix term.  GraniKV's M_eff (Eq. 2)
+ * enters through the items: a group of M_eff stacked rows gives ceil(M_eff/256)
+ * items per KV head and key split.  Dense is chosen only when strictly faster.
+ * Host only. */
 gk_status gk_dispatch(const gk_pool* pool, const gk_plan* plan, gk_backend* choice, double* t_dense_us,
                       double* t_cascade_us);
 gk_status gk_cost_model_set(gk_pool* pool, const gk_cost_model* cm);
@@ -295,8 +295,8 @@ gk_status gk_pool_set_cascade_mode(gk_pool* pool, gk_cascade_mode mode, int32_t 
 gk_status gk_cost_model_get(const gk_pool* pool, gk_cost_model* cm);
 /* Same as gk_cost_model_set from JSON text: {"c_flat_us": .., "bw_flat_gbs": ..,
  * "c_cascade_us": .., "bw_prefix_gbs": .., "bw_suffix_gbs": .., "c_merge_us": ..,
- * "prefix_tile_us": .., "prefix_item_us": .., "gather_sm_gbs": ..,
- * "tc_points": [[M, TFLOP/s], ...]}.  Keys left out keep their current values. */
+ * "prefix_tile_us": .., "prefix_item_us": .., "gather_sm_gbs": .., "c_gather_us": ..}.
+ * Keys left out keep their current values; other keys are skipped. */
 gk_status gk_cost_model_load(gk_pool* pool, const char* json);
 
 /* ---- device error word -------------------------------------------------------- */

@@ -1,4 +1,4 @@
-"""ORACLE (test infrastructure): the per-step backend choice.
+"""ORACLE (test infrastructure): the per-step backend choice and cascade arrangement.
 
 GraniKV Section 3.6, Eq. 2: M_eff(step) = B_step * n_q/kv, the M dimension of the
 stacked shared-prefix contraction.  The pages route on M_eff >= M_sat with an
@@ -9,44 +9,36 @@ predicted time runs (flat wins only when strictly faster):
 
   T_flat    = c_flat + bytes_flat / bw_flat
   T_cascade = c_cascade + T_levels + c_merge * B * Hq
-  T_levels  = sum_g max(bytes_pre_g / bw_prefix, flops_pre_g / TC(M_eff_g))
-              + bytes_suffix / bw_suffix                         (sequential plan)
-            = max(C * prefix_tile + prefix_item,
-                  bytes_suffix / min(bw_suffix, n_gather * gather_sm))   (split plan)
-  TC(M)     = piecewise-linear through the calibrated (M, TFLOP/s) points,
-              proportional to M below the first point, flat above the last.
+  item(C)   = C * prefix_tile + prefix_item        (one prefix work item of C key tiles)
+  T_levels  = max(bytes_pre / bw_prefix, W * item(C)) + c_gather
+              + bytes_suffix / bw_suffix                          (sequential plan)
+            = max(item(C), bytes_suffix / min(bw_suffix, n_gather * gather_sm))   (split plan)
 
-A split plan runs the prefix contraction on n_pre SMs (one work item of C
-128-key tiles each; a group contributes ceil(M/256) row blocks x Hkv heads x
-ceil(ceil(Lp/128)/C) items) beside the suffix gather on the n_gather SMs left.
-The planner takes the C with the smallest split prediction (the largest C among
-equal ones, i.e. the fewest items), among those that leave an SM for the
-gather, then lowers C to the smallest value giving as many items (balanced
-items), and splits when that beats the sequential T_levels.  The gather partition cuts the suffix tokens
+Work items: a group of M_eff stacked rows and Lp keys contributes ceil(M/256)
+row blocks x Hkv heads x ceil(ceil(Lp/128)/C) items, so M_eff enters through the
+item count.  A sequential plan runs them in W = ceil(items/SMs) waves over every
+SM, with C chosen to minimise W * (C + 2.5); then the gather runs over every SM
+as its own launch.  A split plan runs them on n_pre SMs beside the suffix
+gather on the n_gather SMs left, in one launch.  The planner takes the C with
+the smallest split prediction (the largest C among equal ones, i.e. the fewest
+items), among those that leave an SM for the gather, then lowers C to the
+smallest value giving as many items (balanced items), and splits when that
+beats the sequential T_levels.  The gather partition cuts the suffix tokens
 into quotas of ceil(total/n) rounded up to 64 and then to a multiple of 16, so
 it may use fewer CTAs than it was given.
 
-Times are in microseconds, bandwidths in GB/s (1 GB/s = 1e3 bytes per us),
-tensor throughput in TFLOP/s (1e6 flop per us).
+Times are in microseconds, bandwidths in GB/s (1 GB/s = 1e3 bytes per us).
 
 Parity of the choice itself is unpinned by the pages (their threshold is
 specific to the A100); Eq. 2 and the formula are pinned by closed forms.
 """
 from __future__ import annotations
 
+CTA_OVERHEAD_TILES = 2.5   # sequential key split: a CTA's set-up and epilogue, in tiles
+
 
 def m_eff(batch_requests: int, q_per_kv: int) -> int:
     return batch_requests * q_per_kv
-
-
-def tc_at(points, M):
-    pts = sorted((float(m), float(t)) for m, t in points)
-    if M <= pts[0][0]:
-        return pts[0][1] * M / pts[0][0]
-    for (m0, t0), (m1, t1) in zip(pts, pts[1:]):
-        if M <= m1:
-            return t0 + (t1 - t0) * (M - m0) / (m1 - m0)
-    return pts[-1][1]
 
 
 def features(prefix_lens, suffix_lens, group_of, Hq, Hkv, d):
@@ -77,48 +69,75 @@ def gather_ctas(tokens, n):
     return -(-tokens // quota)
 
 
-def sequential_levels(cm, f):
-    t = f["bytes_suffix"] / (cm["bw_suffix_gbs"] * 1e3)
-    for p in f["prefix"]:
-        t += max(p["bytes"] / (cm["bw_prefix_gbs"] * 1e3), p["flops"] / (tc_at(cm["tc_points"], p["M"]) * 1e6))
+def _tiles(f):
+    return [-(-p["M"] // 256) for p in f["prefix"]], [-(-p["lp"] // 128) for p in f["prefix"]]
+
+
+def n_items(f, C):
+    mtiles, ntiles = _tiles(f)
+    return sum(m * f["Hkv"] * -(-n // C) for m, n in zip(mtiles, ntiles))
+
+
+def sequential_tiles(f, num_sms):
+    """Key tiles per item of a sequential plan: the C minimising waves * (C + 2.5)."""
+    _, ntiles = _tiles(f)
+    best, best_c = None, max(ntiles)
+    for C in range(1, max(ntiles) + 1):
+        cost = -(-n_items(f, C) // num_sms) * (C + CTA_OVERHEAD_TILES)
+        if best is None or cost < best - 1e-9:
+            best, best_c = cost, C
+    return best_c
+
+
+def item_us(cm, C):
+    return C * cm["prefix_tile_us"] + cm["prefix_item_us"]
+
+
+def sequential_levels(cm, f, C, num_sms):
+    t = cm["c_gather_us"] + f["bytes_suffix"] / (cm["bw_suffix_gbs"] * 1e3)
+    if f["prefix"]:
+        waves = -(-n_items(f, C) // num_sms)
+        t += max(sum(p["bytes"] for p in f["prefix"]) / (cm["bw_prefix_gbs"] * 1e3), waves * item_us(cm, C))
     return t
 
 
 def split_levels(cm, f, C, n_gather):
     bw = min(cm["bw_suffix_gbs"], n_gather * cm["gather_sm_gbs"])
-    return max(C * cm["prefix_tile_us"] + cm["prefix_item_us"], f["bytes_suffix"] / (bw * 1e3))
+    return max(item_us(cm, C), f["bytes_suffix"] / (bw * 1e3))
 
 
 def arrangement(cm, f, num_sms):
     """-> dict(split, C, n_pre, n_gather): the planner's choice for the step."""
-    pre = f["prefix"]
-    ntiles = [-(-p["lp"] // 128) for p in pre]
-    mtiles = [-(-p["M"] // 256) for p in pre]
-    seq = dict(split=False, C=None, n_pre=None, n_gather=gather_ctas(f["suffix_tokens"], num_sms))
-    if not pre or f["suffix_tokens"] == 0:
+    if not f["prefix"]:
+        return dict(split=False, C=None, n_pre=0, n_gather=gather_ctas(f["suffix_tokens"], num_sms))
+    c_seq = sequential_tiles(f, num_sms)
+    seq = dict(split=False, C=c_seq, n_pre=n_items(f, c_seq), n_gather=gather_ctas(f["suffix_tokens"], num_sms))
+    if f["suffix_tokens"] == 0:
         return seq
     best, best_c = None, None
-    for C in range(max(ntiles), 0, -1):
-        items = sum(m * f["Hkv"] * -(-n // C) for m, n in zip(mtiles, ntiles))
+    for C in range(max(_tiles(f)[1]), 0, -1):
+        items = n_items(f, C)
         if items > num_sms - 1:
             break
         bw = min(cm["bw_suffix_gbs"], (num_sms - items) * cm["gather_sm_gbs"])
-        t = max(C * cm["prefix_tile_us"] + cm["prefix_item_us"], f["bytes_suffix"] / (bw * 1e3))
+        t = max(item_us(cm, C), f["bytes_suffix"] / (bw * 1e3))
         if best is None or t < best - 1e-9:
             best, best_c = t, C
-    if best is None or not best < sequential_levels(cm, f):
+    if best is None or not best < sequential_levels(cm, f, c_seq, num_sms):
         return seq
-    n_pre = sum(m * f["Hkv"] * -(-n // best_c) for m, n in zip(mtiles, ntiles))
-    while best_c > 1 and sum(m * f["Hkv"] * -(-n // (best_c - 1)) for m, n in zip(mtiles, ntiles)) == n_pre:
+    n_pre = n_items(f, best_c)
+    while best_c > 1 and n_items(f, best_c - 1) == n_pre:
         best_c -= 1
-    return dict(split=True, C=min(best_c, max(ntiles)), n_pre=n_pre,
-                n_gather=gather_ctas(f["suffix_tokens"], num_sms - n_pre))
+    return dict(split=True, C=best_c, n_pre=n_pre, n_gather=gather_ctas(f["suffix_tokens"], num_sms - n_pre))
 
 
 def predict(cm, f, num_sms=152):
     t_flat = cm["c_flat_us"] + f["bytes_flat"] / (cm["bw_flat_gbs"] * 1e3)
     a = arrangement(cm, f, num_sms)
-    t_levels = split_levels(cm, f, a["C"], a["n_gather"]) if a["split"] else sequential_levels(cm, f)
+    if a["split"]:
+        t_levels = split_levels(cm, f, a["C"], a["n_gather"])
+    else:
+        t_levels = sequential_levels(cm, f, a["C"], num_sms)
     t_cas = cm["c_cascade_us"] + t_levels + cm["c_merge_us"] * f["B"] * f["Hq"]
     return t_flat, t_cas
 

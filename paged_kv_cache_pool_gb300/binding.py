@@ -58,8 +58,7 @@ class gk_plan_summary(ctypes.Structure):
 class gk_cost_model(ctypes.Structure):
     _fields_ = [("c_flat_us", c_dbl), ("bw_flat_gbs", c_dbl), ("c_cascade_us", c_dbl), ("bw_prefix_gbs", c_dbl),
                 ("bw_suffix_gbs", c_dbl), ("c_merge_us", c_dbl), ("prefix_tile_us", c_dbl), ("prefix_item_us", c_dbl),
-                ("gather_sm_gbs", c_dbl), ("n_tc_points", c_i32), ("reserved0", c_i32),
-                ("tc_m", c_dbl * 16), ("tc_tflops", c_dbl * 16)]
+                ("gather_sm_gbs", c_dbl), ("c_gather_us", c_dbl)]
 
 
 P = ctypes.POINTER
@@ -355,25 +354,17 @@ def gk_dispatch(pool, plan):
 def gk_cost_model_get(pool):
     cm = gk_cost_model()
     _check(lib().gk_cost_model_get(pool, ctypes.byref(cm)), pool)
-    n = cm.n_tc_points
-    d = {k: getattr(cm, k) for k in COST_MODEL_KEYS}
-    d["tc_points"] = [[cm.tc_m[i], cm.tc_tflops[i]] for i in range(n)]
-    return d
+    return {k: getattr(cm, k) for k in COST_MODEL_KEYS}
 
 
 COST_MODEL_KEYS = ("c_flat_us", "bw_flat_gbs", "c_cascade_us", "bw_prefix_gbs", "bw_suffix_gbs", "c_merge_us",
-                   "prefix_tile_us", "prefix_item_us", "gather_sm_gbs")
+                   "prefix_tile_us", "prefix_item_us", "gather_sm_gbs", "c_gather_us")
 
 
 def gk_cost_model_set(pool, cm: dict):
     c = gk_cost_model()
     for k in COST_MODEL_KEYS:
         setattr(c, k, float(cm[k]))
-    pts = cm["tc_points"]
-    c.n_tc_points = len(pts)
-    for i, (m, t) in enumerate(pts):
-        c.tc_m[i] = m
-        c.tc_tflops[i] = t
     _check(lib().gk_cost_model_set(pool, ctypes.byref(c)), pool)
 
 

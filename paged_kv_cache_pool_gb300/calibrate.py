@@ -3,12 +3,12 @@ routing rule stays, its numbers are re-fit per GPU; Appendix B.4b's sweep).
 
 Times, with CUDA events, on one layer of synthetic pools (random bf16 data):
   * the flat backend over several (B, Lp, s)              -> c_flat_us, bw_flat_gbs
-  * the suffix gather over every SM, several volumes        -> bw_suffix_gbs
-  * the prefix kernel at M_eff = B * g from 32 to 2048      -> tc_points (achieved TFLOP/s)
-  * split plans forced to C key tiles per item: the prefix  -> prefix_item_us + C * prefix_tile_us
-    items alone, and the gather alone on the SMs left       -> gather_sm_gbs
+  * the suffix gather over every SM, several volumes        -> c_gather_us + bytes / bw_suffix_gbs
+  * prefix items of C key tiles, forced split plans and the -> prefix_item_us + C * prefix_tile_us
+    sequential plans of several M_eff = B * g
+  * the gather alone on the SMs a split plan leaves it      -> gather_sm_gbs
   * the merge                                               -> c_merge_us per (request, head)
-  * the whole cascade                                       -> c_cascade_us (mean residual)
+  * the whole cascade, both arrangements                    -> c_cascade_us (mean residual)
 and writes the JSON that gk_cost_model_load reads.
 
     python -m paged_kv_cache_pool_gb300.calibrate --out cost_model_gb300.json
@@ -84,24 +84,20 @@ def calibrate(Hq=32, Hkv=8, d=128, device="cuda"):
     kv_tok = 2 * Hkv * d * 2
 
     flat_pts, suf_pts, cas_pts, merge_pts = [], [], [], []
-    tc_points, tile_pts, sm_pts = [], [], []
-    kv_tok = 2 * Hkv * d * 2
+    tile_pts, sm_pts = [], []
     for B, lp, s in [(8, 2048, 256), (32, 4096, 512), (64, 16384, 1024), (128, 8192, 512), (256, 4096, 1024)]:
         c = _Case(eng, B, lp, s, Hq, d)
         t_flat = _time(lambda: gk.gk_decode_dense(pool, None, 0, c.batch, c.plan))
+        t_pre = _time(lambda: gk.gk_cascade_prefix(pool, None, 0, c.batch, c.plan))
         t_suf = _time(lambda: gk.gk_cascade_suffix(pool, None, 0, c.batch, c.plan))
         t_mrg = _time(lambda: gk.gk_cascade_merge(pool, None, 0, c.batch, c.plan))
         t_cas = _time(lambda: gk.gk_decode_cascade(pool, None, 0, c.batch, c.plan))
         flat_pts.append((c.info["dense_bytes"], t_flat))
         suf_pts.append((c.info["suffix_bytes"], t_suf))
         merge_pts.append((B * Hq, t_mrg))
+        if c.info["prefix_ctas"] <= 152:   # one wave of items
+            tile_pts.append((c.info["prefix_tiles_per_item"], t_pre))
         cas_pts.append((dict(c.info), t_cas, B))
-        c.close()
-    # prefix throughput against M_eff at a fixed long prefix
-    for B in (8, 16, 32, 64, 128, 256, 512):
-        c = _Case(eng, B, 8192, 0, Hq, d)
-        t_pre = _time(lambda: gk.gk_cascade_prefix(pool, None, 0, c.batch, c.plan))
-        tc_points.append([float(B * g), c.info["prefix_flops"] / (t_pre * 1e-6) / 1e12])
         c.close()
     # split plans: prefix items of C tiles alone, and the gather alone on the SMs left
     for C in (16, 32, 64, 128):
@@ -117,13 +113,11 @@ def calibrate(Hq=32, Hkv=8, d=128, device="cuda"):
     eng.close()
     torch.cuda.synchronize()
 
+    keep = ("max_m_eff", "prefix_bytes", "prefix_ctas", "suffix_bytes", "suffix_ctas", "cascade_split",
+            "prefix_tiles_per_item")
     return refit(dict(flat=flat_pts, suffix=suf_pts, merge=merge_pts, tile=tile_pts, gather_sm=sm_pts,
-                      cascade=[(i["max_m_eff"], t) for i, t, _ in cas_pts],
-                      cascade_info=[dict(max_m_eff=i["max_m_eff"], prefix_bytes=i["prefix_bytes"],
-                                         prefix_flops=i["prefix_flops"], suffix_bytes=i["suffix_bytes"], B=B,
-                                         Hq=Hq, split=i["cascade_split"], tiles=i["prefix_tiles_per_item"],
-                                         suffix_ctas=i["suffix_ctas"]) for i, _, B in cas_pts],
-                      tc_points=tc_points))
+                      cascade=[t for _, t, _ in cas_pts],
+                      cascade_info=[dict({k: i[k] for k in keep}, B=B, Hq=Hq) for i, _, B in cas_pts]))
 
 
 def _linfit(pts):
@@ -134,36 +128,33 @@ def _linfit(pts):
     return max(0.0, float(c0)), float(slope)
 
 
-def refit(measured):
+def refit(measured, num_sms=152):
     """Cost-model coefficients from the measured points (intercepts are fixed costs)."""
     c_flat, s_flat = _linfit(measured["flat"])
     c_suf, s_suf = _linfit(measured["suffix"])
     c_mrg, s_mrg = _linfit(measured["merge"])
-    tc_points = sorted([list(p) for p in measured["tc_points"]])
+    item, tile = _linfit(measured["tile"])
     cm = dict(c_flat_us=c_flat, bw_flat_gbs=1.0 / max(s_flat, 1e-12) / 1e3, c_cascade_us=0.0,
               bw_prefix_gbs=6000.0, bw_suffix_gbs=1.0 / max(s_suf, 1e-12) / 1e3, c_merge_us=max(s_mrg, 0.0),
-              prefix_tile_us=1.65, prefix_item_us=10.5, gather_sm_gbs=44.0, tc_points=tc_points)
-    if len(measured.get("tile", [])) >= 2:
-        item, tile = _linfit(measured["tile"])
-        cm["prefix_tile_us"], cm["prefix_item_us"] = max(tile, 1e-3), item
+              prefix_tile_us=max(tile, 1e-3), prefix_item_us=item, gather_sm_gbs=44.0, c_gather_us=c_suf)
     # per-SM gather bandwidth: points whose SMs stay well below the all-SM bandwidth
-    per_sm = [bw / n for n, bw in measured.get("gather_sm", []) if n * 50.0 < cm["bw_suffix_gbs"]]
+    per_sm = [bw / n for n, bw in measured["gather_sm"] if n * 50.0 < cm["bw_suffix_gbs"]]
     if per_sm:
         cm["gather_sm_gbs"] = float(np.median(per_sm))
-    # the cascade's fixed cost: the suffix and merge launches' intercepts, plus the mean
-    # residual of the whole cascade over that model when it is positive
-    base = c_suf + c_mrg
+    # the cascade's fixed cost: the merge launch's intercept plus the mean residual
+    # of the whole cascade over the model when it is positive
     res = []
-    for info, (_, t_cas) in zip(measured["cascade_info"], measured["cascade"]):
-        if info.get("split"):
+    for info, t_cas in zip(measured["cascade_info"], measured["cascade"]):
+        item_us = info["prefix_tiles_per_item"] * cm["prefix_tile_us"] + cm["prefix_item_us"]
+        if info["cascade_split"]:
             bw = min(cm["bw_suffix_gbs"], info["suffix_ctas"] * cm["gather_sm_gbs"])
-            levels = max(info["tiles"] * cm["prefix_tile_us"] + cm["prefix_item_us"], info["suffix_bytes"] / (bw * 1e3))
+            levels = max(item_us, info["suffix_bytes"] / (bw * 1e3))
         else:
-            tc = float(np.interp(info["max_m_eff"], [p[0] for p in tc_points], [p[1] for p in tc_points]))
-            levels = (max(info["prefix_bytes"] / (cm["bw_prefix_gbs"] * 1e3), info["prefix_flops"] / (tc * 1e6))
-                      + info["suffix_bytes"] / (cm["bw_suffix_gbs"] * 1e3))
-        res.append(t_cas - (base + levels + cm["c_merge_us"] * info["B"] * info["Hq"]))
-    cm["c_cascade_us"] = base + max(0.0, float(np.mean(res)))
+            waves = -(-info["prefix_ctas"] // num_sms)
+            levels = (max(info["prefix_bytes"] / (cm["bw_prefix_gbs"] * 1e3), waves * item_us) if info["prefix_ctas"] else 0.0)
+            levels += cm["c_gather_us"] + info["suffix_bytes"] / (cm["bw_suffix_gbs"] * 1e3)
+        res.append(t_cas - (c_mrg + levels + cm["c_merge_us"] * info["B"] * info["Hq"]))
+    cm["c_cascade_us"] = c_mrg + max(0.0, float(np.mean(res)))
     cm["measured"] = measured
     return cm
 

@@ -218,10 +218,7 @@ gk_status gk_pool_create(const gk_pool_config* cfg, gk_pool** out) {
   cm.prefix_tile_us = 1.65;
   cm.prefix_item_us = 10.5;
   cm.gather_sm_gbs = 44.0;
-  cm.n_tc_points = 3;
-  cm.tc_m[0] = 128; cm.tc_tflops[0] = 300;
-  cm.tc_m[1] = 512; cm.tc_tflops[1] = 700;
-  cm.tc_m[2] = 1024; cm.tc_tflops[2] = 900;
+  cm.c_gather_us = 10.0;
   *out = p;
   return GK_OK;
 }

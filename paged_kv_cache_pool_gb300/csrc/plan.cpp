@@ -16,8 +16,6 @@
 
 namespace gk {
 
-static double tc_at(const gk_cost_model& cm, double M);
-
 namespace {
 
 constexpr int kGatherQuantum = 16;        // gather CTAs get token quotas in multiples of this
@@ -154,7 +152,9 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   // the other SMs gather the suffix, in one launch.  Predicted
   //   T_split(C) = max(C * prefix_tile_us + prefix_item_us,
   //                    S / min(bw_suffix, (SMs - n_pre) * gather_sm)),
-  // against T_seq = sum_g max(bytes_g / bw_prefix, flops_g / TC(M_g)) + S / bw_suffix.
+  // against the sequential arrangement's W waves of c_seq-tile items:
+  //   T_seq = max(prefix_bytes / bw_prefix, W * (c_seq * prefix_tile_us + prefix_item_us))
+  //           + c_gather + S / bw_suffix.
   // The split is taken when some C is predicted faster than the sequential
   // arrangement; among equal predictions the fewest items (fewest partials)
   // win, and the chosen item count is then spread evenly over the key tiles.
@@ -163,12 +163,14 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   int64_t suffix_tokens = 0;
   for (int32_t r = 0; r < B; ++r) suffix_tokens += pl->reqs[(size_t)r].slen;
   const double S = (double)suffix_tokens * (double)kv_tok;
-  double t_seq = S / (cm.bw_suffix_gbs * 1e3);
-  for (int32_t gi = 0; gi < G; ++gi) {
-    const double lp = (double)pl->reqs[(size_t)members[(size_t)gi][0]].lp;
-    const double tb = lp * (double)kv_tok / (cm.bw_prefix_gbs * 1e3);
-    const double tf = 4.0 * (double)members[(size_t)gi].size() * Hq * lp * d / (tc_at(cm, (double)members[(size_t)gi].size() * g) * 1e6);
-    t_seq += std::max(tb, tf);
+  double t_seq = S / (cm.bw_suffix_gbs * 1e3) + cm.c_gather_us;
+  if (G > 0) {
+    double prefix_bytes = 0.0;
+    for (int32_t gi = 0; gi < G; ++gi)
+      prefix_bytes += (double)pl->reqs[(size_t)members[(size_t)gi][0]].lp * (double)kv_tok;
+    const double waves = (double)((n_items(c_seq) + num_sms - 1) / num_sms);
+    t_seq += std::max(prefix_bytes / (cm.bw_prefix_gbs * 1e3),
+                      waves * (std::min(c_seq, max_ntiles) * cm.prefix_tile_us + cm.prefix_item_us));
   }
   int32_t c_split = 0;
   double t_split = 1e300;
@@ -405,23 +407,10 @@ static void free_plan_buffers(Plan* pl) {
 }
 
 // ---- cost model ----------------------------------------------------------------
-static double tc_at(const gk_cost_model& cm, double M) {
-  int n = cm.n_tc_points;
-  if (M <= cm.tc_m[0]) return cm.tc_tflops[0] * M / cm.tc_m[0];
-  for (int i = 0; i + 1 < n; ++i)
-    if (M <= cm.tc_m[i + 1])
-      return cm.tc_tflops[i] + (cm.tc_tflops[i + 1] - cm.tc_tflops[i]) * (M - cm.tc_m[i]) / (cm.tc_m[i + 1] - cm.tc_m[i]);
-  return cm.tc_tflops[n - 1];
-}
-
 static bool valid_cost_model(const gk_cost_model& cm) {
-  if (cm.n_tc_points < 1 || cm.n_tc_points > 16) return false;
   if (!(cm.bw_flat_gbs > 0 && cm.bw_prefix_gbs > 0 && cm.bw_suffix_gbs > 0)) return false;
   if (!(cm.prefix_tile_us > 0 && cm.prefix_item_us >= 0 && cm.gather_sm_gbs > 0)) return false;
-  for (int i = 0; i < cm.n_tc_points; ++i) {
-    if (!(cm.tc_m[i] > 0 && cm.tc_tflops[i] > 0)) return false;
-    if (i && !(cm.tc_m[i] > cm.tc_m[i - 1])) return false;
-  }
+  if (!(cm.c_flat_us >= 0 && cm.c_cascade_us >= 0 && cm.c_merge_us >= 0 && cm.c_gather_us >= 0)) return false;
   return true;
 }
 
@@ -530,17 +519,18 @@ gk_status gk_dispatch(const gk_pool* pool, const gk_plan* plan, gk_backend* choi
   const Plan& pl = plan->impl;
   double t_flat = cm.c_flat_us + (double)pl.summary.dense_bytes / (cm.bw_flat_gbs * 1e3);
   double t_levels = 0.0;
+  const gk_plan_summary& sm = pl.summary;
+  const double item = sm.prefix_tiles_per_item * cm.prefix_tile_us + cm.prefix_item_us;
   if (pl.split) {
-    const double bw = std::min(cm.bw_suffix_gbs, (double)pl.summary.suffix_ctas * cm.gather_sm_gbs);
-    t_levels = std::max(pl.summary.prefix_tiles_per_item * cm.prefix_tile_us + cm.prefix_item_us,
-                        (double)pl.summary.suffix_bytes / (bw * 1e3));
+    const double bw = std::min(cm.bw_suffix_gbs, (double)sm.suffix_ctas * cm.gather_sm_gbs);
+    t_levels = std::max(item, (double)sm.suffix_bytes / (bw * 1e3));
   } else {
-    for (size_t gi = 0; gi < pl.groups.size(); ++gi) {
-      double tb = (double)pl.group_bytes[gi] / (cm.bw_prefix_gbs * 1e3);
-      double tf = (double)pl.group_flops[gi] / (gk::tc_at(cm, (double)pl.groups[gi].m) * 1e6);
-      t_levels += std::max(tb, tf);
+    if (sm.prefix_ctas > 0) {
+      const int num_sms = pool->impl.dev.num_sms;
+      const double waves = (double)((sm.prefix_ctas + num_sms - 1) / num_sms);
+      t_levels = std::max((double)sm.prefix_bytes / (cm.bw_prefix_gbs * 1e3), waves * item);
     }
-    t_levels += (double)pl.summary.suffix_bytes / (cm.bw_suffix_gbs * 1e3);
+    t_levels += cm.c_gather_us + (double)sm.suffix_bytes / (cm.bw_suffix_gbs * 1e3);
   }
   double t_cas = cm.c_cascade_us + t_levels + cm.c_merge_us * (double)pl.B * pool->impl.cfg.num_q_heads;
   *choice = t_flat < t_cas ? GK_BACKEND_DENSE : GK_BACKEND_CASCADE;
@@ -586,25 +576,9 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
     std::string key;
     if (!rd.str(&key)) return bad("expected a key");
     if (!rd.eat(':')) return bad("expected ':'");
-    if (key == "tc_points") {
-      if (!rd.eat('[')) return bad("tc_points must be an array");
-      int n = 0;
-      while (!rd.eat(']')) {
-        if (n && !rd.eat(',')) return bad("expected ',' in tc_points");
-        if (n >= 16) return bad("at most 16 tc_points");
-        double m, t;
-        if (!rd.eat('[') || !rd.num(&m) || !rd.eat(',') || !rd.num(&t) || !rd.eat(']'))
-          return bad("tc_points entries are [M, TFLOP/s]");
-        cm.tc_m[n] = m;
-        cm.tc_tflops[n] = t;
-        ++n;
-      }
-      cm.n_tc_points = n;
-      continue;
-    }
     static const char* kNumeric[] = {"c_flat_us",      "bw_flat_gbs",    "c_cascade_us",  "bw_prefix_gbs",
                                      "bw_suffix_gbs",  "c_merge_us",     "prefix_tile_us", "prefix_item_us",
-                                     "gather_sm_gbs"};
+                                     "gather_sm_gbs",  "c_gather_us"};
     bool known = false;
     for (const char* k : kNumeric) known = known || key == k;
     if (!known) {
@@ -622,6 +596,7 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
     else if (key == "prefix_tile_us") cm.prefix_tile_us = v;
     else if (key == "prefix_item_us") cm.prefix_item_us = v;
     else if (key == "gather_sm_gbs") cm.gather_sm_gbs = v;
+    else if (key == "c_gather_us") cm.c_gather_us = v;
   }
   return gk_cost_model_set(pool, &cm);
 }

@@ -238,15 +238,13 @@ def test_dispatch_matches_oracle_formula(gk, case):
     cm = dict(c_flat_us=rnd.uniform(2, 20), bw_flat_gbs=rnd.uniform(3000, 7000), c_cascade_us=rnd.uniform(5, 40),
               bw_prefix_gbs=rnd.uniform(3000, 7000), bw_suffix_gbs=rnd.uniform(3000, 7000),
               c_merge_us=rnd.uniform(0, 0.002), prefix_tile_us=rnd.uniform(0.5, 3.0),
-              prefix_item_us=rnd.uniform(0, 20), gather_sm_gbs=rnd.uniform(20, 80),
-              tc_points=[[128, rnd.uniform(100, 400)], [512, rnd.uniform(400, 900)], [2048, rnd.uniform(900, 1600)]])
+              prefix_item_us=rnd.uniform(0, 20), gather_sm_gbs=rnd.uniform(20, 80), c_gather_us=rnd.uniform(0, 20))
     pool = gk.gk_pool_create(1, Hq, Hkv, d, 200000, 64, 1, 0)
     try:
         gk.gk_cost_model_load(pool, json.dumps(cm))
         got_cm = gk.gk_cost_model_get(pool)
         for k in gk.COST_MODEL_KEYS:
             assert got_cm[k] == cm[k]
-        assert got_cm["tc_points"] == cm["tc_points"]
         n_pref = rnd.randint(0, 3)
         pref = [(gk.gk_prefix_alloc(pool, lp), lp) for lp in [rnd.randint(64, 20000) for _ in range(n_pref)]]
         B = rnd.randint(1, 300)
@@ -277,8 +275,8 @@ def test_dispatch_matches_oracle_formula(gk, case):
 def test_cost_model_json_rejects_bad_input(gk):
     pool = _pool(gk)
     try:
-        for bad in ["", "[1]", '{"c_flat_us": }', '{"tc_points": [[1]]}', '{"bw_flat_gbs": -1}',
-                    '{"tc_points": [[512, 1], [128, 2]]}']:
+        for bad in ["", "[1]", '{"c_flat_us": }', '{"prefix_tile_us": 0}', '{"bw_flat_gbs": -1}',
+                    '{"c_gather_us": -1}', '{"gather_sm_gbs": "fast"}']:
             with pytest.raises(gk.GkError) as e:
                 gk.gk_cost_model_load(pool, bad)
             assert e.value.status == gk.GK_ERR_INVALID

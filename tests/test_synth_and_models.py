@@ -82,30 +82,22 @@ def test_eq2_meff_and_a100_threshold_rows():
         assert ("dense" if m >= g["m_sat_a100"] else "cascade") == route
 
 
-def test_tc_curve_closed_form():
-    pts = [[128, 400.0], [512, 1200.0], [1024, 1500.0]]
-    assert dispatch.tc_at(pts, 64) == 200.0
-    assert dispatch.tc_at(pts, 128) == 400.0
-    assert dispatch.tc_at(pts, 320) == 800.0
-    assert dispatch.tc_at(pts, 768) == 1350.0
-    assert dispatch.tc_at(pts, 4096) == 1500.0
-
-
 def test_cost_model_closed_form():
-    # prefix tiles so slow that the split arrangement never wins: the sequential formula
-    cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0,
-              tc_points=[[128, 500.0], [1024, 1500.0]], bw_suffix_gbs=4000.0, c_merge_us=0.001,
-              prefix_tile_us=1e6, prefix_item_us=0.0, gather_sm_gbs=50.0)
-    # one group of 64 requests (g = 4 -> M = 256), Lp = 1000, suffixes 100 each, Hkv = 8, d = 128
+    # the gather on a few SMs so slow that the split arrangement never wins: the sequential formula
+    cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0, bw_suffix_gbs=4000.0,
+              c_merge_us=0.001, prefix_tile_us=2.0, prefix_item_us=3.0, gather_sm_gbs=1.0, c_gather_us=4.0)
+    # one group of 64 requests (g = 4 -> M = 256: one row block), Lp = 1000 (8 key tiles),
+    # suffixes 100 each, Hkv = 8, d = 128
     f = dispatch.features([1000] * 64, [100] * 64, [0] * 64, 32, 8, 128)
     kv = 2 * 8 * 128 * 2
     assert f["bytes_flat"] == 64 * 1100 * kv and f["bytes_suffix"] == 64 * 100 * kv
     assert f["prefix"] == [dict(M=256, bytes=1000 * kv, flops=4 * 64 * 32 * 1000 * 128, lp=1000)]
+    # sequential key split: waves * (C + 2.5) is 3.5 at C = 1 (64 items, one wave)
+    assert dispatch.sequential_tiles(f, 152) == 1 and dispatch.n_items(f, 1) == 64
     t_flat, t_cas = dispatch.predict(cm, f)
     assert math.isclose(t_flat, 5.0 + 64 * 1100 * kv / 4e6)
-    tc = 500.0 + 1000.0 * (256 - 128) / (1024 - 128)
-    t_pre = max(1000 * kv / 5e6, 4 * 64 * 32 * 1000 * 128 / (tc * 1e6))
-    assert math.isclose(t_cas, 10.0 + t_pre + 64 * 100 * kv / 4e6 + 0.001 * 64 * 32)
+    t_levels = max(1000 * kv / 5e6, 1 * (1 * 2.0 + 3.0)) + 4.0 + 64 * 100 * kv / 4e6
+    assert math.isclose(t_cas, 10.0 + t_levels + 0.001 * 64 * 32)
     assert dispatch.choose(cm, f)[0] == ("dense" if t_flat < t_cas else "cascade")
     assert not dispatch.arrangement(cm, f, 152)["split"]
     # a request without a HOT prefix counts only toward the flat and suffix bytes
@@ -115,13 +107,13 @@ def test_cost_model_closed_form():
 
 def test_split_arrangement_worked_example():
     """One group of 64 requests (g = 4 -> one 256-row block), Lp = 16384 (128 key tiles),
-    Hkv = 8, 1000 suffix tokens each; tile 1 us, item 5 us, 50 GB/s per SM, 6000 GB/s.
+    Hkv = 8, 1000 suffix tokens each; tile 1 us, item 5 us, 50 GB/s per SM, 6000 GB/s,
+    4 us for a separate gather launch.
     Items(C) = 8 * ceil(128 / C); T(C) = max(C + 5, S / min(6000, (152 - items) * 50)).
     C = 32..38 leave 120 SMs (S / 6000 GB/s = 43.69 us binds); the largest, 38, wins the
     scan, and 32 is the fewest tiles per item that still gives its 32 items."""
-    cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0,
-              tc_points=[[128, 500.0], [1024, 1500.0]], bw_suffix_gbs=6000.0, c_merge_us=0.001,
-              prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0)
+    cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0, bw_suffix_gbs=6000.0,
+              c_merge_us=0.001, prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0, c_gather_us=4.0)
     f = dispatch.features([16384] * 64, [1000] * 64, [0] * 64, 32, 8, 128)
     S = 64 * 1000 * 4096
     assert f["bytes_suffix"] == S
@@ -131,10 +123,11 @@ def test_split_arrangement_worked_example():
     assert dispatch.gather_ctas(64000, 120) == 118
     t_flat, t_cas = dispatch.predict(cm, f, 152)
     assert math.isclose(t_cas, 10.0 + max(32 + 5.0, S / (118 * 50.0 * 1e3)) + 0.001 * 64 * 32)
-    # the sequential alternative it beat: suffix at 6000 GB/s plus the prefix at TC(256)
-    tc = 500.0 + 1000.0 * (256 - 128) / (1024 - 128)
-    t_seq = S / 6e6 + max(16384 * 4096 / 5e6, 4 * 64 * 32 * 16384 * 128 / (tc * 1e6))
-    assert math.isclose(dispatch.sequential_levels(cm, f), t_seq) and t_seq > 43.69
+    # the sequential alternative it beat: C = 7 (152 items, one wave: waves * (C + 2.5) = 9.5
+    # against 10.5 at C = 8 and 17 at C = 6), the prefix bound by its 67 MB of reads
+    assert dispatch.sequential_tiles(f, 152) == 7 and dispatch.n_items(f, 7) == 152
+    t_seq = max(16384 * 4096 / 5e6, 7 * 1.0 + 5.0) + 4.0 + S / 6e6
+    assert math.isclose(dispatch.sequential_levels(cm, f, 7, 152), t_seq) and t_seq > 43.69
     # no suffix, or no shared prefix: never split
     assert not dispatch.arrangement(cm, dispatch.features([16384] * 64, [0] * 64, [0] * 64, 32, 8, 128), 152)["split"]
     assert not dispatch.arrangement(cm, dispatch.features([0] * 64, [1000] * 64, [-1] * 64, 32, 8, 128), 152)["split"]
