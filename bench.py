@@ -125,8 +125,14 @@ def source_sha256(files):
     return h.hexdigest()
 
 
-def _profile_traffic(kernel_tag, src_files):
-    """dram bytes per launch from the committed ncu summary, if the kernel sources are unchanged."""
+PROFILED_WORKLOAD = "llama8b_32L_lp16384_b64"   # the workload the committed ncu summaries cover
+
+
+def _profile_traffic(kernel_tag, src_files, workload=PROFILED_WORKLOAD):
+    """dram bytes per launch from the committed ncu summary, if it covers this workload and
+    the kernel sources are unchanged."""
+    if not workload.startswith(PROFILED_WORKLOAD):
+        return None
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
     try:
         text = open(path).read()
@@ -399,12 +405,13 @@ def run_ours(a, w):
     kd = kernels[dom]
     if dom == "cascade_levels" and kd["flops"] / kd["bytes"] > tc_peak * 1e3 / hbm:
         roof = {"kernel": dom, "bound": "tensor", "achieved": kd["tflops"], "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": kd["tflops"] / tc_peak, "traffic": _profile_traffic("cascade_levels_llama8b_lp16384_b64", LEVELS_SRC)}
+                "frac": kd["tflops"] / tc_peak,
+                "traffic": _profile_traffic("cascade_levels_llama8b_lp16384_b64", LEVELS_SRC, w.name)}
     else:
         tag = {"cascade_levels": ("cascade_levels_llama8b_lp16384_b64", LEVELS_SRC),
                "dense_gather": ("dense_gather_llama8b_lp16384_b64", GATHER_SRC)}[dom]
         roof = {"kernel": dom, "bound": "hbm", "achieved": kd["gbs"], "peak": hbm, "unit": "GB/s",
-                "frac": kd["gbs"] / hbm, "traffic": _profile_traffic(*tag)}
+                "frac": kd["gbs"] / hbm, "traffic": _profile_traffic(*tag, w.name)}
     roof["peak_source"] = f"{peak_src} ({'bf16_tflops_sustained' if roof['bound'] == 'tensor' else 'hbm_gbs'})"
 
     # ---- e2e: host buffers, copies inside the timed region ----
