@@ -65,6 +65,25 @@ def _dist():
     return rank, world, local
 
 
+def max_over_ranks(x):
+    """The largest of the ranks' values (the job's time for N replicas timed side by
+    side); x itself when the process runs alone.  Works over NCCL or gloo."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], device=dev, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, units_per_replica, elapsed_ms):
+    """Whole-job throughput of `world` replicas that each processed `units_per_replica`
+    in at most `elapsed_ms` (the max over ranks)."""
+    return world * units_per_replica / (elapsed_ms / 1e3)
+
+
 class Clocks:
     """nvidia-smi samples taken while the timed region runs."""
 
@@ -360,12 +379,9 @@ def run_ours(a, w):
     if err:
         raise RuntimeError(f"device error word {err} in the timed region")
     step_choices = choices[n_choice0:]
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms)
     ms_per_step = elapsed_ms / a.steps
-    value = world * B * L * a.steps / (elapsed_ms / 1e3)
+    value = replica_throughput(world, B * L * a.steps, elapsed_ms)
 
     # per-kernel averages over the timed region
     k_ms = {"append": [], "levels": [], "merge": [], "dense": []}
@@ -447,14 +463,10 @@ def run_ours(a, w):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(e0.elapsed_time(e1))
         h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + B * 8 + B * max_blocks * 4
         d2h = ho.numel() * 4 + hl.numel() * 4
-        e2e = {"value": world * B * L * a.steps / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": replica_throughput(world, B * L * a.steps, ems), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ems / a.steps}
 
     if rank != 0:
