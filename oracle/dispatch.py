@@ -12,20 +12,24 @@ predicted time runs (flat wins only when strictly faster):
   item(C)   = C * prefix_tile + prefix_item        (one prefix work item of C key tiles)
   T_levels  = max(bytes_pre / bw_prefix, W * item(C)) + c_gather
               + bytes_suffix / bw_suffix                          (sequential plan)
-            = max(item(C), bytes_suffix / min(bw_suffix, n_gather * gather_sm))   (split plan)
+            = max(item(C), (bytes_suffix / gather_sm + n_pre * item(C)) / SMs,
+                  (bytes_suffix + bytes_pre) / bw_suffix)          (split plan)
 
 Work items: a group of M_eff stacked rows and Lp keys contributes ceil(M/256)
 row blocks x Hkv heads x ceil(ceil(Lp/128)/C) items, so M_eff enters through the
 item count.  A sequential plan runs them in W = ceil(items/SMs) waves over every
 SM, with C chosen to minimise W * (C + 2.5); then the gather runs over every SM
-as its own launch.  A split plan runs them on n_pre SMs beside the suffix
-gather on the n_gather SMs left, in one launch.  The planner takes the C with
-the smallest split prediction (the largest C among equal ones, i.e. the fewest
-items), among those that leave an SM for the gather, then lowers C to the
-smallest value giving as many items (balanced items), and splits when that
-beats the sequential T_levels.  The gather partition cuts the suffix tokens
-into quotas of ceil(total/n) rounded up to 64 and then to a multiple of 16, so
-it may use fewer CTAs than it was given.
+as its own launch.  A split plan is one launch with a CTA per SM: CTA b < n_pre
+first runs prefix item b, and every CTA gathers a slot of the suffix, a prefix
+CTA's slot cut to the time its item leaves (the middle term spreads the
+gather's SM-time and the items over all SMs; the last is HBM).  The planner
+takes the C with the smallest split prediction (the largest C among equal
+ones, i.e. the fewest items), among those with no more items than SMs, then
+lowers C to the smallest value giving as many items (balanced items), and
+splits when that beats the sequential T_levels.  A sequential plan's gather
+partition cuts the suffix tokens into quotas of ceil(total/n) rounded up to 64
+and then to a multiple of 16, so it may use fewer CTAs than SMs; a split
+plan's has one slot per SM.
 
 Times are in microseconds, bandwidths in GB/s (1 GB/s = 1e3 bytes per us).
 
@@ -101,9 +105,11 @@ def sequential_levels(cm, f, C, num_sms):
     return t
 
 
-def split_levels(cm, f, C, n_gather):
-    bw = min(cm["bw_suffix_gbs"], n_gather * cm["gather_sm_gbs"])
-    return max(item_us(cm, C), f["bytes_suffix"] / (bw * 1e3))
+def split_levels(cm, f, C, n_pre, num_sms):
+    it = item_us(cm, C)
+    bytes_pre = sum(p["bytes"] for p in f["prefix"])
+    bal = (f["bytes_suffix"] / (cm["gather_sm_gbs"] * 1e3) + n_pre * it) / num_sms
+    return max(it, bal, (f["bytes_suffix"] + bytes_pre) / (cm["bw_suffix_gbs"] * 1e3))
 
 
 def arrangement(cm, f, num_sms):
@@ -117,10 +123,9 @@ def arrangement(cm, f, num_sms):
     best, best_c = None, None
     for C in range(max(_tiles(f)[1]), 0, -1):
         items = n_items(f, C)
-        if items > num_sms - 1:
+        if items > num_sms:
             break
-        bw = min(cm["bw_suffix_gbs"], (num_sms - items) * cm["gather_sm_gbs"])
-        t = max(item_us(cm, C), f["bytes_suffix"] / (bw * 1e3))
+        t = split_levels(cm, f, C, items, num_sms)
         if best is None or t < best - 1e-9:
             best, best_c = t, C
     if best is None or not best < sequential_levels(cm, f, c_seq, num_sms):
@@ -128,14 +133,14 @@ def arrangement(cm, f, num_sms):
     n_pre = n_items(f, best_c)
     while best_c > 1 and n_items(f, best_c - 1) == n_pre:
         best_c -= 1
-    return dict(split=True, C=best_c, n_pre=n_pre, n_gather=gather_ctas(f["suffix_tokens"], num_sms - n_pre))
+    return dict(split=True, C=best_c, n_pre=n_pre, n_gather=num_sms)
 
 
 def predict(cm, f, num_sms=152):
     t_flat = cm["c_flat_us"] + f["bytes_flat"] / (cm["bw_flat_gbs"] * 1e3)
     a = arrangement(cm, f, num_sms)
     if a["split"]:
-        t_levels = split_levels(cm, f, a["C"], a["n_gather"])
+        t_levels = split_levels(cm, f, a["C"], a["n_pre"], num_sms)
     else:
         t_levels = sequential_levels(cm, f, a["C"], num_sms)
     t_cas = cm["c_cascade_us"] + t_levels + cm["c_merge_us"] * f["B"] * f["Hq"]

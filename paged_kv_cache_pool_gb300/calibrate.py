@@ -6,7 +6,7 @@ Times, with CUDA events, on one layer of synthetic pools (random bf16 data):
   * the suffix gather over every SM, several volumes        -> c_gather_us + bytes / bw_suffix_gbs
   * prefix items of C key tiles, forced split plans and the -> prefix_item_us + C * prefix_tile_us
     sequential plans of several M_eff = B * g
-  * the gather alone on the SMs a split plan leaves it      -> gather_sm_gbs
+  * the gather alone on the SMs long prefix items leave it  -> gather_sm_gbs
   * the merge                                               -> c_merge_us per (request, head)
   * the whole cascade, both arrangements                    -> c_cascade_us (mean residual)
 and writes the JSON that gk_cost_model_load reads.
@@ -99,17 +99,24 @@ def calibrate(Hq=32, Hkv=8, d=128, device="cuda"):
             tile_pts.append((c.info["prefix_tiles_per_item"], t_pre))
         cas_pts.append((dict(c.info), t_cas, B))
         c.close()
-    # split plans: prefix items of C tiles alone, and the gather alone on the SMs left
+    # split plans: prefix items of C tiles alone, and the whole split cascade
     for C in (16, 32, 64, 128):
         c = _Case(eng, 64, 16384, 1024, Hq, d, gk.GK_CASCADE_SPLIT, C)
         if c.info["cascade_split"]:
             t_pre = _time(lambda: gk.gk_cascade_prefix(pool, None, 0, c.batch, c.plan))
-            t_suf = _time(lambda: gk.gk_cascade_suffix(pool, None, 0, c.batch, c.plan))
             t_cas = _time(lambda: gk.gk_decode_cascade(pool, None, 0, c.batch, c.plan))
             tile_pts.append((c.info["prefix_tiles_per_item"], t_pre))
-            sm_pts.append((c.info["suffix_ctas"], c.info["suffix_bytes"] / (t_suf * 1e3)))
             cas_pts.append((dict(c.info), t_cas, 64))
         c.close()
+    # the gather alone on part of the SMs: long items (one key split, 64 of them at
+    # M_eff 2048) leave their CTAs no suffix share, so the suffix runs on the other
+    # SMs only, well below HBM saturation
+    c = _Case(eng, 512, 16384, 128, Hq, d, gk.GK_CASCADE_SPLIT, 128)
+    if c.info["cascade_split"]:
+        t_suf = _time(lambda: gk.gk_cascade_suffix(pool, None, 0, c.batch, c.plan))
+        n_sms = c.info["suffix_ctas"] - c.info["prefix_ctas"]
+        sm_pts.append((n_sms, c.info["suffix_bytes"] / (t_suf * 1e3)))
+    c.close()
     eng.close()
     torch.cuda.synchronize()
 
@@ -137,8 +144,8 @@ def refit(measured, num_sms=152):
     cm = dict(c_flat_us=c_flat, bw_flat_gbs=1.0 / max(s_flat, 1e-12) / 1e3, c_cascade_us=0.0,
               bw_prefix_gbs=6000.0, bw_suffix_gbs=1.0 / max(s_suf, 1e-12) / 1e3, c_merge_us=max(s_mrg, 0.0),
               prefix_tile_us=max(tile, 1e-3), prefix_item_us=item, gather_sm_gbs=44.0, c_gather_us=c_suf)
-    # per-SM gather bandwidth: points whose SMs stay well below the all-SM bandwidth
-    per_sm = [bw / n for n, bw in measured["gather_sm"] if n * 50.0 < cm["bw_suffix_gbs"]]
+    # per-SM gather bandwidth: the suffix alone on the SMs the long items leave it
+    per_sm = [bw / n for n, bw in measured["gather_sm"] if n > 0]
     if per_sm:
         cm["gather_sm_gbs"] = float(np.median(per_sm))
     # the cascade's fixed cost: the merge launch's intercept plus the mean residual
@@ -147,8 +154,8 @@ def refit(measured, num_sms=152):
     for info, t_cas in zip(measured["cascade_info"], measured["cascade"]):
         item_us = info["prefix_tiles_per_item"] * cm["prefix_tile_us"] + cm["prefix_item_us"]
         if info["cascade_split"]:
-            bw = min(cm["bw_suffix_gbs"], info["suffix_ctas"] * cm["gather_sm_gbs"])
-            levels = max(item_us, info["suffix_bytes"] / (bw * 1e3))
+            bal = (info["suffix_bytes"] / (cm["gather_sm_gbs"] * 1e3) + info["prefix_ctas"] * item_us) / num_sms
+            levels = max(item_us, bal, (info["suffix_bytes"] + info["prefix_bytes"]) / (cm["bw_suffix_gbs"] * 1e3))
         else:
             waves = -(-info["prefix_ctas"] // num_sms)
             levels = (max(info["prefix_bytes"] / (cm["bw_prefix_gbs"] * 1e3), waves * item_us) if info["prefix_ctas"] else 0.0)

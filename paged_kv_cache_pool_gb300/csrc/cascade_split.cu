@@ -1,17 +1,17 @@
 // Split cascade launch: the prefix contraction and the suffix gather of one
-// layer (GraniKV Section 3.3, the two levels of the cascade) side by side in
-// one launch, on disjoint sets of SMs.
+// layer (GraniKV Section 3.3, the two levels of the cascade) in one launch,
+// one CTA per SM.
 //
 // The prefix level is a dense contraction on the tensor cores that reads each
 // prefix K/V tile once; the suffix level is a gather bound by HBM.  Run one
 // after the other, every SM first waits on tensor-core work with HBM half
-// idle, then streams with the tensor cores idle.  Here CTA b < n_pre runs
-// prefix work item b (one CTA per SM, so the plan makes the items long: few
-// key splits), and every other CTA runs a slot of the suffix partition, so the
-// tensor-core items and the HBM stream overlap for the whole launch.  The
-// plan picks n_pre so that both sides are predicted to finish together.  Both
-// sides write partial states; the merge (GraniKV Eq. 1) follows as its own
-// launch.
+// idle, then streams with the tensor cores idle, and each launch pays its own
+// ramp and tail.  Here CTA b < n_pre first runs prefix work item b (the plan
+// makes items long: few key splits), then every CTA gathers its slot of the
+// suffix partition; a prefix CTA's slot is cut to the time its item leaves,
+// so that all CTAs are predicted to finish together while the tensor-core
+// items overlap the other SMs' HBM stream.  Both levels write partial states;
+// the merge (GraniKV Eq. 1) follows as its own launch.
 #include "gather_body.cuh"
 #include "prefix_body.cuh"
 
@@ -21,8 +21,8 @@ namespace {
 struct SplitParams {
   prefix::PrefixParams pp;
   gather::GatherParams gp;
-  int32_t n_pre;        // CTAs [0, n_pre) run prefix item b
-  int32_t n_gather;     // CTAs [n_pre, n_pre + n_gather) run suffix slot b - n_pre
+  int32_t n_pre;        // CTAs [0, n_pre) first run prefix item b
+  int32_t n_gather;     // CTAs [0, n_gather) gather suffix slot b
   uint32_t data_bytes;  // shared data area: max of the prefix and gather layouts
 };
 
@@ -62,15 +62,16 @@ __global__ void __launch_bounds__(kSplitThreads, 1) cascade_split_kernel(const S
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     griddep_wait();
-    prefix::prefix_item<D>(f.pp, f.pp.items[b], base, ctl, ctl_ptr, tmem);
+    const bool ok = prefix::prefix_item<D>(f.pp, f.pp.items[b], base, ctl, ctl_ptr, tmem);
     __syncthreads();
     if (warp == 1) {
       tc_fence_after();
       tmem_dealloc(tmem, prefix::kTmemCols);
     }
-  } else if (b - f.n_pre < f.n_gather) {
-    gather::gather_segments<D, G, false>(f.gp, base, b - f.n_pre);
+    if (!ok) return;  // same value on every thread
   }
+  // the item's staging area is free: the gather re-initialises the shared memory
+  if (b < f.n_gather) gather::gather_segments<D, G, false>(f.gp, base, b);
 }
 
 template <int D, int G>
@@ -91,7 +92,7 @@ int launch_cascade_split(const LaunchCommon& lc, void* stream, int32_t layer, co
   fill_gather_params(lc, layer, b, pl, false, &fp.gp);
   fp.n_pre = (int32_t)pl->prefix_items.size();
   fp.n_gather = pl->summary.suffix_ctas;
-  const int ctas = fp.n_pre + fp.n_gather;
+  const int ctas = std::max(fp.n_pre, fp.n_gather);
   if (ctas == 0) return 0;
   const int g = c.num_q_heads / c.num_kv_heads;
   cudaStream_t st = (cudaStream_t)stream;

@@ -59,6 +59,51 @@ void partition_tokens(const std::vector<int64_t>& n, int64_t max_ctas, std::vect
   if (begin->back() != (int32_t)segs->size()) begin->push_back((int32_t)segs->size());
 }
 
+// As partition_tokens, over exactly w.size() CTA slots: slot b's quota is the
+// share w[b] / sum(w) of the tokens, its end rounded to a multiple of
+// kGatherQuantum (the last slot takes the rest); a slot may be empty.
+void partition_tokens_weighted(const std::vector<int64_t>& n, const std::vector<double>& w,
+                               std::vector<int32_t>* begin, std::vector<SegmentDev>* segs) {
+  begin->clear();
+  segs->clear();
+  int64_t total = 0;
+  for (int64_t x : n) total += x;
+  begin->push_back(0);
+  if (total == 0) return;
+  double wsum = 0.0;
+  for (double x : w) wsum += x;
+  // end of each slot in the concatenated token stream
+  std::vector<int64_t> ends(w.size());
+  double acc = 0.0;
+  for (size_t b = 0; b < w.size(); ++b) {
+    acc += w[b];
+    int64_t e = (int64_t)((double)total * acc / wsum + 0.5);
+    e = (e + kGatherQuantum / 2) / kGatherQuantum * kGatherQuantum;
+    e = std::min(total, std::max(e, b ? ends[b - 1] : (int64_t)0));
+    ends[b] = b + 1 == w.size() ? total : e;
+  }
+  size_t slot = 0;
+  int64_t pos = 0;   // tokens of the stream already placed
+  while (slot < w.size() && ends[slot] == 0) {
+    begin->push_back(0);
+    ++slot;
+  }
+  for (size_t r = 0; r < n.size(); ++r) {
+    int64_t t = 0;
+    while (t < n[r]) {
+      const int64_t take = std::min(ends[slot] - pos, n[r] - t);
+      segs->push_back(SegmentDev{(int32_t)r, (int32_t)t, (int32_t)(t + take), -1});
+      t += take;
+      pos += take;
+      while (slot < w.size() && pos == ends[slot]) {
+        begin->push_back((int32_t)segs->size());
+        ++slot;
+      }
+    }
+  }
+  while (begin->size() < w.size() + 1) begin->push_back((int32_t)segs->size());
+}
+
 }  // namespace
 
 gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
@@ -148,13 +193,16 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
       }
     }
   }
-  // Split arrangement: n_pre SMs each run one prefix item of C key tiles while
-  // the other SMs gather the suffix, in one launch.  Predicted
-  //   T_split(C) = max(C * prefix_tile_us + prefix_item_us,
-  //                    S / min(bw_suffix, (SMs - n_pre) * gather_sm)),
-  // against the sequential arrangement's W waves of c_seq-tile items:
-  //   T_seq = max(prefix_bytes / bw_prefix, W * (c_seq * prefix_tile_us + prefix_item_us))
-  //           + c_gather + S / bw_suffix.
+  // Split arrangement: one launch in which CTA b < n_pre first runs one prefix
+  // item of C key tiles, and every CTA (one per SM) gathers a slot of the
+  // suffix, a prefix CTA's slot cut to the time its item leaves.  Predicted
+  //   item(C)   = C * prefix_tile_us + prefix_item_us
+  //   T_split   = max(item(C), (S / gather_sm + n_pre * item(C)) / SMs,
+  //                   (S + prefix_bytes) / bw_suffix)
+  // (the middle term spreads the gather's SM-time and the items over all SMs;
+  // the last is HBM), against the sequential arrangement's W waves of c_seq-tile
+  // items then the gather as a second launch:
+  //   T_seq = max(prefix_bytes / bw_prefix, W * item(c_seq)) + c_gather + S / bw_suffix.
   // The split is taken when some C is predicted faster than the sequential
   // arrangement; among equal predictions the fewest items (fewest partials)
   // win, and the chosen item count is then spread evenly over the key tiles.
@@ -163,27 +211,31 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   int64_t suffix_tokens = 0;
   for (int32_t r = 0; r < B; ++r) suffix_tokens += pl->reqs[(size_t)r].slen;
   const double S = (double)suffix_tokens * (double)kv_tok;
+  double prefix_bytes = 0.0;
+  for (int32_t gi = 0; gi < G; ++gi)
+    prefix_bytes += (double)pl->reqs[(size_t)members[(size_t)gi][0]].lp * (double)kv_tok;
   double t_seq = S / (cm.bw_suffix_gbs * 1e3) + cm.c_gather_us;
   if (G > 0) {
-    double prefix_bytes = 0.0;
-    for (int32_t gi = 0; gi < G; ++gi)
-      prefix_bytes += (double)pl->reqs[(size_t)members[(size_t)gi][0]].lp * (double)kv_tok;
     const double waves = (double)((n_items(c_seq) + num_sms - 1) / num_sms);
     t_seq += std::max(prefix_bytes / (cm.bw_prefix_gbs * 1e3),
                       waves * (std::min(c_seq, max_ntiles) * cm.prefix_tile_us + cm.prefix_item_us));
   }
+  auto item_us = [&](int32_t C) { return C * cm.prefix_tile_us + cm.prefix_item_us; };
+  auto split_us = [&](int32_t C) {
+    const double it = item_us(C);
+    const double bal = (S / (cm.gather_sm_gbs * 1e3) + (double)n_items(C) * it) / num_sms;
+    return std::max(std::max(it, bal), (S + prefix_bytes) / (cm.bw_suffix_gbs * 1e3));
+  };
   int32_t c_split = 0;
   double t_split = 1e300;
   const bool can_split = G > 0 && suffix_tokens > 0 && p->cascade_mode != GK_CASCADE_SEQUENTIAL;
   if (can_split && p->cascade_mode == GK_CASCADE_SPLIT && p->cascade_tiles > 0) {
     const int32_t C = std::min(p->cascade_tiles, max_ntiles);
-    if (n_items(C) <= num_sms - 1) c_split = C;
+    if (n_items(C) <= num_sms) c_split = C;
   } else {
     for (int32_t C = max_ntiles; can_split && C >= 1; --C) {
-      const int64_t items = n_items(C);
-      if (items > num_sms - 1) break;  // items only grow as C shrinks
-      const double bw = std::min(cm.bw_suffix_gbs, (double)(num_sms - items) * cm.gather_sm_gbs);
-      const double t = std::max(C * cm.prefix_tile_us + cm.prefix_item_us, S / (bw * 1e3));
+      if (n_items(C) > num_sms) break;  // items only grow as C shrinks
+      const double t = split_us(C);
       if (t < t_split - 1e-9) {
         t_split = t;
         c_split = C;
@@ -194,6 +246,12 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   while (c_split > 1 && n_items(c_split - 1) == n_items(c_split)) --c_split;
   pl->split = c_split > 0 && (p->cascade_mode == GK_CASCADE_SPLIT || t_split < t_seq);
   const int32_t best_c = pl->split ? c_split : c_seq;
+  // gather weight of a prefix CTA relative to a gather-only CTA (time left after its item)
+  double prefix_cta_share = 1.0;
+  if (pl->split) {
+    const double T = split_us(c_split);
+    prefix_cta_share = std::max(0.0, T - item_us(c_split)) / T;
+  }
   int32_t max_m = 0;
   int64_t pre_bytes = 0, pre_flops = 0;
   for (int32_t gi = 0; gi < G; ++gi) {
@@ -242,8 +300,14 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     suf_tokens += n_suf[(size_t)r];
     dense_tokens += n_dense[(size_t)r];
   }
-  partition_tokens(n_suf, pl->split ? num_sms - (int64_t)pl->prefix_items.size() : num_sms, &pl->suf_seg_begin,
-                   &pl->suf_segs);
+  if (pl->split) {
+    // one slot per SM; the prefix CTAs' slots (the first n_pre) carry their share
+    std::vector<double> w((size_t)num_sms, 1.0);
+    for (size_t b2 = 0; b2 < pl->prefix_items.size() && b2 < w.size(); ++b2) w[b2] = prefix_cta_share;
+    partition_tokens_weighted(n_suf, w, &pl->suf_seg_begin, &pl->suf_segs);
+  } else {
+    partition_tokens(n_suf, num_sms, &pl->suf_seg_begin, &pl->suf_segs);
+  }
   partition_tokens(n_dense, max_ctas, &pl->dense_seg_begin, &pl->dense_segs);
 
   // ---- partial-state entries ----------------------------------------------------
@@ -521,12 +585,12 @@ gk_status gk_dispatch(const gk_pool* pool, const gk_plan* plan, gk_backend* choi
   double t_levels = 0.0;
   const gk_plan_summary& sm = pl.summary;
   const double item = sm.prefix_tiles_per_item * cm.prefix_tile_us + cm.prefix_item_us;
+  const int num_sms = pool->impl.dev.num_sms;
   if (pl.split) {
-    const double bw = std::min(cm.bw_suffix_gbs, (double)sm.suffix_ctas * cm.gather_sm_gbs);
-    t_levels = std::max(item, (double)sm.suffix_bytes / (bw * 1e3));
+    const double bal = ((double)sm.suffix_bytes / (cm.gather_sm_gbs * 1e3) + sm.prefix_ctas * item) / num_sms;
+    t_levels = std::max(std::max(item, bal), (double)(sm.suffix_bytes + sm.prefix_bytes) / (cm.bw_suffix_gbs * 1e3));
   } else {
     if (sm.prefix_ctas > 0) {
-      const int num_sms = pool->impl.dev.num_sms;
       const double waves = (double)((sm.prefix_ctas + num_sms - 1) / num_sms);
       t_levels = std::max((double)sm.prefix_bytes / (cm.bw_prefix_gbs * 1e3), waves * item);
     }

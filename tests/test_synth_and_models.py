@@ -107,27 +107,32 @@ def test_cost_model_closed_form():
 
 def test_split_arrangement_worked_example():
     """One group of 64 requests (g = 4 -> one 256-row block), Lp = 16384 (128 key tiles),
-    Hkv = 8, 1000 suffix tokens each; tile 1 us, item 5 us, 50 GB/s per SM, 6000 GB/s,
-    4 us for a separate gather launch.
-    Items(C) = 8 * ceil(128 / C); T(C) = max(C + 5, S / min(6000, (152 - items) * 50)).
-    C = 32..38 leave 120 SMs (S / 6000 GB/s = 43.69 us binds); the largest, 38, wins the
-    scan, and 32 is the fewest tiles per item that still gives its 32 items."""
+    Hkv = 8, 1000 suffix tokens each; tile 1 us, item 5 us, 50 GB/s per SM, 6000 GB/s over
+    every SM, 4 us for a separate gather launch, 152 SMs.
+    Items(C) = 8 * ceil(128 / C), item(C) = C + 5, and
+    T(C) = max(C + 5, (S / 50 GB/s + items * (C + 5)) / 152, (S + prefix bytes) / 6000 GB/s).
+    HBM binds at 54.875 us from C = 49 down (C = 50 gives 55); the scan keeps 49
+    (24 items), and 43 is the fewest tiles per item that still gives 24 items."""
     cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0, bw_suffix_gbs=6000.0,
               c_merge_us=0.001, prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0, c_gather_us=4.0)
     f = dispatch.features([16384] * 64, [1000] * 64, [0] * 64, 32, 8, 128)
     S = 64 * 1000 * 4096
+    P = 16384 * 4096
     assert f["bytes_suffix"] == S
+    assert math.isclose(dispatch.split_levels(cm, f, 50, 24, 152), 55.0)
+    assert math.isclose(dispatch.split_levels(cm, f, 49, 24, 152), (S + P) / 6e6)
+    # C = 64: 16 items of 69 us; the gather spread over every SM is shorter
+    assert math.isclose(dispatch.split_levels(cm, f, 64, 16, 152), 69.0)
+    assert (S / 50e3 + 16 * 69.0) / 152 < 69.0
     a = dispatch.arrangement(cm, f, 152)
-    assert a == dict(split=True, C=32, n_pre=32, n_gather=118)
-    # the gather partition: quota ceil(64000 / 120) = 534 -> 544 (multiple of 16) -> 118 CTAs
-    assert dispatch.gather_ctas(64000, 120) == 118
+    assert a == dict(split=True, C=43, n_pre=24, n_gather=152)
     t_flat, t_cas = dispatch.predict(cm, f, 152)
-    assert math.isclose(t_cas, 10.0 + max(32 + 5.0, S / (118 * 50.0 * 1e3)) + 0.001 * 64 * 32)
+    assert math.isclose(t_cas, 10.0 + (S + P) / 6e6 + 0.001 * 64 * 32)
     # the sequential alternative it beat: C = 7 (152 items, one wave: waves * (C + 2.5) = 9.5
     # against 10.5 at C = 8 and 17 at C = 6), the prefix bound by its 67 MB of reads
     assert dispatch.sequential_tiles(f, 152) == 7 and dispatch.n_items(f, 7) == 152
-    t_seq = max(16384 * 4096 / 5e6, 7 * 1.0 + 5.0) + 4.0 + S / 6e6
-    assert math.isclose(dispatch.sequential_levels(cm, f, 7, 152), t_seq) and t_seq > 43.69
+    t_seq = max(P / 5e6, 7 * 1.0 + 5.0) + 4.0 + S / 6e6
+    assert math.isclose(dispatch.sequential_levels(cm, f, 7, 152), t_seq) and t_seq > (S + P) / 6e6
     # no suffix, or no shared prefix: never split
     assert not dispatch.arrangement(cm, dispatch.features([16384] * 64, [0] * 64, [0] * 64, 32, 8, 128), 152)["split"]
     assert not dispatch.arrangement(cm, dispatch.features([0] * 64, [1000] * 64, [-1] * 64, 32, 8, 128), 152)["split"]
