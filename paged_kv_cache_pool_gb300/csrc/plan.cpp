@@ -246,11 +246,13 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   while (c_split > 1 && n_items(c_split - 1) == n_items(c_split)) --c_split;
   pl->split = c_split > 0 && (p->cascade_mode == GK_CASCADE_SPLIT || t_split < t_seq);
   const int32_t best_c = pl->split ? c_split : c_seq;
-  // gather weight of a prefix CTA relative to a gather-only CTA (time left after its item)
+  // gather weight of a prefix CTA relative to a gather-only CTA: the time its
+  // item leaves, less the ramp of starting a gather (c_gather_us); a sliver of
+  // suffix would cost more in ramp and partial states than it saves
   double prefix_cta_share = 1.0;
   if (pl->split) {
     const double T = split_us(c_split);
-    prefix_cta_share = std::max(0.0, T - item_us(c_split)) / T;
+    prefix_cta_share = std::max(0.0, T - item_us(c_split) - cm.c_gather_us) / T;
   }
   int32_t max_m = 0;
   int64_t pre_bytes = 0, pre_flops = 0;
