@@ -6,8 +6,10 @@ Workload (default): Llama-3.1-8B attention geometry (Hq 32, Hkv 8, d 128, bf16,
 with suffixes uniform in 256..2048 tokens in a page-size-1 COLD pool with
 shuffled slots.  One step = the whole decode step of all layers:
   host: gk_seq_append_slots (64 tokens), gk_seq_tables, gk_plan_update, gk_dispatch
-  device, per layer: gk_append_kv (the step's token), then the dispatcher's
-  backend (cascade: prefix contraction, suffix gather, LSE merge; or dense).
+  device, per layer: copy-on-write copies if the step has any (gk_append_kv with
+  n = 0), then the dispatcher's backend with the step's token appended by the
+  decode itself (cascade: prefix contraction beside the suffix gather, LSE
+  merge; or dense).
 Metric: decode attention queries/s per layer = B * L / step time.
 
 --impl reference times the fp64 CPU oracle instead (there is no other
@@ -45,6 +47,8 @@ def _args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="run only this many layers (small profiling case)")
+    ap.add_argument("--append", choices=["fused", "separate"], default="fused",
+                    help="the step's new tokens written by the decode itself, or by gk_append_kv first")
     return ap.parse_args()
 
 
@@ -271,11 +275,11 @@ def run_ours(a, w):
     max_len = max(r.suffix_len for r in w.requests) + total_steps + 1
     max_blocks = -(-max_len // P)
     h_table = torch.empty((B, max_blocks), dtype=torch.int32).pin_memory()
-    h_lens = np.empty(B, dtype=np.int32)
     h_slots = torch.empty(B, dtype=torch.int64).pin_memory()
+    d_slots = torch.empty(B, dtype=torch.int64, device="cuda")
+    h_lens = np.empty(B, dtype=np.int32)
     h_cow = torch.empty(2 * B, dtype=torch.int32).pin_memory()
     d_table = torch.empty((B, max_blocks), dtype=torch.int32, device="cuda")
-    d_slots = torch.empty(B, dtype=torch.int64, device="cuda")
     d_cow = torch.empty(2 * B, dtype=torch.int32, device="cuda")
     staged = torch.cuda.Event()
     bases = np.array([gw.bases[r.prefix] if r.prefix >= 0 else -1 for r in w.requests], dtype=np.int64)
@@ -299,8 +303,9 @@ def run_ours(a, w):
             h_cow.numpy()[:2 * ncow] = cow.reshape(-1)
         gk.gk_seq_tables(pool, seqs, max_blocks, h_table.numpy(), h_lens)
         batch.suffix_len[:] = h_lens
-        d_slots.copy_(h_slots, non_blocking=True)
         d_table.copy_(h_table, non_blocking=True)
+        if a.append != "fused":
+            d_slots.copy_(h_slots, non_blocking=True)
         if ncow:
             d_cow[:2 * ncow].copy_(h_cow[:2 * ncow], non_blocking=True)
         staged.record(stream)
@@ -320,9 +325,17 @@ def run_ours(a, w):
             ev = events[l] if (events is not None and l in events) else None
             if ev is not None:
                 ev[0].record(stream)
-            gk.gk_append_kv(pool, stream, l, d_slots, k[l], v[l], d_cow if ncow else None, n=B, n_cow=ncow)
-            launches[0] += 1 + (1 if ncow else 0)
-            batch.set_device(d_q=q[l], d_out=out[l], d_lse=lse[l])
+            if a.append == "fused":
+                # the step's new tokens are appended by the decode itself; copy-on-write
+                # copies, when the step has any, come first
+                if ncow:
+                    gk.gk_append_kv(pool, stream, l, None, None, None, d_cow, n=0, n_cow=ncow)
+                    launches[0] += 1
+                batch.set_device(d_q=q[l], d_out=out[l], d_lse=lse[l], d_new_k=k[l], d_new_v=v[l])
+            else:
+                gk.gk_append_kv(pool, stream, l, d_slots, k[l], v[l], d_cow if ncow else None, n=B, n_cow=ncow)
+                launches[0] += 1 + (1 if ncow else 0)
+                batch.set_device(d_q=q[l], d_out=out[l], d_lse=lse[l])
             if ev is not None:
                 ev[1].record(stream)
             if choice == gk.GK_BACKEND_CASCADE:
@@ -487,7 +500,7 @@ def run_ours(a, w):
         e1.record(stream)
         torch.cuda.synchronize()
         ems = max_over_ranks(e0.elapsed_time(e1))
-        h2d_bytes = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + B * 8 + B * max_blocks * 4
+        h2d_bytes = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + B * max_blocks * 4
         d2h_bytes = ho.numel() * 4 + hl.numel() * 4
         e2e = {"value": replica_throughput(world, B * L * a.steps, ems), "unit": UNIT,
                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "ms_per_step": ems / a.steps,

@@ -156,6 +156,16 @@ typedef struct gk_batch {
   const void* d_q;                /* device bf16 [B][Hq][d] (this layer's queries) */
   float* d_out;                   /* device fp32 [B][Hq][d] */
   float* d_lse;                   /* device fp32 [B][Hq], natural log; may be NULL */
+  /* Optional fused append ("Paged KV cache", How it works step 2: reshape_and_cache),
+   * both NULL or both set: this layer's new token of every request, device bf16
+   * [B][Hkv][d].  Each request's last COLD token (suffix position suffix_len - 1,
+   * reserved by gk_seq_append_slots and present in the block table) is then read
+   * from here instead of the pool, and the decode writes it into the pool slot the
+   * table gives -- what gk_append_kv would have written -- so no separate scatter
+   * launch is needed.  Copy-on-write pairs of the step must be copied first
+   * (gk_append_kv with n = 0).  Requests with suffix_len 0 are unaffected. */
+  const void* d_new_k;
+  const void* d_new_v;
 } gk_batch;
 
 typedef struct gk_plan_summary {

@@ -45,7 +45,7 @@ class gk_batch(ctypes.Structure):
     _fields_ = [("num_requests", c_i32), ("max_blocks", c_i32),
                 ("prefix_hot_base", ctypes.POINTER(c_i64)), ("prefix_len", ctypes.POINTER(c_i32)),
                 ("suffix_len", ctypes.POINTER(c_i32)), ("d_block_table", c_vp), ("d_q", c_vp),
-                ("d_out", c_vp), ("d_lse", c_vp)]
+                ("d_out", c_vp), ("d_lse", c_vp), ("d_new_k", c_vp), ("d_new_v", c_vp)]
 
 
 class gk_plan_summary(ctypes.Structure):
@@ -281,9 +281,12 @@ class Batch:
         self.prefix_len = np.ascontiguousarray(prefix_len, dtype=np.int32)
         self.suffix_len = np.ascontiguousarray(suffix_len, dtype=np.int32)
         self.c = gk_batch(len(self.prefix_len), max_blocks, _i64p(self.prefix_hot_base), _i32p(self.prefix_len),
-                          _i32p(self.suffix_len), _ptr(d_block_table), _ptr(d_q), _ptr(d_out), _ptr(d_lse))
+                          _i32p(self.suffix_len), _ptr(d_block_table), _ptr(d_q), _ptr(d_out), _ptr(d_lse), None, None)
 
-    def set_device(self, d_block_table=None, max_blocks=None, d_q=None, d_out=None, d_lse=None):
+    def set_device(self, d_block_table=None, max_blocks=None, d_q=None, d_out=None, d_lse=None, d_new_k=None,
+                   d_new_v=None):
+        """d_lse, d_new_k and d_new_v are set on every call (None clears them: no LSE
+        output, no fused append); the others keep their value when None."""
         if d_block_table is not None:
             self.c.d_block_table = _ptr(d_block_table)
         if max_blocks is not None:
@@ -293,6 +296,8 @@ class Batch:
         if d_out is not None:
             self.c.d_out = _ptr(d_out)
         self.c.d_lse = _ptr(d_lse)
+        self.c.d_new_k = _ptr(d_new_k)
+        self.c.d_new_v = _ptr(d_new_v)
         return self
 
 

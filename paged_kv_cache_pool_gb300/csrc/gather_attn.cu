@@ -79,6 +79,8 @@ int fill_gather_params(const LaunchCommon& lc, int32_t layer, const gk_batch* b,
   gp.err = lc.d_error;
   gp.q_scale = kLog2e / sqrtf((float)c.head_dim);
   gp.nst = single_cta_stages(c.num_kv_heads, c.head_dim);
+  gp.new_k = (const uint16_t*)b->d_new_k;
+  gp.new_v = (const uint16_t*)b->d_new_v;
   return 0;
 }
 

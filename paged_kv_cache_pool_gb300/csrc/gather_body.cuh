@@ -67,6 +67,10 @@ struct GatherParams {
   int32_t* err;
   float q_scale;  // log2(e) / sqrt(d): scores come out in the log2 domain
   int32_t nst;    // pipeline stages (<= kMaxStages)
+  // fused append (else null): this layer's new token of every request, [B][Hkv][d];
+  // a request's last COLD token is read from here and written into the pool
+  const uint16_t* new_k;
+  const uint16_t* new_v;
 };
 
 // Shared memory: each consumer warp owns a ring of nst stages; a stage holds
@@ -75,8 +79,11 @@ struct GatherParams {
 // ldmatrix reads fall in eight different 16-byte bank groups.
 __host__ __device__ constexpr uint32_t slice_row_bytes(int d) { return (uint32_t)d * 2 + 16; }
 __host__ __device__ constexpr uint32_t warp_stage_bytes(int d) { return 2u * kT * slice_row_bytes(d); }
+// each warp also keeps, per ring stage, which of its tokens was appended this
+// step (fused append) and that token's pool offset
+constexpr uint32_t kFreshRecBytes = 16;
 __host__ __device__ constexpr size_t gather_data_bytes(int hkv, int d, int nst) {
-  return (size_t)hkv * nst * warp_stage_bytes(d);
+  return (size_t)hkv * nst * warp_stage_bytes(d) + (size_t)hkv * kMaxStages * kFreshRecBytes;
 }
 __host__ __device__ constexpr size_t gather_smem_bytes(int hkv, int d, int nst) {
   return 1024 + gather_data_bytes(hkv, d, nst);
@@ -87,7 +94,8 @@ constexpr size_t kSmemPerCtaMax = 232448;
 constexpr size_t kSoleCtaReserve = 1024 + 3072;
 // ring depth when the gather CTA has the SM (and its shared memory) to itself
 __host__ __device__ constexpr int single_cta_stages(int hkv, int d) {
-  const int n = (int)((kSmemPerCtaMax - kSoleCtaReserve) / gather_data_bytes(hkv, d, 1));
+  const int n = (int)((kSmemPerCtaMax - kSoleCtaReserve - (size_t)hkv * kMaxStages * kFreshRecBytes) /
+                      ((size_t)hkv * warp_stage_bytes(d)));
   return n > kMaxStages ? kMaxStages : n;
 }
 
@@ -159,6 +167,10 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
 
   const int h = warp;
   const uint32_t ring = base + (uint32_t)h * nst * WS;
+  // per ring stage, 16 bytes: index in the stage of the request's appended token
+  // (-1: none) and its pool offset (elements, head h; the same for K and V)
+  const uint32_t recs = base + (uint32_t)Hkv * nst * WS + (uint32_t)h * kMaxStages * kFreshRecBytes;
+  const bool fused_append = p.new_k != nullptr;
   const int seg0 = p.seg_begin[cta], seg1 = p.seg_begin[cta + 1];
   const int64_t layer_rows = (int64_t)p.layer * p.cold_slots;
 
@@ -169,16 +181,23 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
   // registers; nothing uses a loaded id until the copy, where the slot
   // arithmetic happens.
   struct Cursor {
-    int sg, t, t1, lp;
+    int sg, t, t1, lp, req, slen;
     const int32_t* table;
     int64_t hot_row0;  // element offset of the (layer, head h) rows of the request's HOT prefix
   };
+  // An entry's scalars share one word (the queue lives in registers): bits 0-4
+  // tokens in the stage (0: no stage), bit 5 a HOT run, bits 6-10 one plus the
+  // index in the stage of the request's appended token (fused append; 0: none),
+  // bits 16-31 the request.
   struct Entry {
     int32_t blk;    // COLD, lane < n: block id of the stage's token `lane`
     int32_t tt0;    // COLD: suffix index of the stage's token 0
-    int32_t n;      // tokens in the stage (0: no stage)
-    int32_t hot;    // 1: a HOT run
+    uint32_t meta;
     int64_t row0;   // HOT: element offset of token 0's row
+    __device__ int n() const { return (int)(meta & 31u); }
+    __device__ bool hot() const { return (meta >> 5) & 1u; }
+    __device__ int fresh() const { return (int)((meta >> 6) & 31u) - 1; }
+    __device__ int req() const { return (int)(meta >> 16); }
   };
   auto cursor_at = [&](int sg) {
     Cursor c{};
@@ -188,6 +207,8 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
       const RequestDev rq = p.reqs[sd.req];
       c.t = sd.t0;
       c.t1 = sd.t1;
+      c.req = sd.req;
+      c.slen = rq.slen;
       c.lp = DENSE ? rq.lp : 0;
       c.table = p.block_table + (int64_t)sd.req * p.max_blocks;
       if (DENSE && c.lp > 0) c.hot_row0 = rq.hot_base * p.L * Hkv * D + ((int64_t)p.layer * Hkv + h) * c.lp * D;
@@ -208,48 +229,74 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
   auto make_entry = [&](const Cursor& c) {
     Entry e{};
     if (c.sg >= seg1) return e;
-    e.n = stage_len(c);
+    const int n = stage_len(c);
+    e.meta = (uint32_t)n | ((uint32_t)c.req << 16);
     if (DENSE && c.t < c.lp) {
-      e.hot = 1;
+      e.meta |= 1u << 5;
       e.row0 = c.hot_row0 + (int64_t)c.t * D;
     } else {
       e.tt0 = c.t - c.lp;
-      e.blk = lane < e.n ? c.table[(e.tt0 + lane) / p.page] : -1;
+      e.blk = lane < n ? c.table[(e.tt0 + lane) / p.page] : -1;
+      const int fi = c.slen - 1 - e.tt0;
+      if (fused_append && fi >= 0 && fi < n) e.meta |= (uint32_t)(fi + 1) << 6;
     }
     return e;
   };
   int issued = 0;
   auto copy_stage = [&](const Entry& e) {
-    if (e.n > 0) {
+    if (e.n() > 0) {
       const uint32_t kdst = ring + (uint32_t)(issued % nst) * WS, vdst = kdst + kT * SR;
-      if (DENSE && e.hot) {
+      if (DENSE && e.hot()) {
         // HOT: the stage's rows of this head are contiguous
-        for (int ci = lane; ci < e.n * CPT; ci += 32) {
+        for (int ci = lane; ci < e.n() * CPT; ci += 32) {
           const uint32_t o = (uint32_t)(ci / CPT) * SR + (ci % CPT) * 16;
           cp_async16(kdst + o, p.hot_k + e.row0 + ci * 8);
           cp_async16(vdst + o, p.hot_v + e.row0 + ci * 8);
         }
       } else {
         // COLD: lane i < n turns its token's block id into the row offset of head h
+        const int n = e.n(), fresh = e.fresh();
         int64_t off = -1;
-        if (lane < e.n) {
+        if (lane < n) {
           if (e.blk >= 0 && e.blk < p.n_blocks)
             off = ((layer_rows + (int64_t)e.blk * p.page + (e.tt0 + lane) % p.page) * Hkv + h) * D;
           else
             report_error(p.err, kErrBounds);
         }
+        // the appended token comes from the new-token arrays (copied after the
+        // loop, which keeps the loop free of branches); its pool slot is written
+        // once the stage lands (see the compute loop)
+        int64_t fresh_off = -1;
+        if (fresh >= 0) {
+          fresh_off = __shfl_sync(0xffffffffu, off, fresh);
+          if (lane == fresh) off = -1;
+        }
+        if (lane == 0)
+          sts128(recs + (uint32_t)(issued % nst) * kFreshRecBytes,
+                 make_uint4((uint32_t)(fresh_off >= 0 ? fresh : -1), (uint32_t)fresh_off,
+                            (uint32_t)(fresh_off >> 32), 0u));
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
           const int ci = lane + 32 * j, tok = ci / CPT, ch = ci % CPT;
           const int64_t src = __shfl_sync(0xffffffffu, off, tok);
-          if (tok < e.n && src >= 0) {
+          if (tok < n && src >= 0) {
             const uint32_t o = (uint32_t)tok * SR + ch * 16;
             cp_async16(kdst + o, p.cold_k + src + ch * 8);
             cp_async16(vdst + o, p.cold_v + src + ch * 8);
           }
         }
+        if (fresh_off >= 0 && lane < CPT) {
+          const int64_t fs = ((int64_t)e.req() * Hkv + h) * D + lane * 8;
+          const uint32_t o = (uint32_t)fresh * SR + lane * 16;
+          cp_async16(kdst + o, p.new_k + fs);
+          cp_async16(vdst + o, p.new_v + fs);
+        }
+        cp_async_commit();
+        ++issued;
+        return;
       }
     }
+    if (lane == 0) sts128(recs + (uint32_t)(issued % nst) * kFreshRecBytes, make_uint4(0xffffffffu, 0u, 0u, 0u));
     cp_async_commit();
     ++issued;
   };
@@ -304,6 +351,18 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
       cp_async_wait_pending(nst - 1);  // stage k has landed (this lane's copies) ...
       __syncwarp();                  // ... and every lane's
       const uint32_t ks = ring + (uint32_t)(k % nst) * WS, vs = ks + kT * SR;
+      if (fused_append) {
+        // the request's appended token is in this stage: put head h's rows into the pool
+        const uint4 rec = lds128(recs + (uint32_t)(k % nst) * kFreshRecBytes);
+        const int ft = (int)rec.x;
+        if (ft >= 0 && lane < CPT) {
+          const int64_t off = (int64_t)(((uint64_t)rec.z << 32) | rec.y);
+          uint16_t* pk = const_cast<uint16_t*>(p.cold_k) + off;
+          uint16_t* pv = const_cast<uint16_t*>(p.cold_v) + off;
+          reinterpret_cast<uint4*>(pk)[lane] = lds128(ks + (uint32_t)ft * SR + lane * 16);
+          reinterpret_cast<uint4*>(pv)[lane] = lds128(vs + (uint32_t)ft * SR + lane * 16);
+        }
+      }
       // address of 16-byte chunk c of token row tok in a slice
       auto chunk_addr = [&](uint32_t slice, int tok, int c) -> uint32_t { return slice + (uint32_t)tok * SR + c * 16; };
       // S^T = K Q_h^T

@@ -674,6 +674,8 @@ static gk_status check_decode(Pool* p, int32_t layer, const gk_batch* b, const P
   if (b->num_requests != pl->B) return gk::fail(p, GK_ERR_INVALID, "batch size differs from the plan");
   if (pl->B > 0 && (!b->d_q || !b->d_out || !b->d_block_table))
     return gk::fail(p, GK_ERR_INVALID, "batch device pointers missing");
+  if ((b->d_new_k == nullptr) != (b->d_new_v == nullptr))
+    return gk::fail(p, GK_ERR_INVALID, "fused append needs both d_new_k and d_new_v");
   return gk::ensure_device(p);
 }
 

@@ -57,6 +57,8 @@ extern "C" gk_status gk_decode_dense_static(gk_pool* pool, void* stream, int32_t
   if (layer < 0 || layer >= p->cfg.num_layers) return gk::fail(p, GK_ERR_INVALID, "layer out of range");
   if (batch->num_requests > 0 && (!batch->d_q || !batch->d_out || !batch->d_block_table))
     return gk::fail(p, GK_ERR_INVALID, "batch device pointers missing");
+  if ((batch->d_new_k == nullptr) != (batch->d_new_v == nullptr))
+    return gk::fail(p, GK_ERR_INVALID, "fused append needs both d_new_k and d_new_v");
   // the pool's error word is allocated when the pool first touches the device;
   // this call does not allocate it
   if (!p->d_error || !p->dev.queried)
