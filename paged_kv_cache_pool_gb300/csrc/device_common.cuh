@@ -241,29 +241,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-// 2^x on the FMA pipe, for x <= 64 (returns 0 below -125).  Range reduction
-// x = n + f with n = round(x) taken from the mantissa of x + 1.5*2^23 and
-// f in [-1/2, 1/2]; 2^f by a cubic fitted here to minimise the relative error
-// on [-1/2, 1/2] (iteratively reweighted least squares, max rel. error
-// 7.6e-5); 2^n is added to the exponent field.  Used where the result is
-// rounded to bf16 next (rel. step 3.9e-3), to offload the MUFU pipe.
-__device__ __forceinline__ void exp2_poly_pair(float xa, float xb, float& ya, float& yb) {
-  const float ca = fmaxf(xa, -125.f), cb = fmaxf(xb, -125.f);
-  const uint64_t magic = f2pack(12582912.f, 12582912.f);
-  const uint64_t t = fadd2(f2pack(ca, cb), magic);
-  float ta, tb;
-  f2unpack(t, ta, tb);
-  const float na = ta - 12582912.f, nb = tb - 12582912.f;
-  uint64_t f = fadd2(f2pack(ca, cb), f2pack(-na, -nb));
-  uint64_t p = ffma2(f, f2pack(0.05517047643661499f, 0.05517047643661499f), f2pack(0.2426084578037262f, 0.2426084578037262f));
-  p = ffma2(f, p, f2pack(0.6932609677314758f, 0.6932609677314758f));
-  p = ffma2(f, p, f2pack(0.9999282360076904f, 0.9999282360076904f));
-  float pa, pb;
-  f2unpack(p, pa, pb);
-  ya = xa < -125.f ? 0.f : __int_as_float(__float_as_int(pa) + (__float_as_int(ta) << 23));
-  yb = xb < -125.f ? 0.f : __int_as_float(__float_as_int(pb) + (__float_as_int(tb) << 23));
-}
-
 // ---- programmatic dependent launch ----------------------------------------------------
 // Kernels of the decode path are launched with programmatic stream
 // serialization: a kernel may start (and do its set-up) while the previous

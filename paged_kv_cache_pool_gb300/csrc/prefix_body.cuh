@@ -361,20 +361,17 @@ __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixI
         }
         m_used = m_new;
       }
-      // P = 2^(s*scale - m): three pairs in four on MUFU, one on the FMA pipe
+      // P = 2^(s*scale - m), every exponential on MUFU: the softmax is bound by
+      // issue on the FMA pipe (scale, max, sum, pack), not by MUFU, so moving
+      // exponentials to a polynomial on the FMA pipe measured slower
       const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2), nm2 = f2pack(-m_used, -m_used);
       uint32_t pk[BN / 2];
       uint64_t sum4[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int c = 0; c < BN / 2; ++c) {
-        float xa, xb, a, b2;
+        float xa, xb;
         f2unpack(ffma2(f2pack(s[2 * c], s[2 * c + 1]), sc2, nm2), xa, xb);
-        if ((c & 3) == 3) {
-          exp2_poly_pair(xa, xb, a, b2);
-        } else {
-          a = ex2(xa);
-          b2 = ex2(xb);
-        }
+        const float a = ex2(xa), b2 = ex2(xb);
         sum4[c & 3] = fadd2(sum4[c & 3], f2pack(a, b2));
         pk[c] = pack_bf16x2(a, b2);
       }
