@@ -202,6 +202,17 @@ gk_status gk_plan_update(gk_plan* plan, const gk_batch* batch, void* stream);
 /* Frees the plan's buffers; its enqueued work must have completed. */
 void gk_plan_destroy(gk_plan* plan);
 gk_status gk_plan_info(const gk_plan* plan, gk_plan_summary* out);
+/* The gather partition of a plan (its host copy): which tokens each CTA gathers.
+ * dense = 0: the cascade suffix partition, 1: the flat one.  The counts come
+ * first: *n_ctas gather CTAs and *n_segs segments.  Then, when begin and segs
+ * are not NULL, begin[0 .. n_ctas] receives the offsets of each CTA's
+ * segments (CTA b: [begin[b], begin[b + 1])) and segs[4 * i .. 4 * i + 3]
+ * segment i: request, first token, end token (in the request's own order: the
+ * dense partition counts the HOT prefix first), and the partial state it
+ * writes (-1: the request's output).  Host only; GK_ERR_INVALID for a NULL
+ * plan or count pointer. */
+gk_status gk_plan_segments(const gk_plan* plan, int32_t dense, int32_t* n_ctas, int32_t* n_segs, int32_t* begin,
+                           int32_t* segs);
 
 /* Flat paged attention (the dense backend): each request attends its prefix
  * (read from HOT, once per request) and its COLD suffix in one online-softmax
@@ -275,9 +286,10 @@ typedef struct gk_cost_model {
  *   sequential plan (W = ceil(prefix_ctas / SMs) waves of prefix items):
  *     T_levels = max(prefix_bytes / bw_prefix, W * (C * prefix_tile + prefix_item))
  *                + c_gather + suffix_bytes / bw_suffix
- *   split plan (see gk_plan_summary.cascade_split):
- *     T_levels = max(C * prefix_tile + prefix_item,
- *                    suffix_bytes / min(bw_suffix, suffix_ctas * gather_sm))
+ *   split plan (see gk_plan_summary.cascade_split; item = C * prefix_tile + prefix_item):
+ *     T_levels = max(item, (suffix_bytes / gather_sm + prefix_ctas * item) / SMs,
+ *                    (suffix_bytes + prefix_bytes) / bw_suffix)
+ *   (the middle term spreads the gather's SM-time and the items over every SM)
  * A plan without prefix work has no prefix term.  GraniKV's M_eff (Eq. 2)
  * enters through the items: a group of M_eff stacked rows gives ceil(M_eff/256)
  * items per KV head and key split.  Dense is chosen only when strictly faster.

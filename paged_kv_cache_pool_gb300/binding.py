@@ -84,6 +84,7 @@ _SIGS = {
     "gk_plan_update": (c_i32, [c_vp, P(gk_batch), c_vp]),
     "gk_plan_destroy": (None, [c_vp]),
     "gk_plan_info": (c_i32, [c_vp, P(gk_plan_summary)]),
+    "gk_plan_segments": (c_i32, [c_vp, c_i32, P(c_i32), P(c_i32), c_vp, c_vp]),
     "gk_decode_dense": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch), c_vp]),
     "gk_decode_cascade": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch), c_vp]),
     "gk_decode_dense_static": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch)]),
@@ -319,6 +320,17 @@ def gk_plan_info(plan):
     s = gk_plan_summary()
     _check(lib().gk_plan_info(plan, ctypes.byref(s)))
     return {name: getattr(s, name) for name, _ in gk_plan_summary._fields_}
+
+
+def gk_plan_segments(plan, dense=False):
+    """(begin [n_ctas + 1], segs [n_segs, 4] = request, t0, t1, entry): the plan's gather partition."""
+    n_ctas, n_segs = c_i32(), c_i32()
+    _check(lib().gk_plan_segments(plan, int(bool(dense)), ctypes.byref(n_ctas), ctypes.byref(n_segs), None, None))
+    begin = np.zeros(n_ctas.value + 1, dtype=np.int32)
+    segs = np.zeros((n_segs.value, 4), dtype=np.int32)
+    _check(lib().gk_plan_segments(plan, int(bool(dense)), ctypes.byref(n_ctas), ctypes.byref(n_segs),
+                                  begin.ctypes.data_as(c_vp), segs.ctypes.data_as(c_vp)))
+    return begin, segs
 
 
 def gk_decode_dense(pool, stream, layer, batch, plan):

@@ -578,6 +578,25 @@ gk_status gk_plan_info(const gk_plan* plan, gk_plan_summary* out) {
   return GK_OK;
 }
 
+gk_status gk_plan_segments(const gk_plan* plan, int32_t dense, int32_t* n_ctas, int32_t* n_segs, int32_t* begin,
+                           int32_t* segs) {
+  if (!plan || !n_ctas || !n_segs) return GK_ERR_INVALID;
+  const Plan& pl = plan->impl;
+  const std::vector<int32_t>& bg = dense ? pl.dense_seg_begin : pl.suf_seg_begin;
+  const std::vector<gk::SegmentDev>& sg = dense ? pl.dense_segs : pl.suf_segs;
+  *n_ctas = bg.empty() ? 0 : (int32_t)bg.size() - 1;
+  *n_segs = (int32_t)sg.size();
+  if (begin) std::copy(bg.begin(), bg.end(), begin);
+  if (segs)
+    for (size_t i = 0; i < sg.size(); ++i) {
+      segs[4 * i] = sg[i].req;
+      segs[4 * i + 1] = sg[i].t0;
+      segs[4 * i + 2] = sg[i].t1;
+      segs[4 * i + 3] = sg[i].entry;
+    }
+  return GK_OK;
+}
+
 gk_status gk_dispatch(const gk_pool* pool, const gk_plan* plan, gk_backend* choice, double* t_dense_us,
                       double* t_cascade_us) {
   if (!pool || !plan || !choice) return GK_ERR_INVALID;

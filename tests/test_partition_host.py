@@ -1,0 +1,129 @@
+"""The gather partitions of a plan (gk_plan_segments), on the host.
+
+Every token of every request is gathered exactly once; a CTA's segments are one
+contiguous piece of the concatenated token stream; the quotas follow the
+planner's rule (equal quotas of at least 64 tokens, multiples of 16, over at
+most one CTA per SM, the last CTA taking the rest; a split plan: one slot per
+SM, its end in the stream rounded to 16, a prefix CTA's slot no larger than a
+gather-only CTA's); the partial states of a request are one contiguous range
+of entries, which is how the merge reads them.
+"""
+import random
+
+import numpy as np
+import pytest
+
+from oracle import dispatch as odisp
+
+SMS = 152
+
+
+@pytest.fixture(scope="module")
+def gk():
+    from paged_kv_cache_pool_gb300 import build
+    build.build()
+    from paged_kv_cache_pool_gb300 import binding
+    return binding
+
+
+def _plan(gk, pool, bases, lps, slens):
+    b = gk.Batch(bases, lps, slens, None, 8192)
+    return b, gk.gk_plan_build(pool, b)
+
+
+def _check_cover(begin, segs, lengths):
+    """Each request's [0, n) covered once; CTA b's segments continue the stream where CTA b-1 stopped."""
+    assert begin[0] == 0 and begin[-1] == len(segs) and np.all(np.diff(begin) >= 0)
+    pos = 0            # position in the concatenated stream
+    starts = np.concatenate([[0], np.cumsum(lengths)])
+    for r, t0, t1, _ in segs.tolist():
+        assert 0 <= t0 < t1 <= lengths[r]
+        assert starts[r] + t0 == pos, "segments leave a gap or overlap in the stream"
+        pos = starts[r] + t1
+    assert pos == sum(lengths)
+
+
+def _tokens(begin, segs):
+    return [int(sum(segs[i, 2] - segs[i, 1] for i in range(begin[b], begin[b + 1]))) for b in range(len(begin) - 1)]
+
+
+def _check_entries(segs, dense):
+    by_req = {}
+    for r, _, _, e in segs.tolist():
+        by_req.setdefault(r, []).append(e)
+    seen = set()
+    for r, es in by_req.items():
+        if dense and es == [-1]:
+            continue       # one segment: it writes the request's output itself
+        assert -1 not in es
+        assert es == list(range(es[0], es[0] + len(es)))     # consecutive, in stream order
+        assert not seen & set(es)
+        seen |= set(es)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_even_partitions(gk, seed):
+    """Sequential cascade and flat partitions of random batches."""
+    rnd = random.Random(seed)
+    pool = gk.gk_pool_create(1, 32, 8, 128, 40000, 1 << 20, 16, 0)
+    try:
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SEQUENTIAL)
+        prefixes = {lp: gk.gk_prefix_alloc(pool, lp) for lp in (300, 2000)}
+        bases, lps, slens = [], [], []
+        for _ in range(rnd.randint(1, 90)):
+            lp = rnd.choice([300, 2000, 0])
+            bases.append(prefixes[lp] if lp else -1)
+            lps.append(lp)
+            slens.append(rnd.choice([0, rnd.randint(1, 40), rnd.randint(1, rnd.choice([200, 3000]))]))
+        _, plan = _plan(gk, pool, bases, lps, slens)
+        s = gk.gk_plan_info(plan)
+        for dense in (False, True):
+            lengths = [lp + sl for lp, sl in zip(lps, slens)] if dense else list(slens)
+            total = sum(lengths)
+            begin, segs = gk.gk_plan_segments(plan, dense)
+            ctas = len(begin) - 1
+            assert ctas == odisp.gather_ctas(total, SMS) == s["dense_ctas" if dense else "suffix_ctas"]
+            _check_cover(begin, segs, lengths)
+            _check_entries(segs, dense)
+            if ctas:
+                quota = -(-max(-(-total // SMS), 64) // 16) * 16
+                t = _tokens(begin, segs)
+                assert t[:-1] == [quota] * (ctas - 1) and 0 < t[-1] <= quota
+        gk.gk_plan_destroy(plan)
+    finally:
+        gk.gk_pool_destroy(pool)
+
+
+@pytest.mark.parametrize("C", [0, 16, 32])
+def test_split_partition(gk, C):
+    """Split plan, one group of 64 requests (Lp 16384, 1000 suffix tokens each):
+    one slot per SM, slot ends on multiples of 16, prefix slots no larger than the others."""
+    pool = gk.gk_pool_create(1, 32, 8, 128, 16384 + 16, 64 * 1000 + 64, 1, 0)
+    try:
+        base = gk.gk_prefix_alloc(pool, 16384)
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SPLIT, C)
+        _, plan = _plan(gk, pool, [base] * 64, [16384] * 64, [1000] * 64)
+        s = gk.gk_plan_info(plan)
+        assert s["cascade_split"] == 1 and s["suffix_ctas"] == SMS
+        n_pre = s["prefix_ctas"]
+        begin, segs = gk.gk_plan_segments(plan, False)
+        _check_cover(begin, segs, [1000] * 64)
+        _check_entries(segs, False)
+        t = _tokens(begin, segs)
+        ends = np.cumsum(t)
+        assert all(e % 16 == 0 for e in ends[:-1]) and ends[-1] == 64000
+        assert max(t[:n_pre]) <= min(t[n_pre:-1])
+        assert max(t[n_pre:-1]) - min(t[n_pre:-1]) <= 16
+        # partial states: one per (request, key split) and one per suffix segment
+        splits = -(-128 // s["prefix_tiles_per_item"])
+        assert s["num_partials"] == 64 * splits + len(segs)
+        gk.gk_plan_destroy(plan)
+    finally:
+        gk.gk_pool_destroy(pool)
+
+
+def test_segments_argument_errors(gk):
+    import ctypes
+    with pytest.raises(gk.GkError):
+        gk._check(gk.lib().gk_plan_segments(None, 0, ctypes.byref(ctypes.c_int32()), ctypes.byref(ctypes.c_int32()),
+                                            None, None))
