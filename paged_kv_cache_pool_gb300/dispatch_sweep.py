@@ -1,0 +1,171 @@
+"""Where the two backends cross on this GPU, and how often the dispatcher routes
+to each (GraniKV Appendix B.4 and B.4b, re-run: the pages fit the saturation
+threshold M_sat = 1024 on A100 and say it must be re-fit on other hardware).
+
+Two parts:
+
+  measure  On one layer of a synthetic pool (random bf16 data), for every cell
+           of an (Lp, B) grid with one shared prefix and suffixes drawn from
+           U{16..512} (the pages' 16..512-token user turns), time the flat
+           (dense) backend and the cascade with CUDA events, L2 flushed before
+           every launch, and record the dispatcher's choice and predictions.
+           Per cell: M_eff = B * g (GraniKV Eq. 2), the faster backend, and the
+           regret of the dispatcher's pick (its time over the faster one's, - 1).
+
+  trace    Host only.  Per (Lp, B) cell, 200 decode steps whose realised batch
+           is B plus a Poisson(B / 8) burst of requests whose prefill overlaps
+           the step (the pages' reason the realised batch exceeds the admission
+           batch), suffixes redrawn every step; the fraction of steps the
+           dispatcher routes to the dense backend (the pages' Table 15).
+
+    python -m paged_kv_cache_pool_gb300.dispatch_sweep measure [--out rows.json]
+    python -m paged_kv_cache_pool_gb300.dispatch_sweep trace
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+
+import numpy as np
+
+from . import binding as gk
+
+LPS = (512, 2048, 8192, 16384)
+BS = (8, 32, 128, 256, 512)
+S_RANGE = (16, 512)
+COST_MODEL = os.path.join(os.path.dirname(os.path.abspath(__file__)), "cost_model_gb300.json")
+
+
+def _load_cost_model(pool, path):
+    if path and os.path.exists(path):
+        with open(path) as f:
+            gk.gk_cost_model_load(pool, f.read())
+
+
+def _suffixes(rng, n):
+    return rng.integers(S_RANGE[0], S_RANGE[1] + 1, n).astype(np.int32)
+
+
+def measure(lps=LPS, bs=BS, Hq=32, Hkv=8, d=128, reps=5, seed=7, cost_model=COST_MODEL):
+    """-> list of per-cell dicts (times in microseconds)."""
+    import torch
+    from .engine import Engine
+    g = Hq // Hkv
+    cold = max(bs) * S_RANGE[1] + 4096
+    eng = Engine(1, Hq, Hkv, d, sum(lps) + 16 * len(lps), cold, 1, seed=1)
+    for t in (eng.hot_k, eng.hot_v, eng.cold_k, eng.cold_v):
+        t.normal_()
+    pool = eng.pool
+    _load_cost_model(pool, cost_model)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=eng.device)   # larger than L2
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        ts = []
+        for _ in range(reps + 1):
+            flush.zero_()
+            ev0.record()
+            fn()
+            ev1.record()
+            torch.cuda.synchronize()
+            ts.append(ev0.elapsed_time(ev1) * 1e3)
+        return float(np.median(ts[1:]))
+
+    rows = []
+    for lp in lps:
+        base = eng.prefix_alloc(lp)
+        for B in bs:
+            rng = np.random.default_rng([seed, lp, B])
+            s = _suffixes(rng, B)
+            seqs = [eng.seq_create() for _ in range(B)]
+            eng.append_slots(np.repeat(np.asarray(seqs, np.int32), s))
+            table = eng.block_tables(seqs)
+            d_table = eng.to_device(table)
+            batch = eng.batch([base] * B, [lp] * B, s.tolist(), d_table, table.shape[1])
+            q = torch.randn((B, Hq, d), device=eng.device).to(torch.bfloat16)
+            out = torch.empty((B, Hq, d), device=eng.device)
+            lse = torch.empty((B, Hq), device=eng.device)
+            batch.set_device(d_q=q, d_out=out, d_lse=lse)
+            plan = gk.gk_plan_build(pool, batch)
+            info = gk.gk_plan_info(plan)
+            choice, p_dense, p_cas = gk.gk_dispatch(pool, plan)
+            t_dense = timed(lambda: gk.gk_decode_dense(pool, None, 0, batch, plan))
+            t_cas = timed(lambda: gk.gk_decode_cascade(pool, None, 0, batch, plan))
+            if gk.gk_device_error(pool) != gk.GK_OK:
+                raise RuntimeError(f"device error at Lp={lp} B={B}")
+            picked = t_dense if choice == gk.GK_BACKEND_DENSE else t_cas
+            rows.append(dict(Lp=lp, B=B, M_eff=B * g, suffix_tokens=int(s.sum()),
+                             t_dense_us=t_dense, t_cascade_us=t_cas,
+                             pred_dense_us=p_dense, pred_cascade_us=p_cas,
+                             choice="dense" if choice == gk.GK_BACKEND_DENSE else "cascade",
+                             faster="dense" if t_dense < t_cas else "cascade",
+                             regret=picked / min(t_dense, t_cas) - 1.0,
+                             split=info["cascade_split"], prefix_ctas=info["prefix_ctas"]))
+            gk.gk_plan_destroy(plan)
+            for sq in seqs:
+                eng.seq_release(sq)
+        gk.gk_prefix_release(pool, base)
+    eng.close()
+    return rows
+
+
+def crossover(rows):
+    """Per Lp: the smallest M_eff of the grid at which dense is measured faster (None: never)."""
+    out = {}
+    for lp in sorted({r["Lp"] for r in rows}):
+        wins = [r["M_eff"] for r in rows if r["Lp"] == lp and r["faster"] == "dense"]
+        out[lp] = min(wins) if wins else None
+    return out
+
+
+def trace(lps=LPS, bs=BS, Hq=32, Hkv=8, d=128, steps=200, seed=11, cost_model=COST_MODEL, num_sms=None):
+    """-> {(Lp, B): fraction of steps routed to dense} on a host-only pool."""
+    burst_max = max(bs) * 2
+    pool = gk.gk_pool_create(1, Hq, Hkv, d, sum(lps) + 16 * len(lps), burst_max * S_RANGE[1] + 4096, 1, 0)
+    try:
+        _load_cost_model(pool, cost_model)
+        frac = {}
+        for lp in lps:
+            base = gk.gk_prefix_alloc(pool, lp)
+            for B in bs:
+                rng = np.random.default_rng([seed, lp, B])
+                dense = 0
+                for _ in range(steps):
+                    n = B + int(rng.poisson(B / 8))
+                    s = _suffixes(rng, n)
+                    batch = gk.Batch([base] * n, [lp] * n, s.tolist(), None, S_RANGE[1])
+                    plan = gk.gk_plan_build(pool, batch)
+                    dense += gk.gk_dispatch(pool, plan)[0] == gk.GK_BACKEND_DENSE
+                    gk.gk_plan_destroy(plan)
+                frac[(lp, B)] = dense / steps
+            gk.gk_prefix_release(pool, base)
+        return frac
+    finally:
+        gk.gk_pool_destroy(pool)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("part", choices=["measure", "trace"])
+    ap.add_argument("--out", default=None)
+    a = ap.parse_args()
+    from . import build
+    build.build()
+    if a.part == "measure":
+        rows = measure()
+        for r in rows:
+            print(json.dumps(r))
+        print(json.dumps({"crossover_M_eff": crossover(rows)}))
+        if a.out:
+            with open(a.out, "w") as f:
+                json.dump(rows, f, indent=1)
+    else:
+        frac = trace()
+        print("routed to dense, Lp x B:", " ".join(f"{B:>6}" for B in BS))
+        for lp in LPS:
+            print(f"{lp:>26}", " ".join(f"{frac[(lp, B)]:6.0%}" for B in BS))
+
+
+if __name__ == "__main__":
+    main()
