@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kSplitThreads, 1) cascade_split_kernel(const S
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    griddep_wait();
+    // the item waits for the kernel before this one itself, after its table reads
     const bool ok = prefix::prefix_item<D>(f.pp, f.pp.items[b], base, ctl, ctl_ptr, tmem);
     __syncthreads();
     if (warp == 1) {

@@ -140,7 +140,10 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, int
 // bytes), `ctl` the control block (kCtlBytes, generic pointer ctl_ptr) whose
 // abort flag is zero on entry; `tmem` holds 512 allocated columns.  The
 // barriers are initialised here and invalidated before returning, so items can
-// run back to back.  Returns false (on every thread) when a wait timed out.
+// run back to back.  The item executes griddepcontrol.wait itself, after the
+// reads of the plan's tables and the barrier set-up (callers do not wait for
+// the previous kernel before calling it).  Returns false (on every thread) when
+// a wait timed out.
 template <int D>
 __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixItemDev it, uint32_t base, uint32_t ctl,
                                             uint8_t* ctl_ptr, uint32_t tmem) {
@@ -161,22 +164,17 @@ __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixI
   const void* tmV = p.tmaps + (size_t)(gr.tmap_index + 1) * 128;
   const int zc = p.layer * p.Hkv + it.head;
 
-  // softmax threads fetch their Q row now, so the global-load latency overlaps the set-up
   const int qi_ = (warp - 2) >> 2;
   const int row_ = (warp & 3) * 32 + lane;
   const int grow_ = row0 + qi_ * BM + row_;
   const bool softmax_warp = warp >= 2 && warp < kRoleWarps;
   const bool row_valid_ = softmax_warp && grow_ < gr.m;
   int req_ = 0, qh_ = 0;
+  int64_t entry_ = -1;  // the row's partial-state slot
   if (row_valid_) {
     req_ = p.prefix_reqs[gr.req_base + grow_ / p.G];
     qh_ = it.head * p.G + grow_ % p.G;
-  }
-  uint4 qrow[D / 8];
-  if (softmax_warp) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)req_ * p.Hq + qh_) * D);
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) qrow[c] = row_valid_ ? src[c] : make_uint4(0, 0, 0, 0);
+    entry_ = (int64_t)p.reqs[req_].entry_cas + it.split;
   }
   if (threadIdx.x == 0) {
     mbar_init(bar(B_QFULL), 256);
@@ -192,11 +190,27 @@ __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixI
     }
     mbar_init(bar(B_OFINAL), 1);
     fence_mbar_init();
-    // the first K/V tiles need nothing but the barriers: start them now so their
-    // latency overlaps the tensor-memory allocation and the Q staging
     if (ntiles > 0) {
       tmap_acquire(tmK);
       tmap_acquire(tmV);
+    }
+  }
+  // Everything above reads only the plan's tables, which the kernels of a step
+  // never write, so it runs while the kernel before this one finishes.  The
+  // queries, the HOT pool (a slab write may precede the decode) and the
+  // partial states (the previous merge reads them) wait for it.
+  griddep_wait();
+  // softmax threads fetch their Q row now, so the global-load latency overlaps the set-up
+  uint4 qrow[D / 8];
+  if (softmax_warp) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)req_ * p.Hq + qh_) * D);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) qrow[c] = row_valid_ ? src[c] : make_uint4(0, 0, 0, 0);
+  }
+  if (threadIdx.x == 0) {
+    // the first K/V tiles need nothing but the barriers: start them now so their
+    // latency overlaps the Q staging
+    if (ntiles > 0) {
       for (int j = 0; j < NST && j < ntiles; ++j) {
         mbar_arrive_expect_tx(bar(B_KFULL + j), Lay::kTile);
         for (int h = 0; h < D / 64; ++h)
@@ -400,20 +414,21 @@ __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixI
       {
         float* dst = nullptr;
         if (row_valid) {
-          const int64_t entry = (int64_t)p.reqs[req].entry_cas + it.split;
-          dst = p.part_o + (entry * p.Hq + qh) * D;
-          p.part_l[entry * p.Hq + qh] = m_used + __log2f(l);
+          dst = p.part_o + (entry_ * p.Hq + qh) * D;
+          p.part_l[entry_ * p.Hq + qh] = m_used + __log2f(l);
         }
         asm volatile("st.shared.u64 [%0], %1;" ::"r"(dst_tab + row * 8), "l"((uint64_t)dst) : "memory");
       }
       const float inv = 1.f / l;
+      // two 32-column loads per wait
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
+      for (int c = 0; c < D / 32; c += 2) {
+        float o[64];
         tmem_ld32(tO(qi) + c * 32 + lane_off, o);
+        tmem_ld32(tO(qi) + (c + 1) * 32 + lane_off, o + 32);
         tc_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
+        for (int e = 0; e < 64; e += 4)
           sts128(stage + row * kRowBytes + (c * 32 + e) * 4,
                  make_uint4(__float_as_uint(o[e] * inv), __float_as_uint(o[e + 1] * inv),
                             __float_as_uint(o[e + 2] * inv), __float_as_uint(o[e + 3] * inv)));
@@ -423,7 +438,7 @@ __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixI
       constexpr int kLanesPerRow = D / 4;
       constexpr int kRowsPerPass = 32 / kLanesPerRow;
       const int sub = lane % kLanesPerRow;
-#pragma unroll 1
+#pragma unroll 4
       for (int r0 = 0; r0 < 32; r0 += kRowsPerPass) {
         const int rr = wq * 32 + r0 + lane / kLanesPerRow;
         uint64_t dst;

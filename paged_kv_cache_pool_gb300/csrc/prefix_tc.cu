@@ -42,11 +42,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_kernel(const PrefixParams 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // plan tables and the HOT pool are not written by the kernels of a decode
-  // step; the queries and the partial-state buffer may be, so wait for them
-  griddep_wait();
-  // one item per CTA: a loop over items here costs the softmax warps registers
+  // one item per CTA: a loop over items here costs the softmax warps registers.
+  // The item waits for the kernel before this one itself, after its table reads.
   if ((int)blockIdx.x < n_items) prefix_item<D>(p, p.items[blockIdx.x], base, ctl, ctl_ptr, tmem);
+  else griddep_wait();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
