@@ -62,6 +62,9 @@ int fill_gather_params(const LaunchCommon& lc, int32_t layer, const gk_batch* b,
   gp.Hkv = c.num_kv_heads;
   gp.Hq = c.num_q_heads;
   gp.page = c.cold_page_size;
+  gp.page_shift = -1;
+  for (int sh = 0; sh < 31; ++sh)
+    if ((1 << sh) == c.cold_page_size) gp.page_shift = sh;
   gp.layer = layer;
   gp.dense = dense ? 1 : 0;
   gp.block_table = b->d_block_table;

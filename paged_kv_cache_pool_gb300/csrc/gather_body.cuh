@@ -51,6 +51,7 @@ struct GatherParams {
   int64_t cold_slots;
   int64_t n_blocks;
   int32_t L, Hkv, Hq, page;
+  int32_t page_shift;  // log2(page) when page is a power of two, else -1
   int32_t layer;
   int32_t dense;
   const int32_t* block_table;
@@ -236,16 +237,17 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
       e.row0 = c.hot_row0 + (int64_t)c.t * D;
     } else {
       e.tt0 = c.t - c.lp;
-      e.blk = lane < n ? c.table[(e.tt0 + lane) / p.page] : -1;
+      const int ti = e.tt0 + lane;
+      e.blk = lane < n ? c.table[p.page_shift >= 0 ? ti >> p.page_shift : ti / p.page] : -1;
       const int fi = c.slen - 1 - e.tt0;
       if (fused_append && fi >= 0 && fi < n) e.meta |= (uint32_t)(fi + 1) << 6;
     }
     return e;
   };
-  int issued = 0;
+  int islot = 0;  // ring slot of the next stage copied
   auto copy_stage = [&](const Entry& e) {
     if (e.n() > 0) {
-      const uint32_t kdst = ring + (uint32_t)(issued % nst) * WS, vdst = kdst + kT * SR;
+      const uint32_t kdst = ring + (uint32_t)islot * WS, vdst = kdst + kT * SR;
       if (DENSE && e.hot()) {
         // HOT: the stage's rows of this head are contiguous
         for (int ci = lane; ci < e.n() * CPT; ci += 32) {
@@ -258,8 +260,10 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
         const int n = e.n(), fresh = e.fresh();
         int64_t off = -1;
         if (lane < n) {
+          const int ti = e.tt0 + lane;
+          const int in_page = p.page_shift >= 0 ? ti & (p.page - 1) : ti % p.page;
           if (e.blk >= 0 && e.blk < p.n_blocks)
-            off = ((layer_rows + (int64_t)e.blk * p.page + (e.tt0 + lane) % p.page) * Hkv + h) * D;
+            off = ((layer_rows + (int64_t)e.blk * p.page + in_page) * Hkv + h) * D;
           else
             report_error(p.err, kErrBounds);
         }
@@ -272,7 +276,7 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
           if (lane == fresh) off = -1;
         }
         if (lane == 0)
-          sts128(recs + (uint32_t)(issued % nst) * kFreshRecBytes,
+          sts128(recs + (uint32_t)islot * kFreshRecBytes,
                  make_uint4((uint32_t)(fresh_off >= 0 ? fresh : -1), (uint32_t)fresh_off,
                             (uint32_t)(fresh_off >> 32), 0u));
 #pragma unroll
@@ -292,13 +296,13 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
           cp_async16(vdst + o, p.new_v + fs);
         }
         cp_async_commit();
-        ++issued;
+        if (++islot == nst) islot = 0;
         return;
       }
     }
-    if (lane == 0) sts128(recs + (uint32_t)(issued % nst) * kFreshRecBytes, make_uint4(0xffffffffu, 0u, 0u, 0u));
+    if (lane == 0) sts128(recs + (uint32_t)islot * kFreshRecBytes, make_uint4(0xffffffffu, 0u, 0u, 0u));
     cp_async_commit();
-    ++issued;
+    if (++islot == nst) islot = 0;
   };
   // the queue: q0 is copied next, q3 was looked up last
   Cursor lk = cursor_at(seg0);
@@ -324,7 +328,7 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
   const int gq = lane >> 2;  // fragment row group
   const int tq = lane & 3;   // fragment column pair
   const int mi = lane >> 3, mj = lane & 7;  // ldmatrix: matrix index, row within it
-  int k = 0;
+  int cslot = 0;  // ring slot of the stage computed next
   for (int sg = seg0; sg < seg1; ++sg) {
     const SegmentDev seg = p.segs[sg];
     const int lp = DENSE ? p.reqs[seg.req].lp : 0;
@@ -350,10 +354,10 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
       issue_next();                  // stage k + nst - 1
       cp_async_wait_pending(nst - 1);  // stage k has landed (this lane's copies) ...
       __syncwarp();                  // ... and every lane's
-      const uint32_t ks = ring + (uint32_t)(k % nst) * WS, vs = ks + kT * SR;
+      const uint32_t ks = ring + (uint32_t)cslot * WS, vs = ks + kT * SR;
       if (fused_append) {
         // the request's appended token is in this stage: put head h's rows into the pool
-        const uint4 rec = lds128(recs + (uint32_t)(k % nst) * kFreshRecBytes);
+        const uint4 rec = lds128(recs + (uint32_t)cslot * kFreshRecBytes);
         const int ft = (int)rec.x;
         if (ft >= 0 && lane < CPT) {
           const int64_t off = (int64_t)(((uint64_t)rec.z << 32) | rec.y);
@@ -365,14 +369,19 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
       }
       // address of 16-byte chunk c of token row tok in a slice
       auto chunk_addr = [&](uint32_t slice, int tok, int c) -> uint32_t { return slice + (uint32_t)tok * SR + c * 16; };
-      // S^T = K Q_h^T
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      // S^T = K Q_h^T, the even and odd k16 steps in two accumulators (two
+      // MMA dependency chains of half the length)
+      float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int kk = 0; kk < KSTEPS; ++kk) {
-        uint32_t a0, a1, a2, a3;
+      for (int kk = 0; kk < KSTEPS; kk += 2) {
+        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
         ldsm_x4(chunk_addr(ks, mj + 8 * (mi & 1), 2 * kk + (mi >> 1)), a0, a1, a2, a3);
+        ldsm_x4(chunk_addr(ks, mj + 8 * (mi & 1), 2 * (kk + 1) + (mi >> 1)), b0, b1, b2, b3);
         mma16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        mma16816(sd, b0, b1, b2, b3, qb[kk + 1][0], qb[kk + 1][1]);
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sc[i] += sd[i];
       // online softmax over the 16 tokens (rows gq and gq+8) for heads 2tq, 2tq+1
       const bool v_lo = gq < n, v_hi = gq + 8 < n;
       const float s00 = v_lo ? sc[0] * p.q_scale : -INFINITY;
@@ -412,7 +421,7 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
       }
       __syncwarp();                  // every lane has read the stage before it is refilled
       t += n;
-      ++k;
+      if (++cslot == nst) cslot = 0;
     }
 
     // finish: the row sums live on the 8 lanes that share tq
