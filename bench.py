@@ -49,6 +49,8 @@ def _args():
     ap.add_argument("--layers", type=int, default=0, help="run only this many layers (small profiling case)")
     ap.add_argument("--append", choices=["fused", "separate"], default="fused",
                     help="the step's new tokens written by the decode itself, or by gk_append_kv first")
+    ap.add_argument("--prefix-tiles", type=int, default=0,
+                    help="split cascade with this many 128-key tiles per prefix item (default: the planner's choice)")
     return ap.parse_args()
 
 
@@ -255,6 +257,8 @@ def run_ours(a, w):
     cm_path = os.path.join(ROOT, "paged_kv_cache_pool_gb300", "cost_model_gb300.json")
     if os.path.exists(cm_path):
         gk.gk_cost_model_load(pool, open(cm_path).read())
+    if a.prefix_tiles > 0:
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SPLIT, a.prefix_tiles)
     L, B, Hq, Hkv, d = w.L, w.B, w.Hq, w.Hkv, w.d
     stream = torch.cuda.current_stream()
     bf = torch.bfloat16

@@ -277,6 +277,8 @@ typedef struct gk_cost_model {
   double prefix_item_us;          /* fixed cost of a prefix work item (of each wave of them) */
   double gather_sm_gbs;           /* suffix gather bandwidth one SM sustains (split plans) */
   double c_gather_us;             /* fixed cost of a separate suffix-gather launch (sequential plans) */
+  double prefix_tile_split_us;    /* prefix_tile_us for an item of a split plan, which runs beside a
+                                     gather that keeps HBM busy (its K/V tiles wait longer) */
 } gk_cost_model;
 
 /* Predict both backends for the plan and pick the smaller:
@@ -286,7 +288,7 @@ typedef struct gk_cost_model {
  *   sequential plan (W = ceil(prefix_ctas / SMs) waves of prefix items):
  *     T_levels = max(prefix_bytes / bw_prefix, W * (C * prefix_tile + prefix_item))
  *                + c_gather + suffix_bytes / bw_suffix
- *   split plan (see gk_plan_summary.cascade_split; item = C * prefix_tile + prefix_item):
+ *   split plan (see gk_plan_summary.cascade_split; item = C * prefix_tile_split + prefix_item):
  *     T_levels = max(item, (suffix_bytes / gather_sm + prefix_ctas * item) / SMs,
  *                    (suffix_bytes + prefix_bytes) / bw_suffix)
  *   (the middle term spreads the gather's SM-time and the items over every SM)
@@ -317,7 +319,8 @@ gk_status gk_pool_set_cascade_mode(gk_pool* pool, gk_cascade_mode mode, int32_t 
 gk_status gk_cost_model_get(const gk_pool* pool, gk_cost_model* cm);
 /* Same as gk_cost_model_set from JSON text: {"c_flat_us": .., "bw_flat_gbs": ..,
  * "c_cascade_us": .., "bw_prefix_gbs": .., "bw_suffix_gbs": .., "c_merge_us": ..,
- * "prefix_tile_us": .., "prefix_item_us": .., "gather_sm_gbs": .., "c_gather_us": ..}.
+ * "prefix_tile_us": .., "prefix_item_us": .., "gather_sm_gbs": .., "c_gather_us": ..,
+ * "prefix_tile_split_us": ..}.
  * Keys left out keep their current values; other keys are skipped. */
 gk_status gk_cost_model_load(gk_pool* pool, const char* json);
 

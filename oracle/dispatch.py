@@ -9,10 +9,11 @@ predicted time runs (flat wins only when strictly faster):
 
   T_flat    = c_flat + bytes_flat / bw_flat
   T_cascade = c_cascade + T_levels + c_merge * B * Hq
-  item(C)   = C * prefix_tile + prefix_item        (one prefix work item of C key tiles)
+  item(C)   = C * prefix_tile + prefix_item        (one prefix work item of C key tiles, alone)
+  item'(C)  = C * prefix_tile_split + prefix_item  (the same beside a gather that keeps HBM busy)
   T_levels  = max(bytes_pre / bw_prefix, W * item(C)) + c_gather
               + bytes_suffix / bw_suffix                          (sequential plan)
-            = max(item(C), (bytes_suffix / gather_sm + n_pre * item(C)) / SMs,
+            = max(item'(C), (bytes_suffix / gather_sm + n_pre * item'(C)) / SMs,
                   (bytes_suffix + bytes_pre) / bw_suffix)          (split plan)
 
 Work items: a group of M_eff stacked rows and Lp keys contributes ceil(M/256)
@@ -24,7 +25,10 @@ first runs prefix item b, and every CTA gathers a slot of the suffix, a prefix
 CTA's slot cut to the time its item leaves (the middle term spreads the
 gather's SM-time and the items over all SMs; the last is HBM).  The planner
 takes the C with the smallest split prediction (the largest C among equal
-ones, i.e. the fewest items), among those with no more items than SMs, then
+ones, i.e. the fewest items), among those with no more items than SMs whose
+prefix CTAs keep a gather share of at least MIN_PREFIX_SHARE (share =
+max(0, T - item'(C) - c_gather) / T; a forced split with no such C takes the
+best prediction), then
 lowers C to the smallest value giving as many items (balanced items), and
 splits when that beats the sequential T_levels.  A sequential plan's gather
 partition cuts the suffix tokens into quotas of ceil(total/n) rounded up to 64
@@ -93,8 +97,9 @@ def sequential_tiles(f, num_sms):
     return best_c
 
 
-def item_us(cm, C):
-    return C * cm["prefix_tile_us"] + cm["prefix_item_us"]
+def item_us(cm, C, split=False):
+    """A prefix item of C key tiles: alone (sequential plans) or beside the gather (split plans)."""
+    return C * cm["prefix_tile_split_us" if split else "prefix_tile_us"] + cm["prefix_item_us"]
 
 
 def sequential_levels(cm, f, C, num_sms):
@@ -105,8 +110,17 @@ def sequential_levels(cm, f, C, num_sms):
     return t
 
 
+# a split C qualifies only if its prefix CTAs keep this share of a gather-only CTA's suffix
+MIN_PREFIX_SHARE = 0.15
+
+
+def prefix_share(cm, C, T):
+    """Gather share of a prefix CTA (relative to a gather-only CTA) for items of C tiles, launch T."""
+    return max(0.0, T - item_us(cm, C, split=True) - cm["c_gather_us"]) / T
+
+
 def split_levels(cm, f, C, n_pre, num_sms):
-    it = item_us(cm, C)
+    it = item_us(cm, C, split=True)
     bytes_pre = sum(p["bytes"] for p in f["prefix"])
     bal = (f["bytes_suffix"] / (cm["gather_sm_gbs"] * 1e3) + n_pre * it) / num_sms
     return max(it, bal, (f["bytes_suffix"] + bytes_pre) / (cm["bw_suffix_gbs"] * 1e3))
@@ -126,6 +140,8 @@ def arrangement(cm, f, num_sms):
         if items > num_sms:
             break
         t = split_levels(cm, f, C, items, num_sms)
+        if prefix_share(cm, C, t) < MIN_PREFIX_SHARE:
+            continue
         if best is None or t < best - 1e-9:
             best, best_c = t, C
     if best is None or not best < sequential_levels(cm, f, c_seq, num_sms):

@@ -58,7 +58,7 @@ class gk_plan_summary(ctypes.Structure):
 class gk_cost_model(ctypes.Structure):
     _fields_ = [("c_flat_us", c_dbl), ("bw_flat_gbs", c_dbl), ("c_cascade_us", c_dbl), ("bw_prefix_gbs", c_dbl),
                 ("bw_suffix_gbs", c_dbl), ("c_merge_us", c_dbl), ("prefix_tile_us", c_dbl), ("prefix_item_us", c_dbl),
-                ("gather_sm_gbs", c_dbl), ("c_gather_us", c_dbl)]
+                ("gather_sm_gbs", c_dbl), ("c_gather_us", c_dbl), ("prefix_tile_split_us", c_dbl)]
 
 
 P = ctypes.POINTER
@@ -375,7 +375,7 @@ def gk_cost_model_get(pool):
 
 
 COST_MODEL_KEYS = ("c_flat_us", "bw_flat_gbs", "c_cascade_us", "bw_prefix_gbs", "bw_suffix_gbs", "c_merge_us",
-                   "prefix_tile_us", "prefix_item_us", "gather_sm_gbs", "c_gather_us")
+                   "prefix_tile_us", "prefix_item_us", "gather_sm_gbs", "c_gather_us", "prefix_tile_split_us")
 
 
 def gk_cost_model_set(pool, cm: dict):

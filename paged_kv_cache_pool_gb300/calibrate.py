@@ -6,6 +6,8 @@ Times, with CUDA events, on one layer of synthetic pools (random bf16 data):
   * the suffix gather over every SM, several volumes        -> c_gather_us + bytes / bw_suffix_gbs
   * prefix items of C key tiles, forced split plans and the -> prefix_item_us + C * prefix_tile_us
     sequential plans of several M_eff = B * g
+  * the tile of an item beside the gather                   -> prefix_tile_split_us = SPLIT_TILE_RATIO *
+                                                               prefix_tile_us
   * the gather alone on the SMs long prefix items leave it  -> gather_sm_gbs
   * the merge                                               -> c_merge_us per (request, head)
   * the whole cascade, both arrangements                    -> c_cascade_us (mean residual)
@@ -127,6 +129,13 @@ def calibrate(Hq=32, Hkv=8, d=128, device="cuda"):
                       cascade_info=[dict({k: i[k] for k in keep}, B=B, Hq=Hq) for i, _, B in cas_pts]))
 
 
+# An item of a split plan shares HBM with a gather that keeps it busy, and its
+# K/V tiles wait longer: on GB300 a 32-tile item beside the benchmark layer's
+# gather ran 1.9-2.0 us per tile against 1.53-1.56 us alone (per-phase
+# %globaltimer stamps in an instrumented build), a ratio of about 1.28.
+SPLIT_TILE_RATIO = 1.28
+
+
 def _linfit(pts):
     x = np.array([p[0] for p in pts], float)
     y = np.array([p[1] for p in pts], float)
@@ -143,7 +152,8 @@ def refit(measured, num_sms=152):
     item, tile = _linfit(measured["tile"])
     cm = dict(c_flat_us=c_flat, bw_flat_gbs=1.0 / max(s_flat, 1e-12) / 1e3, c_cascade_us=0.0,
               bw_prefix_gbs=6000.0, bw_suffix_gbs=1.0 / max(s_suf, 1e-12) / 1e3, c_merge_us=max(s_mrg, 0.0),
-              prefix_tile_us=max(tile, 1e-3), prefix_item_us=item, gather_sm_gbs=44.0, c_gather_us=c_suf)
+              prefix_tile_us=max(tile, 1e-3), prefix_item_us=item, gather_sm_gbs=44.0, c_gather_us=c_suf,
+              prefix_tile_split_us=max(tile, 1e-3) * SPLIT_TILE_RATIO)
     # per-SM gather bandwidth: the suffix alone on the SMs the long items leave it
     per_sm = [bw / n for n, bw in measured["gather_sm"] if n > 0]
     if per_sm:
@@ -152,7 +162,8 @@ def refit(measured, num_sms=152):
     # of the whole cascade over the model when it is positive
     res = []
     for info, t_cas in zip(measured["cascade_info"], measured["cascade"]):
-        item_us = info["prefix_tiles_per_item"] * cm["prefix_tile_us"] + cm["prefix_item_us"]
+        tile_us = cm["prefix_tile_split_us"] if info["cascade_split"] else cm["prefix_tile_us"]
+        item_us = info["prefix_tiles_per_item"] * tile_us + cm["prefix_item_us"]
         if info["cascade_split"]:
             bal = (info["suffix_bytes"] / (cm["gather_sm_gbs"] * 1e3) + info["prefix_ctas"] * item_us) / num_sms
             levels = max(item_us, bal, (info["suffix_bytes"] + info["prefix_bytes"]) / (cm["bw_suffix_gbs"] * 1e3))

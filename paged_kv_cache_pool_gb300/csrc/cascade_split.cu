@@ -89,7 +89,7 @@ int launch_cascade_split(const LaunchCommon& lc, void* stream, int32_t layer, co
   const gk_pool_config& c = *lc.cfg;
   SplitParams fp{};
   fill_prefix_params(lc, layer, b, pl, &fp.pp);
-  fill_gather_params(lc, layer, b, pl, false, &fp.gp);
+  if (int e = fill_gather_params(lc, layer, b, pl, false, &fp.gp)) return e;
   fp.n_pre = (int32_t)pl->prefix_items.size();
   fp.n_gather = pl->summary.suffix_ctas;
   const int ctas = std::max(fp.n_pre, fp.n_gather);

@@ -91,7 +91,7 @@ int launch_gather(const LaunchCommon& lc, void* stream, int32_t layer, const gk_
                   bool dense) {
   const gk_pool_config& c = *lc.cfg;
   GatherParams gp;
-  fill_gather_params(lc, layer, b, pl, dense, &gp);
+  if (int e = fill_gather_params(lc, layer, b, pl, dense, &gp)) return e;
   const int ctas = dense ? pl->summary.dense_ctas : pl->summary.suffix_ctas;
   if (ctas <= 0) return 0;
   const int g = c.num_q_heads / c.num_kv_heads;

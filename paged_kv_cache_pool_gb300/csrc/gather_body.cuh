@@ -39,7 +39,6 @@ namespace gk {
 namespace gather {
 
 constexpr int kT = kGatherT;  // tokens per stage (one m16 / k16 MMA step)
-constexpr int kLookAhead = 4; // block-table reads run this many stages ahead of the copies
 constexpr int kMaxStages = 16;  // ring depth cap (the rings take what shared memory the SM has)
 constexpr int kGatherThreads = 32 * kMaxKvHeads;  // block size of the stand-alone kernel (warps = Hkv)
 
@@ -83,8 +82,12 @@ __host__ __device__ constexpr uint32_t warp_stage_bytes(int d) { return 2u * kT 
 // each warp also keeps, per ring stage, which of its tokens was appended this
 // step (fused append) and that token's pool offset
 constexpr uint32_t kFreshRecBytes = 16;
+// and a ring of nst + 1 slots of the block ids of a stage's tokens (kT int32),
+// filled by cp.async nst + 1 stages ahead of the stage's copies
+constexpr uint32_t kTabSlotBytes = kT * 4;
 __host__ __device__ constexpr size_t gather_data_bytes(int hkv, int d, int nst) {
-  return (size_t)hkv * nst * warp_stage_bytes(d) + (size_t)hkv * kMaxStages * kFreshRecBytes;
+  return (size_t)hkv * nst * warp_stage_bytes(d) + (size_t)hkv * kMaxStages * kFreshRecBytes +
+         (size_t)hkv * (nst + 1) * kTabSlotBytes;
 }
 __host__ __device__ constexpr size_t gather_smem_bytes(int hkv, int d, int nst) {
   return 1024 + gather_data_bytes(hkv, d, nst);
@@ -95,8 +98,8 @@ constexpr size_t kSmemPerCtaMax = 232448;
 constexpr size_t kSoleCtaReserve = 1024 + 3072;
 // ring depth when the gather CTA has the SM (and its shared memory) to itself
 __host__ __device__ constexpr int single_cta_stages(int hkv, int d) {
-  const int n = (int)((kSmemPerCtaMax - kSoleCtaReserve - (size_t)hkv * kMaxStages * kFreshRecBytes) /
-                      ((size_t)hkv * warp_stage_bytes(d)));
+  const int n = (int)((kSmemPerCtaMax - kSoleCtaReserve - (size_t)hkv * (kMaxStages * kFreshRecBytes + kTabSlotBytes)) /
+                      ((size_t)hkv * (warp_stage_bytes(d) + kTabSlotBytes)));
   return n > kMaxStages ? kMaxStages : n;
 }
 
@@ -144,9 +147,10 @@ __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uin
 // return at once.  Each warp streams its own data: it copies its head's K and
 // V slices of the stage nst-1 ahead into its ring with 16-byte cp.async (one
 // commit group per stage), waits for the oldest group, and computes on it, so
-// no warp waits for another.  The block-table lookups of a stage are issued a
-// stage before its copies.  `base` (16-byte aligned) holds
-// gather_data_bytes(Hkv, D, p.nst).  All threads of the CTA call it.
+// no warp waits for another.  The block ids of a stage are read (cp.async,
+// into shared memory) nst + 1 stages before its copies.  `base` (16-byte
+// aligned) holds gather_data_bytes(Hkv, D, p.nst).  All threads of the CTA
+// call it.
 template <int D, int G, bool DENSE>
 __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t base, int cta) {
   constexpr int KSTEPS = D / 16;       // k16 steps of the QK product, m16 tiles of the PV product
@@ -175,31 +179,22 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
   const int seg0 = p.seg_begin[cta], seg1 = p.seg_begin[cta + 1];
   const int64_t layer_rows = (int64_t)p.layer * p.cold_slots;
 
-  // ---- lookups kLookAhead stages ahead of the copies ----
+  // ---- block-id lookups nst + 1 stages ahead of the copies ----
   // A stage's copies need its tokens' block ids, and a table read is a round
-  // trip to memory (the table does not stay in L2 under the KV stream).  So a
-  // stage's ids are read kLookAhead stages before its copies and carried in
-  // registers; nothing uses a loaded id until the copy, where the slot
-  // arithmetic happens.
+  // trip to memory (the table does not stay in L2 under the KV stream).  A
+  // lookup cursor runs nst + 1 stages ahead of the copy cursor and has each
+  // lane cp.async its token's block id into the warp's ring of id slots; the
+  // ids travel in the cp.async groups of the stages copied in between, so a
+  // stage's ids have landed (its group waited for) before the stage is copied,
+  // and no register ever holds an id whose load is still in flight (a register
+  // queue of ids stalls the warp when it shifts).
   struct Cursor {
     int sg, t, t1, lp, req, slen;
     const int32_t* table;
     int64_t hot_row0;  // element offset of the (layer, head h) rows of the request's HOT prefix
   };
-  // An entry's scalars share one word (the queue lives in registers): bits 0-4
-  // tokens in the stage (0: no stage), bit 5 a HOT run, bits 6-10 one plus the
-  // index in the stage of the request's appended token (fused append; 0: none),
-  // bits 16-31 the request.
-  struct Entry {
-    int32_t blk;    // COLD, lane < n: block id of the stage's token `lane`
-    int32_t tt0;    // COLD: suffix index of the stage's token 0
-    uint32_t meta;
-    int64_t row0;   // HOT: element offset of token 0's row
-    __device__ int n() const { return (int)(meta & 31u); }
-    __device__ bool hot() const { return (meta >> 5) & 1u; }
-    __device__ int fresh() const { return (int)((meta >> 6) & 31u) - 1; }
-    __device__ int req() const { return (int)(meta >> 16); }
-  };
+  const uint32_t tabs = base + (uint32_t)Hkv * nst * WS + (uint32_t)Hkv * kMaxStages * kFreshRecBytes +
+                        (uint32_t)h * (nst + 1) * kTabSlotBytes;
   auto cursor_at = [&](int sg) {
     Cursor c{};
     c.sg = sg;
@@ -227,101 +222,99 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
     r.t += stage_len(c);
     return r.t < r.t1 ? r : cursor_at(c.sg + 1);
   };
-  auto make_entry = [&](const Cursor& c) {
-    Entry e{};
-    if (c.sg >= seg1) return e;
-    const int n = stage_len(c);
-    e.meta = (uint32_t)n | ((uint32_t)c.req << 16);
-    if (DENSE && c.t < c.lp) {
-      e.meta |= 1u << 5;
-      e.row0 = c.hot_row0 + (int64_t)c.t * D;
-    } else {
-      e.tt0 = c.t - c.lp;
-      const int ti = e.tt0 + lane;
-      e.blk = lane < n ? c.table[p.page_shift >= 0 ? ti >> p.page_shift : ti / p.page] : -1;
-      const int fi = c.slen - 1 - e.tt0;
-      if (fused_append && fi >= 0 && fi < n) e.meta |= (uint32_t)(fi + 1) << 6;
-    }
-    return e;
-  };
-  int islot = 0;  // ring slot of the next stage copied
-  auto copy_stage = [&](const Entry& e) {
-    if (e.n() > 0) {
-      const uint32_t kdst = ring + (uint32_t)islot * WS, vdst = kdst + kT * SR;
-      if (DENSE && e.hot()) {
-        // HOT: the stage's rows of this head are contiguous
-        for (int ci = lane; ci < e.n() * CPT; ci += 32) {
-          const uint32_t o = (uint32_t)(ci / CPT) * SR + (ci % CPT) * 16;
-          cp_async16(kdst + o, p.hot_k + e.row0 + ci * 8);
-          cp_async16(vdst + o, p.hot_v + e.row0 + ci * 8);
-        }
-      } else {
-        // COLD: lane i < n turns its token's block id into the row offset of head h
-        const int n = e.n(), fresh = e.fresh();
-        int64_t off = -1;
-        if (lane < n) {
-          const int ti = e.tt0 + lane;
-          const int in_page = p.page_shift >= 0 ? ti & (p.page - 1) : ti % p.page;
-          if (e.blk >= 0 && e.blk < p.n_blocks)
-            off = ((layer_rows + (int64_t)e.blk * p.page + in_page) * Hkv + h) * D;
-          else
-            report_error(p.err, kErrBounds);
-        }
-        // the appended token comes from the new-token arrays (copied after the
-        // loop, which keeps the loop free of branches); its pool slot is written
-        // once the stage lands (see the compute loop)
-        int64_t fresh_off = -1;
-        if (fresh >= 0) {
-          fresh_off = __shfl_sync(0xffffffffu, off, fresh);
-          if (lane == fresh) off = -1;
-        }
-        if (lane == 0)
-          sts128(recs + (uint32_t)islot * kFreshRecBytes,
-                 make_uint4((uint32_t)(fresh_off >= 0 ? fresh : -1), (uint32_t)fresh_off,
-                            (uint32_t)(fresh_off >> 32), 0u));
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-          const int ci = lane + 32 * j, tok = ci / CPT, ch = ci % CPT;
-          const int64_t src = __shfl_sync(0xffffffffu, off, tok);
-          if (tok < n && src >= 0) {
-            const uint32_t o = (uint32_t)tok * SR + ch * 16;
-            cp_async16(kdst + o, p.cold_k + src + ch * 8);
-            cp_async16(vdst + o, p.cold_v + src + ch * 8);
-          }
-        }
-        if (fresh_off >= 0 && lane < CPT) {
-          const int64_t fs = ((int64_t)e.req() * Hkv + h) * D + lane * 8;
-          const uint32_t o = (uint32_t)fresh * SR + lane * 16;
-          cp_async16(kdst + o, p.new_k + fs);
-          cp_async16(vdst + o, p.new_v + fs);
-        }
-        cp_async_commit();
-        if (++islot == nst) islot = 0;
-        return;
-      }
-    }
-    if (lane == 0) sts128(recs + (uint32_t)islot * kFreshRecBytes, make_uint4(0xffffffffu, 0u, 0u, 0u));
-    cp_async_commit();
-    if (++islot == nst) islot = 0;
-  };
-  // the queue: q0 is copied next, q3 was looked up last
+  // the lookup cursor: read the block ids of its stage into id slot lslot, move on
   Cursor lk = cursor_at(seg0);
-  Entry q0 = make_entry(lk);
-  lk = advance(lk);
-  Entry q1 = make_entry(lk);
-  lk = advance(lk);
-  Entry q2 = make_entry(lk);
-  lk = advance(lk);
-  Entry q3 = make_entry(lk);
-  lk = advance(lk);
-  auto issue_next = [&]() {
-    copy_stage(q0);
-    q0 = q1;
-    q1 = q2;
-    q2 = q3;
-    q3 = make_entry(lk);
-    lk = advance(lk);
+  int lslot = 0;
+  auto lookup = [&]() {
+    if (lk.sg < seg1) {
+      const int n = stage_len(lk);
+      if (!(DENSE && lk.t < lk.lp) && lane < n) {
+        const int ti = lk.t - lk.lp + lane;
+        const int32_t* src = lk.table + (p.page_shift >= 0 ? ti >> p.page_shift : ti / p.page);
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tabs + (uint32_t)lslot * kTabSlotBytes + lane * 4),
+                     "l"(src) : "memory");
+      }
+      lk = advance(lk);
+    }
+    if (++lslot == nst + 1) lslot = 0;
   };
+  // the copy cursor: issue its stage's copies into ring slot islot, move on
+  Cursor cc = lk;
+  int islot = 0, cidslot = 0;  // ring slot and id slot of the next stage copied
+  auto copy_stage = [&]() {
+    const uint32_t kdst = ring + (uint32_t)islot * WS, vdst = kdst + kT * SR;
+    const uint32_t rec = recs + (uint32_t)islot * kFreshRecBytes;
+    const int n = cc.sg < seg1 ? stage_len(cc) : 0;
+    if (n > 0 && DENSE && cc.t < cc.lp) {
+      // HOT: the stage's rows of this head are contiguous
+      const int64_t row0 = cc.hot_row0 + (int64_t)cc.t * D;
+      for (int ci = lane; ci < n * CPT; ci += 32) {
+        const uint32_t o = (uint32_t)(ci / CPT) * SR + (ci % CPT) * 16;
+        cp_async16(kdst + o, p.hot_k + row0 + ci * 8);
+        cp_async16(vdst + o, p.hot_v + row0 + ci * 8);
+      }
+      if (lane == 0) sts128(rec, make_uint4(0xffffffffu, 0u, 0u, 0u));
+    } else if (n > 0) {
+      // COLD: lane i < n turns its token's block id into the row offset of head h
+      const int tt0 = cc.t - cc.lp;
+      int64_t off = -1;
+      if (lane < n) {
+        int32_t blk;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(blk) : "r"(tabs + (uint32_t)cidslot * kTabSlotBytes + lane * 4));
+        const int ti = tt0 + lane;
+        const int in_page = p.page_shift >= 0 ? ti & (p.page - 1) : ti % p.page;
+        if (blk >= 0 && blk < p.n_blocks)
+          off = ((layer_rows + (int64_t)blk * p.page + in_page) * Hkv + h) * D;
+        else
+          report_error(p.err, kErrBounds);
+      }
+      // the appended token comes from the new-token arrays (copied after the
+      // loop, which keeps the loop free of branches); its pool slot is written
+      // once the stage lands (see the compute loop)
+      const int fi = cc.slen - 1 - tt0;
+      const int fresh = fused_append && fi >= 0 && fi < n ? fi : -1;
+      int64_t fresh_off = -1;
+      if (fresh >= 0) {
+        fresh_off = __shfl_sync(0xffffffffu, off, fresh);
+        if (lane == fresh) off = -1;
+      }
+      if (lane == 0)
+        sts128(rec, make_uint4((uint32_t)(fresh_off >= 0 ? fresh : -1), (uint32_t)fresh_off,
+                               (uint32_t)(fresh_off >> 32), 0u));
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) {
+        const int ci = lane + 32 * j, tok = ci / CPT, ch = ci % CPT;
+        const int64_t src = __shfl_sync(0xffffffffu, off, tok);
+        if (tok < n && src >= 0) {
+          const uint32_t o = (uint32_t)tok * SR + ch * 16;
+          cp_async16(kdst + o, p.cold_k + src + ch * 8);
+          cp_async16(vdst + o, p.cold_v + src + ch * 8);
+        }
+      }
+      if (fresh_off >= 0 && lane < CPT) {
+        const int64_t fs = ((int64_t)cc.req * Hkv + h) * D + lane * 8;
+        const uint32_t o = (uint32_t)fresh * SR + lane * 16;
+        cp_async16(kdst + o, p.new_k + fs);
+        cp_async16(vdst + o, p.new_v + fs);
+      }
+    } else if (lane == 0) {
+      sts128(rec, make_uint4(0xffffffffu, 0u, 0u, 0u));
+    }
+    cp_async_commit();
+    cc = advance(cc);
+    if (++islot == nst) islot = 0;
+    if (++cidslot == nst + 1) cidslot = 0;
+  };
+  // one stage copied, one looked up: the ids read here join the next stage's group
+  auto issue_next = [&]() {
+    copy_stage();
+    lookup();
+  };
+  // the first nst + 1 stages' ids in a group of their own, waited for once
+  for (int i = 0; i < nst + 1; ++i) lookup();
+  cp_async_commit();
+  cp_async_wait_pending(0);
+  __syncwarp();
   for (int i = 0; i < nst - 1; ++i) issue_next();
 
   // ---- compute, segment by segment ----

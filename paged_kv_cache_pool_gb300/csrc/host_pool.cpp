@@ -219,6 +219,7 @@ gk_status gk_pool_create(const gk_pool_config* cfg, gk_pool** out) {
   cm.prefix_item_us = 10.5;
   cm.gather_sm_gbs = 44.0;
   cm.c_gather_us = 10.0;
+  cm.prefix_tile_split_us = 2.1;
   *out = p;
   return GK_OK;
 }

@@ -21,6 +21,10 @@ namespace {
 constexpr int kGatherQuantum = 16;        // gather CTAs get token quotas in multiples of this
 constexpr int kMinGatherQuota = 64;
 constexpr double kPrefixCtaOverheadTiles = 2.5;   // CTA set-up + epilogue, in 128-key tiles
+// A split plan's prefix CTAs keep at least this share of a gather-only CTA's
+// suffix: an item that leaves its CTA nothing to gather ends late beside a
+// gather that keeps HBM busy, and then the other SMs wait for it.
+constexpr double kMinPrefixShare = 0.15;
 
 template <class T>
 size_t append_region(size_t* off, size_t count, size_t align = 16) {
@@ -196,7 +200,7 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   // Split arrangement: one launch in which CTA b < n_pre first runs one prefix
   // item of C key tiles, and every CTA (one per SM) gathers a slot of the
   // suffix, a prefix CTA's slot cut to the time its item leaves.  Predicted
-  //   item(C)   = C * prefix_tile_us + prefix_item_us
+  //   item(C)   = C * prefix_tile_split_us + prefix_item_us
   //   T_split   = max(item(C), (S / gather_sm + n_pre * item(C)) / SMs,
   //                   (S + prefix_bytes) / bw_suffix)
   // (the middle term spreads the gather's SM-time and the items over all SMs;
@@ -220,7 +224,8 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     t_seq += std::max(prefix_bytes / (cm.bw_prefix_gbs * 1e3),
                       waves * (std::min(c_seq, max_ntiles) * cm.prefix_tile_us + cm.prefix_item_us));
   }
-  auto item_us = [&](int32_t C) { return C * cm.prefix_tile_us + cm.prefix_item_us; };
+  // an item of a split plan runs beside a gather that keeps HBM busy: its tiles take longer
+  auto item_us = [&](int32_t C) { return C * cm.prefix_tile_split_us + cm.prefix_item_us; };
   auto split_us = [&](int32_t C) {
     const double it = item_us(C);
     const double bal = (S / (cm.gather_sm_gbs * 1e3) + (double)n_items(C) * it) / num_sms;
@@ -233,12 +238,20 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     const int32_t C = std::min(p->cascade_tiles, max_ntiles);
     if (n_items(C) <= num_sms) c_split = C;
   } else {
-    for (int32_t C = max_ntiles; can_split && C >= 1; --C) {
-      if (n_items(C) > num_sms) break;  // items only grow as C shrinks
-      const double t = split_us(C);
-      if (t < t_split - 1e-9) {
-        t_split = t;
-        c_split = C;
+    // the prefix CTAs' gather share for items of C tiles in a launch of T us
+    auto share_of = [&](int32_t C, double T) { return std::max(0.0, T - item_us(C) - cm.c_gather_us) / T; };
+    for (int pass = 0; pass < 2 && c_split == 0; ++pass) {
+      // pass 0: only splits that leave the prefix CTAs a gather share; pass 1 (a
+      // forced split with none such): the best prediction
+      if (pass == 1 && p->cascade_mode != GK_CASCADE_SPLIT) break;
+      for (int32_t C = max_ntiles; can_split && C >= 1; --C) {
+        if (n_items(C) > num_sms) break;  // items only grow as C shrinks
+        const double t = split_us(C);
+        if (pass == 0 && share_of(C, t) < kMinPrefixShare) continue;
+        if (t < t_split - 1e-9) {
+          t_split = t;
+          c_split = C;
+        }
       }
     }
   }
@@ -475,7 +488,8 @@ static void free_plan_buffers(Plan* pl) {
 // ---- cost model ----------------------------------------------------------------
 static bool valid_cost_model(const gk_cost_model& cm) {
   if (!(cm.bw_flat_gbs > 0 && cm.bw_prefix_gbs > 0 && cm.bw_suffix_gbs > 0)) return false;
-  if (!(cm.prefix_tile_us > 0 && cm.prefix_item_us >= 0 && cm.gather_sm_gbs > 0)) return false;
+  if (!(cm.prefix_tile_us > 0 && cm.prefix_tile_split_us > 0 && cm.prefix_item_us >= 0 && cm.gather_sm_gbs > 0))
+    return false;
   if (!(cm.c_flat_us >= 0 && cm.c_cascade_us >= 0 && cm.c_merge_us >= 0 && cm.c_gather_us >= 0)) return false;
   return true;
 }
@@ -605,13 +619,14 @@ gk_status gk_dispatch(const gk_pool* pool, const gk_plan* plan, gk_backend* choi
   double t_flat = cm.c_flat_us + (double)pl.summary.dense_bytes / (cm.bw_flat_gbs * 1e3);
   double t_levels = 0.0;
   const gk_plan_summary& sm = pl.summary;
-  const double item = sm.prefix_tiles_per_item * cm.prefix_tile_us + cm.prefix_item_us;
   const int num_sms = pool->impl.dev.num_sms;
   if (pl.split) {
+    const double item = sm.prefix_tiles_per_item * cm.prefix_tile_split_us + cm.prefix_item_us;
     const double bal = ((double)sm.suffix_bytes / (cm.gather_sm_gbs * 1e3) + sm.prefix_ctas * item) / num_sms;
     t_levels = std::max(std::max(item, bal), (double)(sm.suffix_bytes + sm.prefix_bytes) / (cm.bw_suffix_gbs * 1e3));
   } else {
     if (sm.prefix_ctas > 0) {
+      const double item = sm.prefix_tiles_per_item * cm.prefix_tile_us + cm.prefix_item_us;
       const double waves = (double)((sm.prefix_ctas + num_sms - 1) / num_sms);
       t_levels = std::max((double)sm.prefix_bytes / (cm.bw_prefix_gbs * 1e3), waves * item);
     }
@@ -663,7 +678,7 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
     if (!rd.eat(':')) return bad("expected ':'");
     static const char* kNumeric[] = {"c_flat_us",      "bw_flat_gbs",    "c_cascade_us",  "bw_prefix_gbs",
                                      "bw_suffix_gbs",  "c_merge_us",     "prefix_tile_us", "prefix_item_us",
-                                     "gather_sm_gbs",  "c_gather_us"};
+                                     "gather_sm_gbs",  "c_gather_us",    "prefix_tile_split_us"};
     bool known = false;
     for (const char* k : kNumeric) known = known || key == k;
     if (!known) {
@@ -682,6 +697,7 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
     else if (key == "prefix_item_us") cm.prefix_item_us = v;
     else if (key == "gather_sm_gbs") cm.gather_sm_gbs = v;
     else if (key == "c_gather_us") cm.c_gather_us = v;
+    else if (key == "prefix_tile_split_us") cm.prefix_tile_split_us = v;
   }
   return gk_cost_model_set(pool, &cm);
 }

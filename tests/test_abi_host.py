@@ -238,6 +238,7 @@ def test_dispatch_matches_oracle_formula(gk, case):
     cm = dict(c_flat_us=rnd.uniform(2, 20), bw_flat_gbs=rnd.uniform(3000, 7000), c_cascade_us=rnd.uniform(5, 40),
               bw_prefix_gbs=rnd.uniform(3000, 7000), bw_suffix_gbs=rnd.uniform(3000, 7000),
               c_merge_us=rnd.uniform(0, 0.002), prefix_tile_us=rnd.uniform(0.5, 3.0),
+              prefix_tile_split_us=rnd.uniform(0.5, 4.0),
               prefix_item_us=rnd.uniform(0, 20), gather_sm_gbs=rnd.uniform(20, 80), c_gather_us=rnd.uniform(0, 20))
     pool = gk.gk_pool_create(1, Hq, Hkv, d, 200000, 64, 1, 0)
     try:

@@ -19,7 +19,8 @@ def sweep():
 
 
 BASE = dict(c_flat_us=14.0, bw_flat_gbs=9000.0, c_cascade_us=10.0, bw_prefix_gbs=6000.0, bw_suffix_gbs=6000.0,
-            c_merge_us=0.001, prefix_tile_us=1.5, prefix_item_us=9.7, gather_sm_gbs=38.0, c_gather_us=7.0)
+            c_merge_us=0.001, prefix_tile_us=1.5, prefix_item_us=9.7, gather_sm_gbs=38.0, c_gather_us=7.0,
+            prefix_tile_split_us=1.9)
 
 
 def _model(tmp_path, **kw):

@@ -85,7 +85,8 @@ def test_eq2_meff_and_a100_threshold_rows():
 def test_cost_model_closed_form():
     # the gather on a few SMs so slow that the split arrangement never wins: the sequential formula
     cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0, bw_suffix_gbs=4000.0,
-              c_merge_us=0.001, prefix_tile_us=2.0, prefix_item_us=3.0, gather_sm_gbs=1.0, c_gather_us=4.0)
+              c_merge_us=0.001, prefix_tile_us=2.0, prefix_item_us=3.0, gather_sm_gbs=1.0, c_gather_us=4.0,
+              prefix_tile_split_us=2.5)
     # one group of 64 requests (g = 4 -> M = 256: one row block), Lp = 1000 (8 key tiles),
     # suffixes 100 each, Hkv = 8, d = 128
     f = dispatch.features([1000] * 64, [100] * 64, [0] * 64, 32, 8, 128)
@@ -109,12 +110,15 @@ def test_split_arrangement_worked_example():
     """One group of 64 requests (g = 4 -> one 256-row block), Lp = 16384 (128 key tiles),
     Hkv = 8, 1000 suffix tokens each; tile 1 us, item 5 us, 50 GB/s per SM, 6000 GB/s over
     every SM, 4 us for a separate gather launch, 152 SMs.
-    Items(C) = 8 * ceil(128 / C), item(C) = C + 5, and
+    Items(C) = 8 * ceil(128 / C), item(C) = C + 5 (the split tile time is 1 us too), and
     T(C) = max(C + 5, (S / 50 GB/s + items * (C + 5)) / 152, (S + prefix bytes) / 6000 GB/s).
-    HBM binds at 54.875 us from C = 49 down (C = 50 gives 55); the scan keeps 49
-    (24 items), and 43 is the fewest tiles per item that still gives 24 items."""
+    HBM binds at 54.875 us from C = 49 down (C = 50 gives 55).  A split C also has to leave
+    the prefix CTAs a gather share (T - item(C) - 4 us) / T of at least 0.15: the 24-item
+    splits (C = 43..49) leave at most 0.05, so the scan keeps the first 32-item one (C = 37,
+    share 0.16), and 32 is the fewest tiles per item that still gives 32 items."""
     cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0, bw_suffix_gbs=6000.0,
-              c_merge_us=0.001, prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0, c_gather_us=4.0)
+              c_merge_us=0.001, prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0, c_gather_us=4.0,
+              prefix_tile_split_us=1.0)
     f = dispatch.features([16384] * 64, [1000] * 64, [0] * 64, 32, 8, 128)
     S = 64 * 1000 * 4096
     P = 16384 * 4096
@@ -125,7 +129,8 @@ def test_split_arrangement_worked_example():
     assert math.isclose(dispatch.split_levels(cm, f, 64, 16, 152), 69.0)
     assert (S / 50e3 + 16 * 69.0) / 152 < 69.0
     a = dispatch.arrangement(cm, f, 152)
-    assert a == dict(split=True, C=43, n_pre=24, n_gather=152)
+    assert a == dict(split=True, C=32, n_pre=32, n_gather=152)
+    assert dispatch.prefix_share(cm, 43, (S + P) / 6e6) < 0.15 <= dispatch.prefix_share(cm, 37, (S + P) / 6e6)
     t_flat, t_cas = dispatch.predict(cm, f, 152)
     assert math.isclose(t_cas, 10.0 + (S + P) / 6e6 + 0.001 * 64 * 32)
     # the sequential alternative it beat: C = 7 (152 items, one wave: waves * (C + 2.5) = 9.5
@@ -133,6 +138,11 @@ def test_split_arrangement_worked_example():
     assert dispatch.sequential_tiles(f, 152) == 7 and dispatch.n_items(f, 7) == 152
     t_seq = max(P / 5e6, 7 * 1.0 + 5.0) + 4.0 + S / 6e6
     assert math.isclose(dispatch.sequential_levels(cm, f, 7, 152), t_seq) and t_seq > (S + P) / 6e6
+    # a split item runs beside the gather: the split formula takes prefix_tile_split_us, the
+    # sequential one prefix_tile_us (C = 64: 16 items of 64 * 2 + 5 = 133 us against 69)
+    cm2 = dict(cm, prefix_tile_split_us=2.0)
+    assert math.isclose(dispatch.split_levels(cm2, f, 64, 16, 152), 133.0)
+    assert math.isclose(dispatch.sequential_levels(cm2, f, 7, 152), t_seq)
     # no suffix, or no shared prefix: never split
     assert not dispatch.arrangement(cm, dispatch.features([16384] * 64, [0] * 64, [0] * 64, 32, 8, 128), 152)["split"]
     assert not dispatch.arrangement(cm, dispatch.features([0] * 64, [1000] * 64, [-1] * 64, 32, 8, 128), 152)["split"]
