@@ -136,19 +136,23 @@ def test_forks_cow_steps_small_bit_exact_pool():
 
 
 def test_page_size_invariance_on_gpu():
-    outs = []
-    for P, seed in ((16, 5), (1, 5), (4, 11)):
+    """The same forked steps at page sizes 16, 1, 4 and two that are not powers of two
+    (3, 6: the gather's slot arithmetic then divides instead of shifting), both backends."""
+    outs = {gk.GK_BACKEND_CASCADE: [], gk.GK_BACKEND_DENSE: []}
+    for P, seed in ((16, 5), (1, 5), (4, 11), (3, 7), (6, 5)):
         w = workloads.config(5, n_parent=2, children=3, Lp=300, suffix_range=(30, 90), steps=3, L=1)
         gw = _wl(w=w, page_size=P, cold_seed=seed)
         try:
             for t in range(w.steps):
                 gw.append_step(t)
-            outs.append(gw.run(0, gk.GK_BACKEND_CASCADE, step=w.steps - 1))
+            for be in outs:
+                outs[be].append(gw.run(0, be, step=w.steps - 1))
         finally:
             gw.close()
-    for O, L in outs[1:]:
-        ok, e = attention_ok(O, L, *outs[0])
-        assert ok and e["max_abs"] < 1e-4, e
+    for be, runs in outs.items():
+        for O, L in runs[1:]:
+            ok, e = attention_ok(O, L, *runs[0])
+            assert ok and e["max_abs"] < 1e-4, (be, e)
 
 
 def test_mutated_oracle_is_rejected():
