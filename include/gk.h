@@ -93,10 +93,29 @@ const char* gk_status_string(gk_status s);
  * (the caller keeps the prefix in COLD; no demotion, Appendix B.10). */
 gk_status gk_prefix_alloc(gk_pool* pool, int64_t prefix_len, int64_t* hot_base);
 /* Return a prefix's range; it merges with adjacent free ranges, and a range
- * ending at the bump pointer lowers it. */
+ * ending at the bump pointer lowers it.  GK_ERR_INVALID for a range held by the
+ * prefix cache below (those leave through gk_prefix_unref and eviction). */
 gk_status gk_prefix_release(gk_pool* pool, int64_t hot_base);
 gk_status gk_hot_stats(const gk_pool* pool, int64_t* bump_top, int64_t* free_ranges,
                        int64_t* free_tokens);
+
+/* HOT prefix cache (GraniKV Section 3.2: a prefix's slab is reference counted;
+ * at zero references it becomes evictable, and LRU eviction returns its range
+ * to the free list, merged with its neighbours, under memory pressure).
+ * key names the prefix's contents (the caller's hash of its tokens).
+ * gk_prefix_acquire: a cached key gains a reference and *hit = 1 (its K/V are
+ * already in the slab).  Otherwise a range is allocated as gk_prefix_alloc
+ * does; while nothing fits, the slab idle longest (no reference since its last
+ * use) is evicted and the allocation retried; the new slab has one reference
+ * and *hit = 0 (the caller writes its K/V, gk_write_prefix_kv).  GK_ERR_HOT_FULL
+ * when nothing fits even after every idle slab is evicted (those stay
+ * evicted); GK_ERR_INVALID when key is cached with another prefix_len.  gk_prefix_unref drops one reference (GK_ERR_INVALID if
+ * the key holds none).  Acquire and unref both count as a use for the LRU
+ * order.  Host only. */
+gk_status gk_prefix_acquire(gk_pool* pool, uint64_t key, int64_t prefix_len, int64_t* hot_base, int32_t* hit);
+gk_status gk_prefix_unref(gk_pool* pool, uint64_t key);
+/* Slabs in the cache, those of them idle, and the tokens the idle ones hold. */
+gk_status gk_hot_cache_stats(const gk_pool* pool, int64_t* cached, int64_t* idle, int64_t* idle_tokens);
 
 /* ---- COLD pool block manager ("Paged KV cache", How it works steps 1-4; Code) - */
 
@@ -125,7 +144,30 @@ gk_status gk_seq_append_slots(gk_pool* pool, int32_t n, const int32_t* seqs, int
 gk_status gk_seq_tables(const gk_pool* pool, int32_t n, const int32_t* seqs, int32_t max_blocks,
                         int32_t* table_out, int32_t* len_out);
 gk_status gk_cold_stats(const gk_pool* pool, int64_t* free_blocks, int64_t* total_blocks);
+/* A block's references: one per sequence holding it, plus one while it is cached. */
 gk_status gk_block_refcount(const gk_pool* pool, int32_t block, int32_t* refcount);
+
+/* COLD prefix caching ("Paged KV cache", How it works, step 5): each full block
+ * is keyed by a hash of its parent block's key and its page_size token ids,
+ *   key(block i) = H(key(block i - 1), tokens[i P .. i P + P)),  key(block -1) = 0,
+ *   H(parent, t[0..P)) = h_P where h_0 = mix(parent + G) and h_{j+1} = mix(h_j XOR t_j * G)
+ * (64-bit arithmetic, t_j taken as an unsigned 32-bit value, G = 0x9E3779B97F4A7C15,
+ * mix = the output function of splitmix64).  The cache holds one reference on
+ * each cached block, so a cached block outlives the sequences that used it;
+ * when the free list is empty, taking a block first releases the least
+ * recently used cached block that no sequence holds (creation of a cached
+ * sequence and caching count as uses).
+ * gk_seq_create_cached: a new sequence that starts with the longest chain of
+ * cached blocks matching tokens[0..n) block by block (each gains a reference);
+ * *n_cached = its length in tokens (a multiple of the page size; their K/V are
+ * already in the pool).  The caller appends and writes the remaining tokens.
+ * gk_seq_cache_blocks: caches seq's full blocks covering tokens[0..n) (at most
+ * its length), skipping keys already cached and blocks cached under another
+ * key; *n_new (may be NULL) = blocks added.  Host only. */
+gk_status gk_seq_create_cached(gk_pool* pool, int32_t n_tokens, const int32_t* tokens, int32_t* seq, int64_t* n_cached);
+gk_status gk_seq_cache_blocks(gk_pool* pool, int32_t seq, int32_t n_tokens, const int32_t* tokens, int32_t* n_new);
+/* Blocks in the cache, and those of them no sequence holds (evictable). */
+gk_status gk_cold_cache_stats(const gk_pool* pool, int64_t* cached_blocks, int64_t* evictable_blocks);
 
 /* ---- KV writes (device) ---------------------------------------------------- */
 

@@ -13,6 +13,15 @@ Restated from "Paged KV cache" (How it works, steps 1-4; Code: BlockPool / Seq):
 * fork(seq): the child shares every block (refcount + 1), nothing is copied;
 * release(seq): every block loses one reference; the sequence becomes empty.
 
+* prefix caching (step 5): a full block is keyed by a hash of its parent
+  block's key and its P token ids; a new request whose leading blocks' keys are
+  cached starts with those blocks (each gains a reference) instead of writing
+  them again.  The cache itself holds one reference on each cached block, so the
+  block survives the requests that used it; when the free list is empty, a
+  block is taken by first dropping the cache's reference on the cached block
+  that no request holds and that was used longest ago (creating a request from
+  the cache and caching a block count as uses).
+
 Initial free order: with seed 0, pops hand out blocks 0, 1, 2, ...  With a
 nonzero seed, pops hand out a Fisher-Yates permutation of 0..n-1 driven by
 splitmix64 (Steele, Lea & Flood 2014) seeded with the seed: for i = n-1 down to
@@ -47,6 +56,23 @@ def initial_order(n: int, seed: int) -> list:
     return order
 
 
+def _mix(z: int) -> int:
+    """The output function of splitmix64 applied to z (64-bit)."""
+    z &= _M64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & _M64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & _M64
+    return z ^ (z >> 31)
+
+
+def block_key(parent: int, tokens) -> int:
+    """Key of a full block: h = mix(parent + G), then h = mix(h XOR t * G) for each
+    token id t (as an unsigned 32-bit value), G = 0x9E3779B97F4A7C15, 64-bit."""
+    h = _mix(parent + _GOLDEN)
+    for t in tokens:
+        h = _mix(h ^ (((t & 0xFFFFFFFF) * _GOLDEN) & _M64))
+    return h
+
+
 def slot_of(table, page_size: int, t: int) -> int:
     """Physical slot of logical token t: table[t // P] * P + t % P."""
     return table[t // page_size] * page_size + t % page_size
@@ -65,11 +91,25 @@ class BlockPool:
         order = initial_order(n_blocks, seed)
         self.free = order[::-1]           # stack: the end is popped first
         self.ref = [0] * n_blocks
+        self.cache = {}                   # block key -> block
+        self.cached = {}                  # block -> [key, last use]
+        self.clock = 0
 
     def num_free(self) -> int:
         return len(self.free)
 
+    def _use(self):
+        self.clock += 1
+        return self.clock
+
     def _take(self):
+        if not self.free:
+            held_by_cache_only = [(u, b) for b, (k, u) in self.cached.items() if self.ref[b] == 1]
+            if held_by_cache_only:
+                _, b = min(held_by_cache_only)
+                key, _ = self.cached.pop(b)
+                del self.cache[key]
+                self._drop(b)
         if not self.free:
             return None
         b = self.free.pop()
@@ -113,3 +153,37 @@ class BlockPool:
             self._drop(b)
         s.table = []
         s.len = 0
+
+    def create_cached(self, tokens):
+        """A new request over the longest cached chain of tokens' leading full blocks -> (Seq, tokens reused)."""
+        s = Seq()
+        key = 0
+        for i in range(len(tokens) // self.P):
+            key = block_key(key, tokens[i * self.P:(i + 1) * self.P])
+            if key not in self.cache:
+                break
+            b = self.cache[key]
+            self.ref[b] += 1
+            self.cached[b][1] = self._use()
+            s.table.append(b)
+        s.len = len(s.table) * self.P
+        return s, s.len
+
+    def cache_blocks(self, s: Seq, tokens) -> int:
+        """Cache s's full blocks covering tokens (up to s.len); keys already cached and
+        blocks cached under another key are left alone -> blocks added."""
+        added = 0
+        key = 0
+        for i in range(min(len(tokens), s.len) // self.P):
+            key = block_key(key, tokens[i * self.P:(i + 1) * self.P])
+            b = s.table[i]
+            if key in self.cache or b in self.cached:
+                continue
+            self.cache[key] = b
+            self.cached[b] = [key, self._use()]
+            self.ref[b] += 1
+            added += 1
+        return added
+
+    def cache_stats(self):
+        return len(self.cached), sum(1 for b in self.cached if self.ref[b] == 1)

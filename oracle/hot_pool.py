@@ -59,3 +59,57 @@ class HotPool:
 
     def free_tokens(self) -> int:
         return self.capacity - sum(self.live.values())
+
+
+class HotPrefixCache:
+    """GraniKV Section 3.2's life cycle of a HOT slab: each shared prefix (named by
+    a caller key) holds one slab and a count of the requests using it; at zero the
+    slab is evictable but still cached, so a later request for the same prefix
+    finds its K/V in place.  An allocation that does not fit evicts evictable
+    slabs, the one unused for longest first, returning each range to the free
+    list (where it merges with its neighbours), until it fits.
+
+    Uses are numbered: every acquire and every release of a reference is a use,
+    and "unused for longest" is the evictable slab with the smallest number."""
+
+    def __init__(self, pool: HotPool):
+        self.pool = pool
+        self.slabs = {}       # key -> dict(base, lp, refs, used)
+        self.clock = 0
+
+    def _use(self):
+        self.clock += 1
+        return self.clock
+
+    def acquire(self, key: int, lp: int):
+        """-> (base, hit)."""
+        slab = self.slabs.get(key)
+        if slab is not None:
+            if slab["lp"] != lp:
+                raise ValueError("key cached with another length")
+            slab["refs"] += 1
+            slab["used"] = self._use()
+            return slab["base"], True
+        while True:
+            try:
+                base = self.pool.alloc(lp)
+                break
+            except HotFull:
+                idle = [(s["used"], k) for k, s in self.slabs.items() if s["refs"] == 0]
+                if not idle:
+                    raise
+                _, victim = min(idle)
+                self.pool.release(self.slabs.pop(victim)["base"])
+        self.slabs[key] = dict(base=base, lp=lp, refs=1, used=self._use())
+        return base, False
+
+    def unref(self, key: int) -> None:
+        slab = self.slabs[key]
+        if slab["refs"] == 0:
+            raise ValueError("no reference held")
+        slab["refs"] -= 1
+        slab["used"] = self._use()
+
+    def stats(self):
+        idle = [s for s in self.slabs.values() if s["refs"] == 0]
+        return len(self.slabs), len(idle), sum(s["lp"] for s in idle)

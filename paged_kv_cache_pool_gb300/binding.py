@@ -70,6 +70,12 @@ _SIGS = {
     "gk_prefix_alloc": (c_i32, [c_vp, c_i64, P(c_i64)]),
     "gk_prefix_release": (c_i32, [c_vp, c_i64]),
     "gk_hot_stats": (c_i32, [c_vp, P(c_i64), P(c_i64), P(c_i64)]),
+    "gk_prefix_acquire": (c_i32, [c_vp, c_u64, c_i64, P(c_i64), P(c_i32)]),
+    "gk_prefix_unref": (c_i32, [c_vp, c_u64]),
+    "gk_hot_cache_stats": (c_i32, [c_vp, P(c_i64), P(c_i64), P(c_i64)]),
+    "gk_seq_create_cached": (c_i32, [c_vp, c_i32, c_vp, P(c_i32), P(c_i64)]),
+    "gk_seq_cache_blocks": (c_i32, [c_vp, c_i32, c_i32, c_vp, P(c_i32)]),
+    "gk_cold_cache_stats": (c_i32, [c_vp, P(c_i64), P(c_i64)]),
     "gk_seq_create": (c_i32, [c_vp, P(c_i32)]),
     "gk_seq_fork": (c_i32, [c_vp, c_i32, P(c_i32)]),
     "gk_seq_release": (c_i32, [c_vp, c_i32]),
@@ -190,6 +196,25 @@ def gk_hot_stats(pool):
     return a.value, b.value, c.value
 
 
+def gk_prefix_acquire(pool, key, prefix_len):
+    """-> (hot_base, hit): a reference on the cached slab of key, allocated (evicting idle slabs) on a miss."""
+    base, hit = c_i64(), c_i32()
+    _check(lib().gk_prefix_acquire(pool, int(key) & ((1 << 64) - 1), int(prefix_len), ctypes.byref(base),
+                                   ctypes.byref(hit)), pool)
+    return base.value, bool(hit.value)
+
+
+def gk_prefix_unref(pool, key):
+    _check(lib().gk_prefix_unref(pool, int(key) & ((1 << 64) - 1)), pool)
+
+
+def gk_hot_cache_stats(pool):
+    """-> (cached slabs, idle slabs, tokens held by idle slabs)."""
+    a, b, c = c_i64(), c_i64(), c_i64()
+    _check(lib().gk_hot_cache_stats(pool, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)), pool)
+    return a.value, b.value, c.value
+
+
 # ---- COLD block manager ----------------------------------------------------------
 def gk_seq_create(pool):
     s = c_i32()
@@ -245,6 +270,29 @@ def gk_seq_tables(pool, seqs, max_blocks, table_out=None, len_out=None):
     assert table_out.dtype == np.int32 and table_out.flags.c_contiguous and table_out.size >= n * max_blocks
     _check(lib().gk_seq_tables(pool, n, _i32p(seqs), max_blocks, _i32p(table_out), _i32p(len_out)), pool)
     return table_out, len_out
+
+
+def gk_seq_create_cached(pool, tokens):
+    """-> (seq, n_cached): a new sequence starting with the longest cached chain of tokens' full blocks."""
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    s, n = c_i32(), c_i64()
+    _check(lib().gk_seq_create_cached(pool, len(t), t.ctypes.data_as(c_vp), ctypes.byref(s), ctypes.byref(n)), pool)
+    return s.value, n.value
+
+
+def gk_seq_cache_blocks(pool, seq, tokens):
+    """Cache seq's full blocks covering tokens; -> blocks newly cached."""
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    n = c_i32()
+    _check(lib().gk_seq_cache_blocks(pool, int(seq), len(t), t.ctypes.data_as(c_vp), ctypes.byref(n)), pool)
+    return n.value
+
+
+def gk_cold_cache_stats(pool):
+    """-> (cached blocks, evictable blocks)."""
+    a, b = c_i64(), c_i64()
+    _check(lib().gk_cold_cache_stats(pool, ctypes.byref(a), ctypes.byref(b)), pool)
+    return a.value, b.value
 
 
 def gk_cold_stats(pool):

@@ -5,8 +5,11 @@
 #include <cuda_runtime_api.h>
 
 #include <cstdint>
+#include <map>
+#include <set>
 #include <string>
 #include <unordered_map>
+#include <utility>
 #include <vector>
 
 #include "../../include/gk.h"
@@ -24,6 +27,22 @@ struct HotAllocator {
   bool release(int64_t base);
 };
 
+// HOT prefix cache (GraniKV Section 3.2): a slab per caller key, reference
+// counted; a slab whose count drops to zero stays cached but evictable, and an
+// allocation that does not fit evicts evictable slabs, least recently used
+// first, until it does.
+struct HotCacheEntry {
+  int64_t base = 0, lp = 0;
+  int64_t refs = 0;
+  uint64_t last_use = 0;
+};
+struct HotCache {
+  std::unordered_map<uint64_t, HotCacheEntry> entries;  // key -> slab
+  std::unordered_map<int64_t, uint64_t> key_of;         // base -> key
+  std::set<std::pair<uint64_t, uint64_t>> idle;         // (last use, key) of slabs with no reference
+  uint64_t tick = 0;
+};
+
 // ---- COLD block manager ("Paged KV cache", How it works; Code) ---------------
 struct Sequence {
   std::vector<int32_t> table;
@@ -37,11 +56,23 @@ struct BlockManager {
   std::vector<int32_t> ref;
   std::vector<Sequence> seqs;
   std::vector<int32_t> free_seq_ids;
+  // Prefix caching ("Paged KV cache", How it works, step 5): full blocks keyed
+  // by a chained hash of their tokens.  The cache holds one reference on each
+  // cached block; when the free stack is empty, take() releases the least
+  // recently used cached block that only the cache still holds.
+  std::unordered_map<uint64_t, int32_t> cache;        // block hash -> block
+  std::unordered_map<int32_t, uint64_t> cached_hash;  // block -> its hash
+  std::unordered_map<int32_t, uint64_t> cached_use;   // block -> last use
+  std::set<std::pair<uint64_t, int32_t>> lru;         // (last use, block) of every cached block
+  uint64_t tick = 0;
 
   void init(int64_t n_blocks, int32_t page_size, uint64_t seed);
-  int32_t take();                    // -1 when empty
+  int32_t take();                    // -1 when empty and nothing is evictable
   void drop(int32_t b);
+  void touch(int32_t b);             // a cached block was used now
 };
+// hash of a full block of page_size tokens under its parent block's hash (0 for the first block)
+uint64_t block_hash(uint64_t parent, const int32_t* tokens, int32_t page_size);
 
 // ---- geometry-dependent kernel limits ---------------------------------------
 constexpr int kPrefixTileM = 128;    // stacked query rows per tensor-core tile
@@ -60,6 +91,7 @@ struct Pool {
   gk_pool_config cfg{};
   bool has_device = false;
   HotAllocator hot;
+  HotCache hot_cache;
   BlockManager cold;
   gk_cost_model cost{};
   gk_cascade_mode cascade_mode = GK_CASCADE_AUTO;

@@ -89,14 +89,53 @@ void BlockManager::init(int64_t n_blocks, int32_t page_size, uint64_t seed) {
   ref.assign((size_t)n_blocks, 0);
   seqs.clear();
   free_seq_ids.clear();
+  cache.clear();
+  cached_hash.clear();
+  cached_use.clear();
+  lru.clear();
+  tick = 0;
 }
 
 int32_t BlockManager::take() {
-  if (free_stack.empty()) return -1;
+  if (free_stack.empty()) {
+    // evict the least recently used cached block that no sequence holds
+    for (auto it = lru.begin(); it != lru.end(); ++it) {
+      const int32_t b = it->second;
+      if (ref[(size_t)b] != 1) continue;
+      cache.erase(cached_hash[b]);
+      cached_hash.erase(b);
+      cached_use.erase(b);
+      lru.erase(it);
+      drop(b);                     // the cache's reference: the block is free now
+      break;
+    }
+    if (free_stack.empty()) return -1;
+  }
   int32_t b = free_stack.back();
   free_stack.pop_back();
   ref[(size_t)b] = 1;
   return b;
+}
+
+void BlockManager::touch(int32_t b) {
+  auto it = cached_use.find(b);
+  if (it == cached_use.end()) return;
+  lru.erase({it->second, b});
+  it->second = ++tick;
+  lru.insert({it->second, b});
+}
+
+// The splitmix64 output function (Steele, Lea & Flood, OOPSLA 2014) as a mixer.
+static uint64_t mix64(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+uint64_t block_hash(uint64_t parent, const int32_t* tokens, int32_t page_size) {
+  uint64_t h = mix64(parent + 0x9E3779B97F4A7C15ull);
+  for (int32_t i = 0; i < page_size; ++i) h = mix64(h ^ ((uint64_t)(uint32_t)tokens[i] * 0x9E3779B97F4A7C15ull));
+  return h;
 }
 
 void BlockManager::drop(int32_t b) {
@@ -244,8 +283,74 @@ gk_status gk_prefix_alloc(gk_pool* pool, int64_t prefix_len, int64_t* hot_base) 
 
 gk_status gk_prefix_release(gk_pool* pool, int64_t hot_base) {
   if (!pool) return GK_ERR_INVALID;
+  if (pool->impl.hot_cache.key_of.count(hot_base))
+    return gk::fail(&pool->impl, GK_ERR_INVALID, "the prefix at this base belongs to the prefix cache (gk_prefix_unref)");
   if (!pool->impl.hot.release(hot_base))
     return gk::fail(&pool->impl, GK_ERR_INVALID, "no live prefix at this base");
+  return GK_OK;
+}
+
+gk_status gk_prefix_acquire(gk_pool* pool, uint64_t key, int64_t prefix_len, int64_t* hot_base, int32_t* hit) {
+  if (!pool || !hot_base || !hit) return GK_ERR_INVALID;
+  Pool* p = &pool->impl;
+  gk::HotCache& hc = p->hot_cache;
+  if (prefix_len <= 0 || prefix_len > INT32_MAX)
+    return gk::fail(p, GK_ERR_INVALID, "prefix_len must be in [1, 2^31)");
+  auto it = hc.entries.find(key);
+  if (it != hc.entries.end()) {
+    gk::HotCacheEntry& e = it->second;
+    if (e.lp != prefix_len) return gk::fail(p, GK_ERR_INVALID, "key is cached with another prefix length");
+    if (e.refs == 0) hc.idle.erase({e.last_use, key});
+    ++e.refs;
+    e.last_use = ++hc.tick;
+    *hot_base = e.base;
+    *hit = 1;
+    return GK_OK;
+  }
+  int64_t base = 0;
+  while (!p->hot.alloc(prefix_len, &base)) {
+    // evict the least recently used slab nobody holds, then try again
+    if (hc.idle.empty()) return gk::fail(p, GK_ERR_HOT_FULL, "no HOT range fits the prefix, even after evicting idle ones");
+    const uint64_t victim = hc.idle.begin()->second;
+    hc.idle.erase(hc.idle.begin());
+    const int64_t vb = hc.entries[victim].base;
+    hc.entries.erase(victim);
+    hc.key_of.erase(vb);
+    p->hot.release(vb);
+  }
+  gk::HotCacheEntry e;
+  e.base = base;
+  e.lp = prefix_len;
+  e.refs = 1;
+  e.last_use = ++hc.tick;
+  hc.entries[key] = e;
+  hc.key_of[base] = key;
+  *hot_base = base;
+  *hit = 0;
+  return GK_OK;
+}
+
+gk_status gk_prefix_unref(gk_pool* pool, uint64_t key) {
+  if (!pool) return GK_ERR_INVALID;
+  Pool* p = &pool->impl;
+  gk::HotCache& hc = p->hot_cache;
+  auto it = hc.entries.find(key);
+  if (it == hc.entries.end() || it->second.refs == 0)
+    return gk::fail(p, GK_ERR_INVALID, "no held prefix under this key");
+  gk::HotCacheEntry& e = it->second;
+  e.last_use = ++hc.tick;
+  if (--e.refs == 0) hc.idle.insert({e.last_use, key});
+  return GK_OK;
+}
+
+gk_status gk_hot_cache_stats(const gk_pool* pool, int64_t* cached, int64_t* idle, int64_t* idle_tokens) {
+  if (!pool) return GK_ERR_INVALID;
+  const gk::HotCache& hc = pool->impl.hot_cache;
+  int64_t tok = 0;
+  for (const auto& ik : hc.idle) tok += hc.entries.at(ik.second).lp;
+  if (cached) *cached = (int64_t)hc.entries.size();
+  if (idle) *idle = (int64_t)hc.idle.size();
+  if (idle_tokens) *idle_tokens = tok;
   return GK_OK;
 }
 
@@ -277,6 +382,61 @@ gk_status gk_seq_fork(gk_pool* pool, int32_t parent, int32_t* child) {
   s->len = par->len;
   for (int32_t b : s->table) ++p->cold.ref[(size_t)b];
   *child = id;
+  return GK_OK;
+}
+
+gk_status gk_seq_create_cached(gk_pool* pool, int32_t n_tokens, const int32_t* tokens, int32_t* seq, int64_t* n_cached) {
+  if (!pool || !seq || !n_cached || n_tokens < 0 || (n_tokens > 0 && !tokens)) return GK_ERR_INVALID;
+  Pool* p = &pool->impl;
+  gk::BlockManager& c = p->cold;
+  const int32_t id = gk::new_seq_id(p);
+  gk::Sequence* s = &c.seqs[(size_t)id];
+  uint64_t h = 0;
+  for (int64_t i = 0; (i + 1) * c.page <= n_tokens; ++i) {
+    h = gk::block_hash(h, tokens + i * c.page, c.page);
+    auto it = c.cache.find(h);
+    if (it == c.cache.end()) break;
+    s->table.push_back(it->second);
+    ++c.ref[(size_t)it->second];
+    c.touch(it->second);
+  }
+  s->len = (int64_t)s->table.size() * c.page;
+  *seq = id;
+  *n_cached = s->len;
+  return GK_OK;
+}
+
+gk_status gk_seq_cache_blocks(gk_pool* pool, int32_t seq, int32_t n_tokens, const int32_t* tokens, int32_t* n_new) {
+  if (!pool || n_tokens < 0 || (n_tokens > 0 && !tokens)) return GK_ERR_INVALID;
+  Pool* p = &pool->impl;
+  gk::BlockManager& c = p->cold;
+  gk::Sequence* s = gk::get_seq(p, seq);
+  if (!s) return gk::fail(p, GK_ERR_INVALID, "unknown sequence");
+  const int64_t full = std::min<int64_t>(n_tokens, s->len) / c.page;
+  int32_t added = 0;
+  uint64_t h = 0;
+  for (int64_t i = 0; i < full; ++i) {
+    h = gk::block_hash(h, tokens + i * c.page, c.page);
+    const int32_t b = s->table[(size_t)i];
+    if (c.cache.count(h) || c.cached_hash.count(b)) continue;
+    c.cache[h] = b;
+    c.cached_hash[b] = h;
+    c.cached_use[b] = ++c.tick;
+    c.lru.insert({c.tick, b});
+    ++c.ref[(size_t)b];          // the cache's reference
+    ++added;
+  }
+  if (n_new) *n_new = added;
+  return GK_OK;
+}
+
+gk_status gk_cold_cache_stats(const gk_pool* pool, int64_t* cached_blocks, int64_t* evictable_blocks) {
+  if (!pool) return GK_ERR_INVALID;
+  const gk::BlockManager& c = pool->impl.cold;
+  int64_t ev = 0;
+  for (const auto& kv : c.cached_hash) ev += c.ref[(size_t)kv.first] == 1 ? 1 : 0;
+  if (cached_blocks) *cached_blocks = (int64_t)c.cached_hash.size();
+  if (evictable_blocks) *evictable_blocks = ev;
   return GK_OK;
 }
 
