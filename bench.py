@@ -51,6 +51,10 @@ def _args():
                     help="the step's new tokens written by the decode itself, or by gk_append_kv first")
     ap.add_argument("--prefix-tiles", type=int, default=0,
                     help="split cascade with this many 128-key tiles per prefix item (default: the planner's choice)")
+    ap.add_argument("--arrangement", choices=["auto", "sequential", "split"], default="auto",
+                    help="cascade arrangement (gk_pool_set_cascade_mode)")
+    ap.add_argument("--gather-partition", choices=["stream", "per-request"], default="stream",
+                    help="work split of the stand-alone gathers (gk_pool_set_gather_partition)")
     return ap.parse_args()
 
 
@@ -259,6 +263,11 @@ def run_ours(a, w):
         gk.gk_cost_model_load(pool, open(cm_path).read())
     if a.prefix_tiles > 0:
         gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SPLIT, a.prefix_tiles)
+    elif a.arrangement != "auto":
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SEQUENTIAL if a.arrangement == "sequential"
+                                    else gk.GK_CASCADE_SPLIT, 0)
+    if a.gather_partition == "per-request":
+        gk.gk_pool_set_gather_partition(pool, gk.GK_PARTITION_PER_REQUEST)
     L, B, Hq, Hkv, d = w.L, w.B, w.Hq, w.Hkv, w.d
     stream = torch.cuda.current_stream()
     bf = torch.bfloat16

@@ -358,6 +358,25 @@ typedef enum gk_cascade_mode {
   GK_CASCADE_SPLIT = 2
 } gk_cascade_mode;
 gk_status gk_pool_set_cascade_mode(gk_pool* pool, gk_cascade_mode mode, int32_t tiles_per_item);
+
+/* How the stand-alone gathers (the flat backend, and the suffix of a sequential
+ * cascade plan) split their tokens over CTAs, in the plans the pool builds from
+ * now on (a split cascade plan always gives each SM one slot of the stream).
+ *  GK_PARTITION_STREAM (default): the requests' tokens as one stream cut into
+ *    equal quotas (at least 64 tokens, multiples of 16) over at most one CTA per
+ *    SM; a quota that crosses a request boundary yields one segment per request.
+ *  GK_PARTITION_PER_REQUEST: Tangram's ahead-of-time partitioning (Algorithm 1,
+ *    with requests as its head groups and their tokens as budgets): target
+ *    tau = max(1, ceil(total / SMs)); request r gets S_r = max(1, ceil(n_r / tau))
+ *    segments of its own tokens, the first n_r mod S_r of them one token longer,
+ *    one CTA each (so up to SMs + B CTAs, in waves).
+ * The choice changes the work lists and the partial states, not the attention
+ * computed.  Host only.  GK_ERR_INVALID for an unknown value. */
+typedef enum gk_gather_partition {
+  GK_PARTITION_STREAM = 0,
+  GK_PARTITION_PER_REQUEST = 1
+} gk_gather_partition;
+gk_status gk_pool_set_gather_partition(gk_pool* pool, gk_gather_partition partition);
 gk_status gk_cost_model_get(const gk_pool* pool, gk_cost_model* cm);
 /* Same as gk_cost_model_set from JSON text: {"c_flat_us": .., "bw_flat_gbs": ..,
  * "c_cascade_us": .., "bw_prefix_gbs": .., "bw_suffix_gbs": .., "c_merge_us": ..,

@@ -166,3 +166,30 @@ def predict(cm, f, num_sms=152):
 def choose(cm, f, num_sms=152):
     t_flat, t_cas = predict(cm, f, num_sms)
     return ("dense" if t_flat < t_cas else "cascade"), t_flat, t_cas
+
+
+def aot_splits(budgets, n_cta):
+    """Tangram, Algorithm 1 (AOT workload partitioning), for one layer, with requests
+    in the place of its head groups and their token counts as the budgets:
+    Omega = sum of the budgets; tau = max(1, ceil(Omega / N_CTA)); each group's
+    split factor S_i = max(1, ceil(Phi_i / tau)).  A request with no tokens has
+    nothing to split and gets no split (the algorithm's max(1, .) would give it an
+    empty one).  -> list of split factors (0 for empty requests)."""
+    omega = sum(budgets)
+    if omega == 0:
+        return [0] * len(budgets)
+    tau = max(1, -(-omega // n_cta))
+    return [max(1, -(-phi // tau)) if phi > 0 else 0 for phi in budgets]
+
+
+def aot_segments(budgets, n_cta):
+    """The segments of each request's tokens under aot_splits: S_r pieces, the first
+    n_r mod S_r of them one token longer -> [(request, t0, t1)] in request order."""
+    out = []
+    for r, (n, s) in enumerate(zip(budgets, aot_splits(budgets, n_cta))):
+        t = 0
+        for i in range(s):
+            ln = n // s + (1 if i < n % s else 0)
+            out.append((r, t, t + ln))
+            t += ln
+    return out

@@ -103,6 +103,7 @@ _SIGS = {
     "gk_cost_model_get": (c_i32, [c_vp, P(gk_cost_model)]),
     "gk_cost_model_load": (c_i32, [c_vp, ctypes.c_char_p]),
     "gk_pool_set_cascade_mode": (c_i32, [c_vp, c_i32, c_i32]),
+    "gk_pool_set_gather_partition": (c_i32, [c_vp, c_i32]),
     "gk_device_error": (c_i32, [c_vp, c_vp, P(c_i32)]),
 }
 
@@ -438,6 +439,13 @@ GK_CASCADE_AUTO, GK_CASCADE_SEQUENTIAL, GK_CASCADE_SPLIT = 0, 1, 2
 
 def gk_pool_set_cascade_mode(pool, mode, tiles_per_item=0):
     _check(lib().gk_pool_set_cascade_mode(pool, int(mode), int(tiles_per_item)), pool)
+
+
+GK_PARTITION_STREAM, GK_PARTITION_PER_REQUEST = 0, 1
+
+
+def gk_pool_set_gather_partition(pool, partition):
+    _check(lib().gk_pool_set_gather_partition(pool, int(partition)), pool)
 
 
 def gk_cost_model_load(pool, json_text: str):

@@ -96,6 +96,7 @@ struct Pool {
   gk_cost_model cost{};
   gk_cascade_mode cascade_mode = GK_CASCADE_AUTO;
   int32_t cascade_tiles = 0;         // GK_CASCADE_SPLIT: tiles per item (0 = best predicted)
+  gk_gather_partition gather_partition = GK_PARTITION_STREAM;  // stand-alone gathers' work split
   std::string last_error;
   DeviceInfo dev;
   int32_t* d_error = nullptr;        // device error word (allocated on first device use)

@@ -63,6 +63,34 @@ void partition_tokens(const std::vector<int64_t>& n, int64_t max_ctas, std::vect
   if (begin->back() != (int32_t)segs->size()) begin->push_back((int32_t)segs->size());
 }
 
+// Tangram's ahead-of-time work partitioning (Algorithm 1) with requests in the
+// place of its head groups and their token counts as budgets: the per-split
+// target is tau = max(1, ceil(total / ctas)), request r takes
+// S_r = max(1, ceil(n_r / tau)) splits, and each split is one CTA's single
+// segment; the first n_r mod S_r splits are one token longer.
+void partition_per_request(const std::vector<int64_t>& n, int64_t ctas, std::vector<int32_t>* begin,
+                           std::vector<SegmentDev>* segs) {
+  begin->clear();
+  segs->clear();
+  begin->push_back(0);
+  int64_t total = 0;
+  for (int64_t x : n) total += x;
+  if (total == 0) return;
+  const int64_t tau = std::max<int64_t>(1, (total + ctas - 1) / ctas);
+  for (size_t r = 0; r < n.size(); ++r) {
+    if (n[r] == 0) continue;
+    const int64_t splits = std::max<int64_t>(1, (n[r] + tau - 1) / tau);
+    const int64_t base = n[r] / splits, extra = n[r] % splits;
+    int64_t t = 0;
+    for (int64_t i = 0; i < splits; ++i) {
+      const int64_t len = base + (i < extra ? 1 : 0);
+      segs->push_back(SegmentDev{(int32_t)r, (int32_t)t, (int32_t)(t + len), -1});
+      t += len;
+      begin->push_back((int32_t)segs->size());
+    }
+  }
+}
+
 // As partition_tokens, over exactly w.size() CTA slots: slot b's quota is the
 // share w[b] / sum(w) of the tokens, its end rounded to a multiple of
 // kGatherQuantum (the last slot takes the rest); a slot may be empty.
@@ -321,9 +349,15 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     for (size_t b2 = 0; b2 < pl->prefix_items.size() && b2 < w.size(); ++b2) w[b2] = prefix_cta_share;
     partition_tokens_weighted(n_suf, w, &pl->suf_seg_begin, &pl->suf_segs);
   } else {
-    partition_tokens(n_suf, num_sms, &pl->suf_seg_begin, &pl->suf_segs);
+    if (p->gather_partition == GK_PARTITION_PER_REQUEST)
+      partition_per_request(n_suf, num_sms, &pl->suf_seg_begin, &pl->suf_segs);
+    else
+      partition_tokens(n_suf, num_sms, &pl->suf_seg_begin, &pl->suf_segs);
   }
-  partition_tokens(n_dense, max_ctas, &pl->dense_seg_begin, &pl->dense_segs);
+  if (p->gather_partition == GK_PARTITION_PER_REQUEST)
+    partition_per_request(n_dense, max_ctas, &pl->dense_seg_begin, &pl->dense_segs);
+  else
+    partition_tokens(n_dense, max_ctas, &pl->dense_seg_begin, &pl->dense_segs);
 
   // ---- partial-state entries ----------------------------------------------------
   // cascade: request r owns [entry_cas, entry_cas + n_entry_cas): its prefix
@@ -646,6 +680,14 @@ gk_status gk_pool_set_cascade_mode(gk_pool* pool, gk_cascade_mode mode, int32_t 
   if (tiles_per_item < 0) return gk::fail(&pool->impl, GK_ERR_INVALID, "tiles_per_item < 0");
   pool->impl.cascade_mode = mode;
   pool->impl.cascade_tiles = tiles_per_item;
+  return GK_OK;
+}
+
+gk_status gk_pool_set_gather_partition(gk_pool* pool, gk_gather_partition partition) {
+  if (!pool) return GK_ERR_INVALID;
+  if (partition != GK_PARTITION_STREAM && partition != GK_PARTITION_PER_REQUEST)
+    return gk::fail(&pool->impl, GK_ERR_INVALID, "unknown gather partition");
+  pool->impl.gather_partition = partition;
   return GK_OK;
 }
 

@@ -84,6 +84,19 @@ def test_small_shared_prefix(lp, B, srange, g):
         gw.close()
 
 
+def test_per_request_partition_multi_prefix():
+    """Tangram's per-request splits (GK_PARTITION_PER_REQUEST) for the flat backend and a
+    sequential cascade: more CTAs than SMs' worth of segments, same attention."""
+    w = workloads.config(4, n_prefix=3, lp_range=(100, 2000), bg_range=(2, 9), suffix_range=(0, 3000), L=1)
+    gw = _wl(w=w)
+    try:
+        gk.gk_pool_set_gather_partition(gw.eng.pool, gk.GK_PARTITION_PER_REQUEST)
+        gk.gk_pool_set_cascade_mode(gw.eng.pool, gk.GK_CASCADE_SEQUENTIAL)
+        _check_both(gw, 0, what="per-request partition")
+    finally:
+        gw.close()
+
+
 def test_multi_prefix_groups_and_cold_prefix():
     """Several HOT groups interleaved in the batch, plus requests whose prefix is in COLD."""
     w = workloads.config(4, n_prefix=3, lp_range=(100, 2000), bg_range=(2, 9), suffix_range=(0, 300), L=2)

@@ -127,3 +127,45 @@ def test_segments_argument_errors(gk):
     with pytest.raises(gk.GkError):
         gk._check(gk.lib().gk_plan_segments(None, 0, ctypes.byref(ctypes.c_int32()), ctypes.byref(ctypes.c_int32()),
                                             None, None))
+
+
+def test_aot_splits_worked_example():
+    """Tangram Algorithm 1 by hand: budgets 10, 7, 3 (and an empty request) over 4 CTAs:
+    Omega = 20, tau = 5, S = ceil(10/5), ceil(7/5), ceil(3/5) = 2, 2, 1."""
+    assert odisp.aot_splits([10, 0, 7, 3], 4) == [2, 0, 2, 1]
+    assert odisp.aot_segments([10, 0, 7, 3], 4) == [(0, 0, 5), (0, 5, 10), (2, 0, 4), (2, 4, 7), (3, 0, 3)]
+    # tau never drops below one token: more CTAs than tokens gives one split per token at most
+    assert odisp.aot_splits([2, 1], 100) == [2, 1]
+    assert odisp.aot_splits([0, 0], 8) == [0, 0]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_per_request_partition_matches_algorithm_1(gk, seed):
+    """GK_PARTITION_PER_REQUEST: one segment per CTA, exactly the oracle's Algorithm-1 pieces,
+    for the flat partition and a sequential plan's suffix partition."""
+    rnd = random.Random(100 + seed)
+    pool = gk.gk_pool_create(1, 32, 8, 128, 40000, 1 << 20, 16, 0)
+    try:
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SEQUENTIAL)
+        gk.gk_pool_set_gather_partition(pool, gk.GK_PARTITION_PER_REQUEST)
+        prefixes = {lp: gk.gk_prefix_alloc(pool, lp) for lp in (300, 2000)}
+        bases, lps, slens = [], [], []
+        for _ in range(rnd.randint(1, 200)):
+            lp = rnd.choice([300, 2000, 0])
+            bases.append(prefixes[lp] if lp else -1)
+            lps.append(lp)
+            slens.append(rnd.choice([0, rnd.randint(1, 40), rnd.randint(1, 5000)]))
+        _, plan = _plan(gk, pool, bases, lps, slens)
+        for dense in (False, True):
+            lengths = [lp + sl for lp, sl in zip(lps, slens)] if dense else list(slens)
+            begin, segs = gk.gk_plan_segments(plan, dense)
+            want = odisp.aot_segments(lengths, SMS)
+            assert [tuple(x) for x in segs[:, :3].tolist()] == want
+            assert begin.tolist() == list(range(len(want) + 1))      # one segment per CTA
+            _check_cover(begin, segs, lengths)
+            _check_entries(segs, dense)
+        gk.gk_plan_destroy(plan)
+        with pytest.raises(gk.GkError):
+            gk.gk_pool_set_gather_partition(pool, 7)
+    finally:
+        gk.gk_pool_destroy(pool)
