@@ -55,6 +55,8 @@ def _args():
                     help="cascade arrangement (gk_pool_set_cascade_mode)")
     ap.add_argument("--gather-partition", choices=["stream", "per-request"], default="stream",
                     help="work split of the stand-alone gathers (gk_pool_set_gather_partition)")
+    ap.add_argument("--no-stages", action="store_true",
+                    help="skip the stand-alone timing of each kernel (the 'stages' object)")
     return ap.parse_args()
 
 
@@ -241,6 +243,90 @@ def _config_dict(w, backend):
 # ----------------------------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------------------------
+def _set_arrangement(gk, pool, a):
+    if a.prefix_tiles > 0:
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SPLIT, a.prefix_tiles)
+    elif a.arrangement != "auto":
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SEQUENTIAL if a.arrangement == "sequential"
+                                    else gk.GK_CASCADE_SPLIT, 0)
+    else:
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_AUTO, 0)
+
+
+def stage_rooflines(gk, torch, pool, batch, w, P, hbm, tc_burst, reps=7):
+    """Each kernel of the path timed alone on layer 0 of the batch as it stands: a sequential
+    cascade plan's prefix contraction (gk_cascade_prefix), suffix gather (gk_cascade_suffix) and
+    merge (gk_cascade_merge), then the dense backend (gk_decode_dense).  L2 is flushed before
+    every launch (leaving it clean); the median of `reps` CUDA-event timings on the launching
+    stream is kept.
+    A kernel timed alone is compared with the burst peaks."""
+    import numpy as np
+    B, Hq, d = w.B, w.Hq, w.d
+    stream = torch.cuda.current_stream()
+    # L2 flush: write a buffer larger than L2, then read another one, so that the timed
+    # kernel starts from a cold L2 holding no dirty lines (their write-back would be timed)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    clean = torch.zeros(256 << 20, dtype=torch.uint8, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        ts = []
+        for _ in range(reps + 1):
+            flush.zero_()
+            clean.max()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts[1:]))          # ms; the first launch is a warm-up
+
+    gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SEQUENTIAL, 0)
+    plan = gk.gk_plan_build(pool, batch)
+    try:
+        info = gk.gk_plan_info(plan)
+        s_tot = int(batch.suffix_len.sum())
+        q_bytes = B * Hq * d * 2
+        state = Hq * (d + 1) * 4                 # one partial state: O row and LSE of every query head
+        _, segs = gk.gk_plan_segments(plan, False)
+        n_suf_part = len(segs)                    # one partial state per suffix segment
+        n_pre_part = info["num_partials"] - n_suf_part
+        t_pre = timed(lambda: gk.gk_cascade_prefix(pool, stream, 0, batch, plan))
+        t_suf = timed(lambda: gk.gk_cascade_suffix(pool, stream, 0, batch, plan))
+        t_mrg = timed(lambda: gk.gk_cascade_merge(pool, stream, 0, batch, plan))
+        t_den = timed(lambda: gk.gk_decode_dense(pool, stream, 0, batch, plan))
+        if gk.gk_device_error(pool, stream):
+            raise RuntimeError("device error word set in the stage timings")
+        flops = info["prefix_flops"]
+        pre_bytes = info["prefix_bytes"] + q_bytes + n_pre_part * state
+        suf_bytes = info["suffix_bytes"] + s_tot * 4 // P + q_bytes + n_suf_part * state
+        den_bytes = info["dense_bytes"] + s_tot * 4 // P + q_bytes + B * Hq * (d + 1) * 4
+        out = {
+            "prefix": {"kernel": "prefix_kernel", "ms": t_pre, "flops": flops, "bytes": pre_bytes,
+                       "items": info["prefix_ctas"], "tiles_per_item": info["prefix_tiles_per_item"],
+                       "tflops": flops / (t_pre * 1e-3) / 1e12, "gbs": pre_bytes / (t_pre * 1e-3) / 1e9},
+            "suffix": {"kernel": "gather_kernel", "ms": t_suf, "bytes": suf_bytes, "ctas": info["suffix_ctas"],
+                       "gbs": suf_bytes / (t_suf * 1e-3) / 1e9},
+            "merge": {"kernel": "merge_kernel", "ms": t_mrg, "partials": info["num_partials"],
+                      "bytes": info["num_partials"] * state + B * state},
+            "dense": {"kernel": "gather_kernel (+ merge_kernel when a request is split)", "ms": t_den,
+                      "bytes": den_bytes, "ctas": info["dense_ctas"], "merge": info["dense_merge"],
+                      "gbs": den_bytes / (t_den * 1e-3) / 1e9},
+        }
+        out["prefix"]["tensor_frac"] = out["prefix"]["tflops"] / tc_burst
+        out["prefix"]["hbm_frac"] = out["prefix"]["gbs"] / hbm
+        out["prefix"]["bound"] = "tensor" if flops / pre_bytes > tc_burst * 1e3 / hbm else "hbm"
+        out["suffix"]["hbm_frac"] = out["suffix"]["gbs"] / hbm
+        out["dense"]["hbm_frac"] = out["dense"]["gbs"] / hbm
+        m = out["merge"]
+        m["gbs"] = m["bytes"] / (t_mrg * 1e-3) / 1e9
+        out["peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tc_burst, "which": "burst (kernels timed alone)"}
+        out["timing"] = f"layer 0, sequential plan, L2 flushed before each launch, median of {reps}"
+        return out
+    finally:
+        gk.gk_plan_destroy(plan)
+
+
 def run_ours(a, w):
     import numpy as np
     import torch
@@ -261,11 +347,7 @@ def run_ours(a, w):
     cm_path = os.path.join(ROOT, "paged_kv_cache_pool_gb300", "cost_model_gb300.json")
     if os.path.exists(cm_path):
         gk.gk_cost_model_load(pool, open(cm_path).read())
-    if a.prefix_tiles > 0:
-        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SPLIT, a.prefix_tiles)
-    elif a.arrangement != "auto":
-        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SEQUENTIAL if a.arrangement == "sequential"
-                                    else gk.GK_CASCADE_SPLIT, 0)
+    _set_arrangement(gk, pool, a)
     if a.gather_partition == "per-request":
         gk.gk_pool_set_gather_partition(pool, gk.GK_PARTITION_PER_REQUEST)
     L, B, Hq, Hkv, d = w.L, w.B, w.Hq, w.Hkv, w.d
@@ -525,6 +607,11 @@ def run_ours(a, w):
             torch.distributed.destroy_process_group()
         gw.close()
         return
+    stages = None
+    if not a.no_stages:
+        stages = stage_rooflines(gk, torch, pool, batch, w, P, hbm,
+                                 float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])))
+        _set_arrangement(gk, pool, a)
     cpu = None
     if not a.no_cpu:
         cpu = cpu_baseline(w)
@@ -539,7 +626,7 @@ def run_ours(a, w):
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic", "config": _config_dict(w, backend_name),
             "clocks": clk, "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roof,
-            "cpu_baseline": cpu, "kernels": kernels, "dispatch": dispatch,
+            "cpu_baseline": cpu, "kernels": kernels, "stages": stages, "dispatch": dispatch,
             "query_rows_per_s": value * Hq,
             "plan": info}
     print(json.dumps(line))

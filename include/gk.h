@@ -66,7 +66,7 @@ typedef struct gk_pool_config {
   int32_t num_kv_heads;      /* 1..8, divides num_q_heads */
   int32_t head_dim;          /* 64 or 128; Hq/Hkv in {1,2,4} at 64, {1,2,4,5,8} at 128 */
   int64_t hot_tokens;        /* HOT capacity in tokens */
-  int64_t cold_slots;        /* COLD capacity in token slots; a multiple of cold_page_size */
+  int64_t cold_slots;        /* COLD capacity in token slots; a multiple of cold_page_size, at most 2^31 - 1 */
   int32_t cold_page_size;    /* P: tokens per COLD block (GraniKV uses 1; "Paged KV cache" uses 16) */
   int32_t reserved0;
   uint64_t seed;             /* 0: blocks are handed out 0,1,2,...; otherwise in a splitmix64-driven

@@ -85,9 +85,16 @@ constexpr uint32_t kFreshRecBytes = 16;
 // and a ring of nst + 1 slots of the block ids of a stage's tokens (kT int32),
 // filled by cp.async nst + 1 stages ahead of the stage's copies
 constexpr uint32_t kTabSlotBytes = kT * 4;
-__host__ __device__ constexpr size_t gather_data_bytes(int hkv, int d, int nst) {
+// and, for the whole CTA, its first kSegCache segment descriptors with the
+// request fields the gather needs (req, t0, t1, entry, slen, lp, hot_base)
+constexpr int kSegCache = 16;
+constexpr uint32_t kSegRecBytes = 32;
+__host__ __device__ constexpr size_t gather_rings_bytes(int hkv, int d, int nst) {
   return (size_t)hkv * nst * warp_stage_bytes(d) + (size_t)hkv * kMaxStages * kFreshRecBytes +
          (size_t)hkv * (nst + 1) * kTabSlotBytes;
+}
+__host__ __device__ constexpr size_t gather_data_bytes(int hkv, int d, int nst) {
+  return gather_rings_bytes(hkv, d, nst) + (size_t)kSegCache * kSegRecBytes;
 }
 __host__ __device__ constexpr size_t gather_smem_bytes(int hkv, int d, int nst) {
   return 1024 + gather_data_bytes(hkv, d, nst);
@@ -98,7 +105,8 @@ constexpr size_t kSmemPerCtaMax = 232448;
 constexpr size_t kSoleCtaReserve = 1024 + 3072;
 // ring depth when the gather CTA has the SM (and its shared memory) to itself
 __host__ __device__ constexpr int single_cta_stages(int hkv, int d) {
-  const int n = (int)((kSmemPerCtaMax - kSoleCtaReserve - (size_t)hkv * (kMaxStages * kFreshRecBytes + kTabSlotBytes)) /
+  const int n = (int)((kSmemPerCtaMax - kSoleCtaReserve - (size_t)kSegCache * kSegRecBytes -
+                       (size_t)hkv * (kMaxStages * kFreshRecBytes + kTabSlotBytes)) /
                       ((size_t)hkv * (warp_stage_bytes(d) + kTabSlotBytes)));
   return n > kMaxStages ? kMaxStages : n;
 }
@@ -164,8 +172,21 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
 
   // Zero the rings once: a partial stage leaves rows past its tokens untouched,
   // and those rows must hold finite values (they meet P = 0 in the MMA).
-  for (uint32_t off = threadIdx.x * 16; off < (uint32_t)gather_data_bytes(Hkv, D, nst); off += blockDim.x * 16)
+  for (uint32_t off = threadIdx.x * 16; off < (uint32_t)gather_rings_bytes(Hkv, D, nst); off += blockDim.x * 16)
     sts128(base + off, make_uint4(0, 0, 0, 0));
+  // The CTA's segment descriptors and their requests' fields, read once into
+  // shared memory: a segment change then costs no round trip to memory.  The
+  // plan's tables are never written by the kernels of a step, so this runs
+  // before the dependency wait, while the kernel before this one finishes.
+  const int seg0 = p.seg_begin[cta], seg1 = p.seg_begin[cta + 1];
+  const uint32_t segc = base + (uint32_t)gather_rings_bytes(Hkv, D, nst);
+  for (int i = threadIdx.x; i < min(seg1 - seg0, kSegCache); i += blockDim.x) {
+    const SegmentDev sd = p.segs[seg0 + i];
+    const RequestDev& rq = p.reqs[sd.req];
+    const int64_t hb = rq.hot_base;
+    sts128(segc + i * kSegRecBytes, make_uint4((uint32_t)sd.req, (uint32_t)sd.t0, (uint32_t)sd.t1, (uint32_t)sd.entry));
+    sts128(segc + i * kSegRecBytes + 16, make_uint4((uint32_t)rq.slen, (uint32_t)rq.lp, (uint32_t)hb, (uint32_t)(hb >> 32)));
+  }
   __syncthreads();
   griddep_wait();   // queries, pool rows and the partial-state buffer are written upstream
   if (warp >= Hkv) return;
@@ -176,8 +197,31 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
   // (-1: none) and its pool offset (elements, head h; the same for K and V)
   const uint32_t recs = base + (uint32_t)Hkv * nst * WS + (uint32_t)h * kMaxStages * kFreshRecBytes;
   const bool fused_append = p.new_k != nullptr;
-  const int seg0 = p.seg_begin[cta], seg1 = p.seg_begin[cta + 1];
   const int64_t layer_rows = (int64_t)p.layer * p.cold_slots;
+  // head h's slice of pool row 0 of this layer; row r's slice is Hkv * D elements further per row
+  const uint16_t* const ck_h = p.cold_k + (layer_rows * Hkv + h) * D;
+  const uint16_t* const cv_h = p.cold_v + (layer_rows * Hkv + h) * D;
+  // segment sg's descriptor and its request's fields (shared-memory copy when cached)
+  struct SegInfo {
+    int req, t0, t1, entry, slen, lp;
+    int64_t hot_base;
+  };
+  auto seg_info = [&](int sg) {
+    SegInfo si;
+    if (sg - seg0 < kSegCache) {
+      const uint4 a = lds128(segc + (sg - seg0) * kSegRecBytes);
+      const uint4 b = lds128(segc + (sg - seg0) * kSegRecBytes + 16);
+      si.req = (int)a.x; si.t0 = (int)a.y; si.t1 = (int)a.z; si.entry = (int)a.w;
+      si.slen = (int)b.x; si.lp = (int)b.y;
+      si.hot_base = (int64_t)(((uint64_t)b.w << 32) | b.z);
+    } else {
+      const SegmentDev sd = p.segs[sg];
+      const RequestDev rq = p.reqs[sd.req];
+      si.req = sd.req; si.t0 = sd.t0; si.t1 = sd.t1; si.entry = sd.entry;
+      si.slen = rq.slen; si.lp = rq.lp; si.hot_base = rq.hot_base;
+    }
+    return si;
+  };
 
   // ---- block-id lookups nst + 1 stages ahead of the copies ----
   // A stage's copies need its tokens' block ids, and a table read is a round
@@ -199,15 +243,14 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
     Cursor c{};
     c.sg = sg;
     if (sg < seg1) {
-      const SegmentDev sd = p.segs[sg];
-      const RequestDev rq = p.reqs[sd.req];
-      c.t = sd.t0;
-      c.t1 = sd.t1;
-      c.req = sd.req;
-      c.slen = rq.slen;
-      c.lp = DENSE ? rq.lp : 0;
-      c.table = p.block_table + (int64_t)sd.req * p.max_blocks;
-      if (DENSE && c.lp > 0) c.hot_row0 = rq.hot_base * p.L * Hkv * D + ((int64_t)p.layer * Hkv + h) * c.lp * D;
+      const SegInfo si = seg_info(sg);
+      c.t = si.t0;
+      c.t1 = si.t1;
+      c.req = si.req;
+      c.slen = si.slen;
+      c.lp = DENSE ? si.lp : 0;
+      c.table = p.block_table + (int64_t)si.req * p.max_blocks;
+      if (DENSE && c.lp > 0) c.hot_row0 = si.hot_base * p.L * Hkv * D + ((int64_t)p.layer * Hkv + h) * c.lp * D;
     }
     return c;
   };
@@ -255,16 +298,17 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
       }
       if (lane == 0) sts128(rec, make_uint4(0xffffffffu, 0u, 0u, 0u));
     } else if (n > 0) {
-      // COLD: lane i < n turns its token's block id into the row offset of head h
+      // COLD: lane i < n turns its token's block id into its pool row (slot;
+      // the pool holds fewer than 2^31 slots)
       const int tt0 = cc.t - cc.lp;
-      int64_t off = -1;
+      int32_t row = -1;
       if (lane < n) {
         int32_t blk;
         asm volatile("ld.shared.b32 %0, [%1];" : "=r"(blk) : "r"(tabs + (uint32_t)cidslot * kTabSlotBytes + lane * 4));
         const int ti = tt0 + lane;
         const int in_page = p.page_shift >= 0 ? ti & (p.page - 1) : ti % p.page;
         if (blk >= 0 && blk < p.n_blocks)
-          off = ((layer_rows + (int64_t)blk * p.page + in_page) * Hkv + h) * D;
+          row = blk * p.page + in_page;
         else
           report_error(p.err, kErrBounds);
       }
@@ -275,8 +319,9 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
       const int fresh = fused_append && fi >= 0 && fi < n ? fi : -1;
       int64_t fresh_off = -1;
       if (fresh >= 0) {
-        fresh_off = __shfl_sync(0xffffffffu, off, fresh);
-        if (lane == fresh) off = -1;
+        const int32_t fr = __shfl_sync(0xffffffffu, row, fresh);
+        if (fr >= 0) fresh_off = ((layer_rows + fr) * Hkv + h) * D;
+        if (lane == fresh) row = -1;
       }
       if (lane == 0)
         sts128(rec, make_uint4((uint32_t)(fresh_off >= 0 ? fresh : -1), (uint32_t)fresh_off,
@@ -284,11 +329,12 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
 #pragma unroll
       for (int j = 0; j < CPL; ++j) {
         const int ci = lane + 32 * j, tok = ci / CPT, ch = ci % CPT;
-        const int64_t src = __shfl_sync(0xffffffffu, off, tok);
-        if (tok < n && src >= 0) {
+        const int32_t r = __shfl_sync(0xffffffffu, row, tok);
+        if (tok < n && r >= 0) {
           const uint32_t o = (uint32_t)tok * SR + ch * 16;
-          cp_async16(kdst + o, p.cold_k + src + ch * 8);
-          cp_async16(vdst + o, p.cold_v + src + ch * 8);
+          const int64_t src = (int64_t)r * (Hkv * D) + ch * 8;
+          cp_async16(kdst + o, ck_h + src);
+          cp_async16(vdst + o, cv_h + src);
         }
       }
       if (fresh_off >= 0 && lane < CPT) {
@@ -310,6 +356,21 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
     copy_stage();
     lookup();
   };
+  // Q_h^T of a segment as the B operand: b[kk][0] = (d 16kk+2tq, +1; head gq),
+  // b[kk][1] = (d +8, +9; head gq).  Each segment's rows are loaded one segment
+  // ahead (the first ones here, before the prologue's waits).
+  const int gq = lane >> 2;  // fragment row group
+  const int tq = lane & 3;   // fragment column pair
+  uint32_t qn[KSTEPS][2];
+  auto load_q = [&](int req) {
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((int64_t)req * p.Hq + h * G + min(gq, G - 1)) * D);
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+      qn[kk][0] = gq < G ? qrow[kk * 8 + tq] : 0u;
+      qn[kk][1] = gq < G ? qrow[kk * 8 + 4 + tq] : 0u;
+    }
+  };
+  if (seg0 < seg1) load_q(seg_info(seg0).req);
   // the first nst + 1 stages' ids in a group of their own, waited for once
   for (int i = 0; i < nst + 1; ++i) lookup();
   cp_async_commit();
@@ -318,24 +379,18 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
   for (int i = 0; i < nst - 1; ++i) issue_next();
 
   // ---- compute, segment by segment ----
-  const int gq = lane >> 2;  // fragment row group
-  const int tq = lane & 3;   // fragment column pair
   const int mi = lane >> 3, mj = lane & 7;  // ldmatrix: matrix index, row within it
   int cslot = 0;  // ring slot of the stage computed next
   for (int sg = seg0; sg < seg1; ++sg) {
-    const SegmentDev seg = p.segs[sg];
-    const int lp = DENSE ? p.reqs[seg.req].lp : 0;
-
-    // Q_h^T as the B operand: b[kk][0] = (d 16kk+2tq, +1; head gq), b[kk][1] = (d +8, +9; head gq)
+    const SegInfo seg = seg_info(sg);
+    const int lp = DENSE ? seg.lp : 0;
     uint32_t qb[KSTEPS][2];
-    {
-      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(p.q + ((int64_t)seg.req * p.Hq + h * G + min(gq, G - 1)) * D);
 #pragma unroll
-      for (int kk = 0; kk < KSTEPS; ++kk) {
-        qb[kk][0] = gq < G ? qrow[kk * 8 + tq] : 0u;
-        qb[kk][1] = gq < G ? qrow[kk * 8 + 4 + tq] : 0u;
-      }
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+      qb[kk][0] = qn[kk][0];
+      qb[kk][1] = qn[kk][1];
     }
+    if (sg + 1 < seg1) load_q(seg_info(sg + 1).req);
     float o[KSTEPS][4];
 #pragma unroll
     for (int mt = 0; mt < KSTEPS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;

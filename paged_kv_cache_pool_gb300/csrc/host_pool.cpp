@@ -230,7 +230,7 @@ gk_status gk_pool_create(const gk_pool_config* cfg, gk_pool** out) {
   bool g_ok = c.head_dim == 128 ? (g == 1 || g == 2 || g == 4 || g == 5 || g == 8) : (g == 1 || g == 2 || g == 4);
   if (!g_ok) return GK_ERR_UNSUPPORTED;
   if (c.hot_tokens < 0 || c.cold_slots < 0 || c.cold_page_size <= 0 ||
-      c.cold_slots % c.cold_page_size != 0 || c.cold_slots / c.cold_page_size > INT32_MAX)
+      c.cold_slots % c.cold_page_size != 0 || c.cold_slots > INT32_MAX)
     return GK_ERR_INVALID;
   bool any = c.hot_k || c.hot_v || c.cold_k || c.cold_v;
   bool all = c.hot_k && c.hot_v && c.cold_k && c.cold_v;

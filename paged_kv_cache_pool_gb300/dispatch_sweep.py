@@ -58,13 +58,17 @@ def measure(lps=LPS, bs=BS, Hq=32, Hkv=8, d=128, reps=5, seed=7, cost_model=COST
         t.normal_()
     pool = eng.pool
     _load_cost_model(pool, cost_model)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=eng.device)   # larger than L2
+    # L2 flush: write a buffer larger than L2, then read another one, so that each timed launch
+    # starts from a cold L2 holding no dirty lines (their write-back would be timed)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=eng.device)
+    clean = torch.zeros(256 << 20, dtype=torch.uint8, device=eng.device)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def timed(fn):
         ts = []
         for _ in range(reps + 1):
             flush.zero_()
+            clean.max()
             ev0.record()
             fn()
             ev1.record()
