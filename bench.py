@@ -147,6 +147,7 @@ class Clocks:
 # sources of each profiled kernel: a committed ncu summary counts only while they are unchanged
 LEVELS_SRC = ("cascade_split.cu", "prefix_body.cuh", "gather_body.cuh", "device_common.cuh")
 GATHER_SRC = ("gather_attn.cu", "gather_body.cuh", "device_common.cuh")
+PREFIX_SRC = ("prefix_tc.cu", "prefix_body.cuh", "device_common.cuh")
 
 
 def source_sha256(files):
@@ -320,6 +321,11 @@ def stage_rooflines(gk, torch, pool, batch, w, P, hbm, tc_burst, reps=7):
         out["dense"]["hbm_frac"] = out["dense"]["gbs"] / hbm
         m = out["merge"]
         m["gbs"] = m["bytes"] / (t_mrg * 1e-3) / 1e9
+        # DRAM bytes per launch from the committed ncu summaries (null unless they cover this
+        # workload and the kernel's sources are unchanged)
+        out["prefix"]["traffic"] = _profile_traffic("prefix_kernel_llama8b_lp16384_b64", PREFIX_SRC, w.name)
+        out["suffix"]["traffic"] = _profile_traffic("suffix_gather_llama8b_lp16384_b64", GATHER_SRC, w.name)
+        out["dense"]["traffic"] = _profile_traffic("dense_gather_llama8b_lp16384_b64", GATHER_SRC, w.name)
         out["peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tc_burst, "which": "burst (kernels timed alone)"}
         out["timing"] = f"layer 0, sequential plan, L2 flushed before each launch, median of {reps}"
         return out

@@ -42,8 +42,6 @@ specific to the A100); Eq. 2 and the formula are pinned by closed forms.
 """
 from __future__ import annotations
 
-CTA_OVERHEAD_TILES = 2.5   # sequential key split: a CTA's set-up and epilogue, in tiles
-
 
 def m_eff(batch_requests: int, q_per_kv: int) -> int:
     return batch_requests * q_per_kv
@@ -86,12 +84,13 @@ def n_items(f, C):
     return sum(m * f["Hkv"] * -(-n // C) for m, n in zip(mtiles, ntiles))
 
 
-def sequential_tiles(f, num_sms):
-    """Key tiles per item of a sequential plan: the C minimising waves * (C + 2.5)."""
+def sequential_tiles(cm, f, num_sms):
+    """Key tiles per item of a sequential plan: the smallest C minimising
+    waves * (C * prefix_tile_us + prefix_item_us), an item's time alone."""
     _, ntiles = _tiles(f)
     best, best_c = None, max(ntiles)
     for C in range(1, max(ntiles) + 1):
-        cost = -(-n_items(f, C) // num_sms) * (C + CTA_OVERHEAD_TILES)
+        cost = -(-n_items(f, C) // num_sms) * item_us(cm, C)
         if best is None or cost < best - 1e-9:
             best, best_c = cost, C
     return best_c
@@ -130,7 +129,7 @@ def arrangement(cm, f, num_sms):
     """-> dict(split, C, n_pre, n_gather): the planner's choice for the step."""
     if not f["prefix"]:
         return dict(split=False, C=None, n_pre=0, n_gather=gather_ctas(f["suffix_tokens"], num_sms))
-    c_seq = sequential_tiles(f, num_sms)
+    c_seq = sequential_tiles(cm, f, num_sms)
     seq = dict(split=False, C=c_seq, n_pre=n_items(f, c_seq), n_gather=gather_ctas(f["suffix_tokens"], num_sms))
     if f["suffix_tokens"] == 0:
         return seq

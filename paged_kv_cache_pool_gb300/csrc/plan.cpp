@@ -20,7 +20,6 @@ namespace {
 
 constexpr int kGatherQuantum = 16;        // gather CTAs get token quotas in multiples of this
 constexpr int kMinGatherQuota = 64;
-constexpr double kPrefixCtaOverheadTiles = 2.5;   // CTA set-up + epilogue, in 128-key tiles
 // A split plan's prefix CTAs keep at least this share of a gather-only CTA's
 // suffix: an item that leaves its CTA nothing to gather ends late beside a
 // gather that keeps HBM busy, and then the other SMs wait for it.
@@ -206,8 +205,9 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     max_ntiles = std::max(max_ntiles, ntiles[(size_t)gi]);
   }
   // Sequential arrangement: every SM takes prefix items (waves of them), then
-  // every SM gathers.  Keys per split balance the waves, counting a CTA's
-  // set-up and epilogue as kPrefixCtaOverheadTiles tiles.
+  // every SM gathers.  Keys per split: the fewest that minimise the waves times
+  // the cost model's time of one item alone (C * prefix_tile + prefix_item).
+  const gk_cost_model& cm = p->cost;
   auto n_items = [&](int32_t C) {
     int64_t units = 0;
     for (int32_t gi = 0; gi < G; ++gi)
@@ -218,7 +218,8 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   {
     double best_cost = 1e300;
     for (int32_t C = 1; G > 0 && C <= max_ntiles; ++C) {
-      const double cost = (double)((n_items(C) + num_sms - 1) / num_sms) * (C + kPrefixCtaOverheadTiles);
+      const double cost =
+          (double)((n_items(C) + num_sms - 1) / num_sms) * (C * cm.prefix_tile_us + cm.prefix_item_us);
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
         c_seq = C;
@@ -238,7 +239,6 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   // The split is taken when some C is predicted faster than the sequential
   // arrangement; among equal predictions the fewest items (fewest partials)
   // win, and the chosen item count is then spread evenly over the key tiles.
-  const gk_cost_model& cm = p->cost;
   const int64_t kv_tok = 2LL * Hkv * d * 2;
   int64_t suffix_tokens = 0;
   for (int32_t r = 0; r < B; ++r) suffix_tokens += pl->reqs[(size_t)r].slen;

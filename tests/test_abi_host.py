@@ -266,6 +266,8 @@ def test_dispatch_matches_oracle_formula(gk, case):
         if arr["split"]:
             assert s["prefix_ctas"] == arr["n_pre"] and s["prefix_tiles_per_item"] == arr["C"]
             assert s["prefix_ctas"] <= 152 and s["suffix_ctas"] == 152
+        elif n_pref and any(g >= 0 for g in grp):
+            assert s["prefix_ctas"] == arr["n_pre"] and s["prefix_tiles_per_item"] == arr["C"]
         assert math.isclose(td, wd, rel_tol=1e-12) and math.isclose(tc, wc, rel_tol=1e-12)
         assert choice == (gk.GK_BACKEND_DENSE if want == "dense" else gk.GK_BACKEND_CASCADE)
         gk.gk_plan_destroy(plan)

@@ -93,8 +93,8 @@ def test_cost_model_closed_form():
     kv = 2 * 8 * 128 * 2
     assert f["bytes_flat"] == 64 * 1100 * kv and f["bytes_suffix"] == 64 * 100 * kv
     assert f["prefix"] == [dict(M=256, bytes=1000 * kv, flops=4 * 64 * 32 * 1000 * 128, lp=1000)]
-    # sequential key split: waves * (C + 2.5) is 3.5 at C = 1 (64 items, one wave)
-    assert dispatch.sequential_tiles(f, 152) == 1 and dispatch.n_items(f, 1) == 64
+    # sequential key split: waves * (C * 2 + 3) is 5 at C = 1 (64 items, one wave)
+    assert dispatch.sequential_tiles(cm, f, 152) == 1 and dispatch.n_items(f, 1) == 64
     t_flat, t_cas = dispatch.predict(cm, f)
     assert math.isclose(t_flat, 5.0 + 64 * 1100 * kv / 4e6)
     t_levels = max(1000 * kv / 5e6, 1 * (1 * 2.0 + 3.0)) + 4.0 + 64 * 100 * kv / 4e6
@@ -133,13 +133,21 @@ def test_split_arrangement_worked_example():
     assert dispatch.prefix_share(cm, 43, (S + P) / 6e6) < 0.15 <= dispatch.prefix_share(cm, 37, (S + P) / 6e6)
     t_flat, t_cas = dispatch.predict(cm, f, 152)
     assert math.isclose(t_cas, 10.0 + (S + P) / 6e6 + 0.001 * 64 * 32)
-    # the sequential alternative it beat: C = 7 (152 items, one wave: waves * (C + 2.5) = 9.5
-    # against 10.5 at C = 8 and 17 at C = 6), the prefix bound by its 67 MB of reads
-    assert dispatch.sequential_tiles(f, 152) == 7 and dispatch.n_items(f, 7) == 152
+    # the sequential alternative it beat: C = 7 (152 items, one wave: waves * (C * 1 + 5) = 12
+    # against 13 at C = 8 and 22 at C = 6), the prefix bound by its 67 MB of reads
+    assert dispatch.sequential_tiles(cm, f, 152) == 7 and dispatch.n_items(f, 7) == 152
     t_seq = max(P / 5e6, 7 * 1.0 + 5.0) + 4.0 + S / 6e6
     assert math.isclose(dispatch.sequential_levels(cm, f, 7, 152), t_seq) and t_seq > (S + P) / 6e6
     # a split item runs beside the gather: the split formula takes prefix_tile_split_us, the
     # sequential one prefix_tile_us (C = 64: 16 items of 64 * 2 + 5 = 133 us against 69)
+    # more rows than one wave of items holds (512 requests: M = 2048, eight row blocks per head,
+    # 64 (row block, head) units of 128 key tiles): with the GB300 fit (1.557 us a tile, 8.63 an
+    # item) one wave of 128 items of 64 tiles (108.3 us) beats three waves of 448 items of 19
+    # tiles (114.6 us) and two of 256 items of 32 (117.0 us)
+    gb = dict(cm, prefix_tile_us=1.557, prefix_item_us=8.63)
+    f512 = dispatch.features([16384] * 512, [100] * 512, [0] * 512, 32, 8, 128)
+    assert dispatch.sequential_tiles(gb, f512, 152) == 64 and dispatch.n_items(f512, 64) == 128
+    assert dispatch.n_items(f512, 19) == 448 and dispatch.n_items(f512, 32) == 256
     cm2 = dict(cm, prefix_tile_split_us=2.0)
     assert math.isclose(dispatch.split_levels(cm2, f, 64, 16, 152), 133.0)
     assert math.isclose(dispatch.sequential_levels(cm2, f, 7, 152), t_seq)
