@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def _args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2)
@@ -101,7 +101,8 @@ class Clocks:
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
+    PERIOD_MS = 50
 
     def __init__(self, gpu_index):
         self.idx = gpu_index
@@ -110,12 +111,14 @@ class Clocks:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
 
-    def stop(self):
+    def stop(self, window=None):
+        """Summary of the samples; with window = (t0, t1) (host epoch seconds around the timed
+        region) only the samples taken inside it count, when there are any."""
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -124,24 +127,39 @@ class Clocks:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                row = (float(f[1]), float(f[2]), [n for n, v in zip(names, f[5:9]) if v.lower() == "active"])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+            t = None
+            if len(f) >= 10:
+                try:
+                    t = time.mktime(time.strptime(f[9].split(".")[0], "%Y/%m/%d %H:%M:%S")) + \
+                        (float("0." + f[9].split(".")[1]) if "." in f[9] else 0.0)
+                except (ValueError, IndexError):
+                    t = None
+            rows.append((t,) + row)
+        inside = rows
+        where = "all samples"
+        if window is not None:
+            t0, t1 = window
+            sel = [r for r in rows if r[0] is not None and t0 - 0.001 <= r[0] <= t1 + 0.001]
+            if sel:
+                inside, where = sel, "inside the timed region"
+            else:
+                where = "none inside the timed region; all samples"
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm.sort()
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(smax), "reasons": sorted(reasons), "samples": len(sm)}
+        sm = sorted(r[1] for r in inside)
+        reasons = sorted({n for r in inside for n in r[3]})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside), "which": where, "period_ms": self.PERIOD_MS}
 
 
 # sources of each profiled kernel: a committed ncu summary counts only while they are unchanged
@@ -481,12 +499,15 @@ def run_ours(a, w):
     torch.cuda.synchronize()
     launches[0] = 0
     n_choice0 = len(choices)
+    w0 = time.time()
     t_start.record(stream)
     for i in range(a.steps):
         step(events[i])
     t_end.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    w1 = time.time()
+    time.sleep(0.1)   # let the sampler report the samples of the region's end
+    clk = clocks.stop((w0, w1))
     gpu_launches = launches[0]
     elapsed_ms = t_start.elapsed_time(t_end)
     err = gk.gk_device_error(pool, stream)
