@@ -521,6 +521,10 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
 // the d-wide rows are then read 16 entries at a time with every load in
 // flight before any is used.  Partial states come from other CTAs, so they are
 // read at L2 (ld.global.cg).
+// ROWS partial-state rows are read per round trip: 8 (128 registers, two
+// 256-thread blocks per SM) or 4 (64 registers, four blocks per SM).  The
+// launch picks the variant with fewer (round trips x waves of warps).
+template <int ROWS>
 __device__ __forceinline__ void merge_head(const float* part_o, const float* part_l, int e0, int ne, int r, int qh,
                                            int Hq, int D, float* out, float* lse) {
   const int lane = threadIdx.x & 31;
@@ -535,11 +539,11 @@ __device__ __forceinline__ void merge_head(const float* part_o, const float* par
                  ? __ldcg(reinterpret_cast<const float4*>(part_o + ((int64_t)(e0 + eb + c + k) * Hq + qh) * D) + lane)
                  : make_float4(0.f, 0.f, 0.f, 0.f);
   };
-  // The LSE of the first 32 partial states and the O rows of the first 8 are
+  // The LSE of the first 32 partial states and the O rows of the first ROWS are
   // requested together: the rows do not depend on the weights, so a request
   // with few partial states waits for one round trip to L2, not two.
   const float l0 = lane < ne ? __ldcg(part_l + (int64_t)(e0 + lane) * Hq + qh) : -INFINITY;
-  float4 v0[8];
+  float4 v0[ROWS];
   load_rows(v0, 0, 0, min(32, ne));
   float mx = l0;
   for (int e = lane + 32; e < ne; e += 32) mx = fmaxf(mx, __ldcg(part_l + (int64_t)(e0 + e) * Hq + qh));
@@ -571,10 +575,10 @@ __device__ __forceinline__ void merge_head(const float* part_o, const float* par
       int c = 0;
       if (eb == 0) {
         accumulate(v0, w, 0);
-        c = 8;
+        c = ROWS;
       }
-      for (; c < nb; c += 8) {
-        float4 v[8];
+      for (; c < nb; c += ROWS) {
+        float4 v[ROWS];
         load_rows(v, eb, c, nb);
         accumulate(v, w, c);
       }
