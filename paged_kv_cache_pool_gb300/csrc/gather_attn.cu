@@ -1,8 +1,5 @@
 // Stand-alone gather attention kernel (suffix level of the cascade, flat
-// backend) and LSE merge kernel; the bodies are in gather_body.cuh.
-#include <algorithm>
-#include <cmath>
-
+// backend); the body is in gather_body.cuh.
 #include "gather_body.cuh"
 
 namespace gk {
@@ -16,23 +13,6 @@ __global__ void __launch_bounds__(kGatherThreads, 1) gather_kernel(const GatherP
   const uint32_t base = (raw + 1023u) & ~1023u;
   griddep_launch_dependents();
   gather_segments<D, G, DENSE>(p, base, blockIdx.x);
-}
-
-template <int ROWS>
-__global__ void __launch_bounds__(256, ROWS == 4 ? 4 : 2) merge_kernel(const float* part_o, const float* part_l,
-                                                                     const RequestDev* __restrict__ reqs, int32_t B,
-                                                                     int32_t dense, int32_t Hq, int32_t D,
-                                                                     float* __restrict__ out, float* __restrict__ lse) {
-  griddep_launch_dependents();
-  const int gw = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
-  if (gw >= B * Hq) return;
-  const int r = gw / Hq, qh = gw % Hq;
-  const RequestDev rq = reqs[r];
-  griddep_wait();
-  const int e0 = dense ? rq.entry_dense : rq.entry_cas;
-  const int ne = dense ? rq.n_entry_dense : rq.n_entry_cas;
-  if (ne < 0) return;  // written directly by its only segment
-  merge_head<ROWS>(part_o, part_l, e0, ne, r, qh, Hq, D, out, lse);
 }
 
 template <int D, int G>
@@ -116,25 +96,6 @@ int launch_gather(const LaunchCommon& lc, void* stream, int32_t layer, const gk_
     }
   }
   return (int)cudaErrorInvalidValue;
-}
-
-int launch_merge(const LaunchCommon& lc, void* stream, const gk_batch* b, const Plan* pl, bool dense) {
-  const gk_pool_config& c = *lc.cfg;
-  const uint8_t* base = (const uint8_t*)pl->d_buf;
-  const int64_t warps = (int64_t)pl->B * c.num_q_heads;
-  const int blocks = (int)((warps + 7) / 8);
-  // Latency-bound: each warp waits ceil(partial states / ROWS) round trips, and
-  // warps run in waves of (SMs x resident warps); take the variant with the
-  // smaller product (the 8-row one on a tie).
-  const double avg = (double)(dense ? pl->n_entries_dense : pl->n_entries_cas) / std::max(1, pl->B);
-  auto cost = [&](int rows, int warps_per_sm) {
-    const int64_t wave = (int64_t)std::max(1, lc.num_sms) * warps_per_sm;
-    return std::ceil(avg / rows) * (double)((warps + wave - 1) / wave);
-  };
-  const bool four = cost(4, 32) < cost(8, 16);
-  return (int)launch_pdl(four ? merge_kernel<4> : merge_kernel<8>, dim3(blocks), dim3(256), 0, (cudaStream_t)stream,
-                         pl->d_part_o, pl->d_part_l, (const RequestDev*)(base + pl->off_reqs), pl->B, dense ? 1 : 0,
-                         c.num_q_heads, c.head_dim, b->d_out, b->d_lse);
 }
 
 }  // namespace gk

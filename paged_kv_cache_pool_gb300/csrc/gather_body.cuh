@@ -513,83 +513,6 @@ __device__ __forceinline__ void gather_segments(const GatherParams& p, uint32_t 
   cp_async_wait_pending(0);
 }
 
-// LSE merge (GraniKV Eq. 1, applied to any number of partial states): for each
-// request and query head, O = sum_e 2^(l_e - m) O_e / sum_e 2^(l_e - m),
-// LSE = (m + log2 sum_e 2^(l_e - m)) * ln 2, with m = max_e l_e (log2 domain).
-// One warp per (request, query head): entries [e0, e0 + ne).  Lane e holds
-// entry e's LSE and weight (entries beyond 32 are folded in a second round);
-// the d-wide rows are then read 16 entries at a time with every load in
-// flight before any is used.  Partial states come from other CTAs, so they are
-// read at L2 (ld.global.cg).
-// ROWS partial-state rows are read per round trip: 8 (128 registers, two
-// 256-thread blocks per SM) or 4 (64 registers, four blocks per SM).  The
-// launch picks the variant with fewer (round trips x waves of warps).
-template <int ROWS>
-__device__ __forceinline__ void merge_head(const float* part_o, const float* part_l, int e0, int ne, int r, int qh,
-                                           int Hq, int D, float* out, float* lse) {
-  const int lane = threadIdx.x & 31;
-  const int vecs = D / 4;  // float4 per row: 16 or 32
-  const bool has = lane < vecs;
-  // rows c .. c + N - 1 of the block of 32 partial states starting at eb (nb of them valid)
-  auto load_rows = [&](auto& v, int eb, int c, int nb) {
-    constexpr int N = sizeof(v) / sizeof(float4);
-#pragma unroll
-    for (int k = 0; k < N; ++k)
-      v[k] = (has && c + k < nb)
-                 ? __ldcg(reinterpret_cast<const float4*>(part_o + ((int64_t)(e0 + eb + c + k) * Hq + qh) * D) + lane)
-                 : make_float4(0.f, 0.f, 0.f, 0.f);
-  };
-  // The LSE of the first 32 partial states and the O rows of the first ROWS are
-  // requested together: the rows do not depend on the weights, so a request
-  // with few partial states waits for one round trip to L2, not two.
-  const float l0 = lane < ne ? __ldcg(part_l + (int64_t)(e0 + lane) * Hq + qh) : -INFINITY;
-  float4 v0[ROWS];
-  load_rows(v0, 0, 0, min(32, ne));
-  float mx = l0;
-  for (int e = lane + 32; e < ne; e += 32) mx = fmaxf(mx, __ldcg(part_l + (int64_t)(e0 + e) * Hq + qh));
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  float z = 0.f;
-  if (mx != -INFINITY) {
-    auto accumulate = [&](const auto& v, float w, int c) {
-      constexpr int N = sizeof(v) / sizeof(float4);
-#pragma unroll
-      for (int k = 0; k < N; ++k) {
-        const float wk = __shfl_sync(0xffffffffu, w, (c + k) & 31);
-        o.x = fmaf(wk, v[k].x, o.x);
-        o.y = fmaf(wk, v[k].y, o.y);
-        o.z = fmaf(wk, v[k].z, o.z);
-        o.w = fmaf(wk, v[k].w, o.w);
-      }
-    };
-    for (int eb = 0; eb < ne; eb += 32) {
-      const int e = eb + lane;
-      const float le = eb == 0 ? l0 : (e < ne ? __ldcg(part_l + (int64_t)(e0 + e) * Hq + qh) : -INFINITY);
-      const float w = e < ne ? ex2(le - mx) : 0.f;
-      float wz = w;
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) wz += __shfl_xor_sync(0xffffffffu, wz, off);
-      z += wz;
-      const int nb = min(32, ne - eb);
-      int c = 0;
-      if (eb == 0) {
-        accumulate(v0, w, 0);
-        c = ROWS;
-      }
-      for (; c < nb; c += ROWS) {
-        float4 v[ROWS];
-        load_rows(v, eb, c, nb);
-        accumulate(v, w, c);
-      }
-    }
-    const float inv = 1.f / z;
-    o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
-  }
-  if (has) reinterpret_cast<float4*>(out + ((int64_t)r * Hq + qh) * D)[lane] = o;
-  if (lane == 0 && lse) lse[(int64_t)r * Hq + qh] = mx == -INFINITY ? -INFINITY : (mx + __log2f(z)) * kLn2;
-}
-
 }  // namespace gather
 
 // kernel arguments of the gather for one layer of a planned batch (dense: the
