@@ -277,7 +277,9 @@ def stage_rooflines(gk, torch, pool, batch, w, P, hbm, tc_burst, reps=7):
     cascade plan's prefix contraction (gk_cascade_prefix), suffix gather (gk_cascade_suffix) and
     merge (gk_cascade_merge), then the dense backend (gk_decode_dense).  L2 is flushed before
     every launch (leaving it clean); the median of `reps` CUDA-event timings on the launching
-    stream is kept.
+    stream is kept.  The prefix contraction and the suffix gather are also timed as a decode
+    step runs them: one launch per layer, back to back (each overlaps its set-up with the end
+    of the one before), time per launch.
     A kernel timed alone is compared with the burst peaks."""
     import numpy as np
     B, Hq, d = w.B, w.Hq, w.d
@@ -300,6 +302,9 @@ def stage_rooflines(gk, torch, pool, batch, w, P, hbm, tc_burst, reps=7):
             ts.append(e0.elapsed_time(e1))
         return float(np.median(ts[1:]))          # ms; the first launch is a warm-up
 
+    # no fused append in these timings: the batch's new-token arrays belong to one layer
+    batch.c.d_new_k = None
+    batch.c.d_new_v = None
     gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SEQUENTIAL, 0)
     plan = gk.gk_plan_build(pool, batch)
     try:
@@ -314,6 +319,21 @@ def stage_rooflines(gk, torch, pool, batch, w, P, hbm, tc_burst, reps=7):
         t_suf = timed(lambda: gk.gk_cascade_suffix(pool, stream, 0, batch, plan))
         t_mrg = timed(lambda: gk.gk_cascade_merge(pool, stream, 0, batch, plan))
         t_den = timed(lambda: gk.gk_decode_dense(pool, stream, 0, batch, plan))
+
+        # the same kernels back to back over every layer, as they run in a decode step's
+        # stream (each layer reads its own pool rows: together far more than L2); per launch
+        def chained(fn):
+            flush.zero_()
+            clean.max()
+            e0.record(stream)
+            for layer in range(w.L):
+                fn(layer)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / w.L
+        chained(lambda l: gk.gk_cascade_prefix(pool, stream, l, batch, plan))   # warm-up
+        c_pre = chained(lambda l: gk.gk_cascade_prefix(pool, stream, l, batch, plan))
+        c_suf = chained(lambda l: gk.gk_cascade_suffix(pool, stream, l, batch, plan))
         if gk.gk_device_error(pool, stream):
             raise RuntimeError("device error word set in the stage timings")
         flops = info["prefix_flops"]
@@ -333,6 +353,11 @@ def stage_rooflines(gk, torch, pool, batch, w, P, hbm, tc_burst, reps=7):
                       "gbs": den_bytes / (t_den * 1e-3) / 1e9},
         }
         out["prefix"]["tensor_frac"] = out["prefix"]["tflops"] / tc_burst
+        out["prefix_chained"] = {"ms": c_pre, "launches": w.L, "tflops": flops / (c_pre * 1e-3) / 1e12,
+                                 "tensor_frac": flops / (c_pre * 1e-3) / 1e12 / tc_burst,
+                                 "gbs": pre_bytes / (c_pre * 1e-3) / 1e9}
+        out["suffix_chained"] = {"ms": c_suf, "launches": w.L, "gbs": suf_bytes / (c_suf * 1e-3) / 1e9,
+                                 "hbm_frac": suf_bytes / (c_suf * 1e-3) / 1e9 / hbm}
         out["prefix"]["hbm_frac"] = out["prefix"]["gbs"] / hbm
         out["prefix"]["bound"] = "tensor" if flops / pre_bytes > tc_burst * 1e3 / hbm else "hbm"
         out["suffix"]["hbm_frac"] = out["suffix"]["gbs"] / hbm
@@ -345,7 +370,9 @@ def stage_rooflines(gk, torch, pool, batch, w, P, hbm, tc_burst, reps=7):
         out["suffix"]["traffic"] = _profile_traffic("suffix_gather_llama8b_lp16384_b64", GATHER_SRC, w.name)
         out["dense"]["traffic"] = _profile_traffic("dense_gather_llama8b_lp16384_b64", GATHER_SRC, w.name)
         out["peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tc_burst, "which": "burst (kernels timed alone)"}
-        out["timing"] = f"layer 0, sequential plan, L2 flushed before each launch, median of {reps}"
+        out["timing"] = (f"layer 0, sequential plan, L2 flushed before each launch, median of {reps}; "
+                         f"*_chained: one launch per layer back to back over the {w.L} layers, L2 flushed "
+                         f"before the chain, time per launch")
         return out
     finally:
         gk.gk_plan_destroy(plan)
