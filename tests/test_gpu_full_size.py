@@ -3,8 +3,9 @@ through the same plan/launch configuration bench.py times.
 
 The pool is allocated for every layer; the layers checked (first and last) are
 filled and decoded, and the oracle computes requests one by one (all query
-heads): every request of both layers for workloads 2 and 3, every request of
-the last layer and a sample of the first for workload 4, samples elsewhere.
+heads): every request of both layers for workloads 2, 3 and 4; for workload 5,
+every request of both layers after the first and the last of its 32 steps, and
+four requests after every step.
 Block tables are compared bit for bit with the oracle block manager for every
 sequence.
 """
@@ -30,10 +31,6 @@ def _built():
     from synth import device
     build.build()
     device.build()
-
-
-def _sample(B):
-    return sorted({0, 1, B // 3, B // 2, (2 * B) // 3, B - 1})
 
 
 def _oracle_tables(w, gw):
@@ -82,8 +79,7 @@ def test_full_size_single_step(n):
         _, seqs = _oracle_tables(w, gw)
         _compare_tables(gw, seqs)
         for layer in (0, w.L - 1):
-            every = n in (2, 3) or layer == w.L - 1
-            _check_layer(gw, layer, list(range(w.B)) if every else _sample(w.B), what=w.name)
+            _check_layer(gw, layer, list(range(w.B)), what=w.name)
         info = gk.gk_plan_info(gw.eng.plan(gw.batch()))
         assert info["num_groups"] == len(w.prefix_lens)
     finally:
@@ -96,7 +92,7 @@ def test_full_size_peaked_queries():
     w = workloads.config(2, q_log2_scale=3)
     gw = GpuWorkload(w, layers=[0])
     try:
-        _check_layer(gw, 0, _sample(w.B), what="peaked " + w.name)
+        _check_layer(gw, 0, list(range(w.B)), what="peaked " + w.name)
     finally:
         gw.close()
 
@@ -109,7 +105,7 @@ def test_full_size_fork_cow_32_steps():
     try:
         bp, seqs = _oracle_tables(w, gw)
         _compare_tables(gw, seqs)
-        reqs = [0, 1, 2, 3, w.B - 1]
+        few = [0, 1, 2, 3]
         n_cow = 0
         for t in range(w.steps):
             slots, cow = gw.append_step(t)
@@ -119,7 +115,9 @@ def test_full_size_fork_cow_32_steps():
             n_cow += len(cow)
             if t in (0, w.steps - 1):
                 for layer in layers:
-                    _check_layer(gw, layer, reqs, step=t, appended=t + 1, what=w.name)
+                    _check_layer(gw, layer, list(range(w.B)), step=t, appended=t + 1, what=w.name)
+            else:
+                _check_layer(gw, layers[0], few, step=t, appended=t + 1, what=w.name)
         # every parent with a partial last block was shared 4 ways: 3 copies each
         assert n_cow == 3 * sum(1 for n in w.parents if n % w.page_size)
         _compare_tables(gw, seqs)
