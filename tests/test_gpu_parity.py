@@ -72,7 +72,10 @@ def test_config1_peaked_queries():
 
 
 @pytest.mark.parametrize("lp,B,srange,g", [(1000, 8, (50, 300), 4), (130, 3, (1, 5), 4), (4096 + 77, 40, (200, 900), 4),
-                                           (777, 20, (0, 40), 5), (300, 33, (10, 200), 8)])
+                                           (777, 20, (0, 40), 5), (300, 33, (10, 200), 8),
+                                           # tiny suffixes: a gather CTA's quota spans dozens of requests,
+                                           # more segments than the shared-memory segment cache holds
+                                           (130, 300, (0, 3), 4)])
 def test_small_shared_prefix(lp, B, srange, g):
     Hkv = 8 if g != 8 else 4
     w = workloads.config(2, B=B, Lp=lp, suffix_range=srange, L=2, Hq=Hkv * g, Hkv=Hkv)
