@@ -19,7 +19,7 @@ predicted time runs (flat wins only when strictly faster):
 Work items: a group of M_eff stacked rows and Lp keys contributes ceil(M/256)
 row blocks x Hkv heads x ceil(ceil(Lp/128)/C) items, so M_eff enters through the
 item count.  A sequential plan runs them in W = ceil(items/SMs) waves over every
-SM, with C chosen to minimise W * (C + 2.5); then the gather runs over every SM
+SM, with C the smallest value minimising W * item(C); then the gather runs over every SM
 as its own launch.  A split plan is one launch with a CTA per SM: CTA b < n_pre
 first runs prefix item b, and every CTA gathers a slot of the suffix, a prefix
 CTA's slot cut to the time its item leaves (the middle term spreads the
