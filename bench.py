@@ -232,7 +232,10 @@ def run_reference(a, w):
     from oracle import attention
     attention.build()
     dt1, _, thr = _oracle_sample(w, 1)
-    n_req = max(1, min(w.B, int(4.0 / max(dt1, 1e-3))))
+    # each timed step a sample of about 4 s, less when many steps are asked for, so that the
+    # whole run stays near two and a half minutes
+    per_step_s = max(0.5, min(4.0, 150.0 / max(1, a.steps)))
+    n_req = max(1, min(w.B, int(per_step_s / max(dt1, 1e-3))))
     for i in range(a.warmup):
         _oracle_sample(w, 1, start=i)
     total_t, total_q = 0.0, 0
