@@ -1,5 +1,6 @@
-// Body of the gather attention (suffix kernel, flat backend) and of the LSE
-// merge, shared by the stand-alone kernels and the split cascade kernel.
+// Body of the gather attention (suffix kernel, flat backend), shared by the
+// stand-alone kernel and the split cascade kernel.  The merge of the partial
+// states is in merge.cu.
 //
 // Suffix kernel (GraniKV Section 3.3 / 3.5, cascade level 1): each request's
 // COLD tokens are gathered through its block table ("Paged KV cache", How it
