@@ -231,8 +231,11 @@ typedef struct gk_plan_summary {
 
 /* Plan one decode step: group requests by HOT prefix (stable, first appearance),
  * split the prefix contraction and the gathers into balanced CTA work lists,
- * and lay out the partial states.  Depends only on the host arrays of the
- * batch, so one plan serves every layer of the step.  When the pool has device
+ * and lay out the partial states.  The grouping is GraniKV Section 3.6's: the
+ * requests that share one HOT prefix stack their B_g * Hq/Hkv query rows per KV
+ * head into one matrix (M_eff of Eq. 2, which also drives gk_dispatch).  Depends
+ * only on the host arrays of the batch, which every layer of a step shares, so
+ * one plan serves every layer of the step.  When the pool has device
  * storage the plan's tables are copied to the device on `stream` and scratch
  * for the partial states is allocated (owned by the plan).  Calls that use a
  * plan must be ordered on one stream. */
@@ -258,7 +261,12 @@ gk_status gk_plan_segments(const gk_plan* plan, int32_t dense, int32_t* n_ctas, 
 
 /* Flat paged attention (the dense backend): each request attends its prefix
  * (read from HOT, once per request) and its COLD suffix in one online-softmax
- * pass; writes d_out and d_lse of the batch for this layer. */
+ * pass; writes d_out and d_lse of the batch for this layer.  This is the decode
+ * of "Paged KV cache", How it works step 3 (the kernel walks each sequence's
+ * block table and reads its K/V in place, token slot by slot), and the
+ * baseline GraniKV compares against (Section 4, the SGLang default: every
+ * request re-reads the shared prefix).  A request split over several CTAs is
+ * merged by GraniKV Eq. 1 (gk_plan_summary.dense_merge). */
 gk_status gk_decode_dense(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch,
                           const gk_plan* plan);
 /* Cascade backend: (a) per prefix group and KV head, all query rows sharing the
@@ -281,7 +289,11 @@ gk_status gk_decode_cascade(gk_pool* pool, void* stream, int32_t layer, const gk
  * until the process exits) and no call allocates device or pinned memory.
  *  - The first call on each device looks the array's address up
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The pool's device must be the current device
+ *    (else GK_ERR_INVALID).
+ *  - Each call copies its work tables from host memory that it frees on
+ *    return, so on a stream that is capturing it does nothing and returns
+ *    GK_ERR_UNSUPPORTED.
  *  - A batch whose tables and partial states exceed 8 MiB is refused with
  *    GK_ERR_INVALID (gk_last_error gives the bytes needed); use the plan path.
  *  - Every call reuses the same array: calls that overlap on the GPU (two

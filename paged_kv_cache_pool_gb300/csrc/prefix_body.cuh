@@ -454,6 +454,15 @@ __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixI
     }
     tc_fence_before();
   }
+  // Drain order on every path, aborted or not: the TMA producer has waited for
+  // its own loads in flight (above); here thread 0 waits for the MMA thread's
+  // final commit, which arrives once every tcgen05.mma it issued has completed
+  // (it commits even after an abort, with or without MMAs issued).  Only then
+  // are the barriers invalidated and, by the caller, tensor memory released.
+  // Softmax warps that gave up skip their own wait for it, so this one is
+  // needed; on the normal path the phase has already completed.  The MMA
+  // thread's waits are bounded, so its commit comes; this wait is bounded too.
+  if (threadIdx.x == 0 && ntiles > 0) mbar_wait(bar(B_OFINAL), 0, nullptr);
   // the staging area is rewritten by the next user of the shared memory through TMA
   fence_async_shared();
   __syncthreads();

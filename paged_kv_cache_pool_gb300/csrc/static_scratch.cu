@@ -9,6 +9,7 @@
 // in the middle of serving.  gk_plan_build allocates device tables and partial
 // states; this entry point instead keeps both in one statically sized array
 // that is part of the loaded library image.
+#include <atomic>
 #include <cstring>
 
 #include "device_common.cuh"
@@ -17,28 +18,36 @@
 namespace gk {
 namespace {
 
-// The scratch: work tables, tensor maps and split-K partial states of one call.
+// The scratch: work tables and split-K partial states of one call.
 // Every GPU that loads libgk holds these bytes until the process exits.
 constexpr size_t kStaticScratchBytes = 8u << 20;
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
-uint8_t* g_scratch_ptr[kMaxDevices] = {};   // device address of g_static_scratch, per device
+// device address of g_static_scratch, per device; host threads making their
+// first call at the same time may both look it up and store the same value
+std::atomic<uint8_t*> g_scratch_ptr[kMaxDevices] = {};
 
 // Once per device, with that device current: host code names the array only
 // through its symbol, so the device address comes from cudaGetSymbolAddress.
+// The current device must be the pool's: another device's copy of the array
+// would be a peer address the kernels must not touch.
 gk_status scratch_address(Pool* p, uint8_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(p, e, "cudaGetDevice");
+  if (dev != p->dev.device)
+    return fail(p, GK_ERR_INVALID, "the current device is not the pool's device (make the pool's device current)");
   if (dev < 0 || dev >= kMaxDevices) return fail(p, GK_ERR_UNSUPPORTED, "device ordinal beyond the static scratch table");
-  if (!g_scratch_ptr[dev]) {
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_static_scratch);
-    if (e != cudaSuccess || !ptr) return cuda_fail(p, e, "cudaGetSymbolAddress(static scratch)");
-    g_scratch_ptr[dev] = (uint8_t*)ptr;
+  uint8_t* ptr = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (!ptr) {
+    void* sym = nullptr;
+    e = cudaGetSymbolAddress(&sym, g_static_scratch);
+    if (e != cudaSuccess || !sym) return cuda_fail(p, e, "cudaGetSymbolAddress(static scratch)");
+    ptr = (uint8_t*)sym;
+    g_scratch_ptr[dev].store(ptr, std::memory_order_release);
   }
-  *out = g_scratch_ptr[dev];
+  *out = ptr;
   return GK_OK;
 }
 
@@ -63,6 +72,13 @@ extern "C" gk_status gk_decode_dense_static(gk_pool* pool, void* stream, int32_t
   // this call does not allocate it
   if (!p->d_error || !p->dev.queried)
     return gk::fail(p, GK_ERR_INVALID, "pool has not been used on the device yet (write its KV first)");
+  // The work tables are copied from host memory that is freed on return; a
+  // capturing stream would record that copy, so it is refused before any work.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t ce = cudaStreamIsCapturing((cudaStream_t)stream, &cap);
+  if (ce != cudaSuccess) return gk::cuda_fail(p, ce, "cudaStreamIsCapturing");
+  if (cap != cudaStreamCaptureStatusNone)
+    return gk::fail(p, GK_ERR_UNSUPPORTED, "gk_decode_dense_static cannot run on a capturing stream");
   uint8_t* scratch = nullptr;
   gk_status st = gk::scratch_address(p, &scratch);
   if (st != GK_OK) return st;
@@ -80,12 +96,11 @@ extern "C" gk_status gk_decode_dense_static(gk_pool* pool, void* stream, int32_t
     off = o + bytes;
     return o;
   };
-  std::vector<uint8_t> tmaps;
-  if (gk::encode_prefix_tmaps(&c, &pl, &tmaps)) return gk::fail(p, GK_ERR_CUDA, "encoding the prefix tensor maps failed");
+  // the dense gather reads no tensor maps (only the prefix contraction does)
   pl.off_reqs = region(pl.reqs.size() * sizeof(gk::RequestDev), 16);
   pl.off_dense_begin = region(pl.dense_seg_begin.size() * sizeof(int32_t), 16);
   pl.off_dense_segs = region(pl.dense_segs.size() * sizeof(gk::SegmentDev), 16);
-  pl.off_tmaps = region(tmaps.size(), 128);
+  pl.off_tmaps = 0;
   const size_t table_bytes = off;
   const size_t entries = (size_t)(pl.n_entries_dense > 0 ? pl.n_entries_dense : 0);
   const size_t po = region(entries * c.num_q_heads * c.head_dim * sizeof(float), 256);
@@ -103,7 +118,6 @@ extern "C" gk_status gk_decode_dense_static(gk_pool* pool, void* stream, int32_t
   put(pl.off_reqs, pl.reqs.data(), pl.reqs.size() * sizeof(gk::RequestDev));
   put(pl.off_dense_begin, pl.dense_seg_begin.data(), pl.dense_seg_begin.size() * sizeof(int32_t));
   put(pl.off_dense_segs, pl.dense_segs.data(), pl.dense_segs.size() * sizeof(gk::SegmentDev));
-  put(pl.off_tmaps, tmaps.data(), tmaps.size());
   cudaError_t e = cudaMemcpyAsync(scratch, host.data(), table_bytes, cudaMemcpyHostToDevice, (cudaStream_t)stream);
   if (e != cudaSuccess) return gk::cuda_fail(p, e, "copying the work tables into the static scratch");
   pl.d_buf = scratch;

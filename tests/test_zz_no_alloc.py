@@ -54,19 +54,58 @@ def test_static_scratch_dense_matches_plan_path_two_calls():
 
 def test_static_scratch_refuses_oversized_batch():
     from paged_kv_cache_pool_gb300.engine import Engine
-    # 64 query heads per request and 320 requests that each span CTA quotas
-    eng = Engine(1, 64, 8, 128, 1, 320 * 2048, 1)
+    # 64 query heads per request; requests of 2047 tokens.  How many partial states
+    # the dense split needs depends on the SM count, so the batch grows until the
+    # plan's own partition needs more than the 8 MiB the scratch holds.
+    Hq, d, lim = 64, 128, 8 << 20
+    eng = Engine(1, Hq, 8, d, 1, 1280 * 2048, 1)
     try:
-        z = torch.zeros((1, 8, 128), dtype=torch.bfloat16, device="cuda")
+        z = torch.zeros((1, 8, d), dtype=torch.bfloat16, device="cuda")
         eng.append_kv(0, torch.zeros(1, dtype=torch.int64, device="cuda"), z, z)   # first device work
         torch.cuda.synchronize()
-        B = 320
-        table = torch.zeros((B, 2048), dtype=torch.int32, device="cuda")
-        q = torch.zeros((B, 64, 128), dtype=torch.bfloat16, device="cuda")
-        out = torch.empty((B, 64, 128), dtype=torch.float32, device="cuda")
-        b = gk.Batch(np.full(B, -1), np.zeros(B), np.full(B, 2047), table, 2048, q, out, None)
+        for B in (320, 640, 1280):
+            table = torch.zeros((B, 2048), dtype=torch.int32, device="cuda")
+            q = torch.zeros((B, Hq, d), dtype=torch.bfloat16, device="cuda")
+            out = torch.empty((B, Hq, d), dtype=torch.float32, device="cuda")
+            b = gk.Batch(np.full(B, -1), np.zeros(B), np.full(B, 2047), table, 2048, q, out, None)
+            plan = gk.gk_plan_build(eng.pool, b)
+            try:
+                _, segs = gk.gk_plan_segments(plan, dense=True)
+            finally:
+                gk.gk_plan_destroy(plan)
+            need = int((segs[:, 3] >= 0).sum()) * Hq * (d + 1) * 4
+            if need > lim:
+                break
+        assert need > lim, f"no batch tried needs more than {lim} bytes of partial states ({need})"
         with pytest.raises(gk.GkError) as e:
             gk.gk_decode_dense_static(eng.pool, None, 0, b)
         assert e.value.status == gk.GK_ERR_INVALID and "scratch" in str(e.value)
     finally:
         eng.close()
+
+
+def test_static_scratch_refuses_a_capturing_stream():
+    """The call copies its tables from host memory it frees on return, so a
+    capturing stream gets GK_ERR_UNSUPPORTED and the capture itself stays valid."""
+    from gpu_workload import GpuWorkload
+    w = workloads.config(2, B=4, Lp=300, suffix_range=(20, 60), L=1)
+    gw = GpuWorkload(w)
+    try:
+        b = gw.batch()
+        q = gw.q(0)
+        out, lse = gw.outputs()
+        b.set_device(d_q=q, d_out=out, d_lse=lse)
+        gk.gk_decode_dense_static(gw.eng.pool, None, 0, b)      # first call: address look-up
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            g.capture_begin()
+            try:
+                with pytest.raises(gk.GkError) as e:
+                    gk.gk_decode_dense_static(gw.eng.pool, s, 0, b)
+            finally:
+                g.capture_end()
+        assert e.value.status == gk.GK_ERR_UNSUPPORTED
+    finally:
+        gw.close()
