@@ -1,16 +1,20 @@
 #!/usr/bin/env python
 """Decode-step benchmark of the shared-prefix paged attention library on GB300.
 
-Workload (default): Llama-3.1-8B attention geometry (Hq 32, Hkv 8, d 128, bf16,
-32 layers), one shared prefix of 16384 tokens in the HOT pool and 64 requests
-with suffixes uniform in 256..2048 tokens in a page-size-1 COLD pool with
-shuffled slots.  One step = the whole decode step of all layers:
-  host: gk_seq_append_slots (64 tokens), gk_seq_tables, gk_plan_update, gk_dispatch
+Workload (default, the largest that fits one GPU): Qwen-2.5-14B attention
+geometry (Hq 40, Hkv 8, d 128, bf16, 48 layers), 8 shared prefixes with lengths
+log-uniform in 2K..16K tokens in the HOT pool, 16..64 requests per prefix (368
+in all, interleaved in the batch) with suffixes uniform in 128..4096 tokens in a
+page-size-1 COLD pool with shuffled slots.  One step = the whole decode step of
+all layers:
+  host: gk_seq_append_slots (one token per request), gk_seq_tables,
+  gk_plan_update, gk_dispatch
   device, per layer: copy-on-write copies if the step has any (gk_append_kv with
   n = 0), then the dispatcher's backend with the step's token appended by the
   decode itself (cascade: prefix contraction beside the suffix gather, LSE
   merge; or dense).
 Metric: decode attention queries/s per layer = B * L / step time.
+--config 2, 3 and 5 select the other multi-agent workloads.
 
 --impl reference times the fp64 CPU oracle instead (there is no other
 implementation to run); each of its steps is a bounded sample of one layer.
@@ -42,7 +46,11 @@ def _args():
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=4)
+    ap.add_argument("--override", action="append", default=[], metavar="KEY=INT",
+                    help="workload override passed to synth.workloads.config (e.g. B=512, Lp=16384)")
+    ap.add_argument("--stages-only", action="store_true",
+                    help="time each kernel alone on layer 0 (the 'stages' object) and print only that")
     ap.add_argument("--backend", choices=["auto", "cascade", "dense"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -102,7 +110,7 @@ class Clocks:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
-    PERIOD_MS = 25
+    PERIOD_MS = 10
 
     def __init__(self, gpu_index):
         self.idx = gpu_index
@@ -117,10 +125,10 @@ class Clocks:
             self.proc = None
 
     def stop(self, window=None):
-        """Summary of the samples; with window = (t0, t1) (host epoch seconds around the timed
-        region) only the samples taken inside it count, when there are any."""
+        """Stop sampling; summary of the samples (see summary)."""
+        self.rows = []
         if not self.proc:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return self.summary(window)
         self.proc.terminate()
         try:
             out, _ = self.proc.communicate(timeout=5)
@@ -128,7 +136,6 @@ class Clocks:
             self.proc.kill()
             out, _ = self.proc.communicate()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        rows = []
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
@@ -144,7 +151,16 @@ class Clocks:
                         (float("0." + f[9].split(".")[1]) if "." in f[9] else 0.0)
                 except (ValueError, IndexError):
                     t = None
-            rows.append((t,) + row)
+            self.rows.append((t,) + row)
+        return self.summary(window)
+
+    def summary(self, window=None):
+        """Median SM clock, max clock and throttle reasons of the samples; with window =
+        (t0, t1) (host epoch seconds around a timed region) only the samples taken inside it
+        count, when there are any."""
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = getattr(self, "rows", [])
         inside = rows
         where = "all samples"
         if window is not None:
@@ -175,15 +191,19 @@ def source_sha256(files):
     return h.hexdigest()
 
 
-PROFILED_WORKLOAD = "llama8b_32L_lp16384_b64"   # the workload the committed ncu summaries cover
+def profile_tag(workload_name):
+    """The name an ncu summary under profiles/ carries for a workload: its geometry and
+    batch without the layer count, the suffix range or a --layers cut (a summary covers
+    one launch, which is the same in every layer)."""
+    t = re.sub(r"_first\d+layers$", "", workload_name)
+    t = re.sub(r"_s\d+-\d+$", "", t)
+    return re.sub(r"_\d+L_", "_", t)
 
 
-def _profile_traffic(kernel_tag, src_files, workload=PROFILED_WORKLOAD):
-    """dram bytes per launch from the committed ncu summary, if it covers this workload and
-    the kernel sources are unchanged."""
-    if not workload.startswith(PROFILED_WORKLOAD):
-        return None
-    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+def _profile_traffic(kernel, src_files, workload_name):
+    """dram bytes per launch from the committed ncu summary profiles/<kernel>_<tag>.md, if
+    there is one for this workload and the kernel sources are unchanged since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{profile_tag(workload_name)}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -193,6 +213,27 @@ def _profile_traffic(kernel_tag, src_files, workload=PROFILED_WORKLOAD):
     if not m or not h:
         return None
     return float(m.group(1)) if source_sha256(src_files) == h.group(1) else None
+
+
+def l2_copy_gbs(torch, mib=24, reps=50):
+    """Copy bandwidth inside L2: two buffers of `mib` MiB (together well under the 126 MB
+    L2) copied back and forth; read + write bytes, best of three CUDA-event runs.  The
+    roof for a kernel whose reads mostly hit L2 (the flat backend's prefix re-reads)."""
+    a = torch.empty(mib << 20, dtype=torch.uint8, device="cuda")
+    b = torch.empty_like(a)
+    a.zero_()
+    for _ in range(10):
+        b.copy_(a)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = 0.0
+    for _ in range(3):
+        e0.record()
+        for i in range(reps):
+            (b if i % 2 == 0 else a).copy_(a if i % 2 == 0 else b)
+        e1.record()
+        torch.cuda.synchronize()
+        best = max(best, 2 * a.numel() * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    return best
 
 
 # ----------------------------------------------------------------------------------------------
@@ -259,7 +300,14 @@ def _config_dict(w, backend):
     return {"workload": w.name, "B": w.B, "layers": w.L, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d,
             "prefix_lens": w.prefix_lens, "suffix_min": min(s), "suffix_max": max(s), "suffix_sum": sum(s),
             "cold_page_size": w.page_size, "backend": backend, "parallelism": "replicas",
-            "l2": "inputs larger than L2 (each layer reads a distinct 352 MiB of K/V; 11 GB per step)"}
+            "l2": f"inputs larger than L2 (each layer reads a distinct {_layer_kv_mib(w)} MiB of K/V; "
+                  f"{_layer_kv_mib(w) * w.L / 1024:.1f} GiB per step)"}
+
+
+def _layer_kv_mib(w):
+    """K/V bytes one layer of the cascade reads: each prefix once, every suffix."""
+    tok = sum(w.prefix_lens) + sum(r.suffix_len for r in w.requests)
+    return int(tok * 2 * w.Hkv * w.d * 2 / 2**20)
 
 
 # ----------------------------------------------------------------------------------------------
@@ -275,7 +323,7 @@ def _set_arrangement(gk, pool, a):
         gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_AUTO, 0)
 
 
-def stage_rooflines(gk, torch, pool, batch, w, P, hbm, tc_burst, reps=7):
+def stage_rooflines(gk, torch, pool, batch, w, P, hbm, tc_burst, l2_gbs, reps=7):
     """Each kernel of the path timed alone on layer 0 of the batch as it stands: a sequential
     cascade plan's prefix contraction (gk_cascade_prefix), suffix gather (gk_cascade_suffix) and
     merge (gk_cascade_merge), then the dense backend (gk_decode_dense).  L2 is flushed before
@@ -283,7 +331,9 @@ def stage_rooflines(gk, torch, pool, batch, w, P, hbm, tc_burst, reps=7):
     stream is kept.  The prefix contraction and the suffix gather are also timed as a decode
     step runs them: one launch per layer, back to back (each overlaps its set-up with the end
     of the one before), time per launch.
-    A kernel timed alone is compared with the burst peaks."""
+    A kernel timed alone is compared with the burst peaks.  The flat backend's prefix
+    re-reads mostly hit L2, so its algorithmic bytes are held to the measured L2 copy
+    bandwidth (l2_gbs) and only its DRAM bytes (from its ncu summary) to HBM."""
     import numpy as np
     B, Hq, d = w.B, w.Hq, w.d
     stream = torch.cuda.current_stream()
@@ -364,21 +414,90 @@ def stage_rooflines(gk, torch, pool, batch, w, P, hbm, tc_burst, reps=7):
         out["prefix"]["hbm_frac"] = out["prefix"]["gbs"] / hbm
         out["prefix"]["bound"] = "tensor" if flops / pre_bytes > tc_burst * 1e3 / hbm else "hbm"
         out["suffix"]["hbm_frac"] = out["suffix"]["gbs"] / hbm
-        out["dense"]["hbm_frac"] = out["dense"]["gbs"] / hbm
         m = out["merge"]
         m["gbs"] = m["bytes"] / (t_mrg * 1e-3) / 1e9
-        # DRAM bytes per launch from the committed ncu summaries (null unless they cover this
+        # DRAM bytes per launch from the committed ncu summaries (null unless one covers this
         # workload and the kernel's sources are unchanged)
-        out["prefix"]["traffic"] = _profile_traffic("prefix_kernel_llama8b_lp16384_b64", PREFIX_SRC, w.name)
-        out["suffix"]["traffic"] = _profile_traffic("suffix_gather_llama8b_lp16384_b64", GATHER_SRC, w.name)
-        out["dense"]["traffic"] = _profile_traffic("dense_gather_llama8b_lp16384_b64", GATHER_SRC, w.name)
-        out["peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tc_burst, "which": "burst (kernels timed alone)"}
+        out["prefix"]["traffic"] = _profile_traffic("prefix_kernel", PREFIX_SRC, w.name)
+        out["suffix"]["traffic"] = _profile_traffic("suffix_gather", GATHER_SRC, w.name)
+        dn = out["dense"]
+        dn["traffic"] = _profile_traffic("dense_gather", GATHER_SRC, w.name)
+        # the flat backend: algorithmic bytes against the L2 roof; DRAM bytes against HBM
+        dn["l2_roof_gbs"] = l2_gbs
+        dn["l2_frac"] = dn["gbs"] / l2_gbs
+        dn["dram_gbs"] = dn["traffic"] / (t_den * 1e-3) / 1e9 if dn["traffic"] else None
+        dn["hbm_frac"] = dn["dram_gbs"] / hbm if dn["dram_gbs"] else None
+        out["peaks"] = {"hbm_gbs": hbm, "bf16_tflops": tc_burst, "l2_copy_gbs": l2_gbs,
+                        "which": "burst (kernels timed alone); L2: measured in this run"}
         out["timing"] = (f"layer 0, sequential plan, L2 flushed before each launch, median of {reps}; "
                          f"*_chained: one launch per layer back to back over the {w.L} layers, L2 flushed "
                          f"before the chain, time per launch")
         return out
     finally:
         gk.gk_plan_destroy(plan)
+
+
+def chained_kernels(gk, torch, pool, batch, plan, w, backend, q_all, out_all, lse_all, chains=5):
+    """Per-launch time of each kernel of the step's backend: the kernel launched for every
+    layer back to back on one stream (each launch overlaps its set-up with the end of the one
+    before, as in a decode step), L2 flushed before each chain, median of `chains` chains.
+    The step's new tokens are in the pool by now, so the chains read them from there."""
+    import numpy as np
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    clean = torch.zeros(256 << 20, dtype=torch.uint8, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    batch.c.d_new_k = None
+    batch.c.d_new_v = None
+
+    def chain(fn):
+        ts = []
+        for _ in range(chains + 1):
+            flush.zero_()
+            clean.max()
+            e0.record(stream)
+            for l in range(w.L):
+                batch.set_device(d_q=q_all[l], d_out=out_all[l], d_lse=lse_all[l])
+                fn(l)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / w.L)
+        return {"ms": float(np.median(ts[1:])), "launches": w.L, "chains": chains}
+
+    out = {}
+    if backend == "cascade":
+        out["cascade_levels"] = chain(lambda l: gk.gk_cascade_levels(pool, stream, l, batch, plan))
+        out["lse_merge"] = chain(lambda l: gk.gk_cascade_merge(pool, stream, l, batch, plan))
+        out["layer"] = chain(lambda l: gk.gk_decode_cascade(pool, stream, l, batch, plan))
+    else:
+        out["dense_gather"] = chain(lambda l: gk.gk_decode_dense(pool, stream, l, batch, plan))
+    if gk.gk_device_error(pool, stream):
+        raise RuntimeError("device error word set in the kernel chains")
+    return out
+
+
+def run_stages_only(a, w):
+    """The 'stages' object alone: each kernel timed by itself on layer 0 of the workload as
+    it is set up (no decode steps before it).  Used to profile one kernel launch."""
+    import torch
+    from gpu_workload import GpuWorkload
+    from paged_kv_cache_pool_gb300 import binding as gk
+    torch.cuda.set_device(0)
+    gw = GpuWorkload(w)
+    try:
+        cm_path = os.path.join(ROOT, "paged_kv_cache_pool_gb300", "cost_model_gb300.json")
+        if os.path.exists(cm_path):
+            gk.gk_cost_model_load(gw.eng.pool, open(cm_path).read())
+        b = gw.batch()
+        q = gw.q(0)
+        out, lse = gw.outputs()
+        b.set_device(d_q=q, d_out=out, d_lse=lse)
+        peaks, _ = _peaks()
+        st = stage_rooflines(gk, torch, gw.eng.pool, b, w, gw.P, float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
+                             float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])), l2_copy_gbs(torch))
+        print(json.dumps({"workload": w.name, "stages": st}))
+    finally:
+        gw.close()
 
 
 def run_ours(a, w):
@@ -442,7 +561,7 @@ def run_ours(a, w):
     choices = []
     predicted = []
 
-    def step(events=None, q=q_all, k=newk, v=newv, out=out_all, lse=lse_all):
+    def step(q=q_all, k=newk, v=newv, out=out_all, lse=lse_all):
         # a0: host plan (append one token per request, tables, plan, dispatch)
         slots, cow = gk.gk_seq_append_slots(pool, seqs)
         staged.synchronize()                    # the previous step's staging copies have left
@@ -471,9 +590,6 @@ def run_ours(a, w):
             choice = forced
         choices.append(choice)
         for l in range(L):
-            ev = events[l] if (events is not None and l in events) else None
-            if ev is not None:
-                ev[0].record(stream)
             if a.append == "fused":
                 # the step's new tokens are appended by the decode itself; copy-on-write
                 # copies, when the step has any, come first
@@ -485,24 +601,12 @@ def run_ours(a, w):
                 gk.gk_append_kv(pool, stream, l, d_slots, k[l], v[l], d_cow if ncow else None, n=B, n_cow=ncow)
                 launches[0] += 1 + (1 if ncow else 0)
                 batch.set_device(d_q=q[l], d_out=out[l], d_lse=lse[l])
-            if ev is not None:
-                ev[1].record(stream)
             if choice == gk.GK_BACKEND_CASCADE:
-                # the probe layer runs gk_decode_cascade's two calls with an event between
-                if ev is not None:
-                    gk.gk_cascade_levels(pool, stream, l, batch, plan[0])
-                    ev[2].record(stream)
-                    gk.gk_cascade_merge(pool, stream, l, batch, plan[0])
-                else:
-                    gk.gk_decode_cascade(pool, stream, l, batch, plan[0])
+                gk.gk_decode_cascade(pool, stream, l, batch, plan[0])
                 launches[0] += (1 if split[0] else 2) + 1
             else:
                 gk.gk_decode_dense(pool, stream, l, batch, plan[0])
-                if ev is not None:
-                    ev[2].record(stream)
                 launches[0] += 1 + dense_merge[0]
-            if ev is not None:
-                ev[3].record(stream)
 
     for _ in range(a.warmup):
         step()
@@ -513,12 +617,7 @@ def run_ours(a, w):
     if world > 1:
         torch.distributed.barrier()
 
-    # ---- timed region: device-resident inputs ----
-    # Per-kernel events bracket one layer per step (a different layer each step):
-    # an event between two kernels stops the next one from launching early, so
-    # the other layers run undisturbed.
-    probe_layer = [i % L for i in range(a.steps)]
-    events = [{probe_layer[i]: [torch.cuda.Event(enable_timing=True) for _ in range(4)]} for i in range(a.steps)]
+    # ---- timed region: device-resident inputs, nothing but the steps in the stream ----
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     vis_list = [x for x in vis.split(",") if x.strip()]
@@ -532,12 +631,10 @@ def run_ours(a, w):
     w0 = time.time()
     t_start.record(stream)
     for i in range(a.steps):
-        step(events[i])
+        step()
     t_end.record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
-    time.sleep(0.1)   # let the sampler report the samples of the region's end
-    clk = clocks.stop((w0, w1))
     gpu_launches = launches[0]
     elapsed_ms = t_start.elapsed_time(t_end)
     err = gk.gk_device_error(pool, stream)
@@ -547,53 +644,6 @@ def run_ours(a, w):
     elapsed_ms = max_over_ranks(elapsed_ms)
     ms_per_step = elapsed_ms / a.steps
     value = replica_throughput(world, B * L * a.steps, elapsed_ms)
-
-    # per-kernel averages over the timed region
-    k_ms = {"append": [], "levels": [], "merge": [], "dense": []}
-    for i in range(a.steps):
-        cas = step_choices[i] == gk.GK_BACKEND_CASCADE
-        for l, e in events[i].items():
-            k_ms["append"].append(e[0].elapsed_time(e[1]))
-            if cas:
-                k_ms["levels"].append(e[1].elapsed_time(e[2]))
-                k_ms["merge"].append(e[2].elapsed_time(e[3]))
-            else:
-                k_ms["dense"].append(e[1].elapsed_time(e[3]))
-    avg = {k: (sum(v) / len(v) if v else None) for k, v in k_ms.items()}
-    info = gk.gk_plan_info(plan[0])
-    peaks, peak_src = _peaks()
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    s_tot = int(batch.suffix_len.sum())
-    # algorithmic bytes per launch (prefix K/V once per group, suffix K/V, slots, queries, partial states)
-    partial_bytes = info["num_partials"] * Hq * (d + 1) * 4
-    levels_bytes = (info["prefix_bytes"] + info["suffix_bytes"] + s_tot * 4 // P + B * Hq * d * 2 + partial_bytes)
-    dense_bytes = info["dense_bytes"] + s_tot * 4 // P + B * Hq * d * 2 + B * Hq * (d + 1) * 4
-    kernels = {}
-    if avg["levels"]:
-        kernels["cascade_levels"] = {"ms": avg["levels"], "bytes": levels_bytes, "flops": info["prefix_flops"],
-                                     "gbs": levels_bytes / (avg["levels"] * 1e-3) / 1e9,
-                                     "tflops": info["prefix_flops"] / (avg["levels"] * 1e-3) / 1e12,
-                                     "arrangement": "split" if info["cascade_split"] else "sequential"}
-    if avg["merge"]:
-        kernels["lse_merge"] = {"ms": avg["merge"]}
-    if avg["dense"]:
-        kernels["dense_gather"] = {"ms": avg["dense"], "bytes": dense_bytes,
-                                   "gbs": dense_bytes / (avg["dense"] * 1e-3) / 1e9}
-    kernels["append_kv"] = {"ms": avg["append"]}
-    # dominant kernel -> roofline (the cascade's two levels are one launch in a split plan)
-    dom = max(((k, v["ms"]) for k, v in kernels.items() if "bytes" in v), key=lambda x: x[1])[0]
-    kd = kernels[dom]
-    if dom == "cascade_levels" and kd["flops"] / kd["bytes"] > tc_peak * 1e3 / hbm:
-        roof = {"kernel": dom, "bound": "tensor", "achieved": kd["tflops"], "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": kd["tflops"] / tc_peak,
-                "traffic": _profile_traffic("cascade_levels_llama8b_lp16384_b64", LEVELS_SRC, w.name)}
-    else:
-        tag = {"cascade_levels": ("cascade_levels_llama8b_lp16384_b64", LEVELS_SRC),
-               "dense_gather": ("dense_gather_llama8b_lp16384_b64", GATHER_SRC)}[dom]
-        roof = {"kernel": dom, "bound": "hbm", "achieved": kd["gbs"], "peak": hbm, "unit": "GB/s",
-                "frac": kd["gbs"] / hbm, "traffic": _profile_traffic(*tag, w.name)}
-    roof["peak_source"] = f"{peak_src} ({'bf16_tflops_sustained' if roof['bound'] == 'tensor' else 'hbm_gbs'})"
 
     # ---- e2e: host buffers, copies inside the timed region ----
     e2e = None
@@ -630,7 +680,7 @@ def run_ours(a, w):
                 i = t % 2
                 stream.wait_event(ev_in[i])
                 stream.wait_event(ev_out[i])   # the step before last has left this output buffer
-                step(None, *dev_in[i], *dev_out[i])
+                step(*dev_in[i], *dev_out[i])
                 ev_used[i].record(stream)
                 if t + 1 < n:
                     h2d(1 - i)
@@ -646,11 +696,13 @@ def run_ours(a, w):
         if world > 1:
             torch.distributed.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        v0 = time.time()
         e0.record(stream)
         copy_s.wait_event(e0)
         run_steps(a.steps)
         e1.record(stream)
         torch.cuda.synchronize()
+        e2e_window = (v0, time.time())
         ems = max_over_ranks(e0.elapsed_time(e1))
         h2d_bytes = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + B * max_blocks * 4
         d2h_bytes = ho.numel() * 4 + hl.numel() * 4
@@ -658,21 +710,69 @@ def run_ours(a, w):
                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "ms_per_step": ems / a.steps,
                "copies": "double-buffered on a second stream, overlapping the neighbouring steps' compute"}
 
+    time.sleep(0.1)   # let the sampler report the samples of the regions' ends
+    clk = clocks.stop((w0, w1))
+    if e2e is not None:
+        e2e["clocks"] = clocks.summary(e2e_window)
+
     if rank != 0:
         if world > 1:
             torch.distributed.barrier()
             torch.distributed.destroy_process_group()
         gw.close()
         return
+
+    # ---- per-kernel times: each kernel of the step's backend launched for every layer back
+    # to back, as the step runs them (no event between two kernels of a layer, which would
+    # stop the next one from starting early); time per launch, after the timed region ----
+    info = gk.gk_plan_info(plan[0])
+    backend_name = "cascade" if step_choices and step_choices[0] == gk.GK_BACKEND_CASCADE else "dense"
+    kernels = chained_kernels(gk, torch, pool, batch, plan[0], w, backend_name, q_all, out_all, lse_all)
+    peaks, peak_src = _peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    l2_gbs = l2_copy_gbs(torch)
+    s_tot = int(batch.suffix_len.sum())
+    # algorithmic bytes per launch (prefix K/V once per group, suffix K/V, slots, queries, partial states)
+    partial_bytes = info["num_partials"] * Hq * (d + 1) * 4
+    levels_bytes = (info["prefix_bytes"] + info["suffix_bytes"] + s_tot * 4 // P + B * Hq * d * 2 + partial_bytes)
+    dense_bytes = info["dense_bytes"] + s_tot * 4 // P + B * Hq * d * 2 + B * Hq * (d + 1) * 4
+    if "cascade_levels" in kernels:
+        kl = kernels["cascade_levels"]
+        kl.update(bytes=levels_bytes, flops=info["prefix_flops"], gbs=levels_bytes / (kl["ms"] * 1e-3) / 1e9,
+                  tflops=info["prefix_flops"] / (kl["ms"] * 1e-3) / 1e12,
+                  arrangement="split" if info["cascade_split"] else "sequential")
+    if "dense_gather" in kernels:
+        kd_ = kernels["dense_gather"]
+        kd_.update(bytes=dense_bytes, gbs=dense_bytes / (kd_["ms"] * 1e-3) / 1e9)
+    # dominant kernel -> roofline (the cascade's two levels are one launch in a split plan)
+    dom = max(((k, v["ms"]) for k, v in kernels.items() if "bytes" in v), key=lambda x: x[1])[0]
+    kd = kernels[dom]
+    if dom == "cascade_levels" and kd["flops"] / kd["bytes"] > tc_peak * 1e3 / hbm:
+        roof = {"kernel": dom, "bound": "tensor", "achieved": kd["tflops"], "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": kd["tflops"] / tc_peak, "traffic": _profile_traffic("cascade_levels", LEVELS_SRC, w.name)}
+    elif dom == "cascade_levels":
+        roof = {"kernel": dom, "bound": "hbm", "achieved": kd["gbs"], "peak": hbm, "unit": "GB/s",
+                "frac": kd["gbs"] / hbm, "traffic": _profile_traffic("cascade_levels", LEVELS_SRC, w.name)}
+    else:
+        # the flat backend re-reads each prefix from L2: its DRAM bytes (ncu) against HBM
+        tr = _profile_traffic("dense_gather", GATHER_SRC, w.name)
+        roof = {"kernel": dom, "bound": "hbm", "achieved": tr / (kd["ms"] * 1e-3) / 1e9 if tr else None,
+                "peak": hbm, "unit": "GB/s", "frac": tr / (kd["ms"] * 1e-3) / 1e9 / hbm if tr else None,
+                "traffic": tr, "algorithmic_gbs": kd["gbs"], "l2_roof_gbs": l2_gbs,
+                "l2_frac": kd["gbs"] / l2_gbs}
+    roof["peak_source"] = f"{peak_src} ({'bf16_tflops_sustained' if roof['bound'] == 'tensor' else 'hbm_gbs'})"
+    roof["timing"] = (f"{kd['launches']} launches back to back (one per layer, L2 flushed before the chain), "
+                      f"median of {kd['chains']} chains; times {L} layers = {kd['ms'] * L:.3f} ms "
+                      f"of the {ms_per_step:.3f} ms step")
     stages = None
     if not a.no_stages:
         stages = stage_rooflines(gk, torch, pool, batch, w, P, hbm,
-                                 float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])))
+                                 float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])), l2_gbs)
         _set_arrangement(gk, pool, a)
     cpu = None
     if not a.no_cpu:
         cpu = cpu_baseline(w)
-    backend_name = "cascade" if step_choices and step_choices[0] == gk.GK_BACKEND_CASCADE else "dense"
     pd, pc = predicted[-1]
     layer_us = ms_per_step * 1e3 / L
     dispatch = {"choice": backend_name, "predicted_dense_us": pd, "predicted_cascade_us": pc,
@@ -696,7 +796,11 @@ def run_ours(a, w):
 def main():
     a = _args()
     from synth import workloads
-    w = workloads.config(a.config)
+    ov = {}
+    for kv in a.override:
+        k, v = kv.split("=", 1)
+        ov[k] = int(v)
+    w = workloads.config(a.config, **ov)
     if a.layers:
         w.L = a.layers
         w.name += f"_first{a.layers}layers"
@@ -707,7 +811,10 @@ def main():
         from synth import device
         build.build()
         device.build()
-        run_ours(a, w)
+        if a.stages_only:
+            run_stages_only(a, w)
+        else:
+            run_ours(a, w)
 
 
 if __name__ == "__main__":

@@ -57,3 +57,24 @@ def test_unavailable_and_empty():
     assert c.stop()["reasons"] == ["nvidia-smi unavailable"]
     c.proc = _FakeSmi("")
     assert c.stop((0.0, 1.0))["reasons"] == ["no samples"]
+
+
+def test_summary_of_a_second_window_after_stop():
+    """The e2e region's clocks come from the same samples, over its own window."""
+    t0 = 1_800_000_000.0
+    lines = [_line(t0 + 0.05, 2070), _line(t0 + 0.10, 2060),
+             _line(t0 + 1.05, 1900, ("Not Active", "Not Active", "Not Active", "Active")),
+             _line(t0 + 1.10, 1950, ("Not Active", "Not Active", "Not Active", "Active"))]
+    c = bench.Clocks("0")
+    c.proc = _FakeSmi("\n".join(lines) + "\n")
+    r = c.stop((t0, t0 + 0.2))
+    assert r["samples"] == 2 and r["reasons"] == []
+    r2 = c.summary((t0 + 1.0, t0 + 1.2))
+    assert r2["samples"] == 2 and r2["reasons"] == ["sw_power_cap"] and r2["sm_mhz"] == 1950.0
+
+
+def test_profile_tag_names_the_workload_not_its_layer_cut():
+    assert bench.profile_tag("qwen14b_48L_8prefix_b368") == "qwen14b_8prefix_b368"
+    assert bench.profile_tag("qwen14b_48L_8prefix_b368_first1layers") == "qwen14b_8prefix_b368"
+    assert bench.profile_tag("llama8b_32L_lp16384_b64_s256-2048") == "llama8b_lp16384_b64"
+    assert bench.profile_tag("llama8b_32L_lp16384_b512_s256-2048_first1layers") == "llama8b_lp16384_b512"
