@@ -227,6 +227,8 @@ typedef struct gk_plan_summary {
                                      the suffix gather (suffix_ctas SMs) side by side in one launch;
                                      0: one after the other, each over every SM */
   int32_t prefix_tiles_per_item;  /* 128-key tiles of the longest prefix work item */
+  int32_t prefix_kernel;          /* prefix work items: GK_PREFIX_TENSOR or GK_PREFIX_WARP */
+  int32_t prefix_rows_per_item;   /* stacked query rows per prefix work item: 256 or 128 */
 } gk_plan_summary;
 
 /* Plan one decode step: group requests by HOT prefix (stable, first appearance),
@@ -333,23 +335,33 @@ typedef struct gk_cost_model {
   double c_gather_us;             /* fixed cost of a separate suffix-gather launch (sequential plans) */
   double prefix_tile_split_us;    /* prefix_tile_us for an item of a split plan, which runs beside a
                                      gather that keeps HBM busy (its K/V tiles wait longer) */
+  double warp_tile_us;            /* one 128-key tile of a warp-MMA prefix item (up to 128 rows) alone */
+  double warp_item_us;            /* fixed cost of a warp-MMA prefix item (of each wave of them) */
+  double warp_tile_split_us;      /* warp_tile_us beside the gather of a split plan */
 } gk_cost_model;
 
 /* Predict both backends for the plan and pick the smaller:
  *   T_dense   = c_flat + dense_bytes / bw_flat
  *   T_cascade = c_cascade + T_levels + c_merge * B * Hq
- * with C = gk_plan_summary.prefix_tiles_per_item key tiles per prefix item and
+ * with C = gk_plan_summary.prefix_tiles_per_item key tiles per prefix item,
+ * (tile, tile_split, item) = (prefix_tile, prefix_tile_split, prefix_item) for
+ * tensor-core items and (warp_tile, warp_tile_split, warp_item) for warp-MMA
+ * items (gk_plan_summary.prefix_kernel), and
  *   sequential plan (W = ceil(prefix_ctas / SMs) waves of prefix items):
- *     T_levels = max(prefix_bytes / bw_prefix, W * (C * prefix_tile + prefix_item))
+ *     T_levels = max(prefix_bytes / bw_prefix, W * (C * tile + item))
  *                + c_gather + suffix_bytes / bw_suffix
- *   split plan (see gk_plan_summary.cascade_split; item = C * prefix_tile_split + prefix_item):
- *     T_levels = max(item, (suffix_bytes / gather_sm + prefix_ctas * item) / SMs,
+ *   split plan (see gk_plan_summary.cascade_split; it = C * tile_split + item):
+ *     T_levels = max(it, (suffix_bytes / gather_sm + prefix_ctas * it) / SMs,
  *                    (suffix_bytes + prefix_bytes) / bw_suffix)
  *   (the middle term spreads the gather's SM-time and the items over every SM)
  * A plan without prefix work has no prefix term.  GraniKV's M_eff (Eq. 2)
- * enters through the items: a group of M_eff stacked rows gives ceil(M_eff/256)
- * items per KV head and key split.  Dense is chosen only when strictly faster.
- * Host only. */
+ * enters through the items: a group of M_eff stacked rows gives
+ * ceil(M_eff / rows per item) items per KV head and key split.  The plan has
+ * already chosen the prefix kernel and the arrangement with the smallest
+ * T_levels (GraniKV Section 3.6's routing between its two prefix kernels, with
+ * the threshold replaced by the measured model), so this call completes the
+ * three-way choice: flat, cascade over tensor-core items, cascade over warp-MMA
+ * items.  Dense is chosen only when strictly faster.  Host only. */
 gk_status gk_dispatch(const gk_pool* pool, const gk_plan* plan, gk_backend* choice, double* t_dense_us,
                       double* t_cascade_us);
 gk_status gk_cost_model_set(gk_pool* pool, const gk_cost_model* cm);
@@ -389,11 +401,33 @@ typedef enum gk_gather_partition {
   GK_PARTITION_PER_REQUEST = 1
 } gk_gather_partition;
 gk_status gk_pool_set_gather_partition(gk_pool* pool, gk_gather_partition partition);
+
+/* Which kernel runs the shared-prefix level of the cascade in the plans the
+ * pool builds from now on.  GraniKV Section 3.5 pairs two: the shared-prefix
+ * matmul ("GKV-dense": every row sharing the prefix stacked into one
+ * tensor-core contraction) and the cascade backend's level-0 kernel
+ * ("GKV-cascade": a FlashAttention-style tiled online softmax that reads the
+ * prefix once), and Section 3.6 routes between them on M_eff.
+ *  GK_PREFIX_AUTO (default): per step, the one whose cascade the cost model
+ *    predicts faster (ties go to the tensor-core items).
+ *  GK_PREFIX_TENSOR: tcgen05 items of 256 stacked rows (two 128-row tiles).
+ *  GK_PREFIX_WARP: warp-MMA items of 128 stacked rows (8 warps x 16 rows), no
+ *    tensor memory; meant for small M_eff.
+ * Either kind writes the same partial states (one per request, query head and
+ * key split); the arrangement (gk_pool_set_cascade_mode) applies to both.
+ * Host only.  GK_ERR_INVALID for an unknown value. */
+typedef enum gk_prefix_kernel {
+  GK_PREFIX_AUTO = 0,
+  GK_PREFIX_TENSOR = 1,
+  GK_PREFIX_WARP = 2
+} gk_prefix_kernel;
+gk_status gk_pool_set_prefix_kernel(gk_pool* pool, gk_prefix_kernel kernel);
 gk_status gk_cost_model_get(const gk_pool* pool, gk_cost_model* cm);
 /* Same as gk_cost_model_set from JSON text: {"c_flat_us": .., "bw_flat_gbs": ..,
  * "c_cascade_us": .., "bw_prefix_gbs": .., "bw_suffix_gbs": .., "c_merge_us": ..,
  * "prefix_tile_us": .., "prefix_item_us": .., "gather_sm_gbs": .., "c_gather_us": ..,
- * "prefix_tile_split_us": ..}.
+ * "prefix_tile_split_us": .., "warp_tile_us": .., "warp_item_us": ..,
+ * "warp_tile_split_us": ..}.
  * Keys left out keep their current values; other keys are skipped. */
 gk_status gk_cost_model_load(gk_pool* pool, const char* json);
 

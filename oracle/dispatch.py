@@ -1,4 +1,4 @@
-"""ORACLE (test infrastructure): the per-step backend choice and cascade arrangement.
+"""ORACLE (test infrastructure): the dispatcher's cost formula and work decomposition.
 
 GraniKV Section 3.6, Eq. 2: M_eff(step) = B_step * n_q/kv, the M dimension of the
 stacked shared-prefix contraction.  The pages route on M_eff >= M_sat with an
@@ -9,38 +9,36 @@ predicted time runs (flat wins only when strictly faster):
 
   T_flat    = c_flat + bytes_flat / bw_flat
   T_cascade = c_cascade + T_levels + c_merge * B * Hq
-  item(C)   = C * prefix_tile + prefix_item        (one prefix work item of C key tiles, alone)
-  item'(C)  = C * prefix_tile_split + prefix_item  (the same beside a gather that keeps HBM busy)
+  item(C)   = C * tile + item_fixed          (one prefix work item of C key tiles, alone)
+  item'(C)  = C * tile_split + item_fixed    (the same beside a gather that keeps HBM busy)
   T_levels  = max(bytes_pre / bw_prefix, W * item(C)) + c_gather
-              + bytes_suffix / bw_suffix                          (sequential plan)
+              + bytes_suffix / bw_suffix                          (sequential plan, W waves)
             = max(item'(C), (bytes_suffix / gather_sm + n_pre * item'(C)) / SMs,
                   (bytes_suffix + bytes_pre) / bw_suffix)          (split plan)
 
-Work items: a group of M_eff stacked rows and Lp keys contributes ceil(M/256)
-row blocks x Hkv heads x ceil(ceil(Lp/128)/C) items, so M_eff enters through the
-item count.  A sequential plan runs them in W = ceil(items/SMs) waves over every
-SM, with C the smallest value minimising W * item(C); then the gather runs over every SM
-as its own launch.  A split plan is one launch with a CTA per SM: CTA b < n_pre
-first runs prefix item b, and every CTA gathers a slot of the suffix, a prefix
-CTA's slot cut to the time its item leaves (the middle term spreads the
-gather's SM-time and the items over all SMs; the last is HBM).  The planner
-takes the C with the smallest split prediction (the largest C among equal
-ones, i.e. the fewest items), among those with no more items than SMs whose
-prefix CTAs keep a gather share of at least MIN_PREFIX_SHARE (share =
-max(0, T - item'(C) - c_gather) / T; a forced split with no such C takes the
-best prediction), then
-lowers C to the smallest value giving as many items (balanced items), and
-splits when that beats the sequential T_levels.  A sequential plan's gather
-partition cuts the suffix tokens into quotas of ceil(total/n) rounded up to 64
-and then to a multiple of 16, so it may use fewer CTAs than SMs; a split
-plan's has one slot per SM.
+with (tile, tile_split, item_fixed) the terms of the plan's prefix kernel:
+tensor-core items (prefix_tile_us, prefix_tile_split_us, prefix_item_us; 256
+stacked rows per item) or warp-MMA items (warp_tile_us, warp_tile_split_us,
+warp_item_us; 128 rows per item), the two prefix kernels Section 3.5 pairs.
+
+Work decomposition (fixed by the kernels' tiling, not a heuristic): a group of
+M_eff stacked rows and Lp keys contributes ceil(M_eff / rows) row blocks x Hkv
+heads x ceil(ceil(Lp / 128) / C) items.
+
+Parity unpinned: which arrangement a plan takes (split or sequential, the key
+tiles per item C, the prefix kernel) is the planner's search over this model,
+and the pages fix none of it (their threshold is specific to the A100).  This
+oracle does not restate that search; it evaluates the formula above for the
+arrangement a plan reports, and the choice itself is held to measurement on
+the GPU (the dispatcher's pick against the faster backend's measured time, and
+each prediction against the measured layer time).
 
 Times are in microseconds, bandwidths in GB/s (1 GB/s = 1e3 bytes per us).
-
-Parity of the choice itself is unpinned by the pages (their threshold is
-specific to the A100); Eq. 2 and the formula are pinned by closed forms.
 """
 from __future__ import annotations
+
+ROWS = {"tensor": 256, "warp": 128}
+KEY_TILE = 128
 
 
 def m_eff(batch_requests: int, q_per_kv: int) -> int:
@@ -66,105 +64,68 @@ def features(prefix_lens, suffix_lens, group_of, Hq, Hkv, d):
         prefix=pre, B=len(group_of), Hq=Hq, Hkv=Hkv, suffix_tokens=sum(suffix_lens))
 
 
+def _ceil(a, b):
+    return -(-a // b)
+
+
+def n_items(f, C, kind="tensor"):
+    """Prefix work items of a plan with C key tiles per item: every (row block, KV head,
+    key split) of every group once."""
+    rows = ROWS[kind]
+    return sum(_ceil(p["M"], rows) * f["Hkv"] * _ceil(_ceil(p["lp"], KEY_TILE), C) for p in f["prefix"])
+
+
 def gather_ctas(tokens, n):
-    """CTAs the gather partition of `tokens` over at most n CTAs uses."""
+    """CTAs the stream partition of `tokens` over at most n CTAs uses: quotas of
+    ceil(tokens / n), at least 64 tokens, rounded up to a multiple of 16."""
     if tokens == 0:
         return 0
-    quota = max(-(-tokens // n), 64)
-    quota = -(-quota // 16) * 16
-    return -(-tokens // quota)
+    quota = max(_ceil(tokens, n), 64)
+    quota = _ceil(quota, 16) * 16
+    return _ceil(tokens, quota)
 
 
-def _tiles(f):
-    return [-(-p["M"] // 256) for p in f["prefix"]], [-(-p["lp"] // 128) for p in f["prefix"]]
+def _terms(cm, kind):
+    if kind == "warp":
+        return cm["warp_tile_us"], cm["warp_tile_split_us"], cm["warp_item_us"]
+    return cm["prefix_tile_us"], cm["prefix_tile_split_us"], cm["prefix_item_us"]
 
 
-def n_items(f, C):
-    mtiles, ntiles = _tiles(f)
-    return sum(m * f["Hkv"] * -(-n // C) for m, n in zip(mtiles, ntiles))
-
-
-def sequential_tiles(cm, f, num_sms):
-    """Key tiles per item of a sequential plan: the smallest C minimising
-    waves * (C * prefix_tile_us + prefix_item_us), an item's time alone."""
-    _, ntiles = _tiles(f)
-    best, best_c = None, max(ntiles)
-    for C in range(1, max(ntiles) + 1):
-        cost = -(-n_items(f, C) // num_sms) * item_us(cm, C)
-        if best is None or cost < best - 1e-9:
-            best, best_c = cost, C
-    return best_c
-
-
-def item_us(cm, C, split=False):
+def item_us(cm, C, split=False, kind="tensor"):
     """A prefix item of C key tiles: alone (sequential plans) or beside the gather (split plans)."""
-    return C * cm["prefix_tile_split_us" if split else "prefix_tile_us"] + cm["prefix_item_us"]
+    tile, tile_split, fixed = _terms(cm, kind)
+    return C * (tile_split if split else tile) + fixed
 
 
-def sequential_levels(cm, f, C, num_sms):
+def sequential_levels(cm, f, C, n_pre, num_sms, kind="tensor"):
     t = cm["c_gather_us"] + f["bytes_suffix"] / (cm["bw_suffix_gbs"] * 1e3)
-    if f["prefix"]:
-        waves = -(-n_items(f, C) // num_sms)
-        t += max(sum(p["bytes"] for p in f["prefix"]) / (cm["bw_prefix_gbs"] * 1e3), waves * item_us(cm, C))
+    if f["prefix"] and n_pre:
+        waves = -(-n_pre // num_sms)
+        t += max(sum(p["bytes"] for p in f["prefix"]) / (cm["bw_prefix_gbs"] * 1e3), waves * item_us(cm, C, kind=kind))
     return t
 
 
-# a split C qualifies only if its prefix CTAs keep this share of a gather-only CTA's suffix
-MIN_PREFIX_SHARE = 0.15
-
-
-def prefix_share(cm, C, T):
-    """Gather share of a prefix CTA (relative to a gather-only CTA) for items of C tiles, launch T."""
-    return max(0.0, T - item_us(cm, C, split=True) - cm["c_gather_us"]) / T
-
-
-def split_levels(cm, f, C, n_pre, num_sms):
-    it = item_us(cm, C, split=True)
+def split_levels(cm, f, C, n_pre, num_sms, kind="tensor"):
+    it = item_us(cm, C, split=True, kind=kind)
     bytes_pre = sum(p["bytes"] for p in f["prefix"])
     bal = (f["bytes_suffix"] / (cm["gather_sm_gbs"] * 1e3) + n_pre * it) / num_sms
     return max(it, bal, (f["bytes_suffix"] + bytes_pre) / (cm["bw_suffix_gbs"] * 1e3))
 
 
-def arrangement(cm, f, num_sms):
-    """-> dict(split, C, n_pre, n_gather): the planner's choice for the step."""
-    if not f["prefix"]:
-        return dict(split=False, C=None, n_pre=0, n_gather=gather_ctas(f["suffix_tokens"], num_sms))
-    c_seq = sequential_tiles(cm, f, num_sms)
-    seq = dict(split=False, C=c_seq, n_pre=n_items(f, c_seq), n_gather=gather_ctas(f["suffix_tokens"], num_sms))
-    if f["suffix_tokens"] == 0:
-        return seq
-    best, best_c = None, None
-    for C in range(max(_tiles(f)[1]), 0, -1):
-        items = n_items(f, C)
-        if items > num_sms:
-            break
-        t = split_levels(cm, f, C, items, num_sms)
-        if prefix_share(cm, C, t) < MIN_PREFIX_SHARE:
-            continue
-        if best is None or t < best - 1e-9:
-            best, best_c = t, C
-    if best is None or not best < sequential_levels(cm, f, c_seq, num_sms):
-        return seq
-    n_pre = n_items(f, best_c)
-    while best_c > 1 and n_items(f, best_c - 1) == n_pre:
-        best_c -= 1
-    return dict(split=True, C=best_c, n_pre=n_pre, n_gather=num_sms)
-
-
-def predict(cm, f, num_sms=152):
+def predict(cm, f, plan, num_sms=152):
+    """(T_flat, T_cascade) for the arrangement a plan reports: plan = dict(split, C, n_pre, kind)."""
     t_flat = cm["c_flat_us"] + f["bytes_flat"] / (cm["bw_flat_gbs"] * 1e3)
-    a = arrangement(cm, f, num_sms)
-    if a["split"]:
-        t_levels = split_levels(cm, f, a["C"], a["n_pre"], num_sms)
+    if plan["split"]:
+        t_levels = split_levels(cm, f, plan["C"], plan["n_pre"], num_sms, plan["kind"])
     else:
-        t_levels = sequential_levels(cm, f, a["C"], num_sms)
+        t_levels = sequential_levels(cm, f, plan["C"], plan["n_pre"], num_sms, plan["kind"])
     t_cas = cm["c_cascade_us"] + t_levels + cm["c_merge_us"] * f["B"] * f["Hq"]
     return t_flat, t_cas
 
 
-def choose(cm, f, num_sms=152):
-    t_flat, t_cas = predict(cm, f, num_sms)
-    return ("dense" if t_flat < t_cas else "cascade"), t_flat, t_cas
+def choose(t_flat, t_cas):
+    """The backend the rule picks from the two predictions (flat only when strictly faster)."""
+    return "dense" if t_flat < t_cas else "cascade"
 
 
 def aot_splits(budgets, n_cta):

@@ -52,13 +52,15 @@ class gk_plan_summary(ctypes.Structure):
     _fields_ = [("num_requests", c_i32), ("num_groups", c_i32), ("max_m_eff", c_i32), ("prefix_ctas", c_i32),
                 ("suffix_ctas", c_i32), ("dense_ctas", c_i32), ("num_partials", c_i32), ("dense_merge", c_i32),
                 ("prefix_bytes", c_i64), ("prefix_flops", c_i64), ("suffix_bytes", c_i64), ("dense_bytes", c_i64),
-                ("cascade_split", c_i32), ("prefix_tiles_per_item", c_i32)]
+                ("cascade_split", c_i32), ("prefix_tiles_per_item", c_i32), ("prefix_kernel", c_i32),
+                ("prefix_rows_per_item", c_i32)]
 
 
 class gk_cost_model(ctypes.Structure):
     _fields_ = [("c_flat_us", c_dbl), ("bw_flat_gbs", c_dbl), ("c_cascade_us", c_dbl), ("bw_prefix_gbs", c_dbl),
                 ("bw_suffix_gbs", c_dbl), ("c_merge_us", c_dbl), ("prefix_tile_us", c_dbl), ("prefix_item_us", c_dbl),
-                ("gather_sm_gbs", c_dbl), ("c_gather_us", c_dbl), ("prefix_tile_split_us", c_dbl)]
+                ("gather_sm_gbs", c_dbl), ("c_gather_us", c_dbl), ("prefix_tile_split_us", c_dbl),
+                ("warp_tile_us", c_dbl), ("warp_item_us", c_dbl), ("warp_tile_split_us", c_dbl)]
 
 
 P = ctypes.POINTER
@@ -104,6 +106,7 @@ _SIGS = {
     "gk_cost_model_load": (c_i32, [c_vp, ctypes.c_char_p]),
     "gk_pool_set_cascade_mode": (c_i32, [c_vp, c_i32, c_i32]),
     "gk_pool_set_gather_partition": (c_i32, [c_vp, c_i32]),
+    "gk_pool_set_prefix_kernel": (c_i32, [c_vp, c_i32]),
     "gk_device_error": (c_i32, [c_vp, c_vp, P(c_i32)]),
 }
 
@@ -424,7 +427,8 @@ def gk_cost_model_get(pool):
 
 
 COST_MODEL_KEYS = ("c_flat_us", "bw_flat_gbs", "c_cascade_us", "bw_prefix_gbs", "bw_suffix_gbs", "c_merge_us",
-                   "prefix_tile_us", "prefix_item_us", "gather_sm_gbs", "c_gather_us", "prefix_tile_split_us")
+                   "prefix_tile_us", "prefix_item_us", "gather_sm_gbs", "c_gather_us", "prefix_tile_split_us",
+                   "warp_tile_us", "warp_item_us", "warp_tile_split_us")
 
 
 def gk_cost_model_set(pool, cm: dict):
@@ -446,6 +450,13 @@ GK_PARTITION_STREAM, GK_PARTITION_PER_REQUEST = 0, 1
 
 def gk_pool_set_gather_partition(pool, partition):
     _check(lib().gk_pool_set_gather_partition(pool, int(partition)), pool)
+
+
+GK_PREFIX_AUTO, GK_PREFIX_TENSOR, GK_PREFIX_WARP = 0, 1, 2
+
+
+def gk_pool_set_prefix_kernel(pool, kernel):
+    _check(lib().gk_pool_set_prefix_kernel(pool, int(kernel)), pool)
 
 
 def gk_cost_model_load(pool, json_text: str):

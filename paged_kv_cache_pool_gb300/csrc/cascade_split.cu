@@ -14,6 +14,7 @@
 // the merge (GraniKV Eq. 1) follows as its own launch.
 #include "gather_body.cuh"
 #include "prefix_body.cuh"
+#include "prefix_warp_body.cuh"
 
 namespace gk {
 namespace {
@@ -32,15 +33,22 @@ static_assert(1024 + kSplitCtlBytes <= gather::kSoleCtaReserve, "control area ex
 template <int D>
 size_t split_data_bytes(int hkv) {
   const size_t g = gather::gather_data_bytes(hkv, D, gather::single_cta_stages(hkv, D));
+  static_assert(prefix_warp::Layout<D>::kData <= prefix::Layout<D>::kData, "warp items fit the prefix layout");
   return g > prefix::Layout<D>::kData ? g : prefix::Layout<D>::kData;
 }
 
 // the block serves both roles: the prefix body's warps and the gather's
 constexpr int kSplitThreads = prefix::kThreads > gather::kGatherThreads ? prefix::kThreads : gather::kGatherThreads;
-static_assert(32 * kMaxKvHeads <= kSplitThreads, "a gather CTA needs a warp per KV head");
+static_assert(32 * kMaxKvHeads <= kSplitThreads && 32 * kMaxKvHeads <= prefix_warp::kThreads,
+              "a gather CTA needs a warp per KV head");
 
-template <int D, int G>
-__global__ void __launch_bounds__(kSplitThreads, 1) cascade_split_kernel(const SplitParams f) {
+// WARP: the prefix items are warp-MMA items (no tensor memory), else tensor-core
+// items; two instantiations, so that neither path's registers constrain the other
+// (warp items and the gather need 256 threads, which leaves each thread up to
+// 255 registers; tensor-core items need 320)
+template <int D, int G, bool WARP>
+__global__ void __launch_bounds__(WARP ? prefix_warp::kThreads : kSplitThreads, 1)
+    cascade_split_kernel(const SplitParams f) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -49,7 +57,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1) cascade_split_kernel(const S
   const int b = blockIdx.x;
 
   griddep_launch_dependents();
-  if (b < f.n_pre) {
+  if (WARP && b < f.n_pre) {
+    if (threadIdx.x == 0) *reinterpret_cast<volatile int*>(ctl_ptr + prefix::kCtlFlag) = 0;
+    __syncthreads();
+    // the item waits for the kernel before this one itself, after its table reads
+    if (!prefix_warp::warp_item<D>(f.pp, f.pp.items[b], base, ctl, ctl_ptr)) return;  // same on every thread
+  } else if (!WARP && b < f.n_pre) {
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl_ptr + prefix::kCtlTmemSlot);
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) *reinterpret_cast<volatile int*>(ctl_ptr + prefix::kCtlFlag) = 0;
@@ -75,12 +88,12 @@ __global__ void __launch_bounds__(kSplitThreads, 1) cascade_split_kernel(const S
 }
 
 template <int D, int G>
-int launch_split_t(const SplitParams& fp, int ctas, cudaStream_t st) {
+int launch_split_t(const SplitParams& fp, int ctas, cudaStream_t st, bool warp_items) {
   const size_t smem = 1024 + fp.data_bytes + kSplitCtlBytes;
-  auto kern = cascade_split_kernel<D, G>;
+  auto kern = warp_items ? cascade_split_kernel<D, G, true> : cascade_split_kernel<D, G, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  return (int)launch_pdl(kern, dim3(ctas), dim3(kSplitThreads), smem, st, fp);
+  return (int)launch_pdl(kern, dim3(ctas), dim3(warp_items ? prefix_warp::kThreads : kSplitThreads), smem, st, fp);
 }
 
 }  // namespace
@@ -91,6 +104,7 @@ int launch_cascade_split(const LaunchCommon& lc, void* stream, int32_t layer, co
   fill_prefix_params(lc, layer, b, pl, &fp.pp);
   if (int e = fill_gather_params(lc, layer, b, pl, false, &fp.gp)) return e;
   fp.n_pre = (int32_t)pl->prefix_items.size();
+  const bool wi = pl->prefix_kind == 1;
   fp.n_gather = pl->summary.suffix_ctas;
   const int ctas = std::max(fp.n_pre, fp.n_gather);
   if (ctas == 0) return 0;
@@ -99,18 +113,18 @@ int launch_cascade_split(const LaunchCommon& lc, void* stream, int32_t layer, co
   if (c.head_dim == 128) {
     fp.data_bytes = (uint32_t)split_data_bytes<128>(c.num_kv_heads);
     switch (g) {
-      case 1: return launch_split_t<128, 1>(fp, ctas, st);
-      case 2: return launch_split_t<128, 2>(fp, ctas, st);
-      case 4: return launch_split_t<128, 4>(fp, ctas, st);
-      case 5: return launch_split_t<128, 5>(fp, ctas, st);
-      case 8: return launch_split_t<128, 8>(fp, ctas, st);
+      case 1: return launch_split_t<128, 1>(fp, ctas, st, wi);
+      case 2: return launch_split_t<128, 2>(fp, ctas, st, wi);
+      case 4: return launch_split_t<128, 4>(fp, ctas, st, wi);
+      case 5: return launch_split_t<128, 5>(fp, ctas, st, wi);
+      case 8: return launch_split_t<128, 8>(fp, ctas, st, wi);
     }
   } else if (c.head_dim == 64) {
     fp.data_bytes = (uint32_t)split_data_bytes<64>(c.num_kv_heads);
     switch (g) {
-      case 1: return launch_split_t<64, 1>(fp, ctas, st);
-      case 2: return launch_split_t<64, 2>(fp, ctas, st);
-      case 4: return launch_split_t<64, 4>(fp, ctas, st);
+      case 1: return launch_split_t<64, 1>(fp, ctas, st, wi);
+      case 2: return launch_split_t<64, 2>(fp, ctas, st, wi);
+      case 4: return launch_split_t<64, 4>(fp, ctas, st, wi);
     }
   }
   return (int)cudaErrorInvalidValue;

@@ -78,6 +78,7 @@ uint64_t block_hash(uint64_t parent, const int32_t* tokens, int32_t page_size);
 constexpr int kPrefixTileM = 128;    // stacked query rows per tensor-core tile
 constexpr int kPrefixRowsPerCta = 2 * kPrefixTileM;  // two Q tiles per prefix CTA
 constexpr int kPrefixTileN = 128;    // prefix keys per tile
+constexpr int kPrefixWarpRows = 128; // stacked query rows per warp-MMA prefix item (8 warps x 16)
 constexpr int kGatherT = 16;         // tokens per gather pipeline stage
 constexpr int kMaxKvHeads = 8;
 
@@ -97,6 +98,7 @@ struct Pool {
   gk_cascade_mode cascade_mode = GK_CASCADE_AUTO;
   int32_t cascade_tiles = 0;         // GK_CASCADE_SPLIT: tiles per item (0 = best predicted)
   gk_gather_partition gather_partition = GK_PARTITION_STREAM;  // stand-alone gathers' work split
+  gk_prefix_kernel prefix_kernel = GK_PREFIX_AUTO;             // which prefix item the plans use
   std::string last_error;
   DeviceInfo dev;
   int32_t* d_error = nullptr;        // device error word (allocated on first device use)
@@ -171,6 +173,7 @@ struct Plan {
   size_t part_entries = 0;
   bool uploaded = false;
   bool split = false;                    // cascade arrangement: prefix items and suffix gather side by side
+  int32_t prefix_kind = 0;               // 0: tensor-core items (256 rows), 1: warp-MMA items (128 rows)
 };
 
 // host half of gk_plan_build: grouping, work lists and partial-state layout (no device work)
@@ -200,8 +203,11 @@ int launch_gather(const LaunchCommon& lc, void* stream, int32_t layer, const gk_
                   const Plan* plan, bool dense);
 int launch_merge(const LaunchCommon& lc, void* stream, const gk_batch* b, const Plan* plan,
                  bool dense);
+// the plan's prefix items as one launch (tensor-core or warp-MMA items, as planned)
 int launch_prefix(const LaunchCommon& lc, void* stream, int32_t layer, const gk_batch* b,
                   const Plan* plan);
+int launch_prefix_warp(const LaunchCommon& lc, void* stream, int32_t layer, const gk_batch* b,
+                       const Plan* plan);
 // split arrangement: the prefix items and the suffix gather of one layer in one
 // launch, on disjoint SMs (the merge follows as its own launch)
 int launch_cascade_split(const LaunchCommon& lc, void* stream, int32_t layer, const gk_batch* b,

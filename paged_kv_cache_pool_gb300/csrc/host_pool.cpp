@@ -259,6 +259,10 @@ gk_status gk_pool_create(const gk_pool_config* cfg, gk_pool** out) {
   cm.gather_sm_gbs = 44.0;
   cm.c_gather_us = 10.0;
   cm.prefix_tile_split_us = 2.1;
+  // warp-MMA prefix items: priced high until a measured model is loaded
+  cm.warp_tile_us = 6.0;
+  cm.warp_item_us = 6.0;
+  cm.warp_tile_split_us = 7.0;
   *out = p;
   return GK_OK;
 }

@@ -192,45 +192,34 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     rq.group = grp;
   }
 
-  // ---- prefix contraction work: choose keys per split to balance the SMs --------
+  // ---- prefix contraction work: kind of item, arrangement, keys per item ---------
   const int num_sms = p->dev.num_sms;
   const int32_t G = (int32_t)members.size();
-  std::vector<int32_t> mtiles((size_t)G), ntiles((size_t)G);
+  std::vector<int32_t> ntiles((size_t)G);
   int32_t max_ntiles = 1;
   for (int32_t gi = 0; gi < G; ++gi) {
-    int32_t m = (int32_t)members[(size_t)gi].size() * g;
     int32_t lp = pl->reqs[(size_t)members[(size_t)gi][0]].lp;
-    mtiles[(size_t)gi] = (m + kPrefixRowsPerCta - 1) / kPrefixRowsPerCta;
     ntiles[(size_t)gi] = (lp + kPrefixTileN - 1) / kPrefixTileN;
     max_ntiles = std::max(max_ntiles, ntiles[(size_t)gi]);
   }
+  const gk_cost_model& cm = p->cost;
+  const int64_t kv_tok = 2LL * Hkv * d * 2;
+  int64_t suffix_tokens = 0;
+  for (int32_t r = 0; r < B; ++r) suffix_tokens += pl->reqs[(size_t)r].slen;
+  const double S = (double)suffix_tokens * (double)kv_tok;
+  double prefix_bytes = 0.0;
+  for (int32_t gi = 0; gi < G; ++gi)
+    prefix_bytes += (double)pl->reqs[(size_t)members[(size_t)gi][0]].lp * (double)kv_tok;
+
+  // One kind of prefix item: `rows` stacked rows per item, its cost-model terms.
   // Sequential arrangement: every SM takes prefix items (waves of them), then
   // every SM gathers.  Keys per split: the fewest that minimise the waves times
-  // the cost model's time of one item alone (C * prefix_tile + prefix_item).
-  const gk_cost_model& cm = p->cost;
-  auto n_items = [&](int32_t C) {
-    int64_t units = 0;
-    for (int32_t gi = 0; gi < G; ++gi)
-      units += (int64_t)mtiles[(size_t)gi] * Hkv * ((ntiles[(size_t)gi] + C - 1) / C);
-    return units;
-  };
-  int32_t c_seq = max_ntiles;
-  {
-    double best_cost = 1e300;
-    for (int32_t C = 1; G > 0 && C <= max_ntiles; ++C) {
-      const double cost =
-          (double)((n_items(C) + num_sms - 1) / num_sms) * (C * cm.prefix_tile_us + cm.prefix_item_us);
-      if (cost < best_cost - 1e-9) {
-        best_cost = cost;
-        c_seq = C;
-      }
-    }
-  }
+  // the time of one item alone (C * tile + item).
   // Split arrangement: one launch in which CTA b < n_pre first runs one prefix
   // item of C key tiles, and every CTA (one per SM) gathers a slot of the
   // suffix, a prefix CTA's slot cut to the time its item leaves.  Predicted
-  //   item(C)   = C * prefix_tile_split_us + prefix_item_us
-  //   T_split   = max(item(C), (S / gather_sm + n_pre * item(C)) / SMs,
+  //   item'(C)  = C * tile_split + item
+  //   T_split   = max(item'(C), (S / gather_sm + n_pre * item'(C)) / SMs,
   //                   (S + prefix_bytes) / bw_suffix)
   // (the middle term spreads the gather's SM-time and the items over all SMs;
   // the last is HBM), against the sequential arrangement's W waves of c_seq-tile
@@ -239,62 +228,108 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   // The split is taken when some C is predicted faster than the sequential
   // arrangement; among equal predictions the fewest items (fewest partials)
   // win, and the chosen item count is then spread evenly over the key tiles.
-  const int64_t kv_tok = 2LL * Hkv * d * 2;
-  int64_t suffix_tokens = 0;
-  for (int32_t r = 0; r < B; ++r) suffix_tokens += pl->reqs[(size_t)r].slen;
-  const double S = (double)suffix_tokens * (double)kv_tok;
-  double prefix_bytes = 0.0;
-  for (int32_t gi = 0; gi < G; ++gi)
-    prefix_bytes += (double)pl->reqs[(size_t)members[(size_t)gi][0]].lp * (double)kv_tok;
-  double t_seq = S / (cm.bw_suffix_gbs * 1e3) + cm.c_gather_us;
-  if (G > 0) {
-    const double waves = (double)((n_items(c_seq) + num_sms - 1) / num_sms);
-    t_seq += std::max(prefix_bytes / (cm.bw_prefix_gbs * 1e3),
-                      waves * (std::min(c_seq, max_ntiles) * cm.prefix_tile_us + cm.prefix_item_us));
-  }
-  // an item of a split plan runs beside a gather that keeps HBM busy: its tiles take longer
-  auto item_us = [&](int32_t C) { return C * cm.prefix_tile_split_us + cm.prefix_item_us; };
-  auto split_us = [&](int32_t C) {
-    const double it = item_us(C);
-    const double bal = (S / (cm.gather_sm_gbs * 1e3) + (double)n_items(C) * it) / num_sms;
-    return std::max(std::max(it, bal), (S + prefix_bytes) / (cm.bw_suffix_gbs * 1e3));
+  struct KindPlan {
+    int32_t rows = 0;
+    std::vector<int32_t> mtiles;
+    double tile = 0, tile_split = 0, item = 0;
+    bool split = false;
+    int32_t c = 0;              // key tiles per item
+    double t_levels = 0;        // predicted levels time of the chosen arrangement
+    double prefix_cta_share = 1.0;
   };
-  int32_t c_split = 0;
-  double t_split = 1e300;
-  const bool can_split = G > 0 && suffix_tokens > 0 && p->cascade_mode != GK_CASCADE_SEQUENTIAL;
-  if (can_split && p->cascade_mode == GK_CASCADE_SPLIT && p->cascade_tiles > 0) {
-    const int32_t C = std::min(p->cascade_tiles, max_ntiles);
-    if (n_items(C) <= num_sms) c_split = C;
-  } else {
-    // the prefix CTAs' gather share for items of C tiles in a launch of T us
-    auto share_of = [&](int32_t C, double T) { return std::max(0.0, T - item_us(C) - cm.c_gather_us) / T; };
-    for (int pass = 0; pass < 2 && c_split == 0; ++pass) {
-      // pass 0: only splits that leave the prefix CTAs a gather share; pass 1 (a
-      // forced split with none such): the best prediction
-      if (pass == 1 && p->cascade_mode != GK_CASCADE_SPLIT) break;
-      for (int32_t C = max_ntiles; can_split && C >= 1; --C) {
-        if (n_items(C) > num_sms) break;  // items only grow as C shrinks
-        const double t = split_us(C);
-        if (pass == 0 && share_of(C, t) < kMinPrefixShare) continue;
-        if (t < t_split - 1e-9) {
-          t_split = t;
-          c_split = C;
+  auto plan_kind = [&](int32_t rows, double tile, double tile_split, double item) {
+    KindPlan k;
+    k.rows = rows;
+    k.tile = tile;
+    k.tile_split = tile_split;
+    k.item = item;
+    k.mtiles.resize((size_t)G);
+    for (int32_t gi = 0; gi < G; ++gi)
+      k.mtiles[(size_t)gi] = ((int32_t)members[(size_t)gi].size() * g + rows - 1) / rows;
+    auto n_items = [&](int32_t C) {
+      int64_t units = 0;
+      for (int32_t gi = 0; gi < G; ++gi)
+        units += (int64_t)k.mtiles[(size_t)gi] * Hkv * ((ntiles[(size_t)gi] + C - 1) / C);
+      return units;
+    };
+    int32_t c_seq = max_ntiles;
+    {
+      double best_cost = 1e300;
+      for (int32_t C = 1; G > 0 && C <= max_ntiles; ++C) {
+        const double cost = (double)((n_items(C) + num_sms - 1) / num_sms) * (C * tile + item);
+        if (cost < best_cost - 1e-9) {
+          best_cost = cost;
+          c_seq = C;
         }
       }
     }
+    double t_seq = S / (cm.bw_suffix_gbs * 1e3) + cm.c_gather_us;
+    if (G > 0) {
+      const double waves = (double)((n_items(c_seq) + num_sms - 1) / num_sms);
+      t_seq += std::max(prefix_bytes / (cm.bw_prefix_gbs * 1e3), waves * (std::min(c_seq, max_ntiles) * tile + item));
+    }
+    auto item_us = [&](int32_t C) { return C * tile_split + item; };
+    auto split_us = [&](int32_t C) {
+      const double it = item_us(C);
+      const double bal = (S / (cm.gather_sm_gbs * 1e3) + (double)n_items(C) * it) / num_sms;
+      return std::max(std::max(it, bal), (S + prefix_bytes) / (cm.bw_suffix_gbs * 1e3));
+    };
+    int32_t c_split = 0;
+    double t_split = 1e300;
+    const bool can_split = G > 0 && suffix_tokens > 0 && p->cascade_mode != GK_CASCADE_SEQUENTIAL;
+    if (can_split && p->cascade_mode == GK_CASCADE_SPLIT && p->cascade_tiles > 0) {
+      const int32_t C = std::min(p->cascade_tiles, max_ntiles);
+      if (n_items(C) <= num_sms) {
+        c_split = C;
+        t_split = split_us(C);
+      }
+    } else {
+      // the prefix CTAs' gather share for items of C tiles in a launch of T us
+      auto share_of = [&](int32_t C, double T) { return std::max(0.0, T - item_us(C) - cm.c_gather_us) / T; };
+      for (int pass = 0; pass < 2 && c_split == 0; ++pass) {
+        // pass 0: only splits that leave the prefix CTAs a gather share; pass 1 (a
+        // forced split with none such): the best prediction
+        if (pass == 1 && p->cascade_mode != GK_CASCADE_SPLIT) break;
+        for (int32_t C = max_ntiles; can_split && C >= 1; --C) {
+          if (n_items(C) > num_sms) break;  // items only grow as C shrinks
+          const double t = split_us(C);
+          if (pass == 0 && share_of(C, t) < kMinPrefixShare) continue;
+          if (t < t_split - 1e-9) {
+            t_split = t;
+            c_split = C;
+          }
+        }
+      }
+    }
+    // balance the chosen split: the fewest tiles per item that gives as many items
+    while (c_split > 1 && n_items(c_split - 1) == n_items(c_split)) --c_split;
+    k.split = c_split > 0 && (p->cascade_mode == GK_CASCADE_SPLIT || t_split < t_seq);
+    k.c = k.split ? c_split : c_seq;
+    k.t_levels = k.split ? split_us(c_split) : t_seq;
+    // gather weight of a prefix CTA relative to a gather-only CTA: the time its
+    // item leaves, less the ramp of starting a gather (c_gather_us); a sliver of
+    // suffix would cost more in ramp and partial states than it saves
+    if (k.split) {
+      const double T = split_us(c_split);
+      k.prefix_cta_share = std::max(0.0, T - item_us(c_split) - cm.c_gather_us) / T;
+    }
+    return k;
+  };
+  KindPlan kp;
+  if (p->prefix_kernel == GK_PREFIX_WARP) {
+    kp = plan_kind(kPrefixWarpRows, cm.warp_tile_us, cm.warp_tile_split_us, cm.warp_item_us);
+  } else {
+    kp = plan_kind(kPrefixRowsPerCta, cm.prefix_tile_us, cm.prefix_tile_split_us, cm.prefix_item_us);
+    if (p->prefix_kernel == GK_PREFIX_AUTO && G > 0) {
+      KindPlan kw = plan_kind(kPrefixWarpRows, cm.warp_tile_us, cm.warp_tile_split_us, cm.warp_item_us);
+      if (kw.t_levels < kp.t_levels - 1e-9) kp = std::move(kw);
+    }
   }
-  // balance the chosen split: the fewest tiles per item that gives as many items
-  while (c_split > 1 && n_items(c_split - 1) == n_items(c_split)) --c_split;
-  pl->split = c_split > 0 && (p->cascade_mode == GK_CASCADE_SPLIT || t_split < t_seq);
-  const int32_t best_c = pl->split ? c_split : c_seq;
-  // gather weight of a prefix CTA relative to a gather-only CTA: the time its
-  // item leaves, less the ramp of starting a gather (c_gather_us); a sliver of
-  // suffix would cost more in ramp and partial states than it saves
-  double prefix_cta_share = 1.0;
-  if (pl->split) {
-    const double T = split_us(c_split);
-    prefix_cta_share = std::max(0.0, T - item_us(c_split) - cm.c_gather_us) / T;
-  }
+  pl->prefix_kind = kp.rows == kPrefixWarpRows ? 1 : 0;
+  pl->split = kp.split;
+  const int32_t best_c = kp.c;
+  const std::vector<int32_t>& mtiles = kp.mtiles;
+  const double prefix_cta_share = kp.prefix_cta_share;
   int32_t max_m = 0;
   int64_t pre_bytes = 0, pre_flops = 0;
   for (int32_t gi = 0; gi < G; ++gi) {
@@ -415,6 +450,8 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   sm.cascade_split = pl->split ? 1 : 0;
   sm.prefix_tiles_per_item = 0;
   for (int32_t gi = 0; gi < G; ++gi) sm.prefix_tiles_per_item = std::max(sm.prefix_tiles_per_item, std::min(best_c, ntiles[(size_t)gi]));
+  sm.prefix_kernel = pl->prefix_kind ? GK_PREFIX_WARP : GK_PREFIX_TENSOR;
+  sm.prefix_rows_per_item = kp.rows;
   return GK_OK;
 }
 
@@ -524,6 +561,7 @@ static bool valid_cost_model(const gk_cost_model& cm) {
   if (!(cm.bw_flat_gbs > 0 && cm.bw_prefix_gbs > 0 && cm.bw_suffix_gbs > 0)) return false;
   if (!(cm.prefix_tile_us > 0 && cm.prefix_tile_split_us > 0 && cm.prefix_item_us >= 0 && cm.gather_sm_gbs > 0))
     return false;
+  if (!(cm.warp_tile_us > 0 && cm.warp_tile_split_us > 0 && cm.warp_item_us >= 0)) return false;
   if (!(cm.c_flat_us >= 0 && cm.c_cascade_us >= 0 && cm.c_merge_us >= 0 && cm.c_gather_us >= 0)) return false;
   return true;
 }
@@ -654,13 +692,17 @@ gk_status gk_dispatch(const gk_pool* pool, const gk_plan* plan, gk_backend* choi
   double t_levels = 0.0;
   const gk_plan_summary& sm = pl.summary;
   const int num_sms = pool->impl.dev.num_sms;
+  const bool warp = pl.prefix_kind == 1;
+  const double tile = warp ? cm.warp_tile_us : cm.prefix_tile_us;
+  const double tile_split = warp ? cm.warp_tile_split_us : cm.prefix_tile_split_us;
+  const double item_fixed = warp ? cm.warp_item_us : cm.prefix_item_us;
   if (pl.split) {
-    const double item = sm.prefix_tiles_per_item * cm.prefix_tile_split_us + cm.prefix_item_us;
+    const double item = sm.prefix_tiles_per_item * tile_split + item_fixed;
     const double bal = ((double)sm.suffix_bytes / (cm.gather_sm_gbs * 1e3) + sm.prefix_ctas * item) / num_sms;
     t_levels = std::max(std::max(item, bal), (double)(sm.suffix_bytes + sm.prefix_bytes) / (cm.bw_suffix_gbs * 1e3));
   } else {
     if (sm.prefix_ctas > 0) {
-      const double item = sm.prefix_tiles_per_item * cm.prefix_tile_us + cm.prefix_item_us;
+      const double item = sm.prefix_tiles_per_item * tile + item_fixed;
       const double waves = (double)((sm.prefix_ctas + num_sms - 1) / num_sms);
       t_levels = std::max((double)sm.prefix_bytes / (cm.bw_prefix_gbs * 1e3), waves * item);
     }
@@ -688,6 +730,14 @@ gk_status gk_pool_set_gather_partition(gk_pool* pool, gk_gather_partition partit
   if (partition != GK_PARTITION_STREAM && partition != GK_PARTITION_PER_REQUEST)
     return gk::fail(&pool->impl, GK_ERR_INVALID, "unknown gather partition");
   pool->impl.gather_partition = partition;
+  return GK_OK;
+}
+
+gk_status gk_pool_set_prefix_kernel(gk_pool* pool, gk_prefix_kernel kernel) {
+  if (!pool) return GK_ERR_INVALID;
+  if (kernel != GK_PREFIX_AUTO && kernel != GK_PREFIX_TENSOR && kernel != GK_PREFIX_WARP)
+    return gk::fail(&pool->impl, GK_ERR_INVALID, "unknown prefix kernel");
+  pool->impl.prefix_kernel = kernel;
   return GK_OK;
 }
 
@@ -720,7 +770,8 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
     if (!rd.eat(':')) return bad("expected ':'");
     static const char* kNumeric[] = {"c_flat_us",      "bw_flat_gbs",    "c_cascade_us",  "bw_prefix_gbs",
                                      "bw_suffix_gbs",  "c_merge_us",     "prefix_tile_us", "prefix_item_us",
-                                     "gather_sm_gbs",  "c_gather_us",    "prefix_tile_split_us"};
+                                     "gather_sm_gbs",  "c_gather_us",    "prefix_tile_split_us",
+                                     "warp_tile_us",   "warp_item_us",   "warp_tile_split_us"};
     bool known = false;
     for (const char* k : kNumeric) known = known || key == k;
     if (!known) {
@@ -740,6 +791,9 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
     else if (key == "gather_sm_gbs") cm.gather_sm_gbs = v;
     else if (key == "c_gather_us") cm.c_gather_us = v;
     else if (key == "prefix_tile_split_us") cm.prefix_tile_split_us = v;
+    else if (key == "warp_tile_us") cm.warp_tile_us = v;
+    else if (key == "warp_item_us") cm.warp_item_us = v;
+    else if (key == "warp_tile_split_us") cm.warp_tile_split_us = v;
   }
   return gk_cost_model_set(pool, &cm);
 }

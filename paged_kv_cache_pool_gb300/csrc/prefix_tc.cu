@@ -136,6 +136,7 @@ int fill_prefix_params(const LaunchCommon& lc, int32_t layer, const gk_batch* b,
 }
 
 int launch_prefix(const LaunchCommon& lc, void* stream, int32_t layer, const gk_batch* b, const Plan* pl) {
+  if (pl->prefix_kind == 1) return launch_prefix_warp(lc, stream, layer, b, pl);
   const gk_pool_config& c = *lc.cfg;
   PrefixParams pp;
   fill_prefix_params(lc, layer, b, pl, &pp);

@@ -6,11 +6,14 @@ Two parts:
 
   measure  On one layer of a synthetic pool (random bf16 data), for every cell
            of an (Lp, B) grid with one shared prefix and suffixes drawn from
-           U{16..512} (the pages' 16..512-token user turns), time the flat
-           (dense) backend and the cascade with CUDA events, L2 flushed before
-           every launch, and record the dispatcher's choice and predictions.
-           Per cell: M_eff = B * g (GraniKV Eq. 2), the faster backend, and the
-           regret of the dispatcher's pick (its time over the faster one's, - 1).
+           U{16..512} (the pages' 16..512-token user turns), time the three
+           choices with CUDA events, L2 flushed before every launch: the flat
+           (dense) backend, the cascade over tensor-core prefix items and the
+           cascade over warp-MMA prefix items (GraniKV Section 3.5's two prefix
+           kernels), each as the planner arranges it, and record the predictions
+           and the pick of the default plan (GK_PREFIX_AUTO, then gk_dispatch).
+           Per cell: M_eff = B * g (GraniKV Eq. 2), the fastest choice, and the
+           regret of the pick (its time over the fastest one's, - 1).
 
   trace    Host only.  Per (Lp, B) cell, 200 decode steps whose realised batch
            is B plus a Poisson(B / 8) burst of requests whose prefill overlaps
@@ -91,22 +94,34 @@ def measure(lps=LPS, bs=BS, Hq=32, Hkv=8, d=128, reps=5, seed=7, cost_model=COST
             out = torch.empty((B, Hq, d), device=eng.device)
             lse = torch.empty((B, Hq), device=eng.device)
             batch.set_device(d_q=q, d_out=out, d_lse=lse)
+            t, pred, arr = {}, {}, {}
+            for kind, kernel in (("tensor", gk.GK_PREFIX_TENSOR), ("warp", gk.GK_PREFIX_WARP)):
+                gk.gk_pool_set_prefix_kernel(pool, kernel)
+                plan = gk.gk_plan_build(pool, batch)
+                info = gk.gk_plan_info(plan)
+                _, p_dense, pred[kind] = gk.gk_dispatch(pool, plan)
+                arr[kind] = dict(split=info["cascade_split"], C=info["prefix_tiles_per_item"],
+                                 n_pre=info["prefix_ctas"], suffix_ctas=info["suffix_ctas"],
+                                 partials=info["num_partials"])
+                t[kind] = timed(lambda: gk.gk_decode_cascade(pool, None, 0, batch, plan))
+                if kind == "tensor":
+                    t["dense"] = timed(lambda: gk.gk_decode_dense(pool, None, 0, batch, plan))
+                gk.gk_plan_destroy(plan)
+            pred["dense"] = p_dense
+            gk.gk_pool_set_prefix_kernel(pool, gk.GK_PREFIX_AUTO)
             plan = gk.gk_plan_build(pool, batch)
-            info = gk.gk_plan_info(plan)
-            choice, p_dense, p_cas = gk.gk_dispatch(pool, plan)
-            t_dense = timed(lambda: gk.gk_decode_dense(pool, None, 0, batch, plan))
-            t_cas = timed(lambda: gk.gk_decode_cascade(pool, None, 0, batch, plan))
+            choice, _, _ = gk.gk_dispatch(pool, plan)
+            auto_kind = "warp" if gk.gk_plan_info(plan)["prefix_kernel"] == gk.GK_PREFIX_WARP else "tensor"
+            gk.gk_plan_destroy(plan)
             if gk.gk_device_error(pool) != gk.GK_OK:
                 raise RuntimeError(f"device error at Lp={lp} B={B}")
-            picked = t_dense if choice == gk.GK_BACKEND_DENSE else t_cas
+            pick = "dense" if choice == gk.GK_BACKEND_DENSE else auto_kind
+            fastest = min(t, key=t.get)
             rows.append(dict(Lp=lp, B=B, M_eff=B * g, suffix_tokens=int(s.sum()),
-                             t_dense_us=t_dense, t_cascade_us=t_cas,
-                             pred_dense_us=p_dense, pred_cascade_us=p_cas,
-                             choice="dense" if choice == gk.GK_BACKEND_DENSE else "cascade",
-                             faster="dense" if t_dense < t_cas else "cascade",
-                             regret=picked / min(t_dense, t_cas) - 1.0,
-                             split=info["cascade_split"], prefix_ctas=info["prefix_ctas"]))
-            gk.gk_plan_destroy(plan)
+                             t_dense_us=t["dense"], t_tensor_us=t["tensor"], t_warp_us=t["warp"],
+                             pred_dense_us=pred["dense"], pred_tensor_us=pred["tensor"], pred_warp_us=pred["warp"],
+                             plan_tensor=arr["tensor"], plan_warp=arr["warp"],
+                             pick=pick, fastest=fastest, regret=t[pick] / t[fastest] - 1.0))
             for sq in seqs:
                 eng.seq_release(sq)
         gk.gk_prefix_release(pool, base)
@@ -115,11 +130,11 @@ def measure(lps=LPS, bs=BS, Hq=32, Hkv=8, d=128, reps=5, seed=7, cost_model=COST
 
 
 def crossover(rows):
-    """Per Lp: the smallest M_eff of the grid at which dense is measured faster (None: never)."""
+    """Per Lp: the M_eff values of the grid at which each choice is measured fastest."""
     out = {}
     for lp in sorted({r["Lp"] for r in rows}):
-        wins = [r["M_eff"] for r in rows if r["Lp"] == lp and r["faster"] == "dense"]
-        out[lp] = min(wins) if wins else None
+        out[lp] = {k: [r["M_eff"] for r in rows if r["Lp"] == lp and r["fastest"] == k]
+                   for k in ("dense", "tensor", "warp")}
     return out
 
 
@@ -160,7 +175,8 @@ def main():
         rows = measure()
         for r in rows:
             print(json.dumps(r))
-        print(json.dumps({"crossover_M_eff": crossover(rows)}))
+        print(json.dumps({"fastest_by_M_eff": crossover(rows),
+                          "max_regret": max(r["regret"] for r in rows)}))
         if a.out:
             with open(a.out, "w") as f:
                 json.dump(rows, f, indent=1)

@@ -231,15 +231,22 @@ def test_plan_summary_against_the_byte_and_flop_model(gk):
         gk.gk_pool_destroy(pool)
 
 
-@pytest.mark.parametrize("case", range(5))
+@pytest.mark.parametrize("case", range(6))
 def test_dispatch_matches_oracle_formula(gk, case):
+    """gk_dispatch's two predictions follow the documented formula (oracle/dispatch.py) for
+    the arrangement and prefix kernel the plan reports, the plan's prefix work covers every
+    (row block, KV head, key split) once, and GK_PREFIX_AUTO takes the kind its own model
+    predicts faster.  Which arrangement the planner searches out is not pinned here (the
+    pages fix no such rule); the GPU tests hold it to measured times."""
     rnd = random.Random(case)
     Hq, Hkv, d = rnd.choice([(32, 8, 128), (40, 8, 128)])
     cm = dict(c_flat_us=rnd.uniform(2, 20), bw_flat_gbs=rnd.uniform(3000, 7000), c_cascade_us=rnd.uniform(5, 40),
               bw_prefix_gbs=rnd.uniform(3000, 7000), bw_suffix_gbs=rnd.uniform(3000, 7000),
               c_merge_us=rnd.uniform(0, 0.002), prefix_tile_us=rnd.uniform(0.5, 3.0),
               prefix_tile_split_us=rnd.uniform(0.5, 4.0),
-              prefix_item_us=rnd.uniform(0, 20), gather_sm_gbs=rnd.uniform(20, 80), c_gather_us=rnd.uniform(0, 20))
+              prefix_item_us=rnd.uniform(0, 20), gather_sm_gbs=rnd.uniform(20, 80), c_gather_us=rnd.uniform(0, 20),
+              warp_tile_us=rnd.uniform(0.3, 4.0), warp_item_us=rnd.uniform(0, 10),
+              warp_tile_split_us=rnd.uniform(0.3, 5.0))
     pool = gk.gk_pool_create(1, Hq, Hkv, d, 200000, 64, 1, 0)
     try:
         gk.gk_cost_model_load(pool, json.dumps(cm))
@@ -248,7 +255,7 @@ def test_dispatch_matches_oracle_formula(gk, case):
             assert got_cm[k] == cm[k]
         n_pref = rnd.randint(0, 3)
         pref = [(gk.gk_prefix_alloc(pool, lp), lp) for lp in [rnd.randint(64, 20000) for _ in range(n_pref)]]
-        B = rnd.randint(1, 300)
+        B = rnd.randint(1, 300) if case % 2 else rnd.randint(1, 12)     # odd cases: small M_eff
         bases, lps, slens, grp = [], [], [], []
         for r in range(B):
             c = rnd.randrange(n_pref + 1) - 1
@@ -256,21 +263,78 @@ def test_dispatch_matches_oracle_formula(gk, case):
             lps.append(pref[c][1] if c >= 0 else 0)
             grp.append(c)
             slens.append(rnd.randint(0, 4000))
-        b, plan = _host_plan(gk, pool, bases, lps, slens)
-        choice, td, tc = gk.gk_dispatch(pool, plan)
         f = odisp.features(lps, slens, grp, Hq, Hkv, d)
-        want, wd, wc = odisp.choose(cm, f)
-        arr = odisp.arrangement(cm, f, 152)
+        pred = {}
+        for kernel, kind in ((gk.GK_PREFIX_TENSOR, "tensor"), (gk.GK_PREFIX_WARP, "warp"), (gk.GK_PREFIX_AUTO, None)):
+            gk.gk_pool_set_prefix_kernel(pool, kernel)
+            b, plan = _host_plan(gk, pool, bases, lps, slens)
+            choice, td, tc = gk.gk_dispatch(pool, plan)
+            s = gk.gk_plan_info(plan)
+            gk.gk_plan_destroy(plan)
+            k = "warp" if s["prefix_kernel"] == gk.GK_PREFIX_WARP else "tensor"
+            if kind:
+                assert k == kind
+            assert s["prefix_rows_per_item"] == odisp.ROWS[k]
+            C = s["prefix_tiles_per_item"]
+            if f["prefix"]:
+                assert C >= 1 and s["prefix_ctas"] == odisp.n_items(f, C, k)
+            else:
+                assert s["prefix_ctas"] == 0 and not s["cascade_split"]
+            if s["cascade_split"]:
+                assert s["prefix_ctas"] <= 152 and s["suffix_ctas"] == 152
+            else:
+                assert s["suffix_ctas"] == odisp.gather_ctas(sum(slens), 152)
+            wd, wc = odisp.predict(cm, f, dict(split=bool(s["cascade_split"]), C=C, n_pre=s["prefix_ctas"], kind=k))
+            assert math.isclose(td, wd, rel_tol=1e-12) and math.isclose(tc, wc, rel_tol=1e-12)
+            assert choice == (gk.GK_BACKEND_DENSE if odisp.choose(wd, wc) == "dense" else gk.GK_BACKEND_CASCADE)
+            pred[kernel] = tc
+        assert pred[gk.GK_PREFIX_AUTO] <= min(pred[gk.GK_PREFIX_TENSOR], pred[gk.GK_PREFIX_WARP]) * (1 + 1e-12)
+        with pytest.raises(gk.GkError):
+            gk.gk_pool_set_prefix_kernel(pool, 3)
+    finally:
+        gk.gk_pool_destroy(pool)
+
+
+def test_planner_search_worked_by_hand(gk):
+    """The planner's documented search (gk.h: gk_pool_set_cascade_mode, gk_dispatch) on
+    cases worked by hand, with warp-MMA items priced out.
+    (1) One group of 64 requests (g = 4 -> one 256-row block per KV head), Lp = 16384 (128
+    key tiles), Hkv = 8, 1000 suffix tokens each; tile 1 us (alone and beside the gather),
+    item 5 us, 50 GB/s per SM, 6000 GB/s over every SM, 4 us for a gather launch, 152 SMs.
+    Split: T(C) = max(C + 5, (S / 50 GB/s + items(C) (C + 5)) / 152, (S + P) / 6000 GB/s)
+    with items(C) = 8 ceil(128 / C); HBM binds at 54.875 us from C = 49 down.  A split C must
+    leave its prefix CTAs a gather share (T - item(C) - 4) / T >= 0.15: the 24-item splits
+    (C = 43..49) leave at most 0.05, so the scan from C = 128 down keeps the first 32-item
+    one (C = 37, share 0.16), balanced to 32 tiles (the fewest giving 32 items).  The
+    sequential alternative (C = 7: 152 items in one wave of 12 us, the prefix bound by its
+    67 MB at 5000 GB/s: 13.4 + 4 + 43.7 = 61.1 us) is slower, so the plan splits.
+    (2) 512 requests (M = 2048: eight row blocks per head), sequential, tile 1.557 us, item
+    8.63 us: one wave of 128 items of 64 tiles (108.3 us) beats three waves of 448 items of
+    19 tiles (114.6 us) and two of 256 items of 32 (117.0 us)."""
+    cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0, bw_suffix_gbs=6000.0,
+              c_merge_us=0.001, prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0, c_gather_us=4.0,
+              prefix_tile_split_us=1.0, warp_tile_us=1e3, warp_item_us=1e3, warp_tile_split_us=1e3)
+    pool = gk.gk_pool_create(1, 32, 8, 128, 16384 + 16, 64, 1, 0)
+    try:
+        gk.gk_cost_model_load(pool, json.dumps(cm))
+        base = gk.gk_prefix_alloc(pool, 16384)
+        b, plan = _host_plan(gk, pool, [base] * 64, [16384] * 64, [1000] * 64)
         s = gk.gk_plan_info(plan)
-        assert s["cascade_split"] == int(arr["split"]) and s["suffix_ctas"] == arr["n_gather"]
-        if arr["split"]:
-            assert s["prefix_ctas"] == arr["n_pre"] and s["prefix_tiles_per_item"] == arr["C"]
-            assert s["prefix_ctas"] <= 152 and s["suffix_ctas"] == 152
-        elif n_pref and any(g >= 0 for g in grp):
-            assert s["prefix_ctas"] == arr["n_pre"] and s["prefix_tiles_per_item"] == arr["C"]
-        assert math.isclose(td, wd, rel_tol=1e-12) and math.isclose(tc, wc, rel_tol=1e-12)
-        assert choice == (gk.GK_BACKEND_DENSE if want == "dense" else gk.GK_BACKEND_CASCADE)
         gk.gk_plan_destroy(plan)
+        assert (s["cascade_split"], s["prefix_tiles_per_item"], s["prefix_ctas"], s["suffix_ctas"]) == (1, 32, 32, 152)
+        assert s["prefix_kernel"] == gk.GK_PREFIX_TENSOR
+        gk.gk_cost_model_load(pool, json.dumps(dict(cm, prefix_tile_us=1.557, prefix_item_us=8.63)))
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SEQUENTIAL)
+        b, plan = _host_plan(gk, pool, [base] * 512, [16384] * 512, [100] * 512)
+        s = gk.gk_plan_info(plan)
+        gk.gk_plan_destroy(plan)
+        assert (s["cascade_split"], s["prefix_tiles_per_item"], s["prefix_ctas"]) == (0, 64, 128)
+        # no suffix, or no shared prefix: never split
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_AUTO)
+        for bl, ll, sl in (([base] * 64, [16384] * 64, [0] * 64), ([-1] * 64, [0] * 64, [1000] * 64)):
+            b, plan = _host_plan(gk, pool, bl, ll, sl)
+            assert gk.gk_plan_info(plan)["cascade_split"] == 0
+            gk.gk_plan_destroy(plan)
     finally:
         gk.gk_pool_destroy(pool)
 

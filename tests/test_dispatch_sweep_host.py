@@ -3,7 +3,7 @@
 The routing trace follows the dispatcher: with a cost model in which the flat
 backend is nearly free every step routes to it, with one in which it is very
 slow none does, the fractions are deterministic for a seed; and the crossover
-summary picks the smallest M_eff at which the flat backend was measured faster.
+summary lists, per prefix length, the M_eff at which each choice was measured fastest.
 """
 import json
 
@@ -45,6 +45,7 @@ def test_trace_follows_the_cost_model(sweep, tmp_path):
 
 
 def test_crossover_summary(sweep):
-    rows = [dict(Lp=512, M_eff=32, faster="cascade"), dict(Lp=512, M_eff=128, faster="dense"),
-            dict(Lp=512, M_eff=512, faster="dense"), dict(Lp=2048, M_eff=32, faster="cascade")]
-    assert sweep.crossover(rows) == {512: 128, 2048: None}
+    rows = [dict(Lp=512, M_eff=32, fastest="warp"), dict(Lp=512, M_eff=128, fastest="dense"),
+            dict(Lp=512, M_eff=512, fastest="dense"), dict(Lp=2048, M_eff=32, fastest="tensor")]
+    assert sweep.crossover(rows) == {512: {"dense": [128, 512], "tensor": [], "warp": [32]},
+                                     2048: {"dense": [], "tensor": [32], "warp": []}}

@@ -11,9 +11,13 @@ Each case is shaped so that every branch of the tensor-core prefix item runs:
     every SM, then the suffix gather);
   * queries as drawn and scaled by 8 (a peaked softmax, whose running maximum
     grows across tiles and takes the lazy-rescale branch).
-Suffixes run from 0 tokens up (an empty side merges to the other).  Both
-backends are held to the fp64 oracle at tests/parity.py's bounds, and the
-cascade's one-call entry point must give the stage-by-stage launches' bits.
+Each plan runs with both prefix kernels: tensor-core items (256 rows: the first
+row block has both Q tiles live, the second only its first) and warp-MMA items
+(128 rows: the third row block has 44 rows, so its last live warp is partly
+empty and five warps sit out).  Suffixes run from 0 tokens up (an empty side
+merges to the other).  Both backends are held to the fp64 oracle at
+tests/parity.py's bounds, and the cascade's one-call entry point must give the
+stage-by-stage launches' bits.
 """
 import numpy as np
 import pytest
@@ -32,6 +36,7 @@ LP = 3 * 128 + 77
 ROWS = 300
 MODES = [("split-2-tiles", gk.GK_CASCADE_SPLIT, 2), ("split-4-tiles", gk.GK_CASCADE_SPLIT, 4),
          ("sequential", gk.GK_CASCADE_SEQUENTIAL, 0)]
+KINDS = [("tensor", gk.GK_PREFIX_TENSOR, 256), ("warp", gk.GK_PREFIX_WARP, 128)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -79,24 +84,54 @@ def test_every_geometry_both_backends(d, g, peaked):
         O_ref, L_ref = reference.expected(w, 0)
         what = f"d={d} g={g}{' peaked' if peaked else ''}"
         seen_splits = set()
-        for name, mode, tiles in MODES:
-            gk.gk_pool_set_cascade_mode(gw.eng.pool, mode, tiles)
-            b = gw.batch()
-            pl = gw.eng.plan(b)
-            info = gk.gk_plan_info(pl)
-            if name.startswith("split-"):
-                # the forced plans: two 256-row blocks x KV heads x key splits of `tiles` tiles
-                assert info["cascade_split"] == 1 and info["prefix_tiles_per_item"] == tiles
-                assert info["prefix_ctas"] == 2 * w.Hkv * (4 // tiles)
-            seen_splits.add(info["cascade_split"])
-            q = gw.q(0)
-            O1, L1 = _decode(gw, b, pl, q, staged=False)
-            O0, L0 = _decode(gw, b, pl, q, staged=True)
-            assert np.array_equal(O1, O0) and np.array_equal(L1, L0), f"{what} {name}: cascade != stages"
-            assert_attention_close(O1, L1, O_ref, L_ref, f"{what} cascade {name}")
+        for kname, kernel, rows in KINDS:
+            gk.gk_pool_set_prefix_kernel(gw.eng.pool, kernel)
+            for name, mode, tiles in MODES:
+                gk.gk_pool_set_cascade_mode(gw.eng.pool, mode, tiles)
+                b = gw.batch()
+                pl = gw.eng.plan(b)
+                info = gk.gk_plan_info(pl)
+                assert info["prefix_kernel"] == kernel and info["prefix_rows_per_item"] == rows
+                if name.startswith("split-"):
+                    # the forced plans: row blocks x KV heads x key splits of `tiles` tiles
+                    assert info["cascade_split"] == 1 and info["prefix_tiles_per_item"] == tiles
+                    assert info["prefix_ctas"] == -(-w.B * g // rows) * w.Hkv * (4 // tiles)
+                seen_splits.add(info["cascade_split"])
+                q = gw.q(0)
+                O1, L1 = _decode(gw, b, pl, q, staged=False)
+                O0, L0 = _decode(gw, b, pl, q, staged=True)
+                tag = f"{what} {kname} {name}"
+                assert np.array_equal(O1, O0) and np.array_equal(L1, L0), f"{tag}: cascade != stages"
+                assert_attention_close(O1, L1, O_ref, L_ref, f"{tag} cascade")
         assert seen_splits == {0, 1}
         gk.gk_pool_set_cascade_mode(gw.eng.pool, gk.GK_CASCADE_AUTO, 0)
+        gk.gk_pool_set_prefix_kernel(gw.eng.pool, gk.GK_PREFIX_AUTO)
         O, L = gw.run(0, gk.GK_BACKEND_DENSE)
         assert_attention_close(O, L, O_ref, L_ref, f"{what} dense")
+    finally:
+        gw.close()
+
+
+@pytest.mark.parametrize("lp,B,g,srange", [(1000, 2, 4, (10, 300)), (130, 8, 4, (0, 5)), (2048 + 5, 8, 4, (16, 512)),
+                                           (512, 32, 4, (16, 512)), (777, 3, 1, (0, 50)), (300, 5, 8, (1, 40))])
+def test_small_m_eff_both_prefix_kernels(lp, B, g, srange):
+    """The regime the warp-MMA items are for (M_eff = B * g of 2 to 128 stacked rows), as
+    the planner arranges it and forced split, with either prefix kernel, against the oracle."""
+    from gpu_workload import GpuWorkload
+    Hkv = 8 if g != 8 else 4
+    w = workloads.config(2, B=B, Lp=lp, suffix_range=srange, L=1, Hq=Hkv * g, Hkv=Hkv)
+    gw = GpuWorkload(w)
+    try:
+        O_ref, L_ref = reference.expected(w, 0)
+        for kname, kernel, _ in KINDS:
+            gk.gk_pool_set_prefix_kernel(gw.eng.pool, kernel)
+            for name, mode, tiles in (("auto", gk.GK_CASCADE_AUTO, 0), ("split-1-tile", gk.GK_CASCADE_SPLIT, 1),
+                                      ("sequential", gk.GK_CASCADE_SEQUENTIAL, 0)):
+                gk.gk_pool_set_cascade_mode(gw.eng.pool, mode, tiles)
+                b = gw.batch()
+                pl = gw.eng.plan(b)
+                assert gk.gk_plan_info(pl)["prefix_kernel"] == kernel
+                O, L = _decode(gw, b, pl, gw.q(0), staged=False)
+                assert_attention_close(O, L, O_ref, L_ref, f"lp={lp} B={B} g={g} {kname} {name}")
     finally:
         gw.close()

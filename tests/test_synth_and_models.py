@@ -82,42 +82,46 @@ def test_eq2_meff_and_a100_threshold_rows():
         assert ("dense" if m >= g["m_sat_a100"] else "cascade") == route
 
 
+CM = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0, bw_suffix_gbs=4000.0,
+          c_merge_us=0.001, prefix_tile_us=2.0, prefix_item_us=3.0, gather_sm_gbs=1.0, c_gather_us=4.0,
+          prefix_tile_split_us=2.5, warp_tile_us=0.5, warp_item_us=1.5, warp_tile_split_us=0.75)
+
+
 def test_cost_model_closed_form():
-    # the gather on a few SMs so slow that the split arrangement never wins: the sequential formula
-    cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0, bw_suffix_gbs=4000.0,
-              c_merge_us=0.001, prefix_tile_us=2.0, prefix_item_us=3.0, gather_sm_gbs=1.0, c_gather_us=4.0,
-              prefix_tile_split_us=2.5)
-    # one group of 64 requests (g = 4 -> M = 256: one row block), Lp = 1000 (8 key tiles),
-    # suffixes 100 each, Hkv = 8, d = 128
+    cm = CM
+    # one group of 64 requests (g = 4 -> M = 256: one tensor-core row block, two warp-MMA
+    # row blocks), Lp = 1000 (8 key tiles), suffixes 100 each, Hkv = 8, d = 128
     f = dispatch.features([1000] * 64, [100] * 64, [0] * 64, 32, 8, 128)
     kv = 2 * 8 * 128 * 2
     assert f["bytes_flat"] == 64 * 1100 * kv and f["bytes_suffix"] == 64 * 100 * kv
     assert f["prefix"] == [dict(M=256, bytes=1000 * kv, flops=4 * 64 * 32 * 1000 * 128, lp=1000)]
-    # sequential key split: waves * (C * 2 + 3) is 5 at C = 1 (64 items, one wave)
-    assert dispatch.sequential_tiles(cm, f, 152) == 1 and dispatch.n_items(f, 1) == 64
-    t_flat, t_cas = dispatch.predict(cm, f)
+    # work decomposition: row blocks x KV heads x key splits
+    assert dispatch.n_items(f, 1) == 64 and dispatch.n_items(f, 8) == 8 and dispatch.n_items(f, 3) == 24
+    assert dispatch.n_items(f, 1, "warp") == 128 and dispatch.n_items(f, 8, "warp") == 16
+    # sequential plan, tensor-core items of one tile: one wave of 64 items, each 2 + 3 us
+    t_flat, t_cas = dispatch.predict(cm, f, dict(split=False, C=1, n_pre=64, kind="tensor"))
     assert math.isclose(t_flat, 5.0 + 64 * 1100 * kv / 4e6)
     t_levels = max(1000 * kv / 5e6, 1 * (1 * 2.0 + 3.0)) + 4.0 + 64 * 100 * kv / 4e6
     assert math.isclose(t_cas, 10.0 + t_levels + 0.001 * 64 * 32)
-    assert dispatch.choose(cm, f)[0] == ("dense" if t_flat < t_cas else "cascade")
-    assert not dispatch.arrangement(cm, f, 152)["split"]
+    assert dispatch.choose(t_flat, t_cas) == ("dense" if t_flat < t_cas else "cascade")
+    assert dispatch.choose(1.0, 1.0) == "cascade"       # flat only when strictly faster
+    # the same with warp items of 4 tiles: 32 items, one wave of 4 * 0.5 + 1.5 us
+    _, t_w = dispatch.predict(cm, f, dict(split=False, C=4, n_pre=32, kind="warp"))
+    assert math.isclose(t_w, 10.0 + max(1000 * kv / 5e6, 3.5) + 4.0 + 64 * 100 * kv / 4e6 + 0.001 * 64 * 32)
+    # 200 items over 152 SMs: two waves
+    assert math.isclose(dispatch.sequential_levels(cm, f, 2, 200, 152),
+                        max(1000 * kv / 5e6, 2 * (2 * 2.0 + 3.0)) + 4.0 + 64 * 100 * kv / 4e6)
     # a request without a HOT prefix counts only toward the flat and suffix bytes
     f2 = dispatch.features([0, 1000], [300, 10], [-1, 0], 32, 8, 128)
     assert f2["bytes_flat"] == 1310 * kv and len(f2["prefix"]) == 1 and f2["prefix"][0]["M"] == 4
 
 
-def test_split_arrangement_worked_example():
+def test_split_formula_worked_example():
     """One group of 64 requests (g = 4 -> one 256-row block), Lp = 16384 (128 key tiles),
     Hkv = 8, 1000 suffix tokens each; tile 1 us, item 5 us, 50 GB/s per SM, 6000 GB/s over
-    every SM, 4 us for a separate gather launch, 152 SMs.
-    Items(C) = 8 * ceil(128 / C), item(C) = C + 5 (the split tile time is 1 us too), and
-    T(C) = max(C + 5, (S / 50 GB/s + items * (C + 5)) / 152, (S + prefix bytes) / 6000 GB/s).
-    HBM binds at 54.875 us from C = 49 down (C = 50 gives 55).  A split C also has to leave
-    the prefix CTAs a gather share (T - item(C) - 4 us) / T of at least 0.15: the 24-item
-    splits (C = 43..49) leave at most 0.05, so the scan keeps the first 32-item one (C = 37,
-    share 0.16), and 32 is the fewest tiles per item that still gives 32 items."""
-    cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0, bw_suffix_gbs=6000.0,
-              c_merge_us=0.001, prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0, c_gather_us=4.0,
+    every SM, 152 SMs.  T(C) = max(C + 5, (S / 50 GB/s + items * (C + 5)) / 152,
+    (S + prefix bytes) / 6000 GB/s): HBM binds at 54.875 us from C = 49 down (C = 50: 55)."""
+    cm = dict(CM, bw_suffix_gbs=6000.0, prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0,
               prefix_tile_split_us=1.0)
     f = dispatch.features([16384] * 64, [1000] * 64, [0] * 64, 32, 8, 128)
     S = 64 * 1000 * 4096
@@ -128,29 +132,15 @@ def test_split_arrangement_worked_example():
     # C = 64: 16 items of 69 us; the gather spread over every SM is shorter
     assert math.isclose(dispatch.split_levels(cm, f, 64, 16, 152), 69.0)
     assert (S / 50e3 + 16 * 69.0) / 152 < 69.0
-    a = dispatch.arrangement(cm, f, 152)
-    assert a == dict(split=True, C=32, n_pre=32, n_gather=152)
-    assert dispatch.prefix_share(cm, 43, (S + P) / 6e6) < 0.15 <= dispatch.prefix_share(cm, 37, (S + P) / 6e6)
-    t_flat, t_cas = dispatch.predict(cm, f, 152)
+    _, t_cas = dispatch.predict(cm, f, dict(split=True, C=32, n_pre=32, kind="tensor"))
     assert math.isclose(t_cas, 10.0 + (S + P) / 6e6 + 0.001 * 64 * 32)
-    # the sequential alternative it beat: C = 7 (152 items, one wave: waves * (C * 1 + 5) = 12
-    # against 13 at C = 8 and 22 at C = 6), the prefix bound by its 67 MB of reads
-    assert dispatch.sequential_tiles(cm, f, 152) == 7 and dispatch.n_items(f, 7) == 152
-    t_seq = max(P / 5e6, 7 * 1.0 + 5.0) + 4.0 + S / 6e6
-    assert math.isclose(dispatch.sequential_levels(cm, f, 7, 152), t_seq) and t_seq > (S + P) / 6e6
-    # a split item runs beside the gather: the split formula takes prefix_tile_split_us, the
-    # sequential one prefix_tile_us (C = 64: 16 items of 64 * 2 + 5 = 133 us against 69)
-    # more rows than one wave of items holds (512 requests: M = 2048, eight row blocks per head,
-    # 64 (row block, head) units of 128 key tiles): with the GB300 fit (1.557 us a tile, 8.63 an
-    # item) one wave of 128 items of 64 tiles (108.3 us) beats three waves of 448 items of 19
-    # tiles (114.6 us) and two of 256 items of 32 (117.0 us)
-    gb = dict(cm, prefix_tile_us=1.557, prefix_item_us=8.63)
-    f512 = dispatch.features([16384] * 512, [100] * 512, [0] * 512, 32, 8, 128)
-    assert dispatch.sequential_tiles(gb, f512, 152) == 64 and dispatch.n_items(f512, 64) == 128
-    assert dispatch.n_items(f512, 19) == 448 and dispatch.n_items(f512, 32) == 256
+    # a split item runs beside the gather: the split formula takes the split tile time
+    # (C = 64: 16 items of 64 * 2 + 5 = 133 us against 69), the sequential one the lone tile
     cm2 = dict(cm, prefix_tile_split_us=2.0)
     assert math.isclose(dispatch.split_levels(cm2, f, 64, 16, 152), 133.0)
-    assert math.isclose(dispatch.sequential_levels(cm2, f, 7, 152), t_seq)
-    # no suffix, or no shared prefix: never split
-    assert not dispatch.arrangement(cm, dispatch.features([16384] * 64, [0] * 64, [0] * 64, 32, 8, 128), 152)["split"]
-    assert not dispatch.arrangement(cm, dispatch.features([0] * 64, [1000] * 64, [-1] * 64, 32, 8, 128), 152)["split"]
+    t_seq = max(P / 5e6, 7 * 1.0 + 5.0) + 4.0 + S / 6e6
+    assert math.isclose(dispatch.sequential_levels(cm2, f, 7, 152, 152), t_seq)
+    # warp-MMA items take their own terms: 2 row blocks x 8 heads x 4 splits of 32 tiles
+    cmw = dict(cm, warp_tile_split_us=3.0, warp_item_us=2.0)
+    assert dispatch.n_items(f, 32, "warp") == 64
+    assert math.isclose(dispatch.split_levels(cmw, f, 32, 64, 152, "warp"), 98.0)
