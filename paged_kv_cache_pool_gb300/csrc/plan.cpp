@@ -228,6 +228,11 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   // The split is taken when some C is predicted faster than the sequential
   // arrangement; among equal predictions the fewest items (fewest partials)
   // win, and the chosen item count is then spread evenly over the key tiles.
+  // Only C whose prefix CTAs keep at least kMinPrefixShare of a gather-only
+  // CTA's share are considered first; when there is none (small steps, where an
+  // item lasts about as long as the whole gather), the best prediction among the
+  // C that leave the gather an SM of its own is taken, its prefix CTAs then
+  // gathering nothing (one launch and the merge instead of three launches).
   struct KindPlan {
     int32_t rows = 0;
     std::vector<int32_t> mtiles;
@@ -269,6 +274,9 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
       t_seq += std::max(prefix_bytes / (cm.bw_prefix_gbs * 1e3), waves * (std::min(c_seq, max_ntiles) * tile + item));
     }
     auto item_us = [&](int32_t C) { return C * tile_split + item; };
+    // the prefix CTAs' gather share (relative to a gather-only CTA) for items of C tiles
+    // in a launch of T us: the time the item leaves, less the ramp of starting a gather
+    auto share_of = [&](int32_t C, double T) { return std::max(0.0, T - item_us(C) - cm.c_gather_us) / T; };
     auto split_us = [&](int32_t C) {
       const double it = item_us(C);
       const double bal = (S / (cm.gather_sm_gbs * 1e3) + (double)n_items(C) * it) / num_sms;
@@ -276,6 +284,7 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     };
     int32_t c_split = 0;
     double t_split = 1e300;
+    int split_pass = 0;
     const bool can_split = G > 0 && suffix_tokens > 0 && p->cascade_mode != GK_CASCADE_SEQUENTIAL;
     if (can_split && p->cascade_mode == GK_CASCADE_SPLIT && p->cascade_tiles > 0) {
       const int32_t C = std::min(p->cascade_tiles, max_ntiles);
@@ -284,16 +293,18 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
         t_split = split_us(C);
       }
     } else {
-      // the prefix CTAs' gather share for items of C tiles in a launch of T us
-      auto share_of = [&](int32_t C, double T) { return std::max(0.0, T - item_us(C) - cm.c_gather_us) / T; };
       for (int pass = 0; pass < 2 && c_split == 0; ++pass) {
-        // pass 0: only splits that leave the prefix CTAs a gather share; pass 1 (a
-        // forced split with none such): the best prediction
-        if (pass == 1 && p->cascade_mode != GK_CASCADE_SPLIT) break;
+        // pass 0: only splits that leave the prefix CTAs a gather share of at least
+        // kMinPrefixShare; pass 1 (none such: small steps whose items take about as
+        // long as the whole gather): the best prediction, the prefix CTAs then
+        // gathering nothing unless their share reaches kMinPrefixShare
+        split_pass = pass;
         for (int32_t C = max_ntiles; can_split && C >= 1; --C) {
           if (n_items(C) > num_sms) break;  // items only grow as C shrinks
           const double t = split_us(C);
           if (pass == 0 && share_of(C, t) < kMinPrefixShare) continue;
+          // the split must leave the gather at least one SM of its own
+          if (pass == 1 && n_items(C) >= num_sms) continue;
           if (t < t_split - 1e-9) {
             t_split = t;
             c_split = C;
@@ -306,12 +317,12 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     k.split = c_split > 0 && (p->cascade_mode == GK_CASCADE_SPLIT || t_split < t_seq);
     k.c = k.split ? c_split : c_seq;
     k.t_levels = k.split ? split_us(c_split) : t_seq;
-    // gather weight of a prefix CTA relative to a gather-only CTA: the time its
-    // item leaves, less the ramp of starting a gather (c_gather_us); a sliver of
-    // suffix would cost more in ramp and partial states than it saves
+    // gather weight of a prefix CTA relative to a gather-only CTA (share_of); a
+    // sliver of suffix would cost more in ramp and partial states than it saves
     if (k.split) {
       const double T = split_us(c_split);
-      k.prefix_cta_share = std::max(0.0, T - item_us(c_split) - cm.c_gather_us) / T;
+      k.prefix_cta_share = share_of(c_split, T);
+      if (split_pass == 1 && k.prefix_cta_share < kMinPrefixShare) k.prefix_cta_share = 0.0;
     }
     return k;
   };
