@@ -229,6 +229,9 @@ typedef struct gk_plan_summary {
   int32_t prefix_tiles_per_item;  /* 128-key tiles of the longest prefix work item */
   int32_t prefix_kernel;          /* prefix work items: GK_PREFIX_TENSOR or GK_PREFIX_WARP */
   int32_t prefix_rows_per_item;   /* stacked query rows per prefix work item: 256 or 128 */
+  int32_t prefix_row_groups;      /* warp items: 16-row groups of the fullest item, rounded up to
+                                     1, 2, 4 or 8; 0 for tensor-core items */
+  int32_t reserved0;
 } gk_plan_summary;
 
 /* Plan one decode step: group requests by HOT prefix (stable, first appearance),
@@ -335,9 +338,11 @@ typedef struct gk_cost_model {
   double c_gather_us;             /* fixed cost of a separate suffix-gather launch (sequential plans) */
   double prefix_tile_split_us;    /* prefix_tile_us for an item of a split plan, which runs beside a
                                      gather that keeps HBM busy (its K/V tiles wait longer) */
-  double warp_tile_us;            /* one 128-key tile of a warp-MMA prefix item (up to 128 rows) alone */
+  double warp_tile_us;            /* one 128-key tile of a warp-MMA prefix item alone: the part that does
+                                     not grow with its rows ... */
+  double warp_group_us;           /* ... plus this much per group of 16 rows (rounded up to 1, 2, 4, 8) */
   double warp_item_us;            /* fixed cost of a warp-MMA prefix item (of each wave of them) */
-  double warp_tile_split_us;      /* warp_tile_us beside the gather of a split plan */
+  double warp_split_ratio;        /* a warp item's tile beside the gather of a split plan, over alone */
 } gk_cost_model;
 
 /* Predict both backends for the plan and pick the smaller:
@@ -345,8 +350,9 @@ typedef struct gk_cost_model {
  *   T_cascade = c_cascade + T_levels + c_merge * B * Hq
  * with C = gk_plan_summary.prefix_tiles_per_item key tiles per prefix item,
  * (tile, tile_split, item) = (prefix_tile, prefix_tile_split, prefix_item) for
- * tensor-core items and (warp_tile, warp_tile_split, warp_item) for warp-MMA
- * items (gk_plan_summary.prefix_kernel), and
+ * tensor-core items and, for warp-MMA items (gk_plan_summary.prefix_kernel),
+ * tile = warp_tile + R * warp_group with R = gk_plan_summary.prefix_row_groups,
+ * tile_split = warp_split_ratio * tile and item = warp_item; and
  *   sequential plan (W = ceil(prefix_ctas / SMs) waves of prefix items):
  *     T_levels = max(prefix_bytes / bw_prefix, W * (C * tile + item))
  *                + c_gather + suffix_bytes / bw_suffix
@@ -426,8 +432,8 @@ gk_status gk_cost_model_get(const gk_pool* pool, gk_cost_model* cm);
 /* Same as gk_cost_model_set from JSON text: {"c_flat_us": .., "bw_flat_gbs": ..,
  * "c_cascade_us": .., "bw_prefix_gbs": .., "bw_suffix_gbs": .., "c_merge_us": ..,
  * "prefix_tile_us": .., "prefix_item_us": .., "gather_sm_gbs": .., "c_gather_us": ..,
- * "prefix_tile_split_us": .., "warp_tile_us": .., "warp_item_us": ..,
- * "warp_tile_split_us": ..}.
+ * "prefix_tile_split_us": .., "warp_tile_us": .., "warp_group_us": .., "warp_item_us": ..,
+ * "warp_split_ratio": ..}.
  * Keys left out keep their current values; other keys are skipped. */
 gk_status gk_cost_model_load(gk_pool* pool, const char* json);
 

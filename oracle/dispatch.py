@@ -18,8 +18,10 @@ predicted time runs (flat wins only when strictly faster):
 
 with (tile, tile_split, item_fixed) the terms of the plan's prefix kernel:
 tensor-core items (prefix_tile_us, prefix_tile_split_us, prefix_item_us; 256
-stacked rows per item) or warp-MMA items (warp_tile_us, warp_tile_split_us,
-warp_item_us; 128 rows per item), the two prefix kernels Section 3.5 pairs.
+stacked rows per item) or warp-MMA items (tile = warp_tile_us + R *
+warp_group_us, tile_split = warp_split_ratio * tile, warp_item_us; 128 rows per
+item), the two prefix kernels Section 3.5 pairs.  R = the 16-row groups of the
+fullest warp item, rounded up to 1, 2, 4 or 8.
 
 Work decomposition (fixed by the kernels' tiling, not a heuristic): a group of
 M_eff stacked rows and Lp keys contributes ceil(M_eff / rows) row blocks x Hkv
@@ -85,40 +87,56 @@ def gather_ctas(tokens, n):
     return _ceil(tokens, quota)
 
 
-def _terms(cm, kind):
+def warp_row_groups(f):
+    """R of a step: 16-row groups of its fullest warp item (min(M_eff, 128) rows of the
+    largest group), rounded up to a power of two; 0 without prefix work."""
+    rows = max([min(p["M"], ROWS["warp"]) for p in f["prefix"]], default=0)
+    if rows == 0:
+        return 0
+    r = 1
+    while r < _ceil(rows, 16):
+        r *= 2
+    return r
+
+
+def _terms(cm, kind, R=0):
     if kind == "warp":
-        return cm["warp_tile_us"], cm["warp_tile_split_us"], cm["warp_item_us"]
+        tile = cm["warp_tile_us"] + R * cm["warp_group_us"]
+        return tile, tile * cm["warp_split_ratio"], cm["warp_item_us"]
     return cm["prefix_tile_us"], cm["prefix_tile_split_us"], cm["prefix_item_us"]
 
 
-def item_us(cm, C, split=False, kind="tensor"):
+def item_us(cm, C, split=False, kind="tensor", R=0):
     """A prefix item of C key tiles: alone (sequential plans) or beside the gather (split plans)."""
-    tile, tile_split, fixed = _terms(cm, kind)
+    tile, tile_split, fixed = _terms(cm, kind, R)
     return C * (tile_split if split else tile) + fixed
 
 
-def sequential_levels(cm, f, C, n_pre, num_sms, kind="tensor"):
+def sequential_levels(cm, f, C, n_pre, num_sms, kind="tensor", R=0):
     t = cm["c_gather_us"] + f["bytes_suffix"] / (cm["bw_suffix_gbs"] * 1e3)
     if f["prefix"] and n_pre:
         waves = -(-n_pre // num_sms)
-        t += max(sum(p["bytes"] for p in f["prefix"]) / (cm["bw_prefix_gbs"] * 1e3), waves * item_us(cm, C, kind=kind))
+        t += max(sum(p["bytes"] for p in f["prefix"]) / (cm["bw_prefix_gbs"] * 1e3),
+                 waves * item_us(cm, C, kind=kind, R=R))
     return t
 
 
-def split_levels(cm, f, C, n_pre, num_sms, kind="tensor"):
-    it = item_us(cm, C, split=True, kind=kind)
+def split_levels(cm, f, C, n_pre, num_sms, kind="tensor", R=0):
+    it = item_us(cm, C, split=True, kind=kind, R=R)
     bytes_pre = sum(p["bytes"] for p in f["prefix"])
     bal = (f["bytes_suffix"] / (cm["gather_sm_gbs"] * 1e3) + n_pre * it) / num_sms
     return max(it, bal, (f["bytes_suffix"] + bytes_pre) / (cm["bw_suffix_gbs"] * 1e3))
 
 
 def predict(cm, f, plan, num_sms=152):
-    """(T_flat, T_cascade) for the arrangement a plan reports: plan = dict(split, C, n_pre, kind)."""
+    """(T_flat, T_cascade) for the arrangement a plan reports: plan = dict(split, C, n_pre, kind);
+    a warp plan's R comes from the step (warp_row_groups)."""
     t_flat = cm["c_flat_us"] + f["bytes_flat"] / (cm["bw_flat_gbs"] * 1e3)
+    R = warp_row_groups(f) if plan["kind"] == "warp" else 0
     if plan["split"]:
-        t_levels = split_levels(cm, f, plan["C"], plan["n_pre"], num_sms, plan["kind"])
+        t_levels = split_levels(cm, f, plan["C"], plan["n_pre"], num_sms, plan["kind"], R)
     else:
-        t_levels = sequential_levels(cm, f, plan["C"], plan["n_pre"], num_sms, plan["kind"])
+        t_levels = sequential_levels(cm, f, plan["C"], plan["n_pre"], num_sms, plan["kind"], R)
     t_cas = cm["c_cascade_us"] + t_levels + cm["c_merge_us"] * f["B"] * f["Hq"]
     return t_flat, t_cas
 

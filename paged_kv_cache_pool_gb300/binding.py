@@ -53,14 +53,15 @@ class gk_plan_summary(ctypes.Structure):
                 ("suffix_ctas", c_i32), ("dense_ctas", c_i32), ("num_partials", c_i32), ("dense_merge", c_i32),
                 ("prefix_bytes", c_i64), ("prefix_flops", c_i64), ("suffix_bytes", c_i64), ("dense_bytes", c_i64),
                 ("cascade_split", c_i32), ("prefix_tiles_per_item", c_i32), ("prefix_kernel", c_i32),
-                ("prefix_rows_per_item", c_i32)]
+                ("prefix_rows_per_item", c_i32), ("prefix_row_groups", c_i32), ("reserved0", c_i32)]
 
 
 class gk_cost_model(ctypes.Structure):
     _fields_ = [("c_flat_us", c_dbl), ("bw_flat_gbs", c_dbl), ("c_cascade_us", c_dbl), ("bw_prefix_gbs", c_dbl),
                 ("bw_suffix_gbs", c_dbl), ("c_merge_us", c_dbl), ("prefix_tile_us", c_dbl), ("prefix_item_us", c_dbl),
                 ("gather_sm_gbs", c_dbl), ("c_gather_us", c_dbl), ("prefix_tile_split_us", c_dbl),
-                ("warp_tile_us", c_dbl), ("warp_item_us", c_dbl), ("warp_tile_split_us", c_dbl)]
+                ("warp_tile_us", c_dbl), ("warp_group_us", c_dbl), ("warp_item_us", c_dbl),
+                ("warp_split_ratio", c_dbl)]
 
 
 P = ctypes.POINTER
@@ -428,7 +429,7 @@ def gk_cost_model_get(pool):
 
 COST_MODEL_KEYS = ("c_flat_us", "bw_flat_gbs", "c_cascade_us", "bw_prefix_gbs", "bw_suffix_gbs", "c_merge_us",
                    "prefix_tile_us", "prefix_item_us", "gather_sm_gbs", "c_gather_us", "prefix_tile_split_us",
-                   "warp_tile_us", "warp_item_us", "warp_tile_split_us")
+                   "warp_tile_us", "warp_group_us", "warp_item_us", "warp_split_ratio")
 
 
 def gk_cost_model_set(pool, cm: dict):

@@ -260,9 +260,10 @@ gk_status gk_pool_create(const gk_pool_config* cfg, gk_pool** out) {
   cm.c_gather_us = 10.0;
   cm.prefix_tile_split_us = 2.1;
   // warp-MMA prefix items: priced high until a measured model is loaded
-  cm.warp_tile_us = 6.0;
-  cm.warp_item_us = 6.0;
-  cm.warp_tile_split_us = 7.0;
+  cm.warp_tile_us = 3.0;
+  cm.warp_group_us = 1.0;
+  cm.warp_item_us = 8.0;
+  cm.warp_split_ratio = 1.3;
   *out = p;
   return GK_OK;
 }

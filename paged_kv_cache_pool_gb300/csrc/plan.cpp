@@ -135,6 +135,18 @@ void partition_tokens_weighted(const std::vector<int64_t>& n, const std::vector<
   while (begin->size() < w.size() + 1) begin->push_back((int32_t)segs->size());
 }
 
+// 16-row groups of the fullest warp-MMA item of a step, rounded up to 1, 2, 4 or
+// 8: a group of M stacked rows fills items of kPrefixWarpRows rows, the last
+// one with M mod kPrefixWarpRows
+int32_t warp_row_groups(const Pool*, const std::vector<std::vector<int32_t>>& members, int32_t g) {
+  int32_t rows = 0;
+  for (const auto& m : members) rows = std::max(rows, std::min<int32_t>((int32_t)m.size() * g, kPrefixWarpRows));
+  const int32_t groups = (rows + 15) / 16;
+  int32_t r = 1;
+  while (r < groups) r *= 2;
+  return rows > 0 ? r : 0;
+}
+
 }  // namespace
 
 gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
@@ -326,13 +338,17 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     }
     return k;
   };
+  // Warp items: a tile costs warp_tile + R * warp_group, R the 16-row groups of the
+  // fullest item rounded up to a power of two (its warps split the keys 8 / R ways).
+  const int32_t warp_groups = warp_row_groups(p, members, g);
+  const double warp_tile = cm.warp_tile_us + warp_groups * cm.warp_group_us;
   KindPlan kp;
   if (p->prefix_kernel == GK_PREFIX_WARP) {
-    kp = plan_kind(kPrefixWarpRows, cm.warp_tile_us, cm.warp_tile_split_us, cm.warp_item_us);
+    kp = plan_kind(kPrefixWarpRows, warp_tile, warp_tile * cm.warp_split_ratio, cm.warp_item_us);
   } else {
     kp = plan_kind(kPrefixRowsPerCta, cm.prefix_tile_us, cm.prefix_tile_split_us, cm.prefix_item_us);
     if (p->prefix_kernel == GK_PREFIX_AUTO && G > 0) {
-      KindPlan kw = plan_kind(kPrefixWarpRows, cm.warp_tile_us, cm.warp_tile_split_us, cm.warp_item_us);
+      KindPlan kw = plan_kind(kPrefixWarpRows, warp_tile, warp_tile * cm.warp_split_ratio, cm.warp_item_us);
       if (kw.t_levels < kp.t_levels - 1e-9) kp = std::move(kw);
     }
   }
@@ -463,6 +479,7 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   for (int32_t gi = 0; gi < G; ++gi) sm.prefix_tiles_per_item = std::max(sm.prefix_tiles_per_item, std::min(best_c, ntiles[(size_t)gi]));
   sm.prefix_kernel = pl->prefix_kind ? GK_PREFIX_WARP : GK_PREFIX_TENSOR;
   sm.prefix_rows_per_item = kp.rows;
+  sm.prefix_row_groups = pl->prefix_kind && G > 0 ? warp_groups : 0;
   return GK_OK;
 }
 
@@ -572,7 +589,8 @@ static bool valid_cost_model(const gk_cost_model& cm) {
   if (!(cm.bw_flat_gbs > 0 && cm.bw_prefix_gbs > 0 && cm.bw_suffix_gbs > 0)) return false;
   if (!(cm.prefix_tile_us > 0 && cm.prefix_tile_split_us > 0 && cm.prefix_item_us >= 0 && cm.gather_sm_gbs > 0))
     return false;
-  if (!(cm.warp_tile_us > 0 && cm.warp_tile_split_us > 0 && cm.warp_item_us >= 0)) return false;
+  if (!(cm.warp_tile_us > 0 && cm.warp_group_us >= 0 && cm.warp_item_us >= 0 && cm.warp_split_ratio > 0))
+    return false;
   if (!(cm.c_flat_us >= 0 && cm.c_cascade_us >= 0 && cm.c_merge_us >= 0 && cm.c_gather_us >= 0)) return false;
   return true;
 }
@@ -704,8 +722,9 @@ gk_status gk_dispatch(const gk_pool* pool, const gk_plan* plan, gk_backend* choi
   const gk_plan_summary& sm = pl.summary;
   const int num_sms = pool->impl.dev.num_sms;
   const bool warp = pl.prefix_kind == 1;
-  const double tile = warp ? cm.warp_tile_us : cm.prefix_tile_us;
-  const double tile_split = warp ? cm.warp_tile_split_us : cm.prefix_tile_split_us;
+  const double wtile = cm.warp_tile_us + pl.summary.prefix_row_groups * cm.warp_group_us;
+  const double tile = warp ? wtile : cm.prefix_tile_us;
+  const double tile_split = warp ? wtile * cm.warp_split_ratio : cm.prefix_tile_split_us;
   const double item_fixed = warp ? cm.warp_item_us : cm.prefix_item_us;
   if (pl.split) {
     const double item = sm.prefix_tiles_per_item * tile_split + item_fixed;
@@ -782,7 +801,8 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
     static const char* kNumeric[] = {"c_flat_us",      "bw_flat_gbs",    "c_cascade_us",  "bw_prefix_gbs",
                                      "bw_suffix_gbs",  "c_merge_us",     "prefix_tile_us", "prefix_item_us",
                                      "gather_sm_gbs",  "c_gather_us",    "prefix_tile_split_us",
-                                     "warp_tile_us",   "warp_item_us",   "warp_tile_split_us"};
+                                     "warp_tile_us",   "warp_group_us",  "warp_item_us",
+                                     "warp_split_ratio"};
     bool known = false;
     for (const char* k : kNumeric) known = known || key == k;
     if (!known) {
@@ -803,8 +823,9 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
     else if (key == "c_gather_us") cm.c_gather_us = v;
     else if (key == "prefix_tile_split_us") cm.prefix_tile_split_us = v;
     else if (key == "warp_tile_us") cm.warp_tile_us = v;
+    else if (key == "warp_group_us") cm.warp_group_us = v;
     else if (key == "warp_item_us") cm.warp_item_us = v;
-    else if (key == "warp_tile_split_us") cm.warp_tile_split_us = v;
+    else if (key == "warp_split_ratio") cm.warp_split_ratio = v;
   }
   return gk_cost_model_set(pool, &cm);
 }

@@ -84,7 +84,7 @@ def test_eq2_meff_and_a100_threshold_rows():
 
 CM = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0, bw_suffix_gbs=4000.0,
           c_merge_us=0.001, prefix_tile_us=2.0, prefix_item_us=3.0, gather_sm_gbs=1.0, c_gather_us=4.0,
-          prefix_tile_split_us=2.5, warp_tile_us=0.5, warp_item_us=1.5, warp_tile_split_us=0.75)
+          prefix_tile_split_us=2.5, warp_tile_us=0.25, warp_group_us=0.03125, warp_item_us=1.5, warp_split_ratio=1.5)
 
 
 def test_cost_model_closed_form():
@@ -105,7 +105,9 @@ def test_cost_model_closed_form():
     assert math.isclose(t_cas, 10.0 + t_levels + 0.001 * 64 * 32)
     assert dispatch.choose(t_flat, t_cas) == ("dense" if t_flat < t_cas else "cascade")
     assert dispatch.choose(1.0, 1.0) == "cascade"       # flat only when strictly faster
-    # the same with warp items of 4 tiles: 32 items, one wave of 4 * 0.5 + 1.5 us
+    # the same with warp items of 4 tiles: 32 items, one wave; the fullest warp item has
+    # 128 rows (8 groups of 16), so a tile costs 0.25 + 8 * 0.03125 = 0.5 us: 4 * 0.5 + 1.5
+    assert dispatch.warp_row_groups(f) == 8
     _, t_w = dispatch.predict(cm, f, dict(split=False, C=4, n_pre=32, kind="warp"))
     assert math.isclose(t_w, 10.0 + max(1000 * kv / 5e6, 3.5) + 4.0 + 64 * 100 * kv / 4e6 + 0.001 * 64 * 32)
     # 200 items over 152 SMs: two waves
@@ -140,7 +142,11 @@ def test_split_formula_worked_example():
     assert math.isclose(dispatch.split_levels(cm2, f, 64, 16, 152), 133.0)
     t_seq = max(P / 5e6, 7 * 1.0 + 5.0) + 4.0 + S / 6e6
     assert math.isclose(dispatch.sequential_levels(cm2, f, 7, 152, 152), t_seq)
-    # warp-MMA items take their own terms: 2 row blocks x 8 heads x 4 splits of 32 tiles
-    cmw = dict(cm, warp_tile_split_us=3.0, warp_item_us=2.0)
+    # warp-MMA items take their own terms: 2 row blocks x 8 heads x 4 splits of 32 tiles,
+    # a tile beside the gather 1.5 * (1 + 8 * 0.125) = 3 us: item 32 * 3 + 2 = 98 us
+    cmw = dict(cm, warp_tile_us=1.0, warp_group_us=0.125, warp_split_ratio=1.5, warp_item_us=2.0)
     assert dispatch.n_items(f, 32, "warp") == 64
-    assert math.isclose(dispatch.split_levels(cmw, f, 32, 64, 152, "warp"), 98.0)
+    assert math.isclose(dispatch.split_levels(cmw, f, 32, 64, 152, "warp", R=8), 98.0)
+    # R rounds the fullest item's 16-row groups up to a power of two
+    for B, R in ((1, 1), (4, 1), (5, 2), (8, 2), (9, 4), (16, 4), (17, 8), (100, 8)):
+        assert dispatch.warp_row_groups(dispatch.features([512] * B, [1] * B, [0] * B, 32, 8, 128)) == R
