@@ -429,6 +429,32 @@ typedef enum gk_prefix_kernel {
 } gk_prefix_kernel;
 gk_status gk_pool_set_prefix_kernel(gk_pool* pool, gk_prefix_kernel kernel);
 gk_status gk_cost_model_get(const gk_pool* pool, gk_cost_model* cm);
+/* Re-fit the cost model on this GPU (GraniKV Section 3.6: the routing rule stays
+ * and its numbers are re-fit per GPU; Appendix B.4b's sweep).  Times, with CUDA
+ * events on `stream` and L2 emptied before every launch, the flat backend, the
+ * suffix gather, the merge, tensor-core and warp-MMA prefix items of several
+ * key-tile counts (warp items with 1, 2 and 8 groups of 16 rows), the gather
+ * beside long items, and whole cascades, on layer 0 of this pool with a
+ * synthetic batch of one shared prefix; fits each gk_cost_model term by least
+ * squares (the cascade's fixed cost is the mean residual of the whole cascades
+ * under gk_dispatch); installs the model in the pool; and, if json_out is not
+ * NULL, writes it to that file in gk_cost_model_load's format with the
+ * measured points under "measured".  Blocking; a few seconds.
+ *  - The pool needs device storage; its K/V contents are read as they are (the
+ *    timings do not depend on the values) and never written.  Cases that do not
+ *    fit its free HOT and COLD space are skipped; with at least 16384 free HOT
+ *    tokens and 262144 free COLD token slots every case runs.  GK_ERR_INVALID
+ *    when too few cases fit to fit every term (the model is left as it was).
+ *  - HOT ranges, sequences and COLD blocks are taken from the pool's allocators
+ *    and given back: afterwards the same blocks are free, though the order in
+ *    which free blocks are handed out may differ.  The pool's cascade mode,
+ *    prefix kernel and gather partition are restored.
+ *  - The calibration's own scratch (queries, outputs, tables, 512 MiB to empty
+ *    L2) is allocated with cudaMalloc and freed before returning.
+ *  - The split-plan tile terms are the alone terms times 1.28, the ratio
+ *    measured on GB300 for a tensor-core item beside a gather that keeps HBM
+ *    busy (warp_split_ratio = 1.28 too). */
+gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_out);
 /* Same as gk_cost_model_set from JSON text: {"c_flat_us": .., "bw_flat_gbs": ..,
  * "c_cascade_us": .., "bw_prefix_gbs": .., "bw_suffix_gbs": .., "c_merge_us": ..,
  * "prefix_tile_us": .., "prefix_item_us": .., "gather_sm_gbs": .., "c_gather_us": ..,

@@ -108,6 +108,7 @@ _SIGS = {
     "gk_pool_set_cascade_mode": (c_i32, [c_vp, c_i32, c_i32]),
     "gk_pool_set_gather_partition": (c_i32, [c_vp, c_i32]),
     "gk_pool_set_prefix_kernel": (c_i32, [c_vp, c_i32]),
+    "gk_calibrate": (c_i32, [c_vp, c_vp, ctypes.c_char_p]),
     "gk_device_error": (c_i32, [c_vp, c_vp, P(c_i32)]),
 }
 
@@ -458,6 +459,10 @@ GK_PREFIX_AUTO, GK_PREFIX_TENSOR, GK_PREFIX_WARP = 0, 1, 2
 
 def gk_pool_set_prefix_kernel(pool, kernel):
     _check(lib().gk_pool_set_prefix_kernel(pool, int(kernel)), pool)
+
+
+def gk_calibrate(pool, stream=None, json_out=None):
+    _check(lib().gk_calibrate(pool, _stream(stream), json_out.encode() if json_out else None), pool)
 
 
 def gk_cost_model_load(pool, json_text: str):

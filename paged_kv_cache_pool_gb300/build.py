@@ -17,7 +17,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgk.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["host_pool.cpp", "plan.cpp", "kv_write.cu", "gather_attn.cu", "merge.cu", "prefix_tc.cu",
-           "prefix_warp.cu", "cascade_split.cu", "static_scratch.cu"]
+           "prefix_warp.cu", "cascade_split.cu", "static_scratch.cu", "calibrate.cu"]
 COMMON = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-lineinfo", "-I" + os.path.join(ROOT, "include")]
 
 

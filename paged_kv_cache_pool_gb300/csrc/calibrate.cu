@@ -1,0 +1,494 @@
+// gk_calibrate: the dispatcher's cost model measured on this GPU.
+//
+// GraniKV Section 3.6 keeps the routing rule and says its threshold must be
+// re-fit on each GPU (Appendix B.4b fits M_sat = 1024 on A100 with a sweep).
+// Here the rule is the cost model of gk_dispatch, and this call is the re-fit:
+// it times the kernels with CUDA events on one layer of the caller's pool, L2
+// emptied before every launch, and fits each term by least squares.
+//   flat backend, several batches            -> c_flat_us + bytes / bw_flat_gbs
+//   suffix gather over every SM               -> c_gather_us + bytes / bw_suffix_gbs
+//   merge                                     -> c_merge_us per (request, query head)
+//   tensor-core prefix items of C key tiles   -> prefix_item_us + C * prefix_tile_us
+//   warp-MMA prefix items, R row groups       -> warp_item_us + C * (warp_tile_us + R * warp_group_us)
+//   the gather alone on the SMs long items leave it -> gather_sm_gbs (median per SM)
+//   the whole cascade, both arrangements      -> c_cascade_us (mean residual)
+// An item beside a gather that keeps HBM busy waits longer for its K/V tiles:
+// per-phase timer stamps in an instrumented build measured 1.9-2.0 us per tile
+// of a tensor-core item beside the gather against 1.53-1.56 alone, a ratio of
+// about 1.28, which both kinds of item take (a fit in place would need split
+// plans whose gather lasts exactly the item, which no fixed pool gives).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <array>
+#include <cmath>
+#include <cstdio>
+#include <string>
+#include <vector>
+
+#include "device_common.cuh"
+#include "gk_internal.h"
+
+namespace gk {
+namespace {
+
+constexpr double kSplitTileRatio = 1.28;
+constexpr double kPrefixBandwidthGbs = 6000.0;   // HOT reads of a sequential plan's prefix launch
+constexpr size_t kFlushBytes = 256u << 20;       // twice this is written and read between launches
+
+// Reads a buffer far larger than L2, so that a timed launch starts from an L2
+// that holds none of its inputs and no dirty lines (whose write-back it would pay).
+__global__ void l2_sweep_kernel(const uint4* __restrict__ p, size_t n, uint32_t* sink) {
+  uint32_t acc = 0;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const uint4 v = __ldcg(p + i);
+    acc ^= v.x ^ v.y ^ v.z ^ v.w;
+  }
+  if (acc == 0x9E3779B9u) *sink = acc;   // keeps the loads; the buffer is zero, so never taken
+}
+
+// Queries for the timings: bf16 values in [-2, 2) from a hash of the index
+// (timing does not depend on them; they only have to be finite).
+__global__ void fill_queries_kernel(uint16_t* q, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    uint32_t h = (uint32_t)i * 2654435761u;
+    h ^= h >> 15;
+    h *= 2246822519u;
+    h ^= h >> 13;
+    const float v = ((float)(h & 0xFFFFu) / 65536.f - 0.5f) * 4.f;
+    q[i] = (uint16_t)(__float_as_uint(v) >> 16);
+  }
+}
+
+// least squares y = c0 + c1 x (the intercept may come out negative)
+bool linfit(const std::vector<std::pair<double, double>>& pts, double* c0, double* c1) {
+  const double n = (double)pts.size();
+  if (pts.size() < 2) return false;
+  double sx = 0, sy = 0, sxx = 0, sxy = 0;
+  for (auto& q : pts) {
+    sx += q.first;
+    sy += q.second;
+    sxx += q.first * q.first;
+    sxy += q.first * q.second;
+  }
+  const double den = n * sxx - sx * sx;
+  if (std::fabs(den) < 1e-30) return false;
+  *c1 = (n * sxy - sx * sy) / den;
+  *c0 = (sy - *c1 * sx) / n;
+  return true;
+}
+
+// least squares y = a0 + a1 x1 + a2 x2 (normal equations, Cramer's rule)
+bool fit3(const std::vector<std::array<double, 3>>& pts, double a[3]) {
+  if (pts.size() < 3) return false;
+  double M[3][3] = {}, v[3] = {};
+  for (auto& q : pts) {
+    const double f[3] = {1.0, q[0], q[1]};
+    for (int i = 0; i < 3; ++i) {
+      v[i] += f[i] * q[2];
+      for (int j = 0; j < 3; ++j) M[i][j] += f[i] * f[j];
+    }
+  }
+  auto det = [](const double m[3][3]) {
+    return m[0][0] * (m[1][1] * m[2][2] - m[1][2] * m[2][1]) - m[0][1] * (m[1][0] * m[2][2] - m[1][2] * m[2][0]) +
+           m[0][2] * (m[1][0] * m[2][1] - m[1][1] * m[2][0]);
+  };
+  const double D = det(M);
+  if (std::fabs(D) < 1e-30) return false;
+  for (int c = 0; c < 3; ++c) {
+    double T[3][3];
+    for (int i = 0; i < 3; ++i)
+      for (int j = 0; j < 3; ++j) T[i][j] = j == c ? v[i] : M[i][j];
+    a[c] = det(T) / D;
+  }
+  return true;
+}
+
+double median(std::vector<double> v) {
+  if (v.empty()) return 0.0;
+  std::sort(v.begin(), v.end());
+  return v[v.size() / 2];
+}
+
+// One calibration run: scratch buffers on the device, timing, and the cases'
+// resources taken from (and given back to) the pool's allocators.
+struct Calib {
+  gk_pool* pool = nullptr;
+  Pool* p = nullptr;
+  cudaStream_t st = nullptr;
+  int32_t max_b = 0, max_blocks = 0;
+  uint16_t* d_q = nullptr;
+  float* d_out = nullptr;
+  float* d_lse = nullptr;
+  int32_t* d_table = nullptr;
+  uint8_t* flush = nullptr;     // 2 * kFlushBytes: written, then the other half read
+  uint32_t* sink = nullptr;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  int reps = 7;
+  std::string why;              // first failure
+
+  bool cuda(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return true;
+    if (why.empty()) why = std::string(what) + ": " + cudaGetErrorString(e);
+    return false;
+  }
+  bool setup(int32_t B, int32_t blocks) {
+    const gk_pool_config& c = p->cfg;
+    max_b = B;
+    max_blocks = blocks;
+    const size_t nq = (size_t)B * c.num_q_heads * c.head_dim;
+    return cuda(cudaMalloc(&d_q, nq * 2), "cudaMalloc(queries)") &&
+           cuda(cudaMalloc(&d_out, nq * 4), "cudaMalloc(outputs)") &&
+           cuda(cudaMalloc(&d_lse, (size_t)B * c.num_q_heads * 4), "cudaMalloc(lse)") &&
+           cuda(cudaMalloc(&d_table, (size_t)B * blocks * 4), "cudaMalloc(block tables)") &&
+           cuda(cudaMalloc(&flush, 2 * kFlushBytes), "cudaMalloc(L2 flush)") &&
+           cuda(cudaMalloc(&sink, 4), "cudaMalloc(sink)") &&
+           cuda(cudaMemsetAsync(flush, 0, 2 * kFlushBytes, st), "cudaMemsetAsync") &&
+           cuda(cudaEventCreate(&e0), "cudaEventCreate") && cuda(cudaEventCreate(&e1), "cudaEventCreate") &&
+           (fill_queries_kernel<<<256, 256, 0, st>>>(d_q, nq), cuda(cudaGetLastError(), "query fill"));
+  }
+  void teardown() {
+    cudaStreamSynchronize(st);
+    for (void* b : {(void*)d_q, (void*)d_out, (void*)d_lse, (void*)d_table, (void*)flush, (void*)sink})
+      if (b) cudaFree(b);
+    if (e0) cudaEventDestroy(e0);
+    if (e1) cudaEventDestroy(e1);
+  }
+  // write one half of the flush buffer and read the other: the next launch meets an L2
+  // with none of its data and nothing dirty
+  bool flush_l2() {
+    return cuda(cudaMemsetAsync(flush, 0, kFlushBytes, st), "cudaMemsetAsync(flush)") &&
+           (l2_sweep_kernel<<<4 * std::max(1, p->dev.num_sms), 512, 0, st>>>(
+                reinterpret_cast<const uint4*>(flush + kFlushBytes), kFlushBytes / 16, sink),
+            cuda(cudaGetLastError(), "L2 sweep"));
+  }
+  // median of `reps` timings (one warm-up launch first), microseconds; < 0 on failure
+  template <class F>
+  double time_us(F launch) {
+    std::vector<double> ts;
+    for (int r = 0; r <= reps; ++r) {
+      if (!flush_l2()) return -1;
+      if (!cuda(cudaEventRecord(e0, st), "cudaEventRecord")) return -1;
+      const gk_status s = launch();
+      if (s != GK_OK) {
+        if (why.empty()) why = std::string("a timed call failed: ") + gk_last_error(pool);
+        return -1;
+      }
+      if (!cuda(cudaEventRecord(e1, st), "cudaEventRecord") || !cuda(cudaEventSynchronize(e1), "cudaEventSynchronize"))
+        return -1;
+      float ms = 0;
+      if (!cuda(cudaEventElapsedTime(&ms, e0, e1), "cudaEventElapsedTime")) return -1;
+      if (r > 0) ts.push_back(ms * 1e3);
+    }
+    return median(ts);
+  }
+};
+
+// One synthetic step: B requests share one HOT prefix of lp tokens, each with a
+// COLD suffix of s tokens, reserved through the pool's own block manager.
+struct Case {
+  int32_t B = 0, lp = 0, s = 0;
+  int64_t hot_base = -1;
+  std::vector<int32_t> seqs, slen, lps;
+  std::vector<int64_t> bases;
+  gk_batch batch{};
+  bool open = false;
+};
+
+// false when the pool has no room for the case (it is then skipped) or on an error (c.why set)
+bool open_case(Calib& c, Case& k, int32_t B, int32_t lp, int32_t s) {
+  k = Case{};
+  k.B = B;
+  k.lp = lp;
+  k.s = s;
+  const int32_t P = c.p->cfg.cold_page_size;
+  const int32_t blocks = (s + P - 1) / P;
+  if (B > c.max_b || blocks > c.max_blocks) return false;
+  if (gk_prefix_alloc(c.pool, lp, &k.hot_base) != GK_OK) return false;
+  for (int32_t r = 0; r < B; ++r) {
+    int32_t sq = -1;
+    if (gk_seq_create(c.pool, &sq) != GK_OK) break;
+    k.seqs.push_back(sq);
+  }
+  k.open = true;
+  if ((int32_t)k.seqs.size() < B) return false;
+  std::vector<int32_t> order((size_t)B * s);
+  for (int32_t r = 0; r < B; ++r) std::fill(order.begin() + (size_t)r * s, order.begin() + (size_t)(r + 1) * s, k.seqs[r]);
+  std::vector<int64_t> slots(order.size());
+  std::vector<int32_t> cow(2 * order.size() + 2);
+  int32_t n_cow = 0, n_done = 0;
+  if (!order.empty() && gk_seq_append_slots(c.pool, (int32_t)order.size(), order.data(), slots.data(), &n_cow,
+                                            cow.data(), &n_done) != GK_OK)
+    return false;   // out of COLD blocks: what was appended is released with the sequences
+  std::vector<int32_t> table((size_t)B * c.max_blocks);
+  k.slen.assign(B, 0);
+  if (gk_seq_tables(c.pool, B, k.seqs.data(), c.max_blocks, table.data(), k.slen.data()) != GK_OK) return false;
+  if (!c.cuda(cudaMemcpyAsync(c.d_table, table.data(), table.size() * 4, cudaMemcpyHostToDevice, c.st),
+              "cudaMemcpyAsync(block tables)") ||
+      !c.cuda(cudaStreamSynchronize(c.st), "cudaStreamSynchronize"))
+    return false;
+  k.bases.assign(B, k.hot_base);
+  k.lps.assign(B, lp);
+  k.batch = gk_batch{};
+  k.batch.num_requests = B;
+  k.batch.max_blocks = c.max_blocks;
+  k.batch.prefix_hot_base = k.bases.data();
+  k.batch.prefix_len = k.lps.data();
+  k.batch.suffix_len = k.slen.data();
+  k.batch.d_block_table = c.d_table;
+  k.batch.d_q = c.d_q;
+  k.batch.d_out = c.d_out;
+  k.batch.d_lse = c.d_lse;
+  return true;
+}
+
+void close_case(Calib& c, Case& k) {
+  if (!k.open) return;
+  for (int32_t sq : k.seqs) gk_seq_release(c.pool, sq);
+  if (k.hot_base >= 0) gk_prefix_release(c.pool, k.hot_base);
+  k = Case{};
+}
+
+}  // namespace
+}  // namespace gk
+
+using gk::Calib;
+using gk::Case;
+
+extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_out) {
+  if (!pool) return GK_ERR_INVALID;
+  gk::Pool* p = &pool->impl;
+  if (!p->has_device) return gk::fail(p, GK_ERR_INVALID, "gk_calibrate needs a pool with device storage");
+  gk_status st = gk::ensure_device(p);
+  if (st != GK_OK) return st;
+  const gk_pool_config cfg = p->cfg;
+  const int32_t g = cfg.num_q_heads / cfg.num_kv_heads;
+  const int num_sms = p->dev.num_sms;
+  // the pool's settings are the calibration's to change; they are put back at the end
+  const gk_cascade_mode mode0 = p->cascade_mode;
+  const int32_t tiles0 = p->cascade_tiles;
+  const gk_prefix_kernel kernel0 = p->prefix_kernel;
+  const gk_gather_partition part0 = p->gather_partition;
+  const gk_cost_model cost0 = p->cost;
+  p->gather_partition = GK_PARTITION_STREAM;
+
+  Calib c;
+  c.pool = pool;
+  c.p = p;
+  c.st = (cudaStream_t)stream;
+  std::vector<gk_plan*> plans;                          // kept for the residual fit
+  std::vector<std::pair<gk_plan*, double>> cascades;    // (plan, measured whole cascade)
+  std::vector<std::pair<double, double>> flat, suffix, merge, tile, gather_sm;
+  std::vector<std::array<double, 3>> warp;              // (C, C * R, us)
+  bool ok = c.setup(512, (1024 + cfg.cold_page_size - 1) / cfg.cold_page_size + 1);
+
+  auto plan_for = [&](Case& k, gk_cascade_mode mode, int32_t tiles, gk_prefix_kernel kern) -> gk_plan* {
+    p->cascade_mode = mode;
+    p->cascade_tiles = tiles;
+    p->prefix_kernel = kern;
+    gk_plan* pl = nullptr;
+    if (gk_plan_build(pool, &k.batch, stream, &pl) != GK_OK) {
+      if (c.why.empty()) c.why = std::string("gk_plan_build: ") + gk_last_error(pool);
+      return nullptr;
+    }
+    plans.push_back(pl);
+    return pl;
+  };
+  auto timed = [&](auto fn) { return c.time_us(fn); };
+  Case k;
+
+  // (1) sequential plans over tensor-core items: flat, suffix gather, merge, prefix items, whole cascade
+  const int32_t base_cases[5][3] = {{8, 2048, 256}, {32, 4096, 512}, {64, 16384, 1024}, {128, 8192, 512}, {256, 4096, 1024}};
+  for (auto& bc : base_cases) {
+    if (!ok) break;
+    if (gk::open_case(c, k, bc[0], bc[1], bc[2])) {
+      gk_plan* pl = plan_for(k, GK_CASCADE_SEQUENTIAL, 0, GK_PREFIX_TENSOR);
+      ok = pl != nullptr;
+      gk_plan_summary sm{};
+      if (ok) gk_plan_info(pl, &sm);
+      double t;
+      if (ok && (ok = (t = timed([&] { return gk_decode_dense(pool, stream, 0, &k.batch, pl); })) >= 0))
+        flat.push_back({(double)sm.dense_bytes, t});
+      if (ok && (ok = (t = timed([&] { return gk_cascade_suffix(pool, stream, 0, &k.batch, pl); })) >= 0))
+        suffix.push_back({(double)sm.suffix_bytes, t});
+      if (ok && (ok = (t = timed([&] { return gk_cascade_merge(pool, stream, 0, &k.batch, pl); })) >= 0))
+        merge.push_back({(double)k.B * cfg.num_q_heads, t});
+      if (ok && sm.prefix_ctas <= num_sms &&
+          (ok = (t = timed([&] { return gk_cascade_prefix(pool, stream, 0, &k.batch, pl); })) >= 0))
+        tile.push_back({(double)sm.prefix_tiles_per_item, t});
+      if (ok && (ok = (t = timed([&] { return gk_decode_cascade(pool, stream, 0, &k.batch, pl); })) >= 0))
+        cascades.push_back({pl, t});
+    } else if (!c.why.empty()) {
+      ok = false;
+    }
+    gk::close_case(c, k);
+  }
+  // (2) split plans with long tensor-core items: the items alone and the whole cascade
+  if (ok && gk::open_case(c, k, 64, 16384, 1024)) {
+    for (int32_t C : {16, 32, 64, 128}) {
+      gk_plan* pl = plan_for(k, GK_CASCADE_SPLIT, C, GK_PREFIX_TENSOR);
+      if (!(ok = pl != nullptr)) break;
+      gk_plan_summary sm{};
+      gk_plan_info(pl, &sm);
+      if (!sm.cascade_split) continue;
+      double t;
+      if (!(ok = (t = timed([&] { return gk_cascade_prefix(pool, stream, 0, &k.batch, pl); })) >= 0)) break;
+      tile.push_back({(double)sm.prefix_tiles_per_item, t});
+      if (!(ok = (t = timed([&] { return gk_decode_cascade(pool, stream, 0, &k.batch, pl); })) >= 0)) break;
+      cascades.push_back({pl, t});
+    }
+  } else if (!c.why.empty()) {
+    ok = false;
+  }
+  gk::close_case(c, k);
+  // (3) the gather alone on the SMs that one-split items (M_eff 512 g) leave it
+  if (ok && gk::open_case(c, k, 512, 16384, 128)) {
+    gk_plan* pl = plan_for(k, GK_CASCADE_SPLIT, 128, GK_PREFIX_TENSOR);
+    gk_plan_summary sm{};
+    double t = -1;
+    if ((ok = pl != nullptr)) {
+      gk_plan_info(pl, &sm);
+      if (sm.cascade_split && sm.suffix_ctas > sm.prefix_ctas) {
+        ok = (t = timed([&] { return gk_cascade_suffix(pool, stream, 0, &k.batch, pl); })) >= 0;
+        if (ok) gather_sm.push_back({(double)(sm.suffix_ctas - sm.prefix_ctas),
+                                     (double)sm.suffix_bytes / (t * 1e3) / (sm.suffix_ctas - sm.prefix_ctas)});
+      }
+    }
+  } else if (!c.why.empty()) {
+    ok = false;
+  }
+  gk::close_case(c, k);
+  // (4) warp-MMA items of 16, 32 and 128 stacked rows (R = 1, 2, 8) and C key tiles
+  for (int32_t rows : {16, 32, 128}) {
+    if (!ok) break;
+    if (gk::open_case(c, k, (rows + g - 1) / g, 16384, 64)) {
+      for (int32_t C : {8, 32, 128}) {
+        gk_plan* pl = plan_for(k, GK_CASCADE_SPLIT, C, GK_PREFIX_WARP);
+        if (!(ok = pl != nullptr)) break;
+        gk_plan_summary sm{};
+        gk_plan_info(pl, &sm);
+        if (!sm.cascade_split) continue;
+        double t;
+        if (!(ok = (t = timed([&] { return gk_cascade_prefix(pool, stream, 0, &k.batch, pl); })) >= 0)) break;
+        warp.push_back({(double)sm.prefix_tiles_per_item, (double)sm.prefix_tiles_per_item * sm.prefix_row_groups, t});
+        if (!(ok = (t = timed([&] { return gk_decode_cascade(pool, stream, 0, &k.batch, pl); })) >= 0)) break;
+        cascades.push_back({pl, t});
+      }
+    } else if (!c.why.empty()) {
+      ok = false;
+    }
+    gk::close_case(c, k);
+  }
+
+  // ---- fits ----
+  gk_cost_model cm = p->cost;
+  double a0 = 0, a1 = 0;
+  if (ok) {
+    std::string miss;
+    if (!gk::linfit(flat, &a0, &a1) || a1 <= 0) miss += " flat";
+    else { cm.c_flat_us = std::max(0.0, a0); cm.bw_flat_gbs = 1.0 / a1 / 1e3; }
+    if (!gk::linfit(suffix, &a0, &a1) || a1 <= 0) miss += " suffix";
+    else { cm.c_gather_us = std::max(0.0, a0); cm.bw_suffix_gbs = 1.0 / a1 / 1e3; }
+    if (!gk::linfit(merge, &a0, &a1)) miss += " merge";
+    else cm.c_merge_us = std::max(0.0, a1);
+    if (!gk::linfit(tile, &a0, &a1) || a1 <= 0) miss += " prefix-items";
+    else {
+      cm.prefix_item_us = std::max(0.0, a0);
+      cm.prefix_tile_us = a1;
+      cm.prefix_tile_split_us = a1 * gk::kSplitTileRatio;
+    }
+    double w[3];
+    if (!gk::fit3(warp, w)) miss += " warp-items";
+    else {
+      // a tile's part that does not grow with the rows must stay positive; if the fit
+      // puts it below zero, refit with it pinned near zero (all of the tile on the rows)
+      cm.warp_item_us = std::max(0.0, w[0]);
+      if (w[1] > 0 && w[2] >= 0) {
+        cm.warp_tile_us = w[1];
+        cm.warp_group_us = w[2];
+      } else {
+        std::vector<std::pair<double, double>> pts;
+        for (auto& q : warp) pts.push_back({q[1], q[2] - cm.warp_item_us});
+        double b0, b1;
+        cm.warp_tile_us = 1e-3;
+        cm.warp_group_us = gk::linfit(pts, &b0, &b1) && b1 > 0 ? b1 : 1.0;
+      }
+      cm.warp_split_ratio = gk::kSplitTileRatio;
+    }
+    std::vector<double> per_sm;
+    for (auto& q : gather_sm) per_sm.push_back(q.second);
+    if (per_sm.empty()) miss += " gather-per-SM";
+    else cm.gather_sm_gbs = gk::median(per_sm);
+    cm.bw_prefix_gbs = gk::kPrefixBandwidthGbs;
+    if (!miss.empty()) {
+      ok = false;
+      c.why = "pool too small to calibrate (no room for the cases of:" + miss +
+              "); give it at least 16384 HOT tokens and 262144 COLD token slots";
+    }
+  }
+  // the cascade's fixed cost: the mean residual of the whole cascade over the model
+  std::vector<std::pair<double, double>> resid;   // (predicted without c_cascade, measured)
+  if (ok) {
+    cm.c_cascade_us = 0.0;
+    p->cost = cm;
+    double sum = 0;
+    for (auto& pc : cascades) {
+      gk_backend choice;
+      double td = 0, tc = 0;
+      gk_dispatch(pool, pc.first, &choice, &td, &tc);
+      resid.push_back({tc, pc.second});
+      sum += pc.second - tc;
+    }
+    cm.c_cascade_us = cascades.empty() ? 0.0 : std::max(0.0, sum / cascades.size());
+  }
+  for (gk_plan* pl : plans) gk_plan_destroy(pl);   // after the stream's work (timed calls synchronised)
+  c.teardown();
+  p->cascade_mode = mode0;
+  p->cascade_tiles = tiles0;
+  p->prefix_kernel = kernel0;
+  p->gather_partition = part0;
+  if (!ok) {
+    p->cost = cost0;   // the model in force before the call is kept on failure
+    return gk::fail(p, c.why.find("pool too small") == 0 ? GK_ERR_INVALID : GK_ERR_CUDA, "gk_calibrate: " + c.why);
+  }
+  st = gk_cost_model_set(pool, &cm);
+  if (st != GK_OK) return st;
+  if (json_out) {
+    FILE* f = std::fopen(json_out, "w");
+    if (!f) return gk::fail(p, GK_ERR_INVALID, std::string("gk_calibrate: cannot write ") + json_out);
+    auto pts = [&](const char* name, const std::vector<std::pair<double, double>>& v, bool last) {
+      std::fprintf(f, "  \"%s\": [", name);
+      for (size_t i = 0; i < v.size(); ++i) std::fprintf(f, "%s[%.6g, %.6g]", i ? ", " : "", v[i].first, v[i].second);
+      std::fprintf(f, "]%s\n", last ? "" : ",");
+    };
+    std::fprintf(f, "{\n");
+    const std::pair<const char*, double> terms[] = {
+        {"c_flat_us", cm.c_flat_us},         {"bw_flat_gbs", cm.bw_flat_gbs},
+        {"c_cascade_us", cm.c_cascade_us},   {"bw_prefix_gbs", cm.bw_prefix_gbs},
+        {"bw_suffix_gbs", cm.bw_suffix_gbs}, {"c_merge_us", cm.c_merge_us},
+        {"prefix_tile_us", cm.prefix_tile_us}, {"prefix_item_us", cm.prefix_item_us},
+        {"gather_sm_gbs", cm.gather_sm_gbs}, {"c_gather_us", cm.c_gather_us},
+        {"prefix_tile_split_us", cm.prefix_tile_split_us}, {"warp_tile_us", cm.warp_tile_us},
+        {"warp_group_us", cm.warp_group_us}, {"warp_item_us", cm.warp_item_us},
+        {"warp_split_ratio", cm.warp_split_ratio}};
+    for (auto& t : terms) std::fprintf(f, " \"%s\": %.17g,\n", t.first, t.second);
+    std::fprintf(f, " \"geometry\": {\"num_q_heads\": %d, \"num_kv_heads\": %d, \"head_dim\": %d, \"sms\": %d},\n",
+                 cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, num_sms);
+    std::fprintf(f, " \"measured\": {\n");
+    pts("flat (dense bytes, us)", flat, false);
+    pts("suffix (suffix bytes, us)", suffix, false);
+    pts("merge (requests x query heads, us)", merge, false);
+    pts("prefix items (tiles per item, us)", tile, false);
+    std::fprintf(f, "  \"warp items (tiles per item, tiles x row groups, us)\": [");
+    for (size_t i = 0; i < warp.size(); ++i)
+      std::fprintf(f, "%s[%.6g, %.6g, %.6g]", i ? ", " : "", warp[i][0], warp[i][1], warp[i][2]);
+    std::fprintf(f, "],\n");
+    pts("gather per SM (SMs, GB/s per SM)", gather_sm, false);
+    pts("cascade (predicted without c_cascade, measured us)", resid, true);
+    std::fprintf(f, " }\n}\n");
+    const bool werr = std::ferror(f) != 0;
+    std::fclose(f);
+    if (werr) return gk::fail(p, GK_ERR_INVALID, std::string("gk_calibrate: writing ") + json_out + " failed");
+  }
+  return GK_OK;
+}

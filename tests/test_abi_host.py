@@ -425,3 +425,17 @@ def test_cascade_mode_forces_the_arrangement(gk):
             gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SPLIT, -1)
     finally:
         gk.gk_pool_destroy(pool)
+
+
+def test_calibrate_needs_device_storage(gk):
+    """gk_calibrate times kernels, so a host-only pool is refused and its model kept."""
+    pool = gk.gk_pool_create(1, 32, 8, 128, 20000, 300000, 1, 0)
+    try:
+        before = gk.gk_cost_model_get(pool)
+        with pytest.raises(gk.GkError) as e:
+            gk.gk_calibrate(pool, None, None)
+        assert e.value.status == gk.GK_ERR_INVALID and "device" in str(e.value)
+        assert gk.gk_cost_model_get(pool) == before
+    finally:
+        gk.gk_pool_destroy(pool)
+    assert gk.lib().gk_calibrate(None, None, None) == gk.GK_ERR_INVALID
