@@ -285,7 +285,11 @@ __device__ __forceinline__ bool warp_item(const prefix::PrefixParams& p, const P
     const int k0 = kslice * kpw;   // this warp's keys of every tile: [k0, k0 + kpw)
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % NST;
-      if (!wait_item(bar(B_FULL + st), (j / NST) & 1, p.err, abort_flag)) { ok = false; break; }
+      // warp-uniform: a lane that gave up takes its whole warp out of the loop
+      if (!__all_sync(0xffffffffu, wait_item(bar(B_FULL + st), (j / NST) & 1, p.err, abort_flag))) {
+        ok = false;
+        break;
+      }
       const uint32_t ks = base + st * Lay::kStage, vs = ks + Lay::kTile;
       const int nvalid = gr.lp - (key0 + j * BN);   // keys of this tile inside the prefix
       if (kw <= 2) {
