@@ -16,23 +16,34 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "liboracle.so")
+# the same loops built with AddressSanitizer and UndefinedBehaviorSanitizer; a
+# process selects it with GK_ORACLE_LIB (and preloads the sanitizer runtimes)
+LIB_SAN = os.path.join(_HERE, "liboracle_san.so")
+SAN_FLAGS = ["-fsanitize=address", "-fsanitize=undefined", "-fno-omit-frame-pointer",
+             "-fno-sanitize-recover=undefined"]
 _lib = None
 
 
-def build(force: bool = False) -> str:
+def build(force: bool = False, sanitized: bool = False) -> str:
     src = os.path.join(_HERE, "attention.c")
-    if force or not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < os.path.getmtime(src):
-        tmp = LIB_PATH + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-o", tmp, src, "-lm"])
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    out = LIB_SAN if sanitized else LIB_PATH
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+        tmp = out + f".tmp{os.getpid()}"
+        env = dict(os.environ)
+        env.pop("LD_PRELOAD", None)
+        flags = SAN_FLAGS if sanitized else []
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", *flags, "-o", tmp, src, "-lm"], env=env)
+        os.replace(tmp, out)
+    return out
 
 
 def _load():
     global _lib
     if _lib is None:
-        build()
-        lib = ctypes.CDLL(LIB_PATH)
+        path = os.environ.get("GK_ORACLE_LIB")
+        if not path:
+            path = build()
+        lib = ctypes.CDLL(path)
         dp = ctypes.POINTER(ctypes.c_double)
         lib.gk_oracle_attend_heads.restype = ctypes.c_int
         lib.gk_oracle_attend_heads.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,

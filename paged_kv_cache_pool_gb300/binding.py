@@ -13,7 +13,8 @@ import os
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libgk.so")
+# GK_LIB_PATH selects another build of the same library (the sanitizer build in the tests)
+LIB_PATH = os.environ.get("GK_LIB_PATH") or os.path.join(_HERE, "libgk.so")
 
 GK_OK = 0
 GK_ERR_INVALID = 1
