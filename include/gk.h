@@ -231,7 +231,8 @@ typedef struct gk_plan_summary {
   int32_t prefix_rows_per_item;   /* stacked query rows per prefix work item: 256 or 128 */
   int32_t prefix_row_groups;      /* warp items: 16-row groups of the fullest item, rounded up to
                                      1, 2, 4 or 8; 0 for tensor-core items */
-  int32_t reserved0;
+  int32_t prefix_ctas_gather;     /* split plans: 1 when the prefix CTAs also gather a share of the
+                                     suffix after their items, 0 when only the other CTAs gather */
 } gk_plan_summary;
 
 /* Plan one decode step: group requests by HOT prefix (stable, first appearance),
@@ -343,11 +344,14 @@ typedef struct gk_cost_model {
   double warp_group_us;           /* ... plus this much per group of 16 rows (rounded up to 1, 2, 4, 8) */
   double warp_item_us;            /* fixed cost of a warp-MMA prefix item (of each wave of them) */
   double warp_split_ratio;        /* a warp item's tile beside the gather of a split plan, over alone */
+  double prefix_cta_ramp_us;      /* split plans: a prefix CTA starts gathering this long after its item */
+  double prefix_cta_gather_ratio; /* ... and gathers at this fraction of a gather-only CTA's rate */
+  double c_merge_state_us;        /* merge cost per partial state of a request (a merge warp's round trips) */
 } gk_cost_model;
 
 /* Predict both backends for the plan and pick the smaller:
  *   T_dense   = c_flat + dense_bytes / bw_flat
- *   T_cascade = c_cascade + T_levels + c_merge * B * Hq
+ *   T_cascade = c_cascade + T_levels + c_merge * B * Hq + c_merge_state * num_partials / B
  * with C = gk_plan_summary.prefix_tiles_per_item key tiles per prefix item,
  * (tile, tile_split, item) = (prefix_tile, prefix_tile_split, prefix_item) for
  * tensor-core items and, for warp-MMA items (gk_plan_summary.prefix_kernel),
@@ -356,18 +360,25 @@ typedef struct gk_cost_model {
  *   sequential plan (W = ceil(prefix_ctas / SMs) waves of prefix items):
  *     T_levels = max(prefix_bytes / bw_prefix, W * (C * tile + item))
  *                + c_gather + suffix_bytes / bw_suffix
- *   split plan (see gk_plan_summary.cascade_split; it = C * tile_split + item):
- *     T_levels = max(it, (suffix_bytes / gather_sm + prefix_ctas * it) / SMs,
- *                    (suffix_bytes + prefix_bytes) / bw_suffix)
- *   (the middle term spreads the gather's SM-time and the items over every SM)
- * A plan without prefix work has no prefix term.  GraniKV's M_eff (Eq. 2)
- * enters through the items: a group of M_eff stacked rows gives
- * ceil(M_eff / rows per item) items per KV head and key split.  The plan has
- * already chosen the prefix kernel and the arrangement with the smallest
- * T_levels (GraniKV Section 3.6's routing between its two prefix kernels, with
- * the threshold replaced by the measured model), so this call completes the
- * three-way choice: flat, cascade over tensor-core items, cascade over warp-MMA
- * items.  Dense is chosen only when strictly faster.  Host only. */
+ *   split plan (see gk_plan_summary.cascade_split; it = C * tile_split + item,
+ *   n = prefix_ctas, A = SMs - n gather-only CTAs, G = suffix_bytes / gather_sm
+ *   the gather's SM-time, e = prefix_cta_gather_ratio, r = prefix_cta_ramp):
+ *     T_gather = (G + A * c_gather + n * e * (it + r)) / (A + n * e)
+ *                when the prefix CTAs gather too (gk_plan_summary.prefix_ctas_gather),
+ *              = c_gather + G / A otherwise;
+ *     T_levels = max(it, T_gather, (suffix_bytes + prefix_bytes) / bw_suffix)
+ *   (gather-only CTAs start after c_gather, prefix CTAs r after their items,
+ *   and all end together; the last term is HBM).
+ * A plan without prefix work has no prefix term, one without suffix work no
+ * gather term.  GraniKV's M_eff (Eq. 2) enters through the items: a group of
+ * M_eff stacked rows gives ceil(M_eff / rows per item) items per KV head and key
+ * split.  The plan has already chosen the prefix kernel and the arrangement
+ * with the smallest predicted time (GraniKV Section 3.6's routing between its
+ * two prefix kernels, with the threshold replaced by the measured model), so
+ * this call completes the three-way choice: flat, cascade over tensor-core
+ * items, cascade over warp-MMA items.  Dense is chosen only when strictly
+ * faster; a negative prediction (a negative c_cascade on a tiny step) counts as
+ * zero.  Host only. */
 gk_status gk_dispatch(const gk_pool* pool, const gk_plan* plan, gk_backend* choice, double* t_dense_us,
                       double* t_cascade_us);
 gk_status gk_cost_model_set(gk_pool* pool, const gk_cost_model* cm);
@@ -451,15 +462,20 @@ gk_status gk_cost_model_get(const gk_pool* pool, gk_cost_model* cm);
  *    prefix kernel and gather partition are restored.
  *  - The calibration's own scratch (queries, outputs, tables, 512 MiB to empty
  *    L2) is allocated with cudaMalloc and freed before returning.
- *  - The split-plan tile terms are the alone terms times 1.28, the ratio
- *    measured on GB300 for a tensor-core item beside a gather that keeps HBM
- *    busy (warp_split_ratio = 1.28 too). */
+ *  - The terms of the split arrangement (prefix_tile_split_us / prefix_tile_us,
+ *    warp_split_ratio, prefix_cta_ramp_us, prefix_cta_gather_ratio) and
+ *    c_cascade_us are fitted to the whole cascades it times (sequential and
+ *    split plans, forced and as the planner arranges them, both prefix kernels):
+ *    a grid search for the smallest largest relative error of T_cascade, the
+ *    other terms held at their own fits.  c_cascade_us may come out negative
+ *    (the terms timed alone each carry a launch that the cascade overlaps). */
 gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_out);
 /* Same as gk_cost_model_set from JSON text: {"c_flat_us": .., "bw_flat_gbs": ..,
  * "c_cascade_us": .., "bw_prefix_gbs": .., "bw_suffix_gbs": .., "c_merge_us": ..,
  * "prefix_tile_us": .., "prefix_item_us": .., "gather_sm_gbs": .., "c_gather_us": ..,
  * "prefix_tile_split_us": .., "warp_tile_us": .., "warp_group_us": .., "warp_item_us": ..,
- * "warp_split_ratio": ..}.
+ * "warp_split_ratio": .., "prefix_cta_ramp_us": .., "prefix_cta_gather_ratio": ..,
+ * "c_merge_state_us": ..}.
  * Keys left out keep their current values; other keys are skipped. */
 gk_status gk_cost_model_load(gk_pool* pool, const char* json);
 

@@ -8,13 +8,19 @@ measured cost model evaluated on the step's plan; the backend with the smaller
 predicted time runs (flat wins only when strictly faster):
 
   T_flat    = c_flat + bytes_flat / bw_flat
-  T_cascade = c_cascade + T_levels + c_merge * B * Hq
+  T_cascade = max(0, c_cascade + T_levels + c_merge * B * Hq + c_merge_state * partials / B)
   item(C)   = C * tile + item_fixed          (one prefix work item of C key tiles, alone)
   item'(C)  = C * tile_split + item_fixed    (the same beside a gather that keeps HBM busy)
   T_levels  = max(bytes_pre / bw_prefix, W * item(C)) + c_gather
               + bytes_suffix / bw_suffix                          (sequential plan, W waves)
-            = max(item'(C), (bytes_suffix / gather_sm + n_pre * item'(C)) / SMs,
-                  (bytes_suffix + bytes_pre) / bw_suffix)          (split plan)
+            = max(item'(C), T_gather, (bytes_suffix + bytes_pre) / bw_suffix)   (split plan)
+  T_gather  = (G + A * c_gather + n * e * (item'(C) + r)) / (A + n * e)   (prefix CTAs gather too)
+            = c_gather + G / A                                    (only the other CTAs gather)
+with n = n_pre prefix CTAs, A = SMs - n gather-only CTAs, G = bytes_suffix /
+gather_sm the gather's SM-time, r = prefix_cta_ramp_us and e =
+prefix_cta_gather_ratio: gather-only CTAs start after c_gather, a prefix CTA r
+after its item and at e of their rate, and all end together.  A step without
+suffix tokens has no gather term (and no c_gather in the sequential plan).
 
 with (tile, tile_split, item_fixed) the terms of the plan's prefix kernel:
 tensor-core items (prefix_tile_us, prefix_tile_split_us, prefix_item_us; 256
@@ -28,7 +34,8 @@ M_eff stacked rows and Lp keys contributes ceil(M_eff / rows) row blocks x Hkv
 heads x ceil(ceil(Lp / 128) / C) items.
 
 Parity unpinned: which arrangement a plan takes (split or sequential, the key
-tiles per item C, the prefix kernel) is the planner's search over this model,
+tiles per item C, the prefix kernel, whether its prefix CTAs also gather) is
+the planner's search over this model,
 and the pages fix none of it (their threshold is specific to the A100).  This
 oracle does not restate that search; it evaluates the formula above for the
 arrangement a plan reports, and the choice itself is held to measurement on
@@ -113,7 +120,7 @@ def item_us(cm, C, split=False, kind="tensor", R=0):
 
 
 def sequential_levels(cm, f, C, n_pre, num_sms, kind="tensor", R=0):
-    t = cm["c_gather_us"] + f["bytes_suffix"] / (cm["bw_suffix_gbs"] * 1e3)
+    t = cm["c_gather_us"] + f["bytes_suffix"] / (cm["bw_suffix_gbs"] * 1e3) if f["bytes_suffix"] else 0.0
     if f["prefix"] and n_pre:
         waves = -(-n_pre // num_sms)
         t += max(sum(p["bytes"] for p in f["prefix"]) / (cm["bw_prefix_gbs"] * 1e3),
@@ -121,23 +128,35 @@ def sequential_levels(cm, f, C, n_pre, num_sms, kind="tensor", R=0):
     return t
 
 
-def split_levels(cm, f, C, n_pre, num_sms, kind="tensor", R=0):
-    it = item_us(cm, C, split=True, kind=kind, R=R)
+def split_levels(cm, f, C, n_pre, num_sms, kind="tensor", R=0, gather=True):
+    it = item_us(cm, C, split=True, kind=kind, R=R) if n_pre else 0.0
     bytes_pre = sum(p["bytes"] for p in f["prefix"])
-    bal = (f["bytes_suffix"] / (cm["gather_sm_gbs"] * 1e3) + n_pre * it) / num_sms
-    return max(it, bal, (f["bytes_suffix"] + bytes_pre) / (cm["bw_suffix_gbs"] * 1e3))
+    t = max(it, (f["bytes_suffix"] + bytes_pre) / (cm["bw_suffix_gbs"] * 1e3))
+    if f["bytes_suffix"] == 0:
+        return t
+    G = f["bytes_suffix"] / (cm["gather_sm_gbs"] * 1e3)
+    A = num_sms - n_pre
+    e, r, cg = cm["prefix_cta_gather_ratio"], cm["prefix_cta_ramp_us"], cm["c_gather_us"]
+    if gather and n_pre:
+        t_gather = (G + A * cg + n_pre * e * (it + r)) / (A + n_pre * e)
+    else:
+        t_gather = cg + G / A
+    return max(t, t_gather)
 
 
 def predict(cm, f, plan, num_sms=152):
-    """(T_flat, T_cascade) for the arrangement a plan reports: plan = dict(split, C, n_pre, kind);
-    a warp plan's R comes from the step (warp_row_groups)."""
+    """(T_flat, T_cascade) for the arrangement a plan reports: plan = dict(split, C, n_pre,
+    kind, gather, partials); a warp plan's R comes from the step (warp_row_groups)."""
     t_flat = cm["c_flat_us"] + f["bytes_flat"] / (cm["bw_flat_gbs"] * 1e3)
     R = warp_row_groups(f) if plan["kind"] == "warp" else 0
     if plan["split"]:
-        t_levels = split_levels(cm, f, plan["C"], plan["n_pre"], num_sms, plan["kind"], R)
+        t_levels = split_levels(cm, f, plan["C"], plan["n_pre"], num_sms, plan["kind"], R, plan["gather"])
     else:
         t_levels = sequential_levels(cm, f, plan["C"], plan["n_pre"], num_sms, plan["kind"], R)
-    t_cas = cm["c_cascade_us"] + t_levels + cm["c_merge_us"] * f["B"] * f["Hq"]
+    merge = cm["c_merge_us"] * f["B"] * f["Hq"]
+    if f["B"]:
+        merge += cm["c_merge_state_us"] * plan["partials"] / f["B"]
+    t_cas = max(0.0, cm["c_cascade_us"] + t_levels + merge)
     return t_flat, t_cas
 
 

@@ -54,7 +54,7 @@ class gk_plan_summary(ctypes.Structure):
                 ("suffix_ctas", c_i32), ("dense_ctas", c_i32), ("num_partials", c_i32), ("dense_merge", c_i32),
                 ("prefix_bytes", c_i64), ("prefix_flops", c_i64), ("suffix_bytes", c_i64), ("dense_bytes", c_i64),
                 ("cascade_split", c_i32), ("prefix_tiles_per_item", c_i32), ("prefix_kernel", c_i32),
-                ("prefix_rows_per_item", c_i32), ("prefix_row_groups", c_i32), ("reserved0", c_i32)]
+                ("prefix_rows_per_item", c_i32), ("prefix_row_groups", c_i32), ("prefix_ctas_gather", c_i32)]
 
 
 class gk_cost_model(ctypes.Structure):
@@ -62,7 +62,8 @@ class gk_cost_model(ctypes.Structure):
                 ("bw_suffix_gbs", c_dbl), ("c_merge_us", c_dbl), ("prefix_tile_us", c_dbl), ("prefix_item_us", c_dbl),
                 ("gather_sm_gbs", c_dbl), ("c_gather_us", c_dbl), ("prefix_tile_split_us", c_dbl),
                 ("warp_tile_us", c_dbl), ("warp_group_us", c_dbl), ("warp_item_us", c_dbl),
-                ("warp_split_ratio", c_dbl)]
+                ("warp_split_ratio", c_dbl), ("prefix_cta_ramp_us", c_dbl), ("prefix_cta_gather_ratio", c_dbl),
+                ("c_merge_state_us", c_dbl)]
 
 
 P = ctypes.POINTER
@@ -431,7 +432,8 @@ def gk_cost_model_get(pool):
 
 COST_MODEL_KEYS = ("c_flat_us", "bw_flat_gbs", "c_cascade_us", "bw_prefix_gbs", "bw_suffix_gbs", "c_merge_us",
                    "prefix_tile_us", "prefix_item_us", "gather_sm_gbs", "c_gather_us", "prefix_tile_split_us",
-                   "warp_tile_us", "warp_group_us", "warp_item_us", "warp_split_ratio")
+                   "warp_tile_us", "warp_group_us", "warp_item_us", "warp_split_ratio", "prefix_cta_ramp_us",
+                   "prefix_cta_gather_ratio", "c_merge_state_us")
 
 
 def gk_cost_model_set(pool, cm: dict):

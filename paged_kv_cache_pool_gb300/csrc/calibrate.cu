@@ -8,15 +8,16 @@
 //   flat backend, several batches            -> c_flat_us + bytes / bw_flat_gbs
 //   suffix gather over every SM               -> c_gather_us + bytes / bw_suffix_gbs
 //   merge                                     -> c_merge_us per (request, query head)
+//                                                + c_merge_state_us per partial state of a request
 //   tensor-core prefix items of C key tiles   -> prefix_item_us + C * prefix_tile_us
 //   warp-MMA prefix items, R row groups       -> warp_item_us + C * (warp_tile_us + R * warp_group_us)
 //   the gather alone on the SMs long items leave it -> gather_sm_gbs (median per SM)
-//   the whole cascade, both arrangements      -> c_cascade_us (mean residual)
-// An item beside a gather that keeps HBM busy waits longer for its K/V tiles:
-// per-phase timer stamps in an instrumented build measured 1.9-2.0 us per tile
-// of a tensor-core item beside the gather against 1.53-1.56 alone, a ratio of
-// about 1.28, which both kinds of item take (a fit in place would need split
-// plans whose gather lasts exactly the item, which no fixed pool gives).
+// The split arrangement's own terms -- how much longer an item's tile takes
+// beside a gather that keeps HBM busy (per kind of item), when and how fast a
+// prefix CTA gathers after its item -- and c_cascade_us are then fitted to the
+// whole cascades timed here (both arrangements, forced and as the planner
+// arranges them, both kinds of item): a grid search for the smallest largest
+// relative error of the predicted cascade, the other terms held at their fits.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -32,7 +33,6 @@
 namespace gk {
 namespace {
 
-constexpr double kSplitTileRatio = 1.28;
 constexpr double kPrefixBandwidthGbs = 6000.0;   // HOT reads of a sequential plan's prefix launch
 constexpr size_t kFlushBytes = 256u << 20;       // twice this is written and read between launches
 
@@ -278,7 +278,8 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
   c.st = (cudaStream_t)stream;
   std::vector<gk_plan*> plans;                          // kept for the residual fit
   std::vector<std::pair<gk_plan*, double>> cascades;    // (plan, measured whole cascade)
-  std::vector<std::pair<double, double>> flat, suffix, merge, tile, gather_sm;
+  std::vector<std::pair<double, double>> flat, suffix, tile, gather_sm;
+  std::vector<std::array<double, 3>> merge;             // (B * Hq, partial states per request, us)
   std::vector<std::array<double, 3>> warp;              // (C, C * R, us)
   bool ok = c.setup(512, (1024 + cfg.cold_page_size - 1) / cfg.cold_page_size + 1);
 
@@ -312,7 +313,7 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
       if (ok && (ok = (t = timed([&] { return gk_cascade_suffix(pool, stream, 0, &k.batch, pl); })) >= 0))
         suffix.push_back({(double)sm.suffix_bytes, t});
       if (ok && (ok = (t = timed([&] { return gk_cascade_merge(pool, stream, 0, &k.batch, pl); })) >= 0))
-        merge.push_back({(double)k.B * cfg.num_q_heads, t});
+        merge.push_back({(double)k.B * cfg.num_q_heads, (double)sm.num_partials / k.B, t});
       if (ok && sm.prefix_ctas <= num_sms &&
           (ok = (t = timed([&] { return gk_cascade_prefix(pool, stream, 0, &k.batch, pl); })) >= 0))
         tile.push_back({(double)sm.prefix_tiles_per_item, t});
@@ -380,6 +381,30 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
     gk::close_case(c, k);
   }
 
+  // (5) steps as the planner arranges them (cascade mode AUTO), each prefix kernel:
+  //     the merge and the whole cascade
+  const int32_t auto_cases[6][3] = {{8, 2048, 256}, {8, 16384, 256}, {32, 8192, 256},
+                                    {128, 512, 256}, {128, 16384, 256}, {512, 4096, 256}};
+  for (auto& ac : auto_cases) {
+    if (!ok) break;
+    if (gk::open_case(c, k, ac[0], ac[1], ac[2])) {
+      for (gk_prefix_kernel kern : {GK_PREFIX_TENSOR, GK_PREFIX_WARP}) {
+        gk_plan* pl = plan_for(k, GK_CASCADE_AUTO, 0, kern);
+        if (!(ok = pl != nullptr)) break;
+        gk_plan_summary sm{};
+        gk_plan_info(pl, &sm);
+        double t;
+        if (!(ok = (t = timed([&] { return gk_cascade_merge(pool, stream, 0, &k.batch, pl); })) >= 0)) break;
+        merge.push_back({(double)k.B * cfg.num_q_heads, (double)sm.num_partials / k.B, t});
+        if (!(ok = (t = timed([&] { return gk_decode_cascade(pool, stream, 0, &k.batch, pl); })) >= 0)) break;
+        cascades.push_back({pl, t});
+      }
+    } else if (!c.why.empty()) {
+      ok = false;
+    }
+    gk::close_case(c, k);
+  }
+
   // ---- fits ----
   gk_cost_model cm = p->cost;
   double a0 = 0, a1 = 0;
@@ -389,13 +414,23 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
     else { cm.c_flat_us = std::max(0.0, a0); cm.bw_flat_gbs = 1.0 / a1 / 1e3; }
     if (!gk::linfit(suffix, &a0, &a1) || a1 <= 0) miss += " suffix";
     else { cm.c_gather_us = std::max(0.0, a0); cm.bw_suffix_gbs = 1.0 / a1 / 1e3; }
-    if (!gk::linfit(merge, &a0, &a1)) miss += " merge";
-    else cm.c_merge_us = std::max(0.0, a1);
+    double mw[3];
+    if (!gk::fit3(merge, mw)) {
+      miss += " merge";
+    } else if (mw[1] >= 0 && mw[2] >= 0) {
+      cm.c_merge_us = mw[1];
+      cm.c_merge_state_us = mw[2];
+    } else {
+      // a negative slope: keep the term that grows with the warps alone
+      std::vector<std::pair<double, double>> pts;
+      for (auto& q : merge) pts.push_back({q[0], q[2]});
+      cm.c_merge_us = gk::linfit(pts, &a0, &a1) ? std::max(0.0, a1) : 0.0;
+      cm.c_merge_state_us = 0.0;
+    }
     if (!gk::linfit(tile, &a0, &a1) || a1 <= 0) miss += " prefix-items";
     else {
       cm.prefix_item_us = std::max(0.0, a0);
       cm.prefix_tile_us = a1;
-      cm.prefix_tile_split_us = a1 * gk::kSplitTileRatio;
     }
     double w[3];
     if (!gk::fit3(warp, w)) miss += " warp-items";
@@ -413,7 +448,6 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
         cm.warp_tile_us = 1e-3;
         cm.warp_group_us = gk::linfit(pts, &b0, &b1) && b1 > 0 ? b1 : 1.0;
       }
-      cm.warp_split_ratio = gk::kSplitTileRatio;
     }
     std::vector<double> per_sm;
     for (auto& q : gather_sm) per_sm.push_back(q.second);
@@ -426,20 +460,65 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
               "); give it at least 16384 HOT tokens and 262144 COLD token slots";
     }
   }
-  // the cascade's fixed cost: the mean residual of the whole cascade over the model
+  // The split arrangement's terms and the cascade's fixed cost, fitted to the whole
+  // cascades: for each point of a grid over (tile ratio of tensor-core items, of
+  // warp items, prefix CTAs' gather ramp, their gather rate), c_cascade minimises
+  // the largest relative error (a convex function of c: ternary search); the grid
+  // point with the smallest such error wins, ties to the smaller mean error.
   std::vector<std::pair<double, double>> resid;   // (predicted without c_cascade, measured)
-  if (ok) {
-    cm.c_cascade_us = 0.0;
-    p->cost = cm;
-    double sum = 0;
+  if (ok && !cascades.empty()) {
+    const int32_t Hq = cfg.num_q_heads;
+    std::vector<double> pred(cascades.size());
+    auto worst = [&](double cc) {
+      double e = 0;
+      for (size_t i = 0; i < cascades.size(); ++i)
+        e = std::max(e, std::fabs(std::max(0.0, pred[i] + cc) - cascades[i].second) / cascades[i].second);
+      return e;
+    };
+    double best_e = 1e300, best_mean = 1e300;
+    gk_cost_model best = cm;
+    for (int it_r = 0; it_r <= 12; ++it_r)
+      for (int iw_r = 0; iw_r <= 12; ++iw_r)
+        for (int i_ramp = 0; i_ramp <= 20; ++i_ramp)
+          for (int i_e = 0; i_e <= 4; ++i_e) {
+            gk_cost_model m = cm;
+            m.prefix_tile_split_us = cm.prefix_tile_us * (1.0 + 0.04 * it_r);
+            m.warp_split_ratio = 1.0 + 0.04 * iw_r;
+            m.prefix_cta_ramp_us = 2.0 * i_ramp;
+            m.prefix_cta_gather_ratio = 0.5 + 0.125 * i_e;
+            m.c_cascade_us = 0.0;
+            for (size_t i = 0; i < cascades.size(); ++i) {
+              double td;
+              gk::predict_plan(m, num_sms, Hq, cascades[i].first->impl, &td, &pred[i]);
+            }
+            // no prediction below zero inside the search, so the error is convex in c
+            double lo = -60.0, hi = 60.0;
+            for (double q : pred) lo = std::max(lo, -q);
+            for (int s2 = 0; s2 < 80; ++s2) {
+              const double m1 = lo + (hi - lo) / 3, m2 = hi - (hi - lo) / 3;
+              if (worst(m1) <= worst(m2)) hi = m2; else lo = m1;
+            }
+            const double cc = 0.5 * (lo + hi);
+            const double e = worst(cc);
+            double mean = 0;
+            for (size_t i = 0; i < cascades.size(); ++i)
+              mean += std::fabs(std::max(0.0, pred[i] + cc) - cascades[i].second) / cascades[i].second;
+            mean /= cascades.size();
+            if (e < best_e - 1e-12 || (e < best_e + 1e-12 && mean < best_mean)) {
+              best_e = e;
+              best_mean = mean;
+              best = m;
+              best.c_cascade_us = cc;
+            }
+          }
+    cm = best;
+    gk_cost_model m0 = cm;
+    m0.c_cascade_us = 0.0;
     for (auto& pc : cascades) {
-      gk_backend choice;
-      double td = 0, tc = 0;
-      gk_dispatch(pool, pc.first, &choice, &td, &tc);
+      double td, tc;
+      gk::predict_plan(m0, num_sms, Hq, pc.first->impl, &td, &tc);
       resid.push_back({tc, pc.second});
-      sum += pc.second - tc;
     }
-    cm.c_cascade_us = cascades.empty() ? 0.0 : std::max(0.0, sum / cascades.size());
   }
   for (gk_plan* pl : plans) gk_plan_destroy(pl);   // after the stream's work (timed calls synchronised)
   c.teardown();
@@ -470,21 +549,36 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
         {"gather_sm_gbs", cm.gather_sm_gbs}, {"c_gather_us", cm.c_gather_us},
         {"prefix_tile_split_us", cm.prefix_tile_split_us}, {"warp_tile_us", cm.warp_tile_us},
         {"warp_group_us", cm.warp_group_us}, {"warp_item_us", cm.warp_item_us},
-        {"warp_split_ratio", cm.warp_split_ratio}};
+        {"warp_split_ratio", cm.warp_split_ratio}, {"prefix_cta_ramp_us", cm.prefix_cta_ramp_us},
+        {"prefix_cta_gather_ratio", cm.prefix_cta_gather_ratio}, {"c_merge_state_us", cm.c_merge_state_us}};
     for (auto& t : terms) std::fprintf(f, " \"%s\": %.17g,\n", t.first, t.second);
     std::fprintf(f, " \"geometry\": {\"num_q_heads\": %d, \"num_kv_heads\": %d, \"head_dim\": %d, \"sms\": %d},\n",
                  cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, num_sms);
     std::fprintf(f, " \"measured\": {\n");
     pts("flat (dense bytes, us)", flat, false);
     pts("suffix (suffix bytes, us)", suffix, false);
-    pts("merge (requests x query heads, us)", merge, false);
+    std::fprintf(f, "  \"merge (requests x query heads, partial states per request, us)\": [");
+    for (size_t i = 0; i < merge.size(); ++i)
+      std::fprintf(f, "%s[%.6g, %.6g, %.6g]", i ? ", " : "", merge[i][0], merge[i][1], merge[i][2]);
+    std::fprintf(f, "],\n");
     pts("prefix items (tiles per item, us)", tile, false);
     std::fprintf(f, "  \"warp items (tiles per item, tiles x row groups, us)\": [");
     for (size_t i = 0; i < warp.size(); ++i)
       std::fprintf(f, "%s[%.6g, %.6g, %.6g]", i ? ", " : "", warp[i][0], warp[i][1], warp[i][2]);
     std::fprintf(f, "],\n");
     pts("gather per SM (SMs, GB/s per SM)", gather_sm, false);
-    pts("cascade (predicted without c_cascade, measured us)", resid, true);
+    pts("cascade (predicted without c_cascade, measured us)", resid, false);
+    // each timed cascade's plan, so that the model can be refitted from this file alone
+    std::fprintf(f, "  \"cascade plans (split, prefix CTAs gather, warp items, tiles per item, prefix CTAs, "
+                    "row groups, suffix bytes, prefix bytes, partial states, requests, measured us)\": [");
+    for (size_t i = 0; i < cascades.size(); ++i) {
+      const gk_plan_summary& q = cascades[i].first->impl.summary;
+      std::fprintf(f, "%s[%d, %d, %d, %d, %d, %d, %lld, %lld, %d, %d, %.6g]", i ? ", " : "", q.cascade_split,
+                   q.prefix_ctas_gather, q.prefix_kernel == GK_PREFIX_WARP ? 1 : 0, q.prefix_tiles_per_item,
+                   q.prefix_ctas, q.prefix_row_groups, (long long)q.suffix_bytes, (long long)q.prefix_bytes,
+                   q.num_partials, q.num_requests, cascades[i].second);
+    }
+    std::fprintf(f, "]\n");
     std::fprintf(f, " }\n}\n");
     const bool werr = std::ferror(f) != 0;
     std::fclose(f);

@@ -179,6 +179,18 @@ struct Plan {
 // host half of gk_plan_build: grouping, work lists and partial-state layout (no device work)
 gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl);
 
+// ---- cost model (plan.cpp) ----------------------------------------------------------
+struct SplitTime {
+  double t;       // predicted levels time of the split launch, us
+  double share;   // a prefix CTA's gather tokens over a gather-only CTA's
+};
+SplitTime split_time(const gk_cost_model& cm, int num_sms, int64_t n_pre, double it, double W, double hbm_us,
+                     bool gather);
+double merge_us(const gk_cost_model& cm, int32_t B, int32_t Hq, int64_t partials);
+// the model's cascade and flat times for a plan (gk_dispatch's predictions)
+void predict_plan(const gk_cost_model& cm, int num_sms, int32_t Hq, const Plan& pl, double* t_dense_us,
+                  double* t_cascade_us);
+
 // ---- status helpers -------------------------------------------------------------
 gk_status fail(Pool* p, gk_status s, const std::string& msg);
 gk_status cuda_fail(Pool* p, int err, const char* what);

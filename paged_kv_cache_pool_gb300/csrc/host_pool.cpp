@@ -264,6 +264,9 @@ gk_status gk_pool_create(const gk_pool_config* cfg, gk_pool** out) {
   cm.warp_group_us = 1.0;
   cm.warp_item_us = 8.0;
   cm.warp_split_ratio = 1.3;
+  cm.prefix_cta_ramp_us = 12.0;
+  cm.prefix_cta_gather_ratio = 1.0;
+  cm.c_merge_state_us = 0.0;
   *out = p;
   return GK_OK;
 }

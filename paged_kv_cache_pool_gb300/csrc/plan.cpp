@@ -25,6 +25,40 @@ constexpr int kMinGatherQuota = 64;
 // gather that keeps HBM busy, and then the other SMs wait for it.
 constexpr double kMinPrefixShare = 0.15;
 
+}  // namespace
+
+// Split launch (one CTA per SM): CTAs [0, n_pre) first run a prefix item of `it`
+// us, and the gather's W SM-us (at a gather-only CTA's rate) are spread over the
+// CTAs so that all end together.  Gather-only CTAs start after c_gather; a prefix
+// CTA starts prefix_cta_ramp after its item and gathers at prefix_cta_gather_ratio
+// of that rate (its first round trips meet an HBM the other SMs keep busy).
+// With gather = false only the gather-only CTAs gather.  hbm_us is the launch's
+// HBM bound.  share = a prefix CTA's tokens over a gather-only CTA's.
+SplitTime split_time(const gk_cost_model& cm, int num_sms, int64_t n_pre, double it, double W, double hbm_us,
+                     bool gather) {
+  SplitTime r{std::max(it, hbm_us), 0.0};
+  if (W <= 0.0) return r;
+  const double cg = cm.c_gather_us, ramp = cm.prefix_cta_ramp_us, e = cm.prefix_cta_gather_ratio;
+  const double n = (double)n_pre, a = (double)(num_sms - n_pre);
+  double T;
+  if (gather && n > 0 && e > 0) {
+    T = (W + a * cg + n * e * (it + ramp)) / (a + n * e);
+    const double busy = T - cg;
+    r.share = busy > 0 ? std::max(0.0, e * (T - it - ramp) / busy) : 0.0;
+  } else {
+    T = a > 0 ? cg + W / a : 1e300;
+  }
+  r.t = std::max(r.t, T);
+  return r;
+}
+
+double merge_us(const gk_cost_model& cm, int32_t B, int32_t Hq, int64_t partials) {
+  if (B <= 0) return 0.0;
+  return cm.c_merge_us * (double)B * Hq + cm.c_merge_state_us * (double)partials / B;
+}
+
+namespace {
+
 template <class T>
 size_t append_region(size_t* off, size_t count, size_t align = 16) {
   size_t o = (*off + align - 1) / align * align;
@@ -149,7 +183,10 @@ int32_t warp_row_groups(const Pool*, const std::vector<std::vector<int32_t>>& me
 
 }  // namespace
 
-gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
+namespace {
+
+// The host plan with prefix items of one kind (GK_PREFIX_TENSOR or GK_PREFIX_WARP).
+gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_kernel kind) {
   const gk_pool_config& c = p->cfg;
   const int32_t B = b->num_requests;
   const int32_t Hkv = c.num_kv_heads, Hq = c.num_q_heads, d = c.head_dim, g = Hq / Hkv;
@@ -286,41 +323,36 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
       t_seq += std::max(prefix_bytes / (cm.bw_prefix_gbs * 1e3), waves * (std::min(c_seq, max_ntiles) * tile + item));
     }
     auto item_us = [&](int32_t C) { return C * tile_split + item; };
-    // the prefix CTAs' gather share (relative to a gather-only CTA) for items of C tiles
-    // in a launch of T us: the time the item leaves, less the ramp of starting a gather
-    auto share_of = [&](int32_t C, double T) { return std::max(0.0, T - item_us(C) - cm.c_gather_us) / T; };
-    auto split_us = [&](int32_t C) {
-      const double it = item_us(C);
-      const double bal = (S / (cm.gather_sm_gbs * 1e3) + (double)n_items(C) * it) / num_sms;
-      return std::max(std::max(it, bal), (S + prefix_bytes) / (cm.bw_suffix_gbs * 1e3));
+    const double W = S / (cm.gather_sm_gbs * 1e3);
+    const double hbm = (S + prefix_bytes) / (cm.bw_suffix_gbs * 1e3);
+    // the split launch for items of C tiles: the prefix CTAs gather a share when it
+    // reaches kMinPrefixShare of a gather-only CTA's, else only the others gather
+    auto split_of = [&](int32_t C, bool* gather) {
+      SplitTime st = split_time(cm, num_sms, n_items(C), item_us(C), W, hbm, true);
+      *gather = st.share >= kMinPrefixShare;
+      if (!*gather) st = split_time(cm, num_sms, n_items(C), item_us(C), W, hbm, false);
+      return st;
     };
     int32_t c_split = 0;
     double t_split = 1e300;
-    int split_pass = 0;
     const bool can_split = G > 0 && suffix_tokens > 0 && p->cascade_mode != GK_CASCADE_SEQUENTIAL;
     if (can_split && p->cascade_mode == GK_CASCADE_SPLIT && p->cascade_tiles > 0) {
       const int32_t C = std::min(p->cascade_tiles, max_ntiles);
       if (n_items(C) <= num_sms) {
+        bool gth;
         c_split = C;
-        t_split = split_us(C);
+        t_split = split_of(C, &gth).t;
       }
     } else {
-      for (int pass = 0; pass < 2 && c_split == 0; ++pass) {
-        // pass 0: only splits that leave the prefix CTAs a gather share of at least
-        // kMinPrefixShare; pass 1 (none such: small steps whose items take about as
-        // long as the whole gather): the best prediction, the prefix CTAs then
-        // gathering nothing unless their share reaches kMinPrefixShare
-        split_pass = pass;
-        for (int32_t C = max_ntiles; can_split && C >= 1; --C) {
-          if (n_items(C) > num_sms) break;  // items only grow as C shrinks
-          const double t = split_us(C);
-          if (pass == 0 && share_of(C, t) < kMinPrefixShare) continue;
-          // the split must leave the gather at least one SM of its own
-          if (pass == 1 && n_items(C) >= num_sms) continue;
-          if (t < t_split - 1e-9) {
-            t_split = t;
-            c_split = C;
-          }
+      for (int32_t C = max_ntiles; can_split && C >= 1; --C) {
+        if (n_items(C) > num_sms) break;  // items only grow as C shrinks
+        bool gth;
+        const double t = split_of(C, &gth).t;
+        // the gather needs an SM of its own unless the prefix CTAs take part
+        if (!gth && n_items(C) >= num_sms) continue;
+        if (t < t_split - 1e-9) {
+          t_split = t;
+          c_split = C;
         }
       }
     }
@@ -328,13 +360,12 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     while (c_split > 1 && n_items(c_split - 1) == n_items(c_split)) --c_split;
     k.split = c_split > 0 && (p->cascade_mode == GK_CASCADE_SPLIT || t_split < t_seq);
     k.c = k.split ? c_split : c_seq;
-    k.t_levels = k.split ? split_us(c_split) : t_seq;
-    // gather weight of a prefix CTA relative to a gather-only CTA (share_of); a
-    // sliver of suffix would cost more in ramp and partial states than it saves
+    k.t_levels = k.split ? t_split : t_seq;
     if (k.split) {
-      const double T = split_us(c_split);
-      k.prefix_cta_share = share_of(c_split, T);
-      if (split_pass == 1 && k.prefix_cta_share < kMinPrefixShare) k.prefix_cta_share = 0.0;
+      bool gth;
+      const SplitTime st = split_of(c_split, &gth);
+      k.t_levels = st.t;
+      k.prefix_cta_share = gth ? st.share : 0.0;
     }
     return k;
   };
@@ -342,16 +373,9 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   // fullest item rounded up to a power of two (its warps split the keys 8 / R ways).
   const int32_t warp_groups = warp_row_groups(p, members, g);
   const double warp_tile = cm.warp_tile_us + warp_groups * cm.warp_group_us;
-  KindPlan kp;
-  if (p->prefix_kernel == GK_PREFIX_WARP) {
-    kp = plan_kind(kPrefixWarpRows, warp_tile, warp_tile * cm.warp_split_ratio, cm.warp_item_us);
-  } else {
-    kp = plan_kind(kPrefixRowsPerCta, cm.prefix_tile_us, cm.prefix_tile_split_us, cm.prefix_item_us);
-    if (p->prefix_kernel == GK_PREFIX_AUTO && G > 0) {
-      KindPlan kw = plan_kind(kPrefixWarpRows, warp_tile, warp_tile * cm.warp_split_ratio, cm.warp_item_us);
-      if (kw.t_levels < kp.t_levels - 1e-9) kp = std::move(kw);
-    }
-  }
+  const KindPlan kp = kind == GK_PREFIX_WARP
+                          ? plan_kind(kPrefixWarpRows, warp_tile, warp_tile * cm.warp_split_ratio, cm.warp_item_us)
+                          : plan_kind(kPrefixRowsPerCta, cm.prefix_tile_us, cm.prefix_tile_split_us, cm.prefix_item_us);
   pl->prefix_kind = kp.rows == kPrefixWarpRows ? 1 : 0;
   pl->split = kp.split;
   const int32_t best_c = kp.c;
@@ -480,6 +504,46 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   sm.prefix_kernel = pl->prefix_kind ? GK_PREFIX_WARP : GK_PREFIX_TENSOR;
   sm.prefix_rows_per_item = kp.rows;
   sm.prefix_row_groups = pl->prefix_kind && G > 0 ? warp_groups : 0;
+  sm.prefix_ctas_gather = pl->split && prefix_cta_share > 0.0 ? 1 : 0;
+  return GK_OK;
+}
+
+}  // namespace
+
+// GK_PREFIX_AUTO plans the step with each kind of prefix item and keeps the one
+// whose whole cascade (levels and merge) the cost model predicts faster, the
+// tensor-core items on a tie: GraniKV Section 3.6's routing between its two
+// prefix kernels, with the measured model in place of the M_sat threshold.
+gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
+  if (p->prefix_kernel != GK_PREFIX_AUTO) return build_host_plan_kind(p, b, pl, p->prefix_kernel);
+  gk_status st = build_host_plan_kind(p, b, pl, GK_PREFIX_TENSOR);
+  if (st != GK_OK || pl->summary.num_groups == 0) return st;
+  Plan w;   // host fields only: no device buffers are made here
+  st = build_host_plan_kind(p, b, &w, GK_PREFIX_WARP);
+  if (st != GK_OK) return st;
+  const int32_t Hq = p->cfg.num_q_heads;
+  double td, t_tensor, t_warp;
+  predict_plan(p->cost, p->dev.num_sms, Hq, *pl, &td, &t_tensor);
+  predict_plan(p->cost, p->dev.num_sms, Hq, w, &td, &t_warp);
+  if (t_warp < t_tensor - 1e-9) {
+    pl->summary = w.summary;
+    pl->groups.swap(w.groups);
+    pl->group_hot_base.swap(w.group_hot_base);
+    pl->prefix_reqs.swap(w.prefix_reqs);
+    pl->prefix_items.swap(w.prefix_items);
+    pl->reqs.swap(w.reqs);
+    pl->suf_seg_begin.swap(w.suf_seg_begin);
+    pl->suf_segs.swap(w.suf_segs);
+    pl->dense_seg_begin.swap(w.dense_seg_begin);
+    pl->dense_segs.swap(w.dense_segs);
+    pl->n_entries_cas = w.n_entries_cas;
+    pl->n_entries_dense = w.n_entries_dense;
+    pl->dense_needs_merge = w.dense_needs_merge;
+    pl->group_bytes.swap(w.group_bytes);
+    pl->group_flops.swap(w.group_flops);
+    pl->split = w.split;
+    pl->prefix_kind = w.prefix_kind;
+  }
   return GK_OK;
 }
 
@@ -591,7 +655,11 @@ static bool valid_cost_model(const gk_cost_model& cm) {
     return false;
   if (!(cm.warp_tile_us > 0 && cm.warp_group_us >= 0 && cm.warp_item_us >= 0 && cm.warp_split_ratio > 0))
     return false;
-  if (!(cm.c_flat_us >= 0 && cm.c_cascade_us >= 0 && cm.c_merge_us >= 0 && cm.c_gather_us >= 0)) return false;
+  if (!(cm.c_flat_us >= 0 && std::isfinite(cm.c_cascade_us) && cm.c_merge_us >= 0 && cm.c_gather_us >= 0))
+    return false;
+  if (!(cm.prefix_cta_ramp_us >= 0 && cm.prefix_cta_gather_ratio > 0 && cm.prefix_cta_gather_ratio <= 1 &&
+        cm.c_merge_state_us >= 0))
+    return false;
   return true;
 }
 
@@ -655,6 +723,36 @@ struct JsonReader {
 
 }  // namespace gk
 
+namespace gk {
+
+void predict_plan(const gk_cost_model& cm, int num_sms, int32_t Hq, const Plan& pl, double* t_dense_us,
+                  double* t_cascade_us) {
+  const gk_plan_summary& sm = pl.summary;
+  *t_dense_us = cm.c_flat_us + (double)sm.dense_bytes / (cm.bw_flat_gbs * 1e3);
+  double t_levels = 0.0;
+  const bool warp = pl.prefix_kind == 1;
+  const double wtile = cm.warp_tile_us + sm.prefix_row_groups * cm.warp_group_us;
+  const double tile = warp ? wtile : cm.prefix_tile_us;
+  const double tile_split = warp ? wtile * cm.warp_split_ratio : cm.prefix_tile_split_us;
+  const double item_fixed = warp ? cm.warp_item_us : cm.prefix_item_us;
+  if (pl.split) {
+    const double it = sm.prefix_ctas > 0 ? sm.prefix_tiles_per_item * tile_split + item_fixed : 0.0;
+    const double W = (double)sm.suffix_bytes / (cm.gather_sm_gbs * 1e3);
+    const double hbm = (double)(sm.suffix_bytes + sm.prefix_bytes) / (cm.bw_suffix_gbs * 1e3);
+    t_levels = split_time(cm, num_sms, sm.prefix_ctas, it, W, hbm, sm.prefix_ctas_gather != 0).t;
+  } else {
+    if (sm.prefix_ctas > 0) {
+      const double item = sm.prefix_tiles_per_item * tile + item_fixed;
+      const double waves = (double)((sm.prefix_ctas + num_sms - 1) / num_sms);
+      t_levels = std::max((double)sm.prefix_bytes / (cm.bw_prefix_gbs * 1e3), waves * item);
+    }
+    if (sm.suffix_bytes > 0) t_levels += cm.c_gather_us + (double)sm.suffix_bytes / (cm.bw_suffix_gbs * 1e3);
+  }
+  *t_cascade_us = std::max(0.0, cm.c_cascade_us + t_levels + merge_us(cm, pl.B, Hq, sm.num_partials));
+}
+
+}  // namespace gk
+
 using gk::Plan;
 using gk::Pool;
 
@@ -715,30 +813,8 @@ gk_status gk_plan_segments(const gk_plan* plan, int32_t dense, int32_t* n_ctas, 
 gk_status gk_dispatch(const gk_pool* pool, const gk_plan* plan, gk_backend* choice, double* t_dense_us,
                       double* t_cascade_us) {
   if (!pool || !plan || !choice) return GK_ERR_INVALID;
-  const gk_cost_model& cm = pool->impl.cost;
-  const Plan& pl = plan->impl;
-  double t_flat = cm.c_flat_us + (double)pl.summary.dense_bytes / (cm.bw_flat_gbs * 1e3);
-  double t_levels = 0.0;
-  const gk_plan_summary& sm = pl.summary;
-  const int num_sms = pool->impl.dev.num_sms;
-  const bool warp = pl.prefix_kind == 1;
-  const double wtile = cm.warp_tile_us + pl.summary.prefix_row_groups * cm.warp_group_us;
-  const double tile = warp ? wtile : cm.prefix_tile_us;
-  const double tile_split = warp ? wtile * cm.warp_split_ratio : cm.prefix_tile_split_us;
-  const double item_fixed = warp ? cm.warp_item_us : cm.prefix_item_us;
-  if (pl.split) {
-    const double item = sm.prefix_tiles_per_item * tile_split + item_fixed;
-    const double bal = ((double)sm.suffix_bytes / (cm.gather_sm_gbs * 1e3) + sm.prefix_ctas * item) / num_sms;
-    t_levels = std::max(std::max(item, bal), (double)(sm.suffix_bytes + sm.prefix_bytes) / (cm.bw_suffix_gbs * 1e3));
-  } else {
-    if (sm.prefix_ctas > 0) {
-      const double item = sm.prefix_tiles_per_item * tile + item_fixed;
-      const double waves = (double)((sm.prefix_ctas + num_sms - 1) / num_sms);
-      t_levels = std::max((double)sm.prefix_bytes / (cm.bw_prefix_gbs * 1e3), waves * item);
-    }
-    t_levels += cm.c_gather_us + (double)sm.suffix_bytes / (cm.bw_suffix_gbs * 1e3);
-  }
-  double t_cas = cm.c_cascade_us + t_levels + cm.c_merge_us * (double)pl.B * pool->impl.cfg.num_q_heads;
+  double t_flat, t_cas;
+  gk::predict_plan(pool->impl.cost, pool->impl.dev.num_sms, pool->impl.cfg.num_q_heads, plan->impl, &t_flat, &t_cas);
   *choice = t_flat < t_cas ? GK_BACKEND_DENSE : GK_BACKEND_CASCADE;
   if (t_dense_us) *t_dense_us = t_flat;
   if (t_cascade_us) *t_cascade_us = t_cas;
@@ -802,7 +878,8 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
                                      "bw_suffix_gbs",  "c_merge_us",     "prefix_tile_us", "prefix_item_us",
                                      "gather_sm_gbs",  "c_gather_us",    "prefix_tile_split_us",
                                      "warp_tile_us",   "warp_group_us",  "warp_item_us",
-                                     "warp_split_ratio"};
+                                     "warp_split_ratio", "prefix_cta_ramp_us", "prefix_cta_gather_ratio",
+                                     "c_merge_state_us"};
     bool known = false;
     for (const char* k : kNumeric) known = known || key == k;
     if (!known) {
@@ -826,6 +903,9 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
     else if (key == "warp_group_us") cm.warp_group_us = v;
     else if (key == "warp_item_us") cm.warp_item_us = v;
     else if (key == "warp_split_ratio") cm.warp_split_ratio = v;
+    else if (key == "prefix_cta_ramp_us") cm.prefix_cta_ramp_us = v;
+    else if (key == "prefix_cta_gather_ratio") cm.prefix_cta_gather_ratio = v;
+    else if (key == "c_merge_state_us") cm.c_merge_state_us = v;
   }
   return gk_cost_model_set(pool, &cm);
 }

@@ -50,7 +50,7 @@ def _suffixes(rng, n):
     return rng.integers(S_RANGE[0], S_RANGE[1] + 1, n).astype(np.int32)
 
 
-def measure(lps=LPS, bs=BS, Hq=32, Hkv=8, d=128, reps=5, seed=7, cost_model=COST_MODEL):
+def measure(lps=LPS, bs=BS, Hq=32, Hkv=8, d=128, reps=7, seed=7, cost_model=COST_MODEL):
     """-> list of per-cell dicts (times in microseconds)."""
     import torch
     from .engine import Engine
@@ -94,19 +94,31 @@ def measure(lps=LPS, bs=BS, Hq=32, Hkv=8, d=128, reps=5, seed=7, cost_model=COST
             out = torch.empty((B, Hq, d), device=eng.device)
             lse = torch.empty((B, Hq), device=eng.device)
             batch.set_device(d_q=q, d_out=out, d_lse=lse)
-            t, pred, arr = {}, {}, {}
+            t, pred, arr, detail = {}, {}, {}, {}
             for kind, kernel in (("tensor", gk.GK_PREFIX_TENSOR), ("warp", gk.GK_PREFIX_WARP)):
                 gk.gk_pool_set_prefix_kernel(pool, kernel)
-                plan = gk.gk_plan_build(pool, batch)
-                info = gk.gk_plan_info(plan)
-                _, p_dense, pred[kind] = gk.gk_dispatch(pool, plan)
-                arr[kind] = dict(split=info["cascade_split"], C=info["prefix_tiles_per_item"],
-                                 n_pre=info["prefix_ctas"], suffix_ctas=info["suffix_ctas"],
-                                 partials=info["num_partials"])
-                t[kind] = timed(lambda: gk.gk_decode_cascade(pool, None, 0, batch, plan))
-                if kind == "tensor":
-                    t["dense"] = timed(lambda: gk.gk_decode_dense(pool, None, 0, batch, plan))
-                gk.gk_plan_destroy(plan)
+                # the planner's arrangement (timed whole, and its levels and merge launches
+                # alone), then the sequential arrangement for the same kind of item
+                for mode, mname in ((gk.GK_CASCADE_AUTO, "auto"), (gk.GK_CASCADE_SEQUENTIAL, "sequential")):
+                    gk.gk_pool_set_cascade_mode(pool, mode, 0)
+                    plan = gk.gk_plan_build(pool, batch)
+                    info = gk.gk_plan_info(plan)
+                    _, p_dense, p_cas = gk.gk_dispatch(pool, plan)
+                    t_cas = timed(lambda: gk.gk_decode_cascade(pool, None, 0, batch, plan))
+                    t_lev = timed(lambda: gk.gk_cascade_levels(pool, None, 0, batch, plan))
+                    t_mrg = timed(lambda: gk.gk_cascade_merge(pool, None, 0, batch, plan))
+                    detail[f"{kind}_{mname}"] = dict(info, t_cascade_us=t_cas, t_levels_us=t_lev, t_merge_us=t_mrg,
+                                                     pred_cascade_us=p_cas)
+                    if mname == "auto":
+                        pred[kind] = p_cas
+                        arr[kind] = dict(split=info["cascade_split"], C=info["prefix_tiles_per_item"],
+                                         n_pre=info["prefix_ctas"], suffix_ctas=info["suffix_ctas"],
+                                         partials=info["num_partials"], gather=info["prefix_ctas_gather"])
+                        t[kind] = t_cas
+                        if kind == "tensor":
+                            t["dense"] = timed(lambda: gk.gk_decode_dense(pool, None, 0, batch, plan))
+                    gk.gk_plan_destroy(plan)
+                gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_AUTO, 0)
             pred["dense"] = p_dense
             gk.gk_pool_set_prefix_kernel(pool, gk.GK_PREFIX_AUTO)
             plan = gk.gk_plan_build(pool, batch)
@@ -120,7 +132,7 @@ def measure(lps=LPS, bs=BS, Hq=32, Hkv=8, d=128, reps=5, seed=7, cost_model=COST
             rows.append(dict(Lp=lp, B=B, M_eff=B * g, suffix_tokens=int(s.sum()),
                              t_dense_us=t["dense"], t_tensor_us=t["tensor"], t_warp_us=t["warp"],
                              pred_dense_us=pred["dense"], pred_tensor_us=pred["tensor"], pred_warp_us=pred["warp"],
-                             plan_tensor=arr["tensor"], plan_warp=arr["warp"],
+                             plan_tensor=arr["tensor"], plan_warp=arr["warp"], plans=detail,
                              pick=pick, fastest=fastest, regret=t[pick] / t[fastest] - 1.0))
             for sq in seqs:
                 eng.seq_release(sq)

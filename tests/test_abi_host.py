@@ -246,7 +246,8 @@ def test_dispatch_matches_oracle_formula(gk, case):
               prefix_tile_split_us=rnd.uniform(0.5, 4.0),
               prefix_item_us=rnd.uniform(0, 20), gather_sm_gbs=rnd.uniform(20, 80), c_gather_us=rnd.uniform(0, 20),
               warp_tile_us=rnd.uniform(0.3, 4.0), warp_group_us=rnd.uniform(0, 0.5), warp_item_us=rnd.uniform(0, 10),
-              warp_split_ratio=rnd.uniform(1.0, 1.6))
+              warp_split_ratio=rnd.uniform(1.0, 1.6), prefix_cta_ramp_us=rnd.uniform(0, 30),
+              prefix_cta_gather_ratio=rnd.uniform(0.3, 1.0), c_merge_state_us=rnd.uniform(0, 2))
     pool = gk.gk_pool_create(1, Hq, Hkv, d, 200000, 64, 1, 0)
     try:
         gk.gk_cost_model_load(pool, json.dumps(cm))
@@ -285,7 +286,9 @@ def test_dispatch_matches_oracle_formula(gk, case):
                 assert s["prefix_ctas"] <= 152 and s["suffix_ctas"] == 152
             else:
                 assert s["suffix_ctas"] == odisp.gather_ctas(sum(slens), 152)
-            wd, wc = odisp.predict(cm, f, dict(split=bool(s["cascade_split"]), C=C, n_pre=s["prefix_ctas"], kind=k))
+            assert s["prefix_ctas_gather"] in ((0, 1) if s["cascade_split"] else (0,))
+            wd, wc = odisp.predict(cm, f, dict(split=bool(s["cascade_split"]), C=C, n_pre=s["prefix_ctas"], kind=k,
+                                               gather=bool(s["prefix_ctas_gather"]), partials=s["num_partials"]))
             assert math.isclose(td, wd, rel_tol=1e-12) and math.isclose(tc, wc, rel_tol=1e-12)
             assert choice == (gk.GK_BACKEND_DENSE if odisp.choose(wd, wc) == "dense" else gk.GK_BACKEND_CASCADE)
             pred[kernel] = tc
@@ -301,29 +304,36 @@ def test_planner_search_worked_by_hand(gk):
     cases worked by hand, with warp-MMA items priced out.
     (1) One group of 64 requests (g = 4 -> one 256-row block per KV head), Lp = 16384 (128
     key tiles), Hkv = 8, 1000 suffix tokens each; tile 1 us (alone and beside the gather),
-    item 5 us, 50 GB/s per SM, 6000 GB/s over every SM, 4 us for a gather launch, 152 SMs.
-    Split: T(C) = max(C + 5, (S / 50 GB/s + items(C) (C + 5)) / 152, (S + P) / 6000 GB/s)
-    with items(C) = 8 ceil(128 / C); HBM binds at 54.875 us from C = 49 down.  A split C must
-    leave its prefix CTAs a gather share (T - item(C) - 4) / T >= 0.15: the 24-item splits
-    (C = 43..49) leave at most 0.05, so the scan from C = 128 down keeps the first 32-item
-    one (C = 37, share 0.16), balanced to 32 tiles (the fewest giving 32 items).  The
-    sequential alternative (C = 7: 152 items in one wave of 12 us, the prefix bound by its
-    67 MB at 5000 GB/s: 13.4 + 4 + 43.7 = 61.1 us) is slower, so the plan splits.
+    item 5 us, 50 GB/s per SM, 6000 GB/s over every SM, 4 us for a gather launch and for a
+    prefix CTA's gather ramp, prefix CTAs gathering at the full rate, 152 SMs.  The gather is
+    W = S / 50 GB/s = 5242.88 SM-us, HBM binds at (S + P) / 6000 GB/s = 54.875 us, and
+    items(C) = 8 ceil(128 / C) of C + 5 us.  With prefix CTAs gathering,
+    T(C) = (W + (152 - n) 4 + n (C + 5 + 4)) / 152 and their share (T - C - 9) / (T - 4);
+    below 0.15 they gather nothing and T(C) = 4 + W / (152 - n).  Scanning from C = 128 down,
+    the 8- and 16-item splits end with their items (C + 5 > 54.875 down to C = 50); C = 49
+    (24 items, share below 0.15, T = 4 + W / 128 = 45.0) is the first at the HBM bound, so it
+    is kept (nothing later is strictly faster) and balanced to C = 43, the fewest tiles giving
+    24 items; its prefix CTAs do not gather.  The sequential alternative (C = 7: 152 items in
+    one wave of 12 us, the prefix bound by its 67 MB at 5000 GB/s: 13.4 + 4 + 43.7 = 61.1 us)
+    is slower, so the plan splits, and T_cascade = 10 + 54.875 + 0.001 * 64 * 32 = 66.923 us.
     (2) 512 requests (M = 2048: eight row blocks per head), sequential, tile 1.557 us, item
     8.63 us: one wave of 128 items of 64 tiles (108.3 us) beats three waves of 448 items of
     19 tiles (114.6 us) and two of 256 items of 32 (117.0 us)."""
     cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0, bw_suffix_gbs=6000.0,
               c_merge_us=0.001, prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0, c_gather_us=4.0,
-              prefix_tile_split_us=1.0, warp_tile_us=1e3, warp_group_us=0.0, warp_item_us=1e3, warp_split_ratio=1.0)
+              prefix_tile_split_us=1.0, warp_tile_us=1e3, warp_group_us=0.0, warp_item_us=1e3, warp_split_ratio=1.0,
+              prefix_cta_ramp_us=4.0, prefix_cta_gather_ratio=1.0, c_merge_state_us=0.0)
     pool = gk.gk_pool_create(1, 32, 8, 128, 16384 + 16, 64, 1, 0)
     try:
         gk.gk_cost_model_load(pool, json.dumps(cm))
         base = gk.gk_prefix_alloc(pool, 16384)
         b, plan = _host_plan(gk, pool, [base] * 64, [16384] * 64, [1000] * 64)
         s = gk.gk_plan_info(plan)
+        t_cas = gk.gk_dispatch(pool, plan)[2]
         gk.gk_plan_destroy(plan)
-        assert (s["cascade_split"], s["prefix_tiles_per_item"], s["prefix_ctas"], s["suffix_ctas"]) == (1, 32, 32, 152)
-        assert s["prefix_kernel"] == gk.GK_PREFIX_TENSOR
+        assert (s["cascade_split"], s["prefix_tiles_per_item"], s["prefix_ctas"], s["suffix_ctas"]) == (1, 43, 24, 152)
+        assert s["prefix_ctas_gather"] == 0 and s["prefix_kernel"] == gk.GK_PREFIX_TENSOR
+        assert math.isclose(t_cas, 10 + (64000 + 16384) * 4096 / 6e3 / 1e3 + 0.001 * 64 * 32, rel_tol=1e-12)
         gk.gk_cost_model_load(pool, json.dumps(dict(cm, prefix_tile_us=1.557, prefix_item_us=8.63)))
         gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SEQUENTIAL)
         b, plan = _host_plan(gk, pool, [base] * 512, [16384] * 512, [100] * 512)

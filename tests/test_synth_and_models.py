@@ -84,7 +84,8 @@ def test_eq2_meff_and_a100_threshold_rows():
 
 CM = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0, bw_suffix_gbs=4000.0,
           c_merge_us=0.001, prefix_tile_us=2.0, prefix_item_us=3.0, gather_sm_gbs=1.0, c_gather_us=4.0,
-          prefix_tile_split_us=2.5, warp_tile_us=0.25, warp_group_us=0.03125, warp_item_us=1.5, warp_split_ratio=1.5)
+          prefix_tile_split_us=2.5, warp_tile_us=0.25, warp_group_us=0.03125, warp_item_us=1.5, warp_split_ratio=1.5,
+          prefix_cta_ramp_us=4.0, prefix_cta_gather_ratio=1.0, c_merge_state_us=0.5)
 
 
 def test_cost_model_closed_form():
@@ -99,17 +100,24 @@ def test_cost_model_closed_form():
     assert dispatch.n_items(f, 1) == 64 and dispatch.n_items(f, 8) == 8 and dispatch.n_items(f, 3) == 24
     assert dispatch.n_items(f, 1, "warp") == 128 and dispatch.n_items(f, 8, "warp") == 16
     # sequential plan, tensor-core items of one tile: one wave of 64 items, each 2 + 3 us
-    t_flat, t_cas = dispatch.predict(cm, f, dict(split=False, C=1, n_pre=64, kind="tensor"))
+    # (8 prefix splits and one suffix segment per request: 576 partial states, 9 a request)
+    t_flat, t_cas = dispatch.predict(cm, f, dict(split=False, C=1, n_pre=64, kind="tensor", gather=False,
+                                                 partials=576))
     assert math.isclose(t_flat, 5.0 + 64 * 1100 * kv / 4e6)
     t_levels = max(1000 * kv / 5e6, 1 * (1 * 2.0 + 3.0)) + 4.0 + 64 * 100 * kv / 4e6
-    assert math.isclose(t_cas, 10.0 + t_levels + 0.001 * 64 * 32)
+    assert math.isclose(t_cas, 10.0 + t_levels + 0.001 * 64 * 32 + 0.5 * 9)
     assert dispatch.choose(t_flat, t_cas) == ("dense" if t_flat < t_cas else "cascade")
     assert dispatch.choose(1.0, 1.0) == "cascade"       # flat only when strictly faster
     # the same with warp items of 4 tiles: 32 items, one wave; the fullest warp item has
     # 128 rows (8 groups of 16), so a tile costs 0.25 + 8 * 0.03125 = 0.5 us: 4 * 0.5 + 1.5
     assert dispatch.warp_row_groups(f) == 8
-    _, t_w = dispatch.predict(cm, f, dict(split=False, C=4, n_pre=32, kind="warp"))
-    assert math.isclose(t_w, 10.0 + max(1000 * kv / 5e6, 3.5) + 4.0 + 64 * 100 * kv / 4e6 + 0.001 * 64 * 32)
+    _, t_w = dispatch.predict(cm, f, dict(split=False, C=4, n_pre=32, kind="warp", gather=False, partials=192))
+    assert math.isclose(t_w, 10.0 + max(1000 * kv / 5e6, 3.5) + 4.0 + 64 * 100 * kv / 4e6 + 0.001 * 64 * 32 + 0.5 * 3)
+    # no suffix: no gather launch in the sequential plan; a negative total counts as zero
+    f0 = dispatch.features([1000] * 64, [0] * 64, [0] * 64, 32, 8, 128)
+    assert math.isclose(dispatch.sequential_levels(cm, f0, 1, 64, 152), max(1000 * kv / 5e6, 5.0))
+    assert dispatch.predict(dict(cm, c_cascade_us=-100.0), f0, dict(split=False, C=1, n_pre=64, kind="tensor",
+                                                                   gather=False, partials=512))[1] == 0.0
     # 200 items over 152 SMs: two waves
     assert math.isclose(dispatch.sequential_levels(cm, f, 2, 200, 152),
                         max(1000 * kv / 5e6, 2 * (2 * 2.0 + 3.0)) + 4.0 + 64 * 100 * kv / 4e6)
@@ -121,21 +129,35 @@ def test_cost_model_closed_form():
 def test_split_formula_worked_example():
     """One group of 64 requests (g = 4 -> one 256-row block), Lp = 16384 (128 key tiles),
     Hkv = 8, 1000 suffix tokens each; tile 1 us, item 5 us, 50 GB/s per SM, 6000 GB/s over
-    every SM, 152 SMs.  T(C) = max(C + 5, (S / 50 GB/s + items * (C + 5)) / 152,
-    (S + prefix bytes) / 6000 GB/s): HBM binds at 54.875 us from C = 49 down (C = 50: 55)."""
+    every SM, 4 us gather ramp for gather-only and for prefix CTAs, 152 SMs.  The gather is
+    W = S / 50 GB/s = 5242.88 SM-us; with n items of C + 5 us whose CTAs gather too,
+    T_gather = (W + (152 - n) 4 + n (C + 5 + 4)) / 152; the levels take
+    max(C + 5, T_gather, (S + prefix bytes) / 6000 GB/s): HBM binds at 54.875 us from
+    C = 49 down (C = 50: 55)."""
     cm = dict(CM, bw_suffix_gbs=6000.0, prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0,
               prefix_tile_split_us=1.0)
     f = dispatch.features([16384] * 64, [1000] * 64, [0] * 64, 32, 8, 128)
     S = 64 * 1000 * 4096
     P = 16384 * 4096
+    W = S / 50e3
     assert f["bytes_suffix"] == S
     assert math.isclose(dispatch.split_levels(cm, f, 50, 24, 152), 55.0)
     assert math.isclose(dispatch.split_levels(cm, f, 49, 24, 152), (S + P) / 6e6)
     # C = 64: 16 items of 69 us; the gather spread over every SM is shorter
     assert math.isclose(dispatch.split_levels(cm, f, 64, 16, 152), 69.0)
-    assert (S / 50e3 + 16 * 69.0) / 152 < 69.0
-    _, t_cas = dispatch.predict(cm, f, dict(split=True, C=32, n_pre=32, kind="tensor"))
-    assert math.isclose(t_cas, 10.0 + (S + P) / 6e6 + 0.001 * 64 * 32)
+    assert (W + 136 * 4 + 16 * 73.0) / 152 < 69.0
+    _, t_cas = dispatch.predict(cm, f, dict(split=True, C=32, n_pre=32, kind="tensor", gather=True, partials=320))
+    assert math.isclose(t_cas, 10.0 + (S + P) / 6e6 + 0.001 * 64 * 32 + 0.5 * 5)
+    # a slow gather binds: 10 GB/s per SM.  Prefix CTAs gathering at the full rate, at half
+    # of it, or not at all (then the 136 others take it all after their 4 us ramp)
+    cm3 = dict(cm, gather_sm_gbs=10.0)
+    W3 = S / 10e3
+    assert math.isclose(dispatch.split_levels(cm3, f, 64, 16, 152), (W3 + 136 * 4 + 16 * 73.0) / 152)
+    assert math.isclose(dispatch.split_levels(dict(cm3, prefix_cta_gather_ratio=0.5), f, 64, 16, 152),
+                        (W3 + 136 * 4 + 16 * 0.5 * 73.0) / (136 + 16 * 0.5))
+    assert math.isclose(dispatch.split_levels(dict(cm3, prefix_cta_ramp_us=20.0), f, 64, 16, 152),
+                        (W3 + 136 * 4 + 16 * 89.0) / 152)
+    assert math.isclose(dispatch.split_levels(cm3, f, 64, 16, 152, gather=False), 4.0 + W3 / 136)
     # a split item runs beside the gather: the split formula takes the split tile time
     # (C = 64: 16 items of 64 * 2 + 5 = 133 us against 69), the sequential one the lone tile
     cm2 = dict(cm, prefix_tile_split_us=2.0)
