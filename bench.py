@@ -179,7 +179,7 @@ class Clocks:
 
 
 # sources of each profiled kernel: a committed ncu summary counts only while they are unchanged
-LEVELS_SRC = ("cascade_split.cu", "prefix_body.cuh", "gather_body.cuh", "device_common.cuh")
+LEVELS_SRC = ("cascade_split.cu", "prefix_body.cuh", "prefix_warp_body.cuh", "gather_body.cuh", "device_common.cuh")
 GATHER_SRC = ("gather_attn.cu", "gather_body.cuh", "device_common.cuh")
 PREFIX_SRC = ("prefix_tc.cu", "prefix_body.cuh", "device_common.cuh")
 

@@ -347,6 +347,12 @@ typedef struct gk_cost_model {
   double prefix_cta_ramp_us;      /* split plans: a prefix CTA starts gathering this long after its item */
   double prefix_cta_gather_ratio; /* ... and gathers at this fraction of a gather-only CTA's rate */
   double c_merge_state_us;        /* merge cost per partial state of a request (a merge warp's round trips) */
+  double prefix_item_split_us;    /* fixed cost of a tensor-core prefix item inside a split launch */
+  double warp_item_split_us;      /* fixed cost of a warp-MMA prefix item inside a split launch */
+  double prefix_item_crowd_us;    /* ... plus this much per prefix item of the launch (their first loads
+                                     contend with each other) */
+  double split_gather_ratio_tensor; /* gather rate in a split launch of tensor-core items, over gather_sm
+                                     (that launch's 320-thread blocks hold the gather to fewer registers) */
 } gk_cost_model;
 
 /* Predict both backends for the plan and pick the smaller:
@@ -356,19 +362,22 @@ typedef struct gk_cost_model {
  * (tile, tile_split, item) = (prefix_tile, prefix_tile_split, prefix_item) for
  * tensor-core items and, for warp-MMA items (gk_plan_summary.prefix_kernel),
  * tile = warp_tile + R * warp_group with R = gk_plan_summary.prefix_row_groups,
- * tile_split = warp_split_ratio * tile and item = warp_item; and
+ * tile_split = warp_split_ratio * tile and item = warp_item; item_split =
+ * (prefix_item_split or warp_item_split) + prefix_item_crowd * prefix_ctas is an
+ * item's fixed cost in a split launch; and
  *   sequential plan (W = ceil(prefix_ctas / SMs) waves of prefix items):
  *     T_levels = max(prefix_bytes / bw_prefix, W * (C * tile + item))
  *                + c_gather + suffix_bytes / bw_suffix
- *   split plan (see gk_plan_summary.cascade_split; it = C * tile_split + item,
+ *   split plan (see gk_plan_summary.cascade_split; it = C * tile_split + item_split,
  *   n = prefix_ctas, A = SMs - n gather-only CTAs, G = suffix_bytes / gather_sm
- *   the gather's SM-time, e = prefix_cta_gather_ratio, r = prefix_cta_ramp):
+ *   the gather's SM-time (gather_sm times split_gather_ratio_tensor for
+ *   tensor-core items), e = prefix_cta_gather_ratio, r = prefix_cta_ramp):
  *     T_gather = (G + A * c_gather + n * e * (it + r)) / (A + n * e)
  *                when the prefix CTAs gather too (gk_plan_summary.prefix_ctas_gather),
- *              = c_gather + G / A otherwise;
+ *              = c_gather + G / A otherwise, and at least c_gather + suffix_bytes / bw_suffix;
  *     T_levels = max(it, T_gather, (suffix_bytes + prefix_bytes) / bw_suffix)
  *   (gather-only CTAs start after c_gather, prefix CTAs r after their items,
- *   and all end together; the last term is HBM).
+ *   and all end together; the gather is held to HBM as a whole, and so is the launch).
  * A plan without prefix work has no prefix term, one without suffix work no
  * gather term.  GraniKV's M_eff (Eq. 2) enters through the items: a group of
  * M_eff stacked rows gives ceil(M_eff / rows per item) items per KV head and key
@@ -463,11 +472,15 @@ gk_status gk_cost_model_get(const gk_pool* pool, gk_cost_model* cm);
  *  - The calibration's own scratch (queries, outputs, tables, 512 MiB to empty
  *    L2) is allocated with cudaMalloc and freed before returning.
  *  - The terms of the split arrangement (prefix_tile_split_us / prefix_tile_us,
- *    warp_split_ratio, prefix_cta_ramp_us, prefix_cta_gather_ratio) and
- *    c_cascade_us are fitted to the whole cascades it times (sequential and
- *    split plans, forced and as the planner arranges them, both prefix kernels):
- *    a grid search for the smallest largest relative error of T_cascade, the
- *    other terms held at their own fits.  c_cascade_us may come out negative
+ *    warp_split_ratio, prefix_item_split_us, warp_item_split_us,
+ *    prefix_item_crowd_us, prefix_cta_ramp_us, prefix_cta_gather_ratio,
+ *    gather_sm_gbs, split_gather_ratio_tensor) and c_cascade_us are fitted to
+ *    the whole cascades it times (sequential and split plans, forced and as the
+ *    planner arranges them, both prefix kernels, a grid of steps with
+ *    16..512-token suffixes, that grid planned again with the first fit): a
+ *    coordinate search over candidate values of each term that minimises the
+ *    largest plus half the mean relative error of T_cascade, the other terms
+ *    held at their own fits.  c_cascade_us may come out negative
  *    (the terms timed alone each carry a launch that the cascade overlaps). */
 gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_out);
 /* Same as gk_cost_model_set from JSON text: {"c_flat_us": .., "bw_flat_gbs": ..,
@@ -475,7 +488,8 @@ gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_out);
  * "prefix_tile_us": .., "prefix_item_us": .., "gather_sm_gbs": .., "c_gather_us": ..,
  * "prefix_tile_split_us": .., "warp_tile_us": .., "warp_group_us": .., "warp_item_us": ..,
  * "warp_split_ratio": .., "prefix_cta_ramp_us": .., "prefix_cta_gather_ratio": ..,
- * "c_merge_state_us": ..}.
+ * "c_merge_state_us": .., "prefix_item_split_us": .., "warp_item_split_us": ..,
+ * "prefix_item_crowd_us": .., "split_gather_ratio_tensor": ..}.
  * Keys left out keep their current values; other keys are skipped. */
 gk_status gk_cost_model_load(gk_pool* pool, const char* json);
 

@@ -10,28 +10,37 @@ predicted time runs (flat wins only when strictly faster):
   T_flat    = c_flat + bytes_flat / bw_flat
   T_cascade = max(0, c_cascade + T_levels + c_merge * B * Hq + c_merge_state * partials / B)
   item(C)   = C * tile + item_fixed          (one prefix work item of C key tiles, alone)
-  item'(C)  = C * tile_split + item_fixed    (the same beside a gather that keeps HBM busy)
+  item'(C)  = C * tile_split + item_split + crowd * n_pre
+                                             (the same inside a split launch, beside a gather
+                                              that keeps HBM busy, among n_pre items whose first
+                                              loads contend)
   T_levels  = max(bytes_pre / bw_prefix, W * item(C)) + c_gather
               + bytes_suffix / bw_suffix                          (sequential plan, W waves)
             = max(item'(C), T_gather, (bytes_suffix + bytes_pre) / bw_suffix)   (split plan)
   T_gather  = (G + A * c_gather + n * e * (item'(C) + r)) / (A + n * e)   (prefix CTAs gather too)
             = c_gather + G / A                                    (only the other CTAs gather)
+              and at least c_gather + bytes_suffix / bw_suffix    (the gather held to HBM)
 with n = n_pre prefix CTAs, A = SMs - n gather-only CTAs, G = bytes_suffix /
-gather_sm the gather's SM-time, r = prefix_cta_ramp_us and e =
+gather_sm the gather's SM-time (gather_sm times split_gather_ratio_tensor in a
+split launch of tensor-core items), r = prefix_cta_ramp_us and e =
 prefix_cta_gather_ratio: gather-only CTAs start after c_gather, a prefix CTA r
 after its item and at e of their rate, and all end together.  A step without
 suffix tokens has no gather term (and no c_gather in the sequential plan).
 
-with (tile, tile_split, item_fixed) the terms of the plan's prefix kernel:
-tensor-core items (prefix_tile_us, prefix_tile_split_us, prefix_item_us; 256
-stacked rows per item) or warp-MMA items (tile = warp_tile_us + R *
-warp_group_us, tile_split = warp_split_ratio * tile, warp_item_us; 128 rows per
-item), the two prefix kernels Section 3.5 pairs.  R = the 16-row groups of the
+with (tile, tile_split, item_fixed, item_split) the terms of the plan's prefix
+kernel: tensor-core items (prefix_tile_us, prefix_tile_split_us, prefix_item_us,
+prefix_item_split_us; 256 stacked rows per item) or warp-MMA items (tile =
+warp_tile_us + R * warp_group_us, tile_split = warp_split_ratio * tile,
+warp_item_us, warp_item_split_us; 128 rows per item), the two prefix kernels
+Section 3.5 pairs, and crowd = prefix_item_crowd_us.  R = the 16-row groups of the
 fullest warp item, rounded up to 1, 2, 4 or 8.
 
 Work decomposition (fixed by the kernels' tiling, not a heuristic): a group of
 M_eff stacked rows and Lp keys contributes ceil(M_eff / rows) row blocks x Hkv
-heads x ceil(ceil(Lp / 128) / C) items.
+heads x ceil(ceil(Lp / 128) / C) key splits.  Each (row block, head, split) is
+one item, except that a tensor-core row block holding at most one 128-row Q tile
+(M_eff mod 256 in 1..128, the group's last block) runs its tiles at about twice
+the rate and so takes two consecutive splits per item: ceil(splits / 2) items.
 
 Parity unpinned: which arrangement a plan takes (split or sequential, the key
 tiles per item C, the prefix kernel, whether its prefix CTAs also gather) is
@@ -48,6 +57,7 @@ from __future__ import annotations
 
 ROWS = {"tensor": 256, "warp": 128}
 KEY_TILE = 128
+Q_TILE = 128        # rows of one tensor-core Q tile (two per tensor-core row block)
 
 
 def m_eff(batch_requests: int, q_per_kv: int) -> int:
@@ -78,10 +88,16 @@ def _ceil(a, b):
 
 
 def n_items(f, C, kind="tensor"):
-    """Prefix work items of a plan with C key tiles per item: every (row block, KV head,
-    key split) of every group once."""
+    """Prefix work items of a plan with C key tiles per split: every (row block, KV head,
+    key split) of every group once, a one-Q-tile tensor-core block's splits two at a time."""
     rows = ROWS[kind]
-    return sum(_ceil(p["M"], rows) * f["Hkv"] * _ceil(_ceil(p["lp"], KEY_TILE), C) for p in f["prefix"])
+    total = 0
+    for p in f["prefix"]:
+        blocks = _ceil(p["M"], rows)
+        splits = _ceil(_ceil(p["lp"], KEY_TILE), C)
+        one = 1 if kind == "tensor" and 0 < p["M"] % rows <= Q_TILE else 0
+        total += (blocks - one) * f["Hkv"] * splits + one * f["Hkv"] * _ceil(splits, 2)
+    return total
 
 
 def gather_ctas(tokens, n):
@@ -109,14 +125,14 @@ def warp_row_groups(f):
 def _terms(cm, kind, R=0):
     if kind == "warp":
         tile = cm["warp_tile_us"] + R * cm["warp_group_us"]
-        return tile, tile * cm["warp_split_ratio"], cm["warp_item_us"]
-    return cm["prefix_tile_us"], cm["prefix_tile_split_us"], cm["prefix_item_us"]
+        return tile, tile * cm["warp_split_ratio"], cm["warp_item_us"], cm["warp_item_split_us"]
+    return cm["prefix_tile_us"], cm["prefix_tile_split_us"], cm["prefix_item_us"], cm["prefix_item_split_us"]
 
 
 def item_us(cm, C, split=False, kind="tensor", R=0):
-    """A prefix item of C key tiles: alone (sequential plans) or beside the gather (split plans)."""
-    tile, tile_split, fixed = _terms(cm, kind, R)
-    return C * (tile_split if split else tile) + fixed
+    """A prefix item of C key tiles: alone (sequential plans) or inside a split launch."""
+    tile, tile_split, fixed, fixed_split = _terms(cm, kind, R)
+    return C * tile_split + fixed_split if split else C * tile + fixed
 
 
 def sequential_levels(cm, f, C, n_pre, num_sms, kind="tensor", R=0):
@@ -129,19 +145,20 @@ def sequential_levels(cm, f, C, n_pre, num_sms, kind="tensor", R=0):
 
 
 def split_levels(cm, f, C, n_pre, num_sms, kind="tensor", R=0, gather=True):
-    it = item_us(cm, C, split=True, kind=kind, R=R) if n_pre else 0.0
+    it = item_us(cm, C, split=True, kind=kind, R=R) + cm["prefix_item_crowd_us"] * n_pre if n_pre else 0.0
     bytes_pre = sum(p["bytes"] for p in f["prefix"])
     t = max(it, (f["bytes_suffix"] + bytes_pre) / (cm["bw_suffix_gbs"] * 1e3))
     if f["bytes_suffix"] == 0:
         return t
-    G = f["bytes_suffix"] / (cm["gather_sm_gbs"] * 1e3)
+    rate = cm["gather_sm_gbs"] * (cm["split_gather_ratio_tensor"] if kind == "tensor" else 1.0)
+    G = f["bytes_suffix"] / (rate * 1e3)
     A = num_sms - n_pre
     e, r, cg = cm["prefix_cta_gather_ratio"], cm["prefix_cta_ramp_us"], cm["c_gather_us"]
     if gather and n_pre:
         t_gather = (G + A * cg + n_pre * e * (it + r)) / (A + n_pre * e)
     else:
         t_gather = cg + G / A
-    return max(t, t_gather)
+    return max(t, t_gather, cg + f["bytes_suffix"] / (cm["bw_suffix_gbs"] * 1e3))
 
 
 def predict(cm, f, plan, num_sms=152):

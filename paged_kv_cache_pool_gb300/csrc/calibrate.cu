@@ -195,14 +195,35 @@ struct Case {
   bool open = false;
 };
 
+// Suffix lengths of a case: s tokens each, or (s < 0) lengths uniform in
+// 16..512 tokens (the pages' user turns) drawn from a generator seeded by -s
+// (splitmix64 increments, the top bits scaled to the range).
+std::vector<int32_t> suffix_lengths(int32_t B, int32_t s) {
+  std::vector<int32_t> out((size_t)B, s);
+  if (s >= 0) return out;
+  uint64_t x = (uint64_t)(-(int64_t)s) * 0x9E3779B97F4A7C15ull;
+  for (auto& v : out) {
+    x += 0x9E3779B97F4A7C15ull;
+    uint64_t z = x;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    v = 16 + (int32_t)((z >> 32) % 497u);
+  }
+  return out;
+}
+
 // false when the pool has no room for the case (it is then skipped) or on an error (c.why set)
 bool open_case(Calib& c, Case& k, int32_t B, int32_t lp, int32_t s) {
   k = Case{};
   k.B = B;
   k.lp = lp;
   k.s = s;
+  const std::vector<int32_t> lens = suffix_lengths(B, s);
   const int32_t P = c.p->cfg.cold_page_size;
-  const int32_t blocks = (s + P - 1) / P;
+  int32_t smax = 0;
+  for (int32_t v : lens) smax = std::max(smax, v);
+  const int32_t blocks = (smax + P - 1) / P;
   if (B > c.max_b || blocks > c.max_blocks) return false;
   if (gk_prefix_alloc(c.pool, lp, &k.hot_base) != GK_OK) return false;
   for (int32_t r = 0; r < B; ++r) {
@@ -212,8 +233,8 @@ bool open_case(Calib& c, Case& k, int32_t B, int32_t lp, int32_t s) {
   }
   k.open = true;
   if ((int32_t)k.seqs.size() < B) return false;
-  std::vector<int32_t> order((size_t)B * s);
-  for (int32_t r = 0; r < B; ++r) std::fill(order.begin() + (size_t)r * s, order.begin() + (size_t)(r + 1) * s, k.seqs[r]);
+  std::vector<int32_t> order;
+  for (int32_t r = 0; r < B; ++r) order.insert(order.end(), (size_t)lens[(size_t)r], k.seqs[(size_t)r]);
   std::vector<int64_t> slots(order.size());
   std::vector<int32_t> cow(2 * order.size() + 2);
   int32_t n_cow = 0, n_done = 0;
@@ -381,29 +402,36 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
     gk::close_case(c, k);
   }
 
-  // (5) steps as the planner arranges them (cascade mode AUTO), each prefix kernel:
-  //     the merge and the whole cascade
-  const int32_t auto_cases[6][3] = {{8, 2048, 256}, {8, 16384, 256}, {32, 8192, 256},
-                                    {128, 512, 256}, {128, 16384, 256}, {512, 4096, 256}};
-  for (auto& ac : auto_cases) {
-    if (!ok) break;
-    if (gk::open_case(c, k, ac[0], ac[1], ac[2])) {
-      for (gk_prefix_kernel kern : {GK_PREFIX_TENSOR, GK_PREFIX_WARP}) {
-        gk_plan* pl = plan_for(k, GK_CASCADE_AUTO, 0, kern);
-        if (!(ok = pl != nullptr)) break;
-        gk_plan_summary sm{};
-        gk_plan_info(pl, &sm);
-        double t;
-        if (!(ok = (t = timed([&] { return gk_cascade_merge(pool, stream, 0, &k.batch, pl); })) >= 0)) break;
-        merge.push_back({(double)k.B * cfg.num_q_heads, (double)sm.num_partials / k.B, t});
-        if (!(ok = (t = timed([&] { return gk_decode_cascade(pool, stream, 0, &k.batch, pl); })) >= 0)) break;
-        cascades.push_back({pl, t});
+  // (5) a grid of steps (Lp x B, suffixes of 16..512 tokens), each prefix kernel,
+  //     arranged by the planner (cascade mode AUTO) and, in the first round,
+  //     sequentially: the merge and the whole cascade.  The second round re-plans
+  //     the grid with the fitted model, whose plans are the ones it will price.
+  auto run_grid = [&](bool sequential_too) {
+    for (int32_t lp : {512, 2048, 8192, 16384})
+      for (int32_t B : {8, 32, 128, 512}) {
+        if (!ok) return;
+        if (gk::open_case(c, k, B, lp, -(lp * 1000 + B))) {
+          for (gk_prefix_kernel kern : {GK_PREFIX_TENSOR, GK_PREFIX_WARP})
+            for (gk_cascade_mode mode : {GK_CASCADE_AUTO, GK_CASCADE_SEQUENTIAL}) {
+              if (!ok) break;
+              if (mode == GK_CASCADE_SEQUENTIAL && !sequential_too) continue;
+              gk_plan* pl = plan_for(k, mode, 0, kern);
+              if (!(ok = pl != nullptr)) break;
+              gk_plan_summary sm{};
+              gk_plan_info(pl, &sm);
+              double t;
+              if (!(ok = (t = timed([&] { return gk_cascade_merge(pool, stream, 0, &k.batch, pl); })) >= 0)) break;
+              merge.push_back({(double)k.B * cfg.num_q_heads, (double)sm.num_partials / k.B, t});
+              if (!(ok = (t = timed([&] { return gk_decode_cascade(pool, stream, 0, &k.batch, pl); })) >= 0)) break;
+              cascades.push_back({pl, t});
+            }
+        } else if (!c.why.empty()) {
+          ok = false;
+        }
+        gk::close_case(c, k);
       }
-    } else if (!c.why.empty()) {
-      ok = false;
-    }
-    gk::close_case(c, k);
-  }
+  };
+  run_grid(true);
 
   // ---- fits ----
   gk_cost_model cm = p->cost;
@@ -461,65 +489,102 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
     }
   }
   // The split arrangement's terms and the cascade's fixed cost, fitted to the whole
-  // cascades: for each point of a grid over (tile ratio of tensor-core items, of
-  // warp items, prefix CTAs' gather ramp, their gather rate), c_cascade minimises
-  // the largest relative error (a convex function of c: ternary search); the grid
-  // point with the smallest such error wins, ties to the smaller mean error.
+  // cascades: tile ratio and fixed cost of an item in a split launch (each kind),
+  // the cost each concurrent item adds to every item's, the prefix CTAs' gather
+  // ramp and rate, the per-SM gather rate (around its own measurement) and its
+  // ratio in tensor-core split launches.  A coordinate search over candidate
+  // values of each term in turn (six passes) minimises the largest plus half the
+  // mean relative error of T_cascade; for each candidate c_cascade minimises the
+  // same (convex in c: ternary search).  Run on the first round's cascades, then,
+  // after the grid is re-planned with that model, on all of them.
   std::vector<std::pair<double, double>> resid;   // (predicted without c_cascade, measured)
-  if (ok && !cascades.empty()) {
+  const gk_cost_model parts = cm;                 // the terms fitted on their own
+  auto fit_cascades = [&]() {
+    if (!ok || cascades.empty()) return;
     const int32_t Hq = cfg.num_q_heads;
-    std::vector<double> pred(cascades.size());
-    auto worst = [&](double cc) {
-      double e = 0;
-      for (size_t i = 0; i < cascades.size(); ++i)
-        e = std::max(e, std::fabs(std::max(0.0, pred[i] + cc) - cascades[i].second) / cascades[i].second);
-      return e;
+    const size_t n = cascades.size();
+    std::vector<double> pred(n);
+    auto score = [&](double cc) {
+      double mx = 0, sum = 0;
+      for (size_t i = 0; i < n; ++i) {
+        const double e = std::fabs(std::max(0.0, pred[i] + cc) - cascades[i].second) / cascades[i].second;
+        mx = std::max(mx, e);
+        sum += e;
+      }
+      return mx + 0.5 * sum / n;
     };
-    double best_e = 1e300, best_mean = 1e300;
-    gk_cost_model best = cm;
-    for (int it_r = 0; it_r <= 12; ++it_r)
-      for (int iw_r = 0; iw_r <= 12; ++iw_r)
-        for (int i_ramp = 0; i_ramp <= 20; ++i_ramp)
-          for (int i_e = 0; i_e <= 4; ++i_e) {
-            gk_cost_model m = cm;
-            m.prefix_tile_split_us = cm.prefix_tile_us * (1.0 + 0.04 * it_r);
-            m.warp_split_ratio = 1.0 + 0.04 * iw_r;
-            m.prefix_cta_ramp_us = 2.0 * i_ramp;
-            m.prefix_cta_gather_ratio = 0.5 + 0.125 * i_e;
-            m.c_cascade_us = 0.0;
-            for (size_t i = 0; i < cascades.size(); ++i) {
-              double td;
-              gk::predict_plan(m, num_sms, Hq, cascades[i].first->impl, &td, &pred[i]);
-            }
-            // no prediction below zero inside the search, so the error is convex in c
-            double lo = -60.0, hi = 60.0;
-            for (double q : pred) lo = std::max(lo, -q);
-            for (int s2 = 0; s2 < 80; ++s2) {
-              const double m1 = lo + (hi - lo) / 3, m2 = hi - (hi - lo) / 3;
-              if (worst(m1) <= worst(m2)) hi = m2; else lo = m1;
-            }
-            const double cc = 0.5 * (lo + hi);
-            const double e = worst(cc);
-            double mean = 0;
-            for (size_t i = 0; i < cascades.size(); ++i)
-              mean += std::fabs(std::max(0.0, pred[i] + cc) - cascades[i].second) / cascades[i].second;
-            mean /= cascades.size();
-            if (e < best_e - 1e-12 || (e < best_e + 1e-12 && mean < best_mean)) {
-              best_e = e;
-              best_mean = mean;
-              best = m;
-              best.c_cascade_us = cc;
-            }
+    // the model's score with its best c_cascade (set in m)
+    auto evaluate = [&](gk_cost_model& m) {
+      m.c_cascade_us = 0.0;
+      for (size_t i = 0; i < n; ++i) {
+        double td;
+        gk::predict_plan(m, num_sms, Hq, cascades[i].first->impl, &td, &pred[i]);
+      }
+      // no prediction below zero inside the search, so the score is convex in c
+      double lo = -60.0, hi = 60.0;
+      for (double q : pred) lo = std::max(lo, -q);
+      for (int s2 = 0; s2 < 50; ++s2) {
+        const double m1 = lo + (hi - lo) / 3, m2 = hi - (hi - lo) / 3;
+        if (score(m1) <= score(m2)) hi = m2; else lo = m1;
+      }
+      m.c_cascade_us = 0.5 * (lo + hi);
+      return score(m.c_cascade_us);
+    };
+    struct Term {
+      double gk_cost_model::*field;
+      std::vector<double> values;
+    };
+    std::vector<Term> terms;
+    auto span = [](double base, double lo, double hi, double step) {
+      std::vector<double> v;
+      for (double x = lo; x <= hi + 1e-9; x += step) v.push_back(std::max(0.0, base + x));
+      return v;
+    };
+    terms.push_back({&gk_cost_model::prefix_tile_split_us, {}});
+    for (double r = 1.0; r <= 1.401; r += 0.05) terms.back().values.push_back(parts.prefix_tile_us * r);
+    terms.push_back({&gk_cost_model::warp_split_ratio, span(0.0, 0.9, 1.4, 0.1)});
+    terms.push_back({&gk_cost_model::prefix_item_split_us, span(parts.prefix_item_us, -4.0, 8.0, 2.0)});
+    terms.push_back({&gk_cost_model::warp_item_split_us, span(parts.warp_item_us, -4.0, 8.0, 2.0)});
+    terms.push_back({&gk_cost_model::prefix_item_crowd_us, span(0.0, 0.0, 0.16, 0.02)});
+    terms.push_back({&gk_cost_model::prefix_cta_ramp_us, span(0.0, 0.0, 40.0, 4.0)});
+    terms.push_back({&gk_cost_model::prefix_cta_gather_ratio, span(0.0, 0.5, 1.0, 0.125)});
+    terms.push_back({&gk_cost_model::gather_sm_gbs, {}});
+    for (double r = 0.8; r <= 1.301; r += 0.1) terms.back().values.push_back(parts.gather_sm_gbs * r);
+    terms.push_back({&gk_cost_model::split_gather_ratio_tensor, span(0.0, 0.5, 1.0, 0.1)});
+    // start from the middle of each range
+    gk_cost_model best = parts;
+    for (auto& t : terms) best.*(t.field) = t.values[t.values.size() / 2];
+    double best_s = evaluate(best);
+    for (int pass = 0; pass < 6; ++pass)
+      for (auto& t : terms)
+        for (double v : t.values) {
+          gk_cost_model m = best;
+          m.*(t.field) = v;
+          const double sc = evaluate(m);
+          if (sc < best_s - 1e-12) {
+            best_s = sc;
+            best = m;
           }
+        }
     cm = best;
+  };
+  fit_cascades();
+  if (ok) {
+    p->cost = cm;          // the second round plans with the fitted model
+    run_grid(false);
+    fit_cascades();
+  }
+  if (ok) {
     gk_cost_model m0 = cm;
     m0.c_cascade_us = 0.0;
     for (auto& pc : cascades) {
       double td, tc;
-      gk::predict_plan(m0, num_sms, Hq, pc.first->impl, &td, &tc);
+      gk::predict_plan(m0, num_sms, cfg.num_q_heads, pc.first->impl, &td, &tc);
       resid.push_back({tc, pc.second});
     }
   }
+  std::vector<gk_plan_summary> cas_plans;        // the timed cascades' plans, for the JSON
+  for (auto& pc : cascades) cas_plans.push_back(pc.first->impl.summary);
   for (gk_plan* pl : plans) gk_plan_destroy(pl);   // after the stream's work (timed calls synchronised)
   c.teardown();
   p->cascade_mode = mode0;
@@ -550,7 +615,10 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
         {"prefix_tile_split_us", cm.prefix_tile_split_us}, {"warp_tile_us", cm.warp_tile_us},
         {"warp_group_us", cm.warp_group_us}, {"warp_item_us", cm.warp_item_us},
         {"warp_split_ratio", cm.warp_split_ratio}, {"prefix_cta_ramp_us", cm.prefix_cta_ramp_us},
-        {"prefix_cta_gather_ratio", cm.prefix_cta_gather_ratio}, {"c_merge_state_us", cm.c_merge_state_us}};
+        {"prefix_cta_gather_ratio", cm.prefix_cta_gather_ratio}, {"c_merge_state_us", cm.c_merge_state_us},
+        {"prefix_item_split_us", cm.prefix_item_split_us}, {"warp_item_split_us", cm.warp_item_split_us},
+        {"prefix_item_crowd_us", cm.prefix_item_crowd_us},
+        {"split_gather_ratio_tensor", cm.split_gather_ratio_tensor}};
     for (auto& t : terms) std::fprintf(f, " \"%s\": %.17g,\n", t.first, t.second);
     std::fprintf(f, " \"geometry\": {\"num_q_heads\": %d, \"num_kv_heads\": %d, \"head_dim\": %d, \"sms\": %d},\n",
                  cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, num_sms);
@@ -572,7 +640,7 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
     std::fprintf(f, "  \"cascade plans (split, prefix CTAs gather, warp items, tiles per item, prefix CTAs, "
                     "row groups, suffix bytes, prefix bytes, partial states, requests, measured us)\": [");
     for (size_t i = 0; i < cascades.size(); ++i) {
-      const gk_plan_summary& q = cascades[i].first->impl.summary;
+      const gk_plan_summary& q = cas_plans[i];
       std::fprintf(f, "%s[%d, %d, %d, %d, %d, %d, %lld, %lld, %d, %d, %.6g]", i ? ", " : "", q.cascade_split,
                    q.prefix_ctas_gather, q.prefix_kernel == GK_PREFIX_WARP ? 1 : 0, q.prefix_tiles_per_item,
                    q.prefix_ctas, q.prefix_row_groups, (long long)q.suffix_bytes, (long long)q.prefix_bytes,

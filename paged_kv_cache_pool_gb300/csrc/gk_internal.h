@@ -121,7 +121,9 @@ struct PrefixItemDev {  // one CTA of the tensor-core prefix kernel
   int32_t group;
   int32_t mblock;      // 256-row block of the stacked Q rows
   int32_t head;
-  int32_t split;
+  int32_t split;       // first key split of the item
+  int32_t splits;      // consecutive key splits it covers (> 1 only for a one-Q-tile row block)
+  int32_t pad0;
 };
 
 struct SegmentDev {     // one contiguous run of one request's tokens inside a gather CTA
@@ -184,8 +186,8 @@ struct SplitTime {
   double t;       // predicted levels time of the split launch, us
   double share;   // a prefix CTA's gather tokens over a gather-only CTA's
 };
-SplitTime split_time(const gk_cost_model& cm, int num_sms, int64_t n_pre, double it, double W, double hbm_us,
-                     bool gather);
+SplitTime split_time(const gk_cost_model& cm, int num_sms, int64_t n_pre, double it, double S, double P,
+                     bool gather, double gather_sm_gbs);
 double merge_us(const gk_cost_model& cm, int32_t B, int32_t Hq, int64_t partials);
 // the model's cascade and flat times for a plan (gk_dispatch's predictions)
 void predict_plan(const gk_cost_model& cm, int num_sms, int32_t Hq, const Plan& pl, double* t_dense_us,

@@ -60,7 +60,9 @@ __global__ void scatter_kernel(uint4* __restrict__ cold_k, uint4* __restrict__ c
 __global__ void hot_slab_write_kernel(uint4* __restrict__ hot_k, uint4* __restrict__ hot_v, int64_t slab_vecs,
                                     int32_t hkv, int32_t d_vecs, int64_t lp, int64_t t0, int64_t n,
                                     const uint4* __restrict__ k, const uint4* __restrict__ v) {
-  griddep_launch_dependents();
+  // No early trigger: the kernel after this one starts only once every slab write
+  // has finished, so the prefix items may fetch HOT tiles before their own
+  // dependency wait (no kernel of a later launch can then overlap a slab write).
   griddep_wait();
   int64_t total = n * hkv * d_vecs;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;

@@ -48,15 +48,19 @@ __device__ __forceinline__ void merge_head(const float* part_o, const float* par
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   float z = 0.f;
   if (mx != -INFINITY) {
+    // a state of weight 0 (LSE -inf: an empty state, whose O row may never have
+    // been written) contributes nothing, whatever its row holds
     auto accumulate = [&](const auto& v, float w, int c) {
       constexpr int N = sizeof(v) / sizeof(float4);
 #pragma unroll
       for (int k = 0; k < N; ++k) {
         const float wk = __shfl_sync(0xffffffffu, w, (c + k) & 31);
-        o.x = fmaf(wk, v[k].x, o.x);
-        o.y = fmaf(wk, v[k].y, o.y);
-        o.z = fmaf(wk, v[k].z, o.z);
-        o.w = fmaf(wk, v[k].w, o.w);
+        if (wk != 0.f) {
+          o.x = fmaf(wk, v[k].x, o.x);
+          o.y = fmaf(wk, v[k].y, o.y);
+          o.z = fmaf(wk, v[k].z, o.z);
+          o.w = fmaf(wk, v[k].w, o.w);
+        }
       }
     };
     for (int eb = 0; eb < ne; eb += 32) {

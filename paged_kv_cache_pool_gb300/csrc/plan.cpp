@@ -28,17 +28,21 @@ constexpr double kMinPrefixShare = 0.15;
 }  // namespace
 
 // Split launch (one CTA per SM): CTAs [0, n_pre) first run a prefix item of `it`
-// us, and the gather's W SM-us (at a gather-only CTA's rate) are spread over the
-// CTAs so that all end together.  Gather-only CTAs start after c_gather; a prefix
-// CTA starts prefix_cta_ramp after its item and gathers at prefix_cta_gather_ratio
-// of that rate (its first round trips meet an HBM the other SMs keep busy).
-// With gather = false only the gather-only CTAs gather.  hbm_us is the launch's
-// HBM bound.  share = a prefix CTA's tokens over a gather-only CTA's.
-SplitTime split_time(const gk_cost_model& cm, int num_sms, int64_t n_pre, double it, double W, double hbm_us,
-                     bool gather) {
-  SplitTime r{std::max(it, hbm_us), 0.0};
-  if (W <= 0.0) return r;
+// us, and the suffix (S bytes; W = S / gather_sm SM-us at a gather-only CTA's
+// rate, gather_sm_gbs for the launch's kind of item) is spread over the CTAs so
+// that all end together.  Gather-only CTAs
+// start after c_gather; a prefix CTA starts prefix_cta_ramp after its item and
+// gathers at prefix_cta_gather_ratio of that rate (its first round trips meet an
+// HBM the other SMs keep busy).  With gather = false only the gather-only CTAs
+// gather.  The gather as a whole takes at least c_gather + S / bw_suffix, and
+// the launch at least (S + P) / bw_suffix (HBM).  share = a prefix CTA's tokens
+// over a gather-only CTA's.
+SplitTime split_time(const gk_cost_model& cm, int num_sms, int64_t n_pre, double it, double S, double P,
+                     bool gather, double gather_sm_gbs) {
+  SplitTime r{std::max(it, (S + P) / (cm.bw_suffix_gbs * 1e3)), 0.0};
+  if (S <= 0.0) return r;
   const double cg = cm.c_gather_us, ramp = cm.prefix_cta_ramp_us, e = cm.prefix_cta_gather_ratio;
+  const double W = S / (gather_sm_gbs * 1e3);
   const double n = (double)n_pre, a = (double)(num_sms - n_pre);
   double T;
   if (gather && n > 0 && e > 0) {
@@ -48,6 +52,7 @@ SplitTime split_time(const gk_cost_model& cm, int num_sms, int64_t n_pre, double
   } else {
     T = a > 0 ? cg + W / a : 1e300;
   }
+  T = std::max(T, cg + S / (cm.bw_suffix_gbs * 1e3));
   r.t = std::max(r.t, T);
   return r;
 }
@@ -267,43 +272,50 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
   // Split arrangement: one launch in which CTA b < n_pre first runs one prefix
   // item of C key tiles, and every CTA (one per SM) gathers a slot of the
   // suffix, a prefix CTA's slot cut to the time its item leaves.  Predicted
-  //   item'(C)  = C * tile_split + item
-  //   T_split   = max(item'(C), (S / gather_sm + n_pre * item'(C)) / SMs,
-  //                   (S + prefix_bytes) / bw_suffix)
-  // (the middle term spreads the gather's SM-time and the items over all SMs;
-  // the last is HBM), against the sequential arrangement's W waves of c_seq-tile
-  // items then the gather as a second launch:
+  //   item'(C)  = C * tile_split + item_split
+  //   T_split   = split_time(): the later of the items and the gather spread over
+  //               the CTAs (gather-only ones from the start, prefix CTAs after their
+  //               items when their share is worth it), held to HBM,
+  // against the sequential arrangement's W waves of c_seq-tile items then the
+  // gather as a second launch:
   //   T_seq = max(prefix_bytes / bw_prefix, W * item(c_seq)) + c_gather + S / bw_suffix.
   // The split is taken when some C is predicted faster than the sequential
   // arrangement; among equal predictions the fewest items (fewest partials)
   // win, and the chosen item count is then spread evenly over the key tiles.
-  // Only C whose prefix CTAs keep at least kMinPrefixShare of a gather-only
-  // CTA's share are considered first; when there is none (small steps, where an
-  // item lasts about as long as the whole gather), the best prediction among the
-  // C that leave the gather an SM of its own is taken, its prefix CTAs then
-  // gathering nothing (one launch and the merge instead of three launches).
+  // Prefix CTAs whose share would fall below kMinPrefixShare of a gather-only
+  // CTA's gather nothing; then the gather needs an SM of its own.
   struct KindPlan {
     int32_t rows = 0;
     std::vector<int32_t> mtiles;
+    std::vector<uint8_t> single;   // the group's last row block fills one Q tile at most
     double tile = 0, tile_split = 0, item = 0;
     bool split = false;
     int32_t c = 0;              // key tiles per item
     double t_levels = 0;        // predicted levels time of the chosen arrangement
     double prefix_cta_share = 1.0;
   };
-  auto plan_kind = [&](int32_t rows, double tile, double tile_split, double item) {
+  auto plan_kind = [&](int32_t rows, double tile, double tile_split, double item, double item_split) {
     KindPlan k;
     k.rows = rows;
     k.tile = tile;
     k.tile_split = tile_split;
     k.item = item;
     k.mtiles.resize((size_t)G);
-    for (int32_t gi = 0; gi < G; ++gi)
-      k.mtiles[(size_t)gi] = ((int32_t)members[(size_t)gi].size() * g + rows - 1) / rows;
+    k.single.assign((size_t)G, 0);
+    for (int32_t gi = 0; gi < G; ++gi) {
+      const int32_t m = (int32_t)members[(size_t)gi].size() * g;
+      k.mtiles[(size_t)gi] = (m + rows - 1) / rows;
+      // a tensor-core row block with one Q tile's rows runs its tiles at about
+      // twice the rate: its items take two key splits each
+      k.single[(size_t)gi] = rows == kPrefixRowsPerCta && m % rows != 0 && m % rows <= kPrefixTileM;
+    }
     auto n_items = [&](int32_t C) {
       int64_t units = 0;
-      for (int32_t gi = 0; gi < G; ++gi)
-        units += (int64_t)k.mtiles[(size_t)gi] * Hkv * ((ntiles[(size_t)gi] + C - 1) / C);
+      for (int32_t gi = 0; gi < G; ++gi) {
+        const int64_t ns = (ntiles[(size_t)gi] + C - 1) / C;
+        const int64_t one = k.single[(size_t)gi];
+        units += ((int64_t)k.mtiles[(size_t)gi] - one) * Hkv * ns + one * Hkv * ((ns + 1) / 2);
+      }
       return units;
     };
     int32_t c_seq = max_ntiles;
@@ -322,15 +334,14 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
       const double waves = (double)((n_items(c_seq) + num_sms - 1) / num_sms);
       t_seq += std::max(prefix_bytes / (cm.bw_prefix_gbs * 1e3), waves * (std::min(c_seq, max_ntiles) * tile + item));
     }
-    auto item_us = [&](int32_t C) { return C * tile_split + item; };
-    const double W = S / (cm.gather_sm_gbs * 1e3);
-    const double hbm = (S + prefix_bytes) / (cm.bw_suffix_gbs * 1e3);
+    auto item_us = [&](int32_t C) { return C * tile_split + item_split + cm.prefix_item_crowd_us * n_items(C); };
     // the split launch for items of C tiles: the prefix CTAs gather a share when it
     // reaches kMinPrefixShare of a gather-only CTA's, else only the others gather
+    const double gsm = rows == kPrefixRowsPerCta ? cm.gather_sm_gbs * cm.split_gather_ratio_tensor : cm.gather_sm_gbs;
     auto split_of = [&](int32_t C, bool* gather) {
-      SplitTime st = split_time(cm, num_sms, n_items(C), item_us(C), W, hbm, true);
+      SplitTime st = split_time(cm, num_sms, n_items(C), item_us(C), S, prefix_bytes, true, gsm);
       *gather = st.share >= kMinPrefixShare;
-      if (!*gather) st = split_time(cm, num_sms, n_items(C), item_us(C), W, hbm, false);
+      if (!*gather) st = split_time(cm, num_sms, n_items(C), item_us(C), S, prefix_bytes, false, gsm);
       return st;
     };
     int32_t c_split = 0;
@@ -374,12 +385,15 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
   const int32_t warp_groups = warp_row_groups(p, members, g);
   const double warp_tile = cm.warp_tile_us + warp_groups * cm.warp_group_us;
   const KindPlan kp = kind == GK_PREFIX_WARP
-                          ? plan_kind(kPrefixWarpRows, warp_tile, warp_tile * cm.warp_split_ratio, cm.warp_item_us)
-                          : plan_kind(kPrefixRowsPerCta, cm.prefix_tile_us, cm.prefix_tile_split_us, cm.prefix_item_us);
+                          ? plan_kind(kPrefixWarpRows, warp_tile, warp_tile * cm.warp_split_ratio, cm.warp_item_us,
+                                      cm.warp_item_split_us)
+                          : plan_kind(kPrefixRowsPerCta, cm.prefix_tile_us, cm.prefix_tile_split_us, cm.prefix_item_us,
+                                      cm.prefix_item_split_us);
   pl->prefix_kind = kp.rows == kPrefixWarpRows ? 1 : 0;
   pl->split = kp.split;
   const int32_t best_c = kp.c;
   const std::vector<int32_t>& mtiles = kp.mtiles;
+  const std::vector<uint8_t>& single = kp.single;
   const double prefix_cta_share = kp.prefix_cta_share;
   int32_t max_m = 0;
   int64_t pre_bytes = 0, pre_flops = 0;
@@ -402,16 +416,23 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
     pre_flops += gf;
   }
   // CTA order: longest splits first; within a length, (group, split, head, row block)
-  // so CTAs reading the same K/V tiles run side by side.
+  // so CTAs reading the same K/V tiles run side by side.  A one-Q-tile row block's
+  // items cover two consecutive splits (the second's entry is left empty).
   struct Item { PrefixItemDev it; int32_t tiles; };
   std::vector<Item> items;
   for (int32_t gi = 0; gi < G; ++gi) {
     const PrefixGroupDev& gd = pl->groups[(size_t)gi];
+    const int32_t last = mtiles[(size_t)gi] - 1;
     for (int32_t s = 0; s < gd.nsplit; ++s) {
-      int32_t t0 = s * gd.split_tiles;
-      int32_t t1 = std::min(ntiles[(size_t)gi], t0 + gd.split_tiles);
       for (int32_t h = 0; h < Hkv; ++h)
-        for (int32_t mt = 0; mt < mtiles[(size_t)gi]; ++mt) items.push_back({PrefixItemDev{gi, mt, h, s}, t1 - t0});
+        for (int32_t mt = 0; mt <= last; ++mt) {
+          const bool pair = single[(size_t)gi] && mt == last;
+          if (pair && s % 2 != 0) continue;
+          const int32_t n = pair ? std::min(2, gd.nsplit - s) : 1;
+          const int32_t t0 = s * gd.split_tiles;
+          const int32_t t1 = std::min(ntiles[(size_t)gi], t0 + n * gd.split_tiles);
+          items.push_back({PrefixItemDev{gi, mt, h, s, n, 0}, t1 - t0});
+        }
     }
   }
   std::stable_sort(items.begin(), items.end(), [](const Item& a, const Item& b2) { return a.tiles > b2.tiles; });
@@ -658,7 +679,8 @@ static bool valid_cost_model(const gk_cost_model& cm) {
   if (!(cm.c_flat_us >= 0 && std::isfinite(cm.c_cascade_us) && cm.c_merge_us >= 0 && cm.c_gather_us >= 0))
     return false;
   if (!(cm.prefix_cta_ramp_us >= 0 && cm.prefix_cta_gather_ratio > 0 && cm.prefix_cta_gather_ratio <= 1 &&
-        cm.c_merge_state_us >= 0))
+        cm.c_merge_state_us >= 0 && cm.prefix_item_split_us >= 0 && cm.warp_item_split_us >= 0 &&
+        cm.prefix_item_crowd_us >= 0 && cm.split_gather_ratio_tensor > 0))
     return false;
   return true;
 }
@@ -735,11 +757,14 @@ void predict_plan(const gk_cost_model& cm, int num_sms, int32_t Hq, const Plan& 
   const double tile = warp ? wtile : cm.prefix_tile_us;
   const double tile_split = warp ? wtile * cm.warp_split_ratio : cm.prefix_tile_split_us;
   const double item_fixed = warp ? cm.warp_item_us : cm.prefix_item_us;
+  const double item_split = warp ? cm.warp_item_split_us : cm.prefix_item_split_us;
   if (pl.split) {
-    const double it = sm.prefix_ctas > 0 ? sm.prefix_tiles_per_item * tile_split + item_fixed : 0.0;
-    const double W = (double)sm.suffix_bytes / (cm.gather_sm_gbs * 1e3);
-    const double hbm = (double)(sm.suffix_bytes + sm.prefix_bytes) / (cm.bw_suffix_gbs * 1e3);
-    t_levels = split_time(cm, num_sms, sm.prefix_ctas, it, W, hbm, sm.prefix_ctas_gather != 0).t;
+    const double it =
+        sm.prefix_ctas > 0 ? sm.prefix_tiles_per_item * tile_split + item_split + cm.prefix_item_crowd_us * sm.prefix_ctas
+                           : 0.0;
+    const double gsm = warp ? cm.gather_sm_gbs : cm.gather_sm_gbs * cm.split_gather_ratio_tensor;
+    t_levels = split_time(cm, num_sms, sm.prefix_ctas, it, (double)sm.suffix_bytes, (double)sm.prefix_bytes,
+                          sm.prefix_ctas_gather != 0, gsm).t;
   } else {
     if (sm.prefix_ctas > 0) {
       const double item = sm.prefix_tiles_per_item * tile + item_fixed;
@@ -879,7 +904,8 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
                                      "gather_sm_gbs",  "c_gather_us",    "prefix_tile_split_us",
                                      "warp_tile_us",   "warp_group_us",  "warp_item_us",
                                      "warp_split_ratio", "prefix_cta_ramp_us", "prefix_cta_gather_ratio",
-                                     "c_merge_state_us"};
+                                     "c_merge_state_us", "prefix_item_split_us", "warp_item_split_us",
+                                     "prefix_item_crowd_us", "split_gather_ratio_tensor"};
     bool known = false;
     for (const char* k : kNumeric) known = known || key == k;
     if (!known) {
@@ -906,6 +932,10 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
     else if (key == "prefix_cta_ramp_us") cm.prefix_cta_ramp_us = v;
     else if (key == "prefix_cta_gather_ratio") cm.prefix_cta_gather_ratio = v;
     else if (key == "c_merge_state_us") cm.c_merge_state_us = v;
+    else if (key == "prefix_item_split_us") cm.prefix_item_split_us = v;
+    else if (key == "warp_item_split_us") cm.warp_item_split_us = v;
+    else if (key == "prefix_item_crowd_us") cm.prefix_item_crowd_us = v;
+    else if (key == "split_gather_ratio_tensor") cm.split_gather_ratio_tensor = v;
   }
   return gk_cost_model_set(pool, &cm);
 }

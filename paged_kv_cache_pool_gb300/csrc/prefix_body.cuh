@@ -25,6 +25,15 @@
 // the output always use the same m, so the result is exact up to rounding.
 // Each item emits a partial state (O normalised, LSE in log2) per row; the merge
 // combines the splits with the suffix states by GraniKV Eq. 1.
+// An item whose rows fit one Q tile (a group's last, partly filled row block)
+// has no second tile to hide its softmax behind; it double-buffers S instead:
+// S(j+2) goes into the buffer P(j) leaves, issued right after PV(j), so the
+// softmax of tile j+1 overlaps PV(j) and S(j+2).  There observing S(j) only
+// proves PV(j-2) finished, so a rescale of O at tile j first waits for PV(j-1)
+// (a barrier committed after every PV).  Such an item may also cover several
+// consecutive key splits of its group (the planner gives it about twice the
+// keys of a full item, as its tiles cost about half): it writes its state to
+// the first split's entry and marks the others empty (LSE -inf).
 //
 // Warp roles (320 threads): warp 0 issues TMA loads (K and V tiles, two
 // stages each), warp 1 owns tensor memory and issues every MMA from one thread,
@@ -78,7 +87,8 @@ enum : int {
   B_SFULL = B_VEMPTY + NST,   // one per Q tile
   B_PFULL = B_SFULL + 2,      // one per Q tile
   B_OFINAL = B_PFULL + 2,
-  B_COUNT = B_OFINAL + 1
+  B_ODONE = B_OFINAL + 1,     // single-tile items: one phase per PV product
+  B_COUNT = B_ODONE + 1
 };
 
 template <int D>
@@ -156,10 +166,10 @@ __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixI
   const PrefixGroupDev gr = p.groups[it.group];
   const int ntiles_all = (gr.lp + BN - 1) / BN;
   const int tile0 = it.split * gr.split_tiles;
-  const int ntiles = min(gr.split_tiles, ntiles_all - tile0);
+  const int ntiles = min(gr.split_tiles * it.splits, ntiles_all - tile0);
   const int key0 = tile0 * BN;
   const int row0 = it.mblock * kPrefixRowsPerCta;
-  const bool two = row0 + BM < gr.m;  // does Q tile 1 hold any row?
+  const bool two = row0 + BM < gr.m;  // does Q tile 1 hold any row?  If not, S is double-buffered
   const void* tmK = p.tmaps + (size_t)gr.tmap_index * 128;
   const void* tmV = p.tmaps + (size_t)(gr.tmap_index + 1) * 128;
   const int zc = p.layer * p.Hkv + it.head;
@@ -189,28 +199,15 @@ __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixI
       mbar_init(bar(B_PFULL + i), 128);
     }
     mbar_init(bar(B_OFINAL), 1);
+    mbar_init(bar(B_ODONE), 1);
     fence_mbar_init();
     if (ntiles > 0) {
       tmap_acquire(tmK);
       tmap_acquire(tmV);
-    }
-  }
-  // Everything above reads only the plan's tables, which the kernels of a step
-  // never write, so it runs while the kernel before this one finishes.  The
-  // queries, the HOT pool (a slab write may precede the decode) and the
-  // partial states (the previous merge reads them) wait for it.
-  griddep_wait();
-  // softmax threads fetch their Q row now, so the global-load latency overlaps the set-up
-  uint4 qrow[D / 8];
-  if (softmax_warp) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)req_ * p.Hq + qh_) * D);
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) qrow[c] = row_valid_ ? src[c] : make_uint4(0, 0, 0, 0);
-  }
-  if (threadIdx.x == 0) {
-    // the first K/V tiles need nothing but the barriers: start them now so their
-    // latency overlaps the Q staging
-    if (ntiles > 0) {
+      // The first K/V tiles need nothing but the barriers and the HOT pool, which no
+      // kernel that may still be running writes (the slab write lets the next
+      // kernel start only once it has finished): start them now, while the kernel
+      // before this one finishes.
       for (int j = 0; j < NST && j < ntiles; ++j) {
         mbar_arrive_expect_tx(bar(B_KFULL + j), Lay::kTile);
         for (int h = 0; h < D / 64; ++h)
@@ -221,6 +218,18 @@ __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixI
       }
     }
   }
+  // Everything above reads only the plan's tables, which the kernels of a step
+  // never write, and the HOT pool, so it runs while the kernel before this one
+  // finishes.  The queries and the partial states (the previous merge reads
+  // them) wait for it.
+  griddep_wait();
+  // softmax threads fetch their Q row now, so the global-load latency overlaps the set-up
+  uint4 qrow[D / 8];
+  if (softmax_warp) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)req_ * p.Hq + qh_) * D);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) qrow[c] = row_valid_ ? src[c] : make_uint4(0, 0, 0, 0);
+  }
   __syncthreads();
   tc_fence_after();
   // columns: S of Q tile i at i*128 (P is written over it); O of Q tile i at 256 + i*128
@@ -229,8 +238,8 @@ __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixI
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------
-    if (lane == 0 && ntiles > NST) {
-      int issued = 2 * NST;
+    if (lane == 0 && ntiles > 0) {
+      int issued = 2 * min(NST, ntiles);   // the first stages, issued before the dependency wait
       for (int j = NST; j < ntiles; ++j) {
         const int st = j % NST, r = j / NST;
         if (!wait_or_abort(bar(B_KEMPTY + st), (r - 1) & 1, p.err, abort_flag)) break;
@@ -265,49 +274,86 @@ __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixI
       const uint32_t tS0 = tmem, tO0 = tmem + 256u;
       bool ok = wait_or_abort(bar0 + 8u * B_QFULL, 0, p.err, abort_flag) &&
                 wait_or_abort(bar0 + 8u * B_KFULL, 0, p.err, abort_flag);
+      // S = Q_i K^T for key tile jt (K stage kst) into TMEM columns dst
+      auto issue_s = [&](uint32_t dst, int i, int kst) {
+        const uint64_t a0 = dQ + ((uint32_t)i * Lay::kQTile >> 4);
+        const uint64_t bk = dK + ((uint32_t)kst * Lay::kTile >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_ss(dst, a0 + (((kk / 4) * kRegionQ + (kk % 4) * 32) >> 4),
+                    bk + (((kk / 4) * kRegionKV + (kk % 4) * 32) >> 4), kIdQK, kk > 0 ? 1u : 0u);
+      };
+      // O_i += P (TMEM columns sbuf) V (V stage vst), accumulating from the first product on
+      auto issue_pv = [&](uint32_t sbuf, uint32_t dO, int vst, bool first) {
+        const uint64_t bv = dV + ((uint32_t)vst * Lay::kTile >> 4);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          tc_mma_ts(dO, sbuf + kk * 8, bv + ((kk * 2048) >> 4), kIdPV, (!first || kk > 0) ? 1u : 0u);
+      };
       if (ok) {
         tc_fence_after();
         for (int i = 0; i < nq; ++i) {
-          const uint64_t a0 = dQ + ((uint32_t)i * Lay::kQTile >> 4);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            tc_mma_ss(tS0 + (uint32_t)i * 128u, a0 + (((kk / 4) * kRegionQ + (kk % 4) * 32) >> 4),
-                      dK + (((kk / 4) * kRegionKV + (kk % 4) * 32) >> 4), kIdQK, kk > 0 ? 1u : 0u);
+          issue_s(tS0 + (uint32_t)i * 128u, i, 0);
           tc_commit(bar0 + 8u * (B_SFULL + i));
         }
         tc_commit(bar0 + 8u * B_KEMPTY);
-      }
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int st = j % NST;
-        const int jn = j + 1;
-        const bool more = jn < ntiles;
-        const int stn = jn % NST;
-        if (!wait_or_abort(bar0 + 8u * (B_VFULL + st), (j / NST) & 1, p.err, abort_flag)) { ok = false; break; }
-        const uint64_t bv = dV + ((uint32_t)st * Lay::kTile >> 4);
-        const uint64_t bk = dK + ((uint32_t)stn * Lay::kTile >> 4);
-        for (int i = 0; i < nq; ++i) {
-          if (!wait_or_abort(bar0 + 8u * (B_PFULL + i), j & 1, p.err, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          // O_i += P_i(j) V_j with P_i(j) as the TMEM A operand ...
-          const uint32_t sbuf = tS0 + (uint32_t)i * 128u;
-          const uint32_t dO = tO0 + (uint32_t)i * 128u;
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            tc_mma_ts(dO, sbuf + kk * 8, bv + ((kk * 2048) >> 4), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
-          // ... then S_i(j+1) over it (in-order completion)
-          if (more) {
-            if (i == 0 && !wait_or_abort(bar0 + 8u * (B_KFULL + stn), (jn / NST) & 1, p.err, abort_flag)) { ok = false; break; }
-            const uint64_t a0 = dQ + ((uint32_t)i * Lay::kQTile >> 4);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              tc_mma_ss(sbuf, a0 + (((kk / 4) * kRegionQ + (kk % 4) * 32) >> 4),
-                        bk + (((kk / 4) * kRegionKV + (kk % 4) * 32) >> 4), kIdQK, kk > 0 ? 1u : 0u);
-            tc_commit(bar0 + 8u * (B_SFULL + i));
+        if (!two && ntiles > 1) {
+          // single tile: S(1) into the second buffer
+          ok = wait_or_abort(bar0 + 8u * (B_KFULL + 1), 0, p.err, abort_flag);
+          if (ok) {
+            tc_fence_after();
+            issue_s(tS0 + 128u, 0, 1);
+            tc_commit(bar0 + 8u * (B_SFULL + 1));
+            tc_commit(bar0 + 8u * (B_KEMPTY + 1));
           }
         }
-        if (!ok) break;
-        tc_commit(bar0 + 8u * (B_VEMPTY + st));
-        if (more) tc_commit(bar0 + 8u * (B_KEMPTY + stn));
+      }
+      if (two) {
+        // PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
+        for (int j = 0; ok && j < ntiles; ++j) {
+          const int st = j % NST;
+          const int jn = j + 1;
+          const bool more = jn < ntiles;
+          const int stn = jn % NST;
+          if (!wait_or_abort(bar0 + 8u * (B_VFULL + st), (j / NST) & 1, p.err, abort_flag)) { ok = false; break; }
+          for (int i = 0; i < nq; ++i) {
+            if (!wait_or_abort(bar0 + 8u * (B_PFULL + i), j & 1, p.err, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            // O_i += P_i(j) V_j with P_i(j) as the TMEM A operand ...
+            const uint32_t sbuf = tS0 + (uint32_t)i * 128u;
+            issue_pv(sbuf, tO0 + (uint32_t)i * 128u, st, j == 0);
+            // ... then S_i(j+1) over it (in-order completion)
+            if (more) {
+              if (i == 0 && !wait_or_abort(bar0 + 8u * (B_KFULL + stn), (jn / NST) & 1, p.err, abort_flag)) { ok = false; break; }
+              issue_s(sbuf, i, stn);
+              tc_commit(bar0 + 8u * (B_SFULL + i));
+            }
+          }
+          if (!ok) break;
+          tc_commit(bar0 + 8u * (B_VEMPTY + st));
+          if (more) tc_commit(bar0 + 8u * (B_KEMPTY + stn));
+        }
+      } else {
+        // one Q tile, S in two buffers: PV(j) from buffer j & 1, then S(j+2) into it
+        for (int j = 0; ok && j < ntiles; ++j) {
+          const int st = j % NST;
+          const int b = j & 1;
+          if (!wait_or_abort(bar0 + 8u * (B_VFULL + st), (j / NST) & 1, p.err, abort_flag)) { ok = false; break; }
+          if (!wait_or_abort(bar0 + 8u * (B_PFULL + b), (j >> 1) & 1, p.err, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sbuf = tS0 + (uint32_t)b * 128u;
+          issue_pv(sbuf, tO0, st, j == 0);
+          tc_commit(bar0 + 8u * (B_VEMPTY + st));
+          tc_commit(bar0 + 8u * B_ODONE);
+          const int jn = j + 2;
+          if (jn < ntiles) {
+            const int stn = jn % NST;
+            if (!wait_or_abort(bar0 + 8u * (B_KFULL + stn), (jn / NST) & 1, p.err, abort_flag)) { ok = false; break; }
+            issue_s(sbuf, 0, stn);
+            tc_commit(bar0 + 8u * (B_SFULL + b));
+            tc_commit(bar0 + 8u * (B_KEMPTY + stn));
+          }
+        }
       }
       // every MMA issued above has finished before the epilogue reads O and TMEM is released
       tc_commit(bar0 + 8u * B_OFINAL);
@@ -334,11 +380,15 @@ __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixI
     float m_used = -INFINITY, l = 0.f;
     bool ok = active;
     for (int j = 0; ok && j < ntiles; ++j) {
-      if (!wait_or_abort(bar(B_SFULL + qi), j & 1, p.err, abort_flag)) { ok = false; break; }
+      // S buffer of this tile: the Q tile's own, or (one Q tile) alternating
+      const int sb = two ? qi : (j & 1);
+      const uint32_t sph = two ? (uint32_t)(j & 1) : (uint32_t)((j >> 1) & 1);
+      // warp-uniform: a lane that gave up takes its whole warp out of the loop
+      if (!__all_sync(0xffffffffu, wait_or_abort(bar(B_SFULL + sb), sph, p.err, abort_flag))) { ok = false; break; }
       tc_fence_after();
       float s[BN];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS(qi) + c * 32 + lane_off, s + c * 32);
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS(sb) + c * 32 + lane_off, s + c * 32);
       tc_wait_ld();
       const int nvalid = gr.lp - (key0 + j * BN);
       if (nvalid < BN) {
@@ -360,7 +410,15 @@ __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixI
       if (__any_sync(0xffffffffu, mx > m_used + 8.0f)) {
         const float m_new = fmaxf(m_used, mx);
         if (j > 0) {
-          // S(j) completed after PV(j-1): O holds keys 0..j-1 scaled by 2^-m_used
+          // two Q tiles: S(j) completed after PV(j-1), so O holds keys 0..j-1 scaled by
+          // 2^-m_used; one Q tile: S(j) only follows PV(j-2), so wait for PV(j-1)
+          if (!two) {
+            if (!__all_sync(0xffffffffu, wait_or_abort(bar(B_ODONE), (uint32_t)((j - 1) & 1), p.err, abort_flag))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
           const float f = ex2(m_used - m_new);
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
@@ -397,10 +455,10 @@ __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixI
       }
       // P over S in TMEM (packed bf16 pairs, key 2c in the low half of column c)
 #pragma unroll
-      for (int c = 0; c < BN / 64; ++c) tmem_st32(tS(qi) + c * 32 + lane_off, reinterpret_cast<const float*>(pk + c * 32));
+      for (int c = 0; c < BN / 64; ++c) tmem_st32(tS(sb) + c * 32 + lane_off, reinterpret_cast<const float*>(pk + c * 32));
       tc_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(B_PFULL + qi));
+      mbar_arrive(bar(B_PFULL + sb));
     }
     if (ok && wait_or_abort(bar(B_OFINAL), 0, p.err, abort_flag)) {
       // Every MMA has finished, so the Q/K/V staging area is free: each thread
@@ -416,6 +474,8 @@ __device__ __forceinline__ bool prefix_item(const PrefixParams& p, const PrefixI
         if (row_valid) {
           dst = p.part_o + (entry_ * p.Hq + qh) * D;
           p.part_l[entry_ * p.Hq + qh] = m_used + __log2f(l);
+          // the further key splits this item covered hold empty states (weight 0)
+          for (int k = 1; k < it.splits; ++k) p.part_l[(entry_ + k) * p.Hq + qh] = -INFINITY;
         }
         asm volatile("st.shared.u64 [%0], %1;" ::"r"(dst_tab + row * 8), "l"((uint64_t)dst) : "memory");
       }

@@ -241,9 +241,11 @@ __device__ __forceinline__ bool warp_item(const prefix::PrefixParams& p, const P
       tmap_acquire(tmV);
     }
   }
-  // The plan's tables above are never written by a step's kernels; the
-  // queries, the HOT pool and the partial states wait for the kernel before.
-  griddep_wait();
+  // The first K/V stages read only the HOT pool, which no kernel that may still
+  // be running writes (the slab write lets the next kernel start only once it
+  // has finished): they start before the dependency wait.  The plan's tables are
+  // never written by a step's kernels; the queries and the partial states wait
+  // for the kernel before.
   int issued = 0;
   if (threadIdx.x == kProducerThread && nact > 0) {
     for (int j = 0; j < NST && j < ntiles; ++j) {
@@ -256,6 +258,7 @@ __device__ __forceinline__ bool warp_item(const prefix::PrefixParams& p, const P
       issued = j + 1;
     }
   }
+  griddep_wait();
   // Row group w's 16 query rows into shared memory by warp w (128-byte swizzled
   // like the K tiles, so the ldmatrix reads of the A fragments are conflict
   // free); rows past M_eff are zero.

@@ -12,7 +12,9 @@ Each case is shaped so that every branch of the tensor-core prefix item runs:
   * queries as drawn and scaled by 8 (a peaked softmax, whose running maximum
     grows across tiles and takes the lazy-rescale branch).
 Each plan runs with both prefix kernels: tensor-core items (256 rows: the first
-row block has both Q tiles live, the second only its first) and warp-MMA items
+row block has both Q tiles live, the second only its first, so its items run S
+double-buffered, take two key splits each where there are two and leave the
+second's entry empty; at g = 5 a request straddles the two blocks) and warp-MMA items
 (128 rows: the third row block has 44 rows, so its last live warp is partly
 empty and five warps sit out).  Suffixes run from 0 tokens up (an empty side
 merges to the other).  Both backends are held to the fp64 oracle at
@@ -93,9 +95,12 @@ def test_every_geometry_both_backends(d, g, peaked):
                 info = gk.gk_plan_info(pl)
                 assert info["prefix_kernel"] == kernel and info["prefix_rows_per_item"] == rows
                 if name.startswith("split-"):
-                    # the forced plans: row blocks x KV heads x key splits of `tiles` tiles
+                    # the forced plans: row blocks x KV heads x key splits of `tiles` tiles, the
+                    # last tensor-core block (44-48 rows: one Q tile) taking two splits per item
                     assert info["cascade_split"] == 1 and info["prefix_tiles_per_item"] == tiles
-                    assert info["prefix_ctas"] == -(-w.B * g // rows) * w.Hkv * (4 // tiles)
+                    full = w.B * g // rows
+                    last = 0 if w.B * g % rows == 0 else (-(-(4 // tiles) // 2) if kname == "tensor" else 4 // tiles)
+                    assert info["prefix_ctas"] == (full * (4 // tiles) + last) * w.Hkv
                 seen_splits.add(info["cascade_split"])
                 q = gw.q(0)
                 O1, L1 = _decode(gw, b, pl, q, staged=False)

@@ -85,7 +85,8 @@ def test_eq2_meff_and_a100_threshold_rows():
 CM = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0, bw_suffix_gbs=4000.0,
           c_merge_us=0.001, prefix_tile_us=2.0, prefix_item_us=3.0, gather_sm_gbs=1.0, c_gather_us=4.0,
           prefix_tile_split_us=2.5, warp_tile_us=0.25, warp_group_us=0.03125, warp_item_us=1.5, warp_split_ratio=1.5,
-          prefix_cta_ramp_us=4.0, prefix_cta_gather_ratio=1.0, c_merge_state_us=0.5)
+          prefix_cta_ramp_us=4.0, prefix_cta_gather_ratio=1.0, c_merge_state_us=0.5, prefix_item_split_us=3.0,
+          warp_item_split_us=1.5, prefix_item_crowd_us=0.0, split_gather_ratio_tensor=1.0)
 
 
 def test_cost_model_closed_form():
@@ -99,6 +100,15 @@ def test_cost_model_closed_form():
     # work decomposition: row blocks x KV heads x key splits
     assert dispatch.n_items(f, 1) == 64 and dispatch.n_items(f, 8) == 8 and dispatch.n_items(f, 3) == 24
     assert dispatch.n_items(f, 1, "warp") == 128 and dispatch.n_items(f, 8, "warp") == 16
+    # a last row block of one Q tile (M = 384: 256 + 128 rows; M = 640 at g = 5: 2 x 256 + 128)
+    # takes two splits per item: 8 heads x (8 + 4) at C = 1, x (3 + 2) at C = 3; at M = 420 the
+    # last block (164 rows) needs both Q tiles and is a full one
+    f384 = dispatch.features([1000] * 96, [100] * 96, [0] * 96, 32, 8, 128)
+    assert dispatch.n_items(f384, 1) == 8 * (8 + 4) and dispatch.n_items(f384, 3) == 8 * (3 + 2)
+    f640 = dispatch.features([1000] * 128, [100] * 128, [0] * 128, 40, 8, 128)
+    assert f640["prefix"][0]["M"] == 640 and dispatch.n_items(f640, 1) == 8 * (2 * 8 + 4)
+    f420 = dispatch.features([1000] * 84, [100] * 84, [0] * 84, 40, 8, 128)
+    assert dispatch.n_items(f420, 1) == 8 * 2 * 8 and dispatch.n_items(f384, 1, "warp") == 3 * 8 * 8
     # sequential plan, tensor-core items of one tile: one wave of 64 items, each 2 + 3 us
     # (8 prefix splits and one suffix segment per request: 576 partial states, 9 a request)
     t_flat, t_cas = dispatch.predict(cm, f, dict(split=False, C=1, n_pre=64, kind="tensor", gather=False,
@@ -135,7 +145,7 @@ def test_split_formula_worked_example():
     max(C + 5, T_gather, (S + prefix bytes) / 6000 GB/s): HBM binds at 54.875 us from
     C = 49 down (C = 50: 55)."""
     cm = dict(CM, bw_suffix_gbs=6000.0, prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0,
-              prefix_tile_split_us=1.0)
+              prefix_tile_split_us=1.0, prefix_item_split_us=5.0)
     f = dispatch.features([16384] * 64, [1000] * 64, [0] * 64, 32, 8, 128)
     S = 64 * 1000 * 4096
     P = 16384 * 4096
@@ -158,15 +168,31 @@ def test_split_formula_worked_example():
     assert math.isclose(dispatch.split_levels(dict(cm3, prefix_cta_ramp_us=20.0), f, 64, 16, 152),
                         (W3 + 136 * 4 + 16 * 89.0) / 152)
     assert math.isclose(dispatch.split_levels(cm3, f, 64, 16, 152, gather=False), 4.0 + W3 / 136)
-    # a split item runs beside the gather: the split formula takes the split tile time
-    # (C = 64: 16 items of 64 * 2 + 5 = 133 us against 69), the sequential one the lone tile
-    cm2 = dict(cm, prefix_tile_split_us=2.0)
-    assert math.isclose(dispatch.split_levels(cm2, f, 64, 16, 152), 133.0)
+    # a split launch of tensor-core items gathers at split_gather_ratio_tensor of the rate;
+    # one of warp items at the full rate
+    assert math.isclose(dispatch.split_levels(dict(cm3, split_gather_ratio_tensor=0.5), f, 64, 16, 152, gather=False),
+                        4.0 + 2 * W3 / 136)
+    assert math.isclose(dispatch.split_levels(dict(cm3, split_gather_ratio_tensor=0.5, warp_item_split_us=5.0), f, 64,
+                                              16, 152, "warp", R=1, gather=False), 4.0 + W3 / 136)
+    # each item of a split launch pays prefix_item_crowd_us per item of the launch
+    assert math.isclose(dispatch.split_levels(dict(cm, prefix_item_crowd_us=0.5), f, 64, 16, 152), 69.0 + 8.0)
+    # a split item runs beside the gather: the split formula takes the split tile time and
+    # the split item's fixed cost (C = 64: 16 items of 64 * 2 + 7 = 135 us against 69), the
+    # sequential one the lone tile and the lone item (7 * 1 + 5)
+    cm2 = dict(cm, prefix_tile_split_us=2.0, prefix_item_split_us=7.0)
+    assert math.isclose(dispatch.split_levels(cm2, f, 64, 16, 152), 135.0)
     t_seq = max(P / 5e6, 7 * 1.0 + 5.0) + 4.0 + S / 6e6
     assert math.isclose(dispatch.sequential_levels(cm2, f, 7, 152, 152), t_seq)
+    # the gather as a whole is held to HBM: at 1000 GB/s over every SM the 262 MB take
+    # 4 + 262.1 us even though the SMs' own rate would finish them sooner
+    cm4 = dict(cm, bw_suffix_gbs=1000.0)
+    assert math.isclose(dispatch.split_levels(cm4, f, 64, 16, 152), (S + P) / 1e6)
+    assert math.isclose(dispatch.split_levels(cm4, f, 64, 16, 152, gather=False), (S + P) / 1e6)
+    assert math.isclose(dispatch.split_levels(dict(cm4, c_gather_us=80.0), f, 64, 16, 152), 80.0 + S / 1e6)
     # warp-MMA items take their own terms: 2 row blocks x 8 heads x 4 splits of 32 tiles,
     # a tile beside the gather 1.5 * (1 + 8 * 0.125) = 3 us: item 32 * 3 + 2 = 98 us
-    cmw = dict(cm, warp_tile_us=1.0, warp_group_us=0.125, warp_split_ratio=1.5, warp_item_us=2.0)
+    cmw = dict(cm, warp_tile_us=1.0, warp_group_us=0.125, warp_split_ratio=1.5, warp_item_us=9.0,
+               warp_item_split_us=2.0)
     assert dispatch.n_items(f, 32, "warp") == 64
     assert math.isclose(dispatch.split_levels(cmw, f, 32, 64, 152, "warp", R=8), 98.0)
     # R rounds the fullest item's 16-row groups up to a power of two
