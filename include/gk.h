@@ -353,6 +353,8 @@ typedef struct gk_cost_model {
                                      contend with each other) */
   double split_gather_ratio_tensor; /* gather rate in a split launch of tensor-core items, over gather_sm
                                      (that launch's 320-thread blocks hold the gather to fewer registers) */
+  double c_gather_split_us;       /* fixed cost of the gather inside a split launch: when its gather-only
+                                     CTAs start (c_gather_us is the stand-alone gather launch's) */
 } gk_cost_model;
 
 /* Predict both backends for the plan and pick the smaller:
@@ -456,8 +458,8 @@ gk_status gk_cost_model_get(const gk_pool* pool, gk_cost_model* cm);
  * key-tile counts (warp items with 1, 2 and 8 groups of 16 rows), the gather
  * beside long items, and whole cascades, on layer 0 of this pool with a
  * synthetic batch of one shared prefix; fits each gk_cost_model term by least
- * squares (the cascade's fixed cost is the mean residual of the whole cascades
- * under gk_dispatch); installs the model in the pool; and, if json_out is not
+ * squares (the flat backend's and the suffix gather's terms by relative error,
+ * so that the smallest steps count as much as the largest); installs the model in the pool; and, if json_out is not
  * NULL, writes it to that file in gk_cost_model_load's format with the
  * measured points under "measured".  Blocking; a few seconds.
  *  - The pool needs device storage; its K/V contents are read as they are (the
@@ -474,8 +476,8 @@ gk_status gk_cost_model_get(const gk_pool* pool, gk_cost_model* cm);
  *  - The terms of the split arrangement (prefix_tile_split_us / prefix_tile_us,
  *    warp_split_ratio, prefix_item_split_us, warp_item_split_us,
  *    prefix_item_crowd_us, prefix_cta_ramp_us, prefix_cta_gather_ratio,
- *    gather_sm_gbs, split_gather_ratio_tensor) and c_cascade_us are fitted to
- *    the whole cascades it times (sequential and split plans, forced and as the
+ *    gather_sm_gbs, split_gather_ratio_tensor, c_gather_split_us) and c_cascade_us
+ *    are fitted to the whole cascades it times (sequential and split plans, forced and as the
  *    planner arranges them, both prefix kernels, a grid of steps with
  *    16..512-token suffixes, that grid planned again with the first fit): a
  *    coordinate search over candidate values of each term that minimises the
@@ -489,7 +491,7 @@ gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_out);
  * "prefix_tile_split_us": .., "warp_tile_us": .., "warp_group_us": .., "warp_item_us": ..,
  * "warp_split_ratio": .., "prefix_cta_ramp_us": .., "prefix_cta_gather_ratio": ..,
  * "c_merge_state_us": .., "prefix_item_split_us": .., "warp_item_split_us": ..,
- * "prefix_item_crowd_us": .., "split_gather_ratio_tensor": ..}.
+ * "prefix_item_crowd_us": .., "split_gather_ratio_tensor": .., "c_gather_split_us": ..}.
  * Keys left out keep their current values; other keys are skipped. */
 gk_status gk_cost_model_load(gk_pool* pool, const char* json);
 

@@ -17,14 +17,15 @@ predicted time runs (flat wins only when strictly faster):
   T_levels  = max(bytes_pre / bw_prefix, W * item(C)) + c_gather
               + bytes_suffix / bw_suffix                          (sequential plan, W waves)
             = max(item'(C), T_gather, (bytes_suffix + bytes_pre) / bw_suffix)   (split plan)
-  T_gather  = (G + A * c_gather + n * e * (item'(C) + r)) / (A + n * e)   (prefix CTAs gather too)
-            = c_gather + G / A                                    (only the other CTAs gather)
-              and at least c_gather + bytes_suffix / bw_suffix    (the gather held to HBM)
+  T_gather  = (G + A * c_gs + n * e * (item'(C) + r)) / (A + n * e)   (prefix CTAs gather too)
+            = c_gs + G / A                                        (only the other CTAs gather)
+              and at least c_gs + bytes_suffix / bw_suffix        (the gather held to HBM)
 with n = n_pre prefix CTAs, A = SMs - n gather-only CTAs, G = bytes_suffix /
 gather_sm the gather's SM-time (gather_sm times split_gather_ratio_tensor in a
 split launch of tensor-core items), r = prefix_cta_ramp_us and e =
-prefix_cta_gather_ratio: gather-only CTAs start after c_gather, a prefix CTA r
-after its item and at e of their rate, and all end together.  A step without
+prefix_cta_gather_ratio: gather-only CTAs start after c_gs = c_gather_split_us (the
+split launch's own fixed cost; c_gather_us is the stand-alone gather launch's), a
+prefix CTA r after its item and at e of their rate, and all end together.  A step without
 suffix tokens has no gather term (and no c_gather in the sequential plan).
 
 with (tile, tile_split, item_fixed, item_split) the terms of the plan's prefix
@@ -153,7 +154,7 @@ def split_levels(cm, f, C, n_pre, num_sms, kind="tensor", R=0, gather=True):
     rate = cm["gather_sm_gbs"] * (cm["split_gather_ratio_tensor"] if kind == "tensor" else 1.0)
     G = f["bytes_suffix"] / (rate * 1e3)
     A = num_sms - n_pre
-    e, r, cg = cm["prefix_cta_gather_ratio"], cm["prefix_cta_ramp_us"], cm["c_gather_us"]
+    e, r, cg = cm["prefix_cta_gather_ratio"], cm["prefix_cta_ramp_us"], cm["c_gather_split_us"]
     if gather and n_pre:
         t_gather = (G + A * cg + n_pre * e * (it + r)) / (A + n_pre * e)
     else:

@@ -7,6 +7,7 @@
 // emptied before every launch, and fits each term by least squares.
 //   flat backend, several batches            -> c_flat_us + bytes / bw_flat_gbs
 //   suffix gather over every SM               -> c_gather_us + bytes / bw_suffix_gbs
+//     (these two by relative error: the smallest steps weigh as much as the largest)
 //   merge                                     -> c_merge_us per (request, query head)
 //                                                + c_merge_state_us per partial state of a request
 //   tensor-core prefix items of C key tiles   -> prefix_item_us + C * prefix_tile_us
@@ -14,7 +15,7 @@
 //   the gather alone on the SMs long items leave it -> gather_sm_gbs (median per SM)
 // The split arrangement's own terms -- how much longer an item's tile takes
 // beside a gather that keeps HBM busy (per kind of item), when and how fast a
-// prefix CTA gathers after its item -- and c_cascade_us are then fitted to the
+// prefix CTA gathers after its item, when the gather-only CTAs start -- and c_cascade_us are then fitted to the
 // whole cascades timed here (both arrangements, forced and as the planner
 // arranges them, both kinds of item): a grid search for the smallest largest
 // relative error of the predicted cascade, the other terms held at their fits.
@@ -60,19 +61,23 @@ __global__ void fill_queries_kernel(uint16_t* q, size_t n) {
   }
 }
 
-// least squares y = c0 + c1 x (the intercept may come out negative)
-bool linfit(const std::vector<std::pair<double, double>>& pts, double* c0, double* c1) {
-  const double n = (double)pts.size();
+// least squares y = c0 + c1 x (the intercept may come out negative).  relative:
+// each point weighted by 1 / y^2, so the fit minimises the relative error, which
+// is what a choice between two predicted times at any scale depends on.
+bool linfit(const std::vector<std::pair<double, double>>& pts, double* c0, double* c1, bool relative = false) {
   if (pts.size() < 2) return false;
-  double sx = 0, sy = 0, sxx = 0, sxy = 0;
+  double n = 0, sx = 0, sy = 0, sxx = 0, sxy = 0;
   for (auto& q : pts) {
-    sx += q.first;
-    sy += q.second;
-    sxx += q.first * q.first;
-    sxy += q.first * q.second;
+    const double w = relative ? 1.0 / (q.second * q.second) : 1.0;
+    if (!std::isfinite(w)) return false;
+    n += w;
+    sx += w * q.first;
+    sy += w * q.second;
+    sxx += w * q.first * q.first;
+    sxy += w * q.first * q.second;
   }
   const double den = n * sxx - sx * sx;
-  if (std::fabs(den) < 1e-30) return false;
+  if (!(std::fabs(den) > 1e-12 * n * sxx)) return false;   // all x (nearly) equal
   *c1 = (n * sxy - sx * sy) / den;
   *c0 = (sy - *c1 * sx) / n;
   return true;
@@ -320,7 +325,8 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
   Case k;
 
   // (1) sequential plans over tensor-core items: flat, suffix gather, merge, prefix items, whole cascade
-  const int32_t base_cases[5][3] = {{8, 2048, 256}, {32, 4096, 512}, {64, 16384, 1024}, {128, 8192, 512}, {256, 4096, 1024}};
+  const int32_t base_cases[6][3] = {{8, 512, 64},     {8, 2048, 256},   {32, 4096, 512},
+                                    {64, 16384, 1024}, {128, 8192, 512}, {256, 4096, 1024}};
   for (auto& bc : base_cases) {
     if (!ok) break;
     if (gk::open_case(c, k, bc[0], bc[1], bc[2])) {
@@ -438,9 +444,9 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
   double a0 = 0, a1 = 0;
   if (ok) {
     std::string miss;
-    if (!gk::linfit(flat, &a0, &a1) || a1 <= 0) miss += " flat";
+    if (!gk::linfit(flat, &a0, &a1, true) || a1 <= 0) miss += " flat";
     else { cm.c_flat_us = std::max(0.0, a0); cm.bw_flat_gbs = 1.0 / a1 / 1e3; }
-    if (!gk::linfit(suffix, &a0, &a1) || a1 <= 0) miss += " suffix";
+    if (!gk::linfit(suffix, &a0, &a1, true) || a1 <= 0) miss += " suffix";
     else { cm.c_gather_us = std::max(0.0, a0); cm.bw_suffix_gbs = 1.0 / a1 / 1e3; }
     double mw[3];
     if (!gk::fit3(merge, mw)) {
@@ -491,8 +497,9 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
   // The split arrangement's terms and the cascade's fixed cost, fitted to the whole
   // cascades: tile ratio and fixed cost of an item in a split launch (each kind),
   // the cost each concurrent item adds to every item's, the prefix CTAs' gather
-  // ramp and rate, the per-SM gather rate (around its own measurement) and its
-  // ratio in tensor-core split launches.  A coordinate search over candidate
+  // ramp and rate, the per-SM gather rate (around its own measurement), its
+  // ratio in tensor-core split launches and when a split launch's gather-only
+  // CTAs start (around the stand-alone gather's c_gather).  A coordinate search over candidate
   // values of each term in turn (six passes) minimises the largest plus half the
   // mean relative error of T_cascade; for each candidate c_cascade minimises the
   // same (convex in c: ternary search).  Run on the first round's cascades, then,
@@ -551,6 +558,7 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
     terms.push_back({&gk_cost_model::gather_sm_gbs, {}});
     for (double r = 0.8; r <= 1.301; r += 0.1) terms.back().values.push_back(parts.gather_sm_gbs * r);
     terms.push_back({&gk_cost_model::split_gather_ratio_tensor, span(0.0, 0.5, 1.0, 0.1)});
+    terms.push_back({&gk_cost_model::c_gather_split_us, span(parts.c_gather_us, -4.0, 24.0, 2.0)});
     // start from the middle of each range
     gk_cost_model best = parts;
     for (auto& t : terms) best.*(t.field) = t.values[t.values.size() / 2];
@@ -618,7 +626,7 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
         {"prefix_cta_gather_ratio", cm.prefix_cta_gather_ratio}, {"c_merge_state_us", cm.c_merge_state_us},
         {"prefix_item_split_us", cm.prefix_item_split_us}, {"warp_item_split_us", cm.warp_item_split_us},
         {"prefix_item_crowd_us", cm.prefix_item_crowd_us},
-        {"split_gather_ratio_tensor", cm.split_gather_ratio_tensor}};
+        {"split_gather_ratio_tensor", cm.split_gather_ratio_tensor}, {"c_gather_split_us", cm.c_gather_split_us}};
     for (auto& t : terms) std::fprintf(f, " \"%s\": %.17g,\n", t.first, t.second);
     std::fprintf(f, " \"geometry\": {\"num_q_heads\": %d, \"num_kv_heads\": %d, \"head_dim\": %d, \"sms\": %d},\n",
                  cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, num_sms);

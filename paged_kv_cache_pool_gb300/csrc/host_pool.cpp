@@ -271,6 +271,7 @@ gk_status gk_pool_create(const gk_pool_config* cfg, gk_pool** out) {
   cm.warp_item_split_us = 8.0;
   cm.prefix_item_crowd_us = 0.0;
   cm.split_gather_ratio_tensor = 1.0;
+  cm.c_gather_split_us = 10.0;
   *out = p;
   return GK_OK;
 }

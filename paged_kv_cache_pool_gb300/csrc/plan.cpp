@@ -31,17 +31,19 @@ constexpr double kMinPrefixShare = 0.15;
 // us, and the suffix (S bytes; W = S / gather_sm SM-us at a gather-only CTA's
 // rate, gather_sm_gbs for the launch's kind of item) is spread over the CTAs so
 // that all end together.  Gather-only CTAs
-// start after c_gather; a prefix CTA starts prefix_cta_ramp after its item and
-// gathers at prefix_cta_gather_ratio of that rate (its first round trips meet an
-// HBM the other SMs keep busy).  With gather = false only the gather-only CTAs
-// gather.  The gather as a whole takes at least c_gather + S / bw_suffix, and
+// start after c_gather_split (the split launch's own fixed cost, fitted apart
+// from the stand-alone gather's c_gather); a prefix CTA starts prefix_cta_ramp
+// after its item and gathers at prefix_cta_gather_ratio of that rate (its first
+// round trips meet an HBM the other SMs keep busy).  With gather = false only the
+// gather-only CTAs gather.  The gather as a whole takes at least c_gather_split +
+// S / bw_suffix, and
 // the launch at least (S + P) / bw_suffix (HBM).  share = a prefix CTA's tokens
 // over a gather-only CTA's.
 SplitTime split_time(const gk_cost_model& cm, int num_sms, int64_t n_pre, double it, double S, double P,
                      bool gather, double gather_sm_gbs) {
   SplitTime r{std::max(it, (S + P) / (cm.bw_suffix_gbs * 1e3)), 0.0};
   if (S <= 0.0) return r;
-  const double cg = cm.c_gather_us, ramp = cm.prefix_cta_ramp_us, e = cm.prefix_cta_gather_ratio;
+  const double cg = cm.c_gather_split_us, ramp = cm.prefix_cta_ramp_us, e = cm.prefix_cta_gather_ratio;
   const double W = S / (gather_sm_gbs * 1e3);
   const double n = (double)n_pre, a = (double)(num_sms - n_pre);
   double T;
@@ -680,7 +682,7 @@ static bool valid_cost_model(const gk_cost_model& cm) {
     return false;
   if (!(cm.prefix_cta_ramp_us >= 0 && cm.prefix_cta_gather_ratio > 0 && cm.prefix_cta_gather_ratio <= 1 &&
         cm.c_merge_state_us >= 0 && cm.prefix_item_split_us >= 0 && cm.warp_item_split_us >= 0 &&
-        cm.prefix_item_crowd_us >= 0 && cm.split_gather_ratio_tensor > 0))
+        cm.prefix_item_crowd_us >= 0 && cm.split_gather_ratio_tensor > 0 && cm.c_gather_split_us >= 0))
     return false;
   return true;
 }
@@ -905,7 +907,7 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
                                      "warp_tile_us",   "warp_group_us",  "warp_item_us",
                                      "warp_split_ratio", "prefix_cta_ramp_us", "prefix_cta_gather_ratio",
                                      "c_merge_state_us", "prefix_item_split_us", "warp_item_split_us",
-                                     "prefix_item_crowd_us", "split_gather_ratio_tensor"};
+                                     "prefix_item_crowd_us", "split_gather_ratio_tensor", "c_gather_split_us"};
     bool known = false;
     for (const char* k : kNumeric) known = known || key == k;
     if (!known) {
@@ -936,6 +938,7 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
     else if (key == "warp_item_split_us") cm.warp_item_split_us = v;
     else if (key == "prefix_item_crowd_us") cm.prefix_item_crowd_us = v;
     else if (key == "split_gather_ratio_tensor") cm.split_gather_ratio_tensor = v;
+    else if (key == "c_gather_split_us") cm.c_gather_split_us = v;
   }
   return gk_cost_model_set(pool, &cm);
 }

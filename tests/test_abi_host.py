@@ -249,7 +249,8 @@ def test_dispatch_matches_oracle_formula(gk, case):
               warp_split_ratio=rnd.uniform(1.0, 1.6), prefix_cta_ramp_us=rnd.uniform(0, 30),
               prefix_cta_gather_ratio=rnd.uniform(0.3, 1.0), c_merge_state_us=rnd.uniform(0, 2),
               prefix_item_split_us=rnd.uniform(0, 20), warp_item_split_us=rnd.uniform(0, 10),
-              prefix_item_crowd_us=rnd.uniform(0, 0.1), split_gather_ratio_tensor=rnd.uniform(0.5, 1.0))
+              prefix_item_crowd_us=rnd.uniform(0, 0.1), split_gather_ratio_tensor=rnd.uniform(0.5, 1.0),
+              c_gather_split_us=rnd.uniform(0, 25))
     pool = gk.gk_pool_create(1, Hq, Hkv, d, 200000, 64, 1, 0)
     try:
         gk.gk_cost_model_load(pool, json.dumps(cm))
@@ -325,7 +326,7 @@ def test_planner_search_worked_by_hand(gk):
               c_merge_us=0.001, prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0, c_gather_us=4.0,
               prefix_tile_split_us=1.0, warp_tile_us=1e3, warp_group_us=0.0, warp_item_us=1e3, warp_split_ratio=1.0,
               prefix_cta_ramp_us=4.0, prefix_cta_gather_ratio=1.0, c_merge_state_us=0.0, prefix_item_split_us=5.0,
-              warp_item_split_us=1e3, prefix_item_crowd_us=0.0, split_gather_ratio_tensor=1.0)
+              warp_item_split_us=1e3, prefix_item_crowd_us=0.0, split_gather_ratio_tensor=1.0, c_gather_split_us=4.0)
     pool = gk.gk_pool_create(1, 32, 8, 128, 16384 + 16, 64, 1, 0)
     try:
         gk.gk_cost_model_load(pool, json.dumps(cm))

@@ -8,7 +8,8 @@ gk_calibrate and the rule is gk_dispatch over the plan the planner arranged
     gk_cost_model_load reads back and that routes shared-prefix workloads to
     the cascade and unshared ones to the flat backend;
   * on a grid of (Lp, B) cells the three choices are timed through the ABI
-    (one layer, L2 emptied before each launch, mean of 11 launches), and the
+    (one layer, L2 emptied before each launch, median of 11 launches, as
+    gk_calibrate times the cases it fits), and the
     default plan's pick (GK_PREFIX_AUTO, then gk_dispatch, with the committed
     GB300 model) must be within 10 % of the fastest choice's time, and each
     choice's predicted time within 25 % of its measured time.  CUDA events on
@@ -114,7 +115,7 @@ def test_dispatcher_against_measured_times(lp, B):
                 e1.record()
                 torch.cuda.synchronize()
                 ts.append(e0.elapsed_time(e1) * 1e3)
-            return float(np.mean(ts[1:]))
+            return float(np.median(ts[1:]))
 
         meas, pred = {}, {}
         for kind, kernel in (("tensor", gk.GK_PREFIX_TENSOR), ("warp", gk.GK_PREFIX_WARP)):

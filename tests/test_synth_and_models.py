@@ -86,7 +86,7 @@ CM = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=50
           c_merge_us=0.001, prefix_tile_us=2.0, prefix_item_us=3.0, gather_sm_gbs=1.0, c_gather_us=4.0,
           prefix_tile_split_us=2.5, warp_tile_us=0.25, warp_group_us=0.03125, warp_item_us=1.5, warp_split_ratio=1.5,
           prefix_cta_ramp_us=4.0, prefix_cta_gather_ratio=1.0, c_merge_state_us=0.5, prefix_item_split_us=3.0,
-          warp_item_split_us=1.5, prefix_item_crowd_us=0.0, split_gather_ratio_tensor=1.0)
+          warp_item_split_us=1.5, prefix_item_crowd_us=0.0, split_gather_ratio_tensor=1.0, c_gather_split_us=4.0)
 
 
 def test_cost_model_closed_form():
@@ -188,7 +188,12 @@ def test_split_formula_worked_example():
     cm4 = dict(cm, bw_suffix_gbs=1000.0)
     assert math.isclose(dispatch.split_levels(cm4, f, 64, 16, 152), (S + P) / 1e6)
     assert math.isclose(dispatch.split_levels(cm4, f, 64, 16, 152, gather=False), (S + P) / 1e6)
-    assert math.isclose(dispatch.split_levels(dict(cm4, c_gather_us=80.0), f, 64, 16, 152), 80.0 + S / 1e6)
+    assert math.isclose(dispatch.split_levels(dict(cm4, c_gather_split_us=80.0), f, 64, 16, 152), 80.0 + S / 1e6)
+    # the split launch's gather starts after its own fixed cost, not the stand-alone
+    # gather launch's: c_gather_us prices only the sequential plan
+    assert math.isclose(dispatch.split_levels(dict(cm3, c_gather_split_us=9.0, c_gather_us=1.0), f, 64, 16, 152,
+                                              gather=False), 9.0 + W3 / 136)
+    assert math.isclose(dispatch.sequential_levels(dict(cm2, c_gather_split_us=50.0), f, 7, 152, 152), t_seq)
     # warp-MMA items take their own terms: 2 row blocks x 8 heads x 4 splits of 32 tiles,
     # a tile beside the gather 1.5 * (1 + 8 * 0.125) = 3 us: item 32 * 3 + 2 = 98 us
     cmw = dict(cm, warp_tile_us=1.0, warp_group_us=0.125, warp_split_ratio=1.5, warp_item_us=9.0,
