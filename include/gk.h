@@ -355,6 +355,8 @@ typedef struct gk_cost_model {
                                      (that launch's 320-thread blocks hold the gather to fewer registers) */
   double c_gather_split_us;       /* fixed cost of the gather inside a split launch: when its gather-only
                                      CTAs start (c_gather_us is the stand-alone gather launch's) */
+  double split_tensor_us;         /* what a split launch of tensor-core items costs over one of warp-MMA
+                                     items (its 320-thread blocks, tensor memory, tensor maps) */
 } gk_cost_model;
 
 /* Predict both backends for the plan and pick the smaller:
@@ -437,7 +439,8 @@ gk_status gk_pool_set_gather_partition(gk_pool* pool, gk_gather_partition partit
  * ("GKV-cascade": a FlashAttention-style tiled online softmax that reads the
  * prefix once), and Section 3.6 routes between them on M_eff.
  *  GK_PREFIX_AUTO (default): per step, the one whose cascade the cost model
- *    predicts faster (ties go to the tensor-core items).
+ *    predicts faster, the tensor-core items only when predicted at least 10 %
+ *    faster (their predictions at small steps run low).
  *  GK_PREFIX_TENSOR: tcgen05 items of 256 stacked rows (two 128-row tiles).
  *  GK_PREFIX_WARP: warp-MMA items of 128 stacked rows (8 warps x 16 rows), no
  *    tensor memory; meant for small M_eff.
@@ -475,15 +478,17 @@ gk_status gk_cost_model_get(const gk_pool* pool, gk_cost_model* cm);
  *    L2) is allocated with cudaMalloc and freed before returning.
  *  - The terms of the split arrangement (prefix_tile_split_us / prefix_tile_us,
  *    warp_split_ratio, prefix_item_split_us, warp_item_split_us,
- *    prefix_item_crowd_us, prefix_cta_ramp_us, prefix_cta_gather_ratio,
- *    gather_sm_gbs, split_gather_ratio_tensor, c_gather_split_us) and c_cascade_us
- *    are fitted to the whole cascades it times (sequential and split plans, forced and as the
- *    planner arranges them, both prefix kernels, a grid of steps with
+ *    prefix_item_crowd_us, prefix_cta_ramp_us, gather_sm_gbs,
+ *    split_gather_ratio_tensor, c_gather_split_us, split_tensor_us) and c_cascade_us are fitted
+ *    to the whole cascades it times (sequential and split plans, forced and as
+ *    the planner arranges them, both prefix kernels, a grid of steps with
  *    16..512-token suffixes, that grid planned again with the first fit): a
  *    coordinate search over candidate values of each term that minimises the
  *    largest plus half the mean relative error of T_cascade, the other terms
  *    held at their own fits.  c_cascade_us may come out negative
- *    (the terms timed alone each carry a launch that the cascade overlaps). */
+ *    (the terms timed alone each carry a launch that the cascade overlaps).
+ *    prefix_cta_gather_ratio is set to 1: once it starts, a prefix CTA gathers
+ *    at a gather-only CTA's rate. */
 gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_out);
 /* Same as gk_cost_model_set from JSON text: {"c_flat_us": .., "bw_flat_gbs": ..,
  * "c_cascade_us": .., "bw_prefix_gbs": .., "bw_suffix_gbs": .., "c_merge_us": ..,
@@ -491,7 +496,8 @@ gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_out);
  * "prefix_tile_split_us": .., "warp_tile_us": .., "warp_group_us": .., "warp_item_us": ..,
  * "warp_split_ratio": .., "prefix_cta_ramp_us": .., "prefix_cta_gather_ratio": ..,
  * "c_merge_state_us": .., "prefix_item_split_us": .., "warp_item_split_us": ..,
- * "prefix_item_crowd_us": .., "split_gather_ratio_tensor": .., "c_gather_split_us": ..}.
+ * "prefix_item_crowd_us": .., "split_gather_ratio_tensor": .., "c_gather_split_us": ..,
+ * "split_tensor_us": ..}.
  * Keys left out keep their current values; other keys are skipped. */
 gk_status gk_cost_model_load(gk_pool* pool, const char* json);
 

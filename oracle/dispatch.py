@@ -16,7 +16,8 @@ predicted time runs (flat wins only when strictly faster):
                                               loads contend)
   T_levels  = max(bytes_pre / bw_prefix, W * item(C)) + c_gather
               + bytes_suffix / bw_suffix                          (sequential plan, W waves)
-            = max(item'(C), T_gather, (bytes_suffix + bytes_pre) / bw_suffix)   (split plan)
+            = max(item'(C), T_gather, (bytes_suffix + bytes_pre) / bw_suffix)
+              + split_tensor (a split launch of tensor-core items)        (split plan)
   T_gather  = (G + A * c_gs + n * e * (item'(C) + r)) / (A + n * e)   (prefix CTAs gather too)
             = c_gs + G / A                                        (only the other CTAs gather)
               and at least c_gs + bytes_suffix / bw_suffix        (the gather held to HBM)
@@ -159,7 +160,8 @@ def split_levels(cm, f, C, n_pre, num_sms, kind="tensor", R=0, gather=True):
         t_gather = (G + A * cg + n_pre * e * (it + r)) / (A + n_pre * e)
     else:
         t_gather = cg + G / A
-    return max(t, t_gather, cg + f["bytes_suffix"] / (cm["bw_suffix_gbs"] * 1e3))
+    t = max(t, t_gather, cg + f["bytes_suffix"] / (cm["bw_suffix_gbs"] * 1e3))
+    return t + (cm["split_tensor_us"] if kind == "tensor" else 0.0)
 
 
 def predict(cm, f, plan, num_sms=152):

@@ -64,7 +64,8 @@ class gk_cost_model(ctypes.Structure):
                 ("warp_tile_us", c_dbl), ("warp_group_us", c_dbl), ("warp_item_us", c_dbl),
                 ("warp_split_ratio", c_dbl), ("prefix_cta_ramp_us", c_dbl), ("prefix_cta_gather_ratio", c_dbl),
                 ("c_merge_state_us", c_dbl), ("prefix_item_split_us", c_dbl), ("warp_item_split_us", c_dbl),
-                ("prefix_item_crowd_us", c_dbl), ("split_gather_ratio_tensor", c_dbl), ("c_gather_split_us", c_dbl)]
+                ("prefix_item_crowd_us", c_dbl), ("split_gather_ratio_tensor", c_dbl), ("c_gather_split_us", c_dbl),
+                ("split_tensor_us", c_dbl)]
 
 
 P = ctypes.POINTER
@@ -435,7 +436,8 @@ COST_MODEL_KEYS = ("c_flat_us", "bw_flat_gbs", "c_cascade_us", "bw_prefix_gbs", 
                    "prefix_tile_us", "prefix_item_us", "gather_sm_gbs", "c_gather_us", "prefix_tile_split_us",
                    "warp_tile_us", "warp_group_us", "warp_item_us", "warp_split_ratio", "prefix_cta_ramp_us",
                    "prefix_cta_gather_ratio", "c_merge_state_us", "prefix_item_split_us", "warp_item_split_us",
-                   "prefix_item_crowd_us", "split_gather_ratio_tensor", "c_gather_split_us")
+                   "prefix_item_crowd_us", "split_gather_ratio_tensor", "c_gather_split_us",
+                   "split_tensor_us")
 
 
 def gk_cost_model_set(pool, cm: dict):

@@ -203,7 +203,9 @@ struct Case {
 // Suffix lengths of a case: s tokens each, or (s < 0) lengths uniform in
 // 16..512 tokens (the pages' user turns) drawn from a generator seeded by -s
 // (splitmix64 increments, the top bits scaled to the range).
-std::vector<int32_t> suffix_lengths(int32_t B, int32_t s) {
+// s >= 0: every suffix s tokens; s < 0: drawn from lo..hi (default 16..512, the
+// pages' user turns) by a splitmix64 stream seeded by -s
+std::vector<int32_t> suffix_lengths(int32_t B, int32_t s, int32_t lo = 16, int32_t hi = 512) {
   std::vector<int32_t> out((size_t)B, s);
   if (s >= 0) return out;
   uint64_t x = (uint64_t)(-(int64_t)s) * 0x9E3779B97F4A7C15ull;
@@ -213,18 +215,18 @@ std::vector<int32_t> suffix_lengths(int32_t B, int32_t s) {
     z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
     z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
     z ^= z >> 31;
-    v = 16 + (int32_t)((z >> 32) % 497u);
+    v = lo + (int32_t)((z >> 32) % (uint32_t)(hi - lo + 1));
   }
   return out;
 }
 
 // false when the pool has no room for the case (it is then skipped) or on an error (c.why set)
-bool open_case(Calib& c, Case& k, int32_t B, int32_t lp, int32_t s) {
+bool open_case(Calib& c, Case& k, int32_t B, int32_t lp, int32_t s, int32_t lo = 16, int32_t hi = 512) {
   k = Case{};
   k.B = B;
   k.lp = lp;
   k.s = s;
-  const std::vector<int32_t> lens = suffix_lengths(B, s);
+  const std::vector<int32_t> lens = suffix_lengths(B, s, lo, hi);
   const int32_t P = c.p->cfg.cold_page_size;
   int32_t smax = 0;
   for (int32_t v : lens) smax = std::max(smax, v);
@@ -307,7 +309,7 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
   std::vector<std::pair<double, double>> flat, suffix, tile, gather_sm;
   std::vector<std::array<double, 3>> merge;             // (B * Hq, partial states per request, us)
   std::vector<std::array<double, 3>> warp;              // (C, C * R, us)
-  bool ok = c.setup(512, (1024 + cfg.cold_page_size - 1) / cfg.cold_page_size + 1);
+  bool ok = c.setup(512, (2048 + cfg.cold_page_size - 1) / cfg.cold_page_size + 1);
 
   auto plan_for = [&](Case& k, gk_cascade_mode mode, int32_t tiles, gk_prefix_kernel kern) -> gk_plan* {
     p->cascade_mode = mode;
@@ -438,6 +440,35 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
       }
   };
   run_grid(true);
+  // (6) steps the size of whole decode layers (long suffixes, hundreds of MB each):
+  //     the arrangement the planner picks for each prefix kernel and, in the
+  //     first round, the sequential one and split launches of tensor-core items
+  //     of 16 and 32 key tiles, so that the split terms are fitted where a
+  //     step's time goes, not only on the short steps of the grid
+  auto run_large = [&](bool forced_too) {
+    const int32_t large_cases[3][5] = {{64, 16384, 256, 2048, 1}, {256, 4096, 64, 1024, 2}, {128, 16384, 512, 2048, 3}};
+    for (auto& lc : large_cases) {
+      if (!ok) return;
+      if (gk::open_case(c, k, lc[0], lc[1], -(1000000 + lc[4]), lc[2], lc[3])) {
+        struct Arr { gk_cascade_mode mode; int32_t tiles; gk_prefix_kernel kern; };
+        const Arr arrs[] = {{GK_CASCADE_AUTO, 0, GK_PREFIX_TENSOR}, {GK_CASCADE_AUTO, 0, GK_PREFIX_WARP},
+                            {GK_CASCADE_SEQUENTIAL, 0, GK_PREFIX_TENSOR}, {GK_CASCADE_SPLIT, 16, GK_PREFIX_TENSOR},
+                            {GK_CASCADE_SPLIT, 32, GK_PREFIX_TENSOR}};
+        for (const Arr& a : arrs) {
+          if (a.mode != GK_CASCADE_AUTO && !forced_too) continue;
+          gk_plan* pl = plan_for(k, a.mode, a.tiles, a.kern);
+          if (!(ok = pl != nullptr)) break;
+          double t;
+          if (!(ok = (t = timed([&] { return gk_decode_cascade(pool, stream, 0, &k.batch, pl); })) >= 0)) break;
+          cascades.push_back({pl, t});
+        }
+      } else if (!c.why.empty()) {
+        ok = false;
+      }
+      gk::close_case(c, k);
+    }
+  };
+  run_large(true);
 
   // ---- fits ----
   gk_cost_model cm = p->cost;
@@ -498,8 +529,9 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
   // cascades: tile ratio and fixed cost of an item in a split launch (each kind),
   // the cost each concurrent item adds to every item's, the prefix CTAs' gather
   // ramp and rate, the per-SM gather rate (around its own measurement), its
-  // ratio in tensor-core split launches and when a split launch's gather-only
-  // CTAs start (around the stand-alone gather's c_gather).  A coordinate search over candidate
+  // ratio in tensor-core split launches, when a split launch's gather-only
+  // CTAs start (around the stand-alone gather's c_gather) and what a split
+  // launch of tensor-core items costs over one of warp-MMA items.  A coordinate search over candidate
   // values of each term in turn (six passes) minimises the largest plus half the
   // mean relative error of T_cascade; for each candidate c_cascade minimises the
   // same (convex in c: ternary search).  Run on the first round's cascades, then,
@@ -553,14 +585,21 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
     terms.push_back({&gk_cost_model::prefix_item_split_us, span(parts.prefix_item_us, -4.0, 8.0, 2.0)});
     terms.push_back({&gk_cost_model::warp_item_split_us, span(parts.warp_item_us, -4.0, 8.0, 2.0)});
     terms.push_back({&gk_cost_model::prefix_item_crowd_us, span(0.0, 0.0, 0.16, 0.02)});
-    terms.push_back({&gk_cost_model::prefix_cta_ramp_us, span(0.0, 0.0, 40.0, 4.0)});
-    terms.push_back({&gk_cost_model::prefix_cta_gather_ratio, span(0.0, 0.5, 1.0, 0.125)});
+    // A prefix CTA gathers with the same code on the same kind of SM as a
+    // gather-only CTA: the model gives it the same rate (ratio 1) and fits only
+    // when it starts.  (Per-CTA %globaltimer timelines of split launches show
+    // prefix CTAs gathering at 0.94-1.0 of a gather-only CTA's rate; the fitted
+    // start is a later one than the timelines show, as it also carries what the
+    // model leaves out of a prefix CTA's short gathers.)
+    terms.push_back({&gk_cost_model::prefix_cta_ramp_us, span(0.0, 0.0, 40.0, 2.0)});
     terms.push_back({&gk_cost_model::gather_sm_gbs, {}});
     for (double r = 0.8; r <= 1.301; r += 0.1) terms.back().values.push_back(parts.gather_sm_gbs * r);
     terms.push_back({&gk_cost_model::split_gather_ratio_tensor, span(0.0, 0.5, 1.0, 0.1)});
     terms.push_back({&gk_cost_model::c_gather_split_us, span(parts.c_gather_us, -4.0, 24.0, 2.0)});
+    terms.push_back({&gk_cost_model::split_tensor_us, span(0.0, 0.0, 12.0, 1.0)});
     // start from the middle of each range
     gk_cost_model best = parts;
+    best.prefix_cta_gather_ratio = 1.0;
     for (auto& t : terms) best.*(t.field) = t.values[t.values.size() / 2];
     double best_s = evaluate(best);
     for (int pass = 0; pass < 6; ++pass)
@@ -580,6 +619,7 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
   if (ok) {
     p->cost = cm;          // the second round plans with the fitted model
     run_grid(false);
+    run_large(false);
     fit_cascades();
   }
   if (ok) {
@@ -626,7 +666,8 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
         {"prefix_cta_gather_ratio", cm.prefix_cta_gather_ratio}, {"c_merge_state_us", cm.c_merge_state_us},
         {"prefix_item_split_us", cm.prefix_item_split_us}, {"warp_item_split_us", cm.warp_item_split_us},
         {"prefix_item_crowd_us", cm.prefix_item_crowd_us},
-        {"split_gather_ratio_tensor", cm.split_gather_ratio_tensor}, {"c_gather_split_us", cm.c_gather_split_us}};
+        {"split_gather_ratio_tensor", cm.split_gather_ratio_tensor}, {"c_gather_split_us", cm.c_gather_split_us},
+        {"split_tensor_us", cm.split_tensor_us}};
     for (auto& t : terms) std::fprintf(f, " \"%s\": %.17g,\n", t.first, t.second);
     std::fprintf(f, " \"geometry\": {\"num_q_heads\": %d, \"num_kv_heads\": %d, \"head_dim\": %d, \"sms\": %d},\n",
                  cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, num_sms);

@@ -272,6 +272,7 @@ gk_status gk_pool_create(const gk_pool_config* cfg, gk_pool** out) {
   cm.prefix_item_crowd_us = 0.0;
   cm.split_gather_ratio_tensor = 1.0;
   cm.c_gather_split_us = 10.0;
+  cm.split_tensor_us = 0.0;
   *out = p;
   return GK_OK;
 }

@@ -24,21 +24,26 @@ constexpr int kMinGatherQuota = 64;
 // suffix: an item that leaves its CTA nothing to gather ends late beside a
 // gather that keeps HBM busy, and then the other SMs wait for it.
 constexpr double kMinPrefixShare = 0.15;
+// The split search prices each item this much longer than the model: per-CTA
+// timelines of split launches put item ends up to about 15 % from the fitted
+// item time.
+constexpr double kSplitItemMargin = 1.15;
+// GK_PREFIX_AUTO keeps tensor-core items only when their cascade is predicted
+// faster than the warp-MMA items' by this factor.
+constexpr double kTensorAutoEdge = 0.9;
 
 }  // namespace
 
 // Split launch (one CTA per SM): CTAs [0, n_pre) first run a prefix item of `it`
 // us, and the suffix (S bytes; W = S / gather_sm SM-us at a gather-only CTA's
 // rate, gather_sm_gbs for the launch's kind of item) is spread over the CTAs so
-// that all end together.  Gather-only CTAs
-// start after c_gather_split (the split launch's own fixed cost, fitted apart
-// from the stand-alone gather's c_gather); a prefix CTA starts prefix_cta_ramp
-// after its item and gathers at prefix_cta_gather_ratio of that rate (its first
-// round trips meet an HBM the other SMs keep busy).  With gather = false only the
+// that all end together.  Gather-only CTAs start after c_gather_split (the split
+// launch's own fixed cost, fitted apart from the stand-alone gather's c_gather);
+// a prefix CTA starts prefix_cta_ramp after its item and gathers at
+// prefix_cta_gather_ratio of that rate.  With gather = false only the
 // gather-only CTAs gather.  The gather as a whole takes at least c_gather_split +
-// S / bw_suffix, and
-// the launch at least (S + P) / bw_suffix (HBM).  share = a prefix CTA's tokens
-// over a gather-only CTA's.
+// S / bw_suffix, and the launch at least (S + P) / bw_suffix (HBM).  share = a
+// prefix CTA's tokens over a gather-only CTA's.
 SplitTime split_time(const gk_cost_model& cm, int num_sms, int64_t n_pre, double it, double S, double P,
                      bool gather, double gather_sm_gbs) {
   SplitTime r{std::max(it, (S + P) / (cm.bw_suffix_gbs * 1e3)), 0.0};
@@ -57,6 +62,39 @@ SplitTime split_time(const gk_cost_model& cm, int num_sms, int64_t n_pre, double
   T = std::max(T, cg + S / (cm.bw_suffix_gbs * 1e3));
   r.t = std::max(r.t, T);
   return r;
+}
+
+// Gather weights of the CTAs of a split launch whose prefix CTAs gather, one
+// prefix item time per prefix CTA (it[b], CTA b < it.size()): items of different
+// lengths leave their CTAs different times to gather.  CTA b starts gathering at
+// s_b = max(c_gather_split, it[b] + prefix_cta_ramp), at prefix_cta_gather_ratio
+// (e) of a gather-only CTA's rate; gather-only CTAs start at c_gather_split.  The
+// common end T is the one at which the CTAs together gather W = S / gather_sm
+// SM-us:  (num_sms - n_pre) (T - c) + sum_b e * max(0, T - s_b) = W  (increasing
+// in T: bisection).  Weight = a CTA's tokens over a gather-only CTA's (1 for
+// those, at most e for the others).
+std::vector<double> split_weights(const gk_cost_model& cm, int num_sms, const std::vector<double>& it, double S,
+                                  double gather_sm_gbs) {
+  std::vector<double> w((size_t)num_sms, 1.0);
+  const double c = cm.c_gather_split_us, e = cm.prefix_cta_gather_ratio;
+  const double W = S / (gather_sm_gbs * 1e3);
+  const size_t n_pre = std::min(it.size(), w.size());
+  std::vector<double> start(n_pre);
+  for (size_t b = 0; b < n_pre; ++b) start[b] = std::max(c, it[b] + cm.prefix_cta_ramp_us);
+  auto capacity = [&](double T) {
+    double cap = (double)(w.size() - n_pre) * std::max(0.0, T - c);
+    for (size_t b = 0; b < n_pre; ++b) cap += e * std::max(0.0, T - start[b]);
+    return cap;
+  };
+  double lo = c, hi = c + 1.0;
+  while (capacity(hi) < W && hi < 1e12) hi = c + 2.0 * (hi - c);
+  for (int i = 0; i < 100; ++i) {
+    const double mid = 0.5 * (lo + hi);
+    (capacity(mid) < W ? lo : hi) = mid;
+  }
+  const double full = std::max(hi - c, 1e-9);
+  for (size_t b = 0; b < n_pre; ++b) w[b] = e * std::max(0.0, hi - start[b]) / full;
+  return w;
 }
 
 double merge_us(const gk_cost_model& cm, int32_t B, int32_t Hq, int64_t partials) {
@@ -290,7 +328,7 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
     int32_t rows = 0;
     std::vector<int32_t> mtiles;
     std::vector<uint8_t> single;   // the group's last row block fills one Q tile at most
-    double tile = 0, tile_split = 0, item = 0;
+    double tile = 0, tile_split = 0, item = 0, item_split = 0;
     bool split = false;
     int32_t c = 0;              // key tiles per item
     double t_levels = 0;        // predicted levels time of the chosen arrangement
@@ -302,6 +340,7 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
     k.tile = tile;
     k.tile_split = tile_split;
     k.item = item;
+    k.item_split = item_split;
     k.mtiles.resize((size_t)G);
     k.single.assign((size_t)G, 0);
     for (int32_t gi = 0; gi < G; ++gi) {
@@ -340,10 +379,12 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
     // the split launch for items of C tiles: the prefix CTAs gather a share when it
     // reaches kMinPrefixShare of a gather-only CTA's, else only the others gather
     const double gsm = rows == kPrefixRowsPerCta ? cm.gather_sm_gbs * cm.split_gather_ratio_tensor : cm.gather_sm_gbs;
-    auto split_of = [&](int32_t C, bool* gather) {
-      SplitTime st = split_time(cm, num_sms, n_items(C), item_us(C), S, prefix_bytes, true, gsm);
+    auto split_of = [&](int32_t C, bool* gather, double margin = 1.0) {
+      const double it = margin * item_us(C);
+      SplitTime st = split_time(cm, num_sms, n_items(C), it, S, prefix_bytes, true, gsm);
       *gather = st.share >= kMinPrefixShare;
-      if (!*gather) st = split_time(cm, num_sms, n_items(C), item_us(C), S, prefix_bytes, false, gsm);
+      if (!*gather) st = split_time(cm, num_sms, n_items(C), it, S, prefix_bytes, false, gsm);
+      if (rows == kPrefixRowsPerCta) st.t += cm.split_tensor_us;
       return st;
     };
     int32_t c_split = 0;
@@ -357,17 +398,23 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
         t_split = split_of(C, &gth).t;
       }
     } else {
+      // items priced kSplitItemMargin long: beside the gather an item's time is
+      // the model's least certain term, and an item that outlasts the gather
+      // holds the whole launch
+      double t_best = 1e300;
       for (int32_t C = max_ntiles; can_split && C >= 1; --C) {
         if (n_items(C) > num_sms) break;  // items only grow as C shrinks
         bool gth;
-        const double t = split_of(C, &gth).t;
+        const double t = split_of(C, &gth, kSplitItemMargin).t;
         // the gather needs an SM of its own unless the prefix CTAs take part
         if (!gth && n_items(C) >= num_sms) continue;
-        if (t < t_split - 1e-9) {
-          t_split = t;
+        if (t < t_best - 1e-9) {
+          t_best = t;
           c_split = C;
         }
       }
+      bool gth;
+      if (c_split > 0) t_split = split_of(c_split, &gth).t;
     }
     // balance the chosen split: the fewest tiles per item that gives as many items
     while (c_split > 1 && n_items(c_split - 1) == n_items(c_split)) --c_split;
@@ -420,7 +467,7 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
   // CTA order: longest splits first; within a length, (group, split, head, row block)
   // so CTAs reading the same K/V tiles run side by side.  A one-Q-tile row block's
   // items cover two consecutive splits (the second's entry is left empty).
-  struct Item { PrefixItemDev it; int32_t tiles; };
+  struct Item { PrefixItemDev it; int32_t tiles; bool pair; };
   std::vector<Item> items;
   for (int32_t gi = 0; gi < G; ++gi) {
     const PrefixGroupDev& gd = pl->groups[(size_t)gi];
@@ -433,7 +480,7 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
           const int32_t n = pair ? std::min(2, gd.nsplit - s) : 1;
           const int32_t t0 = s * gd.split_tiles;
           const int32_t t1 = std::min(ntiles[(size_t)gi], t0 + n * gd.split_tiles);
-          items.push_back({PrefixItemDev{gi, mt, h, s, n, 0}, t1 - t0});
+          items.push_back({PrefixItemDev{gi, mt, h, s, n, 0}, t1 - t0, pair});
         }
     }
   }
@@ -453,9 +500,19 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
     dense_tokens += n_dense[(size_t)r];
   }
   if (pl->split) {
-    // one slot per SM; the prefix CTAs' slots (the first n_pre) carry their share
+    // one slot per SM; a prefix CTA's slot is sized to the time its own item
+    // leaves it (a one-Q-tile block's item runs its tiles at about twice the rate)
     std::vector<double> w((size_t)num_sms, 1.0);
-    for (size_t b2 = 0; b2 < pl->prefix_items.size() && b2 < w.size(); ++b2) w[b2] = prefix_cta_share;
+    if (prefix_cta_share > 0.0) {
+      std::vector<double> it;
+      const double crowd = cm.prefix_item_crowd_us * (double)items.size();
+      for (const Item& x : items) it.push_back((x.pair ? 0.5 : 1.0) * x.tiles * kp.tile_split + kp.item_split + crowd);
+      const double gsm = kp.rows == kPrefixRowsPerCta ? cm.gather_sm_gbs * cm.split_gather_ratio_tensor
+                                                      : cm.gather_sm_gbs;
+      w = split_weights(cm, num_sms, it, (double)S, gsm);
+    } else {
+      for (size_t b2 = 0; b2 < pl->prefix_items.size() && b2 < w.size(); ++b2) w[b2] = 0.0;
+    }
     partition_tokens_weighted(n_suf, w, &pl->suf_seg_begin, &pl->suf_segs);
   } else {
     if (p->gather_partition == GK_PARTITION_PER_REQUEST)
@@ -534,9 +591,12 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
 }  // namespace
 
 // GK_PREFIX_AUTO plans the step with each kind of prefix item and keeps the one
-// whose whole cascade (levels and merge) the cost model predicts faster, the
-// tensor-core items on a tie: GraniKV Section 3.6's routing between its two
-// prefix kernels, with the measured model in place of the M_sat threshold.
+// whose whole cascade (levels and merge) the cost model predicts faster:
+// GraniKV Section 3.6's routing between its two prefix kernels, with the
+// measured model in place of the M_sat threshold.  The tensor-core items must
+// be predicted kTensorAutoEdge faster: on GB300 the model's times for their
+// cascade at small steps came out up to a quarter under the measured ones, the
+// warp-MMA items' within a fifth.
 gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   if (p->prefix_kernel != GK_PREFIX_AUTO) return build_host_plan_kind(p, b, pl, p->prefix_kernel);
   gk_status st = build_host_plan_kind(p, b, pl, GK_PREFIX_TENSOR);
@@ -548,7 +608,7 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   double td, t_tensor, t_warp;
   predict_plan(p->cost, p->dev.num_sms, Hq, *pl, &td, &t_tensor);
   predict_plan(p->cost, p->dev.num_sms, Hq, w, &td, &t_warp);
-  if (t_warp < t_tensor - 1e-9) {
+  if (!(t_tensor < kTensorAutoEdge * t_warp)) {
     pl->summary = w.summary;
     pl->groups.swap(w.groups);
     pl->group_hot_base.swap(w.group_hot_base);
@@ -682,7 +742,8 @@ static bool valid_cost_model(const gk_cost_model& cm) {
     return false;
   if (!(cm.prefix_cta_ramp_us >= 0 && cm.prefix_cta_gather_ratio > 0 && cm.prefix_cta_gather_ratio <= 1 &&
         cm.c_merge_state_us >= 0 && cm.prefix_item_split_us >= 0 && cm.warp_item_split_us >= 0 &&
-        cm.prefix_item_crowd_us >= 0 && cm.split_gather_ratio_tensor > 0 && cm.c_gather_split_us >= 0))
+        cm.prefix_item_crowd_us >= 0 && cm.split_gather_ratio_tensor > 0 && cm.c_gather_split_us >= 0 &&
+        cm.split_tensor_us >= 0))
     return false;
   return true;
 }
@@ -767,6 +828,7 @@ void predict_plan(const gk_cost_model& cm, int num_sms, int32_t Hq, const Plan& 
     const double gsm = warp ? cm.gather_sm_gbs : cm.gather_sm_gbs * cm.split_gather_ratio_tensor;
     t_levels = split_time(cm, num_sms, sm.prefix_ctas, it, (double)sm.suffix_bytes, (double)sm.prefix_bytes,
                           sm.prefix_ctas_gather != 0, gsm).t;
+    if (!warp) t_levels += cm.split_tensor_us;
   } else {
     if (sm.prefix_ctas > 0) {
       const double item = sm.prefix_tiles_per_item * tile + item_fixed;
@@ -907,7 +969,8 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
                                      "warp_tile_us",   "warp_group_us",  "warp_item_us",
                                      "warp_split_ratio", "prefix_cta_ramp_us", "prefix_cta_gather_ratio",
                                      "c_merge_state_us", "prefix_item_split_us", "warp_item_split_us",
-                                     "prefix_item_crowd_us", "split_gather_ratio_tensor", "c_gather_split_us"};
+                                     "prefix_item_crowd_us", "split_gather_ratio_tensor", "c_gather_split_us",
+                                     "split_tensor_us"};
     bool known = false;
     for (const char* k : kNumeric) known = known || key == k;
     if (!known) {
@@ -939,6 +1002,7 @@ gk_status gk_cost_model_load(gk_pool* pool, const char* json) {
     else if (key == "prefix_item_crowd_us") cm.prefix_item_crowd_us = v;
     else if (key == "split_gather_ratio_tensor") cm.split_gather_ratio_tensor = v;
     else if (key == "c_gather_split_us") cm.c_gather_split_us = v;
+    else if (key == "split_tensor_us") cm.split_tensor_us = v;
   }
   return gk_cost_model_set(pool, &cm);
 }

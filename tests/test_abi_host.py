@@ -235,8 +235,8 @@ def test_plan_summary_against_the_byte_and_flop_model(gk):
 def test_dispatch_matches_oracle_formula(gk, case):
     """gk_dispatch's two predictions follow the documented formula (oracle/dispatch.py) for
     the arrangement and prefix kernel the plan reports, the plan's prefix work covers every
-    (row block, KV head, key split) once, and GK_PREFIX_AUTO takes the kind its own model
-    predicts faster.  Which arrangement the planner searches out is not pinned here (the
+    (row block, KV head, key split) once, and GK_PREFIX_AUTO takes the warp-MMA items
+    unless the tensor-core ones are predicted at least 10 % faster.  Which arrangement the planner searches out is not pinned here (the
     pages fix no such rule); the GPU tests hold it to measured times."""
     rnd = random.Random(case)
     Hq, Hkv, d = rnd.choice([(32, 8, 128), (40, 8, 128)])
@@ -250,7 +250,7 @@ def test_dispatch_matches_oracle_formula(gk, case):
               prefix_cta_gather_ratio=rnd.uniform(0.3, 1.0), c_merge_state_us=rnd.uniform(0, 2),
               prefix_item_split_us=rnd.uniform(0, 20), warp_item_split_us=rnd.uniform(0, 10),
               prefix_item_crowd_us=rnd.uniform(0, 0.1), split_gather_ratio_tensor=rnd.uniform(0.5, 1.0),
-              c_gather_split_us=rnd.uniform(0, 25))
+              c_gather_split_us=rnd.uniform(0, 25), split_tensor_us=rnd.uniform(0, 8))
     pool = gk.gk_pool_create(1, Hq, Hkv, d, 200000, 64, 1, 0)
     try:
         gk.gk_cost_model_load(pool, json.dumps(cm))
@@ -295,7 +295,8 @@ def test_dispatch_matches_oracle_formula(gk, case):
             assert math.isclose(td, wd, rel_tol=1e-12) and math.isclose(tc, wc, rel_tol=1e-12)
             assert choice == (gk.GK_BACKEND_DENSE if odisp.choose(wd, wc) == "dense" else gk.GK_BACKEND_CASCADE)
             pred[kernel] = tc
-        assert pred[gk.GK_PREFIX_AUTO] <= min(pred[gk.GK_PREFIX_TENSOR], pred[gk.GK_PREFIX_WARP]) * (1 + 1e-12)
+        t_t, t_w = pred[gk.GK_PREFIX_TENSOR], pred[gk.GK_PREFIX_WARP]
+        assert pred[gk.GK_PREFIX_AUTO] == (t_t if t_t < 0.9 * t_w else t_w)
         with pytest.raises(gk.GkError):
             gk.gk_pool_set_prefix_kernel(pool, 3)
     finally:
@@ -310,15 +311,17 @@ def test_planner_search_worked_by_hand(gk):
     item 5 us, 50 GB/s per SM, 6000 GB/s over every SM, 4 us for a gather launch and for a
     prefix CTA's gather ramp, prefix CTAs gathering at the full rate, 152 SMs.  The gather is
     W = S / 50 GB/s = 5242.88 SM-us, HBM binds at (S + P) / 6000 GB/s = 54.875 us, and
-    items(C) = 8 ceil(128 / C) of C + 5 us.  With prefix CTAs gathering,
-    T(C) = (W + (152 - n) 4 + n (C + 5 + 4)) / 152 and their share (T - C - 9) / (T - 4);
-    below 0.15 they gather nothing and T(C) = 4 + W / (152 - n).  Scanning from C = 128 down,
-    the 8- and 16-item splits end with their items (C + 5 > 54.875 down to C = 50); C = 49
-    (24 items, share below 0.15, T = 4 + W / 128 = 45.0) is the first at the HBM bound, so it
-    is kept (nothing later is strictly faster) and balanced to C = 43, the fewest tiles giving
-    24 items; its prefix CTAs do not gather.  The sequential alternative (C = 7: 152 items in
-    one wave of 12 us, the prefix bound by its 67 MB at 5000 GB/s: 13.4 + 4 + 43.7 = 61.1 us)
-    is slower, so the plan splits, and T_cascade = 10 + 54.875 + 0.001 * 64 * 32 = 66.923 us.
+    items(C) = 8 ceil(128 / C) of C + 5 us, which the search prices 1.15 times longer.  With
+    prefix CTAs gathering, T(C) = (W + (152 - n) 4 + n (it + 4)) / 152 and their share
+    (T - it - 4) / (T - 4); below 0.15 they gather nothing and T(C) = 4 + W / (152 - n).
+    Scanning from C = 128 down, every split up to C = 43 (24 items) ends with its items
+    (1.15 (C + 5) > 54.875); C = 42 (32 items of 54.05 us priced, share below 0.15, T = 4 +
+    W / 120 = 47.7) is the first at the HBM bound and nothing later is strictly faster.
+    Balanced to C = 32, the fewest tiles giving 32 items; at its own price (37 us) the
+    prefix CTAs' share is 0.125, so they gather nothing.  The sequential alternative (C = 7:
+    152 items in one wave of 12 us, the prefix bound by its 67 MB at 5000 GB/s: 13.4 + 4 +
+    43.7 = 61.1 us) is slower, so the plan splits, and T_cascade = 10 + 54.875 +
+    0.001 * 64 * 32 = 66.923 us.
     (2) 512 requests (M = 2048: eight row blocks per head), sequential, tile 1.557 us, item
     8.63 us: one wave of 128 items of 64 tiles (108.3 us) beats three waves of 448 items of
     19 tiles (114.6 us) and two of 256 items of 32 (117.0 us)."""
@@ -326,7 +329,8 @@ def test_planner_search_worked_by_hand(gk):
               c_merge_us=0.001, prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0, c_gather_us=4.0,
               prefix_tile_split_us=1.0, warp_tile_us=1e3, warp_group_us=0.0, warp_item_us=1e3, warp_split_ratio=1.0,
               prefix_cta_ramp_us=4.0, prefix_cta_gather_ratio=1.0, c_merge_state_us=0.0, prefix_item_split_us=5.0,
-              warp_item_split_us=1e3, prefix_item_crowd_us=0.0, split_gather_ratio_tensor=1.0, c_gather_split_us=4.0)
+              warp_item_split_us=1e3, prefix_item_crowd_us=0.0, split_gather_ratio_tensor=1.0, c_gather_split_us=4.0,
+              split_tensor_us=0.0)
     pool = gk.gk_pool_create(1, 32, 8, 128, 16384 + 16, 64, 1, 0)
     try:
         gk.gk_cost_model_load(pool, json.dumps(cm))
@@ -335,7 +339,7 @@ def test_planner_search_worked_by_hand(gk):
         s = gk.gk_plan_info(plan)
         t_cas = gk.gk_dispatch(pool, plan)[2]
         gk.gk_plan_destroy(plan)
-        assert (s["cascade_split"], s["prefix_tiles_per_item"], s["prefix_ctas"], s["suffix_ctas"]) == (1, 43, 24, 152)
+        assert (s["cascade_split"], s["prefix_tiles_per_item"], s["prefix_ctas"], s["suffix_ctas"]) == (1, 32, 32, 152)
         assert s["prefix_ctas_gather"] == 0 and s["prefix_kernel"] == gk.GK_PREFIX_TENSOR
         assert math.isclose(t_cas, 10 + (64000 + 16384) * 4096 / 6e3 / 1e3 + 0.001 * 64 * 32, rel_tol=1e-12)
         gk.gk_cost_model_load(pool, json.dumps(dict(cm, prefix_tile_us=1.557, prefix_item_us=8.63)))

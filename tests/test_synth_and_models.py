@@ -86,7 +86,8 @@ CM = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=50
           c_merge_us=0.001, prefix_tile_us=2.0, prefix_item_us=3.0, gather_sm_gbs=1.0, c_gather_us=4.0,
           prefix_tile_split_us=2.5, warp_tile_us=0.25, warp_group_us=0.03125, warp_item_us=1.5, warp_split_ratio=1.5,
           prefix_cta_ramp_us=4.0, prefix_cta_gather_ratio=1.0, c_merge_state_us=0.5, prefix_item_split_us=3.0,
-          warp_item_split_us=1.5, prefix_item_crowd_us=0.0, split_gather_ratio_tensor=1.0, c_gather_split_us=4.0)
+          warp_item_split_us=1.5, prefix_item_crowd_us=0.0, split_gather_ratio_tensor=1.0, c_gather_split_us=4.0,
+          split_tensor_us=0.0)
 
 
 def test_cost_model_closed_form():
@@ -174,6 +175,11 @@ def test_split_formula_worked_example():
                         4.0 + 2 * W3 / 136)
     assert math.isclose(dispatch.split_levels(dict(cm3, split_gather_ratio_tensor=0.5, warp_item_split_us=5.0), f, 64,
                                               16, 152, "warp", R=1, gather=False), 4.0 + W3 / 136)
+    # a split launch of tensor-core items pays split_tensor_us on top; one of warp items not
+    assert math.isclose(dispatch.split_levels(dict(cm3, split_tensor_us=3.0), f, 64, 16, 152, gather=False),
+                        4.0 + W3 / 136 + 3.0)
+    assert math.isclose(dispatch.split_levels(dict(cm3, split_tensor_us=3.0, warp_item_split_us=5.0), f, 64, 16, 152,
+                                              "warp", R=1, gather=False), 4.0 + W3 / 136)
     # each item of a split launch pays prefix_item_crowd_us per item of the launch
     assert math.isclose(dispatch.split_levels(dict(cm, prefix_item_crowd_us=0.5), f, 64, 16, 152), 69.0 + 8.0)
     # a split item runs beside the gather: the split formula takes the split tile time and
