@@ -40,9 +40,11 @@ fullest warp item, rounded up to 1, 2, 4 or 8.
 Work decomposition (fixed by the kernels' tiling, not a heuristic): a group of
 M_eff stacked rows and Lp keys contributes ceil(M_eff / rows) row blocks x Hkv
 heads x ceil(ceil(Lp / 128) / C) key splits.  Each (row block, head, split) is
-one item, except that a tensor-core row block holding at most one 128-row Q tile
-(M_eff mod 256 in 1..128, the group's last block) runs its tiles at about twice
-the rate and so takes two consecutive splits per item: ceil(splits / 2) items.
+one item, except that in a sequential plan a tensor-core row block holding at
+most one 128-row Q tile (M_eff mod 256 in 1..128, the group's last block) runs
+its tiles at about twice the rate and so takes two consecutive splits per item:
+ceil(splits / 2) items.  (A split plan gives such a block one split per item and
+its CTA a longer share of the gather instead.)
 
 Parity unpinned: which arrangement a plan takes (split or sequential, the key
 tiles per item C, the prefix kernel, whether its prefix CTAs also gather) is
@@ -89,15 +91,16 @@ def _ceil(a, b):
     return -(-a // b)
 
 
-def n_items(f, C, kind="tensor"):
+def n_items(f, C, kind="tensor", paired=True):
     """Prefix work items of a plan with C key tiles per split: every (row block, KV head,
-    key split) of every group once, a one-Q-tile tensor-core block's splits two at a time."""
+    key split) of every group once; with `paired` (sequential plans) a one-Q-tile
+    tensor-core block's splits two at a time."""
     rows = ROWS[kind]
     total = 0
     for p in f["prefix"]:
         blocks = _ceil(p["M"], rows)
         splits = _ceil(_ceil(p["lp"], KEY_TILE), C)
-        one = 1 if kind == "tensor" and 0 < p["M"] % rows <= Q_TILE else 0
+        one = 1 if paired and kind == "tensor" and 0 < p["M"] % rows <= Q_TILE else 0
         total += (blocks - one) * f["Hkv"] * splits + one * f["Hkv"] * _ceil(splits, 2)
     return total
 

@@ -347,18 +347,23 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
       const int32_t m = (int32_t)members[(size_t)gi].size() * g;
       k.mtiles[(size_t)gi] = (m + rows - 1) / rows;
       // a tensor-core row block with one Q tile's rows runs its tiles at about
-      // twice the rate: its items take two key splits each
+      // twice the rate: in a sequential plan its items take two key splits each;
+      // in a split plan one, and its CTA then gathers the longer for it
       k.single[(size_t)gi] = rows == kPrefixRowsPerCta && m % rows != 0 && m % rows <= kPrefixTileM;
     }
-    auto n_items = [&](int32_t C) {
+    // items of a plan with C tiles per split; `paired`: a one-Q-tile block's items
+    // take two splits each (sequential plans)
+    auto count_items = [&](int32_t C, bool paired) {
       int64_t units = 0;
       for (int32_t gi = 0; gi < G; ++gi) {
         const int64_t ns = (ntiles[(size_t)gi] + C - 1) / C;
-        const int64_t one = k.single[(size_t)gi];
+        const int64_t one = paired ? k.single[(size_t)gi] : 0;
         units += ((int64_t)k.mtiles[(size_t)gi] - one) * Hkv * ns + one * Hkv * ((ns + 1) / 2);
       }
       return units;
     };
+    auto n_items = [&](int32_t C) { return count_items(C, true); };
+    auto n_split_items = [&](int32_t C) { return count_items(C, false); };
     int32_t c_seq = max_ntiles;
     {
       double best_cost = 1e300;
@@ -375,15 +380,15 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
       const double waves = (double)((n_items(c_seq) + num_sms - 1) / num_sms);
       t_seq += std::max(prefix_bytes / (cm.bw_prefix_gbs * 1e3), waves * (std::min(c_seq, max_ntiles) * tile + item));
     }
-    auto item_us = [&](int32_t C) { return C * tile_split + item_split + cm.prefix_item_crowd_us * n_items(C); };
+    auto item_us = [&](int32_t C) { return C * tile_split + item_split + cm.prefix_item_crowd_us * n_split_items(C); };
     // the split launch for items of C tiles: the prefix CTAs gather a share when it
     // reaches kMinPrefixShare of a gather-only CTA's, else only the others gather
     const double gsm = rows == kPrefixRowsPerCta ? cm.gather_sm_gbs * cm.split_gather_ratio_tensor : cm.gather_sm_gbs;
     auto split_of = [&](int32_t C, bool* gather, double margin = 1.0) {
       const double it = margin * item_us(C);
-      SplitTime st = split_time(cm, num_sms, n_items(C), it, S, prefix_bytes, true, gsm);
+      SplitTime st = split_time(cm, num_sms, n_split_items(C), it, S, prefix_bytes, true, gsm);
       *gather = st.share >= kMinPrefixShare;
-      if (!*gather) st = split_time(cm, num_sms, n_items(C), it, S, prefix_bytes, false, gsm);
+      if (!*gather) st = split_time(cm, num_sms, n_split_items(C), it, S, prefix_bytes, false, gsm);
       if (rows == kPrefixRowsPerCta) st.t += cm.split_tensor_us;
       return st;
     };
@@ -392,7 +397,7 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
     const bool can_split = G > 0 && suffix_tokens > 0 && p->cascade_mode != GK_CASCADE_SEQUENTIAL;
     if (can_split && p->cascade_mode == GK_CASCADE_SPLIT && p->cascade_tiles > 0) {
       const int32_t C = std::min(p->cascade_tiles, max_ntiles);
-      if (n_items(C) <= num_sms) {
+      if (n_split_items(C) <= num_sms) {
         bool gth;
         c_split = C;
         t_split = split_of(C, &gth).t;
@@ -403,11 +408,11 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
       // holds the whole launch
       double t_best = 1e300;
       for (int32_t C = max_ntiles; can_split && C >= 1; --C) {
-        if (n_items(C) > num_sms) break;  // items only grow as C shrinks
+        if (n_split_items(C) > num_sms) break;  // items only grow as C shrinks
         bool gth;
         const double t = split_of(C, &gth, kSplitItemMargin).t;
         // the gather needs an SM of its own unless the prefix CTAs take part
-        if (!gth && n_items(C) >= num_sms) continue;
+        if (!gth && n_split_items(C) >= num_sms) continue;
         if (t < t_best - 1e-9) {
           t_best = t;
           c_split = C;
@@ -417,7 +422,7 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
       if (c_split > 0) t_split = split_of(c_split, &gth).t;
     }
     // balance the chosen split: the fewest tiles per item that gives as many items
-    while (c_split > 1 && n_items(c_split - 1) == n_items(c_split)) --c_split;
+    while (c_split > 1 && n_split_items(c_split - 1) == n_split_items(c_split)) --c_split;
     k.split = c_split > 0 && (p->cascade_mode == GK_CASCADE_SPLIT || t_split < t_seq);
     k.c = k.split ? c_split : c_seq;
     k.t_levels = k.split ? t_split : t_seq;
@@ -464,10 +469,11 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
     pre_bytes += gb;
     pre_flops += gf;
   }
-  // CTA order: longest splits first; within a length, (group, split, head, row block)
-  // so CTAs reading the same K/V tiles run side by side.  A one-Q-tile row block's
-  // items cover two consecutive splits (the second's entry is left empty).
-  struct Item { PrefixItemDev it; int32_t tiles; bool pair; };
+  // CTA order: longest items first (a one-Q-tile block's tiles count half); within a
+  // length, (group, split, head, row block) so CTAs reading the same K/V tiles run
+  // side by side.  In a sequential plan a one-Q-tile row block's items cover two
+  // consecutive splits (the second's entry is left empty).
+  struct Item { PrefixItemDev it; int32_t tiles; bool half; };
   std::vector<Item> items;
   for (int32_t gi = 0; gi < G; ++gi) {
     const PrefixGroupDev& gd = pl->groups[(size_t)gi];
@@ -475,16 +481,19 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
     for (int32_t s = 0; s < gd.nsplit; ++s) {
       for (int32_t h = 0; h < Hkv; ++h)
         for (int32_t mt = 0; mt <= last; ++mt) {
-          const bool pair = single[(size_t)gi] && mt == last;
+          const bool half = single[(size_t)gi] && mt == last;
+          const bool pair = half && !pl->split;
           if (pair && s % 2 != 0) continue;
           const int32_t n = pair ? std::min(2, gd.nsplit - s) : 1;
           const int32_t t0 = s * gd.split_tiles;
           const int32_t t1 = std::min(ntiles[(size_t)gi], t0 + n * gd.split_tiles);
-          items.push_back({PrefixItemDev{gi, mt, h, s, n, 0}, t1 - t0, pair});
+          items.push_back({PrefixItemDev{gi, mt, h, s, n, 0}, t1 - t0, half});
         }
     }
   }
-  std::stable_sort(items.begin(), items.end(), [](const Item& a, const Item& b2) { return a.tiles > b2.tiles; });
+  std::stable_sort(items.begin(), items.end(), [](const Item& a, const Item& b2) {
+    return (a.half ? a.tiles : 2 * a.tiles) > (b2.half ? b2.tiles : 2 * b2.tiles);
+  });
   for (auto& it : items) pl->prefix_items.push_back(it.it);
 
   // ---- gather work: cascade suffix and dense (flat) ------------------------------
@@ -506,7 +515,7 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
     if (prefix_cta_share > 0.0) {
       std::vector<double> it;
       const double crowd = cm.prefix_item_crowd_us * (double)items.size();
-      for (const Item& x : items) it.push_back((x.pair ? 0.5 : 1.0) * x.tiles * kp.tile_split + kp.item_split + crowd);
+      for (const Item& x : items) it.push_back((x.half ? 0.5 : 1.0) * x.tiles * kp.tile_split + kp.item_split + crowd);
       const double gsm = kp.rows == kPrefixRowsPerCta ? cm.gather_sm_gbs * cm.split_gather_ratio_tensor
                                                       : cm.gather_sm_gbs;
       w = split_weights(cm, num_sms, it, (double)S, gsm);

@@ -95,11 +95,12 @@ def test_every_geometry_both_backends(d, g, peaked):
                 info = gk.gk_plan_info(pl)
                 assert info["prefix_kernel"] == kernel and info["prefix_rows_per_item"] == rows
                 if name.startswith("split-"):
-                    # the forced plans: row blocks x KV heads x key splits of `tiles` tiles, the
-                    # last tensor-core block (44-48 rows: one Q tile) taking two splits per item
+                    # the forced plans: row blocks x KV heads x key splits of `tiles` tiles (in a
+                    # split plan the last tensor-core block, 44-48 rows: one Q tile, takes one
+                    # split per item like the others; sequential plans pair its splits)
                     assert info["cascade_split"] == 1 and info["prefix_tiles_per_item"] == tiles
                     full = w.B * g // rows
-                    last = 0 if w.B * g % rows == 0 else (-(-(4 // tiles) // 2) if kname == "tensor" else 4 // tiles)
+                    last = 0 if w.B * g % rows == 0 else 4 // tiles
                     assert info["prefix_ctas"] == (full * (4 // tiles) + last) * w.Hkv
                 seen_splits.add(info["cascade_split"])
                 q = gw.q(0)

@@ -108,6 +108,8 @@ def test_cost_model_closed_form():
     assert dispatch.n_items(f384, 1) == 8 * (8 + 4) and dispatch.n_items(f384, 3) == 8 * (3 + 2)
     f640 = dispatch.features([1000] * 128, [100] * 128, [0] * 128, 40, 8, 128)
     assert f640["prefix"][0]["M"] == 640 and dispatch.n_items(f640, 1) == 8 * (2 * 8 + 4)
+    # unpaired (split plans): every block takes one split per item
+    assert dispatch.n_items(f384, 1, paired=False) == 8 * 2 * 8 and dispatch.n_items(f640, 3, paired=False) == 8 * 3 * 3
     f420 = dispatch.features([1000] * 84, [100] * 84, [0] * 84, 40, 8, 128)
     assert dispatch.n_items(f420, 1) == 8 * 2 * 8 and dispatch.n_items(f384, 1, "warp") == 3 * 8 * 8
     # sequential plan, tensor-core items of one tile: one wave of 64 items, each 2 + 3 us
