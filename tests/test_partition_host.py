@@ -169,3 +169,60 @@ def test_per_request_partition_matches_algorithm_1(gk, seed):
             gk.gk_pool_set_gather_partition(pool, 7)
     finally:
         gk.gk_pool_destroy(pool)
+
+
+def test_split_slots_follow_each_item(gk):
+    """Split plan over two HOT groups whose items differ in length: the gather slot of each
+    prefix CTA is sized to when its own item ends (gk_plan_build, split arrangement).
+    Groups: 64 requests on a 16384-token prefix (128 key tiles) and 64 on a 4096-token one
+    (32 tiles), g = 4 (one 256-row block per KV head), 1000 suffix tokens each; forced split
+    with 48 tiles per item, which the planner balances to 43 (the fewest tiles giving as
+    many items): items of 43, 43, 42 tiles (group 1) and 32 tiles (group 2), 8 KV heads
+    each, longest first.  Tile 1 us, item 5 us beside the gather, 50 GB/s per SM,
+    gather-only CTAs starting at 4 us and prefix CTAs 4 us after their items, at the same
+    rate.  The common end T solves
+    120 (T - 4) + 16 (T - 52) + 8 (T - 51) + 8 (T - 41) = S / 50 GB/s, and a CTA's slot
+    weighs (T - start) / (T - 4); slot ends are the weighted shares of the token stream
+    rounded to 16 tokens."""
+    cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0, bw_suffix_gbs=6000.0,
+              c_merge_us=0.001, prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0, c_gather_us=4.0,
+              prefix_tile_split_us=1.0, warp_tile_us=1e3, warp_group_us=0.0, warp_item_us=1e3, warp_split_ratio=1.0,
+              prefix_cta_ramp_us=4.0, prefix_cta_gather_ratio=1.0, c_merge_state_us=0.0, prefix_item_split_us=5.0,
+              warp_item_split_us=1e3, prefix_item_crowd_us=0.0, split_gather_ratio_tensor=1.0, c_gather_split_us=4.0,
+              split_tensor_us=0.0)
+    import json
+    pool = gk.gk_pool_create(1, 32, 8, 128, 16384 + 4096 + 32, 128 * 1000 + 64, 1, 0)
+    try:
+        gk.gk_cost_model_load(pool, json.dumps(cm))
+        gk.gk_pool_set_prefix_kernel(pool, gk.GK_PREFIX_TENSOR)
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SPLIT, 48)
+        a, b = gk.gk_prefix_alloc(pool, 16384), gk.gk_prefix_alloc(pool, 4096)
+        bases = [a] * 64 + [b] * 64
+        lps = [16384] * 64 + [4096] * 64
+        slens = [1000] * 128
+        _, plan = _plan(gk, pool, bases, lps, slens)
+        s = gk.gk_plan_info(plan)
+        assert (s["cascade_split"], s["prefix_ctas"], s["prefix_ctas_gather"], s["suffix_ctas"]) == (1, 32, 1, SMS)
+        assert s["prefix_tiles_per_item"] == 43
+        begin, segs = gk.gk_plan_segments(plan, False)
+        _check_cover(begin, segs, slens)
+        _check_entries(segs, False)
+        got = _tokens(begin, segs)
+        gk.gk_plan_destroy(plan)
+    finally:
+        gk.gk_pool_destroy(pool)
+    S_us = 128 * 1000 * 4096 / 50e3                  # the gather in SM-us at 50 GB/s
+    T = (S_us + 120 * 4 + 16 * 52 + 8 * 51 + 8 * 41) / 152
+    assert abs(T - 82.4590) < 1e-3
+    w = [(T - 52) / (T - 4)] * 16 + [(T - 51) / (T - 4)] * 8 + [(T - 41) / (T - 4)] * 8 + [1.0] * 120
+    total, acc, ends = 128000, 0.0, []
+    for x in w:
+        acc += x
+        e = int(total * acc / sum(w) + 0.5)
+        e = (e + 8) // 16 * 16
+        ends.append(min(total, max(e, ends[-1] if ends else 0)))
+    ends[-1] = total
+    want = np.diff([0] + ends).tolist()
+    assert got == want
+    # shorter items, longer gathers: about 0.39 and 0.53 of a gather-only CTA's share
+    assert 0.37 < np.mean(got[:16]) / np.mean(got[32:]) < 0.41 and 0.51 < np.mean(got[24:32]) / np.mean(got[32:]) < 0.55
