@@ -65,6 +65,9 @@ def _args():
                     help="work split of the stand-alone gathers (gk_pool_set_gather_partition)")
     ap.add_argument("--no-stages", action="store_true",
                     help="skip the stand-alone timing of each kernel (the 'stages' object)")
+    ap.add_argument("--no-sm-speeds", action="store_true",
+                    help="plan split launches without per-SM speeds (by default they are measured after the "
+                         "warm-up with gk_sm_speeds_measure)")
     return ap.parse_args()
 
 
@@ -599,6 +602,21 @@ def run_ours(a, w):
     err = gk.gk_device_error(pool, stream)
     if err:
         raise RuntimeError(f"device error word {err} during warm-up")
+    # per-SM gather speeds from the step plan's own suffix gather (layer 0, the step's new
+    # tokens left out so that the pool is not written), then one more warm-up step planned
+    # with them
+    sm_speeds = "off"
+    if not a.no_sm_speeds and int(batch.suffix_len.sum()) > 0:
+        batch.set_device(d_q=q_all[0], d_out=out_all[0], d_lse=lse_all[0])
+        batch.c.d_new_k = None
+        batch.c.d_new_v = None
+        sp = gk.gk_sm_speeds_measure(pool, stream, 0, batch, plan[0], reps=5)
+        sm_speeds = f"measured (gk_sm_speeds_measure, 5 launches; slowest {sp.min():.3f}, fastest {sp.max():.3f})"
+        step()
+        torch.cuda.synchronize()
+        err = gk.gk_device_error(pool, stream)
+        if err:
+            raise RuntimeError(f"device error word {err} after measuring SM speeds")
     if world > 1:
         torch.distributed.barrier()
 
@@ -765,7 +783,7 @@ def run_ours(a, w):
                 "cost_model": "paged_kv_cache_pool_gb300/cost_model_gb300.json" if os.path.exists(cm_path) else "library defaults"}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
             "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic", "config": _config_dict(w, backend_name),
+            "dtype": "bf16", "data": "synthetic", "config": dict(_config_dict(w, backend_name), sm_speeds=sm_speeds),
             "clocks": clk, "e2e": e2e, "gpu_launches": gpu_launches, "roofline": roof,
             "cpu_baseline": cpu, "kernels": kernels, "stages": stages, "dispatch": dispatch,
             "query_rows_per_s": value * Hq,

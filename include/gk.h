@@ -233,6 +233,8 @@ typedef struct gk_plan_summary {
                                      1, 2, 4 or 8; 0 for tensor-core items */
   int32_t prefix_ctas_gather;     /* split plans: 1 when the prefix CTAs also gather a share of the
                                      suffix after their items, 0 when only the other CTAs gather */
+  int32_t sm_slots;               /* split plans: 1 when the slots are planned per SM from the pool's
+                                     SM speeds (gk_pool_set_sm_speeds), 0 when CTA b takes slot b */
 } gk_plan_summary;
 
 /* Plan one decode step: group requests by HOT prefix (stable, first appearance),
@@ -440,7 +442,9 @@ gk_status gk_pool_set_gather_partition(gk_pool* pool, gk_gather_partition partit
  * prefix once), and Section 3.6 routes between them on M_eff.
  *  GK_PREFIX_AUTO (default): per step, the one whose cascade the cost model
  *    predicts faster, the tensor-core items only when predicted at least 10 %
- *    faster (their predictions at small steps run low).
+ *    faster (their predictions at small steps run low) and never when every
+ *    group stacks at most 64 rows per KV head (M_eff <= 64, which a tensor-core
+ *    item pads to 256).
  *  GK_PREFIX_TENSOR: tcgen05 items of 256 stacked rows (two 128-row tiles).
  *  GK_PREFIX_WARP: warp-MMA items of 128 stacked rows (8 warps x 16 rows), no
  *    tensor memory; meant for small M_eff.
@@ -453,6 +457,42 @@ typedef enum gk_prefix_kernel {
   GK_PREFIX_WARP = 2
 } gk_prefix_kernel;
 gk_status gk_pool_set_prefix_kernel(gk_pool* pool, gk_prefix_kernel kernel);
+/* SM-aware split launches (no counterpart in the pages: they assume a uniform
+ * GPU).  On GB300 some SMs gather COLD rows 5-10 % slower than others, the same
+ * from launch to launch, so equal gather slots end at different times and the
+ * launch waits for the slowest.  With SM speeds set, split plans size each
+ * SM's slot by its speed, give the prefix items to the slowest SMs (the longest
+ * item to the slowest), and the split launch's CTA on SM s takes the slot
+ * planned for s (an atomic claim per launch; a slot already taken sends the CTA
+ * to the next free one, so every slot is run exactly once whatever SMs the
+ * CTAs land on).  The results are the same attention whichever slots run where;
+ * the partial-state boundaries, and so the last bits, follow the speeds.
+ *  - gk_pool_set_sm_speeds: n speeds (relative; any positive scale) for SM ids
+ *    0 .. n-1, n = the device's SM count (152 for a pool without device
+ *    storage, which plans as for one GB300); n = 0 clears them (plans as
+ *    without).  Host only.  GK_ERR_INVALID for another n or a speed that is not
+ *    positive and finite.  Plans built before keep their slots.
+ *  - gk_pool_get_sm_speeds: *n = the count set (0 when none) and, when speeds is
+ *    not NULL, the speeds (normalised to mean 1).
+ *  - gk_sm_speeds_measure: runs the plan's gather `reps` times on `stream`,
+ *    each launch alone, with each CTA's SM id and times recorded by the kernel:
+ *    a split plan's own launch (gk_cascade_levels; a slot's rate counts its
+ *    gather, after its item, and prefix and gather-only slots are each scaled
+ *    to their own mean in the launch) or a sequential plan's stand-alone suffix
+ *    gather (gk_cascade_suffix).  An SM's speed is the median over the launches
+ *    of the scaled tokens per us of the slots it ran (slots with under a quarter
+ *    of the largest one's tokens are left out), normalised to mean 1; SMs
+ *    without a sample get 1.  Installs the speeds in the pool and, when speeds
+ *    is not NULL, writes them there (dev SM count entries).  The launches write
+ *    the plan's partial states (and the outputs of requests one CTA covers) and,
+ *    with a fused append, the step's tokens, as the decode calls do.  Blocking;
+ *    allocates and frees its own 32 bytes per CTA of device memory.
+ *    GK_ERR_INVALID when the plan has no suffix segments or reps is not in
+ *    1 .. 64. */
+gk_status gk_pool_set_sm_speeds(gk_pool* pool, const float* speeds, int32_t n);
+gk_status gk_pool_get_sm_speeds(const gk_pool* pool, float* speeds, int32_t* n);
+gk_status gk_sm_speeds_measure(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch,
+                               const gk_plan* plan, int32_t reps, float* speeds);
 gk_status gk_cost_model_get(const gk_pool* pool, gk_cost_model* cm);
 /* Re-fit the cost model on this GPU (GraniKV Section 3.6: the routing rule stays
  * and its numbers are re-fit per GPU; Appendix B.4b's sweep).  Times, with CUDA

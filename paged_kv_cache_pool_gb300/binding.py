@@ -54,7 +54,8 @@ class gk_plan_summary(ctypes.Structure):
                 ("suffix_ctas", c_i32), ("dense_ctas", c_i32), ("num_partials", c_i32), ("dense_merge", c_i32),
                 ("prefix_bytes", c_i64), ("prefix_flops", c_i64), ("suffix_bytes", c_i64), ("dense_bytes", c_i64),
                 ("cascade_split", c_i32), ("prefix_tiles_per_item", c_i32), ("prefix_kernel", c_i32),
-                ("prefix_rows_per_item", c_i32), ("prefix_row_groups", c_i32), ("prefix_ctas_gather", c_i32)]
+                ("prefix_rows_per_item", c_i32), ("prefix_row_groups", c_i32), ("prefix_ctas_gather", c_i32),
+                ("sm_slots", c_i32)]
 
 
 class gk_cost_model(ctypes.Structure):
@@ -112,6 +113,9 @@ _SIGS = {
     "gk_pool_set_cascade_mode": (c_i32, [c_vp, c_i32, c_i32]),
     "gk_pool_set_gather_partition": (c_i32, [c_vp, c_i32]),
     "gk_pool_set_prefix_kernel": (c_i32, [c_vp, c_i32]),
+    "gk_pool_set_sm_speeds": (c_i32, [c_vp, P(ctypes.c_float), c_i32]),
+    "gk_pool_get_sm_speeds": (c_i32, [c_vp, P(ctypes.c_float), P(c_i32)]),
+    "gk_sm_speeds_measure": (c_i32, [c_vp, c_vp, c_i32, P(gk_batch), c_vp, c_i32, P(ctypes.c_float)]),
     "gk_calibrate": (c_i32, [c_vp, c_vp, ctypes.c_char_p]),
     "gk_device_error": (c_i32, [c_vp, c_vp, P(c_i32)]),
 }
@@ -466,6 +470,32 @@ GK_PREFIX_AUTO, GK_PREFIX_TENSOR, GK_PREFIX_WARP = 0, 1, 2
 
 def gk_pool_set_prefix_kernel(pool, kernel):
     _check(lib().gk_pool_set_prefix_kernel(pool, int(kernel)), pool)
+
+
+def gk_pool_set_sm_speeds(pool, speeds):
+    """speeds: one per SM of the device, or None / empty to clear."""
+    if speeds is None or len(speeds) == 0:
+        _check(lib().gk_pool_set_sm_speeds(pool, None, 0), pool)
+        return
+    a = np.ascontiguousarray(speeds, dtype=np.float32)
+    _check(lib().gk_pool_set_sm_speeds(pool, a.ctypes.data_as(P(ctypes.c_float)), len(a)), pool)
+
+
+def gk_pool_get_sm_speeds(pool):
+    n = c_i32()
+    _check(lib().gk_pool_get_sm_speeds(pool, None, ctypes.byref(n)), pool)
+    a = np.zeros(n.value, np.float32)
+    if n.value:
+        _check(lib().gk_pool_get_sm_speeds(pool, a.ctypes.data_as(P(ctypes.c_float)), ctypes.byref(n)), pool)
+    return a
+
+
+def gk_sm_speeds_measure(pool, stream, layer, batch, plan, reps=5):
+    """-> the measured per-SM speeds (installed in the pool)."""
+    n = c_i32()
+    _check(lib().gk_pool_get_sm_speeds(pool, None, ctypes.byref(n)), pool)
+    _check(lib().gk_sm_speeds_measure(pool, _stream(stream), layer, ctypes.byref(batch.c), plan, reps, None), pool)
+    return gk_pool_get_sm_speeds(pool)
 
 
 def gk_calibrate(pool, stream=None, json_out=None):

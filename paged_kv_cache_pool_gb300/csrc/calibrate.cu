@@ -703,3 +703,109 @@ extern "C" gk_status gk_calibrate(gk_pool* pool, void* stream, const char* json_
   }
   return GK_OK;
 }
+
+// Per-SM gather speeds, taken where the plan runs its gather: a split plan's
+// own launch (each slot's SM id, start, end of its item and end of its gather,
+// recorded by the kernel; a slot's rate counts its gather only, and prefix and
+// gather-only slots are each scaled to their own mean in the launch, since a
+// gather that starts beside running items sees another HBM than one that
+// starts after them), or a sequential plan's stand-alone suffix gather (each
+// CTA's SM id, start and end).  Each launch alone.
+extern "C" gk_status gk_sm_speeds_measure(gk_pool* pool, void* stream, int32_t layer, const gk_batch* batch,
+                                          const gk_plan* plan, int32_t reps, float* speeds) {
+  if (!pool || !batch || !plan) return GK_ERR_INVALID;
+  gk::Pool* p = &pool->impl;
+  if (reps < 1 || reps > 64) return gk::fail(p, GK_ERR_INVALID, "reps must be in 1 .. 64");
+  gk_status st = gk::ensure_device(p);
+  if (st != GK_OK) return st;
+  const gk::Plan& pl = plan->impl;
+  if (pl.pool != p) return gk::fail(p, GK_ERR_INVALID, "plan belongs to another pool");
+  if (layer < 0 || layer >= p->cfg.num_layers) return gk::fail(p, GK_ERR_INVALID, "layer out of range");
+  if (!pl.uploaded || !pl.d_buf) return gk::fail(p, GK_ERR_INVALID, "plan has no device tables");
+  const int gctas = pl.summary.suffix_ctas;
+  if (gctas <= 0 || pl.suf_segs.empty() || (int)pl.suf_seg_begin.size() != gctas + 1)
+    return gk::fail(p, GK_ERR_INVALID, "the plan has no suffix segments");
+  const bool split = pl.split;
+  const int n_pre = split ? (int)pl.prefix_items.size() : 0;
+  const int ctas = split ? std::max(n_pre, gctas) : gctas;
+  const int words = split ? 4 : 3;
+  std::vector<int64_t> tok((size_t)ctas, 0);
+  int64_t tmax = 0;
+  for (int b = 0; b < gctas; ++b) {
+    for (int32_t i = pl.suf_seg_begin[(size_t)b]; i < pl.suf_seg_begin[(size_t)b + 1]; ++i)
+      tok[(size_t)b] += pl.suf_segs[(size_t)i].t1 - pl.suf_segs[(size_t)i].t0;
+    tmax = std::max(tmax, tok[(size_t)b]);
+  }
+  const size_t bytes = sizeof(unsigned long long) * words * (size_t)ctas;
+  unsigned long long* d_st = nullptr;
+  cudaError_t e = cudaMalloc(&d_st, bytes);
+  if (e != cudaSuccess) return gk::cuda_fail(p, e, "cudaMalloc(timeline stamps)");
+  std::vector<unsigned long long> h((size_t)words * ctas);
+  const int n_sm = p->dev.num_sms;
+  std::vector<std::vector<double>> rates((size_t)n_sm);
+  cudaStream_t s = (cudaStream_t)stream;
+  for (int r = 0; r < reps && st == GK_OK; ++r) {
+    if ((e = cudaMemsetAsync(d_st, 0, bytes, s)) != cudaSuccess) {
+      st = gk::cuda_fail(p, e, "cudaMemsetAsync(timeline stamps)");
+      break;
+    }
+    gk::LaunchCommon lc{&p->cfg, p->d_error, n_sm};
+    int le;
+    if (split) {
+      lc.split_stamps = d_st;
+      if (!pl.slot_of_sm.empty()) {
+        if (++p->split_epoch == 0) {
+          if ((e = cudaMemsetAsync(p->d_slot_claim, 0, sizeof(uint32_t) * (size_t)n_sm, s)) != cudaSuccess) {
+            st = gk::cuda_fail(p, e, "cudaMemsetAsync(slot claims)");
+            break;
+          }
+          ++p->split_epoch;
+        }
+        lc.slot_claim = p->d_slot_claim;
+        lc.epoch = p->split_epoch;
+      }
+      le = gk::launch_cascade_split(lc, stream, layer, batch, &pl);
+    } else {
+      lc.gather_stamps = d_st;
+      le = gk::launch_gather(lc, stream, layer, batch, &pl, false);
+    }
+    if (le) {
+      st = gk::cuda_fail(p, le, split ? "split cascade kernel" : "suffix gather kernel");
+      break;
+    }
+    if ((e = cudaMemcpyAsync(h.data(), d_st, bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+        (e = cudaStreamSynchronize(s)) != cudaSuccess) {
+      st = gk::cuda_fail(p, e, "reading the timeline stamps");
+      break;
+    }
+    // this launch's rates, each role scaled to its own mean
+    std::vector<std::pair<int, double>> got[2];
+    for (int b = 0; b < ctas; ++b) {
+      const unsigned long long* w = &h[(size_t)words * b];
+      const unsigned long long sm = w[0], t0 = split ? w[2] : w[1], t1 = split ? w[3] : w[2];
+      if (sm >= (unsigned long long)n_sm || t1 <= t0 || 4 * tok[(size_t)b] < tmax) continue;
+      got[b < n_pre ? 1 : 0].push_back({(int)sm, (double)tok[(size_t)b] / ((double)(t1 - t0) * 1e-3)});
+    }
+    for (auto& role : got) {
+      double mean = 0.0;
+      for (auto& x : role) mean += x.second;
+      if (role.empty() || mean <= 0.0) continue;
+      mean /= (double)role.size();
+      for (auto& x : role) rates[(size_t)x.first].push_back(x.second / mean);
+    }
+  }
+  cudaFree(d_st);
+  if (st != GK_OK) return st;
+  std::vector<float> v((size_t)n_sm, 1.0f);
+  int have = 0;
+  for (int sm = 0; sm < n_sm; ++sm)
+    if (!rates[(size_t)sm].empty()) {
+      v[(size_t)sm] = (float)gk::median(rates[(size_t)sm]);
+      ++have;
+    }
+  if (have == 0) return gk::fail(p, GK_ERR_INVALID, "no CTA of the plan's gather gave a speed");
+  st = gk_pool_set_sm_speeds(pool, v.data(), n_sm);
+  if (st != GK_OK) return st;
+  if (speeds) gk_pool_get_sm_speeds(pool, speeds, &have);
+  return GK_OK;
+}

@@ -25,7 +25,34 @@ struct SplitParams {
   int32_t n_pre;        // CTAs [0, n_pre) first run prefix item b
   int32_t n_gather;     // CTAs [0, n_gather) gather suffix slot b
   uint32_t data_bytes;  // shared data area: max of the prefix and gather layouts
+  // SM-indexed slots (plans sized by the pool's SM speeds), else null: the CTA on SM s
+  // takes slot slot_of_sm[s] (its prefix item, if the slot has one, and its gather
+  // slot), claimed in slot_claim with this launch's tag; a slot already taken this
+  // launch sends the CTA to the next free one
+  const int32_t* slot_of_sm;
+  uint32_t* slot_claim;
+  uint32_t epoch;
+  int32_t n_slots;
+  unsigned long long* stamps;  // per slot: SM id, start, gather start, end (%globaltimer), or null
 };
+
+// The slot of the calling CTA (thread 0): its SM's planned slot if free this launch,
+// else the next free one.  Every CTA claims exactly one of the n_slots slots, which
+// the launch has as many CTAs as (atomic claims, no waiting); an SM that runs two
+// CTAs one after the other gives the second another SM's slot.
+__device__ __forceinline__ int claim_slot(const SplitParams& f) {
+  unsigned smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  const int n = f.n_slots;
+  int want = smid < (unsigned)n ? f.slot_of_sm[smid] : (int)(smid % (unsigned)n);
+  if (want < 0 || want >= n) want = 0;
+  for (int k = 0; k < n; ++k) {
+    int t = want + k;
+    if (t >= n) t -= n;
+    if (atomicMax(&f.slot_claim[t], f.epoch) < f.epoch) return t;
+  }
+  return (int)blockIdx.x;  // unreachable: n CTAs claim n slots
+}
 
 constexpr uint32_t kSplitCtlBytes = prefix::kCtlBytes;
 static_assert(1024 + kSplitCtlBytes <= gather::kSoleCtaReserve, "control area exceeds the gather reserve");
@@ -54,7 +81,19 @@ __global__ void __launch_bounds__(WARP ? prefix_warp::kThreads : kSplitThreads, 
   const uint32_t base = (raw + 1023u) & ~1023u;
   const uint32_t ctl = base + f.data_bytes;
   uint8_t* ctl_ptr = smem_raw + (ctl - raw);
-  const int b = blockIdx.x;
+  __shared__ int s_slot;
+  int b = blockIdx.x;
+  if (f.slot_of_sm) {
+    if (threadIdx.x == 0) s_slot = claim_slot(f);
+    __syncthreads();
+    b = s_slot;
+  }
+  if (f.stamps && threadIdx.x == 0) {
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    f.stamps[4 * b] = smid;
+    f.stamps[4 * b + 1] = globaltimer_ns();
+  }
 
   griddep_launch_dependents();
   if (WARP && b < f.n_pre) {
@@ -83,8 +122,10 @@ __global__ void __launch_bounds__(WARP ? prefix_warp::kThreads : kSplitThreads, 
     }
     if (!ok) return;  // same value on every thread
   }
+  if (f.stamps && threadIdx.x == 0) f.stamps[4 * b + 2] = globaltimer_ns();
   // the item's staging area is free: the gather re-initialises the shared memory
   if (b < f.n_gather) gather::gather_segments<D, G, false>(f.gp, base, b);
+  if (f.stamps && (threadIdx.x & 31) == 0) atomicMax(&f.stamps[4 * b + 3], (unsigned long long)globaltimer_ns());
 }
 
 template <int D, int G>
@@ -106,8 +147,16 @@ int launch_cascade_split(const LaunchCommon& lc, void* stream, int32_t layer, co
   fp.n_pre = (int32_t)pl->prefix_items.size();
   const bool wi = pl->prefix_kind == 1;
   fp.n_gather = pl->summary.suffix_ctas;
+  fp.stamps = lc.split_stamps;
   const int ctas = std::max(fp.n_pre, fp.n_gather);
   if (ctas == 0) return 0;
+  if (!pl->slot_of_sm.empty()) {
+    if (!lc.slot_claim || (int)pl->slot_of_sm.size() != ctas) return (int)cudaErrorInvalidValue;
+    fp.slot_of_sm = (const int32_t*)((const uint8_t*)pl->d_buf + pl->off_slot_of_sm);
+    fp.slot_claim = lc.slot_claim;
+    fp.epoch = lc.epoch;
+    fp.n_slots = ctas;
+  }
   const int g = c.num_q_heads / c.num_kv_heads;
   cudaStream_t st = (cudaStream_t)stream;
   if (c.head_dim == 128) {

@@ -6,22 +6,36 @@ namespace gk {
 using namespace gather;
 namespace {
 
+struct GatherLaunch {
+  GatherParams p;
+  unsigned long long* stamps;  // per CTA: SM id, start, end of its gather (%globaltimer), or null
+};
+
 template <int D, int G, bool DENSE>
-__global__ void __launch_bounds__(kGatherThreads, 1) gather_kernel(const GatherParams p) {
+__global__ void __launch_bounds__(kGatherThreads, 1) gather_kernel(const GatherLaunch g) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
+  const int b = blockIdx.x;
+  if (g.stamps && threadIdx.x == 0) {
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    g.stamps[3 * b] = smid;
+    g.stamps[3 * b + 1] = globaltimer_ns();
+  }
   griddep_launch_dependents();
-  gather_segments<D, G, DENSE>(p, base, blockIdx.x);
+  gather_segments<D, G, DENSE>(g.p, base, b);
+  if (g.stamps && (threadIdx.x & 31) == 0) atomicMax(&g.stamps[3 * b + 2], (unsigned long long)globaltimer_ns());
 }
 
 template <int D, int G>
-int launch_gather_t(const GatherParams& gp, int ctas, cudaStream_t st) {
+int launch_gather_t(const GatherLaunch& gl, int ctas, cudaStream_t st) {
+  const GatherParams& gp = gl.p;
   const size_t smem = gather_smem_bytes(gp.Hkv, D, gp.nst);
   auto kern = gp.dense ? gather_kernel<D, G, true> : gather_kernel<D, G, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  e = launch_pdl(kern, dim3(ctas), dim3(32 * gp.Hkv), smem, st, gp);
+  e = launch_pdl(kern, dim3(ctas), dim3(32 * gp.Hkv), smem, st, gl);
   return (int)e;
 }
 
@@ -74,8 +88,9 @@ int fill_gather_params(const LaunchCommon& lc, int32_t layer, const gk_batch* b,
 int launch_gather(const LaunchCommon& lc, void* stream, int32_t layer, const gk_batch* b, const Plan* pl,
                   bool dense) {
   const gk_pool_config& c = *lc.cfg;
-  GatherParams gp;
-  if (int e = fill_gather_params(lc, layer, b, pl, dense, &gp)) return e;
+  GatherLaunch gp;
+  if (int e = fill_gather_params(lc, layer, b, pl, dense, &gp.p)) return e;
+  gp.stamps = lc.gather_stamps;
   const int ctas = dense ? pl->summary.dense_ctas : pl->summary.suffix_ctas;
   if (ctas <= 0) return 0;
   const int g = c.num_q_heads / c.num_kv_heads;

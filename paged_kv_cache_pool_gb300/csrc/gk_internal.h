@@ -102,6 +102,12 @@ struct Pool {
   std::string last_error;
   DeviceInfo dev;
   int32_t* d_error = nullptr;        // device error word (allocated on first device use)
+  // SM-aware split launches: each SM's gather speed relative to the mean (empty: not
+  // used), the per-slot claim words of the split launch and the launch counter that
+  // tags a claim to one launch
+  std::vector<float> sm_speed;
+  uint32_t* d_slot_claim = nullptr;  // [dev.num_sms] (allocated on first device use)
+  uint32_t split_epoch = 0;
   int32_t g() const { return cfg.num_q_heads / cfg.num_kv_heads; }
 };
 
@@ -176,6 +182,10 @@ struct Plan {
   bool uploaded = false;
   bool split = false;                    // cascade arrangement: prefix items and suffix gather side by side
   int32_t prefix_kind = 0;               // 0: tensor-core items (256 rows), 1: warp-MMA items (128 rows)
+  // split plans sized by the pool's SM speeds: slot_of_sm[s] = the work slot (prefix
+  // item and gather slot) planned for SM s; empty: CTA b takes slot b
+  std::vector<int32_t> slot_of_sm;
+  size_t off_slot_of_sm = 0;
 };
 
 // host half of gk_plan_build: grouping, work lists and partial-state layout (no device work)
@@ -203,6 +213,13 @@ struct LaunchCommon {
   const gk_pool_config* cfg;
   int32_t* d_error;
   int num_sms;
+  // split launches of plans with SM-indexed slots: the claim words and this launch's tag
+  uint32_t* slot_claim = nullptr;
+  uint32_t epoch = 0;
+  // stand-alone gathers: per-CTA SM id, start and end (%globaltimer), when not null
+  unsigned long long* gather_stamps = nullptr;
+  // split launches: per-slot SM id, start, start of its gather and end, when not null
+  unsigned long long* split_stamps = nullptr;
 };
 
 int launch_cow_copy(const LaunchCommon& lc, void* stream, int32_t layer, int32_t n_cow,

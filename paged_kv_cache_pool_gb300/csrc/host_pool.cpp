@@ -176,6 +176,14 @@ gk_status ensure_device(Pool* p) {
     e = cudaMemset(p->d_error, 0, sizeof(int32_t));
     if (e != cudaSuccess) return cuda_fail(p, e, "cudaMemset(error word)");
   }
+  if (!p->d_slot_claim) {
+    const size_t bytes = sizeof(uint32_t) * (size_t)p->dev.num_sms;
+    cudaError_t e = cudaMalloc(&p->d_slot_claim, bytes);
+    if (e != cudaSuccess) return cuda_fail(p, e, "cudaMalloc(slot claims)");
+    e = cudaMemset(p->d_slot_claim, 0, bytes);
+    if (e != cudaSuccess) return cuda_fail(p, e, "cudaMemset(slot claims)");
+    p->split_epoch = 0;
+  }
   return GK_OK;
 }
 
@@ -280,6 +288,7 @@ gk_status gk_pool_create(const gk_pool_config* cfg, gk_pool** out) {
 void gk_pool_destroy(gk_pool* pool) {
   if (!pool) return;
   if (pool->impl.d_error) cudaFree(pool->impl.d_error);
+  if (pool->impl.d_slot_claim) cudaFree(pool->impl.d_slot_claim);
   delete pool;
 }
 

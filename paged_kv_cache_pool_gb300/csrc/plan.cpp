@@ -29,8 +29,12 @@ constexpr double kMinPrefixShare = 0.15;
 // item time.
 constexpr double kSplitItemMargin = 1.15;
 // GK_PREFIX_AUTO keeps tensor-core items only when their cascade is predicted
-// faster than the warp-MMA items' by this factor.
+// faster than the warp-MMA items' by this factor, and never for a step whose
+// groups stack at most kWarpOnlyMeff rows per KV head: a tensor-core item pads
+// them to 256 rows, and on the GB300 sweep the warp-MMA items won every such
+// step the model would have given to tensor-core items.
 constexpr double kTensorAutoEdge = 0.9;
+constexpr int32_t kWarpOnlyMeff = 64;
 
 }  // namespace
 
@@ -64,26 +68,33 @@ SplitTime split_time(const gk_cost_model& cm, int num_sms, int64_t n_pre, double
   return r;
 }
 
-// Gather weights of the CTAs of a split launch whose prefix CTAs gather, one
-// prefix item time per prefix CTA (it[b], CTA b < it.size()): items of different
-// lengths leave their CTAs different times to gather.  CTA b starts gathering at
-// s_b = max(c_gather_split, it[b] + prefix_cta_ramp), at prefix_cta_gather_ratio
-// (e) of a gather-only CTA's rate; gather-only CTAs start at c_gather_split.  The
-// common end T is the one at which the CTAs together gather W = S / gather_sm
-// SM-us:  (num_sms - n_pre) (T - c) + sum_b e * max(0, T - s_b) = W  (increasing
-// in T: bisection).  Weight = a CTA's tokens over a gather-only CTA's (1 for
-// those, at most e for the others).
+// Gather weights of the CTAs (slots) of a split launch, one prefix item time per
+// prefix slot (it[b], slot b < it.size(); none when the prefix CTAs do not
+// gather) and one relative gather speed per slot (v[b]: the speed of the SM the
+// slot is planned on, 1 without SM speeds).  Items of different lengths leave
+// their CTAs different times to gather, and SMs gather at different speeds.
+// Slot b starts gathering at s_b = max(c_gather_split, it[b] + prefix_cta_ramp),
+// at prefix_cta_gather_ratio (e) of the rate; gather-only slots at c =
+// c_gather_split.  The common end T is the one at which the slots together gather
+// W = S / gather_sm SM-us:
+//   sum_gather-only v_x (T - c) + sum_b e v_b max(0, T - s_b) = W
+// (increasing in T: bisection).  Weight = a slot's tokens over those of a
+// gather-only slot of speed 1.
 std::vector<double> split_weights(const gk_cost_model& cm, int num_sms, const std::vector<double>& it, double S,
-                                  double gather_sm_gbs) {
+                                  double gather_sm_gbs, const std::vector<double>& v, bool prefix_gathers) {
   std::vector<double> w((size_t)num_sms, 1.0);
   const double c = cm.c_gather_split_us, e = cm.prefix_cta_gather_ratio;
   const double W = S / (gather_sm_gbs * 1e3);
   const size_t n_pre = std::min(it.size(), w.size());
-  std::vector<double> start(n_pre);
-  for (size_t b = 0; b < n_pre; ++b) start[b] = std::max(c, it[b] + cm.prefix_cta_ramp_us);
+  std::vector<double> start(w.size(), c), rate(w.size(), 1.0);
+  for (size_t x = 0; x < w.size(); ++x) rate[x] = x < v.size() ? v[x] : 1.0;
+  for (size_t b = 0; b < n_pre; ++b) {
+    start[b] = std::max(c, it[b] + cm.prefix_cta_ramp_us);
+    rate[b] *= prefix_gathers ? e : 0.0;
+  }
   auto capacity = [&](double T) {
-    double cap = (double)(w.size() - n_pre) * std::max(0.0, T - c);
-    for (size_t b = 0; b < n_pre; ++b) cap += e * std::max(0.0, T - start[b]);
+    double cap = 0.0;
+    for (size_t x = 0; x < w.size(); ++x) cap += rate[x] * std::max(0.0, T - start[x]);
     return cap;
   };
   double lo = c, hi = c + 1.0;
@@ -93,7 +104,7 @@ std::vector<double> split_weights(const gk_cost_model& cm, int num_sms, const st
     (capacity(mid) < W ? lo : hi) = mid;
   }
   const double full = std::max(hi - c, 1e-9);
-  for (size_t b = 0; b < n_pre; ++b) w[b] = e * std::max(0.0, hi - start[b]) / full;
+  for (size_t x = 0; x < w.size(); ++x) w[x] = rate[x] * std::max(0.0, hi - start[x]) / full;
   return w;
 }
 
@@ -508,20 +519,31 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
     suf_tokens += n_suf[(size_t)r];
     dense_tokens += n_dense[(size_t)r];
   }
+  pl->slot_of_sm.clear();
   if (pl->split) {
     // one slot per SM; a prefix CTA's slot is sized to the time its own item
-    // leaves it (a one-Q-tile block's item runs its tiles at about twice the rate)
-    std::vector<double> w((size_t)num_sms, 1.0);
-    if (prefix_cta_share > 0.0) {
-      std::vector<double> it;
-      const double crowd = cm.prefix_item_crowd_us * (double)items.size();
-      for (const Item& x : items) it.push_back((x.half ? 0.5 : 1.0) * x.tiles * kp.tile_split + kp.item_split + crowd);
-      const double gsm = kp.rows == kPrefixRowsPerCta ? cm.gather_sm_gbs * cm.split_gather_ratio_tensor
-                                                      : cm.gather_sm_gbs;
-      w = split_weights(cm, num_sms, it, (double)S, gsm);
-    } else {
-      for (size_t b2 = 0; b2 < pl->prefix_items.size() && b2 < w.size(); ++b2) w[b2] = 0.0;
+    // leaves it (a one-Q-tile block's item runs its tiles at about twice the rate).
+    // With the pool's SM speeds the slots are planned per SM: the slowest SMs
+    // take the prefix items (the longest on the slowest), and every slot's
+    // gather follows its SM's speed.
+    std::vector<double> v((size_t)num_sms, 1.0);
+    if ((int)p->sm_speed.size() == num_sms) {
+      std::vector<int32_t> order((size_t)num_sms);
+      for (int32_t s = 0; s < num_sms; ++s) order[(size_t)s] = s;
+      std::stable_sort(order.begin(), order.end(),
+                       [&](int32_t a, int32_t b2) { return p->sm_speed[(size_t)a] < p->sm_speed[(size_t)b2]; });
+      pl->slot_of_sm.assign((size_t)num_sms, 0);
+      for (int32_t k = 0; k < num_sms; ++k) {
+        pl->slot_of_sm[(size_t)order[(size_t)k]] = k;
+        v[(size_t)k] = p->sm_speed[(size_t)order[(size_t)k]];
+      }
     }
+    std::vector<double> it;
+    const double crowd = cm.prefix_item_crowd_us * (double)items.size();
+    for (const Item& x : items) it.push_back((x.half ? 0.5 : 1.0) * x.tiles * kp.tile_split + kp.item_split + crowd);
+    const double gsm = kp.rows == kPrefixRowsPerCta ? cm.gather_sm_gbs * cm.split_gather_ratio_tensor
+                                                    : cm.gather_sm_gbs;
+    const std::vector<double> w = split_weights(cm, num_sms, it, (double)S, gsm, v, prefix_cta_share > 0.0);
     partition_tokens_weighted(n_suf, w, &pl->suf_seg_begin, &pl->suf_segs);
   } else {
     if (p->gather_partition == GK_PARTITION_PER_REQUEST)
@@ -594,6 +616,7 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
   sm.prefix_rows_per_item = kp.rows;
   sm.prefix_row_groups = pl->prefix_kind && G > 0 ? warp_groups : 0;
   sm.prefix_ctas_gather = pl->split && prefix_cta_share > 0.0 ? 1 : 0;
+  sm.sm_slots = pl->slot_of_sm.empty() ? 0 : 1;
   return GK_OK;
 }
 
@@ -605,7 +628,8 @@ gk_status build_host_plan_kind(Pool* p, const gk_batch* b, Plan* pl, gk_prefix_k
 // measured model in place of the M_sat threshold.  The tensor-core items must
 // be predicted kTensorAutoEdge faster: on GB300 the model's times for their
 // cascade at small steps came out up to a quarter under the measured ones, the
-// warp-MMA items' within a fifth.
+// warp-MMA items' within a fifth.  Steps of at most kWarpOnlyMeff stacked rows
+// per head take the warp-MMA items (the pages' M_eff routing between the two).
 gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   if (p->prefix_kernel != GK_PREFIX_AUTO) return build_host_plan_kind(p, b, pl, p->prefix_kernel);
   gk_status st = build_host_plan_kind(p, b, pl, GK_PREFIX_TENSOR);
@@ -617,7 +641,7 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
   double td, t_tensor, t_warp;
   predict_plan(p->cost, p->dev.num_sms, Hq, *pl, &td, &t_tensor);
   predict_plan(p->cost, p->dev.num_sms, Hq, w, &td, &t_warp);
-  if (!(t_tensor < kTensorAutoEdge * t_warp)) {
+  if (pl->summary.max_m_eff <= kWarpOnlyMeff || !(t_tensor < kTensorAutoEdge * t_warp)) {
     pl->summary = w.summary;
     pl->groups.swap(w.groups);
     pl->group_hot_base.swap(w.group_hot_base);
@@ -635,6 +659,7 @@ gk_status build_host_plan(Pool* p, const gk_batch* b, Plan* pl) {
     pl->group_flops.swap(w.group_flops);
     pl->split = w.split;
     pl->prefix_kind = w.prefix_kind;
+    pl->slot_of_sm.swap(w.slot_of_sm);
   }
   return GK_OK;
 }
@@ -650,6 +675,7 @@ static gk_status upload_plan(Pool* p, Plan* pl, void* stream) {
   pl->off_suf_segs = append_region<SegmentDev>(&off, pl->suf_segs.size());
   pl->off_dense_begin = append_region<int32_t>(&off, pl->dense_seg_begin.size());
   pl->off_dense_segs = append_region<SegmentDev>(&off, pl->dense_segs.size());
+  pl->off_slot_of_sm = append_region<int32_t>(&off, pl->slot_of_sm.size());
   std::vector<uint8_t> tmaps;
   int te = encode_prefix_tmaps(&c, pl, &tmaps);
   if (te) return fail(p, GK_ERR_CUDA, "encoding the prefix tensor maps failed");
@@ -687,6 +713,7 @@ static gk_status upload_plan(Pool* p, Plan* pl, void* stream) {
   put(pl->off_suf_segs, pl->suf_segs.data(), pl->suf_segs.size() * sizeof(SegmentDev));
   put(pl->off_dense_begin, pl->dense_seg_begin.data(), pl->dense_seg_begin.size() * sizeof(int32_t));
   put(pl->off_dense_segs, pl->dense_segs.data(), pl->dense_segs.size() * sizeof(SegmentDev));
+  put(pl->off_slot_of_sm, pl->slot_of_sm.data(), pl->slot_of_sm.size() * sizeof(int32_t));
   put(pl->off_tmaps, tmaps.data(), tmaps.size());
   e = cudaMemcpyAsync(pl->d_buf, h, off, cudaMemcpyHostToDevice, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(p, e, "plan upload");
@@ -945,6 +972,36 @@ gk_status gk_pool_set_prefix_kernel(gk_pool* pool, gk_prefix_kernel kernel) {
   return GK_OK;
 }
 
+gk_status gk_pool_set_sm_speeds(gk_pool* pool, const float* speeds, int32_t n) {
+  if (!pool) return GK_ERR_INVALID;
+  Pool* p = &pool->impl;
+  if (n == 0) {
+    p->sm_speed.clear();
+    return GK_OK;
+  }
+  if (p->has_device) {
+    gk_status st = gk::ensure_device(p);   // the device's SM count
+    if (st != GK_OK) return st;
+  }
+  if (!speeds || n != p->dev.num_sms) return gk::fail(p, GK_ERR_INVALID, "one speed per SM of the device");
+  double sum = 0.0;
+  for (int32_t s = 0; s < n; ++s) {
+    if (!(std::isfinite(speeds[s]) && speeds[s] > 0.0f)) return gk::fail(p, GK_ERR_INVALID, "SM speeds must be positive");
+    sum += speeds[s];
+  }
+  p->sm_speed.assign((size_t)n, 1.0f);
+  for (int32_t s = 0; s < n; ++s) p->sm_speed[(size_t)s] = (float)(speeds[s] * n / sum);
+  return GK_OK;
+}
+
+gk_status gk_pool_get_sm_speeds(const gk_pool* pool, float* speeds, int32_t* n) {
+  if (!pool || !n) return GK_ERR_INVALID;
+  const Pool* p = &pool->impl;
+  *n = (int32_t)p->sm_speed.size();
+  if (speeds) std::copy(p->sm_speed.begin(), p->sm_speed.end(), speeds);
+  return GK_OK;
+}
+
 gk_status gk_cost_model_set(gk_pool* pool, const gk_cost_model* cm) {
   if (!pool || !cm) return GK_ERR_INVALID;
   if (!gk::valid_cost_model(*cm)) return gk::fail(&pool->impl, GK_ERR_INVALID, "invalid cost model");
@@ -1076,6 +1133,18 @@ gk_status gk_cascade_levels(gk_pool* pool, void* stream, int32_t layer, const gk
     return st == GK_OK ? gk_cascade_suffix(pool, stream, layer, batch, plan) : st;
   }
   gk::LaunchCommon lc{&p->cfg, p->d_error, p->dev.num_sms};
+  if (!pl->slot_of_sm.empty()) {
+    // a new tag per launch; when the counter wraps, the claim words are cleared
+    if (!p->d_slot_claim) return gk::fail(p, GK_ERR_INVALID, "pool has no slot-claim words");
+    if (++p->split_epoch == 0) {
+      cudaError_t ce = cudaMemsetAsync(p->d_slot_claim, 0, sizeof(uint32_t) * (size_t)p->dev.num_sms,
+                                       (cudaStream_t)stream);
+      if (ce != cudaSuccess) return gk::cuda_fail(p, ce, "cudaMemsetAsync(slot claims)");
+      ++p->split_epoch;
+    }
+    lc.slot_claim = p->d_slot_claim;
+    lc.epoch = p->split_epoch;
+  }
   int e = gk::launch_cascade_split(lc, stream, layer, batch, pl);
   return e ? gk::cuda_fail(p, e, "split cascade kernel") : GK_OK;
 }

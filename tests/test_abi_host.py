@@ -236,7 +236,8 @@ def test_dispatch_matches_oracle_formula(gk, case):
     """gk_dispatch's two predictions follow the documented formula (oracle/dispatch.py) for
     the arrangement and prefix kernel the plan reports, the plan's prefix work covers every
     (row block, KV head, key split) once, and GK_PREFIX_AUTO takes the warp-MMA items
-    unless the tensor-core ones are predicted at least 10 % faster.  Which arrangement the planner searches out is not pinned here (the
+    unless the tensor-core ones are predicted at least 10 % faster and some group stacks
+    more than 64 rows per head.  Which arrangement the planner searches out is not pinned here (the
     pages fix no such rule); the GPU tests hold it to measured times."""
     rnd = random.Random(case)
     Hq, Hkv, d = rnd.choice([(32, 8, 128), (40, 8, 128)])
@@ -296,7 +297,9 @@ def test_dispatch_matches_oracle_formula(gk, case):
             assert choice == (gk.GK_BACKEND_DENSE if odisp.choose(wd, wc) == "dense" else gk.GK_BACKEND_CASCADE)
             pred[kernel] = tc
         t_t, t_w = pred[gk.GK_PREFIX_TENSOR], pred[gk.GK_PREFIX_WARP]
-        assert pred[gk.GK_PREFIX_AUTO] == (t_t if t_t < 0.9 * t_w else t_w)
+        m_max = max([p["M"] for p in f["prefix"]], default=0)
+        if f["prefix"]:
+            assert pred[gk.GK_PREFIX_AUTO] == (t_t if m_max > 64 and t_t < 0.9 * t_w else t_w)
         with pytest.raises(gk.GkError):
             gk.gk_pool_set_prefix_kernel(pool, 3)
     finally:

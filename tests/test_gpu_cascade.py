@@ -124,3 +124,40 @@ def test_cascade_full_size_llama8b_lp16384_b64():
         assert _check(gw, [0], w.name, requests=[0, 1, w.B // 2, w.B - 1], modes=MODES[:2]) == {0, 1}
     finally:
         gw.close()
+
+
+@pytest.mark.parametrize("lp,B,srange,g", [(4096 + 77, 70, (1, 600), 4), (1000, 8, (50, 300), 5)])
+def test_cascade_sm_speed_slots(lp, B, srange, g):
+    """Split plans planned per SM (gk_pool_set_sm_speeds, or the speeds gk_sm_speeds_measure
+    takes from the plan's own suffix gather): the CTA on each SM claims the slot planned for
+    it, every slot runs exactly once wherever the CTAs land, so the split launch still gives
+    the staged launches' bits, and the outputs hold to the fp64 oracle."""
+    Hkv = 8 if g != 8 else 4
+    w = workloads.config(2, B=B, Lp=lp, suffix_range=srange, L=2, Hq=Hkv * g, Hkv=Hkv)
+    gw = _wl(w=w)
+    try:
+        pool = gw.eng.pool
+        n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+        rng = np.random.default_rng([lp, B])
+        gk.gk_pool_set_sm_speeds(pool, rng.uniform(0.7, 1.3, n_sm))
+        modes = [("split", gk.GK_CASCADE_SPLIT, 0), ("split-short-items", gk.GK_CASCADE_SPLIT, 3)]
+        b = gw.batch()
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SPLIT, 0)
+        pl = gw.eng.plan(b)
+        assert gk.gk_plan_info(pl)["sm_slots"] == 1
+        # three launches in a row: each launch's claims carry a tag of their own
+        assert 1 in _check(gw, [0, 1, 0], f"sm slots lp={lp} B={B} g={g}", modes=modes)
+        # speeds measured from the plan's suffix gather: one per SM, mean 1, all plausible
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SEQUENTIAL, 0)
+        b = gw.batch()
+        pl = gw.eng.plan(b)
+        q = gw.q(0)
+        out, lse = gw.outputs()
+        b.set_device(d_q=q, d_out=out, d_lse=lse)
+        sp = gk.gk_sm_speeds_measure(pool, None, 0, b, pl, reps=3)
+        assert len(sp) == n_sm and abs(float(sp.mean()) - 1.0) < 1e-4 and sp.min() > 0.3 and sp.max() < 3.0
+        assert gw.eng.device_error() == gk.GK_OK
+        assert _check(gw, [1], f"measured sm slots lp={lp} B={B} g={g}", modes=modes[:1]) == {1}
+        gk.gk_pool_set_sm_speeds(pool, None)
+    finally:
+        gw.close()

@@ -226,3 +226,70 @@ def test_split_slots_follow_each_item(gk):
     assert got == want
     # shorter items, longer gathers: about 0.39 and 0.53 of a gather-only CTA's share
     assert 0.37 < np.mean(got[:16]) / np.mean(got[32:]) < 0.41 and 0.51 < np.mean(got[24:32]) / np.mean(got[32:]) < 0.55
+
+
+def test_split_slots_follow_sm_speeds(gk):
+    """With per-SM speeds set (gk_pool_set_sm_speeds), a split plan's slots are planned per
+    SM: the slowest SMs take the prefix items and every gather-only slot's tokens follow
+    its SM's speed.  Same case as the per-item test with every item of one length (C = 32:
+    32 items on the 16384-token group, 8 on the 4096-token one, 40 prefix slots); speeds
+    1 + 0.05 (s mod 9) - 0.2 [s mod 7 == 0], normalised to mean 1.  Without speeds the
+    plan is the one CTA b takes slot b of."""
+    import json
+    cm = dict(c_flat_us=5.0, bw_flat_gbs=4000.0, c_cascade_us=10.0, bw_prefix_gbs=5000.0, bw_suffix_gbs=6000.0,
+              c_merge_us=0.001, prefix_tile_us=1.0, prefix_item_us=5.0, gather_sm_gbs=50.0, c_gather_us=4.0,
+              prefix_tile_split_us=1.0, warp_tile_us=1e3, warp_group_us=0.0, warp_item_us=1e3, warp_split_ratio=1.0,
+              prefix_cta_ramp_us=4.0, prefix_cta_gather_ratio=1.0, c_merge_state_us=0.0, prefix_item_split_us=5.0,
+              warp_item_split_us=1e3, prefix_item_crowd_us=0.0, split_gather_ratio_tensor=1.0, c_gather_split_us=4.0,
+              split_tensor_us=0.0)
+    sp = np.array([1 + 0.05 * (s % 9) - (0.2 if s % 7 == 0 else 0.0) for s in range(SMS)], np.float32)
+    pool = gk.gk_pool_create(1, 32, 8, 128, 16384 + 4096 + 32, 128 * 1000 + 64, 1, 0)
+    try:
+        gk.gk_cost_model_load(pool, json.dumps(cm))
+        gk.gk_pool_set_prefix_kernel(pool, gk.GK_PREFIX_TENSOR)
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SPLIT, 32)
+        a, b = gk.gk_prefix_alloc(pool, 16384), gk.gk_prefix_alloc(pool, 4096)
+        bases, lps, slens = [a] * 64 + [b] * 64, [16384] * 64 + [4096] * 64, [1000] * 128
+        with pytest.raises(gk.GkError):
+            gk.gk_pool_set_sm_speeds(pool, sp[:100])
+        with pytest.raises(gk.GkError):
+            gk.gk_pool_set_sm_speeds(pool, np.where(np.arange(SMS) == 3, -1.0, sp))
+        assert len(gk.gk_pool_get_sm_speeds(pool)) == 0
+        _, plan = _plan(gk, pool, bases, lps, slens)
+        s0 = gk.gk_plan_info(plan)
+        t0 = _tokens(*gk.gk_plan_segments(plan, False))
+        gk.gk_plan_destroy(plan)
+        gk.gk_pool_set_sm_speeds(pool, sp)
+        got = gk.gk_pool_get_sm_speeds(pool)
+        assert np.allclose(got, sp * SMS / sp.sum(), rtol=1e-6) and abs(got.mean() - 1) < 1e-6
+        _, plan = _plan(gk, pool, bases, lps, slens)
+        s = gk.gk_plan_info(plan)
+        begin, segs = gk.gk_plan_segments(plan, False)
+        _check_cover(begin, segs, slens)
+        _check_entries(segs, False)
+        t = _tokens(begin, segs)
+        gk.gk_plan_destroy(plan)
+        gk.gk_pool_set_sm_speeds(pool, None)
+        _, plan = _plan(gk, pool, bases, lps, slens)
+        t2 = _tokens(*gk.gk_plan_segments(plan, False))
+        assert gk.gk_plan_info(plan)["sm_slots"] == 0 and t2 == t0
+        gk.gk_plan_destroy(plan)
+    finally:
+        gk.gk_pool_destroy(pool)
+    assert s0["sm_slots"] == 0 and s["sm_slots"] == 1
+    n_pre = s["prefix_ctas"]
+    assert n_pre == s0["prefix_ctas"] == 40 and s["prefix_ctas_gather"] == 1
+    # slots in order of SM speed: the n_pre slowest take the items, all of 37 us (start 41 us);
+    # the common end T solves  sum_gather-only v (T - 4) + sum_prefix v (T - 41) = S / 50 GB/s
+    v = np.sort(got.astype(np.float64))
+    W = 128 * 1000 * 4096 / 50e3
+    T = (W + 4 * v[n_pre:].sum() + 41 * v[:n_pre].sum()) / v.sum()
+    w = np.concatenate([v[:n_pre] * (T - 41) / (T - 4), v[n_pre:]])
+    total, acc, ends = 128000, 0.0, []
+    for x in w:
+        acc += x
+        e = int(total * acc / w.sum() + 0.5)
+        e = (e + 8) // 16 * 16
+        ends.append(min(total, max(e, ends[-1] if ends else 0)))
+    ends[-1] = total
+    assert t == np.diff([0] + ends).tolist()
