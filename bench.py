@@ -457,6 +457,10 @@ def chained_kernels(gk, torch, pool, batch, plan, w, backend, q_all, out_all, ls
         out["cascade_levels"] = chain(lambda l: gk.gk_cascade_levels(pool, stream, l, batch, plan))
         out["lse_merge"] = chain(lambda l: gk.gk_cascade_merge(pool, stream, l, batch, plan))
         out["layer"] = chain(lambda l: gk.gk_decode_cascade(pool, stream, l, batch, plan))
+        # a chain of merges alone is bound by their launches; inside the step each merge's
+        # launch and set-up overlap the split launch before it, so its cost there is what it
+        # adds to a layer
+        out["lse_merge"]["in_step_ms"] = out["layer"]["ms"] - out["cascade_levels"]["ms"]
     else:
         out["dense_gather"] = chain(lambda l: gk.gk_decode_dense(pool, stream, l, batch, plan))
     if gk.gk_device_error(pool, stream):
