@@ -158,6 +158,16 @@ def test_cascade_sm_speed_slots(lp, B, srange, g):
         assert len(sp) == n_sm and abs(float(sp.mean()) - 1.0) < 1e-4 and sp.min() > 0.3 and sp.max() < 3.0
         assert gw.eng.device_error() == gk.GK_OK
         assert _check(gw, [1], f"measured sm slots lp={lp} B={B} g={g}", modes=modes[:1]) == {1}
+        # measured again from a split plan that already runs per SM (its launches claim slots)
+        gk.gk_pool_set_cascade_mode(pool, gk.GK_CASCADE_SPLIT, 0)
+        b = gw.batch()
+        pl = gw.eng.plan(b)
+        assert gk.gk_plan_info(pl)["sm_slots"] == 1
+        b.set_device(d_q=q, d_out=out, d_lse=lse)
+        sp2 = gk.gk_sm_speeds_measure(pool, None, 0, b, pl, reps=3)
+        assert len(sp2) == n_sm and abs(float(sp2.mean()) - 1.0) < 1e-4 and sp2.min() > 0.3 and sp2.max() < 3.0
+        assert gw.eng.device_error() == gk.GK_OK
+        assert _check(gw, [0], f"re-measured sm slots lp={lp} B={B} g={g}", modes=modes[:1]) == {1}
         gk.gk_pool_set_sm_speeds(pool, None)
     finally:
         gw.close()
