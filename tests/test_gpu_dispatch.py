@@ -26,7 +26,7 @@ import numpy as np
 import pytest
 
 torch = pytest.importorskip("torch")
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.timing]
 
 from paged_kv_cache_pool_gb300 import binding as gk  # noqa: E402
 

@@ -2,8 +2,9 @@
 compiled into the library) must give the plan path's result, call after call.
 
 For callers that cannot allocate device memory while serving (all free HBM
-already handed to the KV pool, or a framework-owned allocator).  Collected last
-so that a failure here comes after every other test has run.
+already handed to the KV pool, or a framework-owned allocator).  Collected after
+every other parity test (only the tests that assert on measured times follow),
+so that a failure here comes after them.
 """
 import numpy as np
 import pytest
