@@ -1,12 +1,16 @@
-"""Decode-step orchestration over libgk: storage allocation, sequences, batches.
+"""Convenience layer over libgk for Python callers: a pool with its storage.
 
-A thin layer over the ``gk_*`` calls for Python users: it allocates the HOT and
-COLD K/V storage as torch CUDA tensors (PyTorch is only the device-memory and
-stream provider here), keeps the host mirrors a batch needs, and strings the
-calls of one decode step together:
+It allocates the HOT and COLD K/V storage as torch CUDA tensors (PyTorch is
+only the device-memory and stream provider here), creates the pool over them,
+keeps the plans it builds so that close() frees them, and names the calls of a
+decode step, which the caller strings together in this order:
 
-  gk_seq_append_slots -> gk_append_kv (per layer) -> gk_plan_build/update
-  -> gk_dispatch -> gk_decode_cascade | gk_decode_dense (per layer).
+  append_slots (gk_seq_append_slots) -> append_kv (gk_append_kv, per layer;
+  or the decode's fused append) -> plan (gk_plan_build / gk_plan_update)
+  -> dispatch (gk_dispatch) -> decode (gk_decode_cascade | gk_decode_dense,
+  per layer).
+
+Every method is one library call; the work is in libgk.
 """
 from __future__ import annotations
 
