@@ -22,6 +22,7 @@ implementation to run); each of its steps is a bounded sample of one layer.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -635,6 +636,11 @@ def run_ours(a, w):
     torch.cuda.synchronize()
     launches[0] = 0
     n_choice0 = len(choices)
+    # Python's cyclic garbage collector stays off inside the timed regions, as timeit keeps
+    # it: a full collection of this process's objects takes tens of ms of host time, which
+    # would otherwise land inside some step's host work
+    gc.collect()
+    gc.disable()
     w0 = time.time()
     t_start.record(stream)
     for i in range(a.steps):
@@ -642,6 +648,7 @@ def run_ours(a, w):
     t_end.record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
+    gc.enable()
     gpu_launches = launches[0]
     elapsed_ms = t_start.elapsed_time(t_end)
     err = gk.gk_device_error(pool, stream)
@@ -663,59 +670,71 @@ def run_ours(a, w):
         hv.copy_(newv)
         ho = torch.empty_like(out_all, device="cpu").pin_memory()
         hl = torch.empty_like(lse_all, device="cpu").pin_memory()
-        # Double-buffered device inputs and outputs: a copy stream moves step t+1's
-        # inputs in and step t's outputs out while the compute stream runs.
-        dev_in = [(torch.empty_like(q_all), torch.empty_like(newk), torch.empty_like(newv)) for _ in range(2)]
-        dev_out = [(torch.empty_like(out_all), torch.empty_like(lse_all)) for _ in range(2)]
-        copy_s = torch.cuda.Stream()
-        ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of buffer i have landed
-        ev_used = [torch.cuda.Event() for _ in range(2)]    # the compute that read/wrote buffer i is done
-        ev_out = [torch.cuda.Event() for _ in range(2)]     # outputs of buffer i have left
+        # Triple-buffered device inputs and outputs, each direction on a copy stream of its
+        # own: step t+1's inputs come in and step t's outputs go out while the compute
+        # stream runs, and a step waits for the outputs of the step three before it to have
+        # left its buffer.  (One copy of a step's inputs or outputs now and then takes tens
+        # of ms longer than its 1.2-1.9 ms; with two buffers and one copy stream those held
+        # up the compute stream.  Copies in chunks of a few layers, each layer waiting for its
+        # own, were slower: the waits and event records between a layer's kernels cost more
+        # than the first and last copies of the region that they shorten.)
+        NB = 3
+        dev_in = [(torch.empty_like(q_all), torch.empty_like(newk), torch.empty_like(newv)) for _ in range(NB)]
+        dev_out = [(torch.empty_like(out_all), torch.empty_like(lse_all)) for _ in range(NB)]
+        h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(NB)]      # inputs of buffer i have landed
+        ev_used = [torch.cuda.Event() for _ in range(NB)]    # the compute that read/wrote buffer i is done
+        ev_out = [torch.cuda.Event() for _ in range(NB)]     # outputs of buffer i have left
         for e in ev_used + ev_out:
             e.record(stream)
 
         def h2d(i):
-            with torch.cuda.stream(copy_s):
-                copy_s.wait_event(ev_used[i])
+            with torch.cuda.stream(h2d_s):
+                h2d_s.wait_event(ev_used[i])
                 for dst, src in zip(dev_in[i], (hq, hk, hv)):
                     dst.copy_(src, non_blocking=True)
-                ev_in[i].record(copy_s)
+                ev_in[i].record(h2d_s)
 
         def run_steps(n):
             h2d(0)
             for t in range(n):
-                i = t % 2
+                i = t % NB
                 stream.wait_event(ev_in[i])
-                stream.wait_event(ev_out[i])   # the step before last has left this output buffer
+                stream.wait_event(ev_out[i])   # step t - NB has left this output buffer
                 step(*dev_in[i], *dev_out[i])
                 ev_used[i].record(stream)
                 if t + 1 < n:
-                    h2d(1 - i)
-                with torch.cuda.stream(copy_s):
-                    copy_s.wait_event(ev_used[i])
+                    h2d((t + 1) % NB)
+                with torch.cuda.stream(d2h_s):
+                    d2h_s.wait_event(ev_used[i])
                     ho.copy_(dev_out[i][0], non_blocking=True)
                     hl.copy_(dev_out[i][1], non_blocking=True)
-                    ev_out[i].record(copy_s)
-            stream.wait_stream(copy_s)
+                    ev_out[i].record(d2h_s)
+            stream.wait_stream(h2d_s)
+            stream.wait_stream(d2h_s)
 
         run_steps(a.warmup)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        gc.collect()
+        gc.disable()
         v0 = time.time()
         e0.record(stream)
-        copy_s.wait_event(e0)
+        h2d_s.wait_event(e0)
+        d2h_s.wait_event(e0)
         run_steps(a.steps)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_window = (v0, time.time())
+        gc.enable()
         ems = max_over_ranks(e0.elapsed_time(e1))
         h2d_bytes = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + B * max_blocks * 4
         d2h_bytes = ho.numel() * 4 + hl.numel() * 4
         e2e = {"value": replica_throughput(world, B * L * a.steps, ems), "unit": UNIT,
                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "ms_per_step": ems / a.steps,
-               "copies": "double-buffered on a second stream, overlapping the neighbouring steps' compute"}
+               "copies": "triple-buffered, one copy stream each way, overlapping the neighbouring steps' compute"}
 
     time.sleep(0.1)   # let the sampler report the samples of the regions' ends
     clk = clocks.stop((w0, w1))
